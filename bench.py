@@ -1,0 +1,375 @@
+"""Benchmark of the page-retrieval sparse-attention path for one chunk.
+
+Workload (default): one layer at the WorldAttention shape -- 12 heads,
+d_k = 128, bf16, 40 cached pages of 12,480 tokens (5 chunks x 8 pages) in HBM,
+prompt embeddings of dim 4096, top-1 chunk then top-4 pages (49,920 tokens),
+4,680 query tokens attending to the gathered buffer + 4,680 local tokens.
+
+One step = the whole path: page summaries of all 40 cached pages, two-stage
+retrieval, gather of the 4 pages (K and V) into the contiguous buffer, and
+block attention.  Inputs are resident in HBM before timing; the page bank
+(3.07 GB) is larger than L2, and each step's summaries stream all of it, so
+L2 holds nothing useful from one step to the next.
+
+Prints one JSON line.  ``--impl reference`` times the fp64 CPU oracle on a
+bounded sample of the same workload instead.
+"""
+
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "chunk attention latency (ms) & TFLOP/s at 49,920 retrieved tokens; gather GB/s"
+WORKLOAD = "worldattention_1layer: H=12 d=128 bf16, 40 pages x 12480 tok, top-1 of 5 chunks, K_p=4 (49,920), n_q=4680 + 4680 local"
+
+H, D, P, N_PAGES, PPC, N_CHUNKS, PDIM, KP, NQ, NLOC = 12, 128, 12480, 40, 8, 5, 4096, 4, 4680, 4680
+
+
+def attn_flops(n_q, n_kv, d, h):
+    """Matmul FLOPs of softmax attention: 2*n_q*n_kv*d for Q K^T and again for P V."""
+    return 4.0 * n_q * n_kv * d * h
+
+
+def peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            j = json.load(f)
+        return j["hbm_gbs"], j["bf16_tflops"], j.get("bf16_tflops_sustained", j["bf16_tflops"]), "measured"
+    except Exception:
+        return 6800.0, 1900.0, 1700.0, "fallback"
+
+
+class Clocks:
+    """nvidia-smi sampling during the timed region."""
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_bench_{os.getpid()}.csv")
+
+    def __enter__(self):
+        try:
+            os.makedirs(os.path.dirname(self.path), exist_ok=True)
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}",
+                 "--query-gpu=index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+                 "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+                 "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap",
+                 "--format=csv,noheader,nounits", "-lms", "100"], stdout=self.f,
+                stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+            self.f.close()
+
+    def summary(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        rows = []
+        try:
+            for line in open(self.path):
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+        except Exception:
+            pass
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons,
+                "samples": len(rows)}
+
+
+def dist_init(args):
+    import torch
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        dist.init_process_group(backend)
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x, world):
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda" if torch.cuda.is_available() else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ----------------------------------------------------------------------------
+# GPU arm
+# ----------------------------------------------------------------------------
+
+def run_gpu(args, world, rank, local):
+    import torch
+
+    import sparse_kv_cache_page_gb300 as wa
+    from sparse_kv_cache_page_gb300 import synth
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    wa.load()
+    c = synth.worldattention_case(device=dev, layer=rank, recall_chunk=3)
+    kp, vp, q, kl, vl = c.k_pages, c.v_pages, c.q, c.k_loc, c.v_loc
+    pcur, pch = c.prompt_cur, c.prompt_chunks
+    kbar = torch.empty((N_PAGES, H, D), dtype=torch.float32, device=dev)
+    idx = torch.empty(KP, dtype=torch.int32, device=dev)
+    kbuf = torch.empty((KP * P, H, D), dtype=torch.bfloat16, device=dev)
+    vbuf = torch.empty_like(kbuf)
+    o = torch.empty_like(q)
+    lse = torch.empty((H, NQ), dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream()
+
+    names = ("summarize", "select", "gather", "attention")
+
+    def step(ev=None):
+        def mark(i):
+            if ev is not None:
+                ev[i].record(stream)
+        mark(0)
+        wa.wa_page_summarize(kp, kbar)
+        mark(1)
+        wa.wa_select_pages(q, kbar, pcur, pch, PPC, KP, idx)
+        mark(2)
+        wa.wa_gather_pages(kp, vp, idx, None, kbuf, vbuf)
+        mark(3)
+        wa.wa_block_attn(q, kbuf, vbuf, kl, vl, o, lse)
+        mark(4)
+
+    for _ in range(args.warmup):
+        step()
+    wa.wa_check()
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
+    barrier(world)
+    torch.cuda.synchronize()
+    with Clocks(local) as clk:
+        t0 = torch.cuda.Event(enable_timing=True)
+        t1 = torch.cuda.Event(enable_timing=True)
+        t0.record(stream)
+        for k in range(args.steps):
+            step(evs[k])
+        t1.record(stream)
+        torch.cuda.synchronize()
+    barrier(world)
+    wa.wa_check()
+    total_ms = max_over_ranks(t0.elapsed_time(t1), world)
+    ms_step = total_ms / args.steps
+    per = {n: statistics.mean(evs[k][i].elapsed_time(evs[k][i + 1]) for k in range(args.steps))
+           for i, n in enumerate(names)}
+
+    # end to end through the public API: per step, the chunk's inputs come from
+    # pinned host memory and the output goes back to pinned host memory
+    hq = q.cpu().pin_memory()
+    hkl, hvl = kl.cpu().pin_memory(), vl.cpu().pin_memory()
+    hpc = pcur.cpu().pin_memory()
+    ho = torch.empty(o.shape, dtype=o.dtype).pin_memory()
+    dq, dkl, dvl, dpc = torch.empty_like(q), torch.empty_like(kl), torch.empty_like(vl), torch.empty_like(pcur)
+
+    def step_e2e():
+        dq.copy_(hq, non_blocking=True)
+        dkl.copy_(hkl, non_blocking=True)
+        dvl.copy_(hvl, non_blocking=True)
+        dpc.copy_(hpc, non_blocking=True)
+        wa.wa_page_summarize(kp, kbar)
+        wa.wa_select_pages(dq, kbar, dpc, pch, PPC, KP, idx)
+        wa.wa_gather_pages(kp, vp, idx, None, kbuf, vbuf)
+        wa.wa_block_attn(dq, kbuf, vbuf, dkl, dvl, o, lse)
+        ho.copy_(o, non_blocking=True)
+
+    for _ in range(max(1, args.warmup)):
+        step_e2e()
+    torch.cuda.synchronize()
+    barrier(world)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        step_e2e()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1), world) / args.steps
+    h2d = sum(t.numel() * t.element_size() for t in (hq, hkl, hvl, hpc))
+    d2h = ho.numel() * ho.element_size()
+
+    hbm, tf_burst, tf_sus, src = peaks()
+    n_kv = KP * P + NLOC
+    flops = attn_flops(NQ, n_kv, D, H)
+    attn_tflops = flops / (per["attention"] * 1e-3) / 1e12
+    gather_bytes = 2 * 2 * KP * P * H * D * 2          # K and V, read + write
+    summ_bytes = N_PAGES * P * H * D * 2
+    value = world * flops / (ms_step * 1e-3) / 1e12
+    line = {
+        "metric": METRIC,
+        "value": round(value, 2),
+        "unit": "TFLOP/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms_step, 4),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic (seeded N(0,1), WorldAttention shapes)",
+        "config": {"workload": WORKLOAD, "l2": "inputs larger than L2 (3.07 GB page bank streamed per step)",
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+                   "value_is": "attention matmul FLOPs of the chunk / whole-step time"},
+        "chunk_latency_ms": round(ms_step, 4),
+        "kernels_ms": {k: round(v, 4) for k, v in per.items()},
+        "attn_tflops": round(attn_tflops, 1),
+        "gather_gbs": round(gather_bytes / (per["gather"] * 1e-3) / 1e9, 1),
+        "summarize_gbs": round(summ_bytes / (per["summarize"] * 1e-3) / 1e9, 1),
+        "roofline": {"bound": "tensor", "achieved": round(attn_tflops, 1), "peak": tf_sus,
+                     "unit": "TFLOP/s", "frac": round(attn_tflops / tf_sus, 4), "traffic": None,
+                     "kernel": "k_block_attn_tc", "peak_source": f"{src} bf16 sustained"},
+        "e2e": {"value": round(world * flops / (e2e_ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
+                "ms_per_step": round(e2e_ms, 4), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "gpu_launches": 4 * args.steps,
+        "clocks": clk.summary(),
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline_sample(c, lambda j: (kp[j], vp[j]))
+    return line
+
+
+# ----------------------------------------------------------------------------
+# CPU oracle arm
+# ----------------------------------------------------------------------------
+
+def cpu_baseline_sample(c, get_page, budget_rows=24):
+    """Time the fp64 oracle, as it stands, on a bounded sample of the workload
+    and scale it to one chunk: one page summary (x40 pages), the two-stage
+    retrieval over 40 summaries, the 4-page gather, and attention for
+    `budget_rows` query rows of every head over all 54,600 keys (x n_q/rows).
+    get_page(j) -> (K_j, V_j) as torch tensors."""
+    import numpy as np
+
+    import oracle as O
+    from sparse_kv_cache_page_gb300 import synth
+
+    t_cpu0, t_wall0 = time.process_time(), time.perf_counter()
+    k0, _ = get_page(0)
+    kp0 = synth.to_oracle(k0)[None]
+    t = time.perf_counter()
+    kbar0 = O.page_summarize(kp0)
+    t_sum = (time.perf_counter() - t) * N_PAGES
+    kbar = np.repeat(kbar0, N_PAGES, axis=0)   # timing stand-in for the other 39 summaries
+    oq = synth.to_oracle(c.q)
+    t = time.perf_counter()
+    idx, _, _ = O.select_pages(oq, kbar, synth.to_oracle(c.prompt_cur),
+                               synth.to_oracle(c.prompt_chunks), PPC, KP)
+    t_sel = time.perf_counter() - t
+    pages = [get_page(int(j)) for j in idx]
+    kps = np.stack([synth.to_oracle(kv[0]) for kv in pages])
+    vps = np.stack([synth.to_oracle(kv[1]) for kv in pages])
+    t = time.perf_counter()
+    kbuf = O.gather_pages(kps, range(KP))
+    vbuf = O.gather_pages(vps, range(KP))
+    t_gat = time.perf_counter() - t
+    rows = np.linspace(0, NQ - 1, budget_rows).astype(int)
+    t = time.perf_counter()
+    O.block_attn(oq, kbuf, vbuf, synth.to_oracle(c.k_loc), synth.to_oracle(c.v_loc), rows=rows)
+    t_att = (time.perf_counter() - t) * NQ / budget_rows
+    wall = time.perf_counter() - t_wall0
+    cpu = time.process_time() - t_cpu0
+    ms = (t_sum + t_sel + t_gat + t_att) * 1e3
+    flops = attn_flops(NQ, KP * P + NLOC, D, H)
+    return {"value": round(flops / (ms * 1e-3) / 1e12, 6), "unit": "TFLOP/s",
+            "chunk_ms": round(ms, 1), "cores": len(os.sched_getaffinity(0)),
+            "cpu_util": round(cpu / max(wall, 1e-9), 2), "kind": "oracle",
+            "sample": f"1 page summary (x{N_PAGES}), retrieval over {N_PAGES} summaries, 4-page "
+                      f"gather, attention for {budget_rows} query rows x {H} heads over "
+                      f"{KP * P + NLOC} keys (x{NQ / budget_rows:.0f}); numpy fp64",
+            "parts_ms": {"summarize": round(t_sum * 1e3, 1), "select": round(t_sel * 1e3, 1),
+                         "gather": round(t_gat * 1e3, 1), "attention": round(t_att * 1e3, 1)}}
+
+
+def run_reference(args, world, rank):
+    from sparse_kv_cache_page_gb300 import synth
+    if rank != 0:
+        return None
+    c = synth.worldattention_case(device="cpu", recall_chunk=3, lazy_pages=True)
+    cache = {}
+
+    def get_page(j):
+        if j not in cache:
+            cache[j] = c.extra["page"](j, "cpu")
+        return cache[j]
+
+    samples = []
+    for _ in range(args.warmup):
+        cpu_baseline_sample(c, get_page, budget_rows=8)
+    for _ in range(args.steps):
+        samples.append(cpu_baseline_sample(c, get_page, budget_rows=8))
+    value = statistics.mean(s["value"] for s in samples)
+    ms = statistics.mean(s["chunk_ms"] for s in samples)
+    return {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": WORKLOAD},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "kind": "oracle",
+                         "cores": samples[0]["cores"], "sample": samples[0]["sample"]},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(3, args.warmup)
+    world, rank, local = dist_init(args)
+    if args.impl == "reference":
+        line = run_reference(args, world, rank)
+    else:
+        line = run_gpu(args, world, rank, local)
+    if rank == 0 and line is not None:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,205 @@
+/*
+ * wa.h -- C ABI of libwa: page-retrieval sparse attention for one generated
+ * chunk of a block-diffusion world model, on one GB300 (sm_103a).
+ *
+ * Sources (page title, section):
+ *   [WA] "WorldAttention: An Efficient Attention Architecture for Interactive
+ *        Video World Models" (review page): HKV section (paper §3.1 HKV) --
+ *        8-frame pages, page mean keys, prompt-stage top-1 chunk by cosine,
+ *        page-stage score alpha = Qbar^T Kbar / sqrt(d_k), top-K_p (K_p = 4);
+ *        Fig. 1 custom-kernels prong -- retrieved pages reorganised into one
+ *        contiguous buffer; HSA section (paper §3.2 HSA) -- Linformer-style
+ *        low-rank branch with per-head E_K, E_V in R^{L x r} and a per-head
+ *        gate fusing the branches.
+ *   [IX] "Inferix: A Block-Diffusion based Next-Generation Inference Engine
+ *        for World Simulation" (summary page): §3 Technical Approach, Step 3
+ *        -- Attention(Q, [K_cache (+) K_t], [V_cache (+) V_t]), no mask; KV
+ *        Cache Manager -- range access, index-based selective fetch, offload
+ *        to main memory.
+ *
+ * Conventions shared by every call
+ *   - Layout is token-major: a KV or Q tensor is [tokens][n_heads][head_dim],
+ *     dense, row stride n_heads*head_dim elements.  A page bank is
+ *     [n_pages][page_tokens][n_heads][head_dim], so page j is one contiguous
+ *     slab of page_tokens*n_heads*head_dim elements.
+ *   - Element types: WA_BF16 (2-byte bfloat16) or WA_F32 (4-byte float).
+ *     Page summaries, scores, prompt embeddings and LSE are always float32.
+ *   - Pointers are device pointers unless stated, 16-byte aligned.  The
+ *     caller owns every buffer.  Every call is asynchronous on `stream`
+ *     (NULL = the legacy default stream) and returns after enqueueing.
+ *   - The library keeps one internal scratch arena per device, allocated
+ *     with cudaMalloc on first need and grown (after a device-wide
+ *     synchronize) when a call needs more; wa_shutdown() frees it.  Calls
+ *     that use scratch (wa_page_summarize, wa_select_pages,
+ *     wa_linear_branch) must not run concurrently on one device.
+ *   - Errors: arguments are validated on the host before any launch; a bad
+ *     argument returns a status and enqueues nothing.  A launch failure
+ *     returns WA_ERR_CUDA.  Kernels never trap: a device-side problem (a
+ *     page index out of range, a wait that timed out) is recorded in a
+ *     device status word that wa_check() reads.  No C++ exception crosses
+ *     this ABI.  Non-finite inputs give unspecified (but memory-safe)
+ *     results.
+ */
+#ifndef WA_H_
+#define WA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+struct CUstream_st;                       /* == cudaStream_t */
+typedef struct CUstream_st* wa_stream_t;
+
+typedef enum {
+  WA_OK = 0,
+  WA_ERR_INVALID_ARG = 1,   /* NULL pointer, non-positive size, k_p too large  */
+  WA_ERR_SHAPE = 2,         /* a size the kernels do not support              */
+  WA_ERR_DTYPE = 3,         /* unknown or unsupported element type            */
+  WA_ERR_ALIGN = 4,         /* pointer not 16-byte aligned                    */
+  WA_ERR_INDEX = 5,         /* page index out of range                        */
+  WA_ERR_OOM = 6,           /* scratch allocation failed                      */
+  WA_ERR_CUDA = 7,          /* CUDA runtime/launch error                      */
+  WA_ERR_TIMEOUT = 8,       /* a device wait exceeded its limit (wa_check)    */
+  WA_ERR_UNIMPLEMENTED = 9
+} wa_status;
+
+typedef enum { WA_F32 = 0, WA_BF16 = 1 } wa_dtype;
+
+/* Human-readable name of a status.  Never NULL. */
+const char* wa_strerror(wa_status s);
+
+/* Library version, e.g. "wa 0.1.0 sm_103a". */
+const char* wa_version(void);
+
+/*
+ * Page summaries ([WA] HKV: each page is scored through its mean key).
+ *
+ *   kbar_out[j][h][e] = (1/page_tokens) * sum_t k_pages[j][t][h][e]
+ *
+ * k_pages  : device, [n_pages][page_tokens][n_heads][head_dim] of `dt`.
+ * kbar_out : device float32 [n_pages][n_heads][head_dim] (written).
+ * Sums are fp32 in a fixed order (deterministic run to run).
+ * Needs n_heads*head_dim <= 8192 and a multiple of 8 (bf16) / 4 (f32).
+ */
+wa_status wa_page_summarize(const void* k_pages, wa_dtype dt, int n_pages, int page_tokens,
+                            int n_heads, int head_dim, float* kbar_out, wa_stream_t stream);
+
+/*
+ * Two-stage page retrieval for one chunk ([WA] HKV, stages 1 and 2).
+ *
+ *   Qbar[h]  = (1/n_q) sum_i q[i][h]                       (mean query)
+ *   stage 1  : c* = argmax_m cos(prompt_cur, prompt_chunks[m]); a zero-norm
+ *              vector has cosine 0; exact ties go to the lowest m.  Chunk m
+ *              owns pages [m*pages_per_chunk, (m+1)*pages_per_chunk).
+ *              With n_chunks == 0 the stage is skipped: every page is a
+ *              candidate and *chunk_out = -1.
+ *   stage 2  : alpha_j = sum_h Qbar[h] . kbar[j][h] / sqrt(head_dim) for each
+ *              candidate j (one page set shared by all heads); keep the k_p
+ *              largest, ties to the lowest page index.
+ *
+ * q            : device [n_q][n_heads][head_dim] of `dt`.
+ * kbar         : device float32 [n_pages][n_heads][head_dim].
+ * prompt_cur   : device float32 [prompt_dim]; prompt_chunks: device float32
+ *                [n_chunks][prompt_dim] (both ignored when n_chunks == 0).
+ * idx_out      : device int32 [k_p], written in ascending page order.
+ * scores_out   : device float32 [k_p], alpha of idx_out (may be NULL).
+ * chunk_out    : device int32 [1], the chunk picked (may be NULL).
+ * k_p must not exceed the candidate count (pages_per_chunk, or n_pages
+ * without the prompt stage) nor 1024: else WA_ERR_INVALID_ARG.  With the
+ * prompt stage, n_chunks*pages_per_chunk must not exceed n_pages.
+ * Indices never return to the host; the call does not synchronize.
+ */
+wa_status wa_select_pages(const void* q, wa_dtype dt, int n_q, int n_heads, int head_dim,
+                          const float* kbar, int n_pages,
+                          const float* prompt_cur, const float* prompt_chunks, int n_chunks,
+                          int prompt_dim, int pages_per_chunk, int k_p,
+                          int32_t* idx_out, float* scores_out, int32_t* chunk_out,
+                          wa_stream_t stream);
+
+/*
+ * Gather of the retrieved pages into one contiguous buffer ([WA] Fig. 1,
+ * custom kernels; [IX] KV Cache Manager, index-based selective fetch):
+ *
+ *   k_buf[s*page_tokens + t] = k_pages[idx[s]][t],  likewise v   (s < k_p)
+ *
+ * Source in device memory: a copy kernel reads the indices from idx_dev
+ * (device int32 [k_p]); an index outside [0, n_pages) makes that slot's rows
+ * zero and is recorded in the status word (WA_ERR_INDEX from wa_check).
+ * Source in pinned host memory (cudaHostAlloc / cudaHostRegister; the DRAM
+ * tier of [WA] HKV and [IX] offload): one cudaMemcpyAsync per page and
+ * tensor on `stream`; the page indices come from idx_host (host int32
+ * [k_p]) and are checked on the host (WA_ERR_INDEX, nothing enqueued).
+ * k_buf, v_buf : device [k_p*page_tokens][n_heads][head_dim] of `dt`.
+ * v_pages/v_buf may be NULL together (keys only).
+ */
+wa_status wa_gather_pages(const void* k_pages, const void* v_pages, wa_dtype dt, int n_pages,
+                          int page_tokens, int n_heads, int head_dim,
+                          const int32_t* idx_dev, const int32_t* idx_host, int k_p,
+                          void* k_buf, void* v_buf, wa_stream_t stream);
+
+/*
+ * Block attention of the chunk's queries over the retrieved buffer plus the
+ * chunk's own KV ([IX] §3 Step 3; no mask, bidirectional):
+ *
+ *   O[i][h]  = sum_k softmax_k(scale * q[i][h] . K[k][h]) V[k][h]
+ *   lse[h][i] = ln sum_k exp(scale * q[i][h] . K[k][h])
+ *   with K = [k_main ; k_loc] and V = [v_main ; v_loc] along tokens.
+ *
+ * q, o     : device [n_q][n_heads][head_dim] of `dt`; o is written (bf16 by
+ *            round-to-nearest-even of the fp32 result, or f32).
+ * k_main, v_main : device [n_main][n_heads][head_dim]; k_loc, v_loc :
+ *            [n_loc][n_heads][head_dim].  Either segment may be empty
+ *            (size 0, pointers may be NULL) but not both.
+ * lse      : device float32 [n_heads][n_q] or NULL.
+ * scale <= 0 means 1/sqrt(head_dim).
+ * WA_BF16 runs on the tensor cores (tcgen05, fp32 accumulation in TMEM) and
+ * needs head_dim == 128.  WA_F32 runs fp32 FMA on the CUDA cores and needs
+ * head_dim <= 256 and a multiple of 4.
+ */
+wa_status wa_block_attn(const void* q, int n_q, const void* k_main, const void* v_main, int n_main,
+                        const void* k_loc, const void* v_loc, int n_loc, wa_dtype dt,
+                        int n_heads, int head_dim, float scale, void* o, float* lse,
+                        wa_stream_t stream);
+
+/*
+ * Linformer-style low-rank branch and gate fusion ([WA] HSA, linear branch;
+ * the projection and gate equations are missing on the page and read as
+ * Linformer and a per-head weighted sum):
+ *
+ *   K'[h] = E_K[h]^T [k_main ; k_loc][h],  V'[h] = E_V[h]^T [v_main ; v_loc][h]
+ *   O_lin[i][h] = sum_r softmax_r(scale * q[i][h] . K'[h][r]) V'[h][r]
+ *   accumulate != 0 :  o = w_attn[h] * o + w_lin[h] * O_lin
+ *   accumulate == 0 :  o = O_lin
+ *
+ * e_k, e_v : device [n_heads][n_main+n_loc][rank] of `dt` (rows aligned to
+ *            [main ; local]).  K', V' are accumulated in fp32 and rounded to
+ *            `dt` before the second contraction.
+ * w_attn, w_lin : device float32 [n_heads] or NULL (= all ones).
+ * WA_BF16 only; needs head_dim == 128 and rank a multiple of 128, <= 512.
+ */
+wa_status wa_linear_branch(const void* q, int n_q, const void* k_main, const void* v_main,
+                           int n_main, const void* k_loc, const void* v_loc, int n_loc,
+                           const void* e_k, const void* e_v, int rank, wa_dtype dt,
+                           int n_heads, int head_dim, float scale,
+                           const float* w_attn, const float* w_lin, int accumulate,
+                           void* o, wa_stream_t stream);
+
+/*
+ * Synchronize `stream`, then read and clear this device's status word.
+ * Returns WA_OK, WA_ERR_INDEX (a gather index was out of range),
+ * WA_ERR_TIMEOUT (a kernel wait gave up; the kernel returned early and its
+ * outputs are invalid) or WA_ERR_CUDA (the stream reported an error).
+ */
+wa_status wa_check(wa_stream_t stream);
+
+/* Free this device's scratch arena (after a device synchronize). */
+wa_status wa_shutdown(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* WA_H_ */

@@ -1,0 +1,192 @@
+"""Python binding of libwa (page-retrieval sparse attention on GB300).
+
+Argument marshalling only: each function checks tensor shapes, takes raw
+pointers and the current CUDA stream, and calls the C entry point of the same
+name in ``lib/libwa.so``.  Every step of the path runs in the library's CUDA
+kernels; there is no fallback -- if the library is missing or a call fails,
+an exception is raised.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+__all__ = [
+    "WaError",
+    "lib_path",
+    "load",
+    "wa_page_summarize",
+    "wa_select_pages",
+    "wa_gather_pages",
+    "wa_block_attn",
+    "wa_linear_branch",
+    "wa_check",
+    "wa_shutdown",
+    "wa_version",
+    "EXPORTED_SYMBOLS",
+]
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+_LIB = None
+
+WA_F32, WA_BF16 = 0, 1
+
+# Every symbol include/wa.h declares.
+EXPORTED_SYMBOLS = ("wa_strerror", "wa_version", "wa_page_summarize", "wa_select_pages",
+                    "wa_gather_pages", "wa_block_attn", "wa_linear_branch", "wa_check",
+                    "wa_shutdown")
+
+
+class WaError(RuntimeError):
+    def __init__(self, fn: str, status: int, msg: str):
+        super().__init__(f"{fn} failed: {msg} (status {status})")
+        self.status = status
+
+
+def lib_path() -> str:
+    return os.path.join(HERE, "lib", "libwa.so")
+
+
+def load():
+    """Load lib/libwa.so (built by ``build.build()``) and declare signatures."""
+    global _LIB
+    if _LIB is not None:
+        return _LIB
+    path = lib_path()
+    if not os.path.exists(path):
+        raise RuntimeError(f"{path} is missing: build it with sparse_kv_cache_page_gb300.build.build()")
+    lib = ctypes.CDLL(path)
+    P, I, F = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
+    sig = {
+        "wa_strerror": (ctypes.c_char_p, [I]),
+        "wa_version": (ctypes.c_char_p, []),
+        "wa_page_summarize": (I, [P, I, I, I, I, I, P, P]),
+        "wa_select_pages": (I, [P, I, I, I, I, P, I, P, P, I, I, I, I, P, P, P, P]),
+        "wa_gather_pages": (I, [P, P, I, I, I, I, I, P, P, I, P, P, P]),
+        "wa_block_attn": (I, [P, I, P, P, I, P, P, I, I, I, I, F, P, P, P]),
+        "wa_linear_branch": (I, [P, I, P, P, I, P, P, I, P, P, I, I, I, I, F, P, P, I, P, P]),
+        "wa_check": (I, [P]),
+        "wa_shutdown": (I, []),
+    }
+    for name, (res, args) in sig.items():
+        fn = getattr(lib, name)
+        fn.restype = res
+        fn.argtypes = args
+    _LIB = lib
+    return lib
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _dt(t: torch.Tensor) -> int:
+    if t.dtype == torch.bfloat16:
+        return WA_BF16
+    if t.dtype == torch.float32:
+        return WA_F32
+    raise TypeError(f"unsupported dtype {t.dtype}")
+
+
+def _ok(fn: str, st: int):
+    if st != 0:
+        raise WaError(fn, st, load().wa_strerror(st).decode())
+
+
+def _need(cond: bool, what: str):
+    if not cond:
+        raise ValueError(what)
+
+
+def wa_version() -> str:
+    return load().wa_version().decode()
+
+
+def wa_page_summarize(k_pages: torch.Tensor, kbar_out: torch.Tensor, stream=None):
+    """kbar_out[j,h,:] = mean_t k_pages[j,t,h,:]; k_pages [n_pages][P][H][d]."""
+    _need(k_pages.dim() == 4 and k_pages.is_contiguous(), "k_pages must be contiguous [n][P][H][d]")
+    n, p, h, d = k_pages.shape
+    _need(kbar_out.shape == (n, h, d) and kbar_out.dtype == torch.float32
+          and kbar_out.is_contiguous(), "kbar_out must be float32 [n][H][d]")
+    _ok("wa_page_summarize", load().wa_page_summarize(_ptr(k_pages), _dt(k_pages), n, p, h, d,
+                                                      _ptr(kbar_out), _stream(stream)))
+
+
+def wa_select_pages(q: torch.Tensor, kbar: torch.Tensor, prompt_cur, prompt_chunks,
+                    pages_per_chunk: int, k_p: int, idx_out: torch.Tensor,
+                    scores_out=None, chunk_out=None, stream=None):
+    """Prompt-stage top-1 chunk (skipped when prompt_chunks is None) and
+    page-stage top-k_p; writes ascending page indices to idx_out (int32)."""
+    _need(q.dim() == 3 and q.is_contiguous(), "q must be contiguous [n_q][H][d]")
+    n_q, h, d = q.shape
+    _need(kbar.dim() == 3 and kbar.shape[1:] == (h, d) and kbar.dtype == torch.float32,
+          "kbar must be float32 [n_pages][H][d]")
+    _need(idx_out.dtype == torch.int32 and idx_out.numel() >= k_p, "idx_out must be int32 [k_p]")
+    n_chunks, pdim = 0, 0
+    if prompt_chunks is not None:
+        n_chunks, pdim = prompt_chunks.shape
+        _need(prompt_cur is not None and prompt_cur.numel() == pdim
+              and prompt_chunks.dtype == torch.float32 and prompt_cur.dtype == torch.float32,
+              "prompt embeddings must be float32")
+    _ok("wa_select_pages", load().wa_select_pages(
+        _ptr(q), _dt(q), n_q, h, d, _ptr(kbar), kbar.shape[0], _ptr(prompt_cur),
+        _ptr(prompt_chunks), n_chunks, pdim, pages_per_chunk, k_p, _ptr(idx_out),
+        _ptr(scores_out), _ptr(chunk_out), _stream(stream)))
+
+
+def wa_gather_pages(k_pages: torch.Tensor, v_pages, idx_dev, idx_host, k_buf: torch.Tensor,
+                    v_buf, stream=None):
+    """k_buf[s*P + t] = k_pages[idx[s]][t] (likewise v).  Device pages use
+    idx_dev (device int32); pinned host pages use idx_host (host int32)."""
+    _need(k_pages.dim() == 4 and k_pages.is_contiguous(), "k_pages must be contiguous [n][P][H][d]")
+    n, p, h, d = k_pages.shape
+    k_p = (idx_dev if idx_dev is not None else idx_host).numel()
+    _need(k_buf.numel() == k_p * p * h * d and k_buf.dtype == k_pages.dtype, "k_buf size/dtype")
+    _ok("wa_gather_pages", load().wa_gather_pages(
+        _ptr(k_pages), _ptr(v_pages), _dt(k_pages), n, p, h, d, _ptr(idx_dev), _ptr(idx_host),
+        k_p, _ptr(k_buf), _ptr(v_buf), _stream(stream)))
+
+
+def _rows(t):
+    return 0 if t is None else t.shape[0]
+
+
+def wa_block_attn(q: torch.Tensor, k_main, v_main, k_loc, v_loc, o: torch.Tensor, lse=None,
+                  scale: float = 0.0, stream=None):
+    """o = softmax(q [k_main; k_loc]^T * scale) [v_main; v_loc]; lse [H][n_q] optional."""
+    _need(q.dim() == 3 and q.is_contiguous() and o.shape == q.shape and o.dtype == q.dtype,
+          "q and o must be contiguous [n_q][H][d] of one dtype")
+    n_q, h, d = q.shape
+    _ok("wa_block_attn", load().wa_block_attn(
+        _ptr(q), n_q, _ptr(k_main), _ptr(v_main), _rows(k_main), _ptr(k_loc), _ptr(v_loc),
+        _rows(k_loc), _dt(q), h, d, float(scale), _ptr(o), _ptr(lse), _stream(stream)))
+
+
+def wa_linear_branch(q: torch.Tensor, k_main, v_main, k_loc, v_loc, e_k: torch.Tensor,
+                     e_v: torch.Tensor, o: torch.Tensor, w_attn=None, w_lin=None,
+                     accumulate: bool = True, scale: float = 0.0, stream=None):
+    """Linformer branch; o = w_attn*o + w_lin*O_lin (accumulate) or o = O_lin."""
+    n_q, h, d = q.shape
+    rank = e_k.shape[-1]
+    _ok("wa_linear_branch", load().wa_linear_branch(
+        _ptr(q), n_q, _ptr(k_main), _ptr(v_main), _rows(k_main), _ptr(k_loc), _ptr(v_loc),
+        _rows(k_loc), _ptr(e_k), _ptr(e_v), rank, _dt(q), h, d, float(scale), _ptr(w_attn),
+        _ptr(w_lin), int(bool(accumulate)), _ptr(o), _stream(stream)))
+
+
+def wa_check(stream=None):
+    """Synchronize the stream and raise if a kernel recorded an error."""
+    _ok("wa_check", load().wa_check(_stream(stream)))
+
+
+def wa_shutdown():
+    _ok("wa_shutdown", load().wa_shutdown())

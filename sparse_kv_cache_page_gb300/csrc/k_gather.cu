@@ -1,0 +1,84 @@
+// Gather of the retrieved pages into one contiguous KV buffer.
+//
+// WorldAttention (review page), Fig. 1 custom-kernels prong: retrieved pages
+// are reorganised into a contiguous buffer so that attention reads dense
+// memory; the page's Tab. 9 breakdown puts "KV reconstruction + contiguous
+// copy" at 31% of HSA time.  Inferix (summary page), KV Cache Manager:
+// index-based selective fetch of cached blocks.
+//
+// A page is one contiguous slab, so the gather is 2*k_p slab copies whose
+// source addresses come from device memory (the indices never visit the
+// host).  Each CTA moves one 64 KiB span of one slab with 16-byte loads,
+// all loads of a thread issued before its stores.
+#include "wa_internal.cuh"
+
+namespace wa {
+namespace {
+
+constexpr int kThreads = 256;
+constexpr int kUnroll = 8;                                    // 16 B vectors per thread per span
+constexpr size_t kSpan = (size_t)kThreads * kUnroll * 16;     // 32 KiB per CTA iteration
+
+__global__ void __launch_bounds__(kThreads)
+k_gather_pages(const uint4* __restrict__ k_pages, const uint4* __restrict__ v_pages,
+               size_t page_vecs, int n_pages, const int32_t* __restrict__ idx, int k_p,
+               uint4* __restrict__ k_buf, uint4* __restrict__ v_buf, size_t spans_per_slab,
+               Ctrl* ctrl) {
+  const int n_tensors = v_pages ? 2 : 1;
+  const size_t total = spans_per_slab * (size_t)k_p * n_tensors;
+  for (size_t w = blockIdx.x; w < total; w += gridDim.x) {
+    const size_t span = w % spans_per_slab;
+    const size_t rest = w / spans_per_slab;
+    const int slot = (int)(rest % k_p);
+    const int tensor = (int)(rest / k_p);
+    const int page = __ldg(idx + slot);
+    const uint4* src = tensor ? v_pages : k_pages;
+    uint4* dst = (tensor ? v_buf : k_buf) + (size_t)slot * page_vecs;
+    const size_t v0 = span * (kSpan / 16);
+    if (page < 0 || page >= n_pages) {
+      // bad index: zero this slot and record it (no trap)
+      for (int u = 0; u < kUnroll; ++u) {
+        const size_t v = v0 + (size_t)u * kThreads + threadIdx.x;
+        if (v < page_vecs) dst[v] = make_uint4(0, 0, 0, 0);
+      }
+      if (threadIdx.x == 0 && span == 0) atomicOr(&ctrl->status, kStatusIndex);
+      continue;
+    }
+    src += (size_t)page * page_vecs;
+    uint4 r[kUnroll];
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u) {
+      const size_t v = v0 + (size_t)u * kThreads + threadIdx.x;
+      if (v < page_vecs) r[u] = __ldcs(src + v);
+    }
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u) {
+      const size_t v = v0 + (size_t)u * kThreads + threadIdx.x;
+      if (v < page_vecs) dst[v] = r[u];
+    }
+  }
+}
+
+}  // namespace
+
+wa_status launch_gather_device(const void* k_pages, const void* v_pages, size_t page_bytes,
+                               int n_pages, const int32_t* idx_dev, int k_p, void* k_buf,
+                               void* v_buf, cudaStream_t s) {
+  Ctrl* ctrl = nullptr;
+  wa_status rc = get_ctrl(&ctrl);
+  if (rc != WA_OK) return rc;
+  const size_t page_vecs = page_bytes / 16;
+  const size_t spans = (page_bytes + kSpan - 1) / kSpan;
+  const size_t total = spans * (size_t)k_p * (v_pages ? 2 : 1);
+  int dev = 0, sms = 148;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  size_t grid = (size_t)sms * 8;   // 8 resident CTAs per SM, grid-stride over spans
+  if (grid > total) grid = total;
+  k_gather_pages<<<(unsigned)grid, kThreads, 0, s>>>(
+      (const uint4*)k_pages, (const uint4*)v_pages, page_vecs, n_pages, idx_dev, k_p,
+      (uint4*)k_buf, (uint4*)v_buf, spans, ctrl);
+  return cuda_status(cudaPeekAtLastError());
+}
+
+}  // namespace wa

@@ -1,0 +1,447 @@
+// Page summaries and two-stage page retrieval.
+//
+// WorldAttention (review page), HKV section (paper §3.1 HKV): every cached
+// 8-frame page is summarised by its mean key; a chunk is scored through its
+// mean query, alpha_{m,j} = Qbar^T Kbar_{m,j} / sqrt(d_k), after a prompt-
+// stage top-1 chunk pick by cosine similarity; the top-K_p pages are kept.
+//
+// Both kernels are HBM-bound column sums over token rows: each thread owns
+// one or more 16-byte column vectors of a token row and walks rows with
+// several independent loads in flight; CTAs of one reduction meet through a
+// "last CTA finishes" ticket (no spin-wait): every CTA stores its partial
+// sums, fences, and takes a ticket; the CTA holding the last ticket adds the
+// partials in a fixed order (deterministic) and runs the tail work.
+#include <math.h>
+
+#include "wa_internal.cuh"
+
+namespace wa {
+namespace {
+
+constexpr int kThreads = 256;
+constexpr int kTargetCtas = 152 * 8;     // 8 resident 256-thread CTAs per SM
+constexpr unsigned kSelectCounter = 4095;
+
+template <typename T> struct VecOf;
+template <> struct VecOf<__nv_bfloat16> { static constexpr int E = 8; };
+template <> struct VecOf<float> { static constexpr int E = 4; };
+
+__device__ __forceinline__ void load_vec(const __nv_bfloat16* p, float (&f)[8]) {
+  uint4 u = __ldg(reinterpret_cast<const uint4*>(p));
+  const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    f[2 * i] = __uint_as_float(w[i] << 16);
+    f[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
+  }
+}
+__device__ __forceinline__ void load_vec(const float* p, float (&f)[4]) {
+  float4 v = __ldg(reinterpret_cast<const float4*>(p));
+  f[0] = v.x; f[1] = v.y; f[2] = v.z; f[3] = v.w;
+}
+
+// Column sums of rows [r0, r1) of a [rows][row_elems] matrix into red[0..row_elems).
+// Thread layout: the first nvec*R threads; vec = tid % nvec, row phase = tid / nvec.
+// VPT > 1 only when R == 1 (nvec > blockDim): thread handles vec, vec+256, ...
+template <typename T, int VPT>
+__device__ void colsum_rows(const T* __restrict__ base, int row_elems, int nvec, int R, int r0,
+                            int r1, float* red /* smem, R*row_elems floats */) {
+  constexpr int E = VecOf<T>::E;
+  constexpr int U = VPT == 1 ? 8 : (VPT == 2 ? 4 : 2);   // rows in flight
+  const int tid = threadIdx.x;
+  const bool active = tid < nvec * R || VPT > 1;
+  const int vec = VPT > 1 ? tid : tid % nvec;
+  const int rp = VPT > 1 ? 0 : tid / nvec;
+  float acc[VPT][E];
+#pragma unroll
+  for (int v = 0; v < VPT; ++v)
+#pragma unroll
+    for (int e = 0; e < E; ++e) acc[v][e] = 0.f;
+  if (active) {
+    int r = r0 + rp;
+    for (; r + (U - 1) * R < r1; r += U * R) {
+      float f[U][VPT][E];
+#pragma unroll
+      for (int u = 0; u < U; ++u)
+#pragma unroll
+        for (int v = 0; v < VPT; ++v) {
+          const int cv = vec + v * kThreads;
+          if (VPT == 1 || cv < nvec)
+            load_vec(base + (size_t)(r + u * R) * row_elems + (size_t)cv * E, f[u][v]);
+          else
+#pragma unroll
+            for (int e = 0; e < E; ++e) f[u][v][e] = 0.f;
+        }
+#pragma unroll
+      for (int u = 0; u < U; ++u)
+#pragma unroll
+        for (int v = 0; v < VPT; ++v)
+#pragma unroll
+          for (int e = 0; e < E; ++e) acc[v][e] += f[u][v][e];
+    }
+    for (; r < r1; r += R) {
+#pragma unroll
+      for (int v = 0; v < VPT; ++v) {
+        const int cv = vec + v * kThreads;
+        if (VPT == 1 || cv < nvec) {
+          float f[E];
+          load_vec(base + (size_t)r * row_elems + (size_t)cv * E, f);
+#pragma unroll
+          for (int e = 0; e < E; ++e) acc[v][e] += f[e];
+        }
+      }
+    }
+#pragma unroll
+    for (int v = 0; v < VPT; ++v) {
+      const int cv = vec + v * kThreads;
+      if (VPT == 1 || cv < nvec)
+#pragma unroll
+        for (int e = 0; e < E; ++e) red[rp * row_elems + cv * E + e] = acc[v][e];
+    }
+  }
+  __syncthreads();
+  // fold the R row phases (fixed order)
+  if (R > 1) {
+    for (int c = tid; c < row_elems; c += blockDim.x) {
+      float s = red[c];
+      for (int p = 1; p < R; ++p) s += red[p * row_elems + c];
+      red[c] = s;
+    }
+    __syncthreads();
+  }
+}
+
+// Returns true in every thread of the CTA that took the last ticket.
+__device__ bool last_ticket(unsigned* counter, unsigned n) {
+  __shared__ unsigned s_ticket;
+  __threadfence();
+  __syncthreads();
+  if (threadIdx.x == 0) s_ticket = atomicAdd(counter, 1u);
+  __syncthreads();
+  const bool last = (s_ticket == n - 1);
+  if (last) __threadfence();
+  return last;
+}
+
+// ---------------------------------------------------------------------------
+// page summaries
+// ---------------------------------------------------------------------------
+template <typename T, int VPT>
+__global__ void __launch_bounds__(kThreads)
+k_page_summarize(const T* __restrict__ pages, int page_tokens, int row_elems, int nvec, int R,
+                 int splits, int rows_per_split, float* __restrict__ partial,
+                 float* __restrict__ kbar, Ctrl* ctrl) {
+  extern __shared__ float red[];
+  const int j = blockIdx.x / splits, s = blockIdx.x % splits;
+  const int r0 = s * rows_per_split;
+  const int r1 = min(page_tokens, r0 + rows_per_split);
+  const T* base = pages + (size_t)j * page_tokens * row_elems;
+  colsum_rows<T, VPT>(base, row_elems, nvec, R, r0, r1, red);
+  const float inv = 1.0f / (float)page_tokens;
+  if (splits == 1) {
+    for (int c = threadIdx.x; c < row_elems; c += blockDim.x)
+      kbar[(size_t)j * row_elems + c] = red[c] * inv;
+    return;
+  }
+  float* mine = partial + ((size_t)j * splits + s) * row_elems;
+  for (int c = threadIdx.x; c < row_elems; c += blockDim.x) mine[c] = red[c];
+  if (!last_ticket(&ctrl->counters[j], (unsigned)splits)) return;
+  const float* pj = partial + (size_t)j * splits * row_elems;
+  for (int c = threadIdx.x; c < row_elems; c += blockDim.x) {
+    float acc = 0.f;
+    for (int p = 0; p < splits; ++p) acc += __ldcg(pj + (size_t)p * row_elems + c);
+    kbar[(size_t)j * row_elems + c] = acc * inv;
+  }
+  if (threadIdx.x == 0) ctrl->counters[j] = 0u;
+}
+
+// ---------------------------------------------------------------------------
+// select: mean query -> prompt top-1 -> page scores -> top-K_p
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+// Orderable key: ascending key = descending score, then ascending candidate.
+__device__ __forceinline__ unsigned long long score_key(float a, unsigned c) {
+  if (a == 0.f) a = 0.f;   // -0 ties +0
+  unsigned u = __float_as_uint(a);
+  u = (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+  return ((unsigned long long)(~u) << 32) | c;
+}
+
+__device__ void bitonic_sort(unsigned long long* keys, int n2) {
+  for (int k = 2; k <= n2; k <<= 1) {
+    for (int j = k >> 1; j > 0; j >>= 1) {
+      for (int i = threadIdx.x; i < n2; i += blockDim.x) {
+        const int ixj = i ^ j;
+        if (ixj > i) {
+          const bool up = (i & k) == 0;
+          const unsigned long long a = keys[i], b = keys[ixj];
+          if ((a > b) == up) { keys[i] = b; keys[ixj] = a; }
+        }
+      }
+      __syncthreads();
+    }
+  }
+}
+
+struct SelectArgs {
+  int n_q, row_elems, nvec, R, splits, rows_per_split;
+  float* partial;
+  const float* kbar;
+  int n_pages, head_dim;
+  const float* prompt_cur;
+  const float* prompt_chunks;
+  int n_chunks, prompt_dim, ppc, k_p;
+  int32_t* idx_out;
+  float* scores_out;
+  int32_t* chunk_out;
+  Ctrl* ctrl;
+  int n_cand_max2;   // power of two >= candidate count
+};
+
+template <typename T, int VPT>
+__global__ void __launch_bounds__(kThreads)
+k_select_pages(const T* __restrict__ q, SelectArgs a) {
+  extern __shared__ float smem[];
+  // phase A: partial column sums of this CTA's query rows
+  const int s = blockIdx.x;
+  const int r0 = s * a.rows_per_split;
+  const int r1 = min(a.n_q, r0 + a.rows_per_split);
+  colsum_rows<T, VPT>(q, a.row_elems, a.nvec, a.R, r0, r1, smem);
+  float* mine = a.partial + (size_t)s * a.row_elems;
+  for (int c = threadIdx.x; c < a.row_elems; c += blockDim.x) mine[c] = smem[c];
+  if (!last_ticket(&a.ctrl->counters[kSelectCounter], (unsigned)a.splits)) return;
+
+  // phase B (one CTA).  smem: qbar[row_elems] | alpha[n2] | keys[n2]
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nwarps = blockDim.x >> 5;
+  float* qbar = smem;
+  float* alpha = qbar + ((a.row_elems + 3) & ~3);
+  unsigned long long* keys =
+      reinterpret_cast<unsigned long long*>(alpha + ((a.n_cand_max2 + 3) & ~3));
+  const float inv_nq = 1.0f / (float)a.n_q;
+  for (int c = tid; c < a.row_elems; c += blockDim.x) {
+    float acc = 0.f;
+    for (int p = 0; p < a.splits; ++p) acc += __ldcg(a.partial + (size_t)p * a.row_elems + c);
+    qbar[c] = acc * inv_nq;
+  }
+
+  // stage 1: prompt top-1 chunk
+  __shared__ float s_red[32];
+  __shared__ int s_idx[32];
+  __shared__ int s_chunk;
+  int cand0 = 0, n_cand = a.n_pages, chunk = -1;
+  if (a.n_chunks > 0) {
+    float np = 0.f;
+    for (int i = tid; i < a.prompt_dim; i += blockDim.x) {
+      const float v = a.prompt_cur[i];
+      np += v * v;
+    }
+    np = warp_sum(np);
+    if (lane == 0) s_red[warp] = np;
+    __syncthreads();
+    if (warp == 0) {
+      float t = lane < nwarps ? s_red[lane] : 0.f;
+      t = warp_sum(t);
+      if (lane == 0) s_red[31] = t;
+    }
+    __syncthreads();
+    np = s_red[31];
+    __syncthreads();
+    float best = -INFINITY;
+    int best_m = 0x7fffffff;
+    for (int m = warp; m < a.n_chunks; m += nwarps) {
+      const float* cm = a.prompt_chunks + (size_t)m * a.prompt_dim;
+      float dot = 0.f, nc = 0.f;
+      for (int i = lane; i < a.prompt_dim; i += 32) {
+        const float c = cm[i];
+        dot += a.prompt_cur[i] * c;
+        nc += c * c;
+      }
+      dot = warp_sum(dot);
+      nc = warp_sum(nc);
+      const float cosv = (np > 0.f && nc > 0.f) ? dot / (sqrtf(np) * sqrtf(nc)) : 0.f;
+      if (cosv > best) { best = cosv; best_m = m; }   // ascending m: first wins a tie
+    }
+    if (lane == 0) { s_red[warp] = best; s_idx[warp] = best_m; }
+    __syncthreads();
+    if (tid == 0) {
+      float b = s_red[0];
+      int bm = s_idx[0];
+      for (int w = 1; w < nwarps; ++w)
+        if (s_red[w] > b || (s_red[w] == b && s_idx[w] < bm)) { b = s_red[w]; bm = s_idx[w]; }
+      s_chunk = bm;
+    }
+    __syncthreads();
+    chunk = s_chunk;
+    cand0 = chunk * a.ppc;
+    n_cand = a.ppc;
+  } else {
+    __syncthreads();
+  }
+
+  // stage 2: alpha_j = sum_c qbar[c] * kbar[j][c] / sqrt(d) over the candidates
+  const float inv_sqrt_d = 1.0f / sqrtf((float)a.head_dim);
+  for (int c = warp; c < n_cand; c += nwarps) {
+    const float* kb = a.kbar + (size_t)(cand0 + c) * a.row_elems;
+    float dot = 0.f;
+    for (int e = lane; e < a.row_elems; e += 32) dot += qbar[e] * kb[e];
+    dot = warp_sum(dot);
+    if (lane == 0) alpha[c] = dot * inv_sqrt_d;
+  }
+  __syncthreads();
+  int n2 = 1;
+  while (n2 < n_cand) n2 <<= 1;
+  for (int i = tid; i < n2; i += blockDim.x)
+    keys[i] = i < n_cand ? score_key(alpha[i], (unsigned)i) : ~0ull;
+  __syncthreads();
+  bitonic_sort(keys, n2);
+  // the first k_p keys are the selection; re-sort them by candidate index
+  int k2 = 1;
+  while (k2 < a.k_p) k2 <<= 1;
+  for (int i = tid; i < k2; i += blockDim.x)
+    keys[i] = i < a.k_p ? (keys[i] & 0xffffffffull) : ~0ull;
+  __syncthreads();
+  bitonic_sort(keys, k2);
+  for (int i = tid; i < a.k_p; i += blockDim.x) {
+    const int c = (int)(keys[i] & 0xffffffffull);
+    a.idx_out[i] = cand0 + c;
+    if (a.scores_out) a.scores_out[i] = alpha[c];
+  }
+  if (tid == 0) {
+    if (a.chunk_out) a.chunk_out[0] = chunk;
+    a.ctrl->counters[kSelectCounter] = 0u;
+  }
+}
+
+struct Plan {
+  int nvec, R, vpt, threads;
+};
+
+template <typename T>
+Plan plan_rows(int row_elems) {
+  Plan p;
+  p.nvec = row_elems / VecOf<T>::E;
+  if (p.nvec <= kThreads) {
+    p.R = kThreads / p.nvec;
+    p.vpt = 1;
+  } else {
+    p.R = 1;
+    p.vpt = (p.nvec + kThreads - 1) / kThreads;
+    p.vpt = p.vpt <= 2 ? 2 : (p.vpt <= 4 ? 4 : 8);
+  }
+  p.threads = kThreads;
+  return p;
+}
+
+template <typename T>
+wa_status summarize_t(const T* pages, int n_pages, int page_tokens, int row_elems, float* kbar,
+                      cudaStream_t st) {
+  Plan p = plan_rows<T>(row_elems);
+  int splits = kTargetCtas / n_pages;
+  if (splits < 1) splits = 1;
+  const int max_splits = (page_tokens + 63) / 64;   // at least 64 rows per CTA
+  if (splits > max_splits) splits = max_splits;
+  if (splits > 64) splits = 64;
+  const int rps = (page_tokens + splits - 1) / splits;
+  splits = (page_tokens + rps - 1) / rps;
+  Scratch sc;
+  wa_status rc = get_scratch((size_t)n_pages * splits * row_elems * sizeof(float), &sc);
+  if (rc != WA_OK) return rc;
+  const size_t smem = (size_t)p.R * row_elems * sizeof(float);
+  dim3 grid((unsigned)(splits * n_pages));
+  switch (p.vpt) {
+#define WA_CASE(V)                                                                          \
+  case V:                                                                                   \
+    if (smem > 48 * 1024)                                                                   \
+      cudaFuncSetAttribute(k_page_summarize<T, V>, cudaFuncAttributeMaxDynamicSharedMemorySize, \
+                           (int)smem);                                                      \
+    k_page_summarize<T, V><<<grid, p.threads, smem, st>>>(pages, page_tokens, row_elems,    \
+                                                          p.nvec, p.R, splits, rps,         \
+                                                          (float*)sc.data, kbar, sc.ctrl);  \
+    break;
+    WA_CASE(1) WA_CASE(2) WA_CASE(4) WA_CASE(8)
+#undef WA_CASE
+    default: return WA_ERR_SHAPE;
+  }
+  return cuda_status(cudaPeekAtLastError());
+}
+
+template <typename T>
+wa_status select_t(const T* q, SelectArgs a, cudaStream_t st) {
+  Plan p = plan_rows<T>(a.row_elems);
+  int splits = a.n_q / 32;
+  if (splits < 1) splits = 1;
+  if (splits > 304) splits = 304;
+  const int rps = (a.n_q + splits - 1) / splits;
+  splits = (a.n_q + rps - 1) / rps;
+  Scratch sc;
+  wa_status rc = get_scratch((size_t)splits * a.row_elems * sizeof(float), &sc);
+  if (rc != WA_OK) return rc;
+  int n_cand = a.n_chunks > 0 ? a.ppc : a.n_pages;
+  int n2 = 1;
+  while (n2 < n_cand) n2 <<= 1;
+  a.nvec = p.nvec;
+  a.R = p.R;
+  a.splits = splits;
+  a.rows_per_split = rps;
+  a.partial = (float*)sc.data;
+  a.ctrl = sc.ctrl;
+  a.n_cand_max2 = n2;
+  size_t smem_a = (size_t)p.R * a.row_elems * sizeof(float);
+  size_t smem_b = (size_t)((a.row_elems + 3) & ~3) * 4 + (size_t)((n2 + 3) & ~3) * 4 +
+                  (size_t)n2 * 8;
+  size_t smem = smem_a > smem_b ? smem_a : smem_b;
+  switch (p.vpt) {
+#define WA_CASE(V)                                                                          \
+  case V:                                                                                   \
+    if (smem > 48 * 1024)                                                                   \
+      cudaFuncSetAttribute(k_select_pages<T, V>, cudaFuncAttributeMaxDynamicSharedMemorySize, \
+                           (int)smem);                                                      \
+    k_select_pages<T, V><<<splits, p.threads, smem, st>>>(q, a);                            \
+    break;
+    WA_CASE(1) WA_CASE(2) WA_CASE(4) WA_CASE(8)
+#undef WA_CASE
+    default: return WA_ERR_SHAPE;
+  }
+  return cuda_status(cudaPeekAtLastError());
+}
+
+}  // namespace
+
+wa_status launch_page_summarize(const void* k_pages, wa_dtype dt, int n_pages, int page_tokens,
+                                int row_elems, float* kbar_out, cudaStream_t s) {
+  if (dt == WA_BF16)
+    return summarize_t((const __nv_bfloat16*)k_pages, n_pages, page_tokens, row_elems, kbar_out,
+                       s);
+  return summarize_t((const float*)k_pages, n_pages, page_tokens, row_elems, kbar_out, s);
+}
+
+wa_status launch_select_pages(const void* q, wa_dtype dt, int n_q, int n_heads, int head_dim,
+                              const float* kbar, int n_pages, const float* prompt_cur,
+                              const float* prompt_chunks, int n_chunks, int prompt_dim,
+                              int pages_per_chunk, int k_p, int32_t* idx_out, float* scores_out,
+                              int32_t* chunk_out, cudaStream_t s) {
+  SelectArgs a{};
+  a.n_q = n_q;
+  a.row_elems = n_heads * head_dim;
+  a.kbar = kbar;
+  a.n_pages = n_pages;
+  a.head_dim = head_dim;
+  a.prompt_cur = prompt_cur;
+  a.prompt_chunks = prompt_chunks;
+  a.n_chunks = n_chunks;
+  a.prompt_dim = prompt_dim;
+  a.ppc = pages_per_chunk;
+  a.k_p = k_p;
+  a.idx_out = idx_out;
+  a.scores_out = scores_out;
+  a.chunk_out = chunk_out;
+  if (dt == WA_BF16) return select_t((const __nv_bfloat16*)q, a, s);
+  return select_t((const float*)q, a, s);
+}
+
+}  // namespace wa

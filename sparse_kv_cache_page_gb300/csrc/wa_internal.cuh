@@ -1,0 +1,82 @@
+// Internal declarations shared by the libwa translation units.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+#include "../../include/wa.h"
+
+namespace wa {
+
+// Device status word bits (OR-ed by kernels, read and cleared by wa_check).
+enum : int {
+  kStatusIndex = 1,     // a gather index was outside [0, n_pages)
+  kStatusTimeout = 2,   // a bounded wait gave up
+};
+
+// Per-device control block at the start of the scratch arena.
+struct Ctrl {
+  int status;           // kStatus* bits
+  int pad[31];
+  unsigned int counters[4096];   // zero between launches; "last CTA" tickets
+};
+
+// Scratch arena of the current device: Ctrl block + `bytes` of data.
+// Grows (after cudaDeviceSynchronize) when a call needs more.
+struct Scratch {
+  Ctrl* ctrl;
+  void* data;
+  size_t bytes;
+};
+wa_status get_scratch(size_t bytes, Scratch* out);
+
+// Status word of the current device (allocates the arena if needed).
+wa_status get_ctrl(Ctrl** out);
+
+inline wa_status cuda_status(cudaError_t e) { return e == cudaSuccess ? WA_OK : WA_ERR_CUDA; }
+
+inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// 2-D bf16 TMA descriptor over a row-major [rows][cols] matrix with a row
+// stride of `row_stride` elements; box = box_rows x box_cols (box_cols * 2
+// bytes <= 128), 128-byte swizzle, out-of-range rows and columns read as 0.
+wa_status make_tmap_2d_bf16(CUtensorMap* map, const void* base, uint64_t cols, uint64_t rows,
+                            uint64_t row_stride, uint32_t box_cols, uint32_t box_rows);
+
+// ---------------------------------------------------------------------------
+// kernel launchers (one per translation unit / kernel family)
+// ---------------------------------------------------------------------------
+wa_status launch_page_summarize(const void* k_pages, wa_dtype dt, int n_pages, int page_tokens,
+                                int row_elems, float* kbar_out, cudaStream_t s);
+
+wa_status launch_select_pages(const void* q, wa_dtype dt, int n_q, int n_heads, int head_dim,
+                              const float* kbar, int n_pages, const float* prompt_cur,
+                              const float* prompt_chunks, int n_chunks, int prompt_dim,
+                              int pages_per_chunk, int k_p, int32_t* idx_out, float* scores_out,
+                              int32_t* chunk_out, cudaStream_t s);
+
+wa_status launch_gather_device(const void* k_pages, const void* v_pages, size_t page_bytes,
+                               int n_pages, const int32_t* idx_dev, int k_p, void* k_buf,
+                               void* v_buf, cudaStream_t s);
+
+wa_status launch_attn_f32(const float* q, int n_q, const float* k_main, const float* v_main,
+                          int n_main, const float* k_loc, const float* v_loc, int n_loc,
+                          int n_heads, int head_dim, float scale, float* o, float* lse,
+                          cudaStream_t s);
+
+// bf16 tensor-core attention.  out_w_old/out_w_new: per-head fusion weights
+// for the epilogue o = w_old[h]*o + w_new[h]*O (accumulate != 0), may be NULL.
+wa_status launch_attn_tc(const void* q, int n_q, const void* k_main, const void* v_main,
+                         int n_main, const void* k_loc, const void* v_loc, int n_loc,
+                         int n_heads, float scale, void* o, float* lse, int accumulate,
+                         const float* w_old, const float* w_new, cudaStream_t s);
+
+wa_status launch_linear_branch(const void* q, int n_q, const void* k_main, const void* v_main,
+                               int n_main, const void* k_loc, const void* v_loc, int n_loc,
+                               const void* e_k, const void* e_v, int rank, int n_heads,
+                               float scale, const float* w_attn, const float* w_lin,
+                               int accumulate, void* o, cudaStream_t s);
+
+}  // namespace wa

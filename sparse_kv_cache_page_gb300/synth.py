@@ -84,7 +84,8 @@ def make_chunk_case(name: str, *, n_heads: int, head_dim: int, page_tokens: int,
                     pages_per_chunk: int, n_chunks: int, prompt_dim: int, k_p: int, n_q: int,
                     n_loc: int, dtype=torch.bfloat16, device="cpu", layer: int = 0,
                     plant_pages=None, plant_strength: float = 0.0,
-                    recall_chunk: int | None = None, std: float = 1.0) -> ChunkCase:
+                    recall_chunk: int | None = None, std: float = 1.0,
+                    lazy_pages: bool = False) -> ChunkCase:
     """Draw one chunk case.  Optional structure (input construction only):
 
     * ``plant_pages`` / ``plant_strength``: a per-head direction u_h ~ N(0,1)
@@ -92,21 +93,31 @@ def make_chunk_case(name: str, *, n_heads: int, head_dim: int, page_tokens: int,
       every query, so those pages are the relevant ones.
     * ``recall_chunk``: the current prompt embedding is that past chunk's
       embedding plus half-scale noise (the "throw the red ball again" recall).
+    * ``lazy_pages``: leave the page bank undrawn; ``case.extra["page"](j)``
+      draws page j on demand.
     """
     H, d = n_heads, head_dim
     c = ChunkCase(name, H, d, page_tokens, n_pages, pages_per_chunk, n_chunks, prompt_dim, k_p,
                   n_q, n_loc, dtype)
     s = lambda t: seed_of(name, layer, t)  # noqa: E731
-    kp = torch.empty((n_pages, page_tokens, H, d), dtype=dtype, device=device)
-    vp = torch.empty_like(kp)
     u = normal((H, d), s("plant_dir"), device) if plant_pages else None
-    for j in range(n_pages):
-        kj = normal((page_tokens, H, d), s(("k_page", j)), device, std=std)
+
+    def page(j, dev=device):
+        """(K, V) of page j, [P][H][d]; the same values whether drawn eagerly
+        with the bank or later on their own."""
+        kj = normal((page_tokens, H, d), s(("k_page", j)), dev, std=std)
         if plant_pages and j in plant_pages:
-            kj += plant_strength * u
-        kp[j] = kj.to(dtype)
-        vp[j] = normal((page_tokens, H, d), s(("v_page", j)), device, dtype, std=std)
-    c.k_pages, c.v_pages = kp, vp
+            kj += plant_strength * u.to(dev)
+        vj = normal((page_tokens, H, d), s(("v_page", j)), dev, dtype, std=std)
+        return kj.to(dtype), vj
+
+    c.extra["page"] = page
+    if not lazy_pages:
+        kp = torch.empty((n_pages, page_tokens, H, d), dtype=dtype, device=device)
+        vp = torch.empty_like(kp)
+        for j in range(n_pages):
+            kp[j], vp[j] = page(j)
+        c.k_pages, c.v_pages = kp, vp
     q = normal((n_q, H, d), s("q"), device, std=std)
     if plant_pages:
         q += plant_strength * u

@@ -1,0 +1,152 @@
+"""GPU parity of block attention through the C ABI against the fp64 oracle:
+bf16 on the tensor cores (max|err| <= 1e-2, mean|err| <= 1e-3) and fp32 on
+the CUDA cores (max|err| <= 1e-5), including ragged tails, empty segments,
+peaked queries (so that a wrong weighting cannot hide inside a broad
+softmax) and the full one-layer WorldAttention shape on sampled rows."""
+
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle as O
+import sparse_kv_cache_page_gb300 as wa
+from sparse_kv_cache_page_gb300 import synth
+from tests._util import LSE_ABS, assert_attn_close, f64, np_of
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+
+
+def _run(q, km, vm, kl, vl, scale=0.0):
+    o = torch.empty_like(q)
+    lse = torch.empty((q.shape[1], q.shape[0]), dtype=torch.float32, device=DEV)
+    d = lambda t: None if t is None else t.to(DEV)  # noqa: E731
+    wa.wa_block_attn(q.to(DEV), d(km), d(vm), d(kl), d(vl), o, lse, scale)
+    wa.wa_check()
+    return o, lse
+
+
+def _oracle(q, km, vm, kl, vl, rows=None, scale=None):
+    n = lambda t: None if t is None else np_of(t)  # noqa: E731
+    return O.block_attn(np_of(q), n(km), n(vm), n(kl), n(vl), scale=scale, rows=rows)
+
+
+def _case(n_q, n_main, n_loc, H, d, dtype, seed, std=1.0):
+    s = lambda *a: synth.seed_of("attn", seed, *a)  # noqa: E731
+    mk = lambda n, t: None if n == 0 else synth.normal((n, H, d), s(t), dtype=dtype, std=std)  # noqa: E731
+    return (synth.normal((n_q, H, d), s("q"), dtype=dtype, std=std), mk(n_main, "km"),
+            mk(n_main, "vm"), mk(n_loc, "kl"), mk(n_loc, "vl"))
+
+
+@pytest.mark.parametrize("n_q,n_main,n_loc,H", [
+    (16, 64, 16, 1),          # the tiny fp32 workload
+    (37, 100, 0, 3),
+    (5, 0, 33, 2),
+    (130, 257, 31, 2),
+])
+def test_attn_f32(n_q, n_main, n_loc, H):
+    q, km, vm, kl, vl = _case(n_q, n_main, n_loc, H, 64, torch.float32, 1)
+    o, lse = _run(q.to(DEV).contiguous(), km, vm, kl, vl)
+    ref_o, ref_lse = _oracle(q, km, vm, kl, vl)
+    assert_attn_close(o, ref_o, torch.float32, "fp32 attention")
+    assert np.abs(f64(lse) - ref_lse).max() <= 1e-5
+
+
+def test_attn_f32_head_dim_256_and_scale():
+    q, km, vm, kl, vl = _case(9, 70, 5, 2, 256, torch.float32, 2)
+    o, lse = _run(q.to(DEV), km, vm, kl, vl, scale=0.03)
+    ref_o, ref_lse = _oracle(q, km, vm, kl, vl, scale=0.03)
+    assert_attn_close(o, ref_o, torch.float32, "fp32 d=256")
+    assert np.abs(f64(lse) - ref_lse).max() <= 1e-5
+
+
+@pytest.mark.parametrize("n_q,n_main,n_loc,H", [
+    (256, 256, 128, 1),       # whole tiles only
+    (300, 500, 77, 2),        # ragged query tile, ragged main and local tails
+    (1, 128, 0, 1),           # one query, main only
+    (129, 0, 200, 3),         # local only
+    (513, 1, 1, 2),           # two keys in total
+    (700, 1000, 300, 1),
+])
+def test_attn_bf16(n_q, n_main, n_loc, H):
+    q, km, vm, kl, vl = _case(n_q, n_main, n_loc, H, 128, torch.bfloat16, 3)
+    o, lse = _run(q.to(DEV), km, vm, kl, vl)
+    ref_o, ref_lse = _oracle(q, km, vm, kl, vl)
+    err_lse = np.abs(f64(lse) - ref_lse).max()
+    err_o = np.abs(f64(o) - ref_o)
+    # report both: a bad S = QK^T shows in LSE, a bad P V only in O
+    assert err_lse <= LSE_ABS and err_o.max() <= 1e-2 and err_o.mean() <= 1e-3, \
+        f"lse {err_lse:.3e} o max {err_o.max():.3e} mean {err_o.mean():.3e}"
+
+
+@pytest.mark.parametrize("gain", [8.0, 1.0, 0.35])
+def test_attn_bf16_peaked_queries(gain):
+    """q_i = gain * k_pi(i): each row concentrates on one key (gain 8), a few
+    keys (gain 1) or spreads (0.35); at gain 8, O must be V at that key."""
+    H, n_main, n_loc, n_q = 2, 640, 130, 300
+    _, km, vm, kl, vl = _case(1, n_main, n_loc, H, 128, torch.bfloat16, 4)
+    kall = torch.cat([km, kl])
+    q, pi = synth.peaked_queries(kall, n_q, seed=5, gain=gain)
+    o, lse = _run(q.to(DEV), km, vm, kl, vl)
+    ref_o, ref_lse = _oracle(q, km, vm, kl, vl)
+    assert_attn_close(o, ref_o, torch.bfloat16, f"peaked gain {gain}")
+    assert np.abs(f64(lse) - ref_lse).max() <= LSE_ABS
+    if gain >= 8.0:
+        vall = torch.cat([vm, vl]).double()
+        np.testing.assert_allclose(f64(o), vall[pi].numpy(), atol=1e-2)
+
+
+def test_attn_bf16_one_hot_values_reveal_key_mapping():
+    """V rows one-hot in the feature axis (key t -> column t mod 128) and
+    queries that point at one key: any mix-up of key order or feature order in
+    the P V product shows as a wrong column."""
+    H, n = 1, 384
+    k = synth.normal((n, H, 128), 6, dtype=torch.bfloat16)
+    v = torch.zeros((n, H, 128), dtype=torch.bfloat16)
+    for t in range(n):
+        v[t, 0, t % 128] = 1.0 + (t // 128)
+    q, pi = synth.peaked_queries(k, 256, seed=7, gain=8.0)
+    o, _ = _run(q.to(DEV), k, v, None, None)
+    ref_o, _ = _oracle(q, k, v, None, None)
+    assert_attn_close(o, ref_o, torch.bfloat16, "one-hot V")
+    got_col = f64(o)[:, 0, :].argmax(axis=1)
+    assert (got_col == (pi.numpy() % 128)).all()
+
+
+def test_attn_bf16_scale_and_reuse_of_output_buffer():
+    q, km, vm, kl, vl = _case(200, 300, 50, 2, 128, torch.bfloat16, 8)
+    o1, _ = _run(q.to(DEV), km, vm, kl, vl, scale=0.05)
+    ref, _ = _oracle(q, km, vm, kl, vl, scale=0.05)
+    assert_attn_close(o1, ref, torch.bfloat16, "scale 0.05")
+    o2, _ = _run(q.to(DEV), km, vm, kl, vl, scale=0.05)
+    assert torch.equal(o1, o2)            # deterministic run to run
+
+
+def test_attn_bf16_worldattention_shape_sampled():
+    """Full one-layer shape: 4,680 queries x 12 heads over 49,920 buffer keys
+    + 4,680 local keys; oracle on 48 sampled rows (incl. the ragged last query
+    tile) for every head, plus finiteness of the whole output."""
+    H, n_q, n_main, n_loc = 12, 4680, 49920, 4680
+    g = lambda n, t: synth.normal((n, H, 128), synth.seed_of("wa_attn", t), device=DEV,  # noqa: E731
+                                  dtype=torch.bfloat16)
+    q, km, vm, kl, vl = g(n_q, "q"), g(n_main, "km"), g(n_main, "vm"), g(n_loc, "kl"), g(n_loc, "vl")
+    o, lse = _run(q, km, vm, kl, vl)
+    assert torch.isfinite(o.float()).all()
+    rows = np.unique(np.concatenate([np.arange(0, n_q, 131), [4607, 4608, 4660, 4679]]))[:48]
+    ref_o, ref_lse = _oracle(q, km, vm, kl, vl, rows=rows)
+    assert_attn_close(o[torch.from_numpy(rows).to(DEV)], ref_o, torch.bfloat16, "full shape")
+    assert np.abs(f64(lse)[:, rows] - ref_lse).max() <= LSE_ABS
+
+
+def test_attn_bf16_peaked_at_full_length():
+    """Peaked rows against the full 54,600-key set: every row's mass sits on
+    one key chosen anywhere in the buffer or the local segment."""
+    H, n_q, n_main, n_loc = 2, 512, 49920, 4680
+    g = lambda n, t: synth.normal((n, H, 128), synth.seed_of("wa_peak", t), dtype=torch.bfloat16)  # noqa: E731
+    km, vm, kl, vl = g(n_main, "km"), g(n_main, "vm"), g(n_loc, "kl"), g(n_loc, "vl")
+    q, pi = synth.peaked_queries(torch.cat([km, kl]), n_q, seed=9, gain=8.0)
+    o, _ = _run(q.to(DEV), km, vm, kl, vl)
+    vall = torch.cat([vm, vl]).double()
+    np.testing.assert_allclose(f64(o), vall[pi].numpy(), atol=1e-2)
