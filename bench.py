@@ -152,7 +152,7 @@ def run_gpu(args, world, rank, local):
     idx = torch.empty(KP, dtype=torch.int32, device=dev)
     kbuf = torch.empty((KP * P, H, D), dtype=torch.bfloat16, device=dev)
     vbuf = torch.empty_like(kbuf)
-    o = torch.empty_like(q)
+    o = torch.empty(q.shape, dtype=torch.float32, device=dev)   # fp32 result (tested tolerance)
     lse = torch.empty((H, NQ), dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream()
 
@@ -268,6 +268,49 @@ def run_gpu(args, world, rank, local):
     return line
 
 
+def run_one_kernel(args, local):
+    """One kernel alone at the workload's shape (inputs drawn directly, no page
+    bank): the attention over a 49,920-token buffer + 4,680 local tokens, or
+    the gather of 4 pages from a 12-page bank.  Used for profiling captures."""
+    import torch
+
+    import sparse_kv_cache_page_gb300 as wa
+    from sparse_kv_cache_page_gb300 import synth
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    wa.load()
+    g = lambda shape, t: synth.normal(shape, synth.seed_of("one_kernel", t), device=dev,  # noqa: E731
+                                      dtype=torch.bfloat16)
+    if args.kernel == "attention":
+        q, kb, vb = g((NQ, H, D), "q"), g((KP * P, H, D), "kb"), g((KP * P, H, D), "vb")
+        kl, vl = g((NLOC, H, D), "kl"), g((NLOC, H, D), "vl")
+        o = torch.empty(q.shape, dtype=torch.float32, device=dev)
+        lse = torch.empty((H, NQ), dtype=torch.float32, device=dev)
+        fn = lambda: wa.wa_block_attn(q, kb, vb, kl, vl, o, lse)  # noqa: E731
+        work, unit = attn_flops(NQ, KP * P + NLOC, D, H) / 1e12, "TFLOP/s"
+    else:
+        kp, vp = g((12, P, H, D), "kp"), g((12, P, H, D), "vp")
+        idx = torch.tensor([9, 2, 5, 11], dtype=torch.int32, device=dev)
+        kb, vb = torch.empty((KP * P, H, D), dtype=torch.bfloat16, device=dev), None
+        vb = torch.empty_like(kb)
+        fn = lambda: wa.wa_gather_pages(kp, vp, idx, None, kb, vb)  # noqa: E731
+        work, unit = 2 * 2 * KP * P * H * D * 2 / 1e9, "GB/s"
+    for _ in range(args.warmup):
+        fn()
+    wa.wa_check()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(args.steps):
+        fn()
+    e1.record()
+    torch.cuda.synchronize()
+    wa.wa_check()
+    ms = e0.elapsed_time(e1) / args.steps
+    return {"kernel": args.kernel, "ms": round(ms, 4), "value": round(work / (ms * 1e-3), 1),
+            "unit": unit, "steps": args.steps, "warmup": args.warmup}
+
+
 # ----------------------------------------------------------------------------
 # CPU oracle arm
 # ----------------------------------------------------------------------------
@@ -357,11 +400,15 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--kernel", default="all", choices=["all", "attention", "gather"],
+                    help="time one kernel alone on its own inputs (for profiling)")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)
     world, rank, local = dist_init(args)
     if args.impl == "reference":
         line = run_reference(args, world, rank)
+    elif args.kernel != "all":
+        line = run_one_kernel(args, local)
     else:
         line = run_gpu(args, world, rank, local)
     if rank == 0 and line is not None:

@@ -148,8 +148,11 @@ wa_status wa_gather_pages(const void* k_pages, const void* v_pages, wa_dtype dt,
  *   lse[h][i] = ln sum_k exp(scale * q[i][h] . K[k][h])
  *   with K = [k_main ; k_loc] and V = [v_main ; v_loc] along tokens.
  *
- * q, o     : device [n_q][n_heads][head_dim] of `dt`; o is written (bf16 by
- *            round-to-nearest-even of the fp32 result, or f32).
+ * q        : device [n_q][n_heads][head_dim] of `dt`.
+ * o        : device [n_q][n_heads][head_dim] of `o_dt`, written: WA_F32 keeps
+ *            the fp32 result; WA_BF16 rounds it to nearest even (adds up to
+ *            half a bf16 ulp, 2^-8 relative).  With dt == WA_F32, o_dt must be
+ *            WA_F32.
  * k_main, v_main : device [n_main][n_heads][head_dim]; k_loc, v_loc :
  *            [n_loc][n_heads][head_dim].  Either segment may be empty
  *            (size 0, pointers may be NULL) but not both.
@@ -161,8 +164,8 @@ wa_status wa_gather_pages(const void* k_pages, const void* v_pages, wa_dtype dt,
  */
 wa_status wa_block_attn(const void* q, int n_q, const void* k_main, const void* v_main, int n_main,
                         const void* k_loc, const void* v_loc, int n_loc, wa_dtype dt,
-                        int n_heads, int head_dim, float scale, void* o, float* lse,
-                        wa_stream_t stream);
+                        int n_heads, int head_dim, float scale, void* o, wa_dtype o_dt,
+                        float* lse, wa_stream_t stream);
 
 /*
  * Linformer-style low-rank branch and gate fusion ([WA] HSA, linear branch;
@@ -177,6 +180,7 @@ wa_status wa_block_attn(const void* q, int n_q, const void* k_main, const void* 
  * e_k, e_v : device [n_heads][n_main+n_loc][rank] of `dt` (rows aligned to
  *            [main ; local]).  K', V' are accumulated in fp32 and rounded to
  *            `dt` before the second contraction.
+ * o        : device [n_q][n_heads][head_dim] of `o_dt` (WA_BF16 or WA_F32).
  * w_attn, w_lin : device float32 [n_heads] or NULL (= all ones).
  * WA_BF16 only; needs head_dim == 128 and rank a multiple of 128, <= 512.
  */
@@ -185,7 +189,7 @@ wa_status wa_linear_branch(const void* q, int n_q, const void* k_main, const voi
                            const void* e_k, const void* e_v, int rank, wa_dtype dt,
                            int n_heads, int head_dim, float scale,
                            const float* w_attn, const float* w_lin, int accumulate,
-                           void* o, wa_stream_t stream);
+                           void* o, wa_dtype o_dt, wa_stream_t stream);
 
 /*
  * Synchronize `stream`, then read and clear this device's status word.

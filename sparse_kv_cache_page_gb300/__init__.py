@@ -66,8 +66,8 @@ def load():
         "wa_page_summarize": (I, [P, I, I, I, I, I, P, P]),
         "wa_select_pages": (I, [P, I, I, I, I, P, I, P, P, I, I, I, I, P, P, P, P]),
         "wa_gather_pages": (I, [P, P, I, I, I, I, I, P, P, I, P, P, P]),
-        "wa_block_attn": (I, [P, I, P, P, I, P, P, I, I, I, I, F, P, P, P]),
-        "wa_linear_branch": (I, [P, I, P, P, I, P, P, I, P, P, I, I, I, I, F, P, P, I, P, P]),
+        "wa_block_attn": (I, [P, I, P, P, I, P, P, I, I, I, I, F, P, I, P, P]),
+        "wa_linear_branch": (I, [P, I, P, P, I, P, P, I, P, P, I, I, I, I, F, P, P, I, P, I, P]),
         "wa_check": (I, [P]),
         "wa_shutdown": (I, []),
     }
@@ -162,13 +162,14 @@ def _rows(t):
 
 def wa_block_attn(q: torch.Tensor, k_main, v_main, k_loc, v_loc, o: torch.Tensor, lse=None,
                   scale: float = 0.0, stream=None):
-    """o = softmax(q [k_main; k_loc]^T * scale) [v_main; v_loc]; lse [H][n_q] optional."""
-    _need(q.dim() == 3 and q.is_contiguous() and o.shape == q.shape and o.dtype == q.dtype,
-          "q and o must be contiguous [n_q][H][d] of one dtype")
+    """o = softmax(q [k_main; k_loc]^T * scale) [v_main; v_loc]; lse [H][n_q] optional.
+    o may be float32 (the fp32 result) or the input dtype."""
+    _need(q.dim() == 3 and q.is_contiguous() and o.shape == q.shape and o.is_contiguous(),
+          "q and o must be contiguous [n_q][H][d]")
     n_q, h, d = q.shape
     _ok("wa_block_attn", load().wa_block_attn(
         _ptr(q), n_q, _ptr(k_main), _ptr(v_main), _rows(k_main), _ptr(k_loc), _ptr(v_loc),
-        _rows(k_loc), _dt(q), h, d, float(scale), _ptr(o), _ptr(lse), _stream(stream)))
+        _rows(k_loc), _dt(q), h, d, float(scale), _ptr(o), _dt(o), _ptr(lse), _stream(stream)))
 
 
 def wa_linear_branch(q: torch.Tensor, k_main, v_main, k_loc, v_loc, e_k: torch.Tensor,
@@ -180,7 +181,7 @@ def wa_linear_branch(q: torch.Tensor, k_main, v_main, k_loc, v_loc, e_k: torch.T
     _ok("wa_linear_branch", load().wa_linear_branch(
         _ptr(q), n_q, _ptr(k_main), _ptr(v_main), _rows(k_main), _ptr(k_loc), _ptr(v_loc),
         _rows(k_loc), _ptr(e_k), _ptr(e_v), rank, _dt(q), h, d, float(scale), _ptr(w_attn),
-        _ptr(w_lin), int(bool(accumulate)), _ptr(o), _stream(stream)))
+        _ptr(w_lin), int(bool(accumulate)), _ptr(o), _dt(o), _stream(stream)))
 
 
 def wa_check(stream=None):

@@ -77,7 +77,7 @@ static_assert(sizeof(Bars) <= 256, "barrier block too large");
 struct Params {
   int n_q, n_heads, n_main, n_loc, nt_main, nt_loc;
   float scale, scale_log2;
-  __nv_bfloat16* o;
+  void* o;
   float* lse;
   int accumulate;
   const float* w_old;
@@ -90,6 +90,46 @@ __device__ __forceinline__ int tile_valid(const Params& p, int j) {
   return min(BN, p.n_loc - (j - p.nt_main) * BN);
 }
 
+// Output row store: 128 values of one (query, head), optionally fused with the
+// values already there (o = w_old * o + w_new * x).
+__device__ __forceinline__ void store_row32(__nv_bfloat16* dst, const float (&x)[32], bool acc,
+                                            float wo) {
+  uint4* d = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+  for (int v = 0; v < 4; ++v) {
+    float y[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) y[e] = x[8 * v + e];
+    if (acc) {
+      const uint4 old = d[v];
+      const uint32_t ow[4] = {old.x, old.y, old.z, old.w};
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        y[2 * e] += wo * __uint_as_float(ow[e] << 16);
+        y[2 * e + 1] += wo * __uint_as_float(ow[e] & 0xffff0000u);
+      }
+    }
+    d[v] = make_uint4(pack_bf16x2(y[0], y[1]), pack_bf16x2(y[2], y[3]), pack_bf16x2(y[4], y[5]),
+                      pack_bf16x2(y[6], y[7]));
+  }
+}
+__device__ __forceinline__ void store_row32(float* dst, const float (&x)[32], bool acc, float wo) {
+  float4* d = reinterpret_cast<float4*>(dst);
+#pragma unroll
+  for (int v = 0; v < 8; ++v) {
+    float4 y = make_float4(x[4 * v], x[4 * v + 1], x[4 * v + 2], x[4 * v + 3]);
+    if (acc) {
+      const float4 old = d[v];
+      y.x += wo * old.x;
+      y.y += wo * old.y;
+      y.z += wo * old.z;
+      y.w += wo * old.w;
+    }
+    d[v] = y;
+  }
+}
+
+template <typename OutT>
 __global__ void __launch_bounds__(kThreads, 1)
 k_block_attn_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_km,
                 const __grid_constant__ CUtensorMap tm_vm, const __grid_constant__ CUtensorMap tm_kl,
@@ -166,6 +206,7 @@ k_block_attn_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         mbar_wait_drain(&bars->q_full, 0, 100000000ull);
       }
     }
+    __syncwarp();   // lanes 1-31 wait here for lane 0: the warp reaches the CTA barrier converged
   } else if (warp == kMmaWarp) {
     if (lane == 0) {
       const uint32_t q_base = smem_u32(smem + SmemLayout::q);
@@ -217,6 +258,7 @@ k_block_attn_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
       mma_commit(&bars->drain);
       mbar_wait_drain(&bars->drain, 0, 1000000000ull);
     }
+    __syncwarp();
   } else {
     // softmax warpgroups
     const int qt = warp >> 2;                       // query tile 0 or 1
@@ -227,30 +269,43 @@ k_block_attn_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     const float sl2 = p.scale_log2;
     float m = -INFINITY, l = 0.f;
     bool ok = true;
+    // Every tcgen05.ld/st below is .sync.aligned: all 32 lanes of the warp must
+    // execute it together, so branch conditions around them are warp-uniform.
     for (int j = 0; j < nkv; ++j) {
-      if (!(ok = mbar_wait(&bars->s_full[qt], j & 1, abort_flag, p.status))) break;
+      ok = __all_sync(0xffffffffu, mbar_wait(&bars->s_full[qt], j & 1, abort_flag, p.status));
+      if (!ok) break;
       tc_fence_after();
       uint32_t sr[4][32];
 #pragma unroll
       for (int c = 0; c < 4; ++c) tmem_ld32(s_addr + 32 * c, sr[c]);
       tmem_ld_wait();
-      const int valid = tile_valid(p, j);
-      float tmax = -INFINITY;
+      const int valid = tile_valid(p, j);   // warp-uniform
+      if (valid < BN) {
 #pragma unroll
-      for (int c = 0; c < 4; ++c)
+        for (int c = 0; c < 4; ++c)
 #pragma unroll
-        for (int e = 0; e < 32; ++e) {
-          float v = __uint_as_float(sr[c][e]);
-          if (32 * c + e >= valid) v = -INFINITY;
-          sr[c][e] = __float_as_uint(v);
-          tmax = fmaxf(tmax, v);
+          for (int e = 0; e < 32; ++e)
+            if (32 * c + e >= valid) sr[c][e] = __float_as_uint(-INFINITY);
+      }
+      float mx[4];
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        mx[c] = __uint_as_float(sr[c][0]);
+#pragma unroll
+        for (int e = 1; e < 31; e += 2)
+          mx[c] = fmax3(mx[c], __uint_as_float(sr[c][e]), __uint_as_float(sr[c][e + 1]));
+        mx[c] = fmaxf(mx[c], __uint_as_float(sr[c][31]));
+      }
+      const float tmax = fmax3(fmaxf(mx[0], mx[1]), mx[2], mx[3]);
+      // rows whose max rose by more than 2^8 (exp2 units) rescale O and l
+      const bool need = j > 0 && (tmax - m) * sl2 > 8.0f;
+      if (j == 0) m = tmax;
+      if (__any_sync(0xffffffffu, need)) {
+        const float f = need ? ex2((m - tmax) * sl2) : 1.0f;
+        if (need) {
+          m = tmax;
+          l *= f;
         }
-      if (j == 0) {
-        m = tmax;
-      } else if ((tmax - m) * sl2 > 8.0f) {
-        const float f = ex2((m - tmax) * sl2);
-        m = tmax;
-        l *= f;
 #pragma unroll 1
         for (int c = 0; c < 4; ++c) {
           uint32_t orow[32];
@@ -261,8 +316,10 @@ k_block_attn_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
           tmem_st32(o_addr + 32 * c, orow);
         }
       }
-      const float msl2 = m * sl2;
-      float rs = 0.f;
+      // p = 2^(s*sl2 - m*sl2) rounded to bf16 for the P V product; the row sum
+      // adds the same rounded values, so numerator and denominator agree.
+      const float nmsl2 = -m * sl2;
+      float rs0 = 0.f, rs1 = 0.f;
 #pragma unroll
       for (int hf = 0; hf < 2; ++hf) {
         uint32_t pk[32];   // bf16 pairs for keys 64*hf .. 64*hf+63
@@ -271,51 +328,44 @@ k_block_attn_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
 #pragma unroll
           for (int e = 0; e < 32; e += 2) {
             const int c = 2 * hf + c2;
-            const float p0 = ex2(fmaf(__uint_as_float(sr[c][e]), sl2, -msl2));
-            const float p1 = ex2(fmaf(__uint_as_float(sr[c][e + 1]), sl2, -msl2));
-            rs += p0 + p1;
-            pk[16 * c2 + (e >> 1)] = pack_bf16x2(p0, p1);
+            float x0, x1;
+            ffma2(x0, x1, __uint_as_float(sr[c][e]), __uint_as_float(sr[c][e + 1]), sl2, sl2,
+                  nmsl2, nmsl2);
+            const uint32_t w = pack_bf16x2(ex2(x0), ex2(x1));
+            pk[16 * c2 + (e >> 1)] = w;
+            fadd2_acc(rs0, rs1, __uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
           }
         tmem_st32(s_addr + 32 * hf, pk);
       }
-      l += rs;
+      l += rs0 + rs1;
       tmem_st_wait();
       tc_fence_before();
       mbar_arrive(&bars->p_ready[qt]);
     }
-    if (ok) ok = mbar_wait(&bars->o_ready[qt], (nkv - 1) & 1, abort_flag, p.status);
+    if (ok)
+      ok = __all_sync(0xffffffffu,
+                      mbar_wait(&bars->o_ready[qt], (nkv - 1) & 1, abort_flag, p.status));
     tc_fence_after();
     const int grow = q0 + qt * BM + row;
-    if (ok && grow < p.n_q) {
+    const bool store = grow < p.n_q;
+    if (ok) {
       const float inv_l = 1.0f / l;
-      __nv_bfloat16* orow_g = p.o + ((size_t)grow * p.n_heads + head) * HD;
+      OutT* orow_g = static_cast<OutT*>(p.o) + ((size_t)(store ? grow : 0) * p.n_heads + head) * HD;
       const float wo = p.accumulate ? (p.w_old ? p.w_old[head] : 1.0f) : 0.0f;
-      const float wn = p.accumulate ? (p.w_new ? p.w_new[head] : 1.0f) : 1.0f;
+      const float wn = (p.accumulate ? (p.w_new ? p.w_new[head] : 1.0f) : 1.0f) * inv_l;
 #pragma unroll 1
       for (int c = 0; c < 4; ++c) {
         uint32_t orow[32];
-        tmem_ld32(o_addr + 32 * c, orow);
+        tmem_ld32(o_addr + 32 * c, orow);   // whole warp
         tmem_ld_wait();
-        uint4* dst = reinterpret_cast<uint4*>(orow_g + 32 * c);
+        if (store) {
+          float x[32];
 #pragma unroll
-        for (int v = 0; v < 4; ++v) {
-          float x[8];
-#pragma unroll
-          for (int e = 0; e < 8; ++e) x[e] = __uint_as_float(orow[8 * v + e]) * inv_l * wn;
-          if (p.accumulate) {
-            const uint4 old = dst[v];
-            const uint32_t ow[4] = {old.x, old.y, old.z, old.w};
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              x[2 * e] += wo * __uint_as_float(ow[e] << 16);
-              x[2 * e + 1] += wo * __uint_as_float(ow[e] & 0xffff0000u);
-            }
-          }
-          dst[v] = make_uint4(pack_bf16x2(x[0], x[1]), pack_bf16x2(x[2], x[3]),
-                              pack_bf16x2(x[4], x[5]), pack_bf16x2(x[6], x[7]));
+          for (int e = 0; e < 32; ++e) x[e] = __uint_as_float(orow[e]) * wn;
+          store_row32(orow_g + 32 * c, x, p.accumulate != 0, wo);
         }
       }
-      if (p.lse) p.lse[(size_t)head * p.n_q + grow] = m * p.scale + logf(l);
+      if (store && p.lse) p.lse[(size_t)head * p.n_q + grow] = m * p.scale + logf(l);
     }
   }
 
@@ -332,8 +382,8 @@ k_block_attn_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
 
 wa_status launch_attn_tc(const void* q, int n_q, const void* k_main, const void* v_main,
                          int n_main, const void* k_loc, const void* v_loc, int n_loc, int n_heads,
-                         float scale, void* o, float* lse, int accumulate, const float* w_old,
-                         const float* w_new, cudaStream_t s) {
+                         float scale, void* o, int o_f32, float* lse, int accumulate,
+                         const float* w_old, const float* w_new, cudaStream_t s) {
   Ctrl* ctrl = nullptr;
   wa_status rc = get_ctrl(&ctrl);
   if (rc != WA_OK) return rc;
@@ -361,24 +411,24 @@ wa_status launch_attn_tc(const void* q, int n_q, const void* k_main, const void*
   p.nt_loc = (n_loc + BN - 1) / BN;
   p.scale = scale;
   p.scale_log2 = scale * 1.4426950408889634f;
-  p.o = static_cast<__nv_bfloat16*>(o);
+  p.o = o;
   p.lse = lse;
   p.accumulate = accumulate;
   p.w_old = w_old;
   p.w_new = w_new;
   p.status = &ctrl->status;
   const int smem = SmemLayout::total + 1024;
-  static bool attr_done[64] = {};
+  static bool attr_done[64][2] = {};
   int dev = 0;
   cudaGetDevice(&dev);
-  if (dev < 64 && !attr_done[dev]) {
-    if (cudaFuncSetAttribute(k_block_attn_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
-        cudaSuccess)
+  auto kern = o_f32 ? k_block_attn_tc<float> : k_block_attn_tc<__nv_bfloat16>;
+  if (dev < 64 && !attr_done[dev][o_f32 ? 1 : 0]) {
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
       return WA_ERR_CUDA;
-    attr_done[dev] = true;
+    attr_done[dev][o_f32 ? 1 : 0] = true;
   }
   dim3 grid((n_q + 2 * BM - 1) / (2 * BM), n_heads);
-  k_block_attn_tc<<<grid, kThreads, smem, s>>>(tq, tkm, tvm, tkl, tvl, p);
+  kern<<<grid, kThreads, smem, s>>>(tq, tkm, tvm, tkl, tvl, p);
   return cuda_status(cudaPeekAtLastError());
 }
 

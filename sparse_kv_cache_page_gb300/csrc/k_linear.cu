@@ -6,7 +6,7 @@ namespace wa {
 
 wa_status launch_linear_branch(const void*, int, const void*, const void*, int, const void*,
                                const void*, int, const void*, const void*, int, int, float,
-                               const float*, const float*, int, void*, cudaStream_t) {
+                               const float*, const float*, int, void*, int, cudaStream_t) {
   return WA_ERR_UNIMPLEMENTED;
 }
 

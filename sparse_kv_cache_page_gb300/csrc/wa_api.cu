@@ -200,9 +200,10 @@ wa_status wa_gather_pages(const void* k_pages, const void* v_pages, wa_dtype dt,
 
 wa_status wa_block_attn(const void* q, int n_q, const void* k_main, const void* v_main, int n_main,
                         const void* k_loc, const void* v_loc, int n_loc, wa_dtype dt,
-                        int n_heads, int head_dim, float scale, void* o, float* lse,
-                        wa_stream_t stream) {
-  if (!dtype_ok(dt)) return WA_ERR_DTYPE;
+                        int n_heads, int head_dim, float scale, void* o, wa_dtype o_dt,
+                        float* lse, wa_stream_t stream) {
+  if (!dtype_ok(dt) || !dtype_ok(o_dt)) return WA_ERR_DTYPE;
+  if (dt == WA_F32 && o_dt != WA_F32) return WA_ERR_DTYPE;
   if (!q || !o || n_q <= 0 || n_main < 0 || n_loc < 0 || n_main + n_loc <= 0)
     return WA_ERR_INVALID_ARG;
   if (n_main > 0 && (!k_main || !v_main)) return WA_ERR_INVALID_ARG;
@@ -222,15 +223,15 @@ wa_status wa_block_attn(const void* q, int n_q, const void* k_main, const void* 
   if (head_dim != 128) return WA_ERR_SHAPE;
   if ((long long)n_heads * 128 > 16384) return WA_ERR_SHAPE;
   return launch_attn_tc(q, n_q, k_main, v_main, n_main, k_loc, v_loc, n_loc, n_heads, scale, o,
-                        lse, 0, nullptr, nullptr, s);
+                        o_dt == WA_F32, lse, 0, nullptr, nullptr, s);
 }
 
 wa_status wa_linear_branch(const void* q, int n_q, const void* k_main, const void* v_main,
                            int n_main, const void* k_loc, const void* v_loc, int n_loc,
                            const void* e_k, const void* e_v, int rank, wa_dtype dt, int n_heads,
                            int head_dim, float scale, const float* w_attn, const float* w_lin,
-                           int accumulate, void* o, wa_stream_t stream) {
-  if (!dtype_ok(dt)) return WA_ERR_DTYPE;
+                           int accumulate, void* o, wa_dtype o_dt, wa_stream_t stream) {
+  if (!dtype_ok(dt) || !dtype_ok(o_dt)) return WA_ERR_DTYPE;
   if (dt != WA_BF16) return WA_ERR_DTYPE;
   if (!q || !o || !e_k || !e_v || n_q <= 0 || n_main < 0 || n_loc < 0 || n_main + n_loc <= 0)
     return WA_ERR_INVALID_ARG;
@@ -244,7 +245,7 @@ wa_status wa_linear_branch(const void* q, int n_q, const void* k_main, const voi
     return WA_ERR_ALIGN;
   if (!(scale > 0.0f)) scale = 1.0f / sqrtf((float)head_dim);
   return launch_linear_branch(q, n_q, k_main, v_main, n_main, k_loc, v_loc, n_loc, e_k, e_v, rank,
-                              n_heads, scale, w_attn, w_lin, accumulate, o,
+                              n_heads, scale, w_attn, w_lin, accumulate, o, o_dt == WA_F32,
                               (cudaStream_t)stream);
 }
 

@@ -70,13 +70,13 @@ wa_status launch_attn_f32(const float* q, int n_q, const float* k_main, const fl
 // for the epilogue o = w_old[h]*o + w_new[h]*O (accumulate != 0), may be NULL.
 wa_status launch_attn_tc(const void* q, int n_q, const void* k_main, const void* v_main,
                          int n_main, const void* k_loc, const void* v_loc, int n_loc,
-                         int n_heads, float scale, void* o, float* lse, int accumulate,
+                         int n_heads, float scale, void* o, int o_f32, float* lse, int accumulate,
                          const float* w_old, const float* w_new, cudaStream_t s);
 
 wa_status launch_linear_branch(const void* q, int n_q, const void* k_main, const void* v_main,
                                int n_main, const void* k_loc, const void* v_loc, int n_loc,
                                const void* e_k, const void* e_v, int rank, int n_heads,
                                float scale, const float* w_attn, const float* w_lin,
-                               int accumulate, void* o, cudaStream_t s);
+                               int accumulate, void* o, int o_f32, cudaStream_t s);
 
 }  // namespace wa

@@ -64,15 +64,18 @@ def test_host_validation_without_gpu(lib):
                                None, None) == 1
     # attention: both segments empty; bf16 head_dim != 128 -> SHAPE
     assert lib.wa_block_attn(fake, 4, None, None, 0, None, None, 0, 1, 1, 128, ctypes.c_float(0),
-                             fake, None, None) == 1
+                             fake, 1, None, None) == 1
     assert lib.wa_block_attn(fake, 4, fake, fake, 8, None, None, 0, 1, 1, 64, ctypes.c_float(0),
-                             fake, None, None) == 2
+                             fake, 1, None, None) == 2
     assert lib.wa_block_attn(fake, 4, fake, fake, 8, None, None, 0, 0, 1, 260, ctypes.c_float(0),
-                             fake, None, None) == 2
+                             fake, 0, None, None) == 2
+    # fp32 inputs with a bf16 output -> WA_ERR_DTYPE
+    assert lib.wa_block_attn(fake, 4, fake, fake, 8, None, None, 0, 0, 1, 64, ctypes.c_float(0),
+                             fake, 1, None, None) == 3
     # gather: v pointer without v buffer
     assert lib.wa_gather_pages(fake, fake, 1, 4, 8, 1, 128, fake, None, 2, fake, None, None) == 1
     # linear branch: fp32 not supported, bad rank
     assert lib.wa_linear_branch(fake, 4, fake, fake, 8, None, None, 0, fake, fake, 256, 0, 1, 128,
-                                ctypes.c_float(0), None, None, 1, fake, None) == 3
+                                ctypes.c_float(0), None, None, 1, fake, 0, None) == 3
     assert lib.wa_linear_branch(fake, 4, fake, fake, 8, None, None, 0, fake, fake, 100, 1, 1, 128,
-                                ctypes.c_float(0), None, None, 1, fake, None) == 2
+                                ctypes.c_float(0), None, None, 1, fake, 1, None) == 2

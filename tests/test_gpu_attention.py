@@ -19,8 +19,11 @@ pytestmark = pytest.mark.gpu
 DEV = "cuda"
 
 
-def _run(q, km, vm, kl, vl, scale=0.0):
-    o = torch.empty_like(q)
+def _run(q, km, vm, kl, vl, scale=0.0, out_dtype=torch.float32):
+    """Attention through the C ABI; fp32 output unless asked otherwise (the
+    stated 1e-2 tolerance is for the fp32 result; a bf16 output adds up to
+    half a bf16 ulp of rounding)."""
+    o = torch.empty(q.shape, dtype=out_dtype, device=DEV)
     lse = torch.empty((q.shape[1], q.shape[0]), dtype=torch.float32, device=DEV)
     d = lambda t: None if t is None else t.to(DEV)  # noqa: E731
     wa.wa_block_attn(q.to(DEV), d(km), d(vm), d(kl), d(vl), o, lse, scale)
@@ -113,6 +116,20 @@ def test_attn_bf16_one_hot_values_reveal_key_mapping():
     assert_attn_close(o, ref_o, torch.bfloat16, "one-hot V")
     got_col = f64(o)[:, 0, :].argmax(axis=1)
     assert (got_col == (pi.numpy() % 128)).all()
+
+
+@pytest.mark.parametrize("n_q,n_main,n_loc", [(300, 500, 77), (64, 1, 1)])
+def test_attn_bf16_output_rounding(n_q, n_main, n_loc):
+    """bf16 output: within 1e-2 of the oracle plus half a bf16 ulp of the
+    rounding the output format itself adds (2^-8 relative)."""
+    q, km, vm, kl, vl = _case(n_q, n_main, n_loc, 2, 128, torch.bfloat16, 10)
+    o, _ = _run(q.to(DEV), km, vm, kl, vl, out_dtype=torch.bfloat16)
+    ref, _ = _oracle(q, km, vm, kl, vl)
+    err = np.abs(f64(o) - ref)
+    bound = 1e-2 + np.abs(ref) * 2.0 ** -8
+    assert (err <= bound).all() and err.mean() <= 1e-3, (err.max(), err.mean())
+    o32, _ = _run(q.to(DEV), km, vm, kl, vl)
+    assert torch.equal(o, o32.to(torch.bfloat16))   # bf16 output = rounded fp32 output
 
 
 def test_attn_bf16_scale_and_reuse_of_output_buffer():
