@@ -153,7 +153,6 @@ def run_gpu(args, world, rank, local):
     kbuf = torch.empty((KP * P, H, D), dtype=torch.bfloat16, device=dev)
     vbuf = torch.empty_like(kbuf)
     o = torch.empty(q.shape, dtype=torch.float32, device=dev)   # fp32 result (tested tolerance)
-    lse = torch.empty((H, NQ), dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream()
 
     names = ("summarize", "select", "gather", "attention")
@@ -169,7 +168,7 @@ def run_gpu(args, world, rank, local):
         mark(2)
         wa.wa_gather_pages(kp, vp, idx, None, kbuf, vbuf)
         mark(3)
-        wa.wa_block_attn(q, kbuf, vbuf, kl, vl, o, lse)
+        wa.wa_block_attn(q, kbuf, vbuf, kl, vl, o)
         mark(4)
 
     for _ in range(args.warmup):
@@ -209,7 +208,7 @@ def run_gpu(args, world, rank, local):
         wa.wa_page_summarize(kp, kbar)
         wa.wa_select_pages(dq, kbar, dpc, pch, PPC, KP, idx)
         wa.wa_gather_pages(kp, vp, idx, None, kbuf, vbuf)
-        wa.wa_block_attn(dq, kbuf, vbuf, dkl, dvl, o, lse)
+        wa.wa_block_attn(dq, kbuf, vbuf, dkl, dvl, o)
         ho.copy_(o, non_blocking=True)
 
     for _ in range(max(1, args.warmup)):
@@ -286,8 +285,7 @@ def run_one_kernel(args, local):
         q, kb, vb = g((NQ, H, D), "q"), g((KP * P, H, D), "kb"), g((KP * P, H, D), "vb")
         kl, vl = g((NLOC, H, D), "kl"), g((NLOC, H, D), "vl")
         o = torch.empty(q.shape, dtype=torch.float32, device=dev)
-        lse = torch.empty((H, NQ), dtype=torch.float32, device=dev)
-        fn = lambda: wa.wa_block_attn(q, kb, vb, kl, vl, o, lse)  # noqa: E731
+        fn = lambda: wa.wa_block_attn(q, kb, vb, kl, vl, o)  # noqa: E731
         work, unit = attn_flops(NQ, KP * P + NLOC, D, H) / 1e12, "TFLOP/s"
     else:
         kp, vp = g((12, P, H, D), "kp"), g((12, P, H, D), "vp")

@@ -8,7 +8,8 @@
 // 4 x 8 x 1,560 = 49,920 retrieved tokens held in HBM (tier L1), staged
 // through on-chip SRAM (tier L0) FlashAttention-style.
 //
-// Design (one CTA = one head x two 128-row query tiles, 10 warps):
+// Design (one CTA = one head x two 128-row query tiles x one range of key
+// tiles; 12 warps in three warpgroups):
 //   warp 8      TMA producer: Q0/Q1 once, then K_j, V_j alternately into a
 //               4-stage ring of 32 KiB slots (two 64-column boxes each,
 //               128-byte swizzle, rows past a segment end read as zero).
@@ -18,15 +19,22 @@
 //               from TMEM (bf16, aliasing S_i) and V_j MN-major from shared
 //               memory.  S_i(j+1) is issued only after O_i += P_i(j) V_j has
 //               completed, because P_i lives in S_i's columns.
+//   warps 10-11 idle (the CTA is three whole warpgroups).
 //   warps 0-3   softmax of query tile 0 (one thread per row = TMEM lane);
 //   warps 4-7   softmax of query tile 1.  Each row keeps a running max m and
-//               sum l; exponentials are taken against m, and O_i and l are
+//               a sum l of the bf16-rounded p (the values the P V product
+//               uses); exponentials are taken against m, and O_i and l are
 //               rescaled only when a tile raises the max by more than 2^8
 //               (in exp2 units), so most tiles skip the O round trip.
 //   TMEM columns: S0 [0,128) S1 [128,256) O0 [256,384) O1 [384,512).
-//   Epilogue: O / l rounded to bf16 (optionally fused with an existing
-//   output: o = w_old[h] * o + w_new[h] * O) and LSE = scale*m + ln l.
+//   Key tiles are split into n_split contiguous ranges so that the grid fills
+//   whole waves of the 152 SMs; each CTA of a split stores its unnormalised
+//   O, m and l to scratch, and the CTA that finishes last for its (head,
+//   query pair) combines them (no spin-wait: a ticket counter).
+//   Epilogue: O / l (fp32 or rounded to bf16; optionally fused with an
+//   existing output: o = w_old[h] * o + w_new[h] * O) and LSE = scale*m + ln l.
 #include <math.h>
+#include <stdlib.h>
 #include <string.h>
 
 #include "tc_ptx.cuh"
@@ -43,9 +51,10 @@ constexpr int HD = 128;                  // head dim
 constexpr int NS = 4;                    // ring slots
 constexpr int kHalfBytes = BN * 64 * 2;  // one 64-column box: 16 KiB
 constexpr int kTileBytes = 2 * kHalfBytes;
-constexpr int kThreads = 320;
+constexpr int kThreads = 384;
 constexpr int kProducerWarp = 8;
 constexpr int kMmaWarp = 9;
+constexpr int kMaxUnits = 8192;          // split attention: one ticket per (head, query pair)
 
 __device__ __forceinline__ uint32_t col_s(int i) { return 128u * i; }          // S_i / P_i
 __device__ __forceinline__ uint32_t col_o(int i) { return 256u + 128u * i; }   // O_i
@@ -71,11 +80,13 @@ struct Bars {
   uint64_t drain;
   uint32_t tmem_base;
   int abort_flag;
+  unsigned ticket;
 };
 static_assert(sizeof(Bars) <= 256, "barrier block too large");
 
 struct Params {
   int n_q, n_heads, n_main, n_loc, nt_main, nt_loc;
+  int n_split, n_qpairs;
   float scale, scale_log2;
   void* o;
   float* lse;
@@ -83,6 +94,9 @@ struct Params {
   const float* w_old;
   const float* w_new;
   int* status;
+  float* part_o;             // [unit][split][256][128] unnormalised O (split > 1)
+  float4* part_ml;           // [unit][split][256] (m, l, l_exact, -)
+  unsigned* counters;        // [unit] tickets, zero between launches
 };
 
 __device__ __forceinline__ int tile_valid(const Params& p, int j) {
@@ -90,8 +104,14 @@ __device__ __forceinline__ int tile_valid(const Params& p, int j) {
   return min(BN, p.n_loc - (j - p.nt_main) * BN);
 }
 
-// Output row store: 128 values of one (query, head), optionally fused with the
-// values already there (o = w_old * o + w_new * x).
+// Key tiles [j0, j1) of split `sp`: contiguous, sizes differ by at most one.
+__device__ __forceinline__ void split_range(int nkv, int n_split, int sp, int& j0, int& j1) {
+  j0 = (int)(((long long)nkv * sp) / n_split);
+  j1 = (int)(((long long)nkv * (sp + 1)) / n_split);
+}
+
+// Output row store: 32 values of one (query, head), optionally fused with the
+// values already there (o = w_old * o + x).
 __device__ __forceinline__ void store_row32(__nv_bfloat16* dst, const float (&x)[32], bool acc,
                                             float wo) {
   uint4* d = reinterpret_cast<uint4*>(dst);
@@ -129,7 +149,11 @@ __device__ __forceinline__ void store_row32(float* dst, const float (&x)[32], bo
   }
 }
 
-template <typename OutT>
+__device__ __forceinline__ void softmax_bar() {   // the 256 softmax threads only
+  asm volatile("bar.sync 1, 256;" ::: "memory");
+}
+
+template <typename OutT, bool kLse>
 __global__ void __launch_bounds__(kThreads, 1)
 k_block_attn_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_km,
                 const __grid_constant__ CUtensorMap tm_vm, const __grid_constant__ CUtensorMap tm_kl,
@@ -140,8 +164,12 @@ k_block_attn_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
   Bars* bars = reinterpret_cast<Bars*>(smem + SmemLayout::bars);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int head = blockIdx.y;
-  const int q0 = blockIdx.x * (2 * BM);
-  const int nkv = p.nt_main + p.nt_loc;
+  const int qpair = blockIdx.x / p.n_split;
+  const int split = blockIdx.x % p.n_split;
+  const int q0 = qpair * (2 * BM);
+  int jb, je;
+  split_range(p.nt_main + p.nt_loc, p.n_split, split, jb, je);
+  const int nloc = je - jb;                 // key tiles of this CTA (>= 1)
   volatile int* abort_flag = &bars->abort_flag;
 
   if (threadIdx.x == 0) {
@@ -168,118 +196,123 @@ k_block_attn_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
   tc_fence_after();
   const uint32_t tmem = bars->tmem_base;
 
-  if (warp == kProducerWarp) {
-    if (lane == 0) {
-      prefetch_tmap(&tm_q);
-      const int xq = head * HD;
-      mbar_arrive_expect_tx(&bars->q_full, 2 * kTileBytes);
-      for (int i = 0; i < 2; ++i)
-        for (int hf = 0; hf < 2; ++hf)
-          tma_load_2d(&tm_q, &bars->q_full, smem + SmemLayout::q + i * kTileBytes + hf * kHalfBytes,
-                      xq + hf * 64, q0 + i * BM);
-      int issued = 0;
-      for (int t = 0; t < 2 * nkv; ++t) {
-        const int slot = t % NS;
-        if (t >= NS && !mbar_wait(&bars->kv_empty[slot], ((t / NS) - 1) & 1, abort_flag, p.status))
-          break;
-        const int j = t >> 1;
-        const bool is_v = t & 1;
-        const CUtensorMap* map;
-        int row;
-        if (j < p.nt_main) {
-          map = is_v ? &tm_vm : &tm_km;
-          row = j * BN;
-        } else {
-          map = is_v ? &tm_vl : &tm_kl;
-          row = (j - p.nt_main) * BN;
-        }
-        uint8_t* dst = smem + SmemLayout::ring + slot * kTileBytes;
-        mbar_arrive_expect_tx(&bars->kv_full[slot], kTileBytes);
-        tma_load_2d(map, &bars->kv_full[slot], dst, xq, row);
-        tma_load_2d(map, &bars->kv_full[slot], dst + kHalfBytes, xq + 64, row);
-        issued = t + 1;
-      }
-      if (*abort_flag) {
-        // drain: wait (bounded) for the copies still in flight
-        for (int t = issued - NS < 0 ? 0 : issued - NS; t < issued; ++t)
-          mbar_wait_drain(&bars->kv_full[t % NS], (t / NS) & 1, 100000000ull);
-        mbar_wait_drain(&bars->q_full, 0, 100000000ull);
-      }
-    }
-    __syncwarp();   // lanes 1-31 wait here for lane 0: the warp reaches the CTA barrier converged
-  } else if (warp == kMmaWarp) {
-    if (lane == 0) {
-      const uint32_t q_base = smem_u32(smem + SmemLayout::q);
-      const uint32_t ring_base = smem_u32(smem + SmemLayout::ring);
-      bool ok = mbar_wait(&bars->q_full, 0, abort_flag, p.status);
-      tc_fence_after();
-      for (int j = 0; ok && j < nkv; ++j) {
-        const int tk = 2 * j, tv = 2 * j + 1;
-        const int sk = tk % NS, sv = tv % NS;
-        if (!(ok = mbar_wait(&bars->kv_full[sk], (tk / NS) & 1, abort_flag, p.status))) break;
-        tc_fence_after();
-        const uint32_t kb = ring_base + sk * kTileBytes;
-        for (int i = 0; i < 2; ++i) {
-          if (j > 0) {
-            if (!(ok = mbar_wait(&bars->o_ready[i], (j - 1) & 1, abort_flag, p.status))) break;
-            tc_fence_after();
+  if (warp >= 8) {
+    // ---------------- warpgroup 2: producer, MMA issuer, two idle warps
+    if (warp == kProducerWarp) {
+      if (lane == 0) {
+        prefetch_tmap(&tm_q);
+        const int xq = head * HD;
+        mbar_arrive_expect_tx(&bars->q_full, 2 * kTileBytes);
+        for (int i = 0; i < 2; ++i)
+          for (int hf = 0; hf < 2; ++hf)
+            tma_load_2d(&tm_q, &bars->q_full,
+                        smem + SmemLayout::q + i * kTileBytes + hf * kHalfBytes, xq + hf * 64,
+                        q0 + i * BM);
+        int issued = 0;
+        for (int t = 0; t < 2 * nloc; ++t) {
+          const int slot = t % NS;
+          if (t >= NS &&
+              !mbar_wait(&bars->kv_empty[slot], ((t / NS) - 1) & 1, abort_flag, p.status))
+            break;
+          const int j = jb + (t >> 1);
+          const bool is_v = t & 1;
+          const CUtensorMap* map;
+          int row;
+          if (j < p.nt_main) {
+            map = is_v ? &tm_vm : &tm_km;
+            row = j * BN;
+          } else {
+            map = is_v ? &tm_vl : &tm_kl;
+            row = (j - p.nt_main) * BN;
           }
-          const uint32_t qb = q_base + i * kTileBytes;
-#pragma unroll
-          for (int ks = 0; ks < HD / 16; ++ks) {
-            const uint32_t off = (ks >> 2) * kHalfBytes + (ks & 3) * 32;
-            mma_ss(tmem + col_s(i), sdesc(qb + off, 16, 1024, kSwizzle128B),
-                   sdesc(kb + off, 16, 1024, kSwizzle128B), kIdescQK, ks > 0);
-          }
-          mma_commit(&bars->s_full[i]);
+          uint8_t* dst = smem + SmemLayout::ring + slot * kTileBytes;
+          mbar_arrive_expect_tx(&bars->kv_full[slot], kTileBytes);
+          tma_load_2d(map, &bars->kv_full[slot], dst, xq, row);
+          tma_load_2d(map, &bars->kv_full[slot], dst + kHalfBytes, xq + 64, row);
+          issued = t + 1;
         }
-        if (!ok) break;
-        mma_commit(&bars->kv_empty[sk]);
-        if (!(ok = mbar_wait(&bars->kv_full[sv], (tv / NS) & 1, abort_flag, p.status))) break;
+        if (*abort_flag) {
+          // drain: wait (bounded) for the copies still in flight
+          for (int t = issued - NS < 0 ? 0 : issued - NS; t < issued; ++t)
+            mbar_wait_drain(&bars->kv_full[t % NS], (t / NS) & 1, 100000000ull);
+          mbar_wait_drain(&bars->q_full, 0, 100000000ull);
+        }
+      }
+      __syncwarp();   // lanes 1-31 wait here for lane 0: the warp reaches the CTA barrier converged
+    } else if (warp == kMmaWarp) {
+      if (lane == 0) {
+        const uint32_t q_base = smem_u32(smem + SmemLayout::q);
+        const uint32_t ring_base = smem_u32(smem + SmemLayout::ring);
+        bool ok = mbar_wait(&bars->q_full, 0, abort_flag, p.status);
         tc_fence_after();
-        const uint32_t vb = ring_base + sv * kTileBytes;
-        for (int i = 0; i < 2; ++i) {
-          if (!(ok = mbar_wait(&bars->p_ready[i], j & 1, abort_flag, p.status))) break;
+        for (int jj = 0; ok && jj < nloc; ++jj) {
+          const int tk = 2 * jj, tv = 2 * jj + 1;
+          const int sk = tk % NS, sv = tv % NS;
+          if (!(ok = mbar_wait(&bars->kv_full[sk], (tk / NS) & 1, abort_flag, p.status))) break;
           tc_fence_after();
+          const uint32_t kb = ring_base + sk * kTileBytes;
+          for (int i = 0; i < 2; ++i) {
+            if (jj > 0) {
+              if (!(ok = mbar_wait(&bars->o_ready[i], (jj - 1) & 1, abort_flag, p.status))) break;
+              tc_fence_after();
+            }
+            const uint32_t qb = q_base + i * kTileBytes;
 #pragma unroll
-          for (int ks = 0; ks < BN / 16; ++ks) {
-            // B = V_j rows [16ks, 16ks+16): MN-major, 64-column boxes 16 KiB apart
-            // (leading byte offset), 8-row groups 1 KiB apart (stride byte offset)
-            mma_ts(tmem + col_o(i), tmem + col_s(i) + ks * 8,
-                   sdesc(vb + ks * 16 * 128, kHalfBytes, 1024, kSwizzle128B), kIdescPV,
-                   (j > 0 || ks > 0) ? 1u : 0u);
+            for (int ks = 0; ks < HD / 16; ++ks) {
+              const uint32_t off = (ks >> 2) * kHalfBytes + (ks & 3) * 32;
+              mma_ss(tmem + col_s(i), sdesc(qb + off, 16, 1024, kSwizzle128B),
+                     sdesc(kb + off, 16, 1024, kSwizzle128B), kIdescQK, ks > 0);
+            }
+            mma_commit(&bars->s_full[i]);
           }
-          mma_commit(&bars->o_ready[i]);
+          if (!ok) break;
+          mma_commit(&bars->kv_empty[sk]);
+          if (!(ok = mbar_wait(&bars->kv_full[sv], (tv / NS) & 1, abort_flag, p.status))) break;
+          tc_fence_after();
+          const uint32_t vb = ring_base + sv * kTileBytes;
+          for (int i = 0; i < 2; ++i) {
+            if (!(ok = mbar_wait(&bars->p_ready[i], jj & 1, abort_flag, p.status))) break;
+            tc_fence_after();
+#pragma unroll
+            for (int ks = 0; ks < BN / 16; ++ks) {
+              // B = V_j rows [16ks, 16ks+16): MN-major, 64-column boxes 16 KiB apart
+              // (leading byte offset), 8-row groups 1 KiB apart (stride byte offset)
+              mma_ts(tmem + col_o(i), tmem + col_s(i) + ks * 8,
+                     sdesc(vb + ks * 16 * 128, kHalfBytes, 1024, kSwizzle128B), kIdescPV,
+                     (jj > 0 || ks > 0) ? 1u : 0u);
+            }
+            mma_commit(&bars->o_ready[i]);
+          }
+          if (!ok) break;
+          mma_commit(&bars->kv_empty[sv]);
         }
-        if (!ok) break;
-        mma_commit(&bars->kv_empty[sv]);
+        // all issued MMAs complete before teardown
+        mma_commit(&bars->drain);
+        mbar_wait_drain(&bars->drain, 0, 1000000000ull);
       }
-      // all issued MMAs complete before teardown
-      mma_commit(&bars->drain);
-      mbar_wait_drain(&bars->drain, 0, 1000000000ull);
+      __syncwarp();
     }
-    __syncwarp();
   } else {
-    // softmax warpgroups
+    // ---------------- warpgroups 0-1: softmax and epilogue
     const int qt = warp >> 2;                       // query tile 0 or 1
     const int row = 32 * (warp & 3) + lane;         // TMEM lane = row of the tile
     const uint32_t lane_addr = tmem + ((uint32_t)(32 * (warp & 3)) << 16);
     const uint32_t s_addr = lane_addr + col_s(qt);
     const uint32_t o_addr = lane_addr + col_o(qt);
     const float sl2 = p.scale_log2;
-    float m = -INFINITY, l = 0.f;
+    float m = -INFINITY, l = 0.f, lx = 0.f;   // lx: exact (unrounded) sum, for the LSE
     bool ok = true;
     // Every tcgen05.ld/st below is .sync.aligned: all 32 lanes of the warp must
     // execute it together, so branch conditions around them are warp-uniform.
-    for (int j = 0; j < nkv; ++j) {
-      ok = __all_sync(0xffffffffu, mbar_wait(&bars->s_full[qt], j & 1, abort_flag, p.status));
+    for (int jj = 0; jj < nloc; ++jj) {
+      ok = __all_sync(0xffffffffu, mbar_wait(&bars->s_full[qt], jj & 1, abort_flag, p.status));
       if (!ok) break;
       tc_fence_after();
       uint32_t sr[4][32];
 #pragma unroll
       for (int c = 0; c < 4; ++c) tmem_ld32(s_addr + 32 * c, sr[c]);
       tmem_ld_wait();
-      const int valid = tile_valid(p, j);   // warp-uniform
+      const int valid = tile_valid(p, jb + jj);   // warp-uniform
       if (valid < BN) {
 #pragma unroll
         for (int c = 0; c < 4; ++c)
@@ -297,29 +330,17 @@ k_block_attn_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         mx[c] = fmaxf(mx[c], __uint_as_float(sr[c][31]));
       }
       const float tmax = fmax3(fmaxf(mx[0], mx[1]), mx[2], mx[3]);
-      // rows whose max rose by more than 2^8 (exp2 units) rescale O and l
-      const bool need = j > 0 && (tmax - m) * sl2 > 8.0f;
-      if (j == 0) m = tmax;
-      if (__any_sync(0xffffffffu, need)) {
-        const float f = need ? ex2((m - tmax) * sl2) : 1.0f;
-        if (need) {
-          m = tmax;
-          l *= f;
-        }
-#pragma unroll 1
-        for (int c = 0; c < 4; ++c) {
-          uint32_t orow[32];
-          tmem_ld32(o_addr + 32 * c, orow);
-          tmem_ld_wait();
-#pragma unroll
-          for (int e = 0; e < 32; ++e) orow[e] = __float_as_uint(__uint_as_float(orow[e]) * f);
-          tmem_st32(o_addr + 32 * c, orow);
-        }
-      }
+      // rows whose max rose by more than 2^8 (exp2 units) move to the new max;
+      // their O and l are rescaled below, once the S registers are free
+      const bool need = jj > 0 && (tmax - m) * sl2 > 8.0f;
+      const float f = need ? ex2((m - tmax) * sl2) : 1.0f;
+      if (jj == 0 || need) m = tmax;
+      l *= f;
+      if (kLse) lx *= f;
       // p = 2^(s*sl2 - m*sl2) rounded to bf16 for the P V product; the row sum
       // adds the same rounded values, so numerator and denominator agree.
       const float nmsl2 = -m * sl2;
-      float rs0 = 0.f, rs1 = 0.f;
+      float rs0 = 0.f, rs1 = 0.f, xs0 = 0.f, xs1 = 0.f;
 #pragma unroll
       for (int hf = 0; hf < 2; ++hf) {
         uint32_t pk[32];   // bf16 pairs for keys 64*hf .. 64*hf+63
@@ -331,41 +352,122 @@ k_block_attn_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             float x0, x1;
             ffma2(x0, x1, __uint_as_float(sr[c][e]), __uint_as_float(sr[c][e + 1]), sl2, sl2,
                   nmsl2, nmsl2);
-            const uint32_t w = pack_bf16x2(ex2(x0), ex2(x1));
+            const float p0 = ex2(x0), p1 = ex2(x1);
+            const uint32_t w = pack_bf16x2(p0, p1);
             pk[16 * c2 + (e >> 1)] = w;
             fadd2_acc(rs0, rs1, __uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
+            if (kLse) fadd2_acc(xs0, xs1, p0, p1);
           }
         tmem_st32(s_addr + 32 * hf, pk);
       }
       l += rs0 + rs1;
+      if (kLse) lx += xs0 + xs1;
+      if (__any_sync(0xffffffffu, need)) {
+#pragma unroll 1
+        for (int c = 0; c < 4; ++c) {
+          uint32_t orow[32];
+          tmem_ld32(o_addr + 32 * c, orow);
+          tmem_ld_wait();
+#pragma unroll
+          for (int e = 0; e < 32; ++e) orow[e] = __float_as_uint(__uint_as_float(orow[e]) * f);
+          tmem_st32(o_addr + 32 * c, orow);
+        }
+      }
       tmem_st_wait();
       tc_fence_before();
       mbar_arrive(&bars->p_ready[qt]);
     }
     if (ok)
       ok = __all_sync(0xffffffffu,
-                      mbar_wait(&bars->o_ready[qt], (nkv - 1) & 1, abort_flag, p.status));
+                      mbar_wait(&bars->o_ready[qt], (nloc - 1) & 1, abort_flag, p.status));
     tc_fence_after();
     const int grow = q0 + qt * BM + row;
     const bool store = grow < p.n_q;
-    if (ok) {
-      const float inv_l = 1.0f / l;
-      OutT* orow_g = static_cast<OutT*>(p.o) + ((size_t)(store ? grow : 0) * p.n_heads + head) * HD;
-      const float wo = p.accumulate ? (p.w_old ? p.w_old[head] : 1.0f) : 0.0f;
-      const float wn = (p.accumulate ? (p.w_new ? p.w_new[head] : 1.0f) : 1.0f) * inv_l;
+    const float wo = p.accumulate ? (p.w_old ? p.w_old[head] : 1.0f) : 0.0f;
+    const float wn0 = p.accumulate ? (p.w_new ? p.w_new[head] : 1.0f) : 1.0f;
+    OutT* orow_g = static_cast<OutT*>(p.o) + ((size_t)(store ? grow : 0) * p.n_heads + head) * HD;
+    if (p.n_split == 1) {
+      if (ok) {
+        const float wn = wn0 / l;
 #pragma unroll 1
-      for (int c = 0; c < 4; ++c) {
-        uint32_t orow[32];
-        tmem_ld32(o_addr + 32 * c, orow);   // whole warp
-        tmem_ld_wait();
-        if (store) {
-          float x[32];
+        for (int c = 0; c < 4; ++c) {
+          uint32_t orow[32];
+          tmem_ld32(o_addr + 32 * c, orow);   // whole warp
+          tmem_ld_wait();
+          if (store) {
+            float x[32];
 #pragma unroll
-          for (int e = 0; e < 32; ++e) x[e] = __uint_as_float(orow[e]) * wn;
-          store_row32(orow_g + 32 * c, x, p.accumulate != 0, wo);
+            for (int e = 0; e < 32; ++e) x[e] = __uint_as_float(orow[e]) * wn;
+            store_row32(orow_g + 32 * c, x, p.accumulate != 0, wo);
+          }
+        }
+        if (kLse && store && p.lse) p.lse[(size_t)head * p.n_q + grow] = m * p.scale + logf(lx);
+      }
+    } else {
+      // split: store this CTA's unnormalised rows, then the last CTA of the
+      // (head, query pair) combines all splits
+      const int unit = head * p.n_qpairs + qpair;
+      const int prow = qt * BM + row;                     // 0..255
+      if (ok) {
+        float* dst = p.part_o + (((size_t)unit * p.n_split + split) * 256 + prow) * HD;
+#pragma unroll 1
+        for (int c = 0; c < 4; ++c) {
+          uint32_t orow[32];
+          tmem_ld32(o_addr + 32 * c, orow);
+          tmem_ld_wait();
+          float4* d4 = reinterpret_cast<float4*>(dst + 32 * c);
+#pragma unroll
+          for (int v = 0; v < 8; ++v)
+            __stcg(d4 + v, make_float4(__uint_as_float(orow[4 * v]), __uint_as_float(orow[4 * v + 1]),
+                                       __uint_as_float(orow[4 * v + 2]),
+                                       __uint_as_float(orow[4 * v + 3])));
+        }
+        __stcg(p.part_ml + ((size_t)unit * p.n_split + split) * 256 + prow, make_float4(m, l, lx, 0.f));
+      }
+      __threadfence();
+      softmax_bar();
+      // every CTA takes its ticket (even after an abort) so the counter returns to 0
+      if (threadIdx.x == 0) bars->ticket = atomicAdd(&p.counters[unit], 1u);
+      softmax_bar();
+      const bool last = bars->ticket == (unsigned)(p.n_split - 1);
+      if (last) {
+        __threadfence();
+        if (threadIdx.x == 0) p.counters[unit] = 0u;
+        if (ok && store) {
+          const float4* ml = p.part_ml + (size_t)unit * p.n_split * 256 + prow;
+          float mm = -INFINITY;
+          for (int s = 0; s < p.n_split; ++s) mm = fmaxf(mm, __ldcg(ml + (size_t)s * 256).x);
+          float den = 0.f, denx = 0.f;
+          for (int s = 0; s < p.n_split; ++s) {
+            const float4 t = __ldcg(ml + (size_t)s * 256);
+            const float w = ex2((t.x - mm) * sl2);
+            den += w * t.y;
+            denx += w * t.z;
+          }
+          const float wn = wn0 / den;
+          const float* src = p.part_o + ((size_t)unit * p.n_split * 256 + prow) * HD;
+#pragma unroll 1
+          for (int c = 0; c < 4; ++c) {
+            float x[32];
+#pragma unroll
+            for (int e = 0; e < 32; ++e) x[e] = 0.f;
+            for (int s = 0; s < p.n_split; ++s) {
+              const float w = ex2((__ldcg(ml + (size_t)s * 256).x - mm) * sl2) * wn;
+              const float4* s4 = reinterpret_cast<const float4*>(src + (size_t)s * 256 * HD + 32 * c);
+#pragma unroll
+              for (int v = 0; v < 8; ++v) {
+                const float4 t = __ldcg(s4 + v);
+                x[4 * v] += w * t.x;
+                x[4 * v + 1] += w * t.y;
+                x[4 * v + 2] += w * t.z;
+                x[4 * v + 3] += w * t.w;
+              }
+            }
+            store_row32(orow_g + 32 * c, x, p.accumulate != 0, wo);
+          }
+          if (kLse && p.lse) p.lse[(size_t)head * p.n_q + grow] = mm * p.scale + logf(denx);
         }
       }
-      if (store && p.lse) p.lse[(size_t)head * p.n_q + grow] = m * p.scale + logf(l);
     }
   }
 
@@ -378,21 +480,57 @@ k_block_attn_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
   }
 }
 
+// Split count: fewest whole waves of the SMs per unit of work; a split adds a
+// small combine cost, so ties keep the smaller count.
+int choose_split(int units, int nkv, int sms) {
+  int best = 1;
+  double best_cost = 1e30;
+  for (int s = 1; s <= 4; ++s) {
+    if (nkv < 2 * s && s > 1) break;
+    if (s > 1 && units > kMaxUnits) break;
+    const long long ctas = (long long)units * s;
+    const double waves = (double)((ctas + sms - 1) / sms);
+    const double cost = waves / s * (s > 1 ? 1.03 : 1.0);
+    if (cost < best_cost - 1e-9) {
+      best_cost = cost;
+      best = s;
+    }
+  }
+  return best;
+}
+
+template <typename OutT, bool kLse>
+wa_status launch_t(const CUtensorMap& tq, const CUtensorMap& tkm, const CUtensorMap& tvm,
+                   const CUtensorMap& tkl, const CUtensorMap& tvl, const Params& p, int n_heads,
+                   cudaStream_t s) {
+  const int smem = SmemLayout::total + 1024;
+  static bool attr_done[64] = {};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  auto kern = k_block_attn_tc<OutT, kLse>;
+  if (dev < 64 && !attr_done[dev]) {
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
+      return WA_ERR_CUDA;
+    attr_done[dev] = true;
+  }
+  dim3 grid(p.n_qpairs * p.n_split, n_heads);
+  kern<<<grid, kThreads, smem, s>>>(tq, tkm, tvm, tkl, tvl, p);
+  return cuda_status(cudaPeekAtLastError());
+}
+
 }  // namespace
 
 wa_status launch_attn_tc(const void* q, int n_q, const void* k_main, const void* v_main,
                          int n_main, const void* k_loc, const void* v_loc, int n_loc, int n_heads,
                          float scale, void* o, int o_f32, float* lse, int accumulate,
                          const float* w_old, const float* w_new, cudaStream_t s) {
-  Ctrl* ctrl = nullptr;
-  wa_status rc = get_ctrl(&ctrl);
-  if (rc != WA_OK) return rc;
   const uint64_t cols = (uint64_t)n_heads * HD;
   CUtensorMap tq, tkm, tvm, tkl, tvl;
   memset(&tkm, 0, sizeof(tkm));
   memset(&tvm, 0, sizeof(tvm));
   memset(&tkl, 0, sizeof(tkl));
   memset(&tvl, 0, sizeof(tvl));
+  wa_status rc;
   if ((rc = make_tmap_2d_bf16(&tq, q, cols, n_q, cols, 64, BM)) != WA_OK) return rc;
   if (n_main > 0) {
     if ((rc = make_tmap_2d_bf16(&tkm, k_main, cols, n_main, cols, 64, BN)) != WA_OK) return rc;
@@ -409,6 +547,18 @@ wa_status launch_attn_tc(const void* q, int n_q, const void* k_main, const void*
   p.n_loc = n_loc;
   p.nt_main = (n_main + BN - 1) / BN;
   p.nt_loc = (n_loc + BN - 1) / BN;
+  p.n_qpairs = (n_q + 2 * BM - 1) / (2 * BM);
+  int dev = 0, sms = 148;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  p.n_split = choose_split(p.n_qpairs * n_heads, p.nt_main + p.nt_loc, sms);
+  // WA_ATTN_SPLIT=n forces the split count (clamped to what the tiles allow)
+  if (const char* env = getenv("WA_ATTN_SPLIT")) {
+    int f = atoi(env);
+    const int nkv = p.nt_main + p.nt_loc;
+    if (f >= 1) p.n_split = f > nkv ? nkv : f;
+    if ((size_t)p.n_qpairs * n_heads > (size_t)kMaxUnits) p.n_split = 1;
+  }
   p.scale = scale;
   p.scale_log2 = scale * 1.4426950408889634f;
   p.o = o;
@@ -416,20 +566,26 @@ wa_status launch_attn_tc(const void* q, int n_q, const void* k_main, const void*
   p.accumulate = accumulate;
   p.w_old = w_old;
   p.w_new = w_new;
-  p.status = &ctrl->status;
-  const int smem = SmemLayout::total + 1024;
-  static bool attr_done[64][2] = {};
-  int dev = 0;
-  cudaGetDevice(&dev);
-  auto kern = o_f32 ? k_block_attn_tc<float> : k_block_attn_tc<__nv_bfloat16>;
-  if (dev < 64 && !attr_done[dev][o_f32 ? 1 : 0]) {
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
-      return WA_ERR_CUDA;
-    attr_done[dev][o_f32 ? 1 : 0] = true;
+  p.part_o = nullptr;
+  p.part_ml = nullptr;
+  p.counters = nullptr;
+  Scratch sc;
+  const size_t units = (size_t)p.n_qpairs * n_heads;
+  const size_t part_o_bytes = p.n_split > 1 ? units * p.n_split * 256 * HD * sizeof(float) : 0;
+  const size_t part_ml_bytes = p.n_split > 1 ? units * p.n_split * 256 * sizeof(float4) : 0;
+  if ((rc = get_scratch(part_o_bytes + part_ml_bytes, &sc)) != WA_OK) return rc;
+  p.status = &sc.ctrl->status;
+  if (p.n_split > 1) {
+    p.part_o = static_cast<float*>(sc.data);
+    p.part_ml = reinterpret_cast<float4*>(static_cast<char*>(sc.data) + part_o_bytes);
+    p.counters = sc.ctrl->attn_counters;
   }
-  dim3 grid((n_q + 2 * BM - 1) / (2 * BM), n_heads);
-  kern<<<grid, kThreads, smem, s>>>(tq, tkm, tvm, tkl, tvl, p);
-  return cuda_status(cudaPeekAtLastError());
+  const bool want_lse = lse != nullptr;
+  if (o_f32)
+    return want_lse ? launch_t<float, true>(tq, tkm, tvm, tkl, tvl, p, n_heads, s)
+                    : launch_t<float, false>(tq, tkm, tvm, tkl, tvl, p, n_heads, s);
+  return want_lse ? launch_t<__nv_bfloat16, true>(tq, tkm, tvm, tkl, tvl, p, n_heads, s)
+                  : launch_t<__nv_bfloat16, false>(tq, tkm, tvm, tkl, tvl, p, n_heads, s);
 }
 
 }  // namespace wa

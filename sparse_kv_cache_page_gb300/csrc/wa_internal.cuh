@@ -20,7 +20,8 @@ enum : int {
 struct Ctrl {
   int status;           // kStatus* bits
   int pad[31];
-  unsigned int counters[4096];   // zero between launches; "last CTA" tickets
+  unsigned int counters[4096];        // zero between launches; "last CTA" tickets
+  unsigned int attn_counters[8192];   // per (head, query-tile pair) of a split attention
 };
 
 // Scratch arena of the current device: Ctrl block + `bytes` of data.

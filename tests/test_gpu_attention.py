@@ -19,16 +19,29 @@ pytestmark = pytest.mark.gpu
 DEV = "cuda"
 
 
-def _run(q, km, vm, kl, vl, scale=0.0, out_dtype=torch.float32):
+def _run(q, km, vm, kl, vl, scale=0.0, out_dtype=torch.float32, want_lse=True):
     """Attention through the C ABI; fp32 output unless asked otherwise (the
     stated 1e-2 tolerance is for the fp32 result; a bf16 output adds up to
     half a bf16 ulp of rounding)."""
     o = torch.empty(q.shape, dtype=out_dtype, device=DEV)
-    lse = torch.empty((q.shape[1], q.shape[0]), dtype=torch.float32, device=DEV)
+    lse = (torch.empty((q.shape[1], q.shape[0]), dtype=torch.float32, device=DEV)
+           if want_lse else None)
     d = lambda t: None if t is None else t.to(DEV)  # noqa: E731
     wa.wa_block_attn(q.to(DEV), d(km), d(vm), d(kl), d(vl), o, lse, scale)
     wa.wa_check()
     return o, lse
+
+
+@pytest.fixture
+def split(monkeypatch):
+    """Force the key-range split count of the tensor-core kernel."""
+    def _set(n):
+        if n is None:
+            monkeypatch.delenv("WA_ATTN_SPLIT", raising=False)
+        else:
+            monkeypatch.setenv("WA_ATTN_SPLIT", str(n))
+    yield _set
+    monkeypatch.delenv("WA_ATTN_SPLIT", raising=False)
 
 
 def _oracle(q, km, vm, kl, vl, rows=None, scale=None):
@@ -141,20 +154,38 @@ def test_attn_bf16_scale_and_reuse_of_output_buffer():
     assert torch.equal(o1, o2)            # deterministic run to run
 
 
+@pytest.mark.parametrize("n_split", [1, 2, 3, 4])
+def test_attn_bf16_split_paths_agree(split, n_split):
+    """Every key-range split count gives the oracle's result (ragged tiles,
+    two heads, output fusion off)."""
+    q, km, vm, kl, vl = _case(300, 1000, 77, 2, 128, torch.bfloat16, 11)
+    split(n_split)
+    o, lse = _run(q.to(DEV), km, vm, kl, vl)
+    ref_o, ref_lse = _oracle(q, km, vm, kl, vl)
+    assert_attn_close(o, ref_o, torch.bfloat16, f"split {n_split}")
+    assert np.abs(f64(lse) - ref_lse).max() <= LSE_ABS
+    o2, _ = _run(q.to(DEV), km, vm, kl, vl, want_lse=False)
+    np.testing.assert_allclose(f64(o2), f64(o), atol=1e-5)
+
+
 def test_attn_bf16_worldattention_shape_sampled():
-    """Full one-layer shape: 4,680 queries x 12 heads over 49,920 buffer keys
-    + 4,680 local keys; oracle on 48 sampled rows (incl. the ragged last query
-    tile) for every head, plus finiteness of the whole output."""
+    """Full one-layer shape, in the launch configuration the benchmark times
+    (fp32 output, no LSE, automatic split): 4,680 queries x 12 heads over
+    49,920 buffer keys + 4,680 local keys; oracle on 48 sampled rows (incl. the
+    ragged last query tile) for every head, plus finiteness of the whole
+    output; then the LSE variant on the same inputs."""
     H, n_q, n_main, n_loc = 12, 4680, 49920, 4680
     g = lambda n, t: synth.normal((n, H, 128), synth.seed_of("wa_attn", t), device=DEV,  # noqa: E731
                                   dtype=torch.bfloat16)
     q, km, vm, kl, vl = g(n_q, "q"), g(n_main, "km"), g(n_main, "vm"), g(n_loc, "kl"), g(n_loc, "vl")
-    o, lse = _run(q, km, vm, kl, vl)
-    assert torch.isfinite(o.float()).all()
+    o, _ = _run(q, km, vm, kl, vl, want_lse=False)
+    assert torch.isfinite(o).all()
     rows = np.unique(np.concatenate([np.arange(0, n_q, 131), [4607, 4608, 4660, 4679]]))[:48]
     ref_o, ref_lse = _oracle(q, km, vm, kl, vl, rows=rows)
     assert_attn_close(o[torch.from_numpy(rows).to(DEV)], ref_o, torch.bfloat16, "full shape")
+    o2, lse = _run(q, km, vm, kl, vl)
     assert np.abs(f64(lse)[:, rows] - ref_lse).max() <= LSE_ABS
+    np.testing.assert_allclose(f64(o2[torch.from_numpy(rows).to(DEV)]), f64(o[torch.from_numpy(rows).to(DEV)]), atol=1e-5)
 
 
 def test_attn_bf16_peaked_at_full_length():
