@@ -120,6 +120,34 @@ wa_status wa_select_pages(const void* q, wa_dtype dt, int n_q, int n_heads, int 
                           wa_stream_t stream);
 
 /*
+ * wa_select_pages without any device allocation (there is no counterpart on
+ * the pages; this is a deployment variant).  Same arguments, results and
+ * errors as wa_select_pages, for callers that must not allocate device
+ * memory once they are running -- a serving process that has handed all free
+ * HBM to its own pool, or a latency-critical loop where a cudaMalloc (and the
+ * device-wide synchronize that growing the library's scratch arena implies)
+ * would stall other work.  This call performs no cudaMalloc or cudaFree.
+ *
+ * Its scratch is a fixed 2 MiB array (plus a 48 KiB control block) compiled
+ * into the library; every GPU that loads the library holds it until the
+ * process exits.  Limit: min(304, max(1, n_q/32)) * n_heads * head_dim * 4
+ * bytes of partial sums must fit in 2 MiB (e.g. n_heads*head_dim = 1536 fits
+ * every n_q); larger requests return WA_ERR_SHAPE and enqueue nothing.
+ * The first call on a device looks up the array's device address with
+ * cudaGetSymbolAddress; make that first call before any stream capture.
+ * Every call shares the one array, which keeps the previous call's contents:
+ * the call clears its ticket counter itself (cudaMemsetAsync on `stream`),
+ * and calls that overlap on the GPU (other streams, other host threads)
+ * race on the array and give wrong results; serialize them.
+ */
+wa_status wa_select_pages_noalloc(const void* q, wa_dtype dt, int n_q, int n_heads, int head_dim,
+                                  const float* kbar, int n_pages,
+                                  const float* prompt_cur, const float* prompt_chunks,
+                                  int n_chunks, int prompt_dim, int pages_per_chunk, int k_p,
+                                  int32_t* idx_out, float* scores_out, int32_t* chunk_out,
+                                  wa_stream_t stream);
+
+/*
  * Gather of the retrieved pages into one contiguous buffer ([WA] Fig. 1,
  * custom kernels; [IX] KV Cache Manager, index-based selective fetch):
  *

@@ -36,8 +36,8 @@ WA_F32, WA_BF16 = 0, 1
 
 # Every symbol include/wa.h declares.
 EXPORTED_SYMBOLS = ("wa_strerror", "wa_version", "wa_page_summarize", "wa_select_pages",
-                    "wa_gather_pages", "wa_block_attn", "wa_linear_branch", "wa_check",
-                    "wa_shutdown")
+                    "wa_select_pages_noalloc", "wa_gather_pages", "wa_block_attn",
+                    "wa_linear_branch", "wa_check", "wa_shutdown")
 
 
 class WaError(RuntimeError):

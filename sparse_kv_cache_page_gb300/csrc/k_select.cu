@@ -12,6 +12,7 @@
 // sums, fences, and takes a ticket; the CTA holding the last ticket adds the
 // partials in a fixed order (deterministic) and runs the tail work.
 #include <math.h>
+#include <mutex>
 
 #include "wa_internal.cuh"
 
@@ -445,3 +446,136 @@ wa_status launch_select_pages(const void* q, wa_dtype dt, int n_q, int n_heads, 
 }
 
 }  // namespace wa
+
+// ---------------------------------------------------------------------------
+// wa_select_pages_noalloc: the same retrieval with its scratch in a fixed
+// array compiled into the library instead of the library's cudaMalloc'd
+// arena.  For callers that must not allocate device memory once they are
+// running: a serving process that has handed all free HBM to its own pool, or
+// a latency-critical loop in which a cudaMalloc -- and the device-wide
+// synchronize that growing the library's arena implies -- would stall other
+// work on the GPU.  There is no counterpart on the pages.
+// ---------------------------------------------------------------------------
+namespace wa {
+namespace {
+
+constexpr size_t kNoAllocPartialBytes = size_t(2) << 20;      // 2 MiB of partial sums
+constexpr size_t kNoAllocCtrlBytes = (sizeof(Ctrl) + 255) & ~size_t(255);
+
+// Every device that loads the library holds this array until the process exits.
+static __device__ __align__(256) unsigned char g_select_scratch[kNoAllocCtrlBytes +
+                                                                 kNoAllocPartialBytes];
+
+std::mutex g_noalloc_mu;
+unsigned char* g_noalloc_ptr[64] = {};   // device address of the array, per device
+
+// Device address of g_select_scratch on the current device (host code must not
+// use the symbol itself: on the host it is only a stand-in).
+wa_status noalloc_scratch(unsigned char** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return WA_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(g_noalloc_mu);
+  if (!g_noalloc_ptr[dev]) {
+    void* ptr = nullptr;
+    if (cudaGetSymbolAddress(&ptr, g_select_scratch) != cudaSuccess || ptr == nullptr) {
+      cudaGetLastError();
+      return WA_ERR_CUDA;
+    }
+    g_noalloc_ptr[dev] = static_cast<unsigned char*>(ptr);
+  }
+  *out = g_noalloc_ptr[dev];
+  return WA_OK;
+}
+
+template <typename T>
+wa_status select_noalloc_t(const T* q, SelectArgs a, cudaStream_t st) {
+  Plan p = plan_rows<T>(a.row_elems);
+  int splits = a.n_q / 32;   // the split rule of the allocating entry point
+  if (splits < 1) splits = 1;
+  if (splits > 304) splits = 304;
+  const int rps = (a.n_q + splits - 1) / splits;
+  splits = (a.n_q + rps - 1) / rps;
+  if ((size_t)splits * a.row_elems * sizeof(float) > kNoAllocPartialBytes) return WA_ERR_SHAPE;
+  unsigned char* base = nullptr;
+  wa_status rc = noalloc_scratch(&base);
+  if (rc != WA_OK) return rc;
+  Ctrl* ctrl = reinterpret_cast<Ctrl*>(base);
+  // the ticket counter must start at zero; the array keeps the last call's contents
+  if (cudaMemsetAsync(&ctrl->counters[kSelectCounter], 0, sizeof(unsigned), st) != cudaSuccess)
+    return WA_ERR_CUDA;
+  int n_cand = a.n_chunks > 0 ? a.ppc : a.n_pages;
+  int n2 = 1;
+  while (n2 < n_cand) n2 <<= 1;
+  a.nvec = p.nvec;
+  a.R = p.R;
+  a.splits = splits;
+  a.rows_per_split = rps;
+  a.partial = reinterpret_cast<float*>(base + kNoAllocCtrlBytes);
+  a.ctrl = ctrl;
+  a.n_cand_max2 = n2;
+  size_t smem_a = (size_t)p.R * a.row_elems * sizeof(float);
+  size_t smem_b = (size_t)((a.row_elems + 3) & ~3) * 4 + (size_t)((n2 + 3) & ~3) * 4 +
+                  (size_t)n2 * 8;
+  size_t smem = smem_a > smem_b ? smem_a : smem_b;
+  switch (p.vpt) {
+#define WA_CASE(V)                                                                          \
+  case V:                                                                                   \
+    if (smem > 48 * 1024)                                                                   \
+      cudaFuncSetAttribute(k_select_pages<T, V>, cudaFuncAttributeMaxDynamicSharedMemorySize, \
+                           (int)smem);                                                      \
+    k_select_pages<T, V><<<splits, p.threads, smem, st>>>(q, a);                            \
+    break;
+    WA_CASE(1) WA_CASE(2) WA_CASE(4) WA_CASE(8)
+#undef WA_CASE
+    default: return WA_ERR_SHAPE;
+  }
+  return cuda_status(cudaPeekAtLastError());
+}
+
+inline bool aligned16_ptr(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+}  // namespace
+}  // namespace wa
+
+extern "C" wa_status wa_select_pages_noalloc(const void* q, wa_dtype dt, int n_q, int n_heads,
+                                             int head_dim, const float* kbar, int n_pages,
+                                             const float* prompt_cur, const float* prompt_chunks,
+                                             int n_chunks, int prompt_dim, int pages_per_chunk,
+                                             int k_p, int32_t* idx_out, float* scores_out,
+                                             int32_t* chunk_out, wa_stream_t stream) {
+  using namespace wa;
+  if (dt != WA_BF16 && dt != WA_F32) return WA_ERR_DTYPE;
+  if (!q || !kbar || !idx_out || n_q <= 0 || n_pages <= 0 || k_p <= 0 || n_chunks < 0)
+    return WA_ERR_INVALID_ARG;
+  if (n_heads <= 0 || head_dim <= 0) return WA_ERR_SHAPE;
+  const long long row = (long long)n_heads * head_dim;
+  if ((row * (dt == WA_BF16 ? 2 : 4)) % 16 != 0 || row > 8192) return WA_ERR_SHAPE;
+  int n_cand = n_pages;
+  if (n_chunks > 0) {
+    if (!prompt_cur || !prompt_chunks || prompt_dim <= 0 || pages_per_chunk <= 0)
+      return WA_ERR_INVALID_ARG;
+    if ((long long)n_chunks * pages_per_chunk > n_pages) return WA_ERR_INVALID_ARG;
+    n_cand = pages_per_chunk;
+  }
+  if (k_p > n_cand || k_p > 1024) return WA_ERR_INVALID_ARG;
+  if (n_cand > 8192) return WA_ERR_SHAPE;
+  if (!aligned16_ptr(q) || !aligned16_ptr(kbar)) return WA_ERR_ALIGN;
+  SelectArgs a{};
+  a.n_q = n_q;
+  a.row_elems = (int)row;
+  a.kbar = kbar;
+  a.n_pages = n_pages;
+  a.head_dim = head_dim;
+  a.prompt_cur = prompt_cur;
+  a.prompt_chunks = prompt_chunks;
+  a.n_chunks = n_chunks;
+  a.prompt_dim = prompt_dim;
+  a.ppc = pages_per_chunk;
+  a.k_p = k_p;
+  a.idx_out = idx_out;
+  a.scores_out = scores_out;
+  a.chunk_out = chunk_out;
+  cudaStream_t st = (cudaStream_t)stream;
+  if (dt == WA_BF16) return select_noalloc_t((const __nv_bfloat16*)q, a, st);
+  return select_noalloc_t((const float*)q, a, st);
+}
