@@ -255,10 +255,10 @@ def block_attn(q, k_main, v_main, k_loc, v_loc, scale: float | None = None,
 
 def linformer_project(kv_cat: np.ndarray, e: np.ndarray) -> np.ndarray:
     """X'_h = E^(h)T X_h for each head: kv_cat [L][H][d], e [H][L][r] -> [H][r][d]."""
-    x = as_f64(kv_cat)
-    ee = as_f64(e)
+    x = np.asarray(kv_cat)
     n_h = x.shape[1]
-    return np.stack([ee[h].T @ x[:, h, :] for h in range(n_h)], axis=0)
+    # one head at a time keeps the fp64 copies small at full size
+    return np.stack([as_f64(e[h]).T @ as_f64(x[:, h, :]) for h in range(n_h)], axis=0)
 
 
 def linear_branch(q, k_cat, v_cat, e_k, e_v, scale: float | None = None, rows=None):

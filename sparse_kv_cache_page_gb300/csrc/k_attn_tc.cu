@@ -523,7 +523,7 @@ wa_status launch_t(const CUtensorMap& tq, const CUtensorMap& tkm, const CUtensor
 wa_status launch_attn_tc(const void* q, int n_q, const void* k_main, const void* v_main,
                          int n_main, const void* k_loc, const void* v_loc, int n_loc, int n_heads,
                          float scale, void* o, int o_f32, float* lse, int accumulate,
-                         const float* w_old, const float* w_new, cudaStream_t s) {
+                         const float* w_old, const float* w_new, int max_split, cudaStream_t s) {
   const uint64_t cols = (uint64_t)n_heads * HD;
   CUtensorMap tq, tkm, tvm, tkl, tvl;
   memset(&tkm, 0, sizeof(tkm));
@@ -559,6 +559,7 @@ wa_status launch_attn_tc(const void* q, int n_q, const void* k_main, const void*
     if (f >= 1) p.n_split = f > nkv ? nkv : f;
     if ((size_t)p.n_qpairs * n_heads > (size_t)kMaxUnits) p.n_split = 1;
   }
+  if (max_split > 0 && p.n_split > max_split) p.n_split = max_split;
   p.scale = scale;
   p.scale_log2 = scale * 1.4426950408889634f;
   p.o = o;

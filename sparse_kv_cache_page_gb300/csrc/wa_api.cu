@@ -223,7 +223,7 @@ wa_status wa_block_attn(const void* q, int n_q, const void* k_main, const void* 
   if (head_dim != 128) return WA_ERR_SHAPE;
   if ((long long)n_heads * 128 > 16384) return WA_ERR_SHAPE;
   return launch_attn_tc(q, n_q, k_main, v_main, n_main, k_loc, v_loc, n_loc, n_heads, scale, o,
-                        o_dt == WA_F32, lse, 0, nullptr, nullptr, s);
+                        o_dt == WA_F32, lse, 0, nullptr, nullptr, 0, s);
 }
 
 wa_status wa_linear_branch(const void* q, int n_q, const void* k_main, const void* v_main,

@@ -46,6 +46,11 @@ inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 
 wa_status make_tmap_2d_bf16(CUtensorMap* map, const void* base, uint64_t cols, uint64_t rows,
                             uint64_t row_stride, uint32_t box_cols, uint32_t box_rows);
 
+// 3-D bf16 TMA descriptor over [d2][d1][d0] (d0 contiguous) with strides s1, s2
+// (elements) for dims 1 and 2; box = 1 x box1 x box0, 128-byte swizzle, zero fill.
+wa_status make_tmap_3d_bf16(CUtensorMap* map, const void* base, uint64_t d0, uint64_t d1,
+                            uint64_t d2, uint64_t s1, uint64_t s2, uint32_t box0, uint32_t box1);
+
 // ---------------------------------------------------------------------------
 // kernel launchers (one per translation unit / kernel family)
 // ---------------------------------------------------------------------------
@@ -67,12 +72,14 @@ wa_status launch_attn_f32(const float* q, int n_q, const float* k_main, const fl
                           int n_heads, int head_dim, float scale, float* o, float* lse,
                           cudaStream_t s);
 
-// bf16 tensor-core attention.  out_w_old/out_w_new: per-head fusion weights
-// for the epilogue o = w_old[h]*o + w_new[h]*O (accumulate != 0), may be NULL.
+// bf16 tensor-core attention.  w_old/w_new: per-head fusion weights for the
+// epilogue o = w_old[h]*o + w_new[h]*O (accumulate != 0), may be NULL.
+// max_split: 0 = choose the key-range split automatically, else an upper
+// bound (1 = no split, which also means no scratch is touched).
 wa_status launch_attn_tc(const void* q, int n_q, const void* k_main, const void* v_main,
                          int n_main, const void* k_loc, const void* v_loc, int n_loc,
                          int n_heads, float scale, void* o, int o_f32, float* lse, int accumulate,
-                         const float* w_old, const float* w_new, cudaStream_t s);
+                         const float* w_old, const float* w_new, int max_split, cudaStream_t s);
 
 wa_status launch_linear_branch(const void* q, int n_q, const void* k_main, const void* v_main,
                                int n_main, const void* k_loc, const void* v_loc, int n_loc,
