@@ -67,7 +67,7 @@ class Clocks:
                  "--query-gpu=index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
                  "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
                  "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap",
-                 "--format=csv,noheader,nounits", "-lms", "100"], stdout=self.f,
+                 "--format=csv,noheader,nounits", "-lms", "20"], stdout=self.f,
                 stderr=subprocess.DEVNULL)
         except Exception:
             self.proc = None
@@ -136,7 +136,7 @@ def max_over_ranks(x, world):
 # GPU arm
 # ----------------------------------------------------------------------------
 
-def run_gpu(args, world, rank, local):
+def run_gpu(args, world, rank, local, hybrid=False):
     import torch
 
     import sparse_kv_cache_page_gb300 as wa
@@ -154,8 +154,14 @@ def run_gpu(args, world, rank, local):
     vbuf = torch.empty_like(kbuf)
     o = torch.empty(q.shape, dtype=torch.float32, device=dev)   # fp32 result (tested tolerance)
     stream = torch.cuda.current_stream()
+    L, RANK = KP * P + NLOC, 256
+    if hybrid:
+        ek = synth.normal((H, L, RANK), synth.seed_of("hybrid", "ek"), dev, torch.bfloat16,
+                          std=L ** -0.5)
+        ev = synth.normal((H, L, RANK), synth.seed_of("hybrid", "ev"), dev, torch.bfloat16,
+                          std=L ** -0.5)
 
-    names = ("summarize", "select", "gather", "attention")
+    names = ("summarize", "select", "gather", "attention") + (("linear",) if hybrid else ())
 
     def step(ev=None):
         def mark(i):
@@ -170,11 +176,15 @@ def run_gpu(args, world, rank, local):
         mark(3)
         wa.wa_block_attn(q, kbuf, vbuf, kl, vl, o)
         mark(4)
+        if hybrid:
+            wa.wa_linear_branch(q, kbuf, vbuf, kl, vl, ek, ev, o)
+            mark(5)
 
     for _ in range(args.warmup):
         step()
     wa.wa_check()
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(len(names) + 1)]
+           for _ in range(args.steps)]
     barrier(world)
     torch.cuda.synchronize()
     with Clocks(local) as clk:
@@ -209,6 +219,8 @@ def run_gpu(args, world, rank, local):
         wa.wa_select_pages(dq, kbar, dpc, pch, PPC, KP, idx)
         wa.wa_gather_pages(kp, vp, idx, None, kbuf, vbuf)
         wa.wa_block_attn(dq, kbuf, vbuf, dkl, dvl, o)
+        if hybrid:
+            wa.wa_linear_branch(dq, kbuf, vbuf, dkl, dvl, ek, ev, o)
         ho.copy_(o, non_blocking=True)
 
     for _ in range(max(1, args.warmup)):
@@ -233,6 +245,7 @@ def run_gpu(args, world, rank, local):
     gather_bytes = 2 * 2 * KP * P * H * D * 2          # K and V, read + write
     summ_bytes = N_PAGES * P * H * D * 2
     value = world * flops / (ms_step * 1e-3) / 1e12
+    launches_per_step = 4 + (3 if hybrid else 0)
     line = {
         "metric": METRIC,
         "value": round(value, 2),
@@ -259,10 +272,16 @@ def run_gpu(args, world, rank, local):
                      "kernel": "k_block_attn_tc", "peak_source": f"{src} bf16 sustained"},
         "e2e": {"value": round(world * flops / (e2e_ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
                 "ms_per_step": round(e2e_ms, 4), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
-        "gpu_launches": 4 * args.steps,
+        "gpu_launches": launches_per_step * args.steps,
         "clocks": clk.summary(),
     }
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+    if hybrid:
+        proj_bytes = 2 * H * L * RANK * 2 + 2 * L * H * D * 2
+        line["config"]["workload"] = ("hybrid: " + WORKLOAD + " + Linformer branch rank 256 "
+                                      "(E_K, E_V [12][54600][256] bf16), equal-weight fusion")
+        line["linear_ms"] = round(per["linear"], 4)
+        line["linear_read_gbs"] = round(proj_bytes / (per["linear"] * 1e-3) / 1e9, 1)
+    if rank == 0 and world == 1 and not args.no_cpu_baseline and not hybrid:
         line["cpu_baseline"] = cpu_baseline_sample(c, lambda j: (kp[j], vp[j]))
     return line
 
@@ -287,6 +306,17 @@ def run_one_kernel(args, local):
         o = torch.empty(q.shape, dtype=torch.float32, device=dev)
         fn = lambda: wa.wa_block_attn(q, kb, vb, kl, vl, o)  # noqa: E731
         work, unit = attn_flops(NQ, KP * P + NLOC, D, H) / 1e12, "TFLOP/s"
+    elif args.kernel == "linear":
+        L, R = KP * P + NLOC, 256
+        q, kb, vb = g((NQ, H, D), "q"), g((KP * P, H, D), "kb"), g((KP * P, H, D), "vb")
+        kl, vl = g((NLOC, H, D), "kl"), g((NLOC, H, D), "vl")
+        ek = synth.normal((H, L, R), synth.seed_of("one_kernel", "ek"), dev, torch.bfloat16,
+                          std=L ** -0.5)
+        ev = synth.normal((H, L, R), synth.seed_of("one_kernel", "ev"), dev, torch.bfloat16,
+                          std=L ** -0.5)
+        o = torch.zeros((NQ, H, D), dtype=torch.float32, device=dev)
+        fn = lambda: wa.wa_linear_branch(q, kb, vb, kl, vl, ek, ev, o)  # noqa: E731
+        work, unit = (2 * H * L * R * 2 + 2 * L * H * D * 2) / 1e9, "GB/s (E + K,V read)"
     else:
         kp, vp = g((12, P, H, D), "kp"), g((12, P, H, D), "vp")
         idx = torch.tensor([9, 2, 5, 11], dtype=torch.int32, device=dev)
@@ -307,6 +337,129 @@ def run_one_kernel(args, local):
     ms = e0.elapsed_time(e1) / args.steps
     return {"kernel": args.kernel, "ms": round(ms, 4), "value": round(work / (ms * 1e-3), 1),
             "unit": unit, "steps": args.steps, "warmup": args.warmup}
+
+
+def run_denoise(args, world, rank, local):
+    """Block-diffusion denoising reuse: a cached 21-frame (32,760-token) KV
+    window per layer, re-attended by a 3-frame query block for 4 denoising
+    steps, each with fresh queries and fresh local K/V.  One bench step = the
+    4 denoising steps of one block."""
+    import torch
+
+    import sparse_kv_cache_page_gb300 as wa
+    from sparse_kv_cache_page_gb300 import synth
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    wa.load()
+    WIN, T = 21 * 1560, 4
+    g = lambda shape, t: synth.normal(shape, synth.seed_of("denoise", rank, t), dev,  # noqa: E731
+                                      torch.bfloat16)
+    kw, vw = g((WIN, H, D), "kw"), g((WIN, H, D), "vw")
+    qs = [g((NQ, H, D), ("q", t)) for t in range(T)]
+    kls = [g((NLOC, H, D), ("kl", t)) for t in range(T)]
+    vls = [g((NLOC, H, D), ("vl", t)) for t in range(T)]
+    o = torch.empty((NQ, H, D), dtype=torch.float32, device=dev)
+
+    def step():
+        for t in range(T):
+            wa.wa_block_attn(qs[t], kw, vw, kls[t], vls[t], o)
+
+    for _ in range(args.warmup):
+        step()
+    wa.wa_check()
+    barrier(world)
+    torch.cuda.synchronize()
+    with Clocks(local) as clk:
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(args.steps):
+            step()
+        e1.record()
+        torch.cuda.synchronize()
+    wa.wa_check()
+    ms = max_over_ranks(e0.elapsed_time(e1), world) / args.steps
+    flops = T * attn_flops(NQ, WIN + NLOC, D, H)
+    return {"metric": METRIC, "value": round(world * flops / (ms * 1e-3) / 1e12, 2),
+            "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(ms, 4), "ms_per_denoising_step": round(ms / T, 4),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic",
+            "config": {"workload": "denoise: 21-frame window (32,760 tokens) reused for 4 "
+                                   "denoising steps, 3-frame query block (4,680) + fresh local "
+                                   "KV, H=12 d=128 bf16", "l2": "window 201 MB per tensor > L2"},
+            "gpu_launches": T * args.steps, "clocks": clk.summary()}
+
+
+def run_stress(args, world, rank, local):
+    """Minute-long stress: layers run one after another; each layer's 120
+    cached pages (K and V, 9.2 GB) live in pinned host memory -- one page store
+    shared by all layers, each layer with its own queries and local KV.  Per
+    layer: top-4 of 120 pages, the 4 pages copied host -> device by the copy
+    engine on a side stream into one of two buffers, attention on the main
+    stream.  Retrieval for all layers runs first (the synthetic queries exist up
+    front), so layer l+1's copy overlaps layer l's attention."""
+    import torch
+
+    import sparse_kv_cache_page_gb300 as wa
+    from sparse_kv_cache_page_gb300 import synth
+    from sparse_kv_cache_page_gb300.tiered import TieredPipeline, TierLayer
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    wa.load()
+    NPG, NL = 120, args.layers
+    g = lambda shape, t: synth.normal(shape, synth.seed_of("stress", rank, t), dev,  # noqa: E731
+                                      torch.bfloat16)
+    hk = torch.empty((NPG, P, H, D), dtype=torch.bfloat16, pin_memory=True)
+    hv = torch.empty((NPG, P, H, D), dtype=torch.bfloat16, pin_memory=True)
+    kbar = torch.empty((NPG, H, D), dtype=torch.float32, device=dev)
+    for j in range(NPG):
+        kj, vj = g((1, P, H, D), ("k", j)), g((1, P, H, D), ("v", j))
+        wa.wa_page_summarize(kj, kbar[j:j + 1])
+        hk[j].copy_(kj[0])
+        hv[j].copy_(vj[0])
+    o = torch.empty((NQ, H, D), dtype=torch.float32, device=dev)
+    layers = [TierLayer(g((NQ, H, D), ("q", l)), g((NLOC, H, D), ("kl", l)),
+                        g((NLOC, H, D), ("vl", l)), kbar, hk, hv, o) for l in range(NL)]
+    pipe = TieredPipeline(KP, P, H, D, device=dev)
+    torch.cuda.synchronize()
+
+    def timed(mode, reps):
+        pipe.run(layers, mode)
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(reps):
+            pipe.run(layers, mode)
+        e1.record()
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / reps
+
+    for _ in range(max(1, args.warmup - 1)):
+        pipe.run(layers)
+    wa.wa_check()
+    reps = max(1, args.steps // 10)
+    with Clocks(local) as clk:
+        t_pipe = timed("pipeline", reps)
+    t_serial = timed("serial", 1)
+    t_copy = timed("copy", 1)
+    t_attn = timed("attn", 1)
+    wa.wa_check()
+    flops = NL * attn_flops(NQ, KP * P + NLOC, D, H)
+    h2d = NL * 2 * KP * P * H * D * 2
+    hidden = max(0.0, min(1.0, (t_copy + t_attn - t_pipe) / t_copy)) if t_copy > 0 else None
+    return {"metric": METRIC, "value": round(world * flops / (t_pipe * 1e-3) / 1e12, 2),
+            "unit": "TFLOP/s", "n_gpus": world, "steps": reps, "warmup": args.warmup,
+            "ms_per_step": round(t_pipe, 3), "ms_per_layer": round(t_pipe / NL, 4),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic",
+            "config": {"workload": f"stress: {NL} layers, 120 pages/layer in pinned host memory "
+                                   "(one 9.2 GB store shared by the layers), top-4 of 120, H=12 "
+                                   "d=128 bf16, 4,680 queries + 4,680 local per layer"},
+            "serial_ms": round(t_serial, 3), "copy_only_ms": round(t_copy, 3),
+            "attn_only_ms": round(t_attn, 3), "h2d_gbs": round(h2d / (t_copy * 1e-3) / 1e9, 1),
+            "copy_hidden_frac": hidden, "gpu_launches": NL * 2, "clocks": clk.summary()}
 
 
 # ----------------------------------------------------------------------------
@@ -394,12 +547,18 @@ def run_reference(args, world, rank):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--kernel", default="all", choices=["all", "attention", "gather"],
+    ap.add_argument("--kernel", default="all", choices=["all", "attention", "gather", "linear"],
                     help="time one kernel alone on its own inputs (for profiling)")
+    ap.add_argument("--workload", default="worldattention",
+                    choices=["worldattention", "denoise", "hybrid", "stress"],
+                    help="worldattention: the headline one-layer chunk; denoise: 4 denoising "
+                         "steps over a cached 21-frame window; hybrid: + Linformer branch; "
+                         "stress: 30 layers with pages in pinned host memory")
+    ap.add_argument("--layers", type=int, default=30, help="stress workload: layers")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)
     world, rank, local = dist_init(args)
@@ -407,6 +566,12 @@ def main():
         line = run_reference(args, world, rank)
     elif args.kernel != "all":
         line = run_one_kernel(args, local)
+    elif args.workload == "denoise":
+        line = run_denoise(args, world, rank, local)
+    elif args.workload == "hybrid":
+        line = run_gpu(args, world, rank, local, hybrid=True)
+    elif args.workload == "stress":
+        line = run_stress(args, world, rank, local)
     else:
         line = run_gpu(args, world, rank, local)
     if rank == 0 and line is not None:

@@ -1,0 +1,84 @@
+"""Layer pipeline over the DRAM tier of the page cache.
+
+WorldAttention (review page), HKV section, tiers L1/L2 (Fig. 2): GPU HBM holds
+only the retrieved pages plus the prompt and page indices, while the pages of
+chunks not in use live in CPU DRAM.  Inferix (summary page), KV Cache Manager:
+offloading to main memory, with selected blocks loaded back before attention.
+
+Here each layer's page bodies sit in pinned host memory and its page
+summaries in HBM.  For a run of layers: retrieval for every layer on the main
+stream, one device->host copy of all page indices, then per layer a
+copy-engine fetch of the K_p selected pages (wa_gather_pages from pinned host
+memory) on a side stream into one of two device buffers, and attention on the
+main stream once that layer's copy has landed.  The fetch of layer l+1 thus
+overlaps the attention of layer l; a buffer is refilled only after the
+attention that read it two layers earlier has finished.
+
+Every step runs in libwa; this module only orders calls on streams.
+"""
+
+from __future__ import annotations
+
+from dataclasses import dataclass
+
+import torch
+
+from . import wa_block_attn, wa_gather_pages, wa_select_pages
+
+
+@dataclass
+class TierLayer:
+    q: torch.Tensor            # [n_q][H][d] device
+    k_loc: torch.Tensor        # [n_loc][H][d] device
+    v_loc: torch.Tensor
+    kbar: torch.Tensor         # [n_pages][H][d] fp32 device (summaries of the host pages)
+    k_host: torch.Tensor       # [n_pages][P][H][d] pinned host
+    v_host: torch.Tensor
+    out: torch.Tensor          # [n_q][H][d] device, fp32 or the input dtype
+
+
+class TieredPipeline:
+    """Double-buffered host->device page fetch overlapped with attention."""
+
+    def __init__(self, k_p: int, page_tokens: int, n_heads: int, head_dim: int,
+                 dtype=torch.bfloat16, device="cuda"):
+        self.k_p = k_p
+        shape = (k_p * page_tokens, n_heads, head_dim)
+        self.bufs = [(torch.empty(shape, dtype=dtype, device=device),
+                      torch.empty(shape, dtype=dtype, device=device)) for _ in range(2)]
+        self.side = torch.cuda.Stream(device=device)
+        self.device = device
+
+    def run(self, layers, mode: str = "pipeline"):
+        """Run all layers.  mode: "pipeline" (copies overlap attention),
+        "serial" (each layer's copy, then its attention, on one stream),
+        "copy" / "attn" (one half only, for timing).  Returns the host page
+        indices [n_layers][k_p] (int32, pinned)."""
+        main = torch.cuda.current_stream(self.device)
+        n = len(layers)
+        idx = torch.empty((n, self.k_p), dtype=torch.int32, device=self.device)
+        idx_h = torch.empty((n, self.k_p), dtype=torch.int32, pin_memory=True)
+        for l, ly in enumerate(layers):
+            wa_select_pages(ly.q, ly.kbar, None, None, 1, self.k_p, idx[l])
+        idx_h.copy_(idx, non_blocking=True)
+        main.synchronize()                         # indices reach the host once
+        ev_copy = [torch.cuda.Event() for _ in range(n)]
+        ev_attn = [torch.cuda.Event() for _ in range(n)]
+        for l, ly in enumerate(layers):
+            kb, vb = self.bufs[l % 2]
+            if mode == "serial":
+                wa_gather_pages(ly.k_host, ly.v_host, None, idx_h[l], kb, vb)
+            elif mode != "attn":
+                with torch.cuda.stream(self.side):
+                    if l >= 2:
+                        self.side.wait_event(ev_attn[l - 2])
+                    wa_gather_pages(ly.k_host, ly.v_host, None, idx_h[l], kb, vb,
+                                    stream=self.side)
+                    ev_copy[l].record(self.side)
+            if mode != "copy":
+                if mode == "pipeline":
+                    main.wait_event(ev_copy[l])
+                wa_block_attn(ly.q, kb, vb, ly.k_loc, ly.v_loc, ly.out)
+                ev_attn[l].record(main)
+        main.wait_stream(self.side)
+        return idx_h
