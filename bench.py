@@ -163,10 +163,10 @@ def run_gpu(args, world, rank, local, hybrid=False):
 
     names = ("summarize", "select", "gather", "attention") + (("linear",) if hybrid else ())
 
-    def step(ev=None):
+    def step(marks=None):
         def mark(i):
-            if ev is not None:
-                ev[i].record(stream)
+            if marks is not None:
+                marks[i].record(stream)
         mark(0)
         wa.wa_page_summarize(kp, kbar)
         mark(1)
@@ -443,6 +443,7 @@ def run_stress(args, world, rank, local):
     with Clocks(local) as clk:
         t_pipe = timed("pipeline", reps)
     t_serial = timed("serial", 1)
+    t_direct = timed("direct", reps)
     t_copy = timed("copy", 1)
     t_attn = timed("attn", 1)
     wa.wa_check()
@@ -457,7 +458,8 @@ def run_stress(args, world, rank, local):
             "config": {"workload": f"stress: {NL} layers, 120 pages/layer in pinned host memory "
                                    "(one 9.2 GB store shared by the layers), top-4 of 120, H=12 "
                                    "d=128 bf16, 4,680 queries + 4,680 local per layer"},
-            "serial_ms": round(t_serial, 3), "copy_only_ms": round(t_copy, 3),
+            "serial_ms": round(t_serial, 3), "direct_ms": round(t_direct, 3),
+            "copy_only_ms": round(t_copy, 3),
             "attn_only_ms": round(t_attn, 3), "h2d_gbs": round(h2d / (t_copy * 1e-3) / 1e9, 1),
             "copy_hidden_frac": hidden, "gpu_launches": NL * 2, "clocks": clk.summary()}
 

@@ -157,9 +157,15 @@ wa_status wa_select_pages_noalloc(const void* q, wa_dtype dt, int n_q, int n_hea
  * (device int32 [k_p]); an index outside [0, n_pages) makes that slot's rows
  * zero and is recorded in the status word (WA_ERR_INDEX from wa_check).
  * Source in pinned host memory (cudaHostAlloc / cudaHostRegister; the DRAM
- * tier of [WA] HKV and [IX] offload): one cudaMemcpyAsync per page and
- * tensor on `stream`; the page indices come from idx_host (host int32
- * [k_p]) and are checked on the host (WA_ERR_INDEX, nothing enqueued).
+ * tier of [WA] HKV and [IX] offload), two ways:
+ *   - idx_host given (host int32 [k_p]): one cudaMemcpyAsync per page and
+ *     tensor on `stream` (copy engine); indices are checked on the host
+ *     (WA_ERR_INDEX, nothing enqueued);
+ *   - idx_host NULL, idx_dev given: the copy kernel reads the pages through
+ *     their device mapping (the GPU's own loads over the CPU-GPU link), so
+ *     the indices never return to the host; bad indices as for a device
+ *     source.  The host memory must be mapped for the device (pinned memory
+ *     under unified addressing is); else WA_ERR_INVALID_ARG.
  * k_buf, v_buf : device [k_p*page_tokens][n_heads][head_dim] of `dt`.
  * v_pages/v_buf may be NULL together (keys only).
  */

@@ -174,7 +174,25 @@ wa_status wa_gather_pages(const void* k_pages, const void* v_pages, wa_dtype dt,
         return WA_ERR_INVALID_ARG;
       }
     }
-    if (!idx_host) return WA_ERR_INVALID_ARG;
+    if (!idx_host) {
+      // device indices: the copy kernel reads the pinned pages through their
+      // device mapping (GPU loads over the CPU-GPU link); no host round trip
+      if (!idx_dev) return WA_ERR_INVALID_ARG;
+      const void* kd = attr.devicePointer;
+      const void* vd = nullptr;
+      if (v_pages) {
+        cudaPointerAttributes av;
+        if (cudaPointerGetAttributes(&av, v_pages) != cudaSuccess) {
+          cudaGetLastError();
+          return WA_ERR_INVALID_ARG;
+        }
+        vd = av.devicePointer;
+        if (!vd) return WA_ERR_INVALID_ARG;
+      }
+      if (!kd) return WA_ERR_INVALID_ARG;
+      if (!aligned16(kd) || (vd && !aligned16(vd))) return WA_ERR_ALIGN;
+      return launch_gather_device(kd, vd, page_bytes, n_pages, idx_dev, k_p, k_buf, v_buf, s);
+    }
     for (int i = 0; i < k_p; ++i)
       if (idx_host[i] < 0 || idx_host[i] >= n_pages) return WA_ERR_INDEX;
     for (int i = 0; i < k_p; ++i) {

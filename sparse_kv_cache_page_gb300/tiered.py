@@ -50,16 +50,21 @@ class TieredPipeline:
         self.device = device
 
     def run(self, layers, mode: str = "pipeline"):
-        """Run all layers.  mode: "pipeline" (copies overlap attention),
-        "serial" (each layer's copy, then its attention, on one stream),
-        "copy" / "attn" (one half only, for timing).  Returns the host page
-        indices [n_layers][k_p] (int32, pinned)."""
+        """Run all layers.  mode: "pipeline" (copy-engine fetches on a side
+        stream overlap attention), "serial" (each layer's copy, then its
+        attention, on one stream), "direct" (the gather kernel reads the pinned
+        pages over the CPU-GPU link on the side stream, indices stay on the
+        device, no host round trip), "copy" / "attn" (one half only, for
+        timing).  Returns the page indices [n_layers][k_p] (int32; pinned host
+        memory, or device memory in "direct" mode)."""
         main = torch.cuda.current_stream(self.device)
         n = len(layers)
         idx = torch.empty((n, self.k_p), dtype=torch.int32, device=self.device)
-        idx_h = torch.empty((n, self.k_p), dtype=torch.int32, pin_memory=True)
         for l, ly in enumerate(layers):
             wa_select_pages(ly.q, ly.kbar, None, None, 1, self.k_p, idx[l])
+        if mode == "direct":
+            return self._run_direct(layers, idx, main)
+        idx_h = torch.empty((n, self.k_p), dtype=torch.int32, pin_memory=True)
         idx_h.copy_(idx, non_blocking=True)
         main.synchronize()                         # indices reach the host once
         ev_copy = [torch.cuda.Event() for _ in range(n)]
@@ -82,3 +87,21 @@ class TieredPipeline:
                 ev_attn[l].record(main)
         main.wait_stream(self.side)
         return idx_h
+
+    def _run_direct(self, layers, idx, main):
+        ev_sel = torch.cuda.Event()
+        ev_sel.record(main)
+        n = len(layers)
+        ev_copy = [torch.cuda.Event() for _ in range(n)]
+        ev_attn = [torch.cuda.Event() for _ in range(n)]
+        for l, ly in enumerate(layers):
+            kb, vb = self.bufs[l % 2]
+            with torch.cuda.stream(self.side):
+                self.side.wait_event(ev_sel if l < 2 else ev_attn[l - 2])
+                wa_gather_pages(ly.k_host, ly.v_host, idx[l], None, kb, vb, stream=self.side)
+                ev_copy[l].record(self.side)
+            main.wait_event(ev_copy[l])
+            wa_block_attn(ly.q, kb, vb, ly.k_loc, ly.v_loc, ly.out)
+            ev_attn[l].record(main)
+        main.wait_stream(self.side)
+        return idx

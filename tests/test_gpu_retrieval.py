@@ -217,3 +217,8 @@ def test_gather_host_pinned_tier():
     with pytest.raises(wa.WaError) as e:
         wa.wa_gather_pages(kp, vp, None, torch.tensor([0, 7, 1], dtype=torch.int32), kb, vb)
     assert e.value.status == 5
+    # device indices: the kernel reads the pinned pages over the CPU-GPU link
+    kb2, vb2 = torch.zeros_like(kb), torch.zeros_like(vb)
+    wa.wa_gather_pages(kp, vp, torch.tensor(idx, dtype=torch.int32, device=DEV), None, kb2, vb2)
+    wa.wa_check()
+    assert torch.equal(kb2, kb) and torch.equal(vb2, vb)

@@ -37,7 +37,7 @@ def test_denoising_reuse_of_a_21_frame_window():
     assert torch.equal(kw, kw0) and torch.equal(vw, vw0)
 
 
-@pytest.mark.parametrize("mode", ["pipeline", "serial"])
+@pytest.mark.parametrize("mode", ["pipeline", "serial", "direct"])
 def test_tiered_layer_pipeline(mode):
     """Three layers, 12 pages of 700 tokens each in pinned host memory, top-4
     per layer; the double-buffered side-stream fetch must give every layer the
@@ -64,6 +64,6 @@ def test_tiered_layer_pipeline(mode):
     torch.cuda.synchronize()
     wa.wa_check()
     for l in range(NL):
-        assert idx_h[l].tolist() == refs[l][0].tolist()
+        assert idx_h[l].cpu().tolist() == refs[l][0].tolist()
         assert {l, 5 + l} <= set(refs[l][0].tolist())
         assert_attn_close(layers[l].out, refs[l][1], torch.bfloat16, f"layer {l}")
