@@ -130,9 +130,10 @@ wa_status wa_select_pages(const void* q, wa_dtype dt, int n_q, int n_heads, int 
  *
  * Its scratch is a fixed 2 MiB array (plus a 48 KiB control block) compiled
  * into the library; every GPU that loads the library holds it until the
- * process exits.  Limit: min(304, max(1, n_q/32)) * n_heads * head_dim * 4
- * bytes of partial sums must fit in 2 MiB (e.g. n_heads*head_dim = 1536 fits
- * every n_q); larger requests return WA_ERR_SHAPE and enqueue nothing.
+ * process exits.  Limit: (S + ceil(S/16)) * n_heads * head_dim * 4 bytes of
+ * partial sums, S = min(304, max(1, n_q/32)), must fit in 2 MiB (e.g.
+ * n_heads*head_dim = 1536 fits every n_q); larger requests return
+ * WA_ERR_SHAPE and enqueue nothing.
  * The first call on a device looks up the array's device address with
  * cudaGetSymbolAddress; make that first call before any stream capture.
  * Every call shares the one array, which keeps the previous call's contents:

@@ -11,15 +11,18 @@
 // Design (one CTA = one head x two 128-row query tiles x one range of key
 // tiles; 12 warps in three warpgroups):
 //   warp 8      TMA producer: Q0/Q1 once, then K_j, V_j alternately into a
-//               4-stage ring of 32 KiB slots (two 64-column boxes each,
+//               5-stage ring of 32 KiB slots (two 64-column boxes each,
 //               128-byte swizzle, rows past a segment end read as zero).
-//   warp 9      TMEM owner (alloc 512 columns) and MMA issuer (one thread):
-//               S_i = Q_i K_j^T into TMEM (M=128, N=128, K=128, both operands
-//               K-major from shared memory), then O_i += P_i V_j with P_i read
-//               from TMEM (bf16, aliasing S_i) and V_j MN-major from shared
-//               memory.  S_i(j+1) is issued only after O_i += P_i(j) V_j has
-//               completed, because P_i lives in S_i's columns.
-//   warps 10-11 idle (the CTA is three whole warpgroups).
+//   warps 9, 10 one MMA issuer thread per query tile i (warp 9 also owns
+//               the 512 TMEM columns): S_i = Q_i K_j^T into TMEM (M=128,
+//               N=128, K=128, both operands K-major from shared memory), then
+//               O_i += P_i V_j with P_i read from TMEM (bf16, aliasing S_i) and
+//               V_j MN-major from shared memory, in two halves of 64 keys as
+//               the softmax publishes them.  S_i(j+1) is issued only after
+//               O_i += P_i(j) V_j has completed, because P_i lives in S_i's
+//               columns.  The two issuers run their chains independently; a
+//               ring slot is refilled once both have released it.
+//   warp 11     idle (the CTA is three whole warpgroups).
 //   warps 0-3   softmax of query tile 0 (one thread per row = TMEM lane);
 //   warps 4-7   softmax of query tile 1.  Each row keeps a running max m and
 //               a sum l of the bf16-rounded p (the values the P V product
@@ -48,12 +51,13 @@ using namespace ptx;
 constexpr int BM = 128;                  // query rows per tile
 constexpr int BN = 128;                  // keys per tile
 constexpr int HD = 128;                  // head dim
-constexpr int NS = 4;                    // ring slots
+constexpr int NS = 5;                    // ring slots
 constexpr int kHalfBytes = BN * 64 * 2;  // one 64-column box: 16 KiB
 constexpr int kTileBytes = 2 * kHalfBytes;
 constexpr int kThreads = 384;
 constexpr int kProducerWarp = 8;
-constexpr int kMmaWarp = 9;
+constexpr int kMmaWarp = 9;              // MMA issuer of query tile 0, TMEM owner
+constexpr int kMmaWarp1 = 10;            // MMA issuer of query tile 1
 constexpr int kMaxUnits = 8192;          // split attention: one ticket per (head, query pair)
 
 __device__ __forceinline__ uint32_t col_s(int i) { return 128u * i; }          // S_i / P_i
@@ -75,7 +79,7 @@ struct Bars {
   uint64_t kv_full[NS];
   uint64_t kv_empty[NS];
   uint64_t s_full[2];
-  uint64_t p_ready[2];
+  uint64_t p_ready[2][2];   // [query tile][key half]
   uint64_t o_ready[2];
   uint64_t drain;
   uint32_t tmem_base;
@@ -176,14 +180,15 @@ k_block_attn_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     mbar_init(&bars->q_full, 1);
     for (int s = 0; s < NS; ++s) {
       mbar_init(&bars->kv_full[s], 1);
-      mbar_init(&bars->kv_empty[s], 1);
+      mbar_init(&bars->kv_empty[s], 2);   // one release per MMA issuer
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&bars->s_full[i], 1);
-      mbar_init(&bars->p_ready[i], 128);
+      mbar_init(&bars->p_ready[i][0], 128);
+      mbar_init(&bars->p_ready[i][1], 128);
       mbar_init(&bars->o_ready[i], 1);
     }
-    mbar_init(&bars->drain, 1);
+    mbar_init(&bars->drain, 2);
     bars->abort_flag = 0;
     fence_mbar_init();
   }
@@ -239,9 +244,10 @@ k_block_attn_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         }
       }
       __syncwarp();   // lanes 1-31 wait here for lane 0: the warp reaches the CTA barrier converged
-    } else if (warp == kMmaWarp) {
+    } else if (warp == kMmaWarp || warp == kMmaWarp1) {
       if (lane == 0) {
-        const uint32_t q_base = smem_u32(smem + SmemLayout::q);
+        const int i = warp - kMmaWarp;   // query tile of this issuer
+        const uint32_t qb = smem_u32(smem + SmemLayout::q) + i * kTileBytes;
         const uint32_t ring_base = smem_u32(smem + SmemLayout::ring);
         bool ok = mbar_wait(&bars->q_full, 0, abort_flag, p.status);
         tc_fence_after();
@@ -249,41 +255,35 @@ k_block_attn_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
           const int tk = 2 * jj, tv = 2 * jj + 1;
           const int sk = tk % NS, sv = tv % NS;
           if (!(ok = mbar_wait(&bars->kv_full[sk], (tk / NS) & 1, abort_flag, p.status))) break;
+          if (jj > 0 && !(ok = mbar_wait(&bars->o_ready[i], (jj - 1) & 1, abort_flag, p.status)))
+            break;
           tc_fence_after();
           const uint32_t kb = ring_base + sk * kTileBytes;
-          for (int i = 0; i < 2; ++i) {
-            if (jj > 0) {
-              if (!(ok = mbar_wait(&bars->o_ready[i], (jj - 1) & 1, abort_flag, p.status))) break;
-              tc_fence_after();
-            }
-            const uint32_t qb = q_base + i * kTileBytes;
 #pragma unroll
-            for (int ks = 0; ks < HD / 16; ++ks) {
-              const uint32_t off = (ks >> 2) * kHalfBytes + (ks & 3) * 32;
-              mma_ss(tmem + col_s(i), sdesc(qb + off, 16, 1024, kSwizzle128B),
-                     sdesc(kb + off, 16, 1024, kSwizzle128B), kIdescQK, ks > 0);
-            }
-            mma_commit(&bars->s_full[i]);
+          for (int ks = 0; ks < HD / 16; ++ks) {
+            const uint32_t off = (ks >> 2) * kHalfBytes + (ks & 3) * 32;
+            mma_ss(tmem + col_s(i), sdesc(qb + off, 16, 1024, kSwizzle128B),
+                   sdesc(kb + off, 16, 1024, kSwizzle128B), kIdescQK, ks > 0);
           }
-          if (!ok) break;
+          mma_commit(&bars->s_full[i]);
           mma_commit(&bars->kv_empty[sk]);
           if (!(ok = mbar_wait(&bars->kv_full[sv], (tv / NS) & 1, abort_flag, p.status))) break;
-          tc_fence_after();
           const uint32_t vb = ring_base + sv * kTileBytes;
-          for (int i = 0; i < 2; ++i) {
-            if (!(ok = mbar_wait(&bars->p_ready[i], jj & 1, abort_flag, p.status))) break;
+          for (int h = 0; h < 2; ++h) {
+            if (!(ok = mbar_wait(&bars->p_ready[i][h], jj & 1, abort_flag, p.status))) break;
             tc_fence_after();
 #pragma unroll
-            for (int ks = 0; ks < BN / 16; ++ks) {
+            for (int kq = 0; kq < 4; ++kq) {
+              const int ks = 4 * h + kq;
               // B = V_j rows [16ks, 16ks+16): MN-major, 64-column boxes 16 KiB apart
               // (leading byte offset), 8-row groups 1 KiB apart (stride byte offset)
               mma_ts(tmem + col_o(i), tmem + col_s(i) + ks * 8,
                      sdesc(vb + ks * 16 * 128, kHalfBytes, 1024, kSwizzle128B), kIdescPV,
                      (jj > 0 || ks > 0) ? 1u : 0u);
             }
-            mma_commit(&bars->o_ready[i]);
           }
           if (!ok) break;
+          mma_commit(&bars->o_ready[i]);
           mma_commit(&bars->kv_empty[sv]);
         }
         // all issued MMAs complete before teardown
@@ -339,6 +339,8 @@ k_block_attn_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
       if (kLse) lx *= f;
       // p = 2^(s*sl2 - m*sl2) rounded to bf16 for the P V product; the row sum
       // adds the same rounded values, so numerator and denominator agree.
+      // Keys 0-63 are published first so that O += P V can start on them
+      // while keys 64-127 are exponentiated.
       const float nmsl2 = -m * sl2;
       float rs0 = 0.f, rs1 = 0.f, xs0 = 0.f, xs1 = 0.f;
 #pragma unroll
@@ -359,23 +361,24 @@ k_block_attn_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             if (kLse) fadd2_acc(xs0, xs1, p0, p1);
           }
         tmem_st32(s_addr + 32 * hf, pk);
+        if (hf == 0 && __any_sync(0xffffffffu, need)) {
+          // rows that moved to a new max rescale O before any P V of this tile
+#pragma unroll 1
+          for (int c = 0; c < 4; ++c) {
+            uint32_t orow[32];
+            tmem_ld32(o_addr + 32 * c, orow);
+            tmem_ld_wait();
+#pragma unroll
+            for (int e = 0; e < 32; ++e) orow[e] = __float_as_uint(__uint_as_float(orow[e]) * f);
+            tmem_st32(o_addr + 32 * c, orow);
+          }
+        }
+        tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive(&bars->p_ready[qt][hf]);
       }
       l += rs0 + rs1;
       if (kLse) lx += xs0 + xs1;
-      if (__any_sync(0xffffffffu, need)) {
-#pragma unroll 1
-        for (int c = 0; c < 4; ++c) {
-          uint32_t orow[32];
-          tmem_ld32(o_addr + 32 * c, orow);
-          tmem_ld_wait();
-#pragma unroll
-          for (int e = 0; e < 32; ++e) orow[e] = __float_as_uint(__uint_as_float(orow[e]) * f);
-          tmem_st32(o_addr + 32 * c, orow);
-        }
-      }
-      tmem_st_wait();
-      tc_fence_before();
-      mbar_arrive(&bars->p_ready[qt]);
     }
     if (ok)
       ok = __all_sync(0xffffffffu,

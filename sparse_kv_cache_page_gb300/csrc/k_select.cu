@@ -189,6 +189,40 @@ __device__ void bitonic_sort(unsigned long long* keys, int n2) {
   }
 }
 
+constexpr int kGroup = 16;   // partial sums reduced per group at the first level
+
+// out[c] = scale * sum_{p < n} rows[p][c] for c < row_elems (row_elems % 4 == 0),
+// p in increasing order; loads of 8 rows in flight per thread.
+__device__ void sum_rows4(const float* rows, int n, int row_elems, float* out, float scale) {
+  const int n4 = row_elems / 4;
+  for (int c = threadIdx.x; c < n4; c += blockDim.x) {
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    int p = 0;
+    for (; p + 8 <= n; p += 8) {
+      float4 v[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u)
+        v[u] = __ldcg(reinterpret_cast<const float4*>(rows + (size_t)(p + u) * row_elems) + c);
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        acc.x += v[u].x;
+        acc.y += v[u].y;
+        acc.z += v[u].z;
+        acc.w += v[u].w;
+      }
+    }
+    for (; p < n; ++p) {
+      const float4 v = __ldcg(reinterpret_cast<const float4*>(rows + (size_t)p * row_elems) + c);
+      acc.x += v.x;
+      acc.y += v.y;
+      acc.z += v.z;
+      acc.w += v.w;
+    }
+    reinterpret_cast<float4*>(out)[c] =
+        make_float4(acc.x * scale, acc.y * scale, acc.z * scale, acc.w * scale);
+  }
+}
+
 struct SelectArgs {
   int n_q, row_elems, nvec, R, splits, rows_per_split;
   float* partial;
@@ -215,7 +249,17 @@ k_select_pages(const T* __restrict__ q, SelectArgs a) {
   colsum_rows<T, VPT>(q, a.row_elems, a.nvec, a.R, r0, r1, smem);
   float* mine = a.partial + (size_t)s * a.row_elems;
   for (int c = threadIdx.x; c < a.row_elems; c += blockDim.x) mine[c] = smem[c];
-  if (!last_ticket(&a.ctrl->counters[kSelectCounter], (unsigned)a.splits)) return;
+  // two-level reduction of the partial sums, each level in a fixed order:
+  // the last CTA of each group of kGroup sums the group, the last group sum
+  // finishes the mean query (short serial chains at both levels)
+  const int g = s / kGroup;
+  const int n_groups = (a.splits + kGroup - 1) / kGroup;
+  const int g0 = g * kGroup, g1 = min(a.splits, g0 + kGroup);
+  if (!last_ticket(&a.ctrl->counters[kSelectCounter - 1 - g], (unsigned)(g1 - g0))) return;
+  float* gsum = a.partial + (size_t)(a.splits + g) * a.row_elems;
+  sum_rows4(a.partial + (size_t)g0 * a.row_elems, g1 - g0, a.row_elems, gsum, 1.0f);
+  if (threadIdx.x == 0) a.ctrl->counters[kSelectCounter - 1 - g] = 0u;
+  if (!last_ticket(&a.ctrl->counters[kSelectCounter], (unsigned)n_groups)) return;
 
   // phase B (one CTA).  smem: qbar[row_elems] | alpha[n2] | keys[n2]
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nwarps = blockDim.x >> 5;
@@ -223,12 +267,9 @@ k_select_pages(const T* __restrict__ q, SelectArgs a) {
   float* alpha = qbar + ((a.row_elems + 3) & ~3);
   unsigned long long* keys =
       reinterpret_cast<unsigned long long*>(alpha + ((a.n_cand_max2 + 3) & ~3));
-  const float inv_nq = 1.0f / (float)a.n_q;
-  for (int c = tid; c < a.row_elems; c += blockDim.x) {
-    float acc = 0.f;
-    for (int p = 0; p < a.splits; ++p) acc += __ldcg(a.partial + (size_t)p * a.row_elems + c);
-    qbar[c] = acc * inv_nq;
-  }
+  sum_rows4(a.partial + (size_t)a.splits * a.row_elems, n_groups, a.row_elems, qbar,
+            1.0f / (float)a.n_q);
+  __syncthreads();
 
   // stage 1: prompt top-1 chunk
   __shared__ float s_red[32];
@@ -380,7 +421,8 @@ wa_status select_t(const T* q, SelectArgs a, cudaStream_t st) {
   const int rps = (a.n_q + splits - 1) / splits;
   splits = (a.n_q + rps - 1) / rps;
   Scratch sc;
-  wa_status rc = get_scratch((size_t)splits * a.row_elems * sizeof(float), &sc);
+  const int n_groups = (splits + kGroup - 1) / kGroup;
+  wa_status rc = get_scratch((size_t)(splits + n_groups) * a.row_elems * sizeof(float), &sc);
   if (rc != WA_OK) return rc;
   int n_cand = a.n_chunks > 0 ? a.ppc : a.n_pages;
   int n2 = 1;
@@ -495,13 +537,16 @@ wa_status select_noalloc_t(const T* q, SelectArgs a, cudaStream_t st) {
   if (splits > 304) splits = 304;
   const int rps = (a.n_q + splits - 1) / splits;
   splits = (a.n_q + rps - 1) / rps;
-  if ((size_t)splits * a.row_elems * sizeof(float) > kNoAllocPartialBytes) return WA_ERR_SHAPE;
+  const int n_groups = (splits + kGroup - 1) / kGroup;
+  if ((size_t)(splits + n_groups) * a.row_elems * sizeof(float) > kNoAllocPartialBytes)
+    return WA_ERR_SHAPE;
   unsigned char* base = nullptr;
   wa_status rc = noalloc_scratch(&base);
   if (rc != WA_OK) return rc;
   Ctrl* ctrl = reinterpret_cast<Ctrl*>(base);
-  // the ticket counter must start at zero; the array keeps the last call's contents
-  if (cudaMemsetAsync(&ctrl->counters[kSelectCounter], 0, sizeof(unsigned), st) != cudaSuccess)
+  // the ticket counters must start at zero; the array keeps the last call's contents
+  if (cudaMemsetAsync(&ctrl->counters[kSelectCounter - n_groups], 0,
+                      (n_groups + 1) * sizeof(unsigned), st) != cudaSuccess)
     return WA_ERR_CUDA;
   int n_cand = a.n_chunks > 0 ? a.ppc : a.n_pages;
   int n2 = 1;
