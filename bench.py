@@ -35,6 +35,10 @@ WORKLOAD = "worldattention_1layer: H=12 d=128 bf16, 40 pages x 12480 tok, top-1 
 
 H, D, P, N_PAGES, PPC, N_CHUNKS, PDIM, KP, NQ, NLOC = 12, 128, 12480, 40, 8, 5, 4096, 4, 4680, 4680
 
+# DRAM bytes read + written per launch of the attention kernel, from one ncu capture of the
+# current kernel (profiles/attention_worldattention_1layer.md); None once the kernel changes.
+ATTN_TRAFFIC_BYTES = 413.9e6
+
 
 def attn_flops(n_q, n_kv, d, h):
     """Matmul FLOPs of softmax attention: 2*n_q*n_kv*d for Q K^T and again for P V."""
@@ -268,7 +272,8 @@ def run_gpu(args, world, rank, local, hybrid=False):
         "gather_gbs": round(gather_bytes / (per["gather"] * 1e-3) / 1e9, 1),
         "summarize_gbs": round(summ_bytes / (per["summarize"] * 1e-3) / 1e9, 1),
         "roofline": {"bound": "tensor", "achieved": round(attn_tflops, 1), "peak": tf_sus,
-                     "unit": "TFLOP/s", "frac": round(attn_tflops / tf_sus, 4), "traffic": None,
+                     "unit": "TFLOP/s", "frac": round(attn_tflops / tf_sus, 4),
+                     "traffic": ATTN_TRAFFIC_BYTES if not hybrid else None,
                      "kernel": "k_block_attn_tc", "peak_source": f"{src} bf16 sustained"},
         "e2e": {"value": round(world * flops / (e2e_ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
                 "ms_per_step": round(e2e_ms, 4), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
