@@ -8,20 +8,18 @@
 // 4 x 8 x 1,560 = 49,920 retrieved tokens held in HBM (tier L1), staged
 // through on-chip SRAM (tier L0) FlashAttention-style.
 //
-// Design (one CTA = one head x two 128-row query tiles x one range of key
+// Design (one CTA = one head x two 128-row query tiles x one range of 64-key
 // tiles; 12 warps in three warpgroups):
 //   warp 8      TMA producer: Q0/Q1 once, then K_j, V_j alternately into a
-//               5-stage ring of 32 KiB slots (two 64-column boxes each,
+//               10-slot ring of 16 KiB (two 64-column boxes of 64 rows each,
 //               128-byte swizzle, rows past a segment end read as zero).
-//   warps 9, 10 one MMA issuer thread per query tile i (warp 9 also owns
-//               the 512 TMEM columns): S_i = Q_i K_j^T into TMEM (M=128,
-//               N=128, K=128, both operands K-major from shared memory), then
-//               O_i += P_i V_j with P_i read from TMEM (bf16, aliasing S_i) and
-//               V_j MN-major from shared memory, in two halves of 64 keys as
-//               the softmax publishes them.  S_i(j+1) is issued only after
-//               O_i += P_i(j) V_j has completed, because P_i lives in S_i's
-//               columns.  The two issuers run their chains independently; a
-//               ring slot is refilled once both have released it.
+//   warps 9, 10 one MMA issuer thread per query tile i (warp 9 also owns the
+//               512 TMEM columns): S_i(j) = Q_i K_j^T into TMEM (M=128, N=64,
+//               K=128, both operands K-major from shared memory), and
+//               O_i += P_i(j) V_j with P_i read from TMEM (bf16) and V_j
+//               MN-major from shared memory (M=128, N=128, K=64).  S runs one
+//               key tile ahead of P V: S_i(j+1) is issued as soon as the
+//               softmax has read S_i(j) out of TMEM.
 //   warp 11     idle (the CTA is three whole warpgroups).
 //   warps 0-3   softmax of query tile 0 (one thread per row = TMEM lane);
 //   warps 4-7   softmax of query tile 1.  Each row keeps a running max m and
@@ -29,7 +27,9 @@
 //               uses); exponentials are taken against m, and O_i and l are
 //               rescaled only when a tile raises the max by more than 2^8
 //               (in exp2 units), so most tiles skip the O round trip.
-//   TMEM columns: S0 [0,128) S1 [128,256) O0 [256,384) O1 [384,512).
+//   TMEM columns of query tile i (base 256 i): S_i [0,64), P_i double-buffered
+//   [64,96) and [96,128), O_i [128,256).  P has its own columns, so no MMA
+//   waits for another to finish before overwriting its operands.
 //   Key tiles are split into n_split contiguous ranges so that the grid fills
 //   whole waves of the 152 SMs; each CTA of a split stores its unnormalised
 //   O, m and l to scratch, and the CTA that finishes last for its (head,
@@ -49,44 +49,49 @@ namespace {
 using namespace ptx;
 
 constexpr int BM = 128;                  // query rows per tile
-constexpr int BN = 128;                  // keys per tile
+constexpr int BN = 64;                   // keys per tile
 constexpr int HD = 128;                  // head dim
-constexpr int NS = 5;                    // ring slots
-constexpr int kHalfBytes = BN * 64 * 2;  // one 64-column box: 16 KiB
-constexpr int kTileBytes = 2 * kHalfBytes;
+constexpr int NS = 10;                   // ring slots (K and V tiles alternate)
+constexpr int kQHalf = BM * 64 * 2;      // Q box: 128 rows x 64 columns = 16 KiB
+constexpr int kQTile = 2 * kQHalf;
+constexpr int kKvHalf = BN * 64 * 2;     // K/V box: 64 rows x 64 columns = 8 KiB
+constexpr int kKvTile = 2 * kKvHalf;
 constexpr int kThreads = 384;
 constexpr int kProducerWarp = 8;
 constexpr int kMmaWarp = 9;              // MMA issuer of query tile 0, TMEM owner
 constexpr int kMmaWarp1 = 10;            // MMA issuer of query tile 1
 constexpr int kMaxUnits = 8192;          // split attention: one ticket per (head, query pair)
 
-__device__ __forceinline__ uint32_t col_s(int i) { return 128u * i; }          // S_i / P_i
-__device__ __forceinline__ uint32_t col_o(int i) { return 256u + 128u * i; }   // O_i
+__device__ __forceinline__ uint32_t col_s(int i) { return 256u * i; }                  // S_i
+__device__ __forceinline__ uint32_t col_p(int i, int b) { return 256u * i + 64u + 32u * b; }
+__device__ __forceinline__ uint32_t col_o(int i) { return 256u * i + 128u; }           // O_i
 
-constexpr uint32_t kIdescQK = idesc_bf16_f32(128, 128, 0, 0);   // A, B K-major
+constexpr uint32_t kIdescQK = idesc_bf16_f32(128, BN, 0, 0);    // A, B K-major
 constexpr uint32_t kIdescPV = idesc_bf16_f32(128, 128, 0, 1);   // A (TMEM) K-major, B MN-major
 
 struct SmemLayout {
   // all offsets from a 1024-byte aligned base
   static constexpr int q = 0;                          // 2 tiles x 32 KiB
-  static constexpr int ring = 2 * kTileBytes;          // NS x 32 KiB
-  static constexpr int bars = ring + NS * kTileBytes;  // mbarriers
-  static constexpr int total = bars + 256;
+  static constexpr int ring = 2 * kQTile;              // NS x 16 KiB
+  static constexpr int bars = ring + NS * kKvTile;     // mbarriers
+  static constexpr int total = bars + 512;
 };
 
 struct Bars {
   uint64_t q_full;
   uint64_t kv_full[NS];
   uint64_t kv_empty[NS];
-  uint64_t s_full[2];
-  uint64_t p_ready[2][2];   // [query tile][key half]
-  uint64_t o_ready[2];
+  uint64_t s_full[2];       // S_i(j) computed
+  uint64_t s_free[2];       // softmax has read S_i(j)
+  uint64_t p_ready[2][2];   // [query tile][P buffer]: P_i(j) written, j % 2 = buffer
+  uint64_t o_ready[2][2];   // [query tile][P buffer]: O_i += P_i(j) V_j done
   uint64_t drain;
   uint32_t tmem_base;
   int abort_flag;
   unsigned ticket;
 };
-static_assert(sizeof(Bars) <= 256, "barrier block too large");
+static_assert(sizeof(Bars) <= 512, "barrier block too large");
+static_assert(SmemLayout::total + 1024 <= 232448, "shared memory per CTA");
 
 struct Params {
   int n_q, n_heads, n_main, n_loc, nt_main, nt_loc;
@@ -184,9 +189,11 @@ k_block_attn_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&bars->s_full[i], 1);
-      mbar_init(&bars->p_ready[i][0], 128);
-      mbar_init(&bars->p_ready[i][1], 128);
-      mbar_init(&bars->o_ready[i], 1);
+      mbar_init(&bars->s_free[i], 128);
+      for (int b = 0; b < 2; ++b) {
+        mbar_init(&bars->p_ready[i][b], 128);
+        mbar_init(&bars->o_ready[i][b], 1);
+      }
     }
     mbar_init(&bars->drain, 2);
     bars->abort_flag = 0;
@@ -202,17 +209,16 @@ k_block_attn_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
   const uint32_t tmem = bars->tmem_base;
 
   if (warp >= 8) {
-    // ---------------- warpgroup 2: producer, MMA issuer, two idle warps
+    // ---------------- warpgroup 2: producer, two MMA issuers, one idle warp
     if (warp == kProducerWarp) {
       if (lane == 0) {
         prefetch_tmap(&tm_q);
         const int xq = head * HD;
-        mbar_arrive_expect_tx(&bars->q_full, 2 * kTileBytes);
+        mbar_arrive_expect_tx(&bars->q_full, 2 * kQTile);
         for (int i = 0; i < 2; ++i)
           for (int hf = 0; hf < 2; ++hf)
-            tma_load_2d(&tm_q, &bars->q_full,
-                        smem + SmemLayout::q + i * kTileBytes + hf * kHalfBytes, xq + hf * 64,
-                        q0 + i * BM);
+            tma_load_2d(&tm_q, &bars->q_full, smem + SmemLayout::q + i * kQTile + hf * kQHalf,
+                        xq + hf * 64, q0 + i * BM);
         int issued = 0;
         for (int t = 0; t < 2 * nloc; ++t) {
           const int slot = t % NS;
@@ -230,10 +236,10 @@ k_block_attn_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             map = is_v ? &tm_vl : &tm_kl;
             row = (j - p.nt_main) * BN;
           }
-          uint8_t* dst = smem + SmemLayout::ring + slot * kTileBytes;
-          mbar_arrive_expect_tx(&bars->kv_full[slot], kTileBytes);
+          uint8_t* dst = smem + SmemLayout::ring + slot * kKvTile;
+          mbar_arrive_expect_tx(&bars->kv_full[slot], kKvTile);
           tma_load_2d(map, &bars->kv_full[slot], dst, xq, row);
-          tma_load_2d(map, &bars->kv_full[slot], dst + kHalfBytes, xq + 64, row);
+          tma_load_2d(map, &bars->kv_full[slot], dst + kKvHalf, xq + 64, row);
           issued = t + 1;
         }
         if (*abort_flag) {
@@ -247,45 +253,49 @@ k_block_attn_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     } else if (warp == kMmaWarp || warp == kMmaWarp1) {
       if (lane == 0) {
         const int i = warp - kMmaWarp;   // query tile of this issuer
-        const uint32_t qb = smem_u32(smem + SmemLayout::q) + i * kTileBytes;
+        const uint32_t qb = smem_u32(smem + SmemLayout::q) + i * kQTile;
         const uint32_t ring_base = smem_u32(smem + SmemLayout::ring);
         bool ok = mbar_wait(&bars->q_full, 0, abort_flag, p.status);
         tc_fence_after();
+        // O_i += P_i(j) V_j, once P_i(j) is published
+        auto issue_pv = [&](int j) -> bool {
+          const int tv = 2 * j + 1, sv = tv % NS, b = j & 1;
+          if (!mbar_wait(&bars->kv_full[sv], (tv / NS) & 1, abort_flag, p.status)) return false;
+          if (!mbar_wait(&bars->p_ready[i][b], (j >> 1) & 1, abort_flag, p.status)) return false;
+          tc_fence_after();
+          const uint32_t vb = ring_base + sv * kKvTile;
+#pragma unroll
+          for (int ks = 0; ks < BN / 16; ++ks) {
+            // B = V_j rows [16ks, 16ks+16): MN-major, 64-column boxes 8 KiB apart
+            // (leading byte offset), 8-row groups 1 KiB apart (stride byte offset)
+            mma_ts(tmem + col_o(i), tmem + col_p(i, b) + ks * 8,
+                   sdesc(vb + ks * 16 * 128, kKvHalf, 1024, kSwizzle128B), kIdescPV,
+                   (j > 0 || ks > 0) ? 1u : 0u);
+          }
+          mma_commit(&bars->o_ready[i][b]);
+          mma_commit(&bars->kv_empty[sv]);
+          return true;
+        };
         for (int jj = 0; ok && jj < nloc; ++jj) {
-          const int tk = 2 * jj, tv = 2 * jj + 1;
-          const int sk = tk % NS, sv = tv % NS;
+          const int tk = 2 * jj, sk = tk % NS;
           if (!(ok = mbar_wait(&bars->kv_full[sk], (tk / NS) & 1, abort_flag, p.status))) break;
-          if (jj > 0 && !(ok = mbar_wait(&bars->o_ready[i], (jj - 1) & 1, abort_flag, p.status)))
+          // S_i(jj) overwrites S_i(jj-1): the softmax must have read it
+          if (jj > 0 && !(ok = mbar_wait(&bars->s_free[i], (jj - 1) & 1, abort_flag, p.status)))
             break;
           tc_fence_after();
-          const uint32_t kb = ring_base + sk * kTileBytes;
+          const uint32_t kb = ring_base + sk * kKvTile;
 #pragma unroll
           for (int ks = 0; ks < HD / 16; ++ks) {
-            const uint32_t off = (ks >> 2) * kHalfBytes + (ks & 3) * 32;
-            mma_ss(tmem + col_s(i), sdesc(qb + off, 16, 1024, kSwizzle128B),
-                   sdesc(kb + off, 16, 1024, kSwizzle128B), kIdescQK, ks > 0);
+            const uint32_t qoff = (ks >> 2) * kQHalf + (ks & 3) * 32;
+            const uint32_t koff = (ks >> 2) * kKvHalf + (ks & 3) * 32;
+            mma_ss(tmem + col_s(i), sdesc(qb + qoff, 16, 1024, kSwizzle128B),
+                   sdesc(kb + koff, 16, 1024, kSwizzle128B), kIdescQK, ks > 0);
           }
           mma_commit(&bars->s_full[i]);
           mma_commit(&bars->kv_empty[sk]);
-          if (!(ok = mbar_wait(&bars->kv_full[sv], (tv / NS) & 1, abort_flag, p.status))) break;
-          const uint32_t vb = ring_base + sv * kTileBytes;
-          for (int h = 0; h < 2; ++h) {
-            if (!(ok = mbar_wait(&bars->p_ready[i][h], jj & 1, abort_flag, p.status))) break;
-            tc_fence_after();
-#pragma unroll
-            for (int kq = 0; kq < 4; ++kq) {
-              const int ks = 4 * h + kq;
-              // B = V_j rows [16ks, 16ks+16): MN-major, 64-column boxes 16 KiB apart
-              // (leading byte offset), 8-row groups 1 KiB apart (stride byte offset)
-              mma_ts(tmem + col_o(i), tmem + col_s(i) + ks * 8,
-                     sdesc(vb + ks * 16 * 128, kHalfBytes, 1024, kSwizzle128B), kIdescPV,
-                     (jj > 0 || ks > 0) ? 1u : 0u);
-            }
-          }
-          if (!ok) break;
-          mma_commit(&bars->o_ready[i]);
-          mma_commit(&bars->kv_empty[sv]);
+          if (jj > 0 && !(ok = issue_pv(jj - 1))) break;
         }
+        if (ok && nloc > 0) ok = issue_pv(nloc - 1);
         // all issued MMAs complete before teardown
         mma_commit(&bars->drain);
         mbar_wait_drain(&bars->drain, 0, 1000000000ull);
@@ -308,30 +318,31 @@ k_block_attn_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
       ok = __all_sync(0xffffffffu, mbar_wait(&bars->s_full[qt], jj & 1, abort_flag, p.status));
       if (!ok) break;
       tc_fence_after();
-      uint32_t sr[4][32];
-#pragma unroll
-      for (int c = 0; c < 4; ++c) tmem_ld32(s_addr + 32 * c, sr[c]);
+      uint32_t sr[2][32];
+      tmem_ld32(s_addr, sr[0]);
+      tmem_ld32(s_addr + 32, sr[1]);
       tmem_ld_wait();
+      tc_fence_before();
+      mbar_arrive(&bars->s_free[qt]);            // S_i(jj+1) may now be computed
       const int valid = tile_valid(p, jb + jj);   // warp-uniform
       if (valid < BN) {
 #pragma unroll
-        for (int c = 0; c < 4; ++c)
+        for (int c = 0; c < 2; ++c)
 #pragma unroll
           for (int e = 0; e < 32; ++e)
             if (32 * c + e >= valid) sr[c][e] = __float_as_uint(-INFINITY);
       }
-      float mx[4];
+      float mx[2];
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
+      for (int c = 0; c < 2; ++c) {
         mx[c] = __uint_as_float(sr[c][0]);
 #pragma unroll
         for (int e = 1; e < 31; e += 2)
           mx[c] = fmax3(mx[c], __uint_as_float(sr[c][e]), __uint_as_float(sr[c][e + 1]));
         mx[c] = fmaxf(mx[c], __uint_as_float(sr[c][31]));
       }
-      const float tmax = fmax3(fmaxf(mx[0], mx[1]), mx[2], mx[3]);
-      // rows whose max rose by more than 2^8 (exp2 units) move to the new max;
-      // their O and l are rescaled below, once the S registers are free
+      const float tmax = fmaxf(mx[0], mx[1]);
+      // rows whose max rose by more than 2^8 (exp2 units) move to the new max
       const bool need = jj > 0 && (tmax - m) * sl2 > 8.0f;
       const float f = need ? ex2((m - tmax) * sl2) : 1.0f;
       if (jj == 0 || need) m = tmax;
@@ -339,50 +350,55 @@ k_block_attn_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
       if (kLse) lx *= f;
       // p = 2^(s*sl2 - m*sl2) rounded to bf16 for the P V product; the row sum
       // adds the same rounded values, so numerator and denominator agree.
-      // Keys 0-63 are published first so that O += P V can start on them
-      // while keys 64-127 are exponentiated.
       const float nmsl2 = -m * sl2;
       float rs0 = 0.f, rs1 = 0.f, xs0 = 0.f, xs1 = 0.f;
+      uint32_t pk[32];
 #pragma unroll
-      for (int hf = 0; hf < 2; ++hf) {
-        uint32_t pk[32];   // bf16 pairs for keys 64*hf .. 64*hf+63
+      for (int c = 0; c < 2; ++c)
 #pragma unroll
-        for (int c2 = 0; c2 < 2; ++c2)
-#pragma unroll
-          for (int e = 0; e < 32; e += 2) {
-            const int c = 2 * hf + c2;
-            float x0, x1;
-            ffma2(x0, x1, __uint_as_float(sr[c][e]), __uint_as_float(sr[c][e + 1]), sl2, sl2,
-                  nmsl2, nmsl2);
-            const float p0 = ex2(x0), p1 = ex2(x1);
-            const uint32_t w = pack_bf16x2(p0, p1);
-            pk[16 * c2 + (e >> 1)] = w;
-            fadd2_acc(rs0, rs1, __uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
-            if (kLse) fadd2_acc(xs0, xs1, p0, p1);
-          }
-        tmem_st32(s_addr + 32 * hf, pk);
-        if (hf == 0 && __any_sync(0xffffffffu, need)) {
-          // rows that moved to a new max rescale O before any P V of this tile
-#pragma unroll 1
-          for (int c = 0; c < 4; ++c) {
-            uint32_t orow[32];
-            tmem_ld32(o_addr + 32 * c, orow);
-            tmem_ld_wait();
-#pragma unroll
-            for (int e = 0; e < 32; ++e) orow[e] = __float_as_uint(__uint_as_float(orow[e]) * f);
-            tmem_st32(o_addr + 32 * c, orow);
-          }
+        for (int e = 0; e < 32; e += 2) {
+          float x0, x1;
+          ffma2(x0, x1, __uint_as_float(sr[c][e]), __uint_as_float(sr[c][e + 1]), sl2, sl2,
+                nmsl2, nmsl2);
+          const float p0 = ex2(x0), p1 = ex2(x1);
+          const uint32_t w = pack_bf16x2(p0, p1);
+          pk[16 * c + (e >> 1)] = w;
+          acc_bf16x2(rs0, rs1, w);
+          if (kLse) fadd2_acc(xs0, xs1, p0, p1);
         }
-        tmem_st_wait();
-        tc_fence_before();
-        mbar_arrive(&bars->p_ready[qt][hf]);
+      // P buffer b was last read by O += P(jj-2) V; a rescale needs O += P(jj-1) V
+      // done.  (Waits are on the per-buffer barrier, at most one phase behind.)
+      const int b = jj & 1;
+      if (jj >= 2)
+        ok = __all_sync(0xffffffffu, mbar_wait(&bars->o_ready[qt][b], ((jj >> 1) - 1) & 1,
+                                               abort_flag, p.status));
+      const bool any_need = __any_sync(0xffffffffu, need);
+      if (ok && any_need)
+        ok = __all_sync(0xffffffffu, mbar_wait(&bars->o_ready[qt][b ^ 1], ((jj - 1) >> 1) & 1,
+                                               abort_flag, p.status));
+      if (!ok) break;
+      tc_fence_after();
+      tmem_st32(lane_addr + col_p(qt, b), pk);
+      if (any_need) {
+#pragma unroll 1
+        for (int c = 0; c < 4; ++c) {
+          uint32_t orow[32];
+          tmem_ld32(o_addr + 32 * c, orow);
+          tmem_ld_wait();
+#pragma unroll
+          for (int e = 0; e < 32; ++e) orow[e] = __float_as_uint(__uint_as_float(orow[e]) * f);
+          tmem_st32(o_addr + 32 * c, orow);
+        }
       }
+      tmem_st_wait();
+      tc_fence_before();
+      mbar_arrive(&bars->p_ready[qt][b]);
       l += rs0 + rs1;
       if (kLse) lx += xs0 + xs1;
     }
     if (ok)
-      ok = __all_sync(0xffffffffu,
-                      mbar_wait(&bars->o_ready[qt], (nloc - 1) & 1, abort_flag, p.status));
+      ok = __all_sync(0xffffffffu, mbar_wait(&bars->o_ready[qt][(nloc - 1) & 1],
+                                             ((nloc - 1) >> 1) & 1, abort_flag, p.status));
     tc_fence_after();
     const int grow = q0 + qt * BM + row;
     const bool store = grow < p.n_q;

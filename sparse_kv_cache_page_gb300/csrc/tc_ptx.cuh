@@ -276,6 +276,17 @@ __device__ __forceinline__ void fadd2_acc(float& d0, float& d1, float a0, float 
       : "f"(a0), "f"(a1));
 }
 
+// (a0, a1) += (the two bf16 halves of w), each added exactly into fp32
+// (mixed-precision add: the bf16 operand is widened without rounding)
+__device__ __forceinline__ void acc_bf16x2(float& a0, float& a1, uint32_t w) {
+  asm("{\n\t.reg .b16 lo, hi;\n\t"
+      "mov.b32 {lo, hi}, %2;\n\t"
+      "add.rn.f32.bf16 %0, lo, %0;\n\t"
+      "add.rn.f32.bf16 %1, hi, %1;\n\t}"
+      : "+f"(a0), "+f"(a1)
+      : "r"(w));
+}
+
 __device__ __forceinline__ float fmax3(float a, float b, float c) {
   float r;
   asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
