@@ -31,8 +31,6 @@
 //   TMEM columns of query tile i (base 256 i): S_i [0,64), P_i double-buffered
 //   [64,96) and [96,128), O_i [128,256).  P has its own columns, so no MMA
 //   waits for another to finish before overwriting its operands.
-//   Each CTA walks its key range starting at an offset set by its query pair,
-//   which spreads the concurrent TMA reads of a head's CTAs over the range.
 //   Key tiles are split into n_split contiguous ranges so that the grid fills
 //   whole waves of the 152 SMs; each CTA of a split stores its unnormalised
 //   O, m and l to scratch, and the CTA that finishes last for its (head,
@@ -183,12 +181,6 @@ k_block_attn_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
   int jb, je;
   split_range(p.nt_main + p.nt_loc, p.n_split, split, jb, je);
   const int nloc = je - jb;                 // key tiles of this CTA (>= 1)
-  // CTAs of one head walk the same key tiles; each query pair starts at its own
-  // offset (and wraps), so that concurrent CTAs read different tiles instead of
-  // all hitting the same L2 lines at once.  Softmax attention is independent
-  // of the key order.
-  const int rot = (int)(((long long)qpair * nloc) / p.n_qpairs);
-  auto tile_of = [&](int jj) { int r = jj + rot; return jb + (r >= nloc ? r - nloc : r); };
   volatile int* abort_flag = &bars->abort_flag;
 
   if (threadIdx.x == 0) {
@@ -236,7 +228,7 @@ k_block_attn_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
           if (t >= NS &&
               !mbar_wait(&bars->kv_empty[slot], ((t / NS) - 1) & 1, abort_flag, p.status))
             break;
-          const int j = tile_of(t >> 1);
+          const int j = jb + (t >> 1);
           const bool is_v = t & 1;
           const CUtensorMap* map;
           int row;
@@ -347,7 +339,7 @@ k_block_attn_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
       tmem_ld_wait();
       tc_fence_before();
       mbar_arrive(&bars->s_free[qt]);            // S_i(jj+1) may now be computed
-      const int valid = tile_valid(p, tile_of(jj));   // warp-uniform
+      const int valid = tile_valid(p, jb + jj);   // warp-uniform
       if (valid < BN) {
 #pragma unroll
         for (int c = 0; c < 2; ++c)
