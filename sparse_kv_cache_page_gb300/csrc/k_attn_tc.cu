@@ -13,15 +13,16 @@
 //   warp 8      TMA producer: Q0/Q1 once, then K_j, V_j alternately into a
 //               10-slot ring of 16 KiB (two 64-column boxes of 64 rows each,
 //               128-byte swizzle, rows past a segment end read as zero).
-//   warp 9      S issuer (one thread; also owns the 512 TMEM columns):
-//               S_i(j) = Q_i K_j^T into TMEM (M=128, N=64, K=128, both
-//               operands K-major from shared memory) for both query tiles,
-//               as soon as K_j has landed and the softmax has read S_i(j-1).
-//   warps 10,11 P V issuers, one thread per query tile: O_i += P_i(j) V_j with
-//               P_i read from TMEM (bf16) and V_j MN-major from shared memory
+//   warps 9, 10 S issuers, one thread per query tile i (warp 9 also owns the
+//               512 TMEM columns): S_i(j) = Q_i K_j^T into TMEM (M=128, N=64,
+//               K=128, both operands K-major from shared memory) as soon as
+//               K_j has landed and the softmax has read S_i(j-1).
+//   warp 11     P V issuer (one thread, both tiles): O_i += P_i(j) V_j with P_i
+//               read from TMEM (bf16) and V_j MN-major from shared memory
 //               (M=128, N=128, K=64), as soon as P_i(j) is published.  The
-//               three issuers wait only on their own inputs, so S runs ahead
-//               of the softmax and P V never holds up the next S.
+//               issuers wait only on their own inputs, so S runs ahead of the
+//               softmax and P V never holds up the next S; two S issuers keep
+//               the tensor pipe fed while one of them is blocked issuing.
 //   warps 0-3   softmax of query tile 0 (one thread per row = TMEM lane);
 //   warps 4-7   softmax of query tile 1.  Each row keeps a running max m and
 //               a sum l of the bf16-rounded p (the values the P V product
@@ -59,8 +60,9 @@ constexpr int kKvHalf = BN * 64 * 2;     // K/V box: 64 rows x 64 columns = 8 Ki
 constexpr int kKvTile = 2 * kKvHalf;
 constexpr int kThreads = 384;
 constexpr int kProducerWarp = 8;
-constexpr int kMmaWarp = 9;              // S issuer, TMEM owner
-constexpr int kPvWarp0 = 10;             // P V issuer of query tile 0 (tile 1: warp 11)
+constexpr int kMmaWarp = 9;              // S issuer of query tile 0, TMEM owner
+constexpr int kMmaWarp1 = 10;            // S issuer of query tile 1
+constexpr int kPvWarp = 11;              // P V issuer of both query tiles
 constexpr int kMaxUnits = 8192;          // split attention: one ticket per (head, query pair)
 
 __device__ __forceinline__ uint32_t col_s(int i) { return 256u * i; }                  // S_i
@@ -187,8 +189,8 @@ k_block_attn_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     mbar_init(&bars->q_full, 1);
     for (int s = 0; s < NS; ++s) {
       mbar_init(&bars->kv_full[s], 1);
-      // even slots hold K (released by the S issuer), odd slots V (by both P V issuers)
-      mbar_init(&bars->kv_empty[s], (s & 1) ? 2 : 1);
+      // even slots hold K (released by both S issuers), odd slots V (by the P V issuer)
+      mbar_init(&bars->kv_empty[s], (s & 1) ? 1 : 2);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&bars->s_full[i], 1);
@@ -212,7 +214,7 @@ k_block_attn_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
   const uint32_t tmem = bars->tmem_base;
 
   if (warp >= 8) {
-    // ---------------- warpgroup 2: producer, S issuer, two P V issuers
+    // ---------------- warpgroup 2: producer, two S issuers, the P V issuer
     if (warp == kProducerWarp) {
       if (lane == 0) {
         prefetch_tmap(&tm_q);
@@ -253,34 +255,30 @@ k_block_attn_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         }
       }
       __syncwarp();   // lanes 1-31 wait here for lane 0: the warp reaches the CTA barrier converged
-    } else if (warp == kMmaWarp) {
+    } else if (warp == kMmaWarp || warp == kMmaWarp1) {
       if (lane == 0) {
-        // S issuer for both query tiles
-        const uint32_t q_base = smem_u32(smem + SmemLayout::q);
+        // S issuer of query tile i
+        const int i = warp - kMmaWarp;
+        const uint32_t qb = smem_u32(smem + SmemLayout::q) + i * kQTile;
         const uint32_t ring_base = smem_u32(smem + SmemLayout::ring);
         bool ok = mbar_wait(&bars->q_full, 0, abort_flag, p.status);
         tc_fence_after();
         for (int jj = 0; ok && jj < nloc; ++jj) {
           const int tk = 2 * jj, sk = tk % NS;
           if (!(ok = mbar_wait(&bars->kv_full[sk], (tk / NS) & 1, abort_flag, p.status))) break;
+          // S_i(jj) overwrites S_i(jj-1): the softmax must have read it
+          if (jj > 0 && !(ok = mbar_wait(&bars->s_free[i], (jj - 1) & 1, abort_flag, p.status)))
+            break;
+          tc_fence_after();
           const uint32_t kb = ring_base + sk * kKvTile;
-          for (int i = 0; i < 2; ++i) {
-            // S_i(jj) overwrites S_i(jj-1): the softmax must have read it
-            if (jj > 0 &&
-                !(ok = mbar_wait(&bars->s_free[i], (jj - 1) & 1, abort_flag, p.status)))
-              break;
-            tc_fence_after();
-            const uint32_t qb = q_base + i * kQTile;
 #pragma unroll
-            for (int ks = 0; ks < HD / 16; ++ks) {
-              const uint32_t qoff = (ks >> 2) * kQHalf + (ks & 3) * 32;
-              const uint32_t koff = (ks >> 2) * kKvHalf + (ks & 3) * 32;
-              mma_ss(tmem + col_s(i), sdesc(qb + qoff, 16, 1024, kSwizzle128B),
-                     sdesc(kb + koff, 16, 1024, kSwizzle128B), kIdescQK, ks > 0);
-            }
-            mma_commit(&bars->s_full[i]);
+          for (int ks = 0; ks < HD / 16; ++ks) {
+            const uint32_t qoff = (ks >> 2) * kQHalf + (ks & 3) * 32;
+            const uint32_t koff = (ks >> 2) * kKvHalf + (ks & 3) * 32;
+            mma_ss(tmem + col_s(i), sdesc(qb + qoff, 16, 1024, kSwizzle128B),
+                   sdesc(kb + koff, 16, 1024, kSwizzle128B), kIdescQK, ks > 0);
           }
-          if (!ok) break;
+          mma_commit(&bars->s_full[i]);
           mma_commit(&bars->kv_empty[sk]);
         }
         // all issued MMAs complete before teardown
@@ -290,26 +288,28 @@ k_block_attn_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
       __syncwarp();
     } else {
       if (lane == 0) {
-        // P V issuer of query tile i
-        const int i = warp - kPvWarp0;
+        // P V issuer of both query tiles
         const uint32_t ring_base = smem_u32(smem + SmemLayout::ring);
         bool ok = true;
         for (int jj = 0; ok && jj < nloc; ++jj) {
           const int tv = 2 * jj + 1, sv = tv % NS, b = jj & 1;
           if (!(ok = mbar_wait(&bars->kv_full[sv], (tv / NS) & 1, abort_flag, p.status))) break;
-          if (!(ok = mbar_wait(&bars->p_ready[i][b], (jj >> 1) & 1, abort_flag, p.status)))
-            break;
-          tc_fence_after();
           const uint32_t vb = ring_base + sv * kKvTile;
+          for (int i = 0; i < 2; ++i) {
+            if (!(ok = mbar_wait(&bars->p_ready[i][b], (jj >> 1) & 1, abort_flag, p.status)))
+              break;
+            tc_fence_after();
 #pragma unroll
-          for (int ks = 0; ks < BN / 16; ++ks) {
-            // B = V_j rows [16ks, 16ks+16): MN-major, 64-column boxes 8 KiB apart
-            // (leading byte offset), 8-row groups 1 KiB apart (stride byte offset)
-            mma_ts(tmem + col_o(i), tmem + col_p(i, b) + ks * 8,
-                   sdesc(vb + ks * 16 * 128, kKvHalf, 1024, kSwizzle128B), kIdescPV,
-                   (jj > 0 || ks > 0) ? 1u : 0u);
+            for (int ks = 0; ks < BN / 16; ++ks) {
+              // B = V_j rows [16ks, 16ks+16): MN-major, 64-column boxes 8 KiB apart
+              // (leading byte offset), 8-row groups 1 KiB apart (stride byte offset)
+              mma_ts(tmem + col_o(i), tmem + col_p(i, b) + ks * 8,
+                     sdesc(vb + ks * 16 * 128, kKvHalf, 1024, kSwizzle128B), kIdescPV,
+                     (jj > 0 || ks > 0) ? 1u : 0u);
+            }
+            mma_commit(&bars->o_ready[i][b]);
           }
-          mma_commit(&bars->o_ready[i][b]);
+          if (!ok) break;
           mma_commit(&bars->kv_empty[sv]);
         }
         mma_commit(&bars->drain);
