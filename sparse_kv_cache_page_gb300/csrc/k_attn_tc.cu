@@ -228,7 +228,7 @@ k_block_attn_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         for (int t = 0; t < 2 * nloc; ++t) {
           const int slot = t % NS;
           if (t >= NS &&
-              !mbar_wait(&bars->kv_empty[slot], ((t / NS) - 1) & 1, abort_flag, p.status))
+              !mbar_wait_sleep(&bars->kv_empty[slot], ((t / NS) - 1) & 1, abort_flag, p.status))
             break;
           const int j = jb + (t >> 1);
           const bool is_v = t & 1;
@@ -261,13 +261,13 @@ k_block_attn_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         const int i = warp - kMmaWarp;
         const uint32_t qb = smem_u32(smem + SmemLayout::q) + i * kQTile;
         const uint32_t ring_base = smem_u32(smem + SmemLayout::ring);
-        bool ok = mbar_wait(&bars->q_full, 0, abort_flag, p.status);
+        bool ok = mbar_wait_sleep(&bars->q_full, 0, abort_flag, p.status);
         tc_fence_after();
         for (int jj = 0; ok && jj < nloc; ++jj) {
           const int tk = 2 * jj, sk = tk % NS;
-          if (!(ok = mbar_wait(&bars->kv_full[sk], (tk / NS) & 1, abort_flag, p.status))) break;
+          if (!(ok = mbar_wait_sleep(&bars->kv_full[sk], (tk / NS) & 1, abort_flag, p.status))) break;
           // S_i(jj) overwrites S_i(jj-1): the softmax must have read it
-          if (jj > 0 && !(ok = mbar_wait(&bars->s_free[i], (jj - 1) & 1, abort_flag, p.status)))
+          if (jj > 0 && !(ok = mbar_wait_sleep(&bars->s_free[i], (jj - 1) & 1, abort_flag, p.status)))
             break;
           tc_fence_after();
           const uint32_t kb = ring_base + sk * kKvTile;
@@ -293,10 +293,10 @@ k_block_attn_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         bool ok = true;
         for (int jj = 0; ok && jj < nloc; ++jj) {
           const int tv = 2 * jj + 1, sv = tv % NS, b = jj & 1;
-          if (!(ok = mbar_wait(&bars->kv_full[sv], (tv / NS) & 1, abort_flag, p.status))) break;
+          if (!(ok = mbar_wait_sleep(&bars->kv_full[sv], (tv / NS) & 1, abort_flag, p.status))) break;
           const uint32_t vb = ring_base + sv * kKvTile;
           for (int i = 0; i < 2; ++i) {
-            if (!(ok = mbar_wait(&bars->p_ready[i][b], (jj >> 1) & 1, abort_flag, p.status)))
+            if (!(ok = mbar_wait_sleep(&bars->p_ready[i][b], (jj >> 1) & 1, abort_flag, p.status)))
               break;
             tc_fence_after();
 #pragma unroll
@@ -347,16 +347,17 @@ k_block_attn_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
           for (int e = 0; e < 32; ++e)
             if (32 * c + e >= valid) sr[c][e] = __float_as_uint(-INFINITY);
       }
-      float mx[2];
+      float mx[4];   // four independent chains over 16 keys each
 #pragma unroll
-      for (int c = 0; c < 2; ++c) {
-        mx[c] = __uint_as_float(sr[c][0]);
+      for (int c = 0; c < 4; ++c) {
+        const uint32_t* v = &sr[c >> 1][(c & 1) * 16];
+        mx[c] = fmax3(__uint_as_float(v[0]), __uint_as_float(v[1]), __uint_as_float(v[2]));
 #pragma unroll
-        for (int e = 1; e < 31; e += 2)
-          mx[c] = fmax3(mx[c], __uint_as_float(sr[c][e]), __uint_as_float(sr[c][e + 1]));
-        mx[c] = fmaxf(mx[c], __uint_as_float(sr[c][31]));
+        for (int e = 3; e < 15; e += 2)
+          mx[c] = fmax3(mx[c], __uint_as_float(v[e]), __uint_as_float(v[e + 1]));
+        mx[c] = fmaxf(mx[c], __uint_as_float(v[15]));
       }
-      const float tmax = fmaxf(mx[0], mx[1]);
+      const float tmax = fmax3(fmaxf(mx[0], mx[1]), mx[2], mx[3]);
       // rows whose max rose by more than 2^8 (exp2 units) move to the new max
       const bool need = jj > 0 && (tmax - m) * sl2 > 8.0f;
       const float f = need ? ex2((m - tmax) * sl2) : 1.0f;
@@ -366,7 +367,7 @@ k_block_attn_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
       // p = 2^(s*sl2 - m*sl2) rounded to bf16 for the P V product; the row sum
       // adds the same rounded values, so numerator and denominator agree.
       const float nmsl2 = -m * sl2;
-      float rs0 = 0.f, rs1 = 0.f, xs0 = 0.f, xs1 = 0.f;
+      float rs[4] = {0.f, 0.f, 0.f, 0.f}, xs[4] = {0.f, 0.f, 0.f, 0.f};
       uint32_t pk[32];
 #pragma unroll
       for (int c = 0; c < 2; ++c)
@@ -378,8 +379,9 @@ k_block_attn_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
           const float p0 = ex2(x0), p1 = ex2(x1);
           const uint32_t w = pack_bf16x2(p0, p1);
           pk[16 * c + (e >> 1)] = w;
-          acc_bf16x2(rs0, rs1, w);
-          if (kLse) fadd2_acc(xs0, xs1, p0, p1);
+          const int a = (e >> 1) & 1;   // alternate two pairs of sum chains
+          acc_bf16x2(rs[2 * a], rs[2 * a + 1], w);
+          if (kLse) fadd2_acc(xs[2 * a], xs[2 * a + 1], p0, p1);
         }
       // P buffer b was last read by O += P(jj-2) V; a rescale needs O += P(jj-1) V
       // done.  (Waits are on the per-buffer barrier, at most one phase behind.)
@@ -408,8 +410,8 @@ k_block_attn_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
       tmem_st_wait();
       tc_fence_before();
       mbar_arrive(&bars->p_ready[qt][b]);
-      l += rs0 + rs1;
-      if (kLse) lx += xs0 + xs1;
+      l += (rs[0] + rs[1]) + (rs[2] + rs[3]);
+      if (kLse) lx += (xs[0] + xs[1]) + (xs[2] + xs[3]);
     }
     if (ok)
       ok = __all_sync(0xffffffffu, mbar_wait(&bars->o_ready[qt][(nloc - 1) & 1],
