@@ -347,17 +347,16 @@ k_block_attn_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
           for (int e = 0; e < 32; ++e)
             if (32 * c + e >= valid) sr[c][e] = __float_as_uint(-INFINITY);
       }
-      float mx[4];   // four independent chains over 16 keys each
+      float mx[2];
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        const uint32_t* v = &sr[c >> 1][(c & 1) * 16];
-        mx[c] = fmax3(__uint_as_float(v[0]), __uint_as_float(v[1]), __uint_as_float(v[2]));
+      for (int c = 0; c < 2; ++c) {
+        mx[c] = __uint_as_float(sr[c][0]);
 #pragma unroll
-        for (int e = 3; e < 15; e += 2)
-          mx[c] = fmax3(mx[c], __uint_as_float(v[e]), __uint_as_float(v[e + 1]));
-        mx[c] = fmaxf(mx[c], __uint_as_float(v[15]));
+        for (int e = 1; e < 31; e += 2)
+          mx[c] = fmax3(mx[c], __uint_as_float(sr[c][e]), __uint_as_float(sr[c][e + 1]));
+        mx[c] = fmaxf(mx[c], __uint_as_float(sr[c][31]));
       }
-      const float tmax = fmax3(fmaxf(mx[0], mx[1]), mx[2], mx[3]);
+      const float tmax = fmaxf(mx[0], mx[1]);
       // rows whose max rose by more than 2^8 (exp2 units) move to the new max
       const bool need = jj > 0 && (tmax - m) * sl2 > 8.0f;
       const float f = need ? ex2((m - tmax) * sl2) : 1.0f;
@@ -367,7 +366,7 @@ k_block_attn_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
       // p = 2^(s*sl2 - m*sl2) rounded to bf16 for the P V product; the row sum
       // adds the same rounded values, so numerator and denominator agree.
       const float nmsl2 = -m * sl2;
-      float rs[4] = {0.f, 0.f, 0.f, 0.f}, xs[4] = {0.f, 0.f, 0.f, 0.f};
+      float rs0 = 0.f, rs1 = 0.f, xs0 = 0.f, xs1 = 0.f;
       uint32_t pk[32];
 #pragma unroll
       for (int c = 0; c < 2; ++c)
@@ -379,9 +378,8 @@ k_block_attn_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
           const float p0 = ex2(x0), p1 = ex2(x1);
           const uint32_t w = pack_bf16x2(p0, p1);
           pk[16 * c + (e >> 1)] = w;
-          const int a = (e >> 1) & 1;   // alternate two pairs of sum chains
-          acc_bf16x2(rs[2 * a], rs[2 * a + 1], w);
-          if (kLse) fadd2_acc(xs[2 * a], xs[2 * a + 1], p0, p1);
+          acc_bf16x2(rs0, rs1, w);
+          if (kLse) fadd2_acc(xs0, xs1, p0, p1);
         }
       // P buffer b was last read by O += P(jj-2) V; a rescale needs O += P(jj-1) V
       // done.  (Waits are on the per-buffer barrier, at most one phase behind.)
@@ -410,8 +408,8 @@ k_block_attn_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
       tmem_st_wait();
       tc_fence_before();
       mbar_arrive(&bars->p_ready[qt][b]);
-      l += (rs[0] + rs[1]) + (rs[2] + rs[3]);
-      if (kLse) lx += (xs[0] + xs[1]) + (xs[2] + xs[3]);
+      l += rs0 + rs1;
+      if (kLse) lx += xs0 + xs1;
     }
     if (ok)
       ok = __all_sync(0xffffffffu, mbar_wait(&bars->o_ready[qt][(nloc - 1) & 1],
