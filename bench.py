@@ -37,7 +37,7 @@ H, D, P, N_PAGES, PPC, N_CHUNKS, PDIM, KP, NQ, NLOC = 12, 128, 12480, 40, 8, 5, 
 
 # DRAM bytes read + written per launch of the attention kernel, from one ncu capture of the
 # current kernel (profiles/attention_worldattention_1layer.md); None once the kernel changes.
-ATTN_TRAFFIC_BYTES = 413.9e6
+ATTN_TRAFFIC_BYTES = 413.93e6
 
 
 def attn_flops(n_q, n_kv, d, h):
@@ -207,40 +207,64 @@ def run_gpu(args, world, rank, local, hybrid=False):
            for i, n in enumerate(names)}
 
     # end to end through the public API: per step, the chunk's inputs come from
-    # pinned host memory and the output goes back to pinned host memory
+    # pinned host memory and the output goes back to pinned host memory.  The
+    # copies run on a copy stream, double-buffered, so that step k+1's inputs
+    # travel while step k computes (every copy is inside the timed region).
     hq = q.cpu().pin_memory()
     hkl, hvl = kl.cpu().pin_memory(), vl.cpu().pin_memory()
     hpc = pcur.cpu().pin_memory()
-    ho = torch.empty(o.shape, dtype=o.dtype).pin_memory()
-    dq, dkl, dvl, dpc = torch.empty_like(q), torch.empty_like(kl), torch.empty_like(vl), torch.empty_like(pcur)
+    ho = [torch.empty(o.shape, dtype=o.dtype).pin_memory() for _ in range(2)]
+    dbuf = [(torch.empty_like(q), torch.empty_like(kl), torch.empty_like(vl), torch.empty_like(pcur),
+             torch.empty_like(o)) for _ in range(2)]
+    cs = torch.cuda.Stream()
 
-    def step_e2e():
-        dq.copy_(hq, non_blocking=True)
-        dkl.copy_(hkl, non_blocking=True)
-        dvl.copy_(hvl, non_blocking=True)
-        dpc.copy_(hpc, non_blocking=True)
-        wa.wa_page_summarize(kp, kbar)
-        wa.wa_select_pages(dq, kbar, dpc, pch, PPC, KP, idx)
-        wa.wa_gather_pages(kp, vp, idx, None, kbuf, vbuf)
-        wa.wa_block_attn(dq, kbuf, vbuf, dkl, dvl, o)
-        if hybrid:
-            wa.wa_linear_branch(dq, kbuf, vbuf, dkl, dvl, ek, ev, o)
-        ho.copy_(o, non_blocking=True)
+    def e2e_run(n):
+        ev_in = [torch.cuda.Event() for _ in range(n + 1)]
+        ev_done = [torch.cuda.Event() for _ in range(n)]
+        cs.wait_stream(stream)
 
-    for _ in range(max(1, args.warmup)):
-        step_e2e()
+        def h2d(k):
+            dq, dkl, dvl, dpc, _ = dbuf[k % 2]
+            with torch.cuda.stream(cs):
+                if k >= 2:
+                    cs.wait_event(ev_done[k - 2])        # buffer k%2 free again
+                dq.copy_(hq, non_blocking=True)
+                dkl.copy_(hkl, non_blocking=True)
+                dvl.copy_(hvl, non_blocking=True)
+                dpc.copy_(hpc, non_blocking=True)
+                ev_in[k].record(cs)
+
+        h2d(0)
+        for k in range(n):
+            if k + 1 < n:
+                h2d(k + 1)
+            dq, dkl, dvl, dpc, do = dbuf[k % 2]
+            stream.wait_event(ev_in[k])
+            wa.wa_page_summarize(kp, kbar)
+            wa.wa_select_pages(dq, kbar, dpc, pch, PPC, KP, idx)
+            wa.wa_gather_pages(kp, vp, idx, None, kbuf, vbuf)
+            wa.wa_block_attn(dq, kbuf, vbuf, dkl, dvl, do)
+            if hybrid:
+                wa.wa_linear_branch(dq, kbuf, vbuf, dkl, dvl, ek, ev, do)
+            ev_done[k].record(stream)
+            with torch.cuda.stream(cs):
+                cs.wait_event(ev_done[k])
+                ho[k % 2].copy_(do, non_blocking=True)
+        stream.wait_stream(cs)
+
+    e2e_run(max(2, args.warmup))
     torch.cuda.synchronize()
     barrier(world)
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
     e0.record(stream)
-    for _ in range(args.steps):
-        step_e2e()
+    e2e_run(args.steps)
     e1.record(stream)
     torch.cuda.synchronize()
     e2e_ms = max_over_ranks(e0.elapsed_time(e1), world) / args.steps
-    h2d = sum(t.numel() * t.element_size() for t in (hq, hkl, hvl, hpc))
-    d2h = ho.numel() * ho.element_size()
+    h2d_bytes = sum(t.numel() * t.element_size() for t in (hq, hkl, hvl, hpc))
+    d2h = ho[0].numel() * ho[0].element_size()
+    assert torch.equal(ho[(args.steps - 1) % 2], dbuf[(args.steps - 1) % 2][4].cpu())
 
     hbm, tf_burst, tf_sus, src = peaks()
     n_kv = KP * P + NLOC
@@ -276,7 +300,9 @@ def run_gpu(args, world, rank, local, hybrid=False):
                      "traffic": ATTN_TRAFFIC_BYTES if not hybrid else None,
                      "kernel": "k_block_attn_tc", "peak_source": f"{src} bf16 sustained"},
         "e2e": {"value": round(world * flops / (e2e_ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
-                "ms_per_step": round(e2e_ms, 4), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+                "ms_per_step": round(e2e_ms, 4), "h2d_bytes_per_step": h2d_bytes,
+                "d2h_bytes_per_step": d2h, "copies": "copy stream, double-buffered, overlapped "
+                                                       "with the previous step's kernels"},
         "gpu_launches": launches_per_step * args.steps,
         "clocks": clk.summary(),
     }
