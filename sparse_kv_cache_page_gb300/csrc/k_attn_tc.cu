@@ -8,30 +8,30 @@
 // 4 x 8 x 1,560 = 49,920 retrieved tokens held in HBM (tier L1), staged
 // through on-chip SRAM (tier L0) FlashAttention-style.
 //
-// Design (one CTA = one head x two 128-row query tiles x one range of 64-key
+// Design (one CTA = one head x two 128-row query tiles x one range of 128-key
 // tiles; 12 warps in three warpgroups):
 //   warp 8      TMA producer: Q0/Q1 once, then K_j, V_j alternately into a
-//               10-slot ring of 16 KiB (two 64-column boxes of 64 rows each,
+//               5-slot ring of 32 KiB (two 64-column boxes of 128 rows each,
 //               128-byte swizzle, rows past a segment end read as zero).
-//   warps 9, 10 S issuers, one thread per query tile i (warp 9 also owns the
-//               512 TMEM columns): S_i(j) = Q_i K_j^T into TMEM (M=128, N=64,
-//               K=128, both operands K-major from shared memory) as soon as
-//               K_j has landed and the softmax has read S_i(j-1).
-//   warp 11     P V issuer (one thread, both tiles): O_i += P_i(j) V_j with P_i
-//               read from TMEM (bf16) and V_j MN-major from shared memory
-//               (M=128, N=128, K=64), as soon as P_i(j) is published.  The
-//               issuers wait only on their own inputs, so S runs ahead of the
-//               softmax and P V never holds up the next S; two S issuers keep
-//               the tensor pipe fed while one of them is blocked issuing.
+//   warp 9      S issuer (one thread; also owns the 512 TMEM columns):
+//               S_0(j) = Q_0 K_j^T, then S_1(j) = Q_1 K_j^T, into the same
+//               128 TMEM columns (M=128, N=128, K=128, both operands K-major
+//               from shared memory), each as soon as the other tile's softmax
+//               has read the previous S out of those columns.
+//   warp 10     P V issuer (one thread, both tiles): O_i += P_i(j) V_j with
+//               P_i read from TMEM (bf16) and V_j MN-major from shared memory
+//               (M=128, N=128, K=128), as soon as P_i(j) is published.
 //   warps 0-3   softmax of query tile 0 (one thread per row = TMEM lane);
 //   warps 4-7   softmax of query tile 1.  Each row keeps a running max m and
 //               a sum l of the bf16-rounded p (the values the P V product
 //               uses); exponentials are taken against m, and O_i and l are
 //               rescaled only when a tile raises the max by more than 2^8
 //               (in exp2 units), so most tiles skip the O round trip.
-//   TMEM columns of query tile i (base 256 i): S_i [0,64), P_i double-buffered
-//   [64,96) and [96,128), O_i [128,256).  P has its own columns, so no MMA
-//   waits for another to finish before overwriting its operands.
+//   TMEM columns: S [0,128) (shared by the two tiles in turn), P_0 [128,192),
+//   P_1 [192,256), O_0 [256,384), O_1 [384,512).  N=128 key tiles halve the
+//   shared-memory reads of Q per key against 64-key tiles: an N=64 S MMA
+//   (4 KiB of Q + 2 KiB of K per 32 tensor cycles) outruns the 128 bytes per
+//   cycle that shared memory delivers, an N=128 one (8 KiB per 64) does not.
 //   Key tiles are split into n_split contiguous ranges so that the grid fills
 //   whole waves of the 152 SMs; each CTA of a split stores its unnormalised
 //   O, m and l to scratch, and the CTA that finishes last for its (head,
@@ -51,23 +51,22 @@ namespace {
 using namespace ptx;
 
 constexpr int BM = 128;                  // query rows per tile
-constexpr int BN = 64;                   // keys per tile
+constexpr int BN = 128;                  // keys per tile
 constexpr int HD = 128;                  // head dim
-constexpr int NS = 10;                   // ring slots (K and V tiles alternate)
+constexpr int NS = 5;                    // ring slots (K and V tiles alternate)
 constexpr int kQHalf = BM * 64 * 2;      // Q box: 128 rows x 64 columns = 16 KiB
 constexpr int kQTile = 2 * kQHalf;
-constexpr int kKvHalf = BN * 64 * 2;     // K/V box: 64 rows x 64 columns = 8 KiB
+constexpr int kKvHalf = BN * 64 * 2;     // K/V box: 128 rows x 64 columns = 16 KiB
 constexpr int kKvTile = 2 * kKvHalf;
 constexpr int kThreads = 384;
 constexpr int kProducerWarp = 8;
-constexpr int kMmaWarp = 9;              // S issuer of query tile 0, TMEM owner
-constexpr int kMmaWarp1 = 10;            // S issuer of query tile 1
-constexpr int kPvWarp = 11;              // P V issuer of both query tiles
+constexpr int kMmaWarp = 9;              // S issuer of both query tiles, TMEM owner
+constexpr int kPvWarp = 10;              // P V issuer of both query tiles
 constexpr int kMaxUnits = 8192;          // split attention: one ticket per (head, query pair)
 
-__device__ __forceinline__ uint32_t col_s(int i) { return 256u * i; }                  // S_i
-__device__ __forceinline__ uint32_t col_p(int i, int b) { return 256u * i + 64u + 32u * b; }
-__device__ __forceinline__ uint32_t col_o(int i) { return 256u * i + 128u; }           // O_i
+constexpr uint32_t kColS = 0;            // S, shared by the two query tiles in turn
+__device__ __forceinline__ uint32_t col_p(int i) { return 128u + 64u * i; }   // P_i (bf16 pairs)
+__device__ __forceinline__ uint32_t col_o(int i) { return 256u + 128u * i; }  // O_i
 
 constexpr uint32_t kIdescQK = idesc_bf16_f32(128, BN, 0, 0);    // A, B K-major
 constexpr uint32_t kIdescPV = idesc_bf16_f32(128, 128, 0, 1);   // A (TMEM) K-major, B MN-major
@@ -84,10 +83,10 @@ struct Bars {
   uint64_t q_full;
   uint64_t kv_full[NS];
   uint64_t kv_empty[NS];
-  uint64_t s_full[2];       // S_i(j) computed
-  uint64_t s_free[2];       // softmax has read S_i(j)
-  uint64_t p_ready[2][2];   // [query tile][P buffer]: P_i(j) written, j % 2 = buffer
-  uint64_t o_ready[2][2];   // [query tile][P buffer]: O_i += P_i(j) V_j done
+  uint64_t s_full[2];       // S_i(j) computed (in the shared S columns)
+  uint64_t s_free[2];       // softmax i has read S_i(j)
+  uint64_t p_ready[2];      // P_i(j) written
+  uint64_t o_ready[2];      // O_i += P_i(j) V_j done
   uint64_t drain;
   uint32_t tmem_base;
   int abort_flag;
@@ -95,7 +94,6 @@ struct Bars {
 };
 static_assert(sizeof(Bars) <= 512, "barrier block too large");
 static_assert(SmemLayout::total + 1024 <= 232448, "shared memory per CTA");
-static_assert(NS % 2 == 0, "slots alternate K and V");
 
 struct Params {
   int n_q, n_heads, n_main, n_loc, nt_main, nt_loc;
@@ -189,18 +187,15 @@ k_block_attn_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     mbar_init(&bars->q_full, 1);
     for (int s = 0; s < NS; ++s) {
       mbar_init(&bars->kv_full[s], 1);
-      // even slots hold K (released by both S issuers), odd slots V (by the P V issuer)
-      mbar_init(&bars->kv_empty[s], (s & 1) ? 1 : 2);
+      mbar_init(&bars->kv_empty[s], 1);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&bars->s_full[i], 1);
       mbar_init(&bars->s_free[i], 128);
-      for (int b = 0; b < 2; ++b) {
-        mbar_init(&bars->p_ready[i][b], 128);
-        mbar_init(&bars->o_ready[i][b], 1);
-      }
+      mbar_init(&bars->p_ready[i], 128);
+      mbar_init(&bars->o_ready[i], 1);
     }
-    mbar_init(&bars->drain, 3);
+    mbar_init(&bars->drain, 2);
     bars->abort_flag = 0;
     fence_mbar_init();
   }
@@ -255,30 +250,37 @@ k_block_attn_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         }
       }
       __syncwarp();   // lanes 1-31 wait here for lane 0: the warp reaches the CTA barrier converged
-    } else if (warp == kMmaWarp || warp == kMmaWarp1) {
+    } else if (warp == kMmaWarp) {
       if (lane == 0) {
-        // S issuer of query tile i
-        const int i = warp - kMmaWarp;
-        const uint32_t qb = smem_u32(smem + SmemLayout::q) + i * kQTile;
+        // S issuer of both query tiles: S_0(j), then S_1(j), into the same
+        // TMEM columns, each once the other tile's softmax has read the last S
+        const uint32_t q_base = smem_u32(smem + SmemLayout::q);
         const uint32_t ring_base = smem_u32(smem + SmemLayout::ring);
         bool ok = mbar_wait_sleep(&bars->q_full, 0, abort_flag, p.status);
         tc_fence_after();
         for (int jj = 0; ok && jj < nloc; ++jj) {
           const int tk = 2 * jj, sk = tk % NS;
           if (!(ok = mbar_wait_sleep(&bars->kv_full[sk], (tk / NS) & 1, abort_flag, p.status))) break;
-          // S_i(jj) overwrites S_i(jj-1): the softmax must have read it
-          if (jj > 0 && !(ok = mbar_wait_sleep(&bars->s_free[i], (jj - 1) & 1, abort_flag, p.status)))
-            break;
-          tc_fence_after();
           const uint32_t kb = ring_base + sk * kKvTile;
+          for (int i = 0; i < 2; ++i) {
+            // the S columns were last read by softmax 1 (tile jj-1) or softmax 0 (tile jj)
+            if (i == 0 && jj > 0 &&
+                !(ok = mbar_wait_sleep(&bars->s_free[1], (jj - 1) & 1, abort_flag, p.status)))
+              break;
+            if (i == 1 && !(ok = mbar_wait_sleep(&bars->s_free[0], jj & 1, abort_flag, p.status)))
+              break;
+            tc_fence_after();
+            const uint32_t qb = q_base + i * kQTile;
 #pragma unroll
-          for (int ks = 0; ks < HD / 16; ++ks) {
-            const uint32_t qoff = (ks >> 2) * kQHalf + (ks & 3) * 32;
-            const uint32_t koff = (ks >> 2) * kKvHalf + (ks & 3) * 32;
-            mma_ss(tmem + col_s(i), sdesc(qb + qoff, 16, 1024, kSwizzle128B),
-                   sdesc(kb + koff, 16, 1024, kSwizzle128B), kIdescQK, ks > 0);
+            for (int ks = 0; ks < HD / 16; ++ks) {
+              const uint32_t qoff = (ks >> 2) * kQHalf + (ks & 3) * 32;
+              const uint32_t koff = (ks >> 2) * kKvHalf + (ks & 3) * 32;
+              mma_ss(tmem + kColS, sdesc(qb + qoff, 16, 1024, kSwizzle128B),
+                     sdesc(kb + koff, 16, 1024, kSwizzle128B), kIdescQK, ks > 0);
+            }
+            mma_commit(&bars->s_full[i]);
           }
-          mma_commit(&bars->s_full[i]);
+          if (!ok) break;
           mma_commit(&bars->kv_empty[sk]);
         }
         // all issued MMAs complete before teardown
@@ -286,28 +288,28 @@ k_block_attn_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         mbar_wait_drain(&bars->drain, 0, 1000000000ull);
       }
       __syncwarp();
-    } else {
+    } else if (warp == kPvWarp) {
       if (lane == 0) {
         // P V issuer of both query tiles
         const uint32_t ring_base = smem_u32(smem + SmemLayout::ring);
         bool ok = true;
         for (int jj = 0; ok && jj < nloc; ++jj) {
-          const int tv = 2 * jj + 1, sv = tv % NS, b = jj & 1;
+          const int tv = 2 * jj + 1, sv = tv % NS;
           if (!(ok = mbar_wait_sleep(&bars->kv_full[sv], (tv / NS) & 1, abort_flag, p.status))) break;
           const uint32_t vb = ring_base + sv * kKvTile;
           for (int i = 0; i < 2; ++i) {
-            if (!(ok = mbar_wait_sleep(&bars->p_ready[i][b], (jj >> 1) & 1, abort_flag, p.status)))
+            if (!(ok = mbar_wait_sleep(&bars->p_ready[i], jj & 1, abort_flag, p.status)))
               break;
             tc_fence_after();
 #pragma unroll
             for (int ks = 0; ks < BN / 16; ++ks) {
               // B = V_j rows [16ks, 16ks+16): MN-major, 64-column boxes 8 KiB apart
               // (leading byte offset), 8-row groups 1 KiB apart (stride byte offset)
-              mma_ts(tmem + col_o(i), tmem + col_p(i, b) + ks * 8,
+              mma_ts(tmem + col_o(i), tmem + col_p(i) + ks * 8,
                      sdesc(vb + ks * 16 * 128, kKvHalf, 1024, kSwizzle128B), kIdescPV,
                      (jj > 0 || ks > 0) ? 1u : 0u);
             }
-            mma_commit(&bars->o_ready[i][b]);
+            mma_commit(&bars->o_ready[i]);
           }
           if (!ok) break;
           mma_commit(&bars->kv_empty[sv]);
@@ -322,7 +324,7 @@ k_block_attn_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     const int qt = warp >> 2;                       // query tile 0 or 1
     const int row = 32 * (warp & 3) + lane;         // TMEM lane = row of the tile
     const uint32_t lane_addr = tmem + ((uint32_t)(32 * (warp & 3)) << 16);
-    const uint32_t s_addr = lane_addr + col_s(qt);
+    const uint32_t s_addr = lane_addr + kColS;
     const uint32_t o_addr = lane_addr + col_o(qt);
     const float sl2 = p.scale_log2;
     float m = -INFINITY, l = 0.f, lx = 0.f;   // lx: exact (unrounded) sum, for the LSE
@@ -333,30 +335,30 @@ k_block_attn_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
       ok = __all_sync(0xffffffffu, mbar_wait(&bars->s_full[qt], jj & 1, abort_flag, p.status));
       if (!ok) break;
       tc_fence_after();
-      uint32_t sr[2][32];
-      tmem_ld32(s_addr, sr[0]);
-      tmem_ld32(s_addr + 32, sr[1]);
+      uint32_t sr[4][32];
+#pragma unroll
+      for (int c = 0; c < 4; ++c) tmem_ld32(s_addr + 32 * c, sr[c]);
       tmem_ld_wait();
       tc_fence_before();
-      mbar_arrive(&bars->s_free[qt]);            // S_i(jj+1) may now be computed
+      mbar_arrive(&bars->s_free[qt]);            // the other tile's S may now be computed
       const int valid = tile_valid(p, jb + jj);   // warp-uniform
       if (valid < BN) {
 #pragma unroll
-        for (int c = 0; c < 2; ++c)
+        for (int c = 0; c < 4; ++c)
 #pragma unroll
           for (int e = 0; e < 32; ++e)
             if (32 * c + e >= valid) sr[c][e] = __float_as_uint(-INFINITY);
       }
-      float mx[2];
+      float mx[4];
 #pragma unroll
-      for (int c = 0; c < 2; ++c) {
+      for (int c = 0; c < 4; ++c) {
         mx[c] = __uint_as_float(sr[c][0]);
 #pragma unroll
         for (int e = 1; e < 31; e += 2)
           mx[c] = fmax3(mx[c], __uint_as_float(sr[c][e]), __uint_as_float(sr[c][e + 1]));
         mx[c] = fmaxf(mx[c], __uint_as_float(sr[c][31]));
       }
-      const float tmax = fmaxf(mx[0], mx[1]);
+      const float tmax = fmax3(fmaxf(mx[0], mx[1]), mx[2], mx[3]);
       // rows whose max rose by more than 2^8 (exp2 units) move to the new max
       const bool need = jj > 0 && (tmax - m) * sl2 > 8.0f;
       const float f = need ? ex2((m - tmax) * sl2) : 1.0f;
@@ -367,9 +369,9 @@ k_block_attn_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
       // adds the same rounded values, so numerator and denominator agree.
       const float nmsl2 = -m * sl2;
       float rs0 = 0.f, rs1 = 0.f, xs0 = 0.f, xs1 = 0.f;
-      uint32_t pk[32];
+      uint32_t pk[2][32];
 #pragma unroll
-      for (int c = 0; c < 2; ++c)
+      for (int c = 0; c < 4; ++c)
 #pragma unroll
         for (int e = 0; e < 32; e += 2) {
           float x0, x1;
@@ -377,24 +379,20 @@ k_block_attn_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                 nmsl2, nmsl2);
           const float p0 = ex2(x0), p1 = ex2(x1);
           const uint32_t w = pack_bf16x2(p0, p1);
-          pk[16 * c + (e >> 1)] = w;
+          pk[c >> 1][16 * (c & 1) + (e >> 1)] = w;
           acc_bf16x2(rs0, rs1, w);
           if (kLse) fadd2_acc(xs0, xs1, p0, p1);
         }
-      // P buffer b was last read by O += P(jj-2) V; a rescale needs O += P(jj-1) V
-      // done.  (Waits are on the per-buffer barrier, at most one phase behind.)
-      const int b = jj & 1;
-      if (jj >= 2)
-        ok = __all_sync(0xffffffffu, mbar_wait(&bars->o_ready[qt][b], ((jj >> 1) - 1) & 1,
-                                               abort_flag, p.status));
-      const bool any_need = __any_sync(0xffffffffu, need);
-      if (ok && any_need)
-        ok = __all_sync(0xffffffffu, mbar_wait(&bars->o_ready[qt][b ^ 1], ((jj - 1) >> 1) & 1,
-                                               abort_flag, p.status));
+      // P_i was last read by O += P(jj-1) V, which must also be done before O
+      // is rescaled.  (The wait is at most one phase behind.)
+      if (jj >= 1)
+        ok = __all_sync(0xffffffffu, mbar_wait(&bars->o_ready[qt], (jj - 1) & 1, abort_flag,
+                                               p.status));
       if (!ok) break;
       tc_fence_after();
-      tmem_st32(lane_addr + col_p(qt, b), pk);
-      if (any_need) {
+      tmem_st32(lane_addr + col_p(qt), pk[0]);
+      tmem_st32(lane_addr + col_p(qt) + 32, pk[1]);
+      if (__any_sync(0xffffffffu, need)) {
 #pragma unroll 1
         for (int c = 0; c < 4; ++c) {
           uint32_t orow[32];
@@ -407,13 +405,13 @@ k_block_attn_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
       }
       tmem_st_wait();
       tc_fence_before();
-      mbar_arrive(&bars->p_ready[qt][b]);
+      mbar_arrive(&bars->p_ready[qt]);
       l += rs0 + rs1;
       if (kLse) lx += xs0 + xs1;
     }
     if (ok)
-      ok = __all_sync(0xffffffffu, mbar_wait(&bars->o_ready[qt][(nloc - 1) & 1],
-                                             ((nloc - 1) >> 1) & 1, abort_flag, p.status));
+      ok = __all_sync(0xffffffffu, mbar_wait(&bars->o_ready[qt], (nloc - 1) & 1, abort_flag,
+                                             p.status));
     tc_fence_after();
     const int grow = q0 + qt * BM + row;
     const bool store = grow < p.n_q;
