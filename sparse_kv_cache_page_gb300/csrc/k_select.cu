@@ -19,8 +19,8 @@
 namespace wa {
 namespace {
 
-constexpr int kThreads = 256;
-constexpr int kTargetCtas = 152 * 8;     // 8 resident 256-thread CTAs per SM
+constexpr int kThreads = 384;           // 2 x 192 16-byte vectors of a 1,536-element bf16 row
+constexpr int kTargetCtas = 152 * 5;     // 5 x 384 threads per SM
 constexpr unsigned kSelectCounter = 4095;
 
 template <typename T> struct VecOf;
@@ -124,6 +124,38 @@ __device__ bool last_ticket(unsigned* counter, unsigned n) {
   return last;
 }
 
+// out[c] = scale * sum_{p < n} rows[p][c] for c < row_elems (row_elems % 4 == 0),
+// p in increasing order; loads of 8 rows in flight per thread.
+__device__ void sum_rows4(const float* rows, int n, int row_elems, float* out, float scale) {
+  const int n4 = row_elems / 4;
+  for (int c = threadIdx.x; c < n4; c += blockDim.x) {
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    int p = 0;
+    for (; p + 8 <= n; p += 8) {
+      float4 v[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u)
+        v[u] = __ldcg(reinterpret_cast<const float4*>(rows + (size_t)(p + u) * row_elems) + c);
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        acc.x += v[u].x;
+        acc.y += v[u].y;
+        acc.z += v[u].z;
+        acc.w += v[u].w;
+      }
+    }
+    for (; p < n; ++p) {
+      const float4 v = __ldcg(reinterpret_cast<const float4*>(rows + (size_t)p * row_elems) + c);
+      acc.x += v.x;
+      acc.y += v.y;
+      acc.z += v.z;
+      acc.w += v.w;
+    }
+    reinterpret_cast<float4*>(out)[c] =
+        make_float4(acc.x * scale, acc.y * scale, acc.z * scale, acc.w * scale);
+  }
+}
+
 // ---------------------------------------------------------------------------
 // page summaries
 // ---------------------------------------------------------------------------
@@ -147,12 +179,9 @@ k_page_summarize(const T* __restrict__ pages, int page_tokens, int row_elems, in
   float* mine = partial + ((size_t)j * splits + s) * row_elems;
   for (int c = threadIdx.x; c < row_elems; c += blockDim.x) mine[c] = red[c];
   if (!last_ticket(&ctrl->counters[j], (unsigned)splits)) return;
-  const float* pj = partial + (size_t)j * splits * row_elems;
-  for (int c = threadIdx.x; c < row_elems; c += blockDim.x) {
-    float acc = 0.f;
-    for (int p = 0; p < splits; ++p) acc += __ldcg(pj + (size_t)p * row_elems + c);
-    kbar[(size_t)j * row_elems + c] = acc * inv;
-  }
+  // the page's partial sums in split order, then the mean
+  sum_rows4(partial + (size_t)j * splits * row_elems, splits, row_elems,
+            kbar + (size_t)j * row_elems, inv);
   if (threadIdx.x == 0) ctrl->counters[j] = 0u;
 }
 
@@ -190,38 +219,6 @@ __device__ void bitonic_sort(unsigned long long* keys, int n2) {
 }
 
 constexpr int kGroup = 16;   // partial sums reduced per group at the first level
-
-// out[c] = scale * sum_{p < n} rows[p][c] for c < row_elems (row_elems % 4 == 0),
-// p in increasing order; loads of 8 rows in flight per thread.
-__device__ void sum_rows4(const float* rows, int n, int row_elems, float* out, float scale) {
-  const int n4 = row_elems / 4;
-  for (int c = threadIdx.x; c < n4; c += blockDim.x) {
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    int p = 0;
-    for (; p + 8 <= n; p += 8) {
-      float4 v[8];
-#pragma unroll
-      for (int u = 0; u < 8; ++u)
-        v[u] = __ldcg(reinterpret_cast<const float4*>(rows + (size_t)(p + u) * row_elems) + c);
-#pragma unroll
-      for (int u = 0; u < 8; ++u) {
-        acc.x += v[u].x;
-        acc.y += v[u].y;
-        acc.z += v[u].z;
-        acc.w += v[u].w;
-      }
-    }
-    for (; p < n; ++p) {
-      const float4 v = __ldcg(reinterpret_cast<const float4*>(rows + (size_t)p * row_elems) + c);
-      acc.x += v.x;
-      acc.y += v.y;
-      acc.z += v.z;
-      acc.w += v.w;
-    }
-    reinterpret_cast<float4*>(out)[c] =
-        make_float4(acc.x * scale, acc.y * scale, acc.z * scale, acc.w * scale);
-  }
-}
 
 struct SelectArgs {
   int n_q, row_elems, nvec, R, splits, rows_per_split;
@@ -383,11 +380,15 @@ template <typename T>
 wa_status summarize_t(const T* pages, int n_pages, int page_tokens, int row_elems, float* kbar,
                       cudaStream_t st) {
   Plan p = plan_rows<T>(row_elems);
-  int splits = kTargetCtas / n_pages;
+  // About two waves of CTAs: a single wave of long row ranges ends with the
+  // slowest range, and more, shorter ranges add partial sums (measured on the
+  // one-layer WorldAttention bank: 0.251 ms with one wave of 256-thread CTAs,
+  // 0.227 ms with two waves of 384-thread CTAs, 0.267 ms with four).
+  int splits = 2 * kTargetCtas / n_pages;
   if (splits < 1) splits = 1;
   const int max_splits = (page_tokens + 63) / 64;   // at least 64 rows per CTA
   if (splits > max_splits) splits = max_splits;
-  if (splits > 64) splits = 64;
+  if (splits > 256) splits = 256;
   const int rps = (page_tokens + splits - 1) / splits;
   splits = (page_tokens + rps - 1) / rps;
   Scratch sc;
