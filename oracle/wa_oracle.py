@@ -40,6 +40,19 @@ design notes):
   with E rows aligned to [gathered buffer ; local KV].
 * The gate equation is missing on the page; fused output is
   O = w_attn[h] * O_attn + w_lin[h] * O_lin, default weights 1 and 1.
+* HSA sparse branch ([WA] HSA section and its appendix notes): key blocks of
+  B_inter = 128 tokens over the retrieved buffer and B_intra = 64 over the
+  chunk's own tokens (a ragged last block keeps its own size); query blocks of
+  B_intra = 64.  The pooled attention map of head h is the softmax over key
+  blocks of scale * Qbar_qb . Kbar_kb (block means), one row per query block;
+  the head's block mass is that map averaged over query blocks.  Selection is
+  per head (the same block set for every query of the head): blocks ordered by
+  mass (ties to the lower block index), the minimal prefix whose cumulative
+  mass reaches tau_h.  The Gini-to-threshold formula is missing on the page;
+  read as tau_h = 1 - G_h with G_h the Gini coefficient of the head's block
+  mass (a uniform head keeps every block, a peaked head few), unless the
+  caller passes tau_h.  The branch output is softmax attention restricted to
+  the selected blocks' tokens.
 
 Array conventions: token-major [tokens][H][d]; pages [n_pages][P][H][d];
 bf16 values are passed as np.uint16 bit patterns and decoded exactly.
@@ -68,6 +81,13 @@ __all__ = [
     "linformer_project",
     "linear_branch",
     "fuse_branches",
+    "block_bounds",
+    "block_means",
+    "key_blocks",
+    "pooled_mass",
+    "gini",
+    "sparse_select",
+    "sparse_attn",
 ]
 
 
@@ -286,3 +306,115 @@ def fuse_branches(o_attn: np.ndarray, o_lin: np.ndarray, w_attn=None, w_lin=None
     wa = np.ones(n_h) if w_attn is None else np.asarray(w_attn, dtype=np.float64)
     wl = np.ones(n_h) if w_lin is None else np.asarray(w_lin, dtype=np.float64)
     return o_attn * wa[None, :, None] + o_lin * wl[None, :, None]
+
+
+# ----------------------------------------------------------------------------
+# [WA] HSA: sparse branch (pooled block map, Gini-adaptive block selection,
+# attention restricted to the selected blocks)
+# ----------------------------------------------------------------------------
+
+def block_bounds(n: int, block: int):
+    """Rows [start, end) of the blocks of ``block`` rows over n rows; the last
+    block is ragged when block does not divide n."""
+    return [(s, min(n, s + block)) for s in range(0, n, block)]
+
+
+def block_means(x, block: int) -> np.ndarray:
+    """Mean of each block of rows: x [n][H][d] -> [n_blocks][H][d] (fp64),
+    a ragged last block divided by its own row count."""
+    xx = as_f64(x)
+    return np.stack([xx[a:b].sum(axis=0) / (b - a) for a, b in block_bounds(len(xx), block)],
+                    axis=0)
+
+
+def key_blocks(n_main: int, n_loc: int, b_inter: int = 128, b_intra: int = 64):
+    """Key blocks in index order: the retrieved buffer in blocks of B_inter,
+    then the chunk's own tokens in blocks of B_intra.  Each entry is
+    (segment, start, end) with segment 0 = buffer, 1 = local."""
+    out = [(0, a, b) for a, b in block_bounds(n_main, b_inter)]
+    out += [(1, a, b) for a, b in block_bounds(n_loc, b_intra)]
+    return out
+
+
+def pooled_mass(q, k_main, k_loc, scale: float | None = None, b_q: int = 64,
+                b_inter: int = 128, b_intra: int = 64) -> np.ndarray:
+    """Block mass of each head: mass[h][kb] = mean over query blocks qb of
+    softmax_kb(scale * Qbar_qb,h . Kbar_kb,h), the pooled attention map of the
+    HSA sparse branch.  Returns [H][n_kb] (each row sums to 1)."""
+    qq = as_f64(q)
+    d = qq.shape[2]
+    if scale is None or scale <= 0:
+        scale = 1.0 / math.sqrt(d)
+    qbar = block_means(qq, b_q)
+    parts = []
+    if k_main is not None and len(k_main) > 0:
+        parts.append(block_means(k_main, b_inter))
+    if k_loc is not None and len(k_loc) > 0:
+        parts.append(block_means(k_loc, b_intra))
+    kbar = np.concatenate(parts, axis=0)
+    n_h = qq.shape[1]
+    mass = np.empty((n_h, kbar.shape[0]), dtype=np.float64)
+    for h in range(n_h):
+        _, _, a = attention_rows(qbar[:, h, :], kbar[:, h, :], kbar[:, h, :], scale)
+        mass[h] = a.mean(axis=0)
+    return mass
+
+
+def gini(m) -> float:
+    """Gini coefficient of a non-negative vector (sorted-rank form):
+    G = sum_i (2 i - n - 1) x_(i) / (n sum x), x_(1) <= ... <= x_(n)."""
+    x = np.sort(np.asarray(m, dtype=np.float64))
+    n = len(x)
+    tot = x.sum()
+    if n == 0 or tot == 0.0:
+        return 0.0
+    i = np.arange(1, n + 1, dtype=np.float64)
+    return float(((2.0 * i - n - 1.0) * x).sum() / (n * tot))
+
+
+def sparse_select(mass: np.ndarray, tau=None):
+    """Per head: G_h = gini(mass[h]); tau_h = 1 - G_h unless given; blocks in
+    order of mass (descending, ties to the lower index); the minimal prefix
+    whose cumulative mass reaches tau_h (at least one block).  Returns
+    (list of ascending block-index arrays per head, G [H], tau [H])."""
+    n_h, n_kb = mass.shape
+    sel, g_all, t_all = [], np.empty(n_h), np.empty(n_h)
+    for h in range(n_h):
+        g = gini(mass[h])
+        t = (1.0 - g) if tau is None else float(tau[h])
+        order = sorted(range(n_kb), key=lambda b: (-mass[h][b], b))
+        acc, k = 0.0, 0
+        for b in order:
+            acc += mass[h][b]
+            k += 1
+            if acc >= t:
+                break
+        sel.append(np.array(sorted(order[:k]), dtype=np.int32))
+        g_all[h], t_all[h] = g, t
+    return sel, g_all, t_all
+
+
+def sparse_attn(q, k_main, v_main, k_loc, v_loc, sel, scale: float | None = None,
+                rows=None, b_inter: int = 128, b_intra: int = 64):
+    """Attention of the chunk's queries restricted, per head, to the tokens of
+    the selected key blocks (ascending block order).  sel: per-head arrays of
+    block indices into key_blocks(n_main, n_loc).  Returns O [len(rows)][H][d]."""
+    qq = as_f64(q)
+    n_q, n_h, d = qq.shape
+    if scale is None or scale <= 0:
+        scale = 1.0 / math.sqrt(d)
+    n_main = 0 if k_main is None else len(k_main)
+    n_loc = 0 if k_loc is None else len(k_loc)
+    blocks = key_blocks(n_main, n_loc, b_inter, b_intra)
+    rows = np.arange(n_q) if rows is None else np.asarray(rows)
+    out = np.empty((len(rows), n_h, d), dtype=np.float64)
+    for h in range(n_h):
+        ks, vs = [], []
+        for b in sel[h]:
+            seg, a, e = blocks[int(b)]
+            src_k, src_v = (k_main, v_main) if seg == 0 else (k_loc, v_loc)
+            ks.append(as_f64(src_k[a:e, h, :]))
+            vs.append(as_f64(src_v[a:e, h, :]))
+        oh, _, _ = attention_rows(qq[rows, h, :], np.concatenate(ks), np.concatenate(vs), scale)
+        out[:, h, :] = oh
+    return out
