@@ -227,6 +227,71 @@ wa_status wa_linear_branch(const void* q, int n_q, const void* k_main, const voi
                            void* o, wa_dtype o_dt, wa_stream_t stream);
 
 /*
+ * Block means ([WA] HSA, sparse branch: pooled tokens of a block):
+ *
+ *   means[b][h][:] = mean of x[r][h][:] over rows r in [b*block, min((b+1)*block, n_rows))
+ *
+ * a ragged last block divided by its own row count.
+ * x         : device [n_rows][n_heads][head_dim] of `dt` (16-byte aligned).
+ * means_out : device float32 [ceil(n_rows/block)][n_heads][head_dim].
+ * Errors: WA_ERR_SHAPE when n_heads*head_dim is not whole 16-byte vectors or
+ * exceeds 8192, or there are more than 4000 blocks.
+ */
+wa_status wa_block_means(const void* x, wa_dtype dt, int n_rows, int block, int n_heads,
+                         int head_dim, float* means_out, wa_stream_t stream);
+
+/*
+ * Block selection of the HSA sparse branch ([WA] HSA: pooled attention map,
+ * head-adaptive cumulative-mass selection; the Gini-to-threshold formula is
+ * missing on the page and read as tau_h = 1 - G_h):
+ *
+ *   A_h[qb][kb] = softmax_kb(scale * qbar[qb][h] . kbar[kb][h])
+ *   mass_h[kb]  = mean over qb of A_h[qb][kb]
+ *   G_h         = Gini coefficient of mass_h
+ *   tau_h       = tau[h] if tau != NULL, else 1 - G_h
+ *   kept_h      = the fewest blocks in order of mass (descending; ties to the
+ *                 lower index) whose cumulative mass reaches tau_h (>= 1 block)
+ *
+ * qbar      : device float32 [n_qb][n_heads][head_dim] (query-block means).
+ * kbar      : device float32 [n_kb][n_heads][head_dim] (key-block means, the
+ *             buffer's blocks first, then the local blocks).
+ * tau       : device float32 [n_heads] or NULL.
+ * sel_out   : device int32 [n_heads][n_kb]: row h starts with the count_out[h]
+ *             kept block indices in ascending order; the rest is unspecified.
+ * count_out : device int32 [n_heads].
+ * gini_out  : device float32 [n_heads] or NULL; mass_out : device float32
+ *             [n_heads][n_kb] or NULL.
+ * scale <= 0 means 1/sqrt(head_dim).  Deterministic (fixed-order sums).
+ * Needs n_qb <= 128 and head_dim <= 256; else WA_ERR_SHAPE.
+ */
+wa_status wa_sparse_select(const float* qbar, int n_qb, const float* kbar, int n_kb, int n_heads,
+                           int head_dim, float scale, const float* tau, int32_t* sel_out,
+                           int32_t* count_out, float* gini_out, float* mass_out,
+                           wa_stream_t stream);
+
+/*
+ * Block-sparse attention of the HSA sparse branch: wa_block_attn restricted,
+ * per head, to the tokens of the kept key blocks:
+ *
+ *   O[i][h] = sum_{k in kept blocks of h} softmax_k(scale * q[i][h] . K[k][h]) V[k][h]
+ *
+ * Key block b < nb = ceil(n_main/block_main) covers buffer rows
+ * [b*block_main, min((b+1)*block_main, n_main)); block b >= nb covers local
+ * rows [(b-nb)*block_loc, ...) of k_loc/v_loc.
+ * sel, count : device int32 [n_heads][nb + ceil(n_loc/block_loc)] and
+ *             [n_heads] as written by wa_sparse_select.  A head with count 0
+ *             gets O = 0 and LSE = -inf; indices must be valid block numbers
+ *             (the kernel does not check them).
+ * block_main, block_loc : 1 .. 128.
+ * Other arguments as for wa_block_attn; WA_BF16 only, head_dim == 128.
+ */
+wa_status wa_sparse_attn(const void* q, int n_q, const void* k_main, const void* v_main, int n_main,
+                         const void* k_loc, const void* v_loc, int n_loc, int block_main,
+                         int block_loc, const int32_t* sel, const int32_t* count, wa_dtype dt,
+                         int n_heads, int head_dim, float scale, void* o, wa_dtype o_dt,
+                         float* lse, wa_stream_t stream);
+
+/*
  * Synchronize `stream`, then read and clear this device's status word.
  * Returns WA_OK, WA_ERR_INDEX (a gather index was out of range),
  * WA_ERR_TIMEOUT (a kernel wait gave up; the kernel returned early and its

@@ -23,6 +23,9 @@ __all__ = [
     "wa_gather_pages",
     "wa_block_attn",
     "wa_linear_branch",
+    "wa_block_means",
+    "wa_sparse_select",
+    "wa_sparse_attn",
     "wa_check",
     "wa_shutdown",
     "wa_version",
@@ -37,7 +40,8 @@ WA_F32, WA_BF16 = 0, 1
 # Every symbol include/wa.h declares.
 EXPORTED_SYMBOLS = ("wa_strerror", "wa_version", "wa_page_summarize", "wa_select_pages",
                     "wa_select_pages_noalloc", "wa_gather_pages", "wa_block_attn",
-                    "wa_linear_branch", "wa_check", "wa_shutdown")
+                    "wa_linear_branch", "wa_block_means", "wa_sparse_select", "wa_sparse_attn",
+                    "wa_check", "wa_shutdown")
 
 
 class WaError(RuntimeError):
@@ -68,6 +72,9 @@ def load():
         "wa_gather_pages": (I, [P, P, I, I, I, I, I, P, P, I, P, P, P]),
         "wa_block_attn": (I, [P, I, P, P, I, P, P, I, I, I, I, F, P, I, P, P]),
         "wa_linear_branch": (I, [P, I, P, P, I, P, P, I, P, P, I, I, I, I, F, P, P, I, P, I, P]),
+        "wa_block_means": (I, [P, I, I, I, I, I, P, P]),
+        "wa_sparse_select": (I, [P, I, P, I, I, I, F, P, P, P, P, P, P]),
+        "wa_sparse_attn": (I, [P, I, P, P, I, P, P, I, I, I, P, P, I, I, I, F, P, I, P, P]),
         "wa_check": (I, [P]),
         "wa_shutdown": (I, []),
     }
@@ -182,6 +189,47 @@ def wa_linear_branch(q: torch.Tensor, k_main, v_main, k_loc, v_loc, e_k: torch.T
         _ptr(q), n_q, _ptr(k_main), _ptr(v_main), _rows(k_main), _ptr(k_loc), _ptr(v_loc),
         _rows(k_loc), _ptr(e_k), _ptr(e_v), rank, _dt(q), h, d, float(scale), _ptr(w_attn),
         _ptr(w_lin), int(bool(accumulate)), _ptr(o), _dt(o), _stream(stream)))
+
+
+def wa_block_means(x: torch.Tensor, block: int, means_out: torch.Tensor, stream=None):
+    """means_out[b,h,:] = mean of x rows [b*block, min((b+1)*block, n)) (ragged last block)."""
+    _need(x.dim() == 3 and x.is_contiguous(), "x must be contiguous [n][H][d]")
+    n, h, d = x.shape
+    nb = (n + block - 1) // block
+    _need(means_out.shape == (nb, h, d) and means_out.dtype == torch.float32
+          and means_out.is_contiguous(), "means_out must be float32 [ceil(n/block)][H][d]")
+    _ok("wa_block_means", load().wa_block_means(_ptr(x), _dt(x), n, int(block), h, d,
+                                                _ptr(means_out), _stream(stream)))
+
+
+def wa_sparse_select(qbar: torch.Tensor, kbar: torch.Tensor, sel_out: torch.Tensor,
+                     count_out: torch.Tensor, tau=None, gini_out=None, mass_out=None,
+                     scale: float = 0.0, stream=None):
+    """HSA block selection: per head, the fewest key blocks (by pooled mass)
+    whose cumulative mass reaches tau_h (= 1 - Gini when tau is None)."""
+    _need(qbar.dim() == 3 and kbar.dim() == 3 and qbar.dtype == torch.float32
+          and kbar.dtype == torch.float32 and qbar.is_contiguous() and kbar.is_contiguous(),
+          "qbar/kbar must be contiguous float32 [n][H][d]")
+    n_qb, h, d = qbar.shape
+    n_kb = kbar.shape[0]
+    _need(sel_out.shape == (h, n_kb) and sel_out.dtype == torch.int32 and count_out.numel() == h
+          and count_out.dtype == torch.int32, "sel_out int32 [H][n_kb], count_out int32 [H]")
+    _ok("wa_sparse_select", load().wa_sparse_select(
+        _ptr(qbar), n_qb, _ptr(kbar), n_kb, h, d, float(scale), _ptr(tau), _ptr(sel_out),
+        _ptr(count_out), _ptr(gini_out), _ptr(mass_out), _stream(stream)))
+
+
+def wa_sparse_attn(q: torch.Tensor, k_main, v_main, k_loc, v_loc, sel: torch.Tensor,
+                   count: torch.Tensor, o: torch.Tensor, block_main: int = 128,
+                   block_loc: int = 64, lse=None, scale: float = 0.0, stream=None):
+    """Attention restricted, per head, to the kept key blocks sel[h][:count[h]]."""
+    _need(q.dim() == 3 and q.is_contiguous() and o.shape == q.shape and o.is_contiguous(),
+          "q and o must be contiguous [n_q][H][d]")
+    n_q, h, d = q.shape
+    _ok("wa_sparse_attn", load().wa_sparse_attn(
+        _ptr(q), n_q, _ptr(k_main), _ptr(v_main), _rows(k_main), _ptr(k_loc), _ptr(v_loc),
+        _rows(k_loc), int(block_main), int(block_loc), _ptr(sel), _ptr(count), _dt(q), h, d,
+        float(scale), _ptr(o), _dt(o), _ptr(lse), _stream(stream)))
 
 
 def wa_check(stream=None):

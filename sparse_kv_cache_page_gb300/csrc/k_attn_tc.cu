@@ -108,11 +108,29 @@ struct Params {
   float* part_o;             // [unit][split][256][128] unnormalised O (split > 1)
   float4* part_ml;           // [unit][split][256] (m, l, l_exact, -)
   unsigned* counters;        // [unit] tickets, zero between launches
+  // block-sparse form (sel != NULL): head h attends to key blocks
+  // sel[h][0 .. count[h]), each a block of b_main buffer rows (index < nb_main)
+  // or of b_loc local rows; dense form: 128-key tiles over [main ; local]
+  const int32_t* sel;
+  const int32_t* sel_count;
+  int sel_stride, nb_main, b_main, b_loc;
 };
 
-__device__ __forceinline__ int tile_valid(const Params& p, int j) {
-  if (j < p.nt_main) return min(BN, p.n_main - j * BN);
-  return min(BN, p.n_loc - (j - p.nt_main) * BN);
+// Key tile j of head h: segment (0 = buffer, 1 = local), first row, valid rows.
+struct TileRef {
+  int seg, row, valid;
+};
+template <bool kSparse>
+__device__ __forceinline__ TileRef tile_ref(const Params& p, int head, int j) {
+  if (kSparse) {
+    const int b = __ldg(p.sel + (size_t)head * p.sel_stride + j);
+    if (b < p.nb_main) return {0, b * p.b_main, min(p.b_main, p.n_main - b * p.b_main)};
+    const int r = (b - p.nb_main) * p.b_loc;
+    return {1, r, min(p.b_loc, p.n_loc - r)};
+  }
+  if (j < p.nt_main) return {0, j * BN, min(BN, p.n_main - j * BN)};
+  const int r = (j - p.nt_main) * BN;
+  return {1, r, min(BN, p.n_loc - r)};
 }
 
 // Key tiles [j0, j1) of split `sp`: contiguous, sizes differ by at most one.
@@ -164,7 +182,7 @@ __device__ __forceinline__ void softmax_bar() {   // the 256 softmax threads onl
   asm volatile("bar.sync 1, 256;" ::: "memory");
 }
 
-template <typename OutT, bool kLse>
+template <typename OutT, bool kLse, bool kSparse>
 __global__ void __launch_bounds__(kThreads, 1)
 k_block_attn_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_km,
                 const __grid_constant__ CUtensorMap tm_vm, const __grid_constant__ CUtensorMap tm_kl,
@@ -179,8 +197,9 @@ k_block_attn_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
   const int split = blockIdx.x % p.n_split;
   const int q0 = qpair * (2 * BM);
   int jb, je;
-  split_range(p.nt_main + p.nt_loc, p.n_split, split, jb, je);
-  const int nloc = je - jb;                 // key tiles of this CTA (>= 1)
+  const int nkv = kSparse ? __ldg(p.sel_count + head) : p.nt_main + p.nt_loc;
+  split_range(nkv, p.n_split, split, jb, je);
+  const int nloc = je - jb;                 // key tiles of this CTA (0 only in the block-sparse form)
   volatile int* abort_flag = &bars->abort_flag;
 
   if (threadIdx.x == 0) {
@@ -225,17 +244,10 @@ k_block_attn_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
           if (t >= NS &&
               !mbar_wait_sleep(&bars->kv_empty[slot], ((t / NS) - 1) & 1, abort_flag, p.status))
             break;
-          const int j = jb + (t >> 1);
+          const TileRef tr = tile_ref<kSparse>(p, head, jb + (t >> 1));
           const bool is_v = t & 1;
-          const CUtensorMap* map;
-          int row;
-          if (j < p.nt_main) {
-            map = is_v ? &tm_vm : &tm_km;
-            row = j * BN;
-          } else {
-            map = is_v ? &tm_vl : &tm_kl;
-            row = (j - p.nt_main) * BN;
-          }
+          const CUtensorMap* map = tr.seg == 0 ? (is_v ? &tm_vm : &tm_km) : (is_v ? &tm_vl : &tm_kl);
+          const int row = tr.row;
           uint8_t* dst = smem + SmemLayout::ring + slot * kKvTile;
           mbar_arrive_expect_tx(&bars->kv_full[slot], kKvTile);
           tma_load_2d(map, &bars->kv_full[slot], dst, xq, row);
@@ -341,7 +353,7 @@ k_block_attn_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
       tmem_ld_wait();
       tc_fence_before();
       mbar_arrive(&bars->s_free[qt]);            // the other tile's S may now be computed
-      const int valid = tile_valid(p, jb + jj);   // warp-uniform
+      const int valid = tile_ref<kSparse>(p, head, jb + jj).valid;   // warp-uniform
       if (valid < BN) {
 #pragma unroll
         for (int c = 0; c < 4; ++c)
@@ -409,7 +421,7 @@ k_block_attn_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
       l += rs0 + rs1;
       if (kLse) lx += xs0 + xs1;
     }
-    if (ok)
+    if (ok && nloc > 0)
       ok = __all_sync(0xffffffffu, mbar_wait(&bars->o_ready[qt], (nloc - 1) & 1, abort_flag,
                                              p.status));
     tc_fence_after();
@@ -420,12 +432,18 @@ k_block_attn_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     OutT* orow_g = static_cast<OutT*>(p.o) + ((size_t)(store ? grow : 0) * p.n_heads + head) * HD;
     if (p.n_split == 1) {
       if (ok) {
-        const float wn = wn0 / l;
+        // a head with no key blocks (block-sparse form) has O = 0, LSE = -inf
+        const float wn = nloc > 0 ? wn0 / l : 0.0f;
 #pragma unroll 1
         for (int c = 0; c < 4; ++c) {
           uint32_t orow[32];
-          tmem_ld32(o_addr + 32 * c, orow);   // whole warp
-          tmem_ld_wait();
+          if (nloc > 0) {
+            tmem_ld32(o_addr + 32 * c, orow);   // whole warp
+            tmem_ld_wait();
+          } else {
+#pragma unroll
+            for (int e = 0; e < 32; ++e) orow[e] = 0u;
+          }
           if (store) {
             float x[32];
 #pragma unroll
@@ -433,7 +451,8 @@ k_block_attn_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             store_row32(orow_g + 32 * c, x, p.accumulate != 0, wo);
           }
         }
-        if (kLse && store && p.lse) p.lse[(size_t)head * p.n_q + grow] = m * p.scale + logf(lx);
+        if (kLse && store && p.lse)
+          p.lse[(size_t)head * p.n_q + grow] = nloc > 0 ? m * p.scale + logf(lx) : -INFINITY;
       }
     } else {
       // split: store this CTA's unnormalised rows, then the last CTA of the
@@ -445,8 +464,13 @@ k_block_attn_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
 #pragma unroll 1
         for (int c = 0; c < 4; ++c) {
           uint32_t orow[32];
-          tmem_ld32(o_addr + 32 * c, orow);
-          tmem_ld_wait();
+          if (nloc > 0) {   // an empty key range (block-sparse form) leaves O = 0, m = -inf, l = 0
+            tmem_ld32(o_addr + 32 * c, orow);
+            tmem_ld_wait();
+          } else {
+#pragma unroll
+            for (int e = 0; e < 32; ++e) orow[e] = 0u;
+          }
           float4* d4 = reinterpret_cast<float4*>(dst + 32 * c);
 #pragma unroll
           for (int v = 0; v < 8; ++v)
@@ -469,14 +493,15 @@ k_block_attn_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
           const float4* ml = p.part_ml + (size_t)unit * p.n_split * 256 + prow;
           float mm = -INFINITY;
           for (int s = 0; s < p.n_split; ++s) mm = fmaxf(mm, __ldcg(ml + (size_t)s * 256).x);
+          const bool none = !(mm > -INFINITY);   // no keys in any split: O = 0, LSE = -inf
           float den = 0.f, denx = 0.f;
           for (int s = 0; s < p.n_split; ++s) {
             const float4 t = __ldcg(ml + (size_t)s * 256);
-            const float w = ex2((t.x - mm) * sl2);
+            const float w = none ? 0.f : ex2((t.x - mm) * sl2);
             den += w * t.y;
             denx += w * t.z;
           }
-          const float wn = wn0 / den;
+          const float wn = none ? 0.f : wn0 / den;
           const float* src = p.part_o + ((size_t)unit * p.n_split * 256 + prow) * HD;
 #pragma unroll 1
           for (int c = 0; c < 4; ++c) {
@@ -484,7 +509,7 @@ k_block_attn_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
 #pragma unroll
             for (int e = 0; e < 32; ++e) x[e] = 0.f;
             for (int s = 0; s < p.n_split; ++s) {
-              const float w = ex2((__ldcg(ml + (size_t)s * 256).x - mm) * sl2) * wn;
+              const float w = none ? 0.f : ex2((__ldcg(ml + (size_t)s * 256).x - mm) * sl2) * wn;
               const float4* s4 = reinterpret_cast<const float4*>(src + (size_t)s * 256 * HD + 32 * c);
 #pragma unroll
               for (int v = 0; v < 8; ++v) {
@@ -497,7 +522,8 @@ k_block_attn_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             }
             store_row32(orow_g + 32 * c, x, p.accumulate != 0, wo);
           }
-          if (kLse && p.lse) p.lse[(size_t)head * p.n_q + grow] = mm * p.scale + logf(denx);
+          if (kLse && p.lse)
+            p.lse[(size_t)head * p.n_q + grow] = none ? -INFINITY : mm * p.scale + logf(denx);
         }
       }
     }
@@ -531,7 +557,7 @@ int choose_split(int units, int nkv, int sms) {
   return best;
 }
 
-template <typename OutT, bool kLse>
+template <typename OutT, bool kLse, bool kSparse>
 wa_status launch_t(const CUtensorMap& tq, const CUtensorMap& tkm, const CUtensorMap& tvm,
                    const CUtensorMap& tkl, const CUtensorMap& tvl, const Params& p, int n_heads,
                    cudaStream_t s) {
@@ -539,7 +565,7 @@ wa_status launch_t(const CUtensorMap& tq, const CUtensorMap& tkm, const CUtensor
   static bool attr_done[64] = {};
   int dev = 0;
   cudaGetDevice(&dev);
-  auto kern = k_block_attn_tc<OutT, kLse>;
+  auto kern = k_block_attn_tc<OutT, kLse, kSparse>;
   if (dev < 64 && !attr_done[dev]) {
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
       return WA_ERR_CUDA;
@@ -555,7 +581,8 @@ wa_status launch_t(const CUtensorMap& tq, const CUtensorMap& tkm, const CUtensor
 wa_status launch_attn_tc(const void* q, int n_q, const void* k_main, const void* v_main,
                          int n_main, const void* k_loc, const void* v_loc, int n_loc, int n_heads,
                          float scale, void* o, int o_f32, float* lse, int accumulate,
-                         const float* w_old, const float* w_new, int max_split, cudaStream_t s) {
+                         const float* w_old, const float* w_new, int max_split, cudaStream_t s,
+                         const SparseBlocks* sparse) {
   const uint64_t cols = (uint64_t)n_heads * HD;
   CUtensorMap tq, tkm, tvm, tkl, tvl;
   memset(&tkm, 0, sizeof(tkm));
@@ -580,14 +607,23 @@ wa_status launch_attn_tc(const void* q, int n_q, const void* k_main, const void*
   p.nt_main = (n_main + BN - 1) / BN;
   p.nt_loc = (n_loc + BN - 1) / BN;
   p.n_qpairs = (n_q + 2 * BM - 1) / (2 * BM);
+  p.sel = sparse ? sparse->sel : nullptr;
+  p.sel_count = sparse ? sparse->count : nullptr;
+  p.sel_stride = sparse ? sparse->stride : 0;
+  p.b_main = sparse ? sparse->b_main : BN;
+  p.b_loc = sparse ? sparse->b_loc : BN;
+  p.nb_main = sparse ? (n_main + p.b_main - 1) / p.b_main : p.nt_main;
+  // the block-sparse form sizes its splits for every block kept (the counts
+  // live on the device); CTAs whose share is empty finish at once
+  const int nkv_max = sparse ? sparse->stride : p.nt_main + p.nt_loc;
   int dev = 0, sms = 148;
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  p.n_split = choose_split(p.n_qpairs * n_heads, p.nt_main + p.nt_loc, sms);
+  p.n_split = choose_split(p.n_qpairs * n_heads, nkv_max, sms);
   // WA_ATTN_SPLIT=n forces the split count (clamped to what the tiles allow)
   if (const char* env = getenv("WA_ATTN_SPLIT")) {
     int f = atoi(env);
-    const int nkv = p.nt_main + p.nt_loc;
+    const int nkv = nkv_max;
     if (f >= 1) p.n_split = f > nkv ? nkv : f;
     if ((size_t)p.n_qpairs * n_heads > (size_t)kMaxUnits) p.n_split = 1;
   }
@@ -615,10 +651,15 @@ wa_status launch_attn_tc(const void* q, int n_q, const void* k_main, const void*
   }
   const bool want_lse = lse != nullptr;
   if (o_f32)
-    return want_lse ? launch_t<float, true>(tq, tkm, tvm, tkl, tvl, p, n_heads, s)
-                    : launch_t<float, false>(tq, tkm, tvm, tkl, tvl, p, n_heads, s);
-  return want_lse ? launch_t<__nv_bfloat16, true>(tq, tkm, tvm, tkl, tvl, p, n_heads, s)
-                  : launch_t<__nv_bfloat16, false>(tq, tkm, tvm, tkl, tvl, p, n_heads, s);
+    return sparse ? (want_lse ? launch_t<float, true, true>(tq, tkm, tvm, tkl, tvl, p, n_heads, s)
+                              : launch_t<float, false, true>(tq, tkm, tvm, tkl, tvl, p, n_heads, s))
+                  : (want_lse ? launch_t<float, true, false>(tq, tkm, tvm, tkl, tvl, p, n_heads, s)
+                              : launch_t<float, false, false>(tq, tkm, tvm, tkl, tvl, p, n_heads, s));
+  return sparse
+             ? (want_lse ? launch_t<__nv_bfloat16, true, true>(tq, tkm, tvm, tkl, tvl, p, n_heads, s)
+                         : launch_t<__nv_bfloat16, false, true>(tq, tkm, tvm, tkl, tvl, p, n_heads, s))
+             : (want_lse ? launch_t<__nv_bfloat16, true, false>(tq, tkm, tvm, tkl, tvl, p, n_heads, s)
+                         : launch_t<__nv_bfloat16, false, false>(tq, tkm, tvm, tkl, tvl, p, n_heads, s));
 }
 
 }  // namespace wa

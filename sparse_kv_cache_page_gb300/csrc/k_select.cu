@@ -20,7 +20,7 @@ namespace wa {
 namespace {
 
 constexpr int kThreads = 384;           // 2 x 192 16-byte vectors of a 1,536-element bf16 row
-constexpr int kTargetCtas = 152 * 5;     // 5 x 384 threads per SM
+constexpr int kTargetCtas = 152 * 5;     // sizing unit for the row-range splits
 constexpr unsigned kSelectCounter = 4095;
 
 template <typename T> struct VecOf;
@@ -159,18 +159,22 @@ __device__ void sum_rows4(const float* rows, int n, int row_elems, float* out, f
 // ---------------------------------------------------------------------------
 // page summaries
 // ---------------------------------------------------------------------------
+// Four resident CTAs per SM (at most 40 registers): five, which the compiler picks
+// otherwise, stream about 8% slower.
 template <typename T, int VPT>
-__global__ void __launch_bounds__(kThreads)
-k_page_summarize(const T* __restrict__ pages, int page_tokens, int row_elems, int nvec, int R,
-                 int splits, int rows_per_split, float* __restrict__ partial,
+__global__ void __launch_bounds__(kThreads, 4)
+k_page_summarize(const T* __restrict__ pages, int page_tokens, int n_rows, int row_elems, int nvec,
+                 int R, int splits, int rows_per_split, float* __restrict__ partial,
                  float* __restrict__ kbar, Ctrl* ctrl) {
   extern __shared__ float red[];
   const int j = blockIdx.x / splits, s = blockIdx.x % splits;
+  // page j holds rows [j P, j P + rows_j) of the n_rows; only the last may be short
+  const int rows_j = min(page_tokens, n_rows - j * page_tokens);
   const int r0 = s * rows_per_split;
-  const int r1 = min(page_tokens, r0 + rows_per_split);
+  const int r1 = min(rows_j, r0 + rows_per_split);
   const T* base = pages + (size_t)j * page_tokens * row_elems;
   colsum_rows<T, VPT>(base, row_elems, nvec, R, r0, r1, red);
-  const float inv = 1.0f / (float)page_tokens;
+  const float inv = 1.0f / (float)rows_j;
   if (splits == 1) {
     for (int c = threadIdx.x; c < row_elems; c += blockDim.x)
       kbar[(size_t)j * row_elems + c] = red[c] * inv;
@@ -377,8 +381,8 @@ Plan plan_rows(int row_elems) {
 }
 
 template <typename T>
-wa_status summarize_t(const T* pages, int n_pages, int page_tokens, int row_elems, float* kbar,
-                      cudaStream_t st) {
+wa_status summarize_t(const T* pages, int n_pages, int page_tokens, int n_rows, int row_elems,
+                      float* kbar, cudaStream_t st) {
   Plan p = plan_rows<T>(row_elems);
   // About two waves of CTAs: a single wave of long row ranges ends with the
   // slowest range, and more, shorter ranges add partial sums (measured on the
@@ -402,7 +406,7 @@ wa_status summarize_t(const T* pages, int n_pages, int page_tokens, int row_elem
     if (smem > 48 * 1024)                                                                   \
       cudaFuncSetAttribute(k_page_summarize<T, V>, cudaFuncAttributeMaxDynamicSharedMemorySize, \
                            (int)smem);                                                      \
-    k_page_summarize<T, V><<<grid, p.threads, smem, st>>>(pages, page_tokens, row_elems,    \
+    k_page_summarize<T, V><<<grid, p.threads, smem, st>>>(pages, page_tokens, n_rows, row_elems, \
                                                           p.nvec, p.R, splits, rps,         \
                                                           (float*)sc.data, kbar, sc.ctrl);  \
     break;
@@ -458,10 +462,19 @@ wa_status select_t(const T* q, SelectArgs a, cudaStream_t st) {
 
 wa_status launch_page_summarize(const void* k_pages, wa_dtype dt, int n_pages, int page_tokens,
                                 int row_elems, float* kbar_out, cudaStream_t s) {
+  const int n_rows = n_pages * page_tokens;
   if (dt == WA_BF16)
-    return summarize_t((const __nv_bfloat16*)k_pages, n_pages, page_tokens, row_elems, kbar_out,
-                       s);
-  return summarize_t((const float*)k_pages, n_pages, page_tokens, row_elems, kbar_out, s);
+    return summarize_t((const __nv_bfloat16*)k_pages, n_pages, page_tokens, n_rows, row_elems,
+                       kbar_out, s);
+  return summarize_t((const float*)k_pages, n_pages, page_tokens, n_rows, row_elems, kbar_out, s);
+}
+
+wa_status launch_block_means(const void* x, wa_dtype dt, int n_rows, int block, int row_elems,
+                             float* means_out, cudaStream_t s) {
+  const int n_blocks = (n_rows + block - 1) / block;
+  if (dt == WA_BF16)
+    return summarize_t((const __nv_bfloat16*)x, n_blocks, block, n_rows, row_elems, means_out, s);
+  return summarize_t((const float*)x, n_blocks, block, n_rows, row_elems, means_out, s);
 }
 
 wa_status launch_select_pages(const void* q, wa_dtype dt, int n_q, int n_heads, int head_dim,

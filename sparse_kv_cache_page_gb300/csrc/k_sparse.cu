@@ -1,0 +1,256 @@
+// Block selection of the HSA sparse branch (WorldAttention review page, HSA
+// section and its appendix notes on the sparse branch): a pooled attention map
+// between query-block means and key-block means, each head's block mass, the
+// Gini coefficient of that mass, and the minimal set of blocks whose
+// cumulative mass reaches the head's threshold.
+//
+// k_pooled_scores  S[h][qb][kb] = scale * Qbar_qb,h . Kbar_kb,h.  Grid (key
+//                  block chunks of 64, heads); the head's query-block means
+//                  and a chunk of key-block means staged in shared memory
+//                  (rows padded to d+1 floats: conflict-free); a thread owns
+//                  one key block and every fourth query block.
+// k_sparse_select  one CTA per head:
+//   1. each query-block row's max and exp-sum (a warp per row, fixed order);
+//   2. mass[kb] = mean over query blocks of the row-normalised exp (fixed order);
+//   3. Gini coefficient from the ascending sort of the mass (bitonic sort of
+//      (mass bits, index) keys; mass >= 0, so the bit pattern orders it);
+//   4. tau = 1 - G unless the caller gives tau[h];
+//   5. blocks ordered by (mass descending, index ascending) with the same sort,
+//      cumulative mass by an inclusive scan in that order; the first position
+//      reaching tau ends the kept set (at least one block);
+//   6. the kept blocks written in ascending block order (scan of flags).
+// Every reduction and scan has a fixed order, so the result is deterministic.
+#include <math.h>
+
+#include "wa_internal.cuh"
+
+namespace wa {
+namespace {
+
+constexpr int kScoreThreads = 256;
+constexpr int kKbChunk = 64;             // key blocks per scores CTA
+constexpr int kQbGroups = kScoreThreads / kKbChunk;
+constexpr int kMaxQbPerThread = 32;      // n_qb <= 128
+constexpr int kSelThreads = 1024;
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  return v;
+}
+
+__global__ void __launch_bounds__(kScoreThreads)
+k_pooled_scores(const float* __restrict__ qbar, int n_qb, const float* __restrict__ kbar, int n_kb,
+                int n_heads, int d, float scale, float* __restrict__ scores) {
+  extern __shared__ float sm[];
+  const int h = blockIdx.y;
+  const int kb0 = blockIdx.x * kKbChunk;
+  const int nk = min(kKbChunk, n_kb - kb0);
+  const int dp = d + 1;
+  float* q_s = sm;                         // [n_qb][d]
+  float* k_s = sm + (size_t)n_qb * d;      // [kKbChunk][d + 1]
+  for (int i = threadIdx.x; i < n_qb * d; i += blockDim.x)
+    q_s[i] = qbar[((size_t)(i / d) * n_heads + h) * d + (i % d)];
+  for (int i = threadIdx.x; i < nk * d; i += blockDim.x)
+    k_s[(i / d) * dp + (i % d)] = kbar[((size_t)(kb0 + i / d) * n_heads + h) * d + (i % d)];
+  __syncthreads();
+  const int kl = threadIdx.x % kKbChunk, g = threadIdx.x / kKbChunk;
+  if (kl >= nk) return;
+  float acc[kMaxQbPerThread];
+#pragma unroll
+  for (int i = 0; i < kMaxQbPerThread; ++i) acc[i] = 0.f;
+  const float* kr = k_s + kl * dp;
+  for (int e = 0; e < d; ++e) {
+    const float kv = kr[e];
+#pragma unroll
+    for (int i = 0; i < kMaxQbPerThread; ++i) {
+      const int qb = g + kQbGroups * i;
+      if (qb < n_qb) acc[i] = fmaf(q_s[qb * d + e], kv, acc[i]);
+    }
+  }
+#pragma unroll
+  for (int i = 0; i < kMaxQbPerThread; ++i) {
+    const int qb = g + kQbGroups * i;
+    if (qb < n_qb) scores[((size_t)h * n_qb + qb) * n_kb + kb0 + kl] = acc[i] * scale;
+  }
+}
+
+// Ascending bitonic sort of n2 (power of two) keys in shared memory.
+__device__ void bitonic_sort(unsigned long long* keys, int n2) {
+  for (int k = 2; k <= n2; k <<= 1) {
+    for (int j = k >> 1; j > 0; j >>= 1) {
+      for (int i = threadIdx.x; i < n2; i += blockDim.x) {
+        const int ixj = i ^ j;
+        if (ixj > i) {
+          const bool up = (i & k) == 0;
+          const unsigned long long a = keys[i], b = keys[ixj];
+          if ((a > b) == up) {
+            keys[i] = b;
+            keys[ixj] = a;
+          }
+        }
+      }
+      __syncthreads();
+    }
+  }
+}
+
+// Inclusive scan of x[0..n2) in place (Hillis-Steele, fixed order); tmp has n2 floats.
+__device__ void scan_inclusive(float* x, float* tmp, int n2) {
+  for (int off = 1; off < n2; off <<= 1) {
+    for (int i = threadIdx.x; i < n2; i += blockDim.x) tmp[i] = x[i] + (i >= off ? x[i - off] : 0.f);
+    __syncthreads();
+    for (int i = threadIdx.x; i < n2; i += blockDim.x) x[i] = tmp[i];
+    __syncthreads();
+  }
+}
+
+// Sum of v over the CTA in a fixed order (warp butterflies, then across warps).
+__device__ float block_sum(float v, float* red) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
+  v = warp_sum(v);
+  __syncthreads();
+  if (lane == 0) red[warp] = v;
+  __syncthreads();
+  return warp_sum(lane < nwarps ? red[lane] : 0.f);
+}
+
+__global__ void __launch_bounds__(kSelThreads)
+k_sparse_select(const float* __restrict__ scores, int n_qb, int n_kb, const float* __restrict__ tau,
+                int32_t* __restrict__ sel, int32_t* __restrict__ count, float* __restrict__ gini_out,
+                float* __restrict__ mass_out, int n2) {
+  extern __shared__ __align__(16) unsigned char smem_raw[];
+  const int h = blockIdx.x;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nwarps = blockDim.x >> 5;
+  unsigned long long* keys = reinterpret_cast<unsigned long long*>(smem_raw);   // [n2]
+  float* mass = reinterpret_cast<float*>(keys + n2);                           // [n2]
+  float* cum = mass + n2;                                                      // [n2]
+  float* tmp = cum + n2;                                                       // [n2]
+  float* red = tmp + n2;                                                       // [32]
+  float* row_max = red + 32;                                                   // [n_qb]
+  float* row_inv = row_max + n_qb;                                             // [n_qb]
+  const float* sh = scores + (size_t)h * n_qb * n_kb;
+  // 1. per query-block row: max and 1 / sum of exp
+  for (int qb = warp; qb < n_qb; qb += nwarps) {
+    const float* row = sh + (size_t)qb * n_kb;
+    float mx = -INFINITY;
+    for (int kb = lane; kb < n_kb; kb += 32) mx = fmaxf(mx, row[kb]);
+    mx = warp_max(mx);
+    float s = 0.f;
+    for (int kb = lane; kb < n_kb; kb += 32) s += expf(row[kb] - mx);
+    s = warp_sum(s);
+    if (lane == 0) {
+      row_max[qb] = mx;
+      row_inv[qb] = 1.0f / s;
+    }
+  }
+  __syncthreads();
+  // 2. block mass, summed over query blocks in order
+  const float inv_q = 1.0f / (float)n_qb;
+  for (int kb = tid; kb < n2; kb += blockDim.x) {
+    float acc = 0.f;
+    if (kb < n_kb)
+      for (int qb = 0; qb < n_qb; ++qb) acc += expf(sh[(size_t)qb * n_kb + kb] - row_max[qb]) * row_inv[qb];
+    mass[kb] = kb < n_kb ? acc * inv_q : 0.f;
+    keys[kb] = kb < n_kb ? ((unsigned long long)__float_as_uint(mass[kb]) << 32) | (unsigned)kb
+                         : ~0ull;
+  }
+  __syncthreads();
+  // 3. Gini coefficient: G = sum_i (2i - n - 1) x_(i) / (n sum x), x ascending, i from 1
+  bitonic_sort(keys, n2);
+  float num = 0.f, tot = 0.f;
+  for (int i = tid; i < n_kb; i += blockDim.x) {
+    const float x = mass[(unsigned)(keys[i] & 0xffffffffu)];
+    num += (float)(2 * (i + 1) - n_kb - 1) * x;
+    tot += x;
+  }
+  num = block_sum(num, red);
+  tot = block_sum(tot, red);
+  const float g = tot > 0.f ? num / ((float)n_kb * tot) : 0.f;
+  // 4. threshold
+  const float t = tau ? tau[h] : 1.0f - g;
+  // 5. mass descending, index ascending; cumulative mass in that order
+  __syncthreads();
+  for (int kb = tid; kb < n2; kb += blockDim.x)
+    keys[kb] = kb < n_kb ? ((unsigned long long)(~__float_as_uint(mass[kb])) << 32) | (unsigned)kb
+                         : ~0ull;
+  __syncthreads();
+  bitonic_sort(keys, n2);
+  for (int i = tid; i < n2; i += blockDim.x)
+    cum[i] = i < n_kb ? mass[(unsigned)(keys[i] & 0xffffffffu)] : 0.f;
+  __syncthreads();
+  scan_inclusive(cum, tmp, n2);
+  // kept = 1 + the number of positions whose cumulative mass is still below tau
+  float below = 0.f;
+  for (int i = tid; i < n_kb; i += blockDim.x) below += (cum[i] < t) ? 1.f : 0.f;
+  below = block_sum(below, red);
+  int kept = (int)below + 1;
+  if (kept > n_kb) kept = n_kb;
+  // 6. kept blocks in ascending block order
+  __syncthreads();
+  for (int i = tid; i < n2; i += blockDim.x) cum[i] = 0.f;
+  __syncthreads();
+  for (int i = tid; i < kept; i += blockDim.x) cum[(unsigned)(keys[i] & 0xffffffffu)] = 1.f;
+  __syncthreads();
+  scan_inclusive(cum, tmp, n2);
+  for (int kb = tid; kb < n_kb; kb += blockDim.x) {
+    const float prev = kb == 0 ? 0.f : cum[kb - 1];
+    if (cum[kb] - prev > 0.5f) sel[(size_t)h * n_kb + (int)(cum[kb] + 0.5f) - 1] = kb;
+    if (mass_out) mass_out[(size_t)h * n_kb + kb] = mass[kb];
+  }
+  if (tid == 0) {
+    count[h] = kept;
+    if (gini_out) gini_out[h] = g;
+  }
+}
+
+}  // namespace
+
+wa_status launch_sparse_select(const float* qbar, int n_qb, const float* kbar, int n_kb,
+                               int n_heads, int head_dim, float scale, const float* tau,
+                               int32_t* sel_out, int32_t* count_out, float* gini_out,
+                               float* mass_out, cudaStream_t s) {
+  Scratch sc;
+  const size_t score_bytes = (size_t)n_heads * n_qb * n_kb * sizeof(float);
+  wa_status rc = get_scratch(score_bytes, &sc);
+  if (rc != WA_OK) return rc;
+  float* scores = static_cast<float*>(sc.data);
+  const size_t smem1 = ((size_t)n_qb * head_dim + (size_t)kKbChunk * (head_dim + 1)) * sizeof(float);
+  static bool attr_done[64] = {};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  int n2 = 1;
+  while (n2 < n_kb) n2 <<= 1;
+  const size_t smem2 = (size_t)n2 * 8 + (size_t)3 * n2 * 4 + 32 * 4 + (size_t)2 * n_qb * 4;
+  if (dev < 64 && !attr_done[dev]) {
+    if (cudaFuncSetAttribute(k_pooled_scores, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             227 * 1024) != cudaSuccess ||
+        cudaFuncSetAttribute(k_sparse_select, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             227 * 1024) != cudaSuccess)
+      return WA_ERR_CUDA;
+    attr_done[dev] = true;
+  }
+  dim3 g1((n_kb + kKbChunk - 1) / kKbChunk, n_heads);
+  k_pooled_scores<<<g1, kScoreThreads, smem1, s>>>(qbar, n_qb, kbar, n_kb, n_heads, head_dim, scale,
+                                                    scores);
+  k_sparse_select<<<n_heads, kSelThreads, smem2, s>>>(scores, n_qb, n_kb, tau, sel_out, count_out,
+                                                      gini_out, mass_out, n2);
+  return cuda_status(cudaPeekAtLastError());
+}
+
+// Limits the host checks before launch_sparse_select.
+int sparse_select_max_qb() { return kQbGroups * kMaxQbPerThread; }
+size_t sparse_select_smem(int n_qb, int n_kb, int head_dim) {
+  int n2 = 1;
+  while (n2 < n_kb) n2 <<= 1;
+  const size_t s1 = ((size_t)n_qb * head_dim + (size_t)kKbChunk * (head_dim + 1)) * sizeof(float);
+  const size_t s2 = (size_t)n2 * 8 + (size_t)3 * n2 * 4 + 32 * 4 + (size_t)2 * n_qb * 4;
+  return s1 > s2 ? s1 : s2;
+}
+
+}  // namespace wa

@@ -244,6 +244,59 @@ wa_status wa_block_attn(const void* q, int n_q, const void* k_main, const void* 
                         o_dt == WA_F32, lse, 0, nullptr, nullptr, 0, s);
 }
 
+wa_status wa_block_means(const void* x, wa_dtype dt, int n_rows, int block, int n_heads,
+                         int head_dim, float* means_out, wa_stream_t stream) {
+  if (!dtype_ok(dt)) return WA_ERR_DTYPE;
+  if (!x || !means_out || n_rows <= 0 || block <= 0) return WA_ERR_INVALID_ARG;
+  if (!row_ok(n_heads, head_dim, dt)) return WA_ERR_SHAPE;
+  if ((long long)n_heads * head_dim > 8192) return WA_ERR_SHAPE;
+  if ((n_rows + (long long)block - 1) / block > 4000) return WA_ERR_SHAPE;
+  if (!aligned16(x) || !aligned16(means_out)) return WA_ERR_ALIGN;
+  return launch_block_means(x, dt, n_rows, block, n_heads * head_dim, means_out,
+                            (cudaStream_t)stream);
+}
+
+wa_status wa_sparse_select(const float* qbar, int n_qb, const float* kbar, int n_kb, int n_heads,
+                           int head_dim, float scale, const float* tau, int32_t* sel_out,
+                           int32_t* count_out, float* gini_out, float* mass_out,
+                           wa_stream_t stream) {
+  if (!qbar || !kbar || !sel_out || !count_out || n_qb <= 0 || n_kb <= 0 || n_heads <= 0 ||
+      head_dim <= 0)
+    return WA_ERR_INVALID_ARG;
+  if (head_dim > 256 || n_qb > sparse_select_max_qb() || n_kb > (1 << 20)) return WA_ERR_SHAPE;
+  if (sparse_select_smem(n_qb, n_kb, head_dim) > 227 * 1024) return WA_ERR_SHAPE;
+  if (!(scale > 0.0f)) scale = 1.0f / sqrtf((float)head_dim);
+  return launch_sparse_select(qbar, n_qb, kbar, n_kb, n_heads, head_dim, scale, tau, sel_out,
+                              count_out, gini_out, mass_out, (cudaStream_t)stream);
+}
+
+wa_status wa_sparse_attn(const void* q, int n_q, const void* k_main, const void* v_main, int n_main,
+                         const void* k_loc, const void* v_loc, int n_loc, int block_main,
+                         int block_loc, const int32_t* sel, const int32_t* count, wa_dtype dt,
+                         int n_heads, int head_dim, float scale, void* o, wa_dtype o_dt,
+                         float* lse, wa_stream_t stream) {
+  if (!dtype_ok(dt) || !dtype_ok(o_dt)) return WA_ERR_DTYPE;
+  if (dt != WA_BF16) return WA_ERR_DTYPE;
+  if (!q || !o || !sel || !count || n_q <= 0 || n_main < 0 || n_loc < 0 || n_main + n_loc <= 0)
+    return WA_ERR_INVALID_ARG;
+  if (n_main > 0 && (!k_main || !v_main)) return WA_ERR_INVALID_ARG;
+  if (n_loc > 0 && (!k_loc || !v_loc)) return WA_ERR_INVALID_ARG;
+  if (block_main < 1 || block_main > 128 || block_loc < 1 || block_loc > 128) return WA_ERR_SHAPE;
+  if (head_dim != 128 || n_heads <= 0 || (long long)n_heads * 128 > 16384) return WA_ERR_SHAPE;
+  if (!aligned16(q) || !aligned16(o) || (n_main > 0 && (!aligned16(k_main) || !aligned16(v_main))) ||
+      (n_loc > 0 && (!aligned16(k_loc) || !aligned16(v_loc))))
+    return WA_ERR_ALIGN;
+  if (!(scale > 0.0f)) scale = 1.0f / sqrtf((float)head_dim);
+  SparseBlocks sb;
+  sb.sel = sel;
+  sb.count = count;
+  sb.b_main = block_main;
+  sb.b_loc = block_loc;
+  sb.stride = (n_main + block_main - 1) / block_main + (n_loc + block_loc - 1) / block_loc;
+  return launch_attn_tc(q, n_q, k_main, v_main, n_main, k_loc, v_loc, n_loc, n_heads, scale, o,
+                        o_dt == WA_F32, lse, 0, nullptr, nullptr, 0, (cudaStream_t)stream, &sb);
+}
+
 wa_status wa_linear_branch(const void* q, int n_q, const void* k_main, const void* v_main,
                            int n_main, const void* k_loc, const void* v_loc, int n_loc,
                            const void* e_k, const void* e_v, int rank, wa_dtype dt, int n_heads,

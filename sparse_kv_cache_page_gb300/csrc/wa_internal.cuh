@@ -76,10 +76,31 @@ wa_status launch_attn_f32(const float* q, int n_q, const float* k_main, const fl
 // epilogue o = w_old[h]*o + w_new[h]*O (accumulate != 0), may be NULL.
 // max_split: 0 = choose the key-range split automatically, else an upper
 // bound (1 = no split, which also means no scratch is touched).
+// Block-sparse form of the attention: head h attends to the key blocks
+// sel[h * stride + t], t < count[h] (device arrays), each block b_main buffer
+// rows (index < ceil(n_main / b_main)) or b_loc local rows; b_main, b_loc <= 128.
+struct SparseBlocks {
+  const int32_t* sel;
+  const int32_t* count;
+  int stride, b_main, b_loc;
+};
 wa_status launch_attn_tc(const void* q, int n_q, const void* k_main, const void* v_main,
                          int n_main, const void* k_loc, const void* v_loc, int n_loc,
                          int n_heads, float scale, void* o, int o_f32, float* lse, int accumulate,
-                         const float* w_old, const float* w_new, int max_split, cudaStream_t s);
+                         const float* w_old, const float* w_new, int max_split, cudaStream_t s,
+                         const SparseBlocks* sparse = nullptr);
+
+// Block means of x [n_rows][row_elems] in blocks of `block` rows (ragged last block).
+wa_status launch_block_means(const void* x, wa_dtype dt, int n_rows, int block, int row_elems,
+                             float* means_out, cudaStream_t s);
+
+// HSA block selection (k_sparse.cu) and the limits its host checks use.
+wa_status launch_sparse_select(const float* qbar, int n_qb, const float* kbar, int n_kb,
+                               int n_heads, int head_dim, float scale, const float* tau,
+                               int32_t* sel_out, int32_t* count_out, float* gini_out,
+                               float* mass_out, cudaStream_t s);
+int sparse_select_max_qb();
+size_t sparse_select_smem(int n_qb, int n_kb, int head_dim);
 
 wa_status launch_linear_branch(const void* q, int n_q, const void* k_main, const void* v_main,
                                int n_main, const void* k_loc, const void* v_loc, int n_loc,
