@@ -317,6 +317,125 @@ def run_gpu(args, world, rank, local, hybrid=False):
     return line
 
 
+def run_hsa(args, world, rank, local):
+    """One chunk with the HSA branches in place of dense attention
+    (WorldAttention review page, HSA section): retrieval as in the headline
+    workload (summaries, two-stage selection, gather), then the sparse branch
+    -- block means of the queries (64), the buffer (128) and the local tokens
+    (64), the pooled block map and Gini-adaptive block selection per head,
+    block-sparse attention over the kept blocks -- and the Linformer branch
+    (rank 256) fused with equal per-head weights.  Synthetic structure: in 4
+    of the 12 heads (0, 3, 6, 9) the queries and one 128-token block of every
+    page share a direction (gain 3), so those heads have peaked block maps;
+    the other heads are N(0,1) with near-uniform maps."""
+    import torch
+
+    import sparse_kv_cache_page_gb300 as wa
+    from sparse_kv_cache_page_gb300 import synth
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    wa.load()
+    c = synth.worldattention_case(device=dev, layer=rank, recall_chunk=3)
+    kp, vp, q, kl, vl = c.k_pages, c.v_pages, c.q, c.k_loc, c.v_loc
+    pcur, pch = c.prompt_cur, c.prompt_chunks
+    peaked = (0, 3, 6, 9)
+    for i, h in enumerate(peaked):
+        u = synth.normal((D,), synth.seed_of("hsa", rank, "dir", h), dev).to(torch.bfloat16)
+        blk = 37 + 11 * i
+        kp[:, blk * 128:(blk + 1) * 128, h, :] += 3.0 * u
+        q[:, h, :] += 3.0 * u
+    kbar = torch.empty((N_PAGES, H, D), dtype=torch.float32, device=dev)
+    idx = torch.empty(KP, dtype=torch.int32, device=dev)
+    kbuf = torch.empty((KP * P, H, D), dtype=torch.bfloat16, device=dev)
+    vbuf = torch.empty_like(kbuf)
+    o = torch.empty(q.shape, dtype=torch.float32, device=dev)
+    nqb, nmb, nlb = -(-NQ // 64), KP * P // 128, -(-NLOC // 64)
+    qbar = torch.empty((nqb, H, D), dtype=torch.float32, device=dev)
+    kbb = torch.empty((nmb + nlb, H, D), dtype=torch.float32, device=dev)
+    sel = torch.empty((H, nmb + nlb), dtype=torch.int32, device=dev)
+    cnt = torch.empty(H, dtype=torch.int32, device=dev)
+    gini = torch.empty(H, dtype=torch.float32, device=dev)
+    L, RANK = KP * P + NLOC, 256
+    ek = synth.normal((H, L, RANK), synth.seed_of("hybrid", "ek"), dev, torch.bfloat16, std=L ** -0.5)
+    ev = synth.normal((H, L, RANK), synth.seed_of("hybrid", "ev"), dev, torch.bfloat16, std=L ** -0.5)
+    stream = torch.cuda.current_stream()
+    names = ("summarize", "select", "gather", "block_means", "block_select", "sparse_attention",
+             "linear")
+
+    def step(marks=None):
+        def mark(i):
+            if marks is not None:
+                marks[i].record(stream)
+        mark(0)
+        wa.wa_page_summarize(kp, kbar)
+        mark(1)
+        wa.wa_select_pages(q, kbar, pcur, pch, PPC, KP, idx)
+        mark(2)
+        wa.wa_gather_pages(kp, vp, idx, None, kbuf, vbuf)
+        mark(3)
+        wa.wa_block_means(q, 64, qbar)
+        wa.wa_block_means(kbuf, 128, kbb[:nmb])
+        wa.wa_block_means(kl, 64, kbb[nmb:])
+        mark(4)
+        wa.wa_sparse_select(qbar, kbb, sel, cnt, gini_out=gini)
+        mark(5)
+        wa.wa_sparse_attn(q, kbuf, vbuf, kl, vl, sel, cnt, o, 128, 64)
+        mark(6)
+        wa.wa_linear_branch(q, kbuf, vbuf, kl, vl, ek, ev, o)
+        mark(7)
+
+    for _ in range(args.warmup):
+        step()
+    wa.wa_check()
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(len(names) + 1)]
+           for _ in range(args.steps)]
+    barrier(world)
+    torch.cuda.synchronize()
+    with Clocks(local) as clk:
+        t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        t0.record(stream)
+        for k in range(args.steps):
+            step(evs[k])
+        t1.record(stream)
+        torch.cuda.synchronize()
+    barrier(world)
+    wa.wa_check()
+    ms = max_over_ranks(t0.elapsed_time(t1), world) / args.steps
+    per = {n: statistics.mean(evs[k][i].elapsed_time(evs[k][i + 1]) for k in range(args.steps))
+           for i, n in enumerate(names)}
+    counts = cnt.cpu().tolist()
+    selc = sel.cpu()
+    kept_keys = []
+    for h in range(H):
+        blocks = selc[h, :counts[h]].tolist()
+        kept_keys.append(sum(128 if b < nmb else min(64, NLOC - 64 * (b - nmb)) for b in blocks))
+    sparse_flops = 4.0 * NQ * D * sum(kept_keys)
+    dense_flops = attn_flops(NQ, KP * P + NLOC, D, H)
+    hbm, tf_burst, tf_sus, src = peaks()
+    sp_tflops = sparse_flops / (per["sparse_attention"] * 1e-3) / 1e12
+    return {
+        "metric": METRIC, "value": round(world * dense_flops / (ms * 1e-3) / 1e12, 2),
+        "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(ms, 4), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic (planted peaked heads 0, 3, 6, 9)",
+        "config": {"workload": "hsa: " + WORKLOAD + " with the HSA branches: sparse (blocks 128 "
+                               "buffer / 64 local / 64 query, tau_h = 1 - Gini) + Linformer "
+                               "rank 256, equal-weight fusion",
+                   "value_is": "dense-equivalent attention FLOPs of the chunk / whole-step time"},
+        "kernels_ms": {k: round(v, 4) for k, v in per.items()},
+        "kept_blocks": counts, "n_blocks": nmb + nlb,
+        "kept_key_fraction": round(sum(kept_keys) / (H * (KP * P + NLOC)), 4),
+        "gini": [round(x, 4) for x in gini.cpu().tolist()],
+        "sparse_attn_tflops": round(sp_tflops, 1),
+        "roofline": {"bound": "tensor", "achieved": round(sp_tflops, 1), "peak": tf_sus,
+                     "unit": "TFLOP/s", "frac": round(sp_tflops / tf_sus, 4), "traffic": None,
+                     "kernel": "k_block_attn_tc (block-sparse form)",
+                     "peak_source": f"{src} bf16 sustained"},
+        "gpu_launches": 12 * args.steps, "clocks": clk.summary(),
+    }
+
+
 def run_one_kernel(args, local):
     """One kernel alone at the workload's shape (inputs drawn directly, no page
     bank): the attention over a 49,920-token buffer + 4,680 local tokens, or
@@ -587,9 +706,10 @@ def main():
     ap.add_argument("--kernel", default="all", choices=["all", "attention", "gather", "linear"],
                     help="time one kernel alone on its own inputs (for profiling)")
     ap.add_argument("--workload", default="worldattention",
-                    choices=["worldattention", "denoise", "hybrid", "stress"],
+                    choices=["worldattention", "denoise", "hybrid", "hsa", "stress"],
                     help="worldattention: the headline one-layer chunk; denoise: 4 denoising "
                          "steps over a cached 21-frame window; hybrid: + Linformer branch; "
+                         "hsa: sparse + Linformer branches in place of dense attention; "
                          "stress: 30 layers with pages in pinned host memory")
     ap.add_argument("--layers", type=int, default=30, help="stress workload: layers")
     args = ap.parse_args()
@@ -603,6 +723,8 @@ def main():
         line = run_denoise(args, world, rank, local)
     elif args.workload == "hybrid":
         line = run_gpu(args, world, rank, local, hybrid=True)
+    elif args.workload == "hsa":
+        line = run_hsa(args, world, rank, local)
     elif args.workload == "stress":
         line = run_stress(args, world, rank, local)
     else:

@@ -262,7 +262,8 @@ wa_status wa_block_means(const void* x, wa_dtype dt, int n_rows, int block, int 
  * gini_out  : device float32 [n_heads] or NULL; mass_out : device float32
  *             [n_heads][n_kb] or NULL.
  * scale <= 0 means 1/sqrt(head_dim).  Deterministic (fixed-order sums).
- * Needs n_qb <= 128 and head_dim <= 256; else WA_ERR_SHAPE.
+ * Needs n_qb <= 4096 and head_dim <= 256, a multiple of 4 (else WA_ERR_SHAPE),
+ * and 16-byte aligned qbar, kbar (else WA_ERR_ALIGN).
  */
 wa_status wa_sparse_select(const float* qbar, int n_qb, const float* kbar, int n_kb, int n_heads,
                            int head_dim, float scale, const float* tau, int32_t* sel_out,
@@ -282,7 +283,9 @@ wa_status wa_sparse_select(const float* qbar, int n_qb, const float* kbar, int n
  *             [n_heads] as written by wa_sparse_select.  A head with count 0
  *             gets O = 0 and LSE = -inf; indices must be valid block numbers
  *             (the kernel does not check them).
- * block_main, block_loc : 1 .. 128.
+ * block_main, block_loc : 1 .. 128; at most 12,000 blocks in all.
+ * Adjacent kept blocks of one segment are processed as one key tile of up to
+ * 128 rows (two 64-token local blocks share a tile).
  * Other arguments as for wa_block_attn; WA_BF16 only, head_dim == 128.
  */
 wa_status wa_sparse_attn(const void* q, int n_q, const void* k_main, const void* v_main, int n_main,

@@ -108,12 +108,12 @@ struct Params {
   float* part_o;             // [unit][split][256][128] unnormalised O (split > 1)
   float4* part_ml;           // [unit][split][256] (m, l, l_exact, -)
   unsigned* counters;        // [unit] tickets, zero between launches
-  // block-sparse form (sel != NULL): head h attends to key blocks
-  // sel[h][0 .. count[h]), each a block of b_main buffer rows (index < nb_main)
-  // or of b_loc local rows; dense form: 128-key tiles over [main ; local]
-  const int32_t* sel;
-  const int32_t* sel_count;
-  int sel_stride, nb_main, b_main, b_loc;
+  // block-sparse form: head h attends to key tiles tiles[h][0 .. tile_count[h]),
+  // each {segment << 30 | first row, rows (<= 128)}; dense form: 128-key tiles
+  // over [main ; local]
+  const int2* tiles;
+  const int32_t* tile_count;
+  int tile_stride;
 };
 
 // Key tile j of head h: segment (0 = buffer, 1 = local), first row, valid rows.
@@ -123,10 +123,8 @@ struct TileRef {
 template <bool kSparse>
 __device__ __forceinline__ TileRef tile_ref(const Params& p, int head, int j) {
   if (kSparse) {
-    const int b = __ldg(p.sel + (size_t)head * p.sel_stride + j);
-    if (b < p.nb_main) return {0, b * p.b_main, min(p.b_main, p.n_main - b * p.b_main)};
-    const int r = (b - p.nb_main) * p.b_loc;
-    return {1, r, min(p.b_loc, p.n_loc - r)};
+    const int2 t = __ldg(p.tiles + (size_t)head * p.tile_stride + j);
+    return {t.x >> 30, t.x & ((1 << 30) - 1), t.y};
   }
   if (j < p.nt_main) return {0, j * BN, min(BN, p.n_main - j * BN)};
   const int r = (j - p.nt_main) * BN;
@@ -197,7 +195,7 @@ k_block_attn_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
   const int split = blockIdx.x % p.n_split;
   const int q0 = qpair * (2 * BM);
   int jb, je;
-  const int nkv = kSparse ? __ldg(p.sel_count + head) : p.nt_main + p.nt_loc;
+  const int nkv = kSparse ? __ldg(p.tile_count + head) : p.nt_main + p.nt_loc;
   split_range(nkv, p.n_split, split, jb, je);
   const int nloc = je - jb;                 // key tiles of this CTA (0 only in the block-sparse form)
   volatile int* abort_flag = &bars->abort_flag;
@@ -538,6 +536,56 @@ k_block_attn_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
   }
 }
 
+// Key tiles of the block-sparse form, one CTA per head.  A segment's blocks
+// of b rows are grouped m = floor(128 / b) to a tile by block number (blocks
+// m t .. m t + m - 1 of the segment); kept blocks of one group that follow
+// each other share a tile, others get tiles of their own.  Entry i of the
+// head's kept list starts a tile unless it continues the previous entry:
+// same group, block number one higher.  Tile k starts at the k-th starting
+// entry (an exclusive scan of the start flags, fixed order).
+__global__ void __launch_bounds__(128)
+k_sparse_tiles(const int32_t* __restrict__ sel, const int32_t* __restrict__ count, int stride,
+               int nb_main, int b_main, int b_loc, int n_main, int n_loc, int2* __restrict__ tiles,
+               int32_t* __restrict__ tile_count) {
+  extern __shared__ int32_t blk[];             // [stride] kept blocks, then [128] partial counts
+  int32_t* part = blk + stride;
+  const int h = blockIdx.x;
+  const int n = min(max(__ldg(count + h), 0), stride);
+  for (int i = threadIdx.x; i < n; i += blockDim.x) blk[i] = __ldg(sel + (size_t)h * stride + i);
+  __syncthreads();
+  const int m_main = max(1, BN / b_main), m_loc = max(1, BN / b_loc);
+  auto group_of = [&](int b) {
+    return b < nb_main ? b / m_main : (1 << 29) + (b - nb_main) / m_loc;
+  };
+  auto starts = [&](int i) {
+    if (i == 0) return true;
+    const int b = blk[i], pb = blk[i - 1];
+    return !(pb == b - 1 && group_of(pb) == group_of(b));
+  };
+  // each thread takes a contiguous chunk of the list
+  const int chunk = (n + blockDim.x - 1) / blockDim.x;
+  const int i0 = min(n, (int)threadIdx.x * chunk), i1 = min(n, i0 + chunk);
+  int mine = 0;
+  for (int i = i0; i < i1; ++i) mine += starts(i) ? 1 : 0;
+  part[threadIdx.x] = mine;
+  __syncthreads();
+  int t = 0;   // exclusive prefix over the threads before this one, in order
+  for (int k = 0; k < (int)threadIdx.x; ++k) t += part[k];
+  int2* out = tiles + (size_t)h * stride;
+  for (int i = i0; i < i1; ++i) {
+    if (!starts(i)) continue;
+    const int b = blk[i];
+    int e = i;
+    while (e + 1 < n && !starts(e + 1)) ++e;       // the tile's last kept block
+    const int sg = b < nb_main ? 0 : 1;
+    const int r0 = sg == 0 ? b * b_main : (b - nb_main) * b_loc;
+    const int be = blk[e];
+    const int r_end = sg == 0 ? min(n_main, (be + 1) * b_main) : min(n_loc, (be - nb_main + 1) * b_loc);
+    out[t++] = make_int2((sg << 30) | r0, r_end - r0);
+  }
+  if (threadIdx.x == blockDim.x - 1) tile_count[h] = t;
+}
+
 // Split count: fewest whole waves of the SMs per unit of work; a split adds a
 // small combine cost, so ties keep the smaller count.
 int choose_split(int units, int nkv, int sms) {
@@ -607,12 +655,9 @@ wa_status launch_attn_tc(const void* q, int n_q, const void* k_main, const void*
   p.nt_main = (n_main + BN - 1) / BN;
   p.nt_loc = (n_loc + BN - 1) / BN;
   p.n_qpairs = (n_q + 2 * BM - 1) / (2 * BM);
-  p.sel = sparse ? sparse->sel : nullptr;
-  p.sel_count = sparse ? sparse->count : nullptr;
-  p.sel_stride = sparse ? sparse->stride : 0;
-  p.b_main = sparse ? sparse->b_main : BN;
-  p.b_loc = sparse ? sparse->b_loc : BN;
-  p.nb_main = sparse ? (n_main + p.b_main - 1) / p.b_main : p.nt_main;
+  p.tiles = nullptr;
+  p.tile_count = nullptr;
+  p.tile_stride = sparse ? sparse->stride : 0;
   // the block-sparse form sizes its splits for every block kept (the counts
   // live on the device); CTAs whose share is empty finish at once
   const int nkv_max = sparse ? sparse->stride : p.nt_main + p.nt_loc;
@@ -640,13 +685,30 @@ wa_status launch_attn_tc(const void* q, int n_q, const void* k_main, const void*
   p.counters = nullptr;
   Scratch sc;
   const size_t units = (size_t)p.n_qpairs * n_heads;
+  // scratch: [tiles (block-sparse form)][split partials]
+  const size_t tile_bytes =
+      sparse ? (((size_t)n_heads * p.tile_stride * sizeof(int2) + n_heads * sizeof(int32_t)) + 255) &
+                   ~(size_t)255
+             : 0;
   const size_t part_o_bytes = p.n_split > 1 ? units * p.n_split * 256 * HD * sizeof(float) : 0;
   const size_t part_ml_bytes = p.n_split > 1 ? units * p.n_split * 256 * sizeof(float4) : 0;
-  if ((rc = get_scratch(part_o_bytes + part_ml_bytes, &sc)) != WA_OK) return rc;
+  if ((rc = get_scratch(tile_bytes + part_o_bytes + part_ml_bytes, &sc)) != WA_OK) return rc;
   p.status = &sc.ctrl->status;
+  char* base = static_cast<char*>(sc.data);
+  if (sparse) {
+    int2* tiles = reinterpret_cast<int2*>(base);
+    int32_t* tcount = reinterpret_cast<int32_t*>(tiles + (size_t)n_heads * p.tile_stride);
+    const int nb_main = (n_main + sparse->b_main - 1) / sparse->b_main;
+    k_sparse_tiles<<<n_heads, 128, (p.tile_stride + 128) * sizeof(int32_t), s>>>(
+        sparse->sel, sparse->count, p.tile_stride, nb_main, sparse->b_main, sparse->b_loc, n_main,
+        n_loc, tiles, tcount);
+    if ((rc = cuda_status(cudaPeekAtLastError())) != WA_OK) return rc;
+    p.tiles = tiles;
+    p.tile_count = tcount;
+  }
   if (p.n_split > 1) {
-    p.part_o = static_cast<float*>(sc.data);
-    p.part_ml = reinterpret_cast<float4*>(static_cast<char*>(sc.data) + part_o_bytes);
+    p.part_o = reinterpret_cast<float*>(base + tile_bytes);
+    p.part_ml = reinterpret_cast<float4*>(base + tile_bytes + part_o_bytes);
     p.counters = sc.ctrl->attn_counters;
   }
   const bool want_lse = lse != nullptr;

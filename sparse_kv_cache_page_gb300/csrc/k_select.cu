@@ -390,7 +390,7 @@ wa_status summarize_t(const T* pages, int n_pages, int page_tokens, int n_rows, 
   // 0.227 ms with two waves of 384-thread CTAs, 0.267 ms with four).
   int splits = 2 * kTargetCtas / n_pages;
   if (splits < 1) splits = 1;
-  const int max_splits = (page_tokens + 63) / 64;   // at least 64 rows per CTA
+  const int max_splits = (page_tokens + 15) / 16;   // at least 16 rows per CTA
   if (splits > max_splits) splits = max_splits;
   if (splits > 256) splits = 256;
   const int rps = (page_tokens + splits - 1) / splits;

@@ -4,11 +4,9 @@
 // Gini coefficient of that mass, and the minimal set of blocks whose
 // cumulative mass reaches the head's threshold.
 //
-// k_pooled_scores  S[h][qb][kb] = scale * Qbar_qb,h . Kbar_kb,h.  Grid (key
-//                  block chunks of 64, heads); the head's query-block means
-//                  and a chunk of key-block means staged in shared memory
-//                  (rows padded to d+1 floats: conflict-free); a thread owns
-//                  one key block and every fourth query block.
+// k_pooled_scores  S[h][qb][kb] = scale * Qbar_qb,h . Kbar_kb,h: one thread per
+//                  (query block, key block) in 32 x 32 tiles, rows staged in
+//                  shared memory.
 // k_sparse_select  one CTA per head:
 //   1. each query-block row's max and exp-sum (a warp per row, fixed order);
 //   2. mass[kb] = mean over query blocks of the row-normalised exp (fixed order);
@@ -27,10 +25,8 @@
 namespace wa {
 namespace {
 
-constexpr int kScoreThreads = 256;
-constexpr int kKbChunk = 64;             // key blocks per scores CTA
-constexpr int kQbGroups = kScoreThreads / kKbChunk;
-constexpr int kMaxQbPerThread = 32;      // n_qb <= 128
+constexpr int kScoreThreads = 1024;     // 32 query blocks x 32 key blocks per CTA
+constexpr int kMaxQb = 4096;
 constexpr int kSelThreads = 1024;
 
 __device__ __forceinline__ float warp_sum(float v) {
@@ -47,37 +43,41 @@ __device__ __forceinline__ float warp_max(float v) {
 __global__ void __launch_bounds__(kScoreThreads)
 k_pooled_scores(const float* __restrict__ qbar, int n_qb, const float* __restrict__ kbar, int n_kb,
                 int n_heads, int d, float scale, float* __restrict__ scores) {
-  extern __shared__ float sm[];
-  const int h = blockIdx.y;
-  const int kb0 = blockIdx.x * kKbChunk;
-  const int nk = min(kKbChunk, n_kb - kb0);
-  const int dp = d + 1;
-  float* q_s = sm;                         // [n_qb][d]
-  float* k_s = sm + (size_t)n_qb * d;      // [kKbChunk][d + 1]
-  for (int i = threadIdx.x; i < n_qb * d; i += blockDim.x)
-    q_s[i] = qbar[((size_t)(i / d) * n_heads + h) * d + (i % d)];
-  for (int i = threadIdx.x; i < nk * d; i += blockDim.x)
-    k_s[(i / d) * dp + (i % d)] = kbar[((size_t)(kb0 + i / d) * n_heads + h) * d + (i % d)];
+  // CTA: 32 query blocks x 32 key blocks of one head; warp w = query block
+  // qb0 + w, lane = key block kb0 + lane; rows staged in shared memory with
+  // a 4-float pad (16-byte reads of 8 lanes hit distinct banks)
+  extern __shared__ __align__(16) float sm[];
+  const int h = blockIdx.z;
+  const int kb0 = blockIdx.x * 32, qb0 = blockIdx.y * 32;
+  const int dp = d + 4;
+  float* q_s = sm;                // [32][d + 4]
+  float* k_s = sm + 32 * dp;      // [32][d + 4]
+  const int d4 = d / 4;
+  for (int i = threadIdx.x; i < 32 * d4; i += blockDim.x) {
+    const int r = i / d4, c = (i % d4) * 4;
+    const int qb = qb0 + r, kb = kb0 + r;
+    const float4 zq = qb < n_qb ? *reinterpret_cast<const float4*>(qbar + ((size_t)qb * n_heads + h) * d + c)
+                                : make_float4(0.f, 0.f, 0.f, 0.f);
+    const float4 zk = kb < n_kb ? *reinterpret_cast<const float4*>(kbar + ((size_t)kb * n_heads + h) * d + c)
+                                : make_float4(0.f, 0.f, 0.f, 0.f);
+    *reinterpret_cast<float4*>(q_s + r * dp + c) = zq;
+    *reinterpret_cast<float4*>(k_s + r * dp + c) = zk;
+  }
   __syncthreads();
-  const int kl = threadIdx.x % kKbChunk, g = threadIdx.x / kKbChunk;
-  if (kl >= nk) return;
-  float acc[kMaxQbPerThread];
-#pragma unroll
-  for (int i = 0; i < kMaxQbPerThread; ++i) acc[i] = 0.f;
-  const float* kr = k_s + kl * dp;
-  for (int e = 0; e < d; ++e) {
-    const float kv = kr[e];
-#pragma unroll
-    for (int i = 0; i < kMaxQbPerThread; ++i) {
-      const int qb = g + kQbGroups * i;
-      if (qb < n_qb) acc[i] = fmaf(q_s[qb * d + e], kv, acc[i]);
-    }
+  const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int qb = qb0 + w, kb = kb0 + lane;
+  const float4* qr = reinterpret_cast<const float4*>(q_s + w * dp);
+  const float4* kr = reinterpret_cast<const float4*>(k_s + lane * dp);
+  float acc0 = 0.f, acc1 = 0.f;
+#pragma unroll 8
+  for (int e = 0; e < d4; ++e) {
+    const float4 a = qr[e], b = kr[e];
+    acc0 = fmaf(a.x, b.x, acc0);
+    acc1 = fmaf(a.y, b.y, acc1);
+    acc0 = fmaf(a.z, b.z, acc0);
+    acc1 = fmaf(a.w, b.w, acc1);
   }
-#pragma unroll
-  for (int i = 0; i < kMaxQbPerThread; ++i) {
-    const int qb = g + kQbGroups * i;
-    if (qb < n_qb) scores[((size_t)h * n_qb + qb) * n_kb + kb0 + kl] = acc[i] * scale;
-  }
+  if (qb < n_qb && kb < n_kb) scores[((size_t)h * n_qb + qb) * n_kb + kb] = (acc0 + acc1) * scale;
 }
 
 // Ascending bitonic sort of n2 (power of two) keys in shared memory.
@@ -120,6 +120,7 @@ __device__ float block_sum(float v, float* red) {
   return warp_sum(lane < nwarps ? red[lane] : 0.f);
 }
 
+template <bool kStage>
 __global__ void __launch_bounds__(kSelThreads)
 k_sparse_select(const float* __restrict__ scores, int n_qb, int n_kb, const float* __restrict__ tau,
                 int32_t* __restrict__ sel, int32_t* __restrict__ count, float* __restrict__ gini_out,
@@ -135,6 +136,18 @@ k_sparse_select(const float* __restrict__ scores, int n_qb, int n_kb, const floa
   float* row_max = red + 32;                                                   // [n_qb]
   float* row_inv = row_max + n_qb;                                             // [n_qb]
   const float* sh = scores + (size_t)h * n_qb * n_kb;
+  if (kStage) {
+    // the head's score slab in shared memory (n_qb * n_kb floats, 16-byte chunks)
+    const int off = 5 * n2 + 32 + 2 * n_qb;                 // floats before the slab
+    float* stage = reinterpret_cast<float*>(smem_raw) + off + ((4 - (off & 3)) & 3);
+    const int n = n_qb * n_kb;
+    const float4* src4 = reinterpret_cast<const float4*>(sh);
+    float4* dst4 = reinterpret_cast<float4*>(stage);
+    for (int i = tid; i < n / 4; i += blockDim.x) dst4[i] = __ldg(src4 + i);
+    for (int i = (n / 4) * 4 + tid; i < n; i += blockDim.x) stage[i] = __ldg(sh + i);
+    __syncthreads();
+    sh = stage;
+  }
   // 1. per query-block row: max and 1 / sum of exp
   for (int qb = warp; qb < n_qb; qb += nwarps) {
     const float* row = sh + (size_t)qb * n_kb;
@@ -154,8 +167,10 @@ k_sparse_select(const float* __restrict__ scores, int n_qb, int n_kb, const floa
   const float inv_q = 1.0f / (float)n_qb;
   for (int kb = tid; kb < n2; kb += blockDim.x) {
     float acc = 0.f;
-    if (kb < n_kb)
+    if (kb < n_kb) {
+#pragma unroll 8
       for (int qb = 0; qb < n_qb; ++qb) acc += expf(sh[(size_t)qb * n_kb + kb] - row_max[qb]) * row_inv[qb];
+    }
     mass[kb] = kb < n_kb ? acc * inv_q : 0.f;
     keys[kb] = kb < n_kb ? ((unsigned long long)__float_as_uint(mass[kb]) << 32) | (unsigned)kb
                          : ~0ull;
@@ -220,35 +235,45 @@ wa_status launch_sparse_select(const float* qbar, int n_qb, const float* kbar, i
   wa_status rc = get_scratch(score_bytes, &sc);
   if (rc != WA_OK) return rc;
   float* scores = static_cast<float*>(sc.data);
-  const size_t smem1 = ((size_t)n_qb * head_dim + (size_t)kKbChunk * (head_dim + 1)) * sizeof(float);
+  const size_t smem1 = (size_t)64 * (head_dim + 4) * sizeof(float);
   static bool attr_done[64] = {};
   int dev = 0;
   cudaGetDevice(&dev);
   int n2 = 1;
   while (n2 < n_kb) n2 <<= 1;
   const size_t smem2 = (size_t)n2 * 8 + (size_t)3 * n2 * 4 + 32 * 4 + (size_t)2 * n_qb * 4;
+  // the score slab goes to shared memory when it fits (scores are in the scratch arena, so
+  // the slab offset of every head keeps 16-byte alignment when n_qb * n_kb % 4 == 0)
+  const size_t slab = (size_t)n_qb * n_kb * sizeof(float) + 16;
+  const bool stage = smem2 + slab <= 220 * 1024 && ((size_t)n_qb * n_kb) % 4 == 0;
   if (dev < 64 && !attr_done[dev]) {
     if (cudaFuncSetAttribute(k_pooled_scores, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              227 * 1024) != cudaSuccess ||
-        cudaFuncSetAttribute(k_sparse_select, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        cudaFuncSetAttribute(k_sparse_select<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             227 * 1024) != cudaSuccess ||
+        cudaFuncSetAttribute(k_sparse_select<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              227 * 1024) != cudaSuccess)
       return WA_ERR_CUDA;
     attr_done[dev] = true;
   }
-  dim3 g1((n_kb + kKbChunk - 1) / kKbChunk, n_heads);
+  dim3 g1((n_kb + 31) / 32, (n_qb + 31) / 32, n_heads);
   k_pooled_scores<<<g1, kScoreThreads, smem1, s>>>(qbar, n_qb, kbar, n_kb, n_heads, head_dim, scale,
                                                     scores);
-  k_sparse_select<<<n_heads, kSelThreads, smem2, s>>>(scores, n_qb, n_kb, tau, sel_out, count_out,
-                                                      gini_out, mass_out, n2);
+  if (stage)
+    k_sparse_select<true><<<n_heads, kSelThreads, smem2 + slab, s>>>(
+        scores, n_qb, n_kb, tau, sel_out, count_out, gini_out, mass_out, n2);
+  else
+    k_sparse_select<false><<<n_heads, kSelThreads, smem2, s>>>(
+        scores, n_qb, n_kb, tau, sel_out, count_out, gini_out, mass_out, n2);
   return cuda_status(cudaPeekAtLastError());
 }
 
 // Limits the host checks before launch_sparse_select.
-int sparse_select_max_qb() { return kQbGroups * kMaxQbPerThread; }
+int sparse_select_max_qb() { return kMaxQb; }
 size_t sparse_select_smem(int n_qb, int n_kb, int head_dim) {
   int n2 = 1;
   while (n2 < n_kb) n2 <<= 1;
-  const size_t s1 = ((size_t)n_qb * head_dim + (size_t)kKbChunk * (head_dim + 1)) * sizeof(float);
+  const size_t s1 = (size_t)64 * (head_dim + 4) * sizeof(float);
   const size_t s2 = (size_t)n2 * 8 + (size_t)3 * n2 * 4 + 32 * 4 + (size_t)2 * n_qb * 4;
   return s1 > s2 ? s1 : s2;
 }

@@ -263,7 +263,9 @@ wa_status wa_sparse_select(const float* qbar, int n_qb, const float* kbar, int n
   if (!qbar || !kbar || !sel_out || !count_out || n_qb <= 0 || n_kb <= 0 || n_heads <= 0 ||
       head_dim <= 0)
     return WA_ERR_INVALID_ARG;
-  if (head_dim > 256 || n_qb > sparse_select_max_qb() || n_kb > (1 << 20)) return WA_ERR_SHAPE;
+  if (head_dim > 256 || head_dim % 4 != 0 || n_qb > sparse_select_max_qb() || n_kb > (1 << 20))
+    return WA_ERR_SHAPE;
+  if (!aligned16(qbar) || !aligned16(kbar)) return WA_ERR_ALIGN;
   if (sparse_select_smem(n_qb, n_kb, head_dim) > 227 * 1024) return WA_ERR_SHAPE;
   if (!(scale > 0.0f)) scale = 1.0f / sqrtf((float)head_dim);
   return launch_sparse_select(qbar, n_qb, kbar, n_kb, n_heads, head_dim, scale, tau, sel_out,
@@ -282,6 +284,9 @@ wa_status wa_sparse_attn(const void* q, int n_q, const void* k_main, const void*
   if (n_main > 0 && (!k_main || !v_main)) return WA_ERR_INVALID_ARG;
   if (n_loc > 0 && (!k_loc || !v_loc)) return WA_ERR_INVALID_ARG;
   if (block_main < 1 || block_main > 128 || block_loc < 1 || block_loc > 128) return WA_ERR_SHAPE;
+  if ((n_main + (long long)block_main - 1) / block_main +
+          (n_loc + (long long)block_loc - 1) / block_loc > 12000)
+    return WA_ERR_SHAPE;
   if (head_dim != 128 || n_heads <= 0 || (long long)n_heads * 128 > 16384) return WA_ERR_SHAPE;
   if (!aligned16(q) || !aligned16(o) || (n_main > 0 && (!aligned16(k_main) || !aligned16(v_main))) ||
       (n_loc > 0 && (!aligned16(k_loc) || !aligned16(v_loc))))
