@@ -40,6 +40,11 @@ design notes):
   with E rows aligned to [gathered buffer ; local KV].
 * The gate equation is missing on the page; fused output is
   O = w_attn[h] * O_attn + w_lin[h] * O_lin, default weights 1 and 1.
+* Per-head page selection (the per-head variant of the page stage): the
+  prompt stage is shared; head h scores pages on its own slice,
+  alpha_{j,h} = Qbar_h . Kbar_{j,h} / sqrt(d_k), keeps its own top-K_p (same
+  tie rule, ascending), and the buffer keeps the token-major layout with head
+  h's slice taken from head h's pages.
 * HSA sparse branch ([WA] HSA section and its appendix notes): key blocks of
   B_inter = 128 tokens over the retrieved buffer and B_intra = 64 over the
   chunk's own tokens (a ragged last block keeps its own size); query blocks of
@@ -88,6 +93,9 @@ __all__ = [
     "gini",
     "sparse_select",
     "sparse_attn",
+    "page_scores_per_head",
+    "select_pages_per_head",
+    "gather_pages_per_head",
 ]
 
 
@@ -417,4 +425,49 @@ def sparse_attn(q, k_main, v_main, k_loc, v_loc, sel, scale: float | None = None
             vs.append(as_f64(src_v[a:e, h, :]))
         oh, _, _ = attention_rows(qq[rows, h, :], np.concatenate(ks), np.concatenate(vs), scale)
         out[:, h, :] = oh
+    return out
+
+
+# ----------------------------------------------------------------------------
+# [WA] HKV page stage, one page set per head
+# ----------------------------------------------------------------------------
+
+def page_scores_per_head(qbar: np.ndarray, kbar: np.ndarray, pages, head_dim: int) -> np.ndarray:
+    """alpha[h][c] = Qbar_h . Kbar_{j_c,h} / sqrt(d_k) for the candidates j_c."""
+    qb = as_f64(qbar)
+    kb = as_f64(kbar)
+    return np.array([[float(np.dot(qb[h], kb[j, h])) / math.sqrt(head_dim) for j in pages]
+                     for h in range(qb.shape[0])], dtype=np.float64)
+
+
+def select_pages_per_head(q, kbar, prompt_cur, prompt_chunks, pages_per_chunk: int, k_p: int):
+    """Shared prompt stage, then each head's top-K_p candidates by its own
+    score (ties to the lowest page index, ascending).  Returns (idx [H][k_p],
+    alpha_of_idx [H][k_p], chunk)."""
+    kb = as_f64(kbar)
+    n_pages, n_h, d = kb.shape
+    qbar = mean_query(q)
+    if prompt_chunks is None or len(prompt_chunks) == 0:
+        chunk = -1
+    else:
+        chunk = prompt_top1(prompt_cur, prompt_chunks)
+    cand = candidate_pages(n_pages, chunk, pages_per_chunk)
+    alpha = page_scores_per_head(qbar, kb, cand, d)
+    idx = np.empty((n_h, k_p), dtype=np.int32)
+    sc = np.empty((n_h, k_p), dtype=np.float64)
+    for h in range(n_h):
+        idx[h], sc[h] = topk_pages(alpha[h], cand, k_p)
+    return idx, sc, chunk
+
+
+def gather_pages_per_head(pages: np.ndarray, idx) -> np.ndarray:
+    """buf[s*P + t][h] = pages[idx[h][s]][t][h]: a byte copy per head slice."""
+    pg = np.asarray(pages)
+    idx = np.asarray(idx)
+    n_h, k_p = idx.shape
+    p_tok = pg.shape[1]
+    out = np.empty((k_p * p_tok,) + pg.shape[2:], dtype=pg.dtype)
+    for h in range(n_h):
+        for s_ in range(k_p):
+            out[s_ * p_tok:(s_ + 1) * p_tok, h] = pg[int(idx[h, s_]), :, h]
     return out

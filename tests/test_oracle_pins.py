@@ -337,3 +337,60 @@ def test_planted_mistakes_are_caught(monkeypatch, golden_dir):
     monkeypatch.setattr(O, "topk_pages", _mutant_topk)
     with pytest.raises(AssertionError):
         test_topk_ties_lowest_index()
+
+
+# ----------------------------------------------------------------------------
+# per-head page sets
+# ----------------------------------------------------------------------------
+
+def test_per_head_scores_bruteforce_and_sum():
+    """alpha[h][j] is the mean over (query, key) pairs of head h of q.k/sqrt(d),
+    pair by pair; summed over heads it is the shared page score."""
+    n_pages, P, n_q, H, d = 5, 6, 4, 3, 8
+    kp = _rand((n_pages, P, H, d), 51)
+    q = _rand((n_q, H, d), 52)
+    qb, kb = O.mean_query(q), O.page_summarize(kp)
+    a = O.page_scores_per_head(qb, kb, range(n_pages), d)
+    for h in range(H):
+        for j in range(n_pages):
+            brute = sum(float(np.dot(q[i, h], kp[j, t, h])) for i in range(n_q)
+                        for t in range(P)) / (n_q * P * math.sqrt(d))
+            assert abs(a[h, j] - brute) <= 1e-12 * max(1.0, abs(brute))
+    np.testing.assert_allclose(a.sum(axis=0), O.page_scores(qb, kb, range(n_pages), d),
+                               rtol=1e-12, atol=1e-14)
+
+
+def test_per_head_selection_one_head_is_shared_selection():
+    kp = _rand((12, 7, 1, 16), 53)
+    q = _rand((9, 1, 16), 54)
+    kb = O.page_summarize(kp)
+    pc, cur = _rand((3, 10), 55), _rand((10,), 56)
+    idx_h, sc_h, ch_h = O.select_pages_per_head(q, kb, cur, pc, 4, 2)
+    idx, sc, ch = O.select_pages(q, kb, cur, pc, 4, 2)
+    assert ch_h == ch and idx_h[0].tolist() == idx.tolist()
+    np.testing.assert_allclose(sc_h[0], sc, rtol=1e-15)
+
+
+def test_per_head_topk_bruteforce():
+    """With distinct scores each head's top-k_p set is the unique k_p-subset of
+    largest score sum: checked over all subsets."""
+    kp = _rand((9, 3, 4, 8), 57)
+    q = _rand((5, 4, 8), 58)
+    kb = O.page_summarize(kp)
+    idx, _, _ = O.select_pages_per_head(q, kb, None, None, 1, 3)
+    a = O.page_scores_per_head(O.mean_query(q), kb, range(9), 8)
+    for h in range(4):
+        best = max(itertools.combinations(range(9), 3), key=lambda c: sum(a[h, j] for j in c))
+        assert idx[h].tolist() == sorted(best)
+
+
+def test_per_head_gather_bitexact_and_shared_case():
+    kp = (np.arange(6 * 4 * 3 * 2, dtype=np.uint16).reshape(6, 4, 3, 2) * 7) ^ 0x3f00
+    idx = np.array([[5, 1], [0, 3], [2, 2]], dtype=np.int32)
+    buf = O.gather_pages_per_head(kp, idx)
+    for h in range(3):
+        for s_ in range(2):
+            for t in range(4):
+                assert (buf[s_ * 4 + t, h] == kp[idx[h, s_], t, h]).all()
+    same = np.array([[4, 1]] * 3, dtype=np.int32)
+    assert (O.gather_pages_per_head(kp, same) == O.gather_pages(kp, [4, 1])).all()
