@@ -176,6 +176,41 @@ wa_status wa_gather_pages(const void* k_pages, const void* v_pages, wa_dtype dt,
                           void* k_buf, void* v_buf, wa_stream_t stream);
 
 /*
+ * Per-head page selection (the per-head variant of the page stage, [WA] HKV
+ * stage 2 scored one head at a time): the prompt stage as in
+ * wa_select_pages, then for every head h
+ *
+ *   alpha[h][j] = qbar[h] . kbar[j][h] / sqrt(head_dim)
+ *
+ * and head h's top-k_p candidates (ties to the lower page index), ascending.
+ * idx_out    : device int32 [n_heads][k_p]; scores_out: device float32
+ *              [n_heads][k_p] or NULL; chunk_out: device int32 [1] or NULL.
+ * Other arguments and errors as for wa_select_pages.
+ */
+wa_status wa_select_pages_per_head(const void* q, wa_dtype dt, int n_q, int n_heads, int head_dim,
+                                   const float* kbar, int n_pages, const float* prompt_cur,
+                                   const float* prompt_chunks, int n_chunks, int prompt_dim,
+                                   int pages_per_chunk, int k_p, int32_t* idx_out,
+                                   float* scores_out, int32_t* chunk_out, wa_stream_t stream);
+
+/*
+ * Per-head gather: each head's slice of the contiguous buffer comes from that
+ * head's pages,
+ *
+ *   k_buf[s*page_tokens + t][h][:] = k_pages[idx[h][s]][t][h][:]   (likewise V),
+ *
+ * so the buffer keeps the token-major [k_p*page_tokens][n_heads][head_dim]
+ * layout that wa_block_attn reads.  idx_dev: device int32 [n_heads][k_p].
+ * Device sources only (pages in pinned host memory: WA_ERR_INVALID_ARG); a
+ * head row must be whole 16-byte vectors (WA_ERR_SHAPE).  Bad indices zero
+ * the head's slice of that slot and record WA_ERR_INDEX for wa_check.
+ */
+wa_status wa_gather_pages_per_head(const void* k_pages, const void* v_pages, wa_dtype dt,
+                                   int n_pages, int page_tokens, int n_heads, int head_dim,
+                                   const int32_t* idx_dev, int k_p, void* k_buf, void* v_buf,
+                                   wa_stream_t stream);
+
+/*
  * Block attention of the chunk's queries over the retrieved buffer plus the
  * chunk's own KV ([IX] §3 Step 3; no mask, bidirectional):
  *

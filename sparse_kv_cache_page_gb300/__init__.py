@@ -21,6 +21,8 @@ __all__ = [
     "wa_page_summarize",
     "wa_select_pages",
     "wa_gather_pages",
+    "wa_select_pages_per_head",
+    "wa_gather_pages_per_head",
     "wa_block_attn",
     "wa_linear_branch",
     "wa_block_means",
@@ -41,7 +43,8 @@ WA_F32, WA_BF16 = 0, 1
 EXPORTED_SYMBOLS = ("wa_strerror", "wa_version", "wa_page_summarize", "wa_select_pages",
                     "wa_select_pages_noalloc", "wa_gather_pages", "wa_block_attn",
                     "wa_linear_branch", "wa_block_means", "wa_sparse_select", "wa_sparse_attn",
-                    "wa_check", "wa_shutdown")
+                    "wa_select_pages_per_head", "wa_gather_pages_per_head", "wa_check",
+                    "wa_shutdown")
 
 
 class WaError(RuntimeError):
@@ -70,6 +73,8 @@ def load():
         "wa_page_summarize": (I, [P, I, I, I, I, I, P, P]),
         "wa_select_pages": (I, [P, I, I, I, I, P, I, P, P, I, I, I, I, P, P, P, P]),
         "wa_gather_pages": (I, [P, P, I, I, I, I, I, P, P, I, P, P, P]),
+        "wa_select_pages_per_head": (I, [P, I, I, I, I, P, I, P, P, I, I, I, I, P, P, P, P]),
+        "wa_gather_pages_per_head": (I, [P, P, I, I, I, I, I, P, I, P, P, P]),
         "wa_block_attn": (I, [P, I, P, P, I, P, P, I, I, I, I, F, P, I, P, P]),
         "wa_linear_branch": (I, [P, I, P, P, I, P, P, I, P, P, I, I, I, I, F, P, P, I, P, I, P]),
         "wa_block_means": (I, [P, I, I, I, I, I, P, P]),
@@ -161,6 +166,43 @@ def wa_gather_pages(k_pages: torch.Tensor, v_pages, idx_dev, idx_host, k_buf: to
     _ok("wa_gather_pages", load().wa_gather_pages(
         _ptr(k_pages), _ptr(v_pages), _dt(k_pages), n, p, h, d, _ptr(idx_dev), _ptr(idx_host),
         k_p, _ptr(k_buf), _ptr(v_buf), _stream(stream)))
+
+
+def wa_select_pages_per_head(q: torch.Tensor, kbar: torch.Tensor, prompt_cur, prompt_chunks,
+                             pages_per_chunk: int, k_p: int, idx_out: torch.Tensor,
+                             scores_out=None, chunk_out=None, stream=None):
+    """Prompt-stage top-1 chunk, then a top-k_p page set per head (scored on
+    that head's slice); idx_out int32 [H][k_p], ascending per head."""
+    _need(q.dim() == 3 and q.is_contiguous(), "q must be contiguous [n_q][H][d]")
+    n_q, h, d = q.shape
+    _need(kbar.dim() == 3 and kbar.shape[1:] == (h, d) and kbar.dtype == torch.float32,
+          "kbar must be float32 [n_pages][H][d]")
+    _need(idx_out.dtype == torch.int32 and idx_out.numel() >= h * k_p,
+          "idx_out must be int32 [H][k_p]")
+    n_chunks, pdim = 0, 0
+    if prompt_chunks is not None:
+        n_chunks, pdim = prompt_chunks.shape
+        _need(prompt_cur is not None and prompt_cur.numel() == pdim
+              and prompt_chunks.dtype == torch.float32 and prompt_cur.dtype == torch.float32,
+              "prompt embeddings must be float32")
+    _ok("wa_select_pages_per_head", load().wa_select_pages_per_head(
+        _ptr(q), _dt(q), n_q, h, d, _ptr(kbar), kbar.shape[0], _ptr(prompt_cur),
+        _ptr(prompt_chunks), n_chunks, pdim, pages_per_chunk, k_p, _ptr(idx_out),
+        _ptr(scores_out), _ptr(chunk_out), _stream(stream)))
+
+
+def wa_gather_pages_per_head(k_pages: torch.Tensor, v_pages, idx_dev: torch.Tensor,
+                             k_buf: torch.Tensor, v_buf, stream=None):
+    """k_buf[s*P + t][h] = k_pages[idx_dev[h][s]][t][h] (likewise v); device pages."""
+    _need(k_pages.dim() == 4 and k_pages.is_contiguous(), "k_pages must be contiguous [n][P][H][d]")
+    n, p, h, d = k_pages.shape
+    _need(idx_dev.dim() == 2 and idx_dev.shape[0] == h and idx_dev.dtype == torch.int32,
+          "idx_dev must be int32 [H][k_p]")
+    k_p = idx_dev.shape[1]
+    _need(k_buf.numel() == k_p * p * h * d and k_buf.dtype == k_pages.dtype, "k_buf size/dtype")
+    _ok("wa_gather_pages_per_head", load().wa_gather_pages_per_head(
+        _ptr(k_pages), _ptr(v_pages), _dt(k_pages), n, p, h, d, _ptr(idx_dev), k_p, _ptr(k_buf),
+        _ptr(v_buf), _stream(stream)))
 
 
 def _rows(t):

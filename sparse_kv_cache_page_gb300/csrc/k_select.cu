@@ -237,6 +237,7 @@ struct SelectArgs {
   int32_t* chunk_out;
   Ctrl* ctrl;
   int n_cand_max2;   // power of two >= candidate count
+  int per_head;      // 0: one page set scored over all heads; 1: a page set per head
 };
 
 template <typename T, int VPT>
@@ -326,33 +327,40 @@ k_select_pages(const T* __restrict__ q, SelectArgs a) {
     __syncthreads();
   }
 
-  // stage 2: alpha_j = sum_c qbar[c] * kbar[j][c] / sqrt(d) over the candidates
+  // stage 2: alpha_j = sum_c qbar[c] * kbar[j][c] / sqrt(d) over the candidates,
+  // c over all heads (one page set) or over one head's slice (a set per head)
   const float inv_sqrt_d = 1.0f / sqrtf((float)a.head_dim);
-  for (int c = warp; c < n_cand; c += nwarps) {
-    const float* kb = a.kbar + (size_t)(cand0 + c) * a.row_elems;
-    float dot = 0.f;
-    for (int e = lane; e < a.row_elems; e += 32) dot += qbar[e] * kb[e];
-    dot = warp_sum(dot);
-    if (lane == 0) alpha[c] = dot * inv_sqrt_d;
-  }
-  __syncthreads();
-  int n2 = 1;
-  while (n2 < n_cand) n2 <<= 1;
-  for (int i = tid; i < n2; i += blockDim.x)
-    keys[i] = i < n_cand ? score_key(alpha[i], (unsigned)i) : ~0ull;
-  __syncthreads();
-  bitonic_sort(keys, n2);
-  // the first k_p keys are the selection; re-sort them by candidate index
-  int k2 = 1;
-  while (k2 < a.k_p) k2 <<= 1;
-  for (int i = tid; i < k2; i += blockDim.x)
-    keys[i] = i < a.k_p ? (keys[i] & 0xffffffffull) : ~0ull;
-  __syncthreads();
-  bitonic_sort(keys, k2);
-  for (int i = tid; i < a.k_p; i += blockDim.x) {
-    const int c = (int)(keys[i] & 0xffffffffull);
-    a.idx_out[i] = cand0 + c;
-    if (a.scores_out) a.scores_out[i] = alpha[c];
+  const int n_sets = a.per_head ? a.row_elems / a.head_dim : 1;
+  for (int hs = 0; hs < n_sets; ++hs) {
+    const int e0 = a.per_head ? hs * a.head_dim : 0;
+    const int e1 = a.per_head ? e0 + a.head_dim : a.row_elems;
+    for (int c = warp; c < n_cand; c += nwarps) {
+      const float* kb = a.kbar + (size_t)(cand0 + c) * a.row_elems;
+      float dot = 0.f;
+      for (int e = e0 + lane; e < e1; e += 32) dot += qbar[e] * kb[e];
+      dot = warp_sum(dot);
+      if (lane == 0) alpha[c] = dot * inv_sqrt_d;
+    }
+    __syncthreads();
+    int n2 = 1;
+    while (n2 < n_cand) n2 <<= 1;
+    for (int i = tid; i < n2; i += blockDim.x)
+      keys[i] = i < n_cand ? score_key(alpha[i], (unsigned)i) : ~0ull;
+    __syncthreads();
+    bitonic_sort(keys, n2);
+    // the first k_p keys are the selection; re-sort them by candidate index
+    int k2 = 1;
+    while (k2 < a.k_p) k2 <<= 1;
+    for (int i = tid; i < k2; i += blockDim.x)
+      keys[i] = i < a.k_p ? (keys[i] & 0xffffffffull) : ~0ull;
+    __syncthreads();
+    bitonic_sort(keys, k2);
+    for (int i = tid; i < a.k_p; i += blockDim.x) {
+      const int c = (int)(keys[i] & 0xffffffffull);
+      a.idx_out[hs * a.k_p + i] = cand0 + c;
+      if (a.scores_out) a.scores_out[hs * a.k_p + i] = alpha[c];
+    }
+    __syncthreads();   // alpha and keys are reused by the next set
   }
   if (tid == 0) {
     if (a.chunk_out) a.chunk_out[0] = chunk;
@@ -481,8 +489,9 @@ wa_status launch_select_pages(const void* q, wa_dtype dt, int n_q, int n_heads, 
                               const float* kbar, int n_pages, const float* prompt_cur,
                               const float* prompt_chunks, int n_chunks, int prompt_dim,
                               int pages_per_chunk, int k_p, int32_t* idx_out, float* scores_out,
-                              int32_t* chunk_out, cudaStream_t s) {
+                              int32_t* chunk_out, cudaStream_t s, int per_head) {
   SelectArgs a{};
+  a.per_head = per_head;
   a.n_q = n_q;
   a.row_elems = n_heads * head_dim;
   a.kbar = kbar;

@@ -145,6 +145,55 @@ wa_status wa_select_pages(const void* q, wa_dtype dt, int n_q, int n_heads, int 
                              scores_out, chunk_out, (cudaStream_t)stream);
 }
 
+wa_status wa_select_pages_per_head(const void* q, wa_dtype dt, int n_q, int n_heads, int head_dim,
+                                   const float* kbar, int n_pages, const float* prompt_cur,
+                                   const float* prompt_chunks, int n_chunks, int prompt_dim,
+                                   int pages_per_chunk, int k_p, int32_t* idx_out,
+                                   float* scores_out, int32_t* chunk_out, wa_stream_t stream) {
+  if (!dtype_ok(dt)) return WA_ERR_DTYPE;
+  if (!q || !kbar || !idx_out || n_q <= 0 || n_pages <= 0 || k_p <= 0 || n_chunks < 0)
+    return WA_ERR_INVALID_ARG;
+  if (!row_ok(n_heads, head_dim, dt)) return WA_ERR_SHAPE;
+  if ((long long)n_heads * head_dim > 8192) return WA_ERR_SHAPE;
+  int n_cand = n_pages;
+  if (n_chunks > 0) {
+    if (!prompt_cur || !prompt_chunks || prompt_dim <= 0 || pages_per_chunk <= 0)
+      return WA_ERR_INVALID_ARG;
+    if ((long long)n_chunks * pages_per_chunk > n_pages) return WA_ERR_INVALID_ARG;
+    n_cand = pages_per_chunk;
+  }
+  if (k_p > n_cand || k_p > 1024) return WA_ERR_INVALID_ARG;
+  if (n_cand > 8192) return WA_ERR_SHAPE;
+  if (!aligned16(q) || !aligned16(kbar)) return WA_ERR_ALIGN;
+  return launch_select_pages(q, dt, n_q, n_heads, head_dim, kbar, n_pages, prompt_cur,
+                             prompt_chunks, n_chunks, prompt_dim, pages_per_chunk, k_p, idx_out,
+                             scores_out, chunk_out, (cudaStream_t)stream, 1);
+}
+
+wa_status wa_gather_pages_per_head(const void* k_pages, const void* v_pages, wa_dtype dt,
+                                   int n_pages, int page_tokens, int n_heads, int head_dim,
+                                   const int32_t* idx_dev, int k_p, void* k_buf, void* v_buf,
+                                   wa_stream_t stream) {
+  if (!dtype_ok(dt)) return WA_ERR_DTYPE;
+  if (!k_pages || !k_buf || !idx_dev || n_pages <= 0 || page_tokens <= 0 || k_p <= 0)
+    return WA_ERR_INVALID_ARG;
+  if ((v_pages == nullptr) != (v_buf == nullptr)) return WA_ERR_INVALID_ARG;
+  if (!row_ok(n_heads, head_dim, dt)) return WA_ERR_SHAPE;
+  if ((head_dim * esize(dt)) % 16 != 0) return WA_ERR_SHAPE;
+  if (!aligned16(k_pages) || !aligned16(k_buf) || (v_pages && (!aligned16(v_pages) ||
+      !aligned16(v_buf))))
+    return WA_ERR_ALIGN;
+  cudaPointerAttributes attr;
+  if (cudaPointerGetAttributes(&attr, k_pages) != cudaSuccess) {
+    cudaGetLastError();
+    return WA_ERR_INVALID_ARG;
+  }
+  if (attr.type != cudaMemoryTypeDevice) return WA_ERR_INVALID_ARG;
+  return launch_gather_per_head(k_pages, v_pages, n_pages, page_tokens, n_heads,
+                                (size_t)head_dim * esize(dt), idx_dev, k_p, k_buf, v_buf,
+                                (cudaStream_t)stream);
+}
+
 wa_status wa_gather_pages(const void* k_pages, const void* v_pages, wa_dtype dt, int n_pages,
                           int page_tokens, int n_heads, int head_dim, const int32_t* idx_dev,
                           const int32_t* idx_host, int k_p, void* k_buf, void* v_buf,

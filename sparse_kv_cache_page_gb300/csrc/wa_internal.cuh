@@ -61,7 +61,14 @@ wa_status launch_select_pages(const void* q, wa_dtype dt, int n_q, int n_heads, 
                               const float* kbar, int n_pages, const float* prompt_cur,
                               const float* prompt_chunks, int n_chunks, int prompt_dim,
                               int pages_per_chunk, int k_p, int32_t* idx_out, float* scores_out,
-                              int32_t* chunk_out, cudaStream_t s);
+                              int32_t* chunk_out, cudaStream_t s, int per_head = 0);
+
+// Per-head gather: k_buf[s*P + t][h] = k_pages[idx[h*k_p + s]][t][h] (and V); 16-byte
+// vectors of each head row, indices read on the device.
+wa_status launch_gather_per_head(const void* k_pages, const void* v_pages, int n_pages,
+                                 int page_tokens, int n_heads, size_t head_row_bytes,
+                                 const int32_t* idx_dev, int k_p, void* k_buf, void* v_buf,
+                                 cudaStream_t s);
 
 wa_status launch_gather_device(const void* k_pages, const void* v_pages, size_t page_bytes,
                                int n_pages, const int32_t* idx_dev, int k_p, void* k_buf,
