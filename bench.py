@@ -140,7 +140,7 @@ def max_over_ranks(x, world):
 # GPU arm
 # ----------------------------------------------------------------------------
 
-def run_gpu(args, world, rank, local, hybrid=False):
+def run_gpu(args, world, rank, local, hybrid=False, per_head=False):
     import torch
 
     import sparse_kv_cache_page_gb300 as wa
@@ -153,10 +153,17 @@ def run_gpu(args, world, rank, local, hybrid=False):
     kp, vp, q, kl, vl = c.k_pages, c.v_pages, c.q, c.k_loc, c.v_loc
     pcur, pch = c.prompt_cur, c.prompt_chunks
     kbar = torch.empty((N_PAGES, H, D), dtype=torch.float32, device=dev)
-    idx = torch.empty(KP, dtype=torch.int32, device=dev)
+    idx = torch.empty((H, KP) if per_head else (KP,), dtype=torch.int32, device=dev)
     kbuf = torch.empty((KP * P, H, D), dtype=torch.bfloat16, device=dev)
     vbuf = torch.empty_like(kbuf)
     o = torch.empty(q.shape, dtype=torch.float32, device=dev)   # fp32 result (tested tolerance)
+    select = wa.wa_select_pages_per_head if per_head else wa.wa_select_pages
+
+    def gather(idx_):
+        if per_head:
+            wa.wa_gather_pages_per_head(kp, vp, idx_, kbuf, vbuf)
+        else:
+            wa.wa_gather_pages(kp, vp, idx_, None, kbuf, vbuf)
     stream = torch.cuda.current_stream()
     L, RANK = KP * P + NLOC, 256
     if hybrid:
@@ -174,9 +181,9 @@ def run_gpu(args, world, rank, local, hybrid=False):
         mark(0)
         wa.wa_page_summarize(kp, kbar)
         mark(1)
-        wa.wa_select_pages(q, kbar, pcur, pch, PPC, KP, idx)
+        select(q, kbar, pcur, pch, PPC, KP, idx)
         mark(2)
-        wa.wa_gather_pages(kp, vp, idx, None, kbuf, vbuf)
+        gather(idx)
         mark(3)
         wa.wa_block_attn(q, kbuf, vbuf, kl, vl, o)
         mark(4)
@@ -241,8 +248,8 @@ def run_gpu(args, world, rank, local, hybrid=False):
             dq, dkl, dvl, dpc, do = dbuf[k % 2]
             stream.wait_event(ev_in[k])
             wa.wa_page_summarize(kp, kbar)
-            wa.wa_select_pages(dq, kbar, dpc, pch, PPC, KP, idx)
-            wa.wa_gather_pages(kp, vp, idx, None, kbuf, vbuf)
+            select(dq, kbar, dpc, pch, PPC, KP, idx)
+            gather(idx)
             wa.wa_block_attn(dq, kbuf, vbuf, dkl, dvl, do)
             if hybrid:
                 wa.wa_linear_branch(dq, kbuf, vbuf, dkl, dvl, ek, ev, do)
@@ -306,13 +313,18 @@ def run_gpu(args, world, rank, local, hybrid=False):
         "gpu_launches": launches_per_step * args.steps,
         "clocks": clk.summary(),
     }
+    if per_head:
+        line["config"]["workload"] = ("per_head: " + WORKLOAD + " with a top-4 page set per head "
+                                      "(per-head scores, per-head gather into the token-major "
+                                      "buffer)")
+        line.pop("cpu_baseline", None)
     if hybrid:
         proj_bytes = 2 * H * L * RANK * 2 + 2 * L * H * D * 2
         line["config"]["workload"] = ("hybrid: " + WORKLOAD + " + Linformer branch rank 256 "
                                       "(E_K, E_V [12][54600][256] bf16), equal-weight fusion")
         line["linear_ms"] = round(per["linear"], 4)
         line["linear_read_gbs"] = round(proj_bytes / (per["linear"] * 1e-3) / 1e9, 1)
-    if rank == 0 and world == 1 and not args.no_cpu_baseline and not hybrid:
+    if rank == 0 and world == 1 and not args.no_cpu_baseline and not hybrid and not per_head:
         line["cpu_baseline"] = cpu_baseline_sample(c, lambda j: (kp[j], vp[j]))
     return line
 
@@ -706,10 +718,11 @@ def main():
     ap.add_argument("--kernel", default="all", choices=["all", "attention", "gather", "linear"],
                     help="time one kernel alone on its own inputs (for profiling)")
     ap.add_argument("--workload", default="worldattention",
-                    choices=["worldattention", "denoise", "hybrid", "hsa", "stress"],
+                    choices=["worldattention", "denoise", "hybrid", "hsa", "per_head", "stress"],
                     help="worldattention: the headline one-layer chunk; denoise: 4 denoising "
                          "steps over a cached 21-frame window; hybrid: + Linformer branch; "
                          "hsa: sparse + Linformer branches in place of dense attention; "
+                         "per_head: a page set per head; "
                          "stress: 30 layers with pages in pinned host memory")
     ap.add_argument("--layers", type=int, default=30, help="stress workload: layers")
     args = ap.parse_args()
@@ -725,6 +738,8 @@ def main():
         line = run_gpu(args, world, rank, local, hybrid=True)
     elif args.workload == "hsa":
         line = run_hsa(args, world, rank, local)
+    elif args.workload == "per_head":
+        line = run_gpu(args, world, rank, local, per_head=True)
     elif args.workload == "stress":
         line = run_stress(args, world, rank, local)
     else:
