@@ -330,6 +330,74 @@ wa_status wa_sparse_attn(const void* q, int n_q, const void* k_main, const void*
                          float* lse, wa_stream_t stream);
 
 /*
+ * KV cache manager around the path ([WA] HKV tiers L1/L2 and Fig. 2; [IX]
+ * KV Cache Manager: append a clean block, range access, index-based selective
+ * fetch, offload to main memory).  A host-side runtime over the calls above:
+ *
+ *   - pages of page_tokens tokens, pages_per_chunk per appended chunk, numbered
+ *     in append order (chunk m owns pages m*ppc .. m*ppc + ppc - 1);
+ *   - an HBM tier of hbm_pages page slots (K and V) and a pinned DRAM tier of
+ *     host_pages slots; page summaries and prompt embeddings of every page stay
+ *     in HBM;
+ *   - append: pages to free HBM slots, the least recently used resident page
+ *     offloaded to DRAM (copy engine) when none is free; summaries computed at
+ *     insert;
+ *   - retrieve: wa_select_pages over the cached pages, indices to the host (one
+ *     synchronisation of `stream`), each page copied into the caller's buffer
+ *     from its tier; pages fetched from DRAM are promoted back to HBM, swapping
+ *     with the least recently used page not selected now;
+ *   - window: the last n tokens of the sequence, contiguous (range access).
+ * The LRU clock ticks once per append and per retrieval (ties: lower page).
+ * dry_run != 0 makes a cache with no device memory and no CUDA calls whose
+ * placement decisions can be driven with wa_cache_touch (host-logic tests).
+ * Not thread-safe; one cache per layer.
+ */
+typedef struct wa_cache wa_cache;
+
+typedef struct {
+  int n_heads, head_dim;
+  wa_dtype dtype;
+  int page_tokens;      /* tokens per page */
+  int pages_per_chunk;  /* pages per appended chunk */
+  int prompt_dim;       /* prompt embedding size; 0: no prompt stage */
+  int hbm_pages;        /* HBM tier capacity (pages, >= 1) */
+  int host_pages;       /* pinned DRAM tier capacity (pages, >= 0) */
+  int max_chunks;       /* chunks the cache can hold */
+  int dry_run;          /* 1: placement only, no device memory or copies */
+} wa_cache_config;
+
+typedef struct {
+  int n_pages, n_chunks, in_hbm, in_host;
+  long long offloads, promotions;             /* page moves HBM -> DRAM, DRAM -> HBM */
+  long long bytes_h2d, bytes_d2h, bytes_d2d;  /* K+V bytes moved (dry run: planned) */
+} wa_cache_stats;
+
+/* Errors: WA_ERR_INVALID_ARG, WA_ERR_DTYPE, WA_ERR_SHAPE (head rows not whole
+ * 16-byte vectors), WA_ERR_OOM (allocation failed). */
+wa_status wa_cache_create(const wa_cache_config* cfg, wa_cache** out);
+/* Synchronizes the device (unless dry_run) and frees the cache. */
+wa_status wa_cache_destroy(wa_cache* cache);
+/* k, v: device [pages_per_chunk*page_tokens][n_heads][head_dim] of dtype (page
+ * major); prompt: device float32 [prompt_dim] (NULL if prompt_dim == 0).
+ * WA_ERR_OOM when both tiers or max_chunks are full. */
+wa_status wa_cache_append_chunk(wa_cache* cache, const void* k, const void* v, const float* prompt,
+                                wa_stream_t stream);
+/* q: device [n_q][n_heads][head_dim]; prompt_cur: device float32 [prompt_dim] or
+ * NULL (no prompt stage: every page is a candidate); k_buf, v_buf: device
+ * [k_p*page_tokens][n_heads][head_dim]; idx_out: host int32 [k_p] (ascending). */
+wa_status wa_cache_retrieve(wa_cache* cache, const void* q, int n_q, const float* prompt_cur,
+                            int k_p, void* k_buf, void* v_buf, int32_t* idx_out,
+                            wa_stream_t stream);
+/* k_out, v_out: device [n_tokens][n_heads][head_dim]: the last n_tokens tokens. */
+wa_status wa_cache_window(wa_cache* cache, int n_tokens, void* k_out, void* v_out,
+                          wa_stream_t stream);
+/* Dry-run caches only: use pages as one retrieval would (LRU and promotion). */
+wa_status wa_cache_touch(wa_cache* cache, const int32_t* pages, int n);
+/* tier: 0 HBM, 1 DRAM; slot within the tier.  WA_ERR_INDEX for unknown pages. */
+wa_status wa_cache_page_location(const wa_cache* cache, int page, int* tier, int* slot);
+wa_status wa_cache_get_stats(const wa_cache* cache, wa_cache_stats* out);
+
+/*
  * Synchronize `stream`, then read and clear this device's status word.
  * Returns WA_OK, WA_ERR_INDEX (a gather index was out of range),
  * WA_ERR_TIMEOUT (a kernel wait gave up; the kernel returned early and its

@@ -28,6 +28,7 @@ __all__ = [
     "wa_block_means",
     "wa_sparse_select",
     "wa_sparse_attn",
+    "WaCache",
     "wa_check",
     "wa_shutdown",
     "wa_version",
@@ -43,8 +44,22 @@ WA_F32, WA_BF16 = 0, 1
 EXPORTED_SYMBOLS = ("wa_strerror", "wa_version", "wa_page_summarize", "wa_select_pages",
                     "wa_select_pages_noalloc", "wa_gather_pages", "wa_block_attn",
                     "wa_linear_branch", "wa_block_means", "wa_sparse_select", "wa_sparse_attn",
-                    "wa_select_pages_per_head", "wa_gather_pages_per_head", "wa_check",
-                    "wa_shutdown")
+                    "wa_select_pages_per_head", "wa_gather_pages_per_head", "wa_cache_create",
+                    "wa_cache_destroy", "wa_cache_append_chunk", "wa_cache_retrieve",
+                    "wa_cache_window", "wa_cache_touch", "wa_cache_page_location",
+                    "wa_cache_get_stats", "wa_check", "wa_shutdown")
+
+
+class _CacheConfig(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int) for n in ("n_heads", "head_dim", "dtype", "page_tokens",
+                                             "pages_per_chunk", "prompt_dim", "hbm_pages",
+                                             "host_pages", "max_chunks", "dry_run")]
+
+
+class _CacheStats(ctypes.Structure):
+    _fields_ = ([(n, ctypes.c_int) for n in ("n_pages", "n_chunks", "in_hbm", "in_host")]
+                + [(n, ctypes.c_longlong) for n in ("offloads", "promotions", "bytes_h2d",
+                                                    "bytes_d2h", "bytes_d2d")])
 
 
 class WaError(RuntimeError):
@@ -80,6 +95,14 @@ def load():
         "wa_block_means": (I, [P, I, I, I, I, I, P, P]),
         "wa_sparse_select": (I, [P, I, P, I, I, I, F, P, P, P, P, P, P]),
         "wa_sparse_attn": (I, [P, I, P, P, I, P, P, I, I, I, P, P, I, I, I, F, P, I, P, P]),
+        "wa_cache_create": (I, [ctypes.POINTER(_CacheConfig), ctypes.POINTER(P)]),
+        "wa_cache_destroy": (I, [P]),
+        "wa_cache_append_chunk": (I, [P, P, P, P, P]),
+        "wa_cache_retrieve": (I, [P, P, I, P, I, P, P, P, P]),
+        "wa_cache_window": (I, [P, I, P, P, P]),
+        "wa_cache_touch": (I, [P, P, I]),
+        "wa_cache_page_location": (I, [P, I, ctypes.POINTER(I), ctypes.POINTER(I)]),
+        "wa_cache_get_stats": (I, [P, ctypes.POINTER(_CacheStats)]),
         "wa_check": (I, [P]),
         "wa_shutdown": (I, []),
     }
@@ -272,6 +295,68 @@ def wa_sparse_attn(q: torch.Tensor, k_main, v_main, k_loc, v_loc, sel: torch.Ten
         _ptr(q), n_q, _ptr(k_main), _ptr(v_main), _rows(k_main), _ptr(k_loc), _ptr(v_loc),
         _rows(k_loc), int(block_main), int(block_loc), _ptr(sel), _ptr(count), _dt(q), h, d,
         float(scale), _ptr(o), _dt(o), _ptr(lse), _stream(stream)))
+
+
+class WaCache:
+    """KV cache manager (libwa wa_cache_*): HBM and pinned-DRAM page tiers,
+    summaries at insert, retrieval with LRU offload and promotion, window
+    access.  ``dry_run`` caches plan placements without any CUDA work."""
+
+    def __init__(self, n_heads: int, head_dim: int, page_tokens: int, pages_per_chunk: int,
+                 hbm_pages: int, host_pages: int, max_chunks: int, prompt_dim: int = 0,
+                 dtype=torch.bfloat16, dry_run: bool = False):
+        cfg = _CacheConfig(n_heads, head_dim, WA_BF16 if dtype == torch.bfloat16 else WA_F32,
+                           page_tokens, pages_per_chunk, prompt_dim, hbm_pages, host_pages,
+                           max_chunks, int(bool(dry_run)))
+        h = ctypes.c_void_p()
+        _ok("wa_cache_create", load().wa_cache_create(ctypes.byref(cfg), ctypes.byref(h)))
+        self._h = h
+        self.cfg = cfg
+
+    def close(self):
+        if self._h:
+            _ok("wa_cache_destroy", load().wa_cache_destroy(self._h))
+            self._h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:   # interpreter shutdown
+            pass
+
+    def append(self, k, v, prompt=None, stream=None):
+        _ok("wa_cache_append_chunk", load().wa_cache_append_chunk(
+            self._h, _ptr(k), _ptr(v), _ptr(prompt),
+            None if self.cfg.dry_run else _stream(stream)))
+
+    def retrieve(self, q: torch.Tensor, prompt_cur, k_p: int, k_buf: torch.Tensor,
+                 v_buf: torch.Tensor, stream=None):
+        """Indices (ascending) of the k_p pages copied into k_buf / v_buf."""
+        idx = (ctypes.c_int32 * k_p)()
+        _ok("wa_cache_retrieve", load().wa_cache_retrieve(
+            self._h, _ptr(q), q.shape[0], _ptr(prompt_cur), k_p, _ptr(k_buf), _ptr(v_buf),
+            ctypes.cast(idx, ctypes.c_void_p), _stream(stream)))
+        return list(idx)
+
+    def window(self, n_tokens: int, k_out: torch.Tensor, v_out: torch.Tensor, stream=None):
+        _ok("wa_cache_window", load().wa_cache_window(self._h, n_tokens, _ptr(k_out), _ptr(v_out),
+                                                      _stream(stream)))
+
+    def touch(self, pages):
+        arr = (ctypes.c_int32 * len(pages))(*pages)
+        _ok("wa_cache_touch", load().wa_cache_touch(self._h, ctypes.cast(arr, ctypes.c_void_p),
+                                                    len(pages)))
+
+    def location(self, page: int):
+        t, s = ctypes.c_int(), ctypes.c_int()
+        _ok("wa_cache_page_location", load().wa_cache_page_location(
+            self._h, page, ctypes.byref(t), ctypes.byref(s)))
+        return t.value, s.value
+
+    def stats(self) -> dict:
+        st = _CacheStats()
+        _ok("wa_cache_get_stats", load().wa_cache_get_stats(self._h, ctypes.byref(st)))
+        return {n: getattr(st, n) for n, _ in _CacheStats._fields_}
 
 
 def wa_check(stream=None):
