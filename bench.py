@@ -448,6 +448,84 @@ def run_hsa(args, world, rank, local):
     }
 
 
+def run_cache(args, world, rank, local):
+    """Generation loop over the KV cache manager: 12 chunks (a 60-second video
+    as 12 five-second chunks, WorldAttention review page, worked example), each
+    8 pages of 12,480 tokens, an HBM tier of 16 pages and a pinned DRAM tier of
+    96.  Per chunk after the first: retrieval of the top-4 pages (prompt stage
+    over the past chunks, page stage, pages fetched from either tier, DRAM pages
+    promoted), attention of the chunk's queries over them plus the chunk's own
+    KV, then the chunk's KV appended (summaries at insert, least recently used
+    pages offloaded to DRAM).  One bench step = the 11 chunks of one video."""
+    import torch
+
+    import sparse_kv_cache_page_gb300 as wa
+    from sparse_kv_cache_page_gb300 import synth
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    wa.load()
+    NCH, PDIM = 12, 4096
+    g = lambda shape, t, dt=torch.bfloat16: synth.normal(shape, synth.seed_of("cache", rank, t),  # noqa: E731
+                                                         dev, dt)
+    ks = [g((PPC * P, H, D), ("k", m)) for m in range(NCH)]
+    vs = [g((PPC * P, H, D), ("v", m)) for m in range(NCH)]
+    prompts = [g((PDIM,), ("prompt", m), torch.float32) for m in range(NCH)]
+    qs = [g((NQ, H, D), ("q", m)) for m in range(NCH)]
+    # chunk m's prompt recalls an earlier chunk, (5 m + 3) mod m (a scene revisited)
+    curs = [None] + [prompts[(5 * m + 3) % m] + 0.5 * g((PDIM,), ("cur", m), torch.float32)
+                     for m in range(1, NCH)]
+    kb = torch.empty((KP * P, H, D), dtype=torch.bfloat16, device=dev)
+    vb = torch.empty_like(kb)
+    o = torch.empty((NQ, H, D), dtype=torch.float32, device=dev)
+
+    # the tiers are allocated once (8.5 GB of HBM and pinned DRAM); each video
+    # starts from an emptied cache (wa_cache_reset), outside the timed loop
+    cache = wa.WaCache(H, D, P, PPC, hbm_pages=16, host_pages=96, max_chunks=NCH,
+                       prompt_dim=PDIM)
+
+    def video():
+        cache.append(ks[0], vs[0], prompts[0])
+        for m in range(1, NCH):
+            cache.retrieve(qs[m], curs[m], KP, kb, vb)
+            wa.wa_block_attn(qs[m], kb, vb, ks[m][:NLOC], vs[m][:NLOC], o)
+            cache.append(ks[m], vs[m], prompts[m])
+
+    for _ in range(max(1, args.warmup - 2)):
+        cache.reset()
+        video()
+    torch.cuda.synchronize()
+    steps = max(1, min(args.steps, 5))
+    total = 0.0
+    with Clocks(local) as clk:
+        for _ in range(steps):
+            cache.reset()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            video()
+            e1.record()
+            torch.cuda.synchronize()
+            total += e0.elapsed_time(e1)
+    st = cache.stats()
+    cache.close()
+    ms = max_over_ranks(total, world) / steps
+    flops = (NCH - 1) * attn_flops(NQ, KP * P + NLOC, D, H)
+    return {"metric": METRIC, "value": round(world * flops / (ms * 1e-3) / 1e12, 2),
+            "unit": "TFLOP/s", "n_gpus": world, "steps": steps, "warmup": args.warmup,
+            "ms_per_step": round(ms, 3), "ms_per_chunk": round(ms / (NCH - 1), 3),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic",
+            "config": {"workload": "cache: 12 chunks x 8 pages x 12,480 tokens through the KV "
+                                   "cache manager (HBM tier 16 pages, pinned DRAM tier 96), "
+                                   "retrieve top-4 + attention + append per chunk, H=12 d=128 bf16",
+                       "value_is": "attention FLOPs of the 11 chunks / whole-loop time "
+                                   "(appends, offloads, fetches and promotions included; tier "
+                                   "allocation excluded)"},
+            "cache_stats_per_video": st,
+            "gpu_launches": steps * (NCH + 2 * (NCH - 1)),   # summaries per append; select + attention
+            "clocks": clk.summary()}
+
+
 def run_one_kernel(args, local):
     """One kernel alone at the workload's shape (inputs drawn directly, no page
     bank): the attention over a 49,920-token buffer + 4,680 local tokens, or
@@ -718,11 +796,13 @@ def main():
     ap.add_argument("--kernel", default="all", choices=["all", "attention", "gather", "linear"],
                     help="time one kernel alone on its own inputs (for profiling)")
     ap.add_argument("--workload", default="worldattention",
-                    choices=["worldattention", "denoise", "hybrid", "hsa", "per_head", "stress"],
+                    choices=["worldattention", "denoise", "hybrid", "hsa", "per_head", "cache",
+                             "stress"],
                     help="worldattention: the headline one-layer chunk; denoise: 4 denoising "
                          "steps over a cached 21-frame window; hybrid: + Linformer branch; "
                          "hsa: sparse + Linformer branches in place of dense attention; "
-                         "per_head: a page set per head; "
+                         "per_head: a page set per head; cache: 12-chunk generation loop "
+                         "through the KV cache manager; "
                          "stress: 30 layers with pages in pinned host memory")
     ap.add_argument("--layers", type=int, default=30, help="stress workload: layers")
     args = ap.parse_args()
@@ -740,6 +820,8 @@ def main():
         line = run_hsa(args, world, rank, local)
     elif args.workload == "per_head":
         line = run_gpu(args, world, rank, local, per_head=True)
+    elif args.workload == "cache":
+        line = run_cache(args, world, rank, local)
     elif args.workload == "stress":
         line = run_stress(args, world, rank, local)
     else:

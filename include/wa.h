@@ -377,6 +377,9 @@ typedef struct {
 wa_status wa_cache_create(const wa_cache_config* cfg, wa_cache** out);
 /* Synchronizes the device (unless dry_run) and frees the cache. */
 wa_status wa_cache_destroy(wa_cache* cache);
+/* Empties the cache for a new sequence, keeping its memory (synchronizes the
+ * device unless dry_run). */
+wa_status wa_cache_reset(wa_cache* cache);
 /* k, v: device [pages_per_chunk*page_tokens][n_heads][head_dim] of dtype (page
  * major); prompt: device float32 [prompt_dim] (NULL if prompt_dim == 0).
  * WA_ERR_OOM when both tiers or max_chunks are full. */

@@ -45,7 +45,8 @@ EXPORTED_SYMBOLS = ("wa_strerror", "wa_version", "wa_page_summarize", "wa_select
                     "wa_select_pages_noalloc", "wa_gather_pages", "wa_block_attn",
                     "wa_linear_branch", "wa_block_means", "wa_sparse_select", "wa_sparse_attn",
                     "wa_select_pages_per_head", "wa_gather_pages_per_head", "wa_cache_create",
-                    "wa_cache_destroy", "wa_cache_append_chunk", "wa_cache_retrieve",
+                    "wa_cache_destroy", "wa_cache_reset", "wa_cache_append_chunk",
+                    "wa_cache_retrieve",
                     "wa_cache_window", "wa_cache_touch", "wa_cache_page_location",
                     "wa_cache_get_stats", "wa_check", "wa_shutdown")
 
@@ -97,6 +98,7 @@ def load():
         "wa_sparse_attn": (I, [P, I, P, P, I, P, P, I, I, I, P, P, I, I, I, F, P, I, P, P]),
         "wa_cache_create": (I, [ctypes.POINTER(_CacheConfig), ctypes.POINTER(P)]),
         "wa_cache_destroy": (I, [P]),
+        "wa_cache_reset": (I, [P]),
         "wa_cache_append_chunk": (I, [P, P, P, P, P]),
         "wa_cache_retrieve": (I, [P, P, I, P, I, P, P, P, P]),
         "wa_cache_window": (I, [P, I, P, P, P]),
@@ -323,6 +325,10 @@ class WaCache:
             self.close()
         except Exception:   # interpreter shutdown
             pass
+
+    def reset(self):
+        """Empty the cache for a new sequence; the tiers' memory is kept."""
+        _ok("wa_cache_reset", load().wa_cache_reset(self._h))
 
     def append(self, k, v, prompt=None, stream=None):
         _ok("wa_cache_append_chunk", load().wa_cache_append_chunk(

@@ -227,6 +227,19 @@ wa_status wa_cache_destroy(wa_cache* c) {
   return WA_OK;
 }
 
+wa_status wa_cache_reset(wa_cache* c) {
+  if (!c) return WA_ERR_INVALID_ARG;
+  if (!c->cfg.dry_run) cudaDeviceSynchronize();   // no copy may still read or write a slot
+  c->table.clear();
+  std::fill(c->hbm_owner.begin(), c->hbm_owner.end(), -1);
+  std::fill(c->host_owner.begin(), c->host_owner.end(), -1);
+  c->n_pages = 0;
+  c->n_chunks = 0;
+  c->clock = 0;
+  c->stats = wa_cache_stats{};
+  return WA_OK;
+}
+
 wa_status wa_cache_append_chunk(wa_cache* c, const void* k, const void* v, const float* prompt,
                                 wa_stream_t stream) {
   if (!c) return WA_ERR_INVALID_ARG;
