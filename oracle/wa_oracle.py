@@ -45,6 +45,12 @@ design notes):
   alpha_{j,h} = Qbar_h . Kbar_{j,h} / sqrt(d_k), keeps its own top-K_p (same
   tie rule, ascending), and the buffer keeps the token-major layout with head
   h's slice taken from head h's pages.
+* Compressed DRAM tier (the pages name FP8 / FP4 storage only in passing):
+  each (token, head) row of d values is stored as FP8 E4M3 codes with one
+  fp32 scale, s = amax(|row|) / 448 and code = E4M3 round-to-nearest-even of
+  x / s (both divisions in IEEE fp32); decoding multiplies the code's value by
+  s in fp32 and rounds to bf16 for the attention buffer.  A row of zeros has
+  s = 0 and codes 0.
 * HSA sparse branch ([WA] HSA section and its appendix notes): key blocks of
   B_inter = 128 tokens over the retrieved buffer and B_intra = 64 over the
   chunk's own tokens (a ragged last block keeps its own size); query blocks of
@@ -96,6 +102,10 @@ __all__ = [
     "page_scores_per_head",
     "select_pages_per_head",
     "gather_pages_per_head",
+    "e4m3_values",
+    "e4m3_round",
+    "fp8_encode_rows",
+    "fp8_decode_rows",
 ]
 
 
@@ -471,3 +481,66 @@ def gather_pages_per_head(pages: np.ndarray, idx) -> np.ndarray:
         for s_ in range(k_p):
             out[s_ * p_tok:(s_ + 1) * p_tok, h] = pg[int(idx[h, s_]), :, h]
     return out
+
+
+# ----------------------------------------------------------------------------
+# Compressed DRAM tier: FP8 E4M3 page codec with one fp32 scale per row
+# ----------------------------------------------------------------------------
+
+def e4m3_values() -> np.ndarray:
+    """Value of each of the 256 E4M3 codes (sign bit, 4 exponent bits with
+    bias 7, 3 mantissa bits; exponent 0 is subnormal; S.1111.111 is NaN; no
+    infinities).  Returns float64 [256]."""
+    out = np.empty(256, dtype=np.float64)
+    for c in range(256):
+        sign = -1.0 if c & 0x80 else 1.0
+        e = (c >> 3) & 0xF
+        m = c & 0x7
+        if e == 0xF and m == 0x7:
+            out[c] = np.nan
+        elif e == 0:
+            out[c] = sign * (m / 8.0) * 2.0 ** -6
+        else:
+            out[c] = sign * (1.0 + m / 8.0) * 2.0 ** (e - 7)
+    return out
+
+
+def e4m3_round(q: np.ndarray) -> np.ndarray:
+    """E4M3 code of each fp32 value by round-to-nearest, ties to the even code
+    (mantissa LSB 0), the sign kept (also for a zero result); values in
+    (448, 464) round to 448, larger ones are rejected.  Returns uint8 codes."""
+    q = np.asarray(q, dtype=np.float64)
+    vals = e4m3_values()
+    pos = np.arange(0, 0x7F)                      # codes 0x00 .. 0x7E, increasing values
+    pv = vals[pos]
+    a = np.abs(q)
+    if np.any(a >= 464.0):                       # 464 would round past the largest finite
+        raise ValueError("value outside the E4M3 range")
+    hi = np.searchsorted(pv, a, side="left")      # first value >= a
+    hi = np.minimum(hi, len(pv) - 1)
+    lo = np.maximum(hi - 1, 0)
+    d_lo, d_hi = a - pv[lo], pv[hi] - a
+    take_hi = (d_hi < d_lo) | ((d_hi == d_lo) & ((pos[hi] & 1) == 0) & (hi != lo))
+    code = np.where(take_hi, pos[hi], pos[lo]).astype(np.uint8)
+    code = np.where(pv[hi] == a, pos[hi], code).astype(np.uint8)
+    sign = np.signbit(q).astype(np.uint8) << 7    # IEEE: the sign survives a zero result
+    return code | sign
+
+
+def fp8_encode_rows(x):
+    """x [n][H][d] (bf16 bits or float) -> (codes uint8 [n][H][d], scales
+    float32 [n][H]): s = fp32(amax / 448), codes = E4M3 RNE of fp32(x / s)."""
+    xx = as_f64(x).astype(np.float32)             # exact: bf16 values are fp32 values
+    amax = np.abs(xx).max(axis=2)
+    s = (amax / np.float32(448.0)).astype(np.float32)
+    safe = np.where(s > 0, s, np.float32(1.0)).astype(np.float32)
+    q = (xx / safe[:, :, None]).astype(np.float32)
+    codes = e4m3_round(q)
+    codes[s == 0] = 0
+    return codes, s
+
+
+def fp8_decode_rows(codes, scales) -> np.ndarray:
+    """fp32(value(code) * s) per element: [n][H][d] float32."""
+    v = e4m3_values()[np.asarray(codes)].astype(np.float32)
+    return (v * np.asarray(scales, dtype=np.float32)[:, :, None]).astype(np.float32)
