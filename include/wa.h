@@ -330,6 +330,32 @@ wa_status wa_sparse_attn(const void* q, int n_q, const void* k_main, const void*
                          float* lse, wa_stream_t stream);
 
 /*
+ * Compressed DRAM tier: FP8 E4M3 codec for pages ([WA] HKV tier L2; pages
+ * crossing the CPU-GPU link as FP8 halve the bytes).  Per (token, head) row
+ * of head_dim values: s = amax(|row|) / 448 and code = E4M3 round-to-nearest-
+ * even of x / s (IEEE fp32 divisions); decoding writes bf16 RNE(value(code) * s).
+ * A zero row has s = 0 and codes 0.  head_dim must be 64, 128 or 256
+ * (WA_ERR_SHAPE); all pointers 16-byte aligned (WA_ERR_ALIGN).  Codes and
+ * scales may be device memory or pinned host memory (read or written through
+ * the device mapping, i.e. across the link); x and out are device memory.
+ *
+ * wa_fp8_encode       : x bf16 [n_tokens][n_heads][head_dim] -> codes uint8
+ *                       [n_tokens][n_heads][head_dim], scales float32 [n_tokens][n_heads].
+ * wa_fp8_decode       : the inverse, into out bf16 [n_tokens][n_heads][head_dim].
+ * wa_gather_pages_fp8 : out[s*page_tokens + t] = decode(page idx_dev[s], token t) for
+ *                       code pages [n_pages][page_tokens][n_heads][head_dim] and scale
+ *                       pages [n_pages][page_tokens][n_heads]; idx_dev device int32 [k_p];
+ *                       a bad index zeroes the slot and records WA_ERR_INDEX.
+ */
+wa_status wa_fp8_encode(const void* x, int n_tokens, int n_heads, int head_dim, uint8_t* codes_out,
+                        float* scales_out, wa_stream_t stream);
+wa_status wa_fp8_decode(const uint8_t* codes, const float* scales, int n_tokens, int n_heads,
+                        int head_dim, void* out, wa_stream_t stream);
+wa_status wa_gather_pages_fp8(const uint8_t* code_pages, const float* scale_pages, int n_pages,
+                              int page_tokens, int n_heads, int head_dim, const int32_t* idx_dev,
+                              int k_p, void* buf_out, wa_stream_t stream);
+
+/*
  * KV cache manager around the path ([WA] HKV tiers L1/L2 and Fig. 2; [IX]
  * KV Cache Manager: append a clean block, range access, index-based selective
  * fetch, offload to main memory).  A host-side runtime over the calls above:

@@ -106,6 +106,7 @@ __all__ = [
     "e4m3_round",
     "fp8_encode_rows",
     "fp8_decode_rows",
+    "bf16_bits",
 ]
 
 
@@ -544,3 +545,10 @@ def fp8_decode_rows(codes, scales) -> np.ndarray:
     """fp32(value(code) * s) per element: [n][H][d] float32."""
     v = e4m3_values()[np.asarray(codes)].astype(np.float32)
     return (v * np.asarray(scales, dtype=np.float32)[:, :, None]).astype(np.float32)
+
+
+def bf16_bits(x) -> np.ndarray:
+    """bf16 bit patterns of fp32 values, round to nearest even (finite inputs)."""
+    u = np.asarray(x, dtype=np.float32).view(np.uint32).astype(np.uint64)
+    rounded = u + 0x7FFF + ((u >> 16) & 1)
+    return (rounded >> 16).astype(np.uint16)

@@ -29,6 +29,9 @@ __all__ = [
     "wa_sparse_select",
     "wa_sparse_attn",
     "WaCache",
+    "wa_fp8_encode",
+    "wa_fp8_decode",
+    "wa_gather_pages_fp8",
     "wa_check",
     "wa_shutdown",
     "wa_version",
@@ -48,7 +51,8 @@ EXPORTED_SYMBOLS = ("wa_strerror", "wa_version", "wa_page_summarize", "wa_select
                     "wa_cache_destroy", "wa_cache_reset", "wa_cache_append_chunk",
                     "wa_cache_retrieve",
                     "wa_cache_window", "wa_cache_touch", "wa_cache_page_location",
-                    "wa_cache_get_stats", "wa_check", "wa_shutdown")
+                    "wa_cache_get_stats", "wa_fp8_encode", "wa_fp8_decode",
+                    "wa_gather_pages_fp8", "wa_check", "wa_shutdown")
 
 
 class _CacheConfig(ctypes.Structure):
@@ -105,6 +109,9 @@ def load():
         "wa_cache_touch": (I, [P, P, I]),
         "wa_cache_page_location": (I, [P, I, ctypes.POINTER(I), ctypes.POINTER(I)]),
         "wa_cache_get_stats": (I, [P, ctypes.POINTER(_CacheStats)]),
+        "wa_fp8_encode": (I, [P, I, I, I, P, P, P]),
+        "wa_fp8_decode": (I, [P, P, I, I, I, P, P]),
+        "wa_gather_pages_fp8": (I, [P, P, I, I, I, I, P, I, P, P]),
         "wa_check": (I, [P]),
         "wa_shutdown": (I, []),
     }
@@ -297,6 +304,33 @@ def wa_sparse_attn(q: torch.Tensor, k_main, v_main, k_loc, v_loc, sel: torch.Ten
         _ptr(q), n_q, _ptr(k_main), _ptr(v_main), _rows(k_main), _ptr(k_loc), _ptr(v_loc),
         _rows(k_loc), int(block_main), int(block_loc), _ptr(sel), _ptr(count), _dt(q), h, d,
         float(scale), _ptr(o), _dt(o), _ptr(lse), _stream(stream)))
+
+
+def wa_fp8_encode(x: torch.Tensor, codes_out: torch.Tensor, scales_out: torch.Tensor, stream=None):
+    """FP8 E4M3 codes and per-(token, head) scales of a bf16 [n][H][d] tensor;
+    codes uint8 [n][H][d] and scales float32 [n][H] on the device or pinned."""
+    n, h, d = x.shape
+    _need(codes_out.dtype == torch.uint8 and codes_out.numel() == n * h * d
+          and scales_out.dtype == torch.float32 and scales_out.numel() == n * h,
+          "codes uint8 [n][H][d], scales float32 [n][H]")
+    _ok("wa_fp8_encode", load().wa_fp8_encode(_ptr(x), n, h, d, _ptr(codes_out), _ptr(scales_out),
+                                              _stream(stream)))
+
+
+def wa_fp8_decode(codes: torch.Tensor, scales: torch.Tensor, out: torch.Tensor, stream=None):
+    n, h, d = out.shape
+    _ok("wa_fp8_decode", load().wa_fp8_decode(_ptr(codes), _ptr(scales), n, h, d, _ptr(out),
+                                              _stream(stream)))
+
+
+def wa_gather_pages_fp8(code_pages: torch.Tensor, scale_pages: torch.Tensor, idx_dev: torch.Tensor,
+                        buf_out: torch.Tensor, stream=None):
+    """buf_out[s*P + t] = decode(code_pages[idx[s]][t]) (bf16); pages on the
+    device or in pinned host memory."""
+    n, p, h, d = code_pages.shape
+    _ok("wa_gather_pages_fp8", load().wa_gather_pages_fp8(
+        _ptr(code_pages), _ptr(scale_pages), n, p, h, d, _ptr(idx_dev), idx_dev.numel(),
+        _ptr(buf_out), _stream(stream)))
 
 
 class WaCache:

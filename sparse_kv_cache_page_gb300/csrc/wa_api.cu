@@ -293,6 +293,63 @@ wa_status wa_block_attn(const void* q, int n_q, const void* k_main, const void* 
                         o_dt == WA_F32, lse, 0, nullptr, nullptr, 0, s);
 }
 
+// Device-usable address of p: device memory as is, pinned host memory through
+// its device mapping; NULL if neither.
+static const void* device_view(const void* p) {
+  cudaPointerAttributes a;
+  if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+    cudaGetLastError();
+    return nullptr;
+  }
+  if (a.type == cudaMemoryTypeDevice || a.type == cudaMemoryTypeManaged) return p;
+  if (a.type == cudaMemoryTypeHost) return a.devicePointer;
+  return nullptr;
+}
+
+static bool fp8_shape_ok(int n_heads, int head_dim) {
+  return n_heads > 0 && (head_dim == 64 || head_dim == 128 || head_dim == 256);
+}
+
+wa_status wa_fp8_encode(const void* x, int n_tokens, int n_heads, int head_dim, uint8_t* codes_out,
+                        float* scales_out, wa_stream_t stream) {
+  if (!x || !codes_out || !scales_out || n_tokens <= 0) return WA_ERR_INVALID_ARG;
+  if (!fp8_shape_ok(n_heads, head_dim)) return WA_ERR_SHAPE;
+  if (!aligned16(x) || !aligned16(codes_out) || !aligned16(scales_out)) return WA_ERR_ALIGN;
+  void* c = const_cast<void*>(device_view(codes_out));
+  float* sc = static_cast<float*>(const_cast<void*>(device_view(scales_out)));
+  if (!c || !sc || !device_view(x)) return WA_ERR_INVALID_ARG;
+  return launch_fp8_encode(x, (size_t)n_tokens * n_heads, head_dim, c, sc, (cudaStream_t)stream);
+}
+
+wa_status wa_fp8_decode(const uint8_t* codes, const float* scales, int n_tokens, int n_heads,
+                        int head_dim, void* out, wa_stream_t stream) {
+  if (!codes || !scales || !out || n_tokens <= 0) return WA_ERR_INVALID_ARG;
+  if (!fp8_shape_ok(n_heads, head_dim)) return WA_ERR_SHAPE;
+  if (!aligned16(codes) || !aligned16(scales) || !aligned16(out)) return WA_ERR_ALIGN;
+  const void* c = device_view(codes);
+  const float* sc = static_cast<const float*>(device_view(scales));
+  if (!c || !sc) return WA_ERR_INVALID_ARG;
+  const size_t rows = (size_t)n_tokens * n_heads;
+  return launch_fp8_decode(c, sc, nullptr, 1, rows, rows, head_dim, out, (cudaStream_t)stream);
+}
+
+wa_status wa_gather_pages_fp8(const uint8_t* code_pages, const float* scale_pages, int n_pages,
+                              int page_tokens, int n_heads, int head_dim, const int32_t* idx_dev,
+                              int k_p, void* buf_out, wa_stream_t stream) {
+  if (!code_pages || !scale_pages || !idx_dev || !buf_out || n_pages <= 0 || page_tokens <= 0 ||
+      k_p <= 0)
+    return WA_ERR_INVALID_ARG;
+  if (!fp8_shape_ok(n_heads, head_dim)) return WA_ERR_SHAPE;
+  if (!aligned16(code_pages) || !aligned16(scale_pages) || !aligned16(buf_out))
+    return WA_ERR_ALIGN;
+  const void* c = device_view(code_pages);
+  const float* sc = static_cast<const float*>(device_view(scale_pages));
+  if (!c || !sc) return WA_ERR_INVALID_ARG;
+  const size_t page_rows = (size_t)page_tokens * n_heads;
+  return launch_fp8_decode(c, sc, idx_dev, n_pages, page_rows, page_rows * k_p, head_dim, buf_out,
+                           (cudaStream_t)stream);
+}
+
 wa_status wa_block_means(const void* x, wa_dtype dt, int n_rows, int block, int n_heads,
                          int head_dim, float* means_out, wa_stream_t stream) {
   if (!dtype_ok(dt)) return WA_ERR_DTYPE;

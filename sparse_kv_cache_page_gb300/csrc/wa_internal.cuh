@@ -97,6 +97,14 @@ wa_status launch_attn_tc(const void* q, int n_q, const void* k_main, const void*
                          const float* w_old, const float* w_new, int max_split, cudaStream_t s,
                          const SparseBlocks* sparse = nullptr);
 
+// FP8 E4M3 page codec (k_fp8.cu).  Rows are (token, head) rows of head_dim
+// values; codes and scales may live in pinned host memory (device-mapped pointers).
+wa_status launch_fp8_encode(const void* src, size_t n_rows, int head_dim, void* codes,
+                            float* scales, cudaStream_t s);
+wa_status launch_fp8_decode(const void* codes, const float* scales, const int32_t* idx, int n_pages,
+                            size_t page_rows, size_t n_rows, int head_dim, void* out,
+                            cudaStream_t s);
+
 // Block means of x [n_rows][row_elems] in blocks of `block` rows (ragged last block).
 wa_status launch_block_means(const void* x, wa_dtype dt, int n_rows, int block, int row_elems,
                              float* means_out, cudaStream_t s);

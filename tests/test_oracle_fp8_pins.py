@@ -69,3 +69,11 @@ def test_row_scale_and_error_bound():
 def test_encode_rejects_out_of_range_rounding():
     with pytest.raises(ValueError):
         O.e4m3_round(np.array([464.0]))
+
+
+def test_bf16_bits_agrees_with_torch():
+    rng = np.random.default_rng(5)
+    x = np.concatenate([rng.standard_normal(10000) * 7, rng.standard_normal(1000) * 1e-30,
+                        [0.0, -0.0, 1.0, -2.5, 65504.0]]).astype(np.float32)
+    ref = torch.from_numpy(x).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    assert np.array_equal(O.bf16_bits(x), ref)
