@@ -653,15 +653,24 @@ def run_stress(args, world, rank, local):
                                       torch.bfloat16)
     hk = torch.empty((NPG, P, H, D), dtype=torch.bfloat16, pin_memory=True)
     hv = torch.empty((NPG, P, H, D), dtype=torch.bfloat16, pin_memory=True)
+    # the compressed tier: the same pages as FP8 E4M3 codes + per-row scales
+    kc = torch.empty((NPG, P, H, D), dtype=torch.uint8, pin_memory=True)
+    vc = torch.empty((NPG, P, H, D), dtype=torch.uint8, pin_memory=True)
+    ksc = torch.empty((NPG, P, H), dtype=torch.float32, pin_memory=True)
+    vsc = torch.empty((NPG, P, H), dtype=torch.float32, pin_memory=True)
     kbar = torch.empty((NPG, H, D), dtype=torch.float32, device=dev)
     for j in range(NPG):
         kj, vj = g((1, P, H, D), ("k", j)), g((1, P, H, D), ("v", j))
         wa.wa_page_summarize(kj, kbar[j:j + 1])
         hk[j].copy_(kj[0])
         hv[j].copy_(vj[0])
+        wa.wa_fp8_encode(kj[0], kc[j], ksc[j])
+        wa.wa_fp8_encode(vj[0], vc[j], vsc[j])
+    torch.cuda.synchronize()
     o = torch.empty((NQ, H, D), dtype=torch.float32, device=dev)
     layers = [TierLayer(g((NQ, H, D), ("q", l)), g((NLOC, H, D), ("kl", l)),
-                        g((NLOC, H, D), ("vl", l)), kbar, hk, hv, o) for l in range(NL)]
+                        g((NLOC, H, D), ("vl", l)), kbar, hk, hv, o, kc, ksc, vc, vsc)
+              for l in range(NL)]
     pipe = TieredPipeline(KP, P, H, D, device=dev)
     torch.cuda.synchronize()
 
@@ -684,6 +693,8 @@ def run_stress(args, world, rank, local):
         t_pipe = timed("pipeline", reps)
     t_serial = timed("serial", 1)
     t_direct = timed("direct", reps)
+    t_fp8 = timed("fp8", reps)
+    t_fp8p = timed("fp8_pipeline", reps)
     t_copy = timed("copy", 1)
     t_attn = timed("attn", 1)
     wa.wa_check()
@@ -699,6 +710,8 @@ def run_stress(args, world, rank, local):
                                    "(one 9.2 GB store shared by the layers), top-4 of 120, H=12 "
                                    "d=128 bf16, 4,680 queries + 4,680 local per layer"},
             "serial_ms": round(t_serial, 3), "direct_ms": round(t_direct, 3),
+            "fp8_tier_ms": round(t_fp8, 3), "fp8_tier_pipeline_ms": round(t_fp8p, 3),
+            "fp8_tier_link_bytes_per_layer": 2 * KP * P * H * (D + 4),
             "copy_only_ms": round(t_copy, 3),
             "attn_only_ms": round(t_attn, 3), "h2d_gbs": round(h2d / (t_copy * 1e-3) / 1e9, 1),
             "copy_hidden_frac": hidden, "gpu_launches": NL * 2, "clocks": clk.summary()}

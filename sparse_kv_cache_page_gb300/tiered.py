@@ -23,7 +23,7 @@ from dataclasses import dataclass
 
 import torch
 
-from . import wa_block_attn, wa_gather_pages, wa_select_pages
+from . import wa_block_attn, wa_gather_pages, wa_gather_pages_fp8, wa_select_pages
 
 
 @dataclass
@@ -35,6 +35,12 @@ class TierLayer:
     k_host: torch.Tensor       # [n_pages][P][H][d] pinned host
     v_host: torch.Tensor
     out: torch.Tensor          # [n_q][H][d] device, fp32 or the input dtype
+    # compressed copy of the page bodies (FP8 E4M3 codes [n_pages][P][H][d] and
+    # scales [n_pages][P][H], pinned host), used by the "fp8" mode
+    k_codes: torch.Tensor | None = None
+    k_scales: torch.Tensor | None = None
+    v_codes: torch.Tensor | None = None
+    v_scales: torch.Tensor | None = None
 
 
 class TieredPipeline:
@@ -48,6 +54,31 @@ class TieredPipeline:
                       torch.empty(shape, dtype=dtype, device=device)) for _ in range(2)]
         self.side = torch.cuda.Stream(device=device)
         self.device = device
+        self.k_p, self.page_tokens, self.n_heads, self.head_dim = k_p, page_tokens, n_heads, head_dim
+        self.stage = None     # FP8 staging pages, allocated on first "fp8_pipeline" run
+
+    def _staging(self):
+        if self.stage is None:
+            P, H, d = self.page_tokens, self.n_heads, self.head_dim
+            mk = lambda *shape, dt: torch.empty(shape, dtype=dt, device=self.device)  # noqa: E731
+            self.stage = [dict(kc=mk(self.k_p, P, H, d, dt=torch.uint8),
+                               vc=mk(self.k_p, P, H, d, dt=torch.uint8),
+                               ks=mk(self.k_p, P, H, dt=torch.float32),
+                               vs=mk(self.k_p, P, H, dt=torch.float32)) for _ in range(2)]
+            self.ident = torch.arange(self.k_p, dtype=torch.int32, device=self.device)
+        return self.stage
+
+    def _fetch_fp8(self, ly, idx_host, st):
+        """Copy-engine fetch of k_p FP8 pages (codes viewed as 2-byte elements,
+        scales as one-float rows) into a staging slot."""
+        P, H, d = self.page_tokens, self.n_heads, self.head_dim
+        bf = lambda t: t.view(torch.bfloat16)  # noqa: E731
+        wa_gather_pages(bf(ly.k_codes), bf(ly.v_codes), None, idx_host, bf(st["kc"]), bf(st["vc"]),
+                        stream=self.side)
+        # a page's scales as one row of P*H floats (16-byte rows need P*H % 4 == 0)
+        wa_gather_pages(ly.k_scales.view(-1, 1, 1, P * H), ly.v_scales.view(-1, 1, 1, P * H), None,
+                        idx_host, st["ks"].view(-1, 1, P * H), st["vs"].view(-1, 1, P * H),
+                        stream=self.side)
 
     def run(self, layers, mode: str = "pipeline"):
         """Run all layers.  mode: "pipeline" (copy-engine fetches on a side
@@ -55,20 +86,43 @@ class TieredPipeline:
         attention, on one stream), "direct" (the gather kernel reads the pinned
         pages over the CPU-GPU link on the side stream, indices stay on the
         device, no host round trip), "copy" / "attn" (one half only, for
-        timing).  Returns the page indices [n_layers][k_p] (int32; pinned host
-        memory, or device memory in "direct" mode)."""
+        timing), "fp8" (as "direct", but the pages cross the link as FP8 codes
+        and scales and are decoded to bf16 on the device: the compressed DRAM
+        tier), "fp8_pipeline" (the FP8 pages fetched by the copy engine on the
+        side stream into a staging slot, decoded on the main stream before
+        the layer's attention).  Returns the page indices [n_layers][k_p]
+        (int32; pinned host memory, or device memory in "direct" and "fp8"
+        modes)."""
         main = torch.cuda.current_stream(self.device)
         n = len(layers)
         idx = torch.empty((n, self.k_p), dtype=torch.int32, device=self.device)
         for l, ly in enumerate(layers):
             wa_select_pages(ly.q, ly.kbar, None, None, 1, self.k_p, idx[l])
-        if mode == "direct":
-            return self._run_direct(layers, idx, main)
+        if mode in ("direct", "fp8"):
+            return self._run_direct(layers, idx, main, fp8=mode == "fp8")
         idx_h = torch.empty((n, self.k_p), dtype=torch.int32, pin_memory=True)
         idx_h.copy_(idx, non_blocking=True)
         main.synchronize()                         # indices reach the host once
         ev_copy = [torch.cuda.Event() for _ in range(n)]
         ev_attn = [torch.cuda.Event() for _ in range(n)]
+        if mode == "fp8_pipeline":
+            stage = self._staging()
+            ev_dec = [torch.cuda.Event() for _ in range(n)]
+            for l, ly in enumerate(layers):
+                kb, vb = self.bufs[l % 2]
+                st = stage[l % 2]
+                with torch.cuda.stream(self.side):
+                    if l >= 2:
+                        self.side.wait_event(ev_dec[l - 2])
+                    self._fetch_fp8(ly, idx_h[l], st)
+                    ev_copy[l].record(self.side)
+                main.wait_event(ev_copy[l])
+                wa_gather_pages_fp8(st["kc"], st["ks"], self.ident, kb)
+                wa_gather_pages_fp8(st["vc"], st["vs"], self.ident, vb)
+                ev_dec[l].record(main)
+                wa_block_attn(ly.q, kb, vb, ly.k_loc, ly.v_loc, ly.out)
+            main.wait_stream(self.side)
+            return idx_h
         for l, ly in enumerate(layers):
             kb, vb = self.bufs[l % 2]
             if mode == "serial":
@@ -88,7 +142,7 @@ class TieredPipeline:
         main.wait_stream(self.side)
         return idx_h
 
-    def _run_direct(self, layers, idx, main):
+    def _run_direct(self, layers, idx, main, fp8=False):
         ev_sel = torch.cuda.Event()
         ev_sel.record(main)
         n = len(layers)
@@ -98,7 +152,11 @@ class TieredPipeline:
             kb, vb = self.bufs[l % 2]
             with torch.cuda.stream(self.side):
                 self.side.wait_event(ev_sel if l < 2 else ev_attn[l - 2])
-                wa_gather_pages(ly.k_host, ly.v_host, idx[l], None, kb, vb, stream=self.side)
+                if fp8:
+                    wa_gather_pages_fp8(ly.k_codes, ly.k_scales, idx[l], kb, stream=self.side)
+                    wa_gather_pages_fp8(ly.v_codes, ly.v_scales, idx[l], vb, stream=self.side)
+                else:
+                    wa_gather_pages(ly.k_host, ly.v_host, idx[l], None, kb, vb, stream=self.side)
                 ev_copy[l].record(self.side)
             main.wait_event(ev_copy[l])
             wa_block_attn(ly.q, kb, vb, ly.k_loc, ly.v_loc, ly.out)
