@@ -77,3 +77,21 @@ def test_bf16_bits_agrees_with_torch():
                         [0.0, -0.0, 1.0, -2.5, 65504.0]]).astype(np.float32)
     ref = torch.from_numpy(x).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
     assert np.array_equal(O.bf16_bits(x), ref)
+
+
+def test_round_trip_is_idempotent():
+    """Re-encoding a decoded page (bf16) gives the same codes and scales: the
+    row maximum decodes back to itself (its code is 448 and 448 * s rounds to
+    the bf16 maximum), so the scale repeats, and every decoded value is within
+    a bf16 rounding (2^-9 relative) of an E4M3 value, far inside that value's
+    rounding interval (2^-4 relative).  A page that leaves HBM twice in a
+    compressed DRAM tier is therefore quantised once."""
+    rng = np.random.default_rng(11)
+    x = rng.standard_normal((200, 3, 128)) * np.exp(rng.standard_normal((200, 3, 1)) * 4.0)
+    x[5, 1] = 0.0                                             # a zero row
+    xb = O.bf16_bits(x.astype(np.float32))
+    c1, s1 = O.fp8_encode_rows(xb)
+    y = O.bf16_bits(O.fp8_decode_rows(c1, s1))
+    c2, s2 = O.fp8_encode_rows(y)
+    assert np.array_equal(s1, s2) and np.array_equal(c1, c2)
+    assert np.array_equal(O.bf16_bits(O.fp8_decode_rows(c2, s2)), y)
