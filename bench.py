@@ -18,6 +18,7 @@ bounded sample of the same workload instead.
 from __future__ import annotations
 
 import argparse
+import contextlib
 import json
 import math
 import os
@@ -479,36 +480,42 @@ def run_cache(args, world, rank, local):
     vb = torch.empty_like(kb)
     o = torch.empty((NQ, H, D), dtype=torch.float32, device=dev)
 
-    # the tiers are allocated once (8.5 GB of HBM and pinned DRAM); each video
-    # starts from an emptied cache (wa_cache_reset), outside the timed loop
-    cache = wa.WaCache(H, D, P, PPC, hbm_pages=16, host_pages=96, max_chunks=NCH,
-                       prompt_dim=PDIM)
-
-    def video():
+    # the tiers are allocated once per cache (HBM slots, staging ring and pinned
+    # DRAM: 9 GB with bf16 DRAM pages); each video starts from an emptied cache
+    # (wa_cache_reset), outside the timed loop
+    def video(cache):
         cache.append(ks[0], vs[0], prompts[0])
         for m in range(1, NCH):
             cache.retrieve(qs[m], curs[m], KP, kb, vb)
             wa.wa_block_attn(qs[m], kb, vb, ks[m][:NLOC], vs[m][:NLOC], o)
             cache.append(ks[m], vs[m], prompts[m])
+        cache.wait_copies()          # the last offloads belong to this video too
 
-    for _ in range(max(1, args.warmup - 2)):
-        cache.reset()
-        video()
-    torch.cuda.synchronize()
-    steps = max(1, min(args.steps, 5))
-    total = 0.0
-    with Clocks(local) as clk:
-        for _ in range(steps):
+    def timed(dram_fp8, clk=None):
+        cache = wa.WaCache(H, D, P, PPC, hbm_pages=16, host_pages=96, max_chunks=NCH,
+                           prompt_dim=PDIM, dram_fp8=dram_fp8)
+        for _ in range(max(1, args.warmup - 2)):
             cache.reset()
-            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            e0.record()
-            video()
-            e1.record()
-            torch.cuda.synchronize()
-            total += e0.elapsed_time(e1)
-    st = cache.stats()
-    cache.close()
-    ms = max_over_ranks(total, world) / steps
+            video(cache)
+        torch.cuda.synchronize()
+        steps = max(1, min(args.steps, 5))
+        total = 0.0
+        with (clk if clk is not None else contextlib.nullcontext()):
+            for _ in range(steps):
+                cache.reset()
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record()
+                video(cache)
+                e1.record()
+                torch.cuda.synchronize()
+                total += e0.elapsed_time(e1)
+        st = cache.stats()
+        cache.close()
+        return max_over_ranks(total, world) / steps, steps, st
+
+    clk = Clocks(local)
+    ms, steps, st = timed(False, clk)
+    ms8, _, st8 = timed(True)
     flops = (NCH - 1) * attn_flops(NQ, KP * P + NLOC, D, H)
     return {"metric": METRIC, "value": round(world * flops / (ms * 1e-3) / 1e12, 2),
             "unit": "TFLOP/s", "n_gpus": world, "steps": steps, "warmup": args.warmup,
@@ -516,12 +523,15 @@ def run_cache(args, world, rank, local):
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
             "data": "synthetic",
             "config": {"workload": "cache: 12 chunks x 8 pages x 12,480 tokens through the KV "
-                                   "cache manager (HBM tier 16 pages, pinned DRAM tier 96), "
-                                   "retrieve top-4 + attention + append per chunk, H=12 d=128 bf16",
+                                   "cache manager (HBM tier 16 pages, pinned DRAM tier 96, "
+                                   "inclusive, offloads on a copy stream), retrieve top-4 + "
+                                   "attention + append per chunk, H=12 d=128 bf16",
                        "value_is": "attention FLOPs of the 11 chunks / whole-loop time "
-                                   "(appends, offloads, fetches and promotions included; tier "
-                                   "allocation excluded)"},
+                                   "(appends, offloads, fetches and promotions included, the "
+                                   "last offloads waited for; tier allocation excluded)"},
             "cache_stats_per_video": st,
+            "fp8_dram_tier": {"ms_per_step": round(ms8, 3), "ms_per_chunk": round(ms8 / (NCH - 1), 3),
+                              "cache_stats_per_video": st8},
             "gpu_launches": steps * (NCH + 2 * (NCH - 1)),   # summaries per append; select + attention
             "clocks": clk.summary()}
 

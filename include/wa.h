@@ -362,21 +362,35 @@ wa_status wa_gather_pages_fp8(const uint8_t* code_pages, const float* scale_page
  *
  *   - pages of page_tokens tokens, pages_per_chunk per appended chunk, numbered
  *     in append order (chunk m owns pages m*ppc .. m*ppc + ppc - 1);
- *   - an HBM tier of hbm_pages page slots (K and V) and a pinned DRAM tier of
- *     host_pages slots; page summaries and prompt embeddings of every page stay
- *     in HBM;
- *   - append: pages to free HBM slots, the least recently used resident page
- *     offloaded to DRAM (copy engine) when none is free; summaries computed at
- *     insert;
+ *   - an HBM tier of hbm_pages page slots (K and V) and a pinned, device-mapped
+ *     DRAM tier of host_pages slots; page summaries and prompt embeddings of
+ *     every page stay in HBM;
+ *   - the DRAM tier is inclusive: a page keeps its DRAM copy when promoted
+ *     back to HBM (pages never change once appended), so evicting it again
+ *     copies nothing;
+ *   - dram_fp8 != 0 stores DRAM pages as FP8 E4M3 codes with per-(token, head)
+ *     scales (the wa_fp8_encode format; bf16 caches with head_dim 64, 128 or
+ *     256): a page read back from DRAM is decode(encode(page)), bit for bit,
+ *     and stays so when promoted (its HBM copy is the decoded page);
+ *   - append: pages to free HBM slots; when none is free the least recently
+ *     used resident page leaves HBM: with no copy if it has a DRAM copy, else
+ *     offloaded to the lowest free DRAM slot, or, with none free, to the slot of
+ *     the most recently used page holding both copies (whose DRAM copy is
+ *     dropped); summaries computed at insert;
+ *   - offloads run on an internal copy stream from a device staging ring of
+ *     pages_per_chunk + 4 pages, so they overlap the caller's later work;
+ *     reads of a DRAM slot wait (device-side) for its copy to land;
  *   - retrieve: wa_select_pages over the cached pages, indices to the host (one
  *     synchronisation of `stream`), each page copied into the caller's buffer
- *     from its tier; pages fetched from DRAM are promoted back to HBM, swapping
- *     with the least recently used page not selected now;
+ *     from HBM if it has an HBM copy, else from DRAM; pages found only in DRAM
+ *     are promoted to HBM from the caller's buffer (a promotion that finds no
+ *     DRAM slot for its victim gives up the promoted page's own DRAM copy);
  *   - window: the last n tokens of the sequence, contiguous (range access).
  * The LRU clock ticks once per append and per retrieval (ties: lower page).
- * dry_run != 0 makes a cache with no device memory and no CUDA calls whose
- * placement decisions can be driven with wa_cache_touch (host-logic tests).
- * Not thread-safe; one cache per layer.
+ * Every call of one cache must use the same stream (its copies are ordered
+ * against that stream).  dry_run != 0 makes a cache with no device memory and
+ * no CUDA calls whose placement decisions can be driven with wa_cache_touch
+ * (host-logic tests).  Not thread-safe; one cache per layer.
  */
 typedef struct wa_cache wa_cache;
 
@@ -390,16 +404,23 @@ typedef struct {
   int host_pages;       /* pinned DRAM tier capacity (pages, >= 0) */
   int max_chunks;       /* chunks the cache can hold */
   int dry_run;          /* 1: placement only, no device memory or copies */
+  int dram_fp8;         /* 1: DRAM tier holds FP8 E4M3 codes + scales */
 } wa_cache_config;
 
 typedef struct {
-  int n_pages, n_chunks, in_hbm, in_host;
-  long long offloads, promotions;             /* page moves HBM -> DRAM, DRAM -> HBM */
-  long long bytes_h2d, bytes_d2h, bytes_d2d;  /* K+V bytes moved (dry run: planned) */
+  int n_pages, n_chunks;
+  int in_hbm, in_host;                        /* pages with an HBM / a DRAM copy */
+  long long offloads, promotions;             /* page copies HBM -> DRAM, DRAM -> HBM */
+  long long bytes_h2d, bytes_d2h, bytes_d2d;  /* K+V bytes moved (dry run: planned); DRAM
+                                                 bytes in the tier's format, staging
+                                                 copies not counted */
+  long long evictions;                        /* HBM copies dropped with no copy */
+  long long reclaims;                         /* DRAM copies dropped to free a slot */
 } wa_cache_stats;
 
-/* Errors: WA_ERR_INVALID_ARG, WA_ERR_DTYPE, WA_ERR_SHAPE (head rows not whole
- * 16-byte vectors), WA_ERR_OOM (allocation failed). */
+/* Errors: WA_ERR_INVALID_ARG, WA_ERR_DTYPE (also dram_fp8 with a non-bf16
+ * dtype), WA_ERR_SHAPE (head rows not whole 16-byte vectors; dram_fp8 with
+ * head_dim not 64, 128 or 256), WA_ERR_OOM (allocation failed). */
 wa_status wa_cache_create(const wa_cache_config* cfg, wa_cache** out);
 /* Synchronizes the device (unless dry_run) and frees the cache. */
 wa_status wa_cache_destroy(wa_cache* cache);
@@ -422,8 +443,15 @@ wa_status wa_cache_window(wa_cache* cache, int n_tokens, void* k_out, void* v_ou
                           wa_stream_t stream);
 /* Dry-run caches only: use pages as one retrieval would (LRU and promotion). */
 wa_status wa_cache_touch(wa_cache* cache, const int32_t* pages, int n);
-/* tier: 0 HBM, 1 DRAM; slot within the tier.  WA_ERR_INDEX for unknown pages. */
+/* Where a read of the page goes: tier 0 (HBM) with its HBM slot if it has an
+ * HBM copy, else tier 1 with its DRAM slot.  WA_ERR_INDEX for unknown pages. */
 wa_status wa_cache_page_location(const wa_cache* cache, int page, int* tier, int* slot);
+/* Both copies of a page: its HBM slot and its DRAM slot, -1 where it has none. */
+wa_status wa_cache_page_slots(const wa_cache* cache, int page, int* hbm_slot, int* host_slot);
+/* Make `stream` wait (device-side, no host synchronisation) for every offload
+ * copy issued so far, e.g. to time a loop whole or before reading DRAM slots on
+ * the host.  A no-op for dry-run caches. */
+wa_status wa_cache_wait_copies(wa_cache* cache, wa_stream_t stream);
 wa_status wa_cache_get_stats(const wa_cache* cache, wa_cache_stats* out);
 
 /*

@@ -51,20 +51,23 @@ EXPORTED_SYMBOLS = ("wa_strerror", "wa_version", "wa_page_summarize", "wa_select
                     "wa_cache_destroy", "wa_cache_reset", "wa_cache_append_chunk",
                     "wa_cache_retrieve",
                     "wa_cache_window", "wa_cache_touch", "wa_cache_page_location",
-                    "wa_cache_get_stats", "wa_fp8_encode", "wa_fp8_decode",
+                    "wa_cache_get_stats", "wa_cache_page_slots", "wa_cache_wait_copies",
+                    "wa_fp8_encode", "wa_fp8_decode",
                     "wa_gather_pages_fp8", "wa_check", "wa_shutdown")
 
 
 class _CacheConfig(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int) for n in ("n_heads", "head_dim", "dtype", "page_tokens",
                                              "pages_per_chunk", "prompt_dim", "hbm_pages",
-                                             "host_pages", "max_chunks", "dry_run")]
+                                             "host_pages", "max_chunks", "dry_run",
+                                             "dram_fp8")]
 
 
 class _CacheStats(ctypes.Structure):
     _fields_ = ([(n, ctypes.c_int) for n in ("n_pages", "n_chunks", "in_hbm", "in_host")]
                 + [(n, ctypes.c_longlong) for n in ("offloads", "promotions", "bytes_h2d",
-                                                    "bytes_d2h", "bytes_d2d")])
+                                                    "bytes_d2h", "bytes_d2d", "evictions",
+                                                    "reclaims")])
 
 
 class WaError(RuntimeError):
@@ -109,6 +112,8 @@ def load():
         "wa_cache_touch": (I, [P, P, I]),
         "wa_cache_page_location": (I, [P, I, ctypes.POINTER(I), ctypes.POINTER(I)]),
         "wa_cache_get_stats": (I, [P, ctypes.POINTER(_CacheStats)]),
+        "wa_cache_page_slots": (I, [P, I, ctypes.POINTER(I), ctypes.POINTER(I)]),
+        "wa_cache_wait_copies": (I, [P, P]),
         "wa_fp8_encode": (I, [P, I, I, I, P, P, P]),
         "wa_fp8_decode": (I, [P, P, I, I, I, P, P]),
         "wa_gather_pages_fp8": (I, [P, P, I, I, I, I, P, I, P, P]),
@@ -334,16 +339,17 @@ def wa_gather_pages_fp8(code_pages: torch.Tensor, scale_pages: torch.Tensor, idx
 
 
 class WaCache:
-    """KV cache manager (libwa wa_cache_*): HBM and pinned-DRAM page tiers,
-    summaries at insert, retrieval with LRU offload and promotion, window
-    access.  ``dry_run`` caches plan placements without any CUDA work."""
+    """KV cache manager (libwa wa_cache_*): HBM and inclusive pinned-DRAM page
+    tiers (optionally FP8 in DRAM), summaries at insert, retrieval with LRU
+    eviction, overlapped offloads and promotion, window access.  ``dry_run``
+    caches plan placements without any CUDA work."""
 
     def __init__(self, n_heads: int, head_dim: int, page_tokens: int, pages_per_chunk: int,
                  hbm_pages: int, host_pages: int, max_chunks: int, prompt_dim: int = 0,
-                 dtype=torch.bfloat16, dry_run: bool = False):
+                 dtype=torch.bfloat16, dry_run: bool = False, dram_fp8: bool = False):
         cfg = _CacheConfig(n_heads, head_dim, WA_BF16 if dtype == torch.bfloat16 else WA_F32,
                            page_tokens, pages_per_chunk, prompt_dim, hbm_pages, host_pages,
-                           max_chunks, int(bool(dry_run)))
+                           max_chunks, int(bool(dry_run)), int(bool(dram_fp8)))
         h = ctypes.c_void_p()
         _ok("wa_cache_create", load().wa_cache_create(ctypes.byref(cfg), ctypes.byref(h)))
         self._h = h
@@ -392,6 +398,18 @@ class WaCache:
         _ok("wa_cache_page_location", load().wa_cache_page_location(
             self._h, page, ctypes.byref(t), ctypes.byref(s)))
         return t.value, s.value
+
+    def slots(self, page: int):
+        """(HBM slot, DRAM slot) of a page, -1 where it has no copy."""
+        h, x = ctypes.c_int(), ctypes.c_int()
+        _ok("wa_cache_page_slots", load().wa_cache_page_slots(
+            self._h, page, ctypes.byref(h), ctypes.byref(x)))
+        return h.value, x.value
+
+    def wait_copies(self, stream=None):
+        """Make the stream wait for every offload copy issued so far."""
+        _ok("wa_cache_wait_copies", load().wa_cache_wait_copies(
+            self._h, None if self.cfg.dry_run else _stream(stream)))
 
     def stats(self) -> dict:
         st = _CacheStats()

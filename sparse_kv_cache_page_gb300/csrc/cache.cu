@@ -8,19 +8,35 @@
 // Inferix (summary page), KV Cache Manager: append a clean block's KV, range
 // (window) access, index-based selective fetch, offload to main memory.
 //
-// Host-side runtime (no kernels of its own):
-//   * page table: logical page p (chunk p / ppc) -> tier (HBM / DRAM) and slot;
+// Host-side runtime around a few kernels of the library:
+//   * page table: logical page p (chunk p / ppc) -> HBM slot and/or DRAM slot.
+//     The DRAM tier is inclusive: pages never change once appended, so a
+//     page's DRAM copy stays valid after it is promoted back to HBM, and
+//     evicting such a page again moves no bytes;
 //   * HBM tier: one device pool of hbm_pages page slots (K and V); DRAM tier:
-//     one pinned pool of host_pages slots; summaries [max pages][H][d] and
-//     prompt embeddings [max chunks][prompt_dim] stay in HBM for every page;
+//     one pinned, device-mapped pool of host_pages slots, holding either the
+//     cache's dtype or FP8 E4M3 codes plus per-(token, head) scales (dram_fp8,
+//     the compressed tier: half the bytes across the CPU-GPU link);
+//     summaries [max pages][H][d] and prompt embeddings [max chunks][prompt_dim]
+//     stay in HBM for every page;
 //   * append: the chunk's pages go to free HBM slots; when none is free the
-//     least recently used resident page moves to the DRAM tier (copy engine);
+//     least recently used resident page leaves HBM -- with no copy when it
+//     already has a DRAM copy, else offloaded to a free DRAM slot (or to one
+//     reclaimed from the most recently used page that holds both copies);
 //     page summaries are computed at insert (wa_page_summarize on the chunk);
+//   * offloads overlap the caller's work: the victim is copied (or FP8-encoded)
+//     into a device staging ring on the caller's stream, which then reuses the
+//     HBM slot at once, and an internal copy stream moves the staging slot to
+//     DRAM.  Events order every reuse: a staging slot is rewritten only after
+//     its copy to DRAM finished, a DRAM slot is read only after its copy
+//     landed, and each copy to DRAM starts after the caller's stream reached
+//     the staging write (so after every earlier read of the DRAM slot);
 //   * retrieve: prompt stage + page stage over the summaries (wa_select_pages),
-//     the K_p indices to the host (one stream synchronisation), each selected
-//     page copied into the caller's buffer from its tier; a page fetched from
-//     DRAM is promoted back to HBM, swapping with the least recently used page
-//     not selected in this retrieval;
+//     the K_p indices written to mapped host memory (one stream
+//     synchronisation, no copy-engine transfer to queue behind offloads), each selected
+//     page copied into the caller's buffer from its tier (FP8 pages decoded
+//     straight from DRAM through the device mapping); a page found only in
+//     DRAM is promoted to HBM from the caller's buffer;
 //   * window: the last n tokens of the sequence, contiguous, from either tier.
 // The least-recently-used clock ticks once per append and per retrieval.
 // dry_run caches do no CUDA work at all: moves are planned and counted, so
@@ -36,12 +52,14 @@
 
 struct wa_cache {
   wa_cache_config cfg;
-  size_t page_bytes = 0;          // one tensor (K or V) of one page
+  size_t page_bytes = 0;          // one tensor (K or V) of one page in HBM
+  size_t host_page_bytes = 0;     // the same in the DRAM tier (slot stride)
+  size_t code_bytes = 0;          // FP8 tier: codes of one page tensor; its scales follow
   int n_pages = 0, n_chunks = 0;
   unsigned long long clock = 0;
   struct Entry {
-    int tier;                     // 0 HBM, 1 DRAM
-    int slot;
+    int hbm;                      // HBM slot or -1
+    int host;                     // DRAM slot or -1
     unsigned long long last_use;
   };
   std::vector<Entry> table;       // by logical page
@@ -49,12 +67,24 @@ struct wa_cache {
   std::vector<int> host_owner;
   char* hbm_k = nullptr;
   char* hbm_v = nullptr;
-  char* host_k = nullptr;
+  char* host_k = nullptr;         // pinned, device-mapped
   char* host_v = nullptr;
+  char* host_k_dev = nullptr;     // their device addresses
+  char* host_v_dev = nullptr;
+  char* stage_k = nullptr;        // staging ring [n_stage][host_page_bytes]
+  char* stage_v = nullptr;
+  int n_stage = 0, next_stage = 0;
+  cudaStream_t copy = nullptr;    // staging -> DRAM copies
+  cudaEvent_t filled = nullptr;   // caller's stream passed a staging write
+  cudaEvent_t drained = nullptr;  // copy stream passed its latest copy
+  std::vector<cudaEvent_t> stage_done;  // staging slot's last copy out finished
+  std::vector<cudaEvent_t> host_ready;  // DRAM slot's last copy in finished
+  std::vector<char> stage_pending, host_pending;
+  bool copies_issued = false;
   float* kbar = nullptr;          // [max_pages][H][d]
   float* prompts = nullptr;       // [max_chunks][prompt_dim]
-  int32_t* idx_dev = nullptr;     // [k_p max]
-  int32_t* idx_host = nullptr;    // pinned
+  int32_t* idx_host = nullptr;    // [k_p max], pinned and device-mapped
+  int32_t* idx_dev = nullptr;     // its device address
   int idx_cap = 0;
   wa_cache_stats stats{};
 };
@@ -65,6 +95,7 @@ using wa::cuda_status;
 
 inline bool dt_ok(wa_dtype dt) { return dt == WA_BF16 || dt == WA_F32; }
 inline size_t dt_size(wa_dtype dt) { return dt == WA_BF16 ? 2 : 4; }
+inline bool fp8(const wa_cache* c) { return c->cfg.dram_fp8 != 0; }
 
 int free_slot(const std::vector<int>& owner) {
   for (size_t s = 0; s < owner.size(); ++s)
@@ -72,26 +103,24 @@ int free_slot(const std::vector<int>& owner) {
   return -1;
 }
 
-// Least recently used page in `tier`, skipping pages marked in `keep`
+// Least recently used page with an HBM copy, skipping pages marked in `keep`
 // (ties to the lower page number).
-int lru_page(const wa_cache* c, int tier, const std::vector<char>* keep) {
+int lru_resident(const wa_cache* c, const std::vector<char>* keep) {
   int best = -1;
   for (int p = 0; p < c->n_pages; ++p) {
     const wa_cache::Entry& e = c->table[p];
-    if (e.tier != tier || (keep && (*keep)[p])) continue;
+    if (e.hbm < 0 || (keep && (*keep)[p])) continue;
     if (best < 0 || e.last_use < c->table[best].last_use) best = p;
   }
   return best;
 }
 
-char* tier_ptr(wa_cache* c, int tier, int slot, bool v) {
-  char* base = tier == 0 ? (v ? c->hbm_v : c->hbm_k) : (v ? c->host_v : c->host_k);
-  return base + (size_t)slot * c->page_bytes;
+char* hbm_ptr(wa_cache* c, int slot, bool v) {
+  return (v ? c->hbm_v : c->hbm_k) + (size_t)slot * c->page_bytes;
 }
-
-wa_status copy_page(wa_cache* c, void* dst, const void* src, cudaMemcpyKind kind, cudaStream_t s) {
-  if (c->cfg.dry_run) return WA_OK;
-  return cuda_status(cudaMemcpyAsync(dst, src, c->page_bytes, kind, s));
+char* host_ptr(wa_cache* c, int slot, bool v, bool device_address) {
+  char* base = device_address ? (v ? c->host_v_dev : c->host_k_dev) : (v ? c->host_v : c->host_k);
+  return base + (size_t)slot * c->host_page_bytes;
 }
 
 void count_bytes(wa_cache* c, cudaMemcpyKind kind, size_t bytes) {
@@ -100,82 +129,183 @@ void count_bytes(wa_cache* c, cudaMemcpyKind kind, size_t bytes) {
   else c->stats.bytes_d2d += (long long)bytes;
 }
 
-// Move page p from HBM to a free DRAM slot (K and V).
-wa_status offload(wa_cache* c, int p, cudaStream_t s) {
-  const int hs = free_slot(c->host_owner);
-  if (hs < 0) return WA_ERR_OOM;
-  wa_cache::Entry& e = c->table[p];
-  for (int t = 0; t < 2; ++t) {
-    wa_status rc = copy_page(c, tier_ptr(c, 1, hs, t), tier_ptr(c, 0, e.slot, t),
-                             cudaMemcpyDeviceToHost, s);
-    if (rc != WA_OK) return rc;
-    count_bytes(c, cudaMemcpyDeviceToHost, c->page_bytes);
+// Bytes of `rows` (token, head) rows in the DRAM tier's format.
+size_t host_row_bytes(const wa_cache* c, size_t rows) {
+  const size_t d = (size_t)c->cfg.head_dim;
+  return fp8(c) ? rows * (d + sizeof(float)) : rows * d * dt_size(c->cfg.dtype);
+}
+
+// Make `s` wait until DRAM slot x holds its latest copy.
+wa_status wait_host_slot(wa_cache* c, int x, cudaStream_t s) {
+  if (c->cfg.dry_run || !c->host_pending[x]) return WA_OK;
+  return cuda_status(cudaStreamWaitEvent(s, c->host_ready[x], 0));
+}
+
+// A DRAM slot for an offload: a free one, else one reclaimed from the most
+// recently used page holding both copies (ties: lower page), else (for a
+// promotion whose data is already on the device) the promoted page's own.
+int acquire_host_slot(wa_cache* c, int self_page) {
+  int x = free_slot(c->host_owner);
+  if (x >= 0) return x;
+  int w = -1;
+  for (int p = 0; p < c->n_pages; ++p) {
+    const wa_cache::Entry& e = c->table[p];
+    if (e.hbm >= 0 && e.host >= 0 && (w < 0 || e.last_use > c->table[w].last_use)) w = p;
   }
-  c->hbm_owner[e.slot] = -1;
-  c->host_owner[hs] = p;
-  e.tier = 1;
-  e.slot = hs;
+  if (w < 0 && self_page >= 0 && c->table[self_page].host >= 0) w = self_page;
+  if (w < 0) return -1;
+  x = c->table[w].host;
+  c->table[w].host = -1;
+  c->host_owner[x] = -1;
+  c->stats.reclaims++;
+  return x;
+}
+
+// Copy page v (HBM only) to DRAM slot x through the staging ring.
+wa_status offload(wa_cache* c, int v, int x, cudaStream_t s) {
+  wa_cache::Entry& e = c->table[v];
+  if (!c->cfg.dry_run) {
+    const int r = c->next_stage;
+    c->next_stage = (r + 1) % c->n_stage;
+    if (c->stage_pending[r] && cudaStreamWaitEvent(s, c->stage_done[r], 0) != cudaSuccess)
+      return WA_ERR_CUDA;
+    const size_t rows = (size_t)c->cfg.page_tokens * c->cfg.n_heads;
+    for (int t = 0; t < 2; ++t) {
+      char* st = (t ? c->stage_v : c->stage_k) + (size_t)r * c->host_page_bytes;
+      wa_status rc =
+          fp8(c) ? wa::launch_fp8_encode(hbm_ptr(c, e.hbm, t), rows, c->cfg.head_dim, st,
+                                         reinterpret_cast<float*>(st + c->code_bytes), s)
+                 : cuda_status(cudaMemcpyAsync(st, hbm_ptr(c, e.hbm, t), c->page_bytes,
+                                               cudaMemcpyDeviceToDevice, s));
+      if (rc != WA_OK) return rc;
+    }
+    if (cudaEventRecord(c->filled, s) != cudaSuccess ||
+        cudaStreamWaitEvent(c->copy, c->filled, 0) != cudaSuccess)
+      return WA_ERR_CUDA;
+    for (int t = 0; t < 2; ++t) {
+      const char* st = (t ? c->stage_v : c->stage_k) + (size_t)r * c->host_page_bytes;
+      if (cudaMemcpyAsync(host_ptr(c, x, t, false), st, c->host_page_bytes,
+                          cudaMemcpyDeviceToHost, c->copy) != cudaSuccess)
+        return WA_ERR_CUDA;
+    }
+    if (cudaEventRecord(c->stage_done[r], c->copy) != cudaSuccess ||
+        cudaEventRecord(c->host_ready[x], c->copy) != cudaSuccess)
+      return WA_ERR_CUDA;
+    c->stage_pending[r] = 1;
+    c->host_pending[x] = 1;
+    c->copies_issued = true;
+  }
+  count_bytes(c, cudaMemcpyDeviceToHost, 2 * c->host_page_bytes);
+  c->host_owner[x] = v;
+  e.host = x;
   c->stats.offloads++;
   return WA_OK;
 }
 
-// A free HBM slot, offloading the least recently used resident page (not in
+// Take page v out of HBM (its slot is then free).
+wa_status evict(wa_cache* c, int v, int self_page, cudaStream_t s) {
+  wa_cache::Entry& e = c->table[v];
+  if (e.host >= 0) {
+    c->stats.evictions++;
+  } else {
+    const int x = acquire_host_slot(c, self_page);
+    if (x < 0) return WA_ERR_OOM;
+    wa_status rc = offload(c, v, x, s);
+    if (rc != WA_OK) return rc;
+  }
+  c->hbm_owner[e.hbm] = -1;
+  e.hbm = -1;
+  return WA_OK;
+}
+
+// A free HBM slot, evicting the least recently used resident page (not in
 // `keep`) when none is free.
-wa_status hbm_slot(wa_cache* c, const std::vector<char>* keep, cudaStream_t s, int* slot) {
+wa_status hbm_slot(wa_cache* c, const std::vector<char>* keep, int self_page, cudaStream_t s,
+                   int* slot) {
   int hs = free_slot(c->hbm_owner);
   if (hs < 0) {
-    const int victim = lru_page(c, 0, keep);
+    const int victim = lru_resident(c, keep);
     if (victim < 0) return WA_ERR_OOM;
-    const int vslot = c->table[victim].slot;
-    wa_status rc = offload(c, victim, s);
+    hs = c->table[victim].hbm;
+    wa_status rc = evict(c, victim, self_page, s);
     if (rc != WA_OK) return rc;
-    hs = vslot;
   }
   *slot = hs;
   return WA_OK;
 }
 
-// Promote page p (in DRAM) into HBM: the least recently used resident page
-// not in `keep` moves to DRAM first when HBM is full.  When the page's K and V
-// are already on the device (from_k, from_v: the caller's retrieval buffer,
-// filled earlier on the same stream) its DRAM slot is released first, so the
-// evicted page can take it (a swap); otherwise the page is copied from DRAM.
+// Promote page p (DRAM only) into HBM from its copy in the caller's buffer
+// (from_k, from_v: filled earlier on the same stream).  Its DRAM copy stays.
 wa_status promote(wa_cache* c, int p, const std::vector<char>& keep, const char* from_k,
                   const char* from_v, cudaStream_t s) {
-  wa_cache::Entry& e = c->table[p];
-  const int old_host = e.slot;
-  const bool on_device = (from_k && from_v) || c->cfg.dry_run;
-  if (on_device) c->host_owner[old_host] = -1;
   int hs = -1;
-  wa_status rc = hbm_slot(c, &keep, s, &hs);
+  wa_status rc = hbm_slot(c, &keep, p, s, &hs);
   if (rc != WA_OK) return rc;
-  for (int t = 0; t < 2; ++t) {
-    const char* src = on_device ? (t ? from_v : from_k) : tier_ptr(c, 1, old_host, t);
-    const cudaMemcpyKind kind = on_device ? cudaMemcpyDeviceToDevice : cudaMemcpyHostToDevice;
-    rc = copy_page(c, tier_ptr(c, 0, hs, t), src, kind, s);
-    if (rc != WA_OK) return rc;
-    count_bytes(c, kind, c->page_bytes);
+  if (!c->cfg.dry_run) {
+    for (int t = 0; t < 2; ++t)
+      if (cudaMemcpyAsync(hbm_ptr(c, hs, t), t ? from_v : from_k, c->page_bytes,
+                          cudaMemcpyDeviceToDevice, s) != cudaSuccess)
+        return WA_ERR_CUDA;
   }
-  if (!on_device) c->host_owner[old_host] = -1;
+  count_bytes(c, cudaMemcpyDeviceToDevice, 2 * c->page_bytes);
   c->hbm_owner[hs] = p;
-  e.tier = 0;
-  e.slot = hs;
+  c->table[p].hbm = hs;
   c->stats.promotions++;
   return WA_OK;
+}
+
+// Copy `rows` (token, head) rows of page p, starting at row r0, into dst
+// (K or V) from the page's HBM copy if it has one, else from DRAM.
+wa_status read_page(wa_cache* c, int p, bool v, size_t r0, size_t rows, char* dst,
+                    cudaStream_t s) {
+  const wa_cache::Entry& e = c->table[p];
+  const size_t row_bytes = (size_t)c->cfg.head_dim * dt_size(c->cfg.dtype);
+  if (e.hbm >= 0) {
+    count_bytes(c, cudaMemcpyDeviceToDevice, rows * row_bytes);
+    return cuda_status(cudaMemcpyAsync(dst, hbm_ptr(c, e.hbm, v) + r0 * row_bytes,
+                                       rows * row_bytes, cudaMemcpyDeviceToDevice, s));
+  }
+  wa_status rc = wait_host_slot(c, e.host, s);
+  if (rc != WA_OK) return rc;
+  count_bytes(c, cudaMemcpyHostToDevice, host_row_bytes(c, rows));
+  if (fp8(c)) {
+    const char* base = host_ptr(c, e.host, v, true);
+    const uint8_t* codes = reinterpret_cast<const uint8_t*>(base) + r0 * c->cfg.head_dim;
+    const float* scales = reinterpret_cast<const float*>(base + c->code_bytes) + r0;
+    return wa::launch_fp8_decode(codes, scales, nullptr, 1, rows, rows, c->cfg.head_dim, dst, s);
+  }
+  return cuda_status(cudaMemcpyAsync(dst, host_ptr(c, e.host, v, false) + r0 * row_bytes,
+                                     rows * row_bytes, cudaMemcpyHostToDevice, s));
 }
 
 void release(wa_cache* c) {
   if (!c->cfg.dry_run) {
     cudaFree(c->hbm_k);
     cudaFree(c->hbm_v);
+    cudaFree(c->stage_k);
+    cudaFree(c->stage_v);
     cudaFreeHost(c->host_k);
     cudaFreeHost(c->host_v);
     cudaFree(c->kbar);
     cudaFree(c->prompts);
-    cudaFree(c->idx_dev);
     cudaFreeHost(c->idx_host);
+    for (cudaEvent_t ev : c->stage_done) cudaEventDestroy(ev);
+    for (cudaEvent_t ev : c->host_ready) cudaEventDestroy(ev);
+    if (c->filled) cudaEventDestroy(c->filled);
+    if (c->drained) cudaEventDestroy(c->drained);
+    if (c->copy) cudaStreamDestroy(c->copy);
   }
   delete c;
+}
+
+bool make_events(std::vector<cudaEvent_t>* evs, int n) {
+  evs->reserve(n);
+  for (int i = 0; i < n; ++i) {
+    cudaEvent_t ev = nullptr;
+    if (cudaEventCreateWithFlags(&ev, cudaEventDisableTiming) != cudaSuccess) return false;
+    evs->push_back(ev);
+  }
+  return true;
 }
 
 }  // namespace
@@ -191,30 +321,49 @@ wa_status wa_cache_create(const wa_cache_config* cfg, wa_cache** out) {
       g.hbm_pages <= 0 || g.host_pages < 0 || g.max_chunks <= 0 || g.prompt_dim < 0)
     return WA_ERR_INVALID_ARG;
   if (((long long)g.n_heads * g.head_dim * dt_size(g.dtype)) % 16 != 0) return WA_ERR_SHAPE;
+  if (g.dram_fp8) {
+    if (g.dtype != WA_BF16) return WA_ERR_DTYPE;
+    if (g.head_dim != 64 && g.head_dim != 128 && g.head_dim != 256) return WA_ERR_SHAPE;
+  }
   wa_cache* c = new (std::nothrow) wa_cache();
   if (!c) return WA_ERR_OOM;
   c->cfg = g;
-  c->page_bytes = (size_t)g.page_tokens * g.n_heads * g.head_dim * dt_size(g.dtype);
+  const size_t rows = (size_t)g.page_tokens * g.n_heads;
+  c->page_bytes = rows * g.head_dim * dt_size(g.dtype);
+  c->code_bytes = g.dram_fp8 ? rows * g.head_dim : 0;
+  c->host_page_bytes =
+      g.dram_fp8 ? c->code_bytes + (rows * sizeof(float) + 15) / 16 * 16 : c->page_bytes;
   c->hbm_owner.assign(g.hbm_pages, -1);
   c->host_owner.assign(g.host_pages, -1);
   c->table.reserve((size_t)g.max_chunks * g.pages_per_chunk);
   if (!g.dry_run) {
     const size_t max_pages = (size_t)g.max_chunks * g.pages_per_chunk;
+    c->n_stage = g.host_pages > 0 ? g.pages_per_chunk + 4 : 0;
     bool ok = cudaMalloc(&c->hbm_k, c->page_bytes * g.hbm_pages) == cudaSuccess &&
               cudaMalloc(&c->hbm_v, c->page_bytes * g.hbm_pages) == cudaSuccess &&
               cudaMalloc(&c->kbar, max_pages * g.n_heads * g.head_dim * sizeof(float)) == cudaSuccess &&
               cudaMalloc(&c->prompts, (size_t)g.max_chunks * (g.prompt_dim > 0 ? g.prompt_dim : 1) *
-                                          sizeof(float)) == cudaSuccess;
+                                          sizeof(float)) == cudaSuccess &&
+              cudaEventCreateWithFlags(&c->filled, cudaEventDisableTiming) == cudaSuccess &&
+              cudaEventCreateWithFlags(&c->drained, cudaEventDisableTiming) == cudaSuccess &&
+              cudaStreamCreateWithFlags(&c->copy, cudaStreamNonBlocking) == cudaSuccess &&
+              make_events(&c->stage_done, c->n_stage) && make_events(&c->host_ready, g.host_pages);
     if (ok && g.host_pages > 0)
-      ok = cudaHostAlloc((void**)&c->host_k, c->page_bytes * g.host_pages, cudaHostAllocDefault) ==
-               cudaSuccess &&
-           cudaHostAlloc((void**)&c->host_v, c->page_bytes * g.host_pages, cudaHostAllocDefault) ==
-               cudaSuccess;
+      ok = cudaMalloc(&c->stage_k, c->host_page_bytes * c->n_stage) == cudaSuccess &&
+           cudaMalloc(&c->stage_v, c->host_page_bytes * c->n_stage) == cudaSuccess &&
+           cudaHostAlloc((void**)&c->host_k, c->host_page_bytes * g.host_pages,
+                         cudaHostAllocMapped) == cudaSuccess &&
+           cudaHostAlloc((void**)&c->host_v, c->host_page_bytes * g.host_pages,
+                         cudaHostAllocMapped) == cudaSuccess &&
+           cudaHostGetDevicePointer((void**)&c->host_k_dev, c->host_k, 0) == cudaSuccess &&
+           cudaHostGetDevicePointer((void**)&c->host_v_dev, c->host_v, 0) == cudaSuccess;
     if (!ok) {
       cudaGetLastError();
       release(c);
       return WA_ERR_OOM;
     }
+    c->stage_pending.assign(c->n_stage, 0);
+    c->host_pending.assign(g.host_pages, 0);
   }
   *out = c;
   return WA_OK;
@@ -229,7 +378,13 @@ wa_status wa_cache_destroy(wa_cache* c) {
 
 wa_status wa_cache_reset(wa_cache* c) {
   if (!c) return WA_ERR_INVALID_ARG;
-  if (!c->cfg.dry_run) cudaDeviceSynchronize();   // no copy may still read or write a slot
+  if (!c->cfg.dry_run) {
+    cudaDeviceSynchronize();   // no copy may still read or write a slot
+    std::fill(c->stage_pending.begin(), c->stage_pending.end(), 0);
+    std::fill(c->host_pending.begin(), c->host_pending.end(), 0);
+    c->next_stage = 0;
+    c->copies_issued = false;
+  }
   c->table.clear();
   std::fill(c->hbm_owner.begin(), c->hbm_owner.end(), -1);
   std::fill(c->host_owner.begin(), c->host_owner.end(), -1);
@@ -238,6 +393,13 @@ wa_status wa_cache_reset(wa_cache* c) {
   c->clock = 0;
   c->stats = wa_cache_stats{};
   return WA_OK;
+}
+
+wa_status wa_cache_wait_copies(wa_cache* c, wa_stream_t stream) {
+  if (!c) return WA_ERR_INVALID_ARG;
+  if (c->cfg.dry_run || !c->copies_issued) return WA_OK;
+  if (cudaEventRecord(c->drained, c->copy) != cudaSuccess) return WA_ERR_CUDA;
+  return cuda_status(cudaStreamWaitEvent((cudaStream_t)stream, c->drained, 0));
 }
 
 wa_status wa_cache_append_chunk(wa_cache* c, const void* k, const void* v, const float* prompt,
@@ -272,24 +434,26 @@ wa_status wa_cache_append_chunk(wa_cache* c, const void* k, const void* v, const
     c->n_pages = p + 1;
     keep[p] = 1;
     int hs = -1;
-    wa_status rc = hbm_slot(c, &keep, s, &hs);
+    wa_status rc = hbm_slot(c, &keep, -1, s, &hs);
     if (rc != WA_OK) return rc;
-    for (int t = 0; t < 2; ++t) {
-      const char* src = static_cast<const char*>(t ? v : k);
-      rc = copy_page(c, tier_ptr(c, 0, hs, t), src ? src + (size_t)j * c->page_bytes : nullptr,
-                     cudaMemcpyDeviceToDevice, s);
-      if (rc != WA_OK) return rc;
-      count_bytes(c, cudaMemcpyDeviceToDevice, c->page_bytes);
+    if (!g.dry_run) {
+      for (int t = 0; t < 2; ++t) {
+        const char* src = static_cast<const char*>(t ? v : k) + (size_t)j * c->page_bytes;
+        if (cudaMemcpyAsync(hbm_ptr(c, hs, t), src, c->page_bytes, cudaMemcpyDeviceToDevice, s) !=
+            cudaSuccess)
+          return WA_ERR_CUDA;
+      }
     }
+    count_bytes(c, cudaMemcpyDeviceToDevice, 2 * c->page_bytes);
     c->hbm_owner[hs] = p;
-    c->table[p].tier = 0;
-    c->table[p].slot = hs;
+    c->table[p].hbm = hs;
   }
   c->n_chunks++;
   return WA_OK;
 }
 
-// Mark pages as used by one retrieval: LRU update, and pages in DRAM promoted to HBM.
+// Mark pages as used by one retrieval: LRU update, and pages found only in
+// DRAM promoted to HBM from the caller's buffer (dev_k[i], dev_v[i]).
 static wa_status use_pages(wa_cache* c, const int32_t* pages, int n, const char* const* dev_k,
                            const char* const* dev_v, cudaStream_t s) {
   c->clock++;
@@ -301,7 +465,7 @@ static wa_status use_pages(wa_cache* c, const int32_t* pages, int n, const char*
   for (int i = 0; i < n; ++i) {
     wa_cache::Entry& e = c->table[pages[i]];
     e.last_use = c->clock;
-    if (e.tier == 1) {
+    if (e.hbm < 0) {
       wa_status rc = promote(c, pages[i], keep, dev_k ? dev_k[i] : nullptr,
                              dev_v ? dev_v[i] : nullptr, s);
       if (rc != WA_OK) return rc;
@@ -323,17 +487,22 @@ wa_status wa_cache_retrieve(wa_cache* c, const void* q, int n_q, const float* pr
   const wa_cache_config& g = c->cfg;
   if (c->n_pages == 0) return WA_ERR_INVALID_ARG;
   cudaStream_t s = (cudaStream_t)stream;
+  // The selection kernel writes the indices straight into mapped host memory:
+  // a device-to-host copy here would queue behind the offloads on the copy
+  // engine, and the host waits for the indices.
   if (c->idx_cap < k_p) {
-    if (c->idx_dev) {
-      cudaFree(c->idx_dev);
+    if (c->idx_host) {
       cudaFreeHost(c->idx_host);
-      c->idx_dev = nullptr;
       c->idx_host = nullptr;
+      c->idx_dev = nullptr;
     }
-    if (cudaMalloc(&c->idx_dev, k_p * sizeof(int32_t)) != cudaSuccess ||
-        cudaHostAlloc((void**)&c->idx_host, k_p * sizeof(int32_t), cudaHostAllocDefault) !=
-            cudaSuccess) {
+    if (cudaHostAlloc((void**)&c->idx_host, k_p * sizeof(int32_t), cudaHostAllocMapped) !=
+            cudaSuccess ||
+        cudaHostGetDevicePointer((void**)&c->idx_dev, c->idx_host, 0) != cudaSuccess) {
       cudaGetLastError();
+      if (c->idx_host) cudaFreeHost(c->idx_host);
+      c->idx_host = nullptr;
+      c->idx_dev = nullptr;
       c->idx_cap = 0;
       return WA_ERR_OOM;
     }
@@ -345,27 +514,21 @@ wa_status wa_cache_retrieve(wa_cache* c, const void* q, int n_q, const float* pr
                                  prompts ? c->n_chunks : 0, g.prompt_dim, g.pages_per_chunk, k_p,
                                  c->idx_dev, nullptr, nullptr, stream);
   if (rc != WA_OK) return rc;
-  if (cudaMemcpyAsync(c->idx_host, c->idx_dev, k_p * sizeof(int32_t), cudaMemcpyDeviceToHost, s) !=
-          cudaSuccess ||
-      cudaStreamSynchronize(s) != cudaSuccess)
-    return WA_ERR_CUDA;
+  if (cudaStreamSynchronize(s) != cudaSuccess) return WA_ERR_CUDA;
   memcpy(idx_out, c->idx_host, k_p * sizeof(int32_t));
   std::vector<const char*> dk(k_p), dv(k_p);
+  const size_t rows = (size_t)g.page_tokens * g.n_heads;
   for (int i = 0; i < k_p; ++i) {
     const int p = idx_out[i];
     if (p < 0 || p >= c->n_pages) return WA_ERR_INDEX;
-    const wa_cache::Entry& e = c->table[p];
     char* dst_k = static_cast<char*>(k_buf) + (size_t)i * c->page_bytes;
     char* dst_v = static_cast<char*>(v_buf) + (size_t)i * c->page_bytes;
-    const cudaMemcpyKind kind = e.tier == 0 ? cudaMemcpyDeviceToDevice : cudaMemcpyHostToDevice;
-    rc = copy_page(c, dst_k, tier_ptr(c, e.tier, e.slot, false), kind, s);
-    if (rc == WA_OK) rc = copy_page(c, dst_v, tier_ptr(c, e.tier, e.slot, true), kind, s);
+    rc = read_page(c, p, false, 0, rows, dst_k, s);
+    if (rc == WA_OK) rc = read_page(c, p, true, 0, rows, dst_v, s);
     if (rc != WA_OK) return rc;
-    count_bytes(c, kind, 2 * c->page_bytes);
     dk[i] = dst_k;
     dv[i] = dst_v;
   }
-  // pages that came from DRAM are promoted from the caller's buffer (device to device)
   return use_pages(c, idx_out, k_p, dk.data(), dv.data(), s);
 }
 
@@ -376,22 +539,18 @@ wa_status wa_cache_window(wa_cache* c, int n_tokens, void* k_out, void* v_out, w
   const long long total = (long long)c->n_pages * g.page_tokens;
   if (n_tokens > total) return WA_ERR_SHAPE;
   cudaStream_t s = (cudaStream_t)stream;
-  const size_t row = c->page_bytes / g.page_tokens;
-  long long first = total - n_tokens;                 // first token of the window
+  const size_t row_bytes = (size_t)g.n_heads * g.head_dim * dt_size(g.dtype);   // one token
+  const long long first = total - n_tokens;            // first token of the window
   size_t out_off = 0;
   for (int p = (int)(first / g.page_tokens); p < c->n_pages; ++p) {
     const long long t0 = std::max(first, (long long)p * g.page_tokens) - (long long)p * g.page_tokens;
-    const size_t bytes = (size_t)(g.page_tokens - t0) * row;
-    const wa_cache::Entry& e = c->table[p];
-    const cudaMemcpyKind kind = e.tier == 0 ? cudaMemcpyDeviceToDevice : cudaMemcpyHostToDevice;
+    const size_t toks = (size_t)(g.page_tokens - t0);
     for (int t = 0; t < 2; ++t) {
-      if (cudaMemcpyAsync(static_cast<char*>(t ? v_out : k_out) + out_off,
-                          tier_ptr(c, e.tier, e.slot, t) + (size_t)t0 * row, bytes, kind, s) !=
-          cudaSuccess)
-        return WA_ERR_CUDA;
+      wa_status rc = read_page(c, p, t, (size_t)t0 * g.n_heads, toks * g.n_heads,
+                               static_cast<char*>(t ? v_out : k_out) + out_off, s);
+      if (rc != WA_OK) return rc;
     }
-    count_bytes(c, kind, 2 * bytes);
-    out_off += bytes;
+    out_off += toks * row_bytes;
   }
   return WA_OK;
 }
@@ -399,8 +558,17 @@ wa_status wa_cache_window(wa_cache* c, int n_tokens, void* k_out, void* v_out, w
 wa_status wa_cache_page_location(const wa_cache* c, int page, int* tier, int* slot) {
   if (!c || !tier || !slot) return WA_ERR_INVALID_ARG;
   if (page < 0 || page >= c->n_pages) return WA_ERR_INDEX;
-  *tier = c->table[page].tier;
-  *slot = c->table[page].slot;
+  const wa_cache::Entry& e = c->table[page];
+  *tier = e.hbm >= 0 ? 0 : 1;
+  *slot = e.hbm >= 0 ? e.hbm : e.host;
+  return WA_OK;
+}
+
+wa_status wa_cache_page_slots(const wa_cache* c, int page, int* hbm_slot, int* host_slot) {
+  if (!c || !hbm_slot || !host_slot) return WA_ERR_INVALID_ARG;
+  if (page < 0 || page >= c->n_pages) return WA_ERR_INDEX;
+  *hbm_slot = c->table[page].hbm;
+  *host_slot = c->table[page].host;
   return WA_OK;
 }
 
@@ -411,7 +579,10 @@ wa_status wa_cache_get_stats(const wa_cache* c, wa_cache_stats* out) {
   out->n_chunks = c->n_chunks;
   out->in_hbm = 0;
   out->in_host = 0;
-  for (int p = 0; p < c->n_pages; ++p) (c->table[p].tier == 0 ? out->in_hbm : out->in_host)++;
+  for (int p = 0; p < c->n_pages; ++p) {
+    out->in_hbm += c->table[p].hbm >= 0;
+    out->in_host += c->table[p].host >= 0;
+  }
   return WA_OK;
 }
 

@@ -9,7 +9,8 @@
 //   bf16 RNE( fp32(value(code) * s) ).
 // A zero row has s = 0 and codes 0.
 //
-// One warp per row (d = 32 e, e in {2, 4, 8} values per lane).  The
+// One warp per row (d = 32 e, e in {2, 4, 8} values per lane), four rows in
+// flight per warp.  The
 // gather-decode kernel reads the selected pages' codes and scales where they
 // live -- device memory or pinned host memory through its device mapping, so
 // a fetch from the DRAM tier moves the FP8 bytes only -- and writes the bf16
@@ -22,6 +23,7 @@ namespace wa {
 namespace {
 
 constexpr int kThreads = 256;
+constexpr int kRows = 4;      // rows per warp per step
 
 __device__ __forceinline__ uint16_t enc2(float lo, float hi) {
   uint16_t r;
@@ -51,30 +53,41 @@ __device__ __forceinline__ void unpack_bf16(const typename Vec<E>::In& in, float
   }
 }
 
+// Each warp takes kRows consecutive rows per step: their loads are issued
+// together, so enough bytes are in flight to stream at HBM (or link) speed.
 template <int E>
 __global__ void __launch_bounds__(kThreads)
 k_fp8_encode(const __nv_bfloat16* __restrict__ src, size_t n_rows, uint8_t* __restrict__ codes,
              float* __restrict__ scales) {
+  using In = typename Vec<E>::In;
   const int lane = threadIdx.x & 31;
-  const size_t warps = (size_t)gridDim.x * (kThreads / 32);
-  for (size_t r = (size_t)blockIdx.x * (kThreads / 32) + (threadIdx.x >> 5); r < n_rows; r += warps) {
-    using In = typename Vec<E>::In;
-    const In in = __ldcs(reinterpret_cast<const In*>(src + r * 32 * E) + lane);
-    float x[E];
-    unpack_bf16<E>(in, x);
-    float amax = 0.f;
+  const size_t step = (size_t)gridDim.x * (kThreads / 32) * kRows;
+  for (size_t r0 = ((size_t)blockIdx.x * (kThreads / 32) + (threadIdx.x >> 5)) * kRows; r0 < n_rows;
+       r0 += step) {
+    In in[kRows];
 #pragma unroll
-    for (int i = 0; i < E; ++i) amax = fmaxf(amax, fabsf(x[i]));
+    for (int j = 0; j < kRows; ++j)
+      if (r0 + j < n_rows) in[j] = __ldcs(reinterpret_cast<const In*>(src + (r0 + j) * 32 * E) + lane);
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
-    const float s = __fdiv_rn(amax, 448.0f);
-    typename Vec<E>::Code out;
-    uint16_t* o16 = reinterpret_cast<uint16_t*>(&out);
+    for (int j = 0; j < kRows; ++j) {
+      if (r0 + j >= n_rows) break;
+      const size_t r = r0 + j;
+      float x[E];
+      unpack_bf16<E>(in[j], x);
+      float amax = 0.f;
 #pragma unroll
-    for (int i = 0; i < E / 2; ++i)
-      o16[i] = s > 0.f ? enc2(__fdiv_rn(x[2 * i], s), __fdiv_rn(x[2 * i + 1], s)) : (uint16_t)0;
-    reinterpret_cast<typename Vec<E>::Code*>(codes + r * 32 * E)[lane] = out;
-    if (lane == 0) scales[r] = s;
+      for (int i = 0; i < E; ++i) amax = fmaxf(amax, fabsf(x[i]));
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+      const float s = __fdiv_rn(amax, 448.0f);
+      typename Vec<E>::Code out;
+      uint16_t* o16 = reinterpret_cast<uint16_t*>(&out);
+#pragma unroll
+      for (int i = 0; i < E / 2; ++i)
+        o16[i] = s > 0.f ? enc2(__fdiv_rn(x[2 * i], s), __fdiv_rn(x[2 * i + 1], s)) : (uint16_t)0;
+      reinterpret_cast<typename Vec<E>::Code*>(codes + r * 32 * E)[lane] = out;
+      if (lane == 0) scales[r] = s;
+    }
   }
 }
 
@@ -84,36 +97,52 @@ __global__ void __launch_bounds__(kThreads)
 k_fp8_decode(const uint8_t* __restrict__ codes, const float* __restrict__ scales,
              const int32_t* __restrict__ idx, int n_pages, size_t page_rows, size_t n_rows,
              __nv_bfloat16* __restrict__ out, Ctrl* ctrl) {
+  using Code = typename Vec<E>::Code;
   const int lane = threadIdx.x & 31;
-  const size_t warps = (size_t)gridDim.x * (kThreads / 32);
-  for (size_t r = (size_t)blockIdx.x * (kThreads / 32) + (threadIdx.x >> 5); r < n_rows; r += warps) {
-    size_t src_row = r;
-    bool bad = false;
-    if (idx) {
-      const int page = __ldg(idx + r / page_rows);
-      bad = page < 0 || page >= n_pages;
-      src_row = (size_t)(bad ? 0 : page) * page_rows + r % page_rows;
-    }
-    typename Vec<E>::In o;
-    uint32_t* ow = reinterpret_cast<uint32_t*>(&o);
-    if (bad) {
+  const size_t step = (size_t)gridDim.x * (kThreads / 32) * kRows;
+  for (size_t r0 = ((size_t)blockIdx.x * (kThreads / 32) + (threadIdx.x >> 5)) * kRows; r0 < n_rows;
+       r0 += step) {
+    Code c[kRows];
+    float sc[kRows];
+    bool bad[kRows];
 #pragma unroll
-      for (int i = 0; i < E / 2; ++i) ow[i] = 0u;
-      if (lane == 0 && r % page_rows == 0) atomicOr(&ctrl->status, kStatusIndex);
-    } else {
-      const typename Vec<E>::Code c = reinterpret_cast<const typename Vec<E>::Code*>(
-          codes + src_row * 32 * E)[lane];
-      const float s = scales[src_row];
-      const uint16_t* c16 = reinterpret_cast<const uint16_t*>(&c);
-#pragma unroll
-      for (int i = 0; i < E / 2; ++i) {
-        const float2 v = dec2(c16[i]);
-        const __nv_bfloat16 lo = __float2bfloat16_rn(__fmul_rn(v.x, s));
-        const __nv_bfloat16 hi = __float2bfloat16_rn(__fmul_rn(v.y, s));
-        ow[i] = (uint32_t)__bfloat16_as_ushort(lo) | ((uint32_t)__bfloat16_as_ushort(hi) << 16);
+    for (int j = 0; j < kRows; ++j) {
+      const size_t r = r0 + j;
+      bad[j] = false;
+      if (r >= n_rows) continue;
+      size_t src_row = r;
+      if (idx) {
+        const int page = __ldg(idx + r / page_rows);
+        bad[j] = page < 0 || page >= n_pages;
+        src_row = (size_t)(bad[j] ? 0 : page) * page_rows + r % page_rows;
+      }
+      if (!bad[j]) {
+        c[j] = reinterpret_cast<const Code*>(codes + src_row * 32 * E)[lane];
+        sc[j] = scales[src_row];
       }
     }
-    reinterpret_cast<typename Vec<E>::In*>(out + r * 32 * E)[lane] = o;
+#pragma unroll
+    for (int j = 0; j < kRows; ++j) {
+      const size_t r = r0 + j;
+      if (r >= n_rows) break;
+      typename Vec<E>::In o;
+      uint32_t* ow = reinterpret_cast<uint32_t*>(&o);
+      if (bad[j]) {
+#pragma unroll
+        for (int i = 0; i < E / 2; ++i) ow[i] = 0u;
+        if (lane == 0 && r % page_rows == 0) atomicOr(&ctrl->status, kStatusIndex);
+      } else {
+        const uint16_t* c16 = reinterpret_cast<const uint16_t*>(&c[j]);
+#pragma unroll
+        for (int i = 0; i < E / 2; ++i) {
+          const float2 v = dec2(c16[i]);
+          const __nv_bfloat16 lo = __float2bfloat16_rn(__fmul_rn(v.x, sc[j]));
+          const __nv_bfloat16 hi = __float2bfloat16_rn(__fmul_rn(v.y, sc[j]));
+          ow[i] = (uint32_t)__bfloat16_as_ushort(lo) | ((uint32_t)__bfloat16_as_ushort(hi) << 16);
+        }
+      }
+      reinterpret_cast<typename Vec<E>::In*>(out + r * 32 * E)[lane] = o;
+    }
   }
 }
 
@@ -121,7 +150,8 @@ unsigned grid_for(size_t rows) {
   int dev = 0, sms = 148;
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  const size_t need = (rows + kThreads / 32 - 1) / (kThreads / 32);
+  const size_t per_block = (size_t)(kThreads / 32) * kRows;
+  const size_t need = (rows + per_block - 1) / per_block;
   const size_t cap = (size_t)sms * 8;
   return (unsigned)(need < cap ? need : cap);
 }

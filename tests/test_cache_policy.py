@@ -2,14 +2,19 @@
 caches (no device memory, no CUDA calls): page placement across the HBM and
 DRAM tiers under appends and retrievals, checked against a reference model
 written here from the stated policy -- pages to free HBM slots (lowest slot
-first), the least recently used resident page (ties: lower page) offloaded to
-the lowest free DRAM slot when HBM is full, pages of the current append or
-retrieval never evicted, a page used from DRAM promoted back to HBM after
-releasing its DRAM slot, one clock tick per append and per retrieval."""
+first); when HBM is full the least recently used resident page (ties: lower
+page) leaves it, pages of the current append or retrieval never; a leaving
+page with a DRAM copy moves nothing (the DRAM tier is inclusive: pages never
+change once appended), one without is offloaded to the lowest free DRAM slot,
+else to the slot of the most recently used page holding both copies (ties:
+lower page), else, in a promotion, to the promoted page's own; a page used
+from DRAM only is promoted back to HBM and keeps its DRAM copy; one clock
+tick per append and per retrieval."""
 
 import random
 
 import pytest
+import torch
 
 import sparse_kv_cache_page_gb300 as wa
 
@@ -17,30 +22,40 @@ import sparse_kv_cache_page_gb300 as wa
 class Model:
     def __init__(self, hbm, host, ppc):
         self.hbm, self.host, self.ppc = [None] * hbm, [None] * host, ppc
-        self.tab, self.clock, self.n, self.off, self.pro = {}, 0, 0, 0, 0
+        self.tab, self.clock, self.n = {}, 0, 0      # page -> [hbm slot, host slot, last use]
+        self.off = self.pro = self.evi = self.rec = 0
 
     @staticmethod
     def _free(arr):
         return next((i for i, x in enumerate(arr) if x is None), None)
 
-    def _lru(self, tier, keep):
-        c = [p for p, (t, _, _) in self.tab.items() if t == tier and p not in keep]
-        return min(c, key=lambda p: (self.tab[p][2], p)) if c else None
+    def _host_slot(self, self_page):
+        x = self._free(self.host)
+        if x is not None:
+            return x
+        both = [p for p, (h, hx, _) in self.tab.items() if h is not None and hx is not None]
+        w = min(both, key=lambda p: (-self.tab[p][2], p)) if both else None
+        if w is None and self_page is not None and self.tab[self_page][1] is not None:
+            w = self_page
+        assert w is not None
+        x = self.tab[w][1]
+        self.tab[w][1], self.host[x] = None, None
+        self.rec += 1
+        return x
 
-    def _offload(self, p):
-        hs = self._free(self.host)
-        assert hs is not None
-        _, s, u = self.tab[p]
-        self.hbm[s], self.host[hs] = None, p
-        self.tab[p] = (1, hs, u)
-        self.off += 1
-
-    def _hbm_slot(self, keep):
+    def _hbm_slot(self, keep, self_page=None):
         s = self._free(self.hbm)
         if s is None:
-            v = self._lru(0, keep)
-            s = self.tab[v][1]
-            self._offload(v)
+            res = [p for p, (h, _, _) in self.tab.items() if h is not None and p not in keep]
+            v = min(res, key=lambda p: (self.tab[p][2], p))
+            s = self.tab[v][0]
+            if self.tab[v][1] is not None:
+                self.evi += 1
+            else:
+                x = self._host_slot(self_page)
+                self.host[x], self.tab[v][1] = v, x
+                self.off += 1
+            self.hbm[s], self.tab[v][0] = None, None
         return s
 
     def append(self):
@@ -49,24 +64,28 @@ class Model:
         for _ in range(self.ppc):
             p = self.n
             self.n += 1
-            self.tab[p] = (-1, -1, self.clock)
+            self.tab[p] = [None, None, self.clock]
             keep.add(p)
             s = self._hbm_slot(keep)
-            self.hbm[s] = p
-            self.tab[p] = (0, s, self.clock)
+            self.hbm[s], self.tab[p][0] = p, s
 
     def touch(self, pages):
         self.clock += 1
         keep = set(pages)
         for p in pages:
-            t, s, _ = self.tab[p]
-            self.tab[p] = (t, s, self.clock)
-            if t == 1:
-                self.host[s] = None
-                hs = self._hbm_slot(keep)
-                self.hbm[hs] = p
-                self.tab[p] = (0, hs, self.clock)
+            self.tab[p][2] = self.clock
+            if self.tab[p][0] is None:
+                s = self._hbm_slot(keep, self_page=p)
+                self.hbm[s], self.tab[p][0] = p, s
                 self.pro += 1
+
+    def location(self, p):
+        h, x, _ = self.tab[p]
+        return (0, h) if h is not None else (1, x)
+
+    def slots(self, p):
+        h, x, _ = self.tab[p]
+        return (-1 if h is None else h, -1 if x is None else x)
 
 
 def _cache(hbm, host, ppc, max_chunks=64, page_tokens=16):
@@ -90,24 +109,63 @@ def test_placement_matches_reference_model(hbm, host, ppc, seed):
             c.touch(pages)
             m.touch(pages)
         for p in range(m.n):
-            assert c.location(p) == m.tab[p][:2], f"step {step}, page {p}"
+            assert c.location(p) == m.location(p), f"step {step}, page {p}"
+            assert c.slots(p) == m.slots(p), f"step {step}, page {p}"
         st = c.stats()
         assert st["n_pages"] == m.n and st["offloads"] == m.off and st["promotions"] == m.pro
+        assert st["evictions"] == m.evi and st["reclaims"] == m.rec
         assert st["in_hbm"] == sum(x is not None for x in m.hbm) <= hbm
-        assert st["in_hbm"] + st["in_host"] == m.n
+        assert st["in_host"] == sum(x is not None for x in m.host) <= host
+        # every page has at least one copy
+        assert all(c.slots(p) != (-1, -1) for p in range(m.n))
 
 
-def test_bytes_planned():
-    c = _cache(2, 4, 2, page_tokens=16)
-    page = 16 * 4 * 64 * 2
+@pytest.mark.parametrize("dram_fp8", [False, True])
+def test_bytes_planned(dram_fp8):
+    c = wa.WaCache(4, 64, 16, 2, hbm_pages=2, host_pages=4, max_chunks=64, dry_run=True,
+                   dram_fp8=dram_fp8)
+    page = 16 * 4 * 64 * 2                                  # bf16 K (or V) of one page
+    host_page = 16 * 4 * 64 + 16 * 4 * 4 if dram_fp8 else page   # FP8 codes + fp32 scales
     c.append(None, None)
     c.append(None, None)            # pages 0, 1 offloaded
-    c.touch([0])                    # page 0 back, page 2 (oldest of chunk 1) out
+    c.touch([0])                    # page 0 back (keeps its DRAM copy), page 2 out
     st = c.stats()
     assert st["bytes_d2d"] == 4 * 2 * page + 2 * page    # appends + the promotion
-    assert st["bytes_d2h"] == 3 * 2 * page               # three offloads
-    assert (st["offloads"], st["promotions"]) == (3, 1)
-    assert c.location(0) == (0, 0) and c.location(2)[0] == 1
+    assert st["bytes_d2h"] == 3 * 2 * host_page          # three offloads
+    assert (st["offloads"], st["promotions"], st["evictions"]) == (3, 1, 0)
+    assert c.location(0) == (0, 0) and c.slots(0) == (0, 0) and c.location(2) == (1, 2)
+    c.touch([2])                    # page 2 back, page 3 (HBM only) offloaded
+    c.touch([3])                    # page 3 back, page 0 leaves HBM with no copy
+    st = c.stats()
+    assert (st["offloads"], st["promotions"], st["evictions"]) == (4, 3, 1)
+    assert st["bytes_d2h"] == 4 * 2 * host_page
+    assert c.slots(0) == (-1, 0) and c.slots(3) == (0, 3)
+    assert (st["in_hbm"], st["in_host"]) == (2, 4)
+
+
+def test_reclaim_and_own_slot_fallback():
+    # DRAM full of DRAM-only pages: a promotion's victim takes the promoted page's slot
+    c, m = _cache(2, 2, 1), Model(2, 2, 1)
+    for _ in range(4):
+        c.append(None, None)
+        m.append()
+    c.touch([0])
+    m.touch([0])
+    assert c.slots(0) == m.slots(0) == (0, -1) and c.slots(2) == m.slots(2) == (-1, 0)
+    assert c.stats()["reclaims"] == 1
+    # a spare DRAM slot makes a page with both copies, whose DRAM copy is reclaimed next
+    c, m = _cache(3, 4, 1), Model(3, 4, 1)
+    for _ in range(6):
+        c.append(None, None)
+        m.append()
+    c.touch([0])
+    m.touch([0])
+    assert c.slots(0) == (0, 0) and c.slots(3) == (-1, 3)
+    c.touch([1])
+    m.touch([1])
+    assert c.slots(0) == (0, -1) and c.slots(4) == (-1, 0) and c.slots(1) == (1, 1)
+    st = c.stats()
+    assert (st["reclaims"], st["offloads"]) == (m.rec, m.off) == (1, 5)
 
 
 def test_capacity_and_argument_errors():
@@ -134,6 +192,14 @@ def test_capacity_and_argument_errors():
     with pytest.raises(wa.WaError) as e:
         wa.WaCache(3, 3, 16, 2, hbm_pages=2, host_pages=2, max_chunks=4, dry_run=True)
     assert e.value.status == 2      # head rows not whole 16-byte vectors
+    with pytest.raises(wa.WaError) as e:
+        wa.WaCache(4, 96, 16, 2, hbm_pages=2, host_pages=2, max_chunks=4, dry_run=True,
+                   dram_fp8=True)
+    assert e.value.status == 2      # FP8 tier: head_dim 64, 128 or 256
+    with pytest.raises(wa.WaError) as e:
+        wa.WaCache(4, 64, 16, 2, hbm_pages=2, host_pages=2, max_chunks=4, dry_run=True,
+                   dtype=torch.float32, dram_fp8=True)
+    assert e.value.status == 3      # FP8 tier: bf16 caches only
 
 
 def test_current_pages_never_evicted():

@@ -28,13 +28,15 @@ def _rows(n, H, d, seed):
     return x.to(torch.bfloat16)
 
 
-@pytest.mark.parametrize("d", [64, 128, 256])
-def test_encode_decode_bitexact(d):
-    x = _rows(300, 3, d, d)
-    codes = torch.empty((300, 3, d), dtype=torch.uint8, device=DEV)
-    scales = torch.empty((300, 3), dtype=torch.float32, device=DEV)
+@pytest.mark.parametrize("d,n,H", [(64, 300, 3), (128, 300, 3), (256, 300, 3), (128, 301, 3),
+                                   (64, 7, 1)])
+def test_encode_decode_bitexact(d, n, H):
+    """Whole and ragged row counts (the kernels take four rows per warp step)."""
+    x = _rows(n, H, d, d + n)
+    codes = torch.empty((n, H, d), dtype=torch.uint8, device=DEV)
+    scales = torch.empty((n, H), dtype=torch.float32, device=DEV)
     wa.wa_fp8_encode(x.to(DEV), codes, scales)
-    out = torch.empty((300, 3, d), dtype=torch.bfloat16, device=DEV)
+    out = torch.empty((n, H, d), dtype=torch.bfloat16, device=DEV)
     wa.wa_fp8_decode(codes, scales, out)
     wa.wa_check()
     rc, rs = O.fp8_encode_rows(np_of(x))
