@@ -278,6 +278,8 @@ def run_gpu(args, world, rank, local, hybrid=False, per_head=False):
     n_kv = KP * P + NLOC
     flops = attn_flops(NQ, n_kv, D, H)
     attn_tflops = flops / (per["attention"] * 1e-3) / 1e12
+    context = None if (hybrid or per_head or args.no_context) else sdpa_context(q, kbuf, vbuf, kl,
+                                                                                vl, flops)
     gather_bytes = 2 * 2 * KP * P * H * D * 2          # K and V, read + write
     summ_bytes = N_PAGES * P * H * D * 2
     value = world * flops / (ms_step * 1e-3) / 1e12
@@ -314,6 +316,8 @@ def run_gpu(args, world, rank, local, hybrid=False, per_head=False):
         "gpu_launches": launches_per_step * args.steps,
         "clocks": clk.summary(),
     }
+    if context is not None:
+        line["context_sdpa"] = context
     if per_head:
         line["config"]["workload"] = ("per_head: " + WORKLOAD + " with a top-4 page set per head "
                                       "(per-head scores, per-head gather into the token-major "
@@ -328,6 +332,42 @@ def run_gpu(args, world, rank, local, hybrid=False, per_head=False):
     if rank == 0 and world == 1 and not args.no_cpu_baseline and not hybrid and not per_head:
         line["cpu_baseline"] = cpu_baseline_sample(c, lambda j: (kp[j], vp[j]))
     return line
+
+
+def sdpa_context(q, kbuf, vbuf, kl, vl, flops):
+    """Context only, not on the path: PyTorch's own attention
+    (torch.nn.functional.scaled_dot_product_attention) on the same bf16 queries
+    and [buffer (+) local] keys and values, per backend PyTorch offers here,
+    head-major copies made outside the timing, bf16 output."""
+    import torch
+    import torch.nn.functional as F
+    from torch.nn.attention import SDPBackend, sdpa_kernel
+
+    qh = q.permute(1, 0, 2).unsqueeze(0).contiguous()
+    kh = torch.cat([kbuf, kl]).permute(1, 0, 2).unsqueeze(0).contiguous()
+    vh = torch.cat([vbuf, vl]).permute(1, 0, 2).unsqueeze(0).contiguous()
+    out = {}
+    for name in ("CUDNN_ATTENTION", "FLASH_ATTENTION", "EFFICIENT_ATTENTION"):
+        be = getattr(SDPBackend, name, None)
+        if be is None:
+            continue
+        try:
+            with sdpa_kernel([be]):
+                for _ in range(3):
+                    F.scaled_dot_product_attention(qh, kh, vh)
+                torch.cuda.synchronize()
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record()
+                for _ in range(10):
+                    F.scaled_dot_product_attention(qh, kh, vh)
+                e1.record()
+                torch.cuda.synchronize()
+            ms = e0.elapsed_time(e1) / 10
+            out[name.lower()] = {"ms": round(ms, 4), "tflops": round(flops / (ms * 1e-3) / 1e12, 1)}
+        except Exception as e:   # backend not available for this GPU / shape
+            out[name.lower()] = {"unavailable": type(e).__name__}
+    del qh, kh, vh
+    return out
 
 
 def run_hsa(args, world, rank, local):
@@ -816,6 +856,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-context", action="store_true",
+                    help="skip the PyTorch attention context timing")
     ap.add_argument("--kernel", default="all", choices=["all", "attention", "gather", "linear"],
                     help="time one kernel alone on its own inputs (for profiling)")
     ap.add_argument("--workload", default="worldattention",
