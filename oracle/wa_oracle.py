@@ -51,6 +51,14 @@ design notes):
   x / s (both divisions in IEEE fp32); decoding multiplies the code's value by
   s in fp32 and rounds to bf16 for the attention buffer.  A row of zeros has
   s = 0 and codes 0.
+  The NVFP4 form of the tier (FP4 E2M1 values with E4M3 scales per 16-element
+  block, the format the pages' "FP4" storage points to) keeps per row an fp32
+  scale g = amax(|row|) / 2688 (2688 = 6 * 448), per block of 16 an E4M3
+  scale sb = E4M3 RNE of amax(|block|) / (6 g), and per element the E2M1
+  round-to-nearest-even (saturating at 6) of x / (sb * g); every product and
+  quotient is one IEEE fp32 operation, in that order.  Decoding multiplies the
+  E2M1 value by sb * g in fp32 and rounds to bf16.  Codes pack two elements per
+  byte, the even element in the low nibble.
 * HSA sparse branch ([WA] HSA section and its appendix notes): key blocks of
   B_inter = 128 tokens over the retrieved buffer and B_intra = 64 over the
   chunk's own tokens (a ragged last block keeps its own size); query blocks of
@@ -106,6 +114,10 @@ __all__ = [
     "e4m3_round",
     "fp8_encode_rows",
     "fp8_decode_rows",
+    "e2m1_values",
+    "e2m1_round",
+    "nvfp4_encode_rows",
+    "nvfp4_decode_rows",
     "bf16_bits",
 ]
 
@@ -552,3 +564,80 @@ def bf16_bits(x) -> np.ndarray:
     u = np.asarray(x, dtype=np.float32).view(np.uint32).astype(np.uint64)
     rounded = u + 0x7FFF + ((u >> 16) & 1)
     return (rounded >> 16).astype(np.uint16)
+
+
+# ----------------------------------------------------------------------------
+# Compressed DRAM tier, NVFP4 form: E2M1 codes, E4M3 scales per 16 elements,
+# one fp32 scale per row
+# ----------------------------------------------------------------------------
+
+E2M1_MAGNITUDES = (0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0)
+
+
+def e2m1_values() -> np.ndarray:
+    """Value of each of the 16 E2M1 codes: sign bit 3, then 2 exponent bits
+    (bias 1) and 1 mantissa bit; exponent 0 is subnormal (0 and 0.5).  Built
+    from the field definitions, returns float64 [16]."""
+    out = np.empty(16, dtype=np.float64)
+    for c in range(16):
+        sign = -1.0 if c & 0x8 else 1.0
+        e = (c >> 1) & 0x3
+        m = c & 0x1
+        mag = (m / 2.0) if e == 0 else (1.0 + m / 2.0) * 2.0 ** (e - 1)
+        out[c] = sign * mag
+    return out
+
+
+def e2m1_round(q: np.ndarray) -> np.ndarray:
+    """E2M1 code (0..15) of each fp32 value: round to nearest, ties to the even
+    code (mantissa bit 0), magnitudes above 6 saturate to 6, the sign kept (also
+    for a zero result).  Returns uint8 codes."""
+    q = np.asarray(q, dtype=np.float64)
+    mags = np.array(E2M1_MAGNITUDES)
+    a = np.minimum(np.abs(q), 6.0)
+    hi = np.minimum(np.searchsorted(mags, a, side="left"), 7)   # first magnitude >= a
+    lo = np.maximum(hi - 1, 0)
+    d_lo, d_hi = a - mags[lo], mags[hi] - a
+    pick_hi = (d_hi < d_lo) | ((d_hi == d_lo) & (hi % 2 == 0))
+    code = np.where(a == mags[hi], hi, np.where(pick_hi, hi, lo)).astype(np.uint8)
+    neg = (q < 0) | ((q == 0) & np.signbit(q))
+    return (code | np.where(neg, 8, 0)).astype(np.uint8)
+
+
+def nvfp4_encode_rows(x):
+    """x [n][H][d] (bf16 bits or float, d a multiple of 16) -> (codes uint8
+    [n][H][d/2], two per byte with the even element low; block scales uint8
+    (E4M3 codes) [n][H][d/16]; row scales float32 [n][H])."""
+    xx = as_f64(x).astype(np.float32)                     # exact for bf16 inputs
+    n, h, d = xx.shape
+    f32 = np.float32
+    g = (np.abs(xx).max(axis=2) / f32(2688.0)).astype(f32)          # row scale
+    blocks = xx.reshape(n, h, d // 16, 16)
+    bamax = np.abs(blocks).max(axis=3)
+    den = (g * f32(6.0)).astype(f32)
+    safe_den = np.where(den > 0, den, f32(1.0)).astype(f32)
+    sb_val = (bamax / safe_den[:, :, None]).astype(f32)
+    sb = e4m3_round(np.where(den[:, :, None] > 0, sb_val, f32(0.0)))
+    es = (e4m3_values()[sb].astype(f32) * g[:, :, None]).astype(f32)  # element scale per block
+    safe_es = np.where(es > 0, es, f32(1.0)).astype(f32)
+    q = (blocks / safe_es[:, :, :, None]).astype(f32)
+    c = e2m1_round(q)
+    c[np.broadcast_to((es <= 0)[:, :, :, None], c.shape)] = 0
+    c = c.reshape(n, h, d)
+    codes = (c[:, :, 0::2] | (c[:, :, 1::2] << 4)).astype(np.uint8)
+    return codes, sb.astype(np.uint8), g
+
+
+def nvfp4_decode_rows(codes, bscales, rscales) -> np.ndarray:
+    """fp32( value(code) * fp32(value(sb) * g) ) per element: [n][H][d] float32."""
+    codes = np.asarray(codes, dtype=np.uint8)
+    n, h, half = codes.shape
+    d = 2 * half
+    c = np.empty((n, h, d), dtype=np.uint8)
+    c[:, :, 0::2] = codes & 0x0F
+    c[:, :, 1::2] = codes >> 4
+    f32 = np.float32
+    es = (e4m3_values()[np.asarray(bscales)].astype(f32)
+          * np.asarray(rscales, dtype=f32)[:, :, None]).astype(f32)
+    v = e2m1_values()[c].astype(f32).reshape(n, h, d // 16, 16)
+    return (v * es[:, :, :, None]).astype(f32).reshape(n, h, d)
