@@ -356,6 +356,38 @@ wa_status wa_gather_pages_fp8(const uint8_t* code_pages, const float* scale_page
                               int k_p, void* buf_out, wa_stream_t stream);
 
 /*
+ * Compressed DRAM tier, NVFP4 form ([WA] HKV tier L2 with FP4 pages): per
+ * (token, head) row of head_dim values, g = amax(|row|) / 2688 (fp32), per
+ * block of 16 values an E4M3 scale sb = E4M3 RNE of amax(|block|) / (6 g), and
+ * per value the E2M1 round-to-nearest-even (saturating at 6) of x / (sb * g);
+ * each quotient and product one IEEE fp32 operation.  Decoding writes
+ * bf16 RNE(value(code) * (value(sb) * g)).  A zero row has g = 0, zero block
+ * scales and codes 0.  head_dim must be 64, 128 or 256 (WA_ERR_SHAPE); all
+ * pointers 16-byte aligned (WA_ERR_ALIGN).  Codes and scales may be device
+ * memory or pinned host memory (read or written through the device mapping).
+ *
+ * wa_nvfp4_encode       : x bf16 [n_tokens][n_heads][head_dim] -> codes uint8
+ *                         [n_tokens][n_heads][head_dim/2] (two values per byte, the
+ *                         even one in bits 0-3), block scales uint8 (E4M3 codes)
+ *                         [n_tokens][n_heads][head_dim/16], row scales float32
+ *                         [n_tokens][n_heads].
+ * wa_nvfp4_decode       : the inverse, into out bf16 [n_tokens][n_heads][head_dim].
+ * wa_gather_pages_nvfp4 : out[s*page_tokens + t] = decode(page idx_dev[s], token t) over
+ *                         pages of page_tokens tokens in the three arrays above;
+ *                         idx_dev device int32 [k_p]; a bad index zeroes the slot and
+ *                         records WA_ERR_INDEX.
+ */
+wa_status wa_nvfp4_encode(const void* x, int n_tokens, int n_heads, int head_dim,
+                          uint8_t* codes_out, uint8_t* bscales_out, float* rscales_out,
+                          wa_stream_t stream);
+wa_status wa_nvfp4_decode(const uint8_t* codes, const uint8_t* bscales, const float* rscales,
+                          int n_tokens, int n_heads, int head_dim, void* out, wa_stream_t stream);
+wa_status wa_gather_pages_nvfp4(const uint8_t* code_pages, const uint8_t* bscale_pages,
+                                const float* rscale_pages, int n_pages, int page_tokens,
+                                int n_heads, int head_dim, const int32_t* idx_dev, int k_p,
+                                void* buf_out, wa_stream_t stream);
+
+/*
  * KV cache manager around the path ([WA] HKV tiers L1/L2 and Fig. 2; [IX]
  * KV Cache Manager: append a clean block, range access, index-based selective
  * fetch, offload to main memory).  A host-side runtime over the calls above:

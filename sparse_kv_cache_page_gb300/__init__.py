@@ -32,6 +32,9 @@ __all__ = [
     "wa_fp8_encode",
     "wa_fp8_decode",
     "wa_gather_pages_fp8",
+    "wa_nvfp4_encode",
+    "wa_nvfp4_decode",
+    "wa_gather_pages_nvfp4",
     "wa_check",
     "wa_shutdown",
     "wa_version",
@@ -52,7 +55,8 @@ EXPORTED_SYMBOLS = ("wa_strerror", "wa_version", "wa_page_summarize", "wa_select
                     "wa_cache_retrieve",
                     "wa_cache_window", "wa_cache_touch", "wa_cache_page_location",
                     "wa_cache_get_stats", "wa_cache_page_slots", "wa_cache_wait_copies",
-                    "wa_fp8_encode", "wa_fp8_decode",
+                    "wa_fp8_encode", "wa_fp8_decode", "wa_nvfp4_encode", "wa_nvfp4_decode",
+                    "wa_gather_pages_nvfp4",
                     "wa_gather_pages_fp8", "wa_check", "wa_shutdown")
 
 
@@ -117,6 +121,9 @@ def load():
         "wa_fp8_encode": (I, [P, I, I, I, P, P, P]),
         "wa_fp8_decode": (I, [P, P, I, I, I, P, P]),
         "wa_gather_pages_fp8": (I, [P, P, I, I, I, I, P, I, P, P]),
+        "wa_nvfp4_encode": (I, [P, I, I, I, P, P, P, P]),
+        "wa_nvfp4_decode": (I, [P, P, P, I, I, I, P, P]),
+        "wa_gather_pages_nvfp4": (I, [P, P, P, I, I, I, I, P, I, P, P]),
         "wa_check": (I, [P]),
         "wa_shutdown": (I, []),
     }
@@ -336,6 +343,39 @@ def wa_gather_pages_fp8(code_pages: torch.Tensor, scale_pages: torch.Tensor, idx
     _ok("wa_gather_pages_fp8", load().wa_gather_pages_fp8(
         _ptr(code_pages), _ptr(scale_pages), n, p, h, d, _ptr(idx_dev), idx_dev.numel(),
         _ptr(buf_out), _stream(stream)))
+
+
+def wa_nvfp4_encode(x: torch.Tensor, codes_out: torch.Tensor, bscales_out: torch.Tensor,
+                    rscales_out: torch.Tensor, stream=None):
+    """NVFP4 form of a bf16 [n][H][d] tensor: E2M1 codes uint8 [n][H][d/2], E4M3
+    block scales uint8 [n][H][d/16], fp32 row scales [n][H]; on the device or pinned."""
+    n, h, d = x.shape
+    _need(codes_out.dtype == torch.uint8 and codes_out.numel() == n * h * d // 2
+          and bscales_out.dtype == torch.uint8 and bscales_out.numel() == n * h * d // 16
+          and rscales_out.dtype == torch.float32 and rscales_out.numel() == n * h,
+          "codes uint8 [n][H][d/2], block scales uint8 [n][H][d/16], row scales float32 [n][H]")
+    _ok("wa_nvfp4_encode", load().wa_nvfp4_encode(_ptr(x), n, h, d, _ptr(codes_out),
+                                                  _ptr(bscales_out), _ptr(rscales_out),
+                                                  _stream(stream)))
+
+
+def wa_nvfp4_decode(codes: torch.Tensor, bscales: torch.Tensor, rscales: torch.Tensor,
+                    out: torch.Tensor, stream=None):
+    n, h, d = out.shape
+    _ok("wa_nvfp4_decode", load().wa_nvfp4_decode(_ptr(codes), _ptr(bscales), _ptr(rscales), n, h,
+                                                  d, _ptr(out), _stream(stream)))
+
+
+def wa_gather_pages_nvfp4(code_pages: torch.Tensor, bscale_pages: torch.Tensor,
+                          rscale_pages: torch.Tensor, idx_dev: torch.Tensor, buf_out: torch.Tensor,
+                          stream=None):
+    """buf_out[s*P + t] = decode of page idx[s], token t (bf16); code pages
+    [n][P][H][d/2], block scales [n][P][H][d/16], row scales [n][P][H], on the
+    device or in pinned host memory."""
+    n, p, h, half = code_pages.shape
+    _ok("wa_gather_pages_nvfp4", load().wa_gather_pages_nvfp4(
+        _ptr(code_pages), _ptr(bscale_pages), _ptr(rscale_pages), n, p, h, 2 * half,
+        _ptr(idx_dev), idx_dev.numel(), _ptr(buf_out), _stream(stream)))
 
 
 class WaCache:

@@ -350,6 +350,55 @@ wa_status wa_gather_pages_fp8(const uint8_t* code_pages, const float* scale_page
                            (cudaStream_t)stream);
 }
 
+wa_status wa_nvfp4_encode(const void* x, int n_tokens, int n_heads, int head_dim,
+                          uint8_t* codes_out, uint8_t* bscales_out, float* rscales_out,
+                          wa_stream_t stream) {
+  if (!x || !codes_out || !bscales_out || !rscales_out || n_tokens <= 0) return WA_ERR_INVALID_ARG;
+  if (!fp8_shape_ok(n_heads, head_dim)) return WA_ERR_SHAPE;
+  if (!aligned16(x) || !aligned16(codes_out) || !aligned16(bscales_out) || !aligned16(rscales_out))
+    return WA_ERR_ALIGN;
+  void* c = const_cast<void*>(device_view(codes_out));
+  void* b = const_cast<void*>(device_view(bscales_out));
+  float* r = static_cast<float*>(const_cast<void*>(device_view(rscales_out)));
+  if (!c || !b || !r || !device_view(x)) return WA_ERR_INVALID_ARG;
+  return launch_nvfp4_encode(x, (size_t)n_tokens * n_heads, head_dim, c, b, r,
+                             (cudaStream_t)stream);
+}
+
+wa_status wa_nvfp4_decode(const uint8_t* codes, const uint8_t* bscales, const float* rscales,
+                          int n_tokens, int n_heads, int head_dim, void* out, wa_stream_t stream) {
+  if (!codes || !bscales || !rscales || !out || n_tokens <= 0) return WA_ERR_INVALID_ARG;
+  if (!fp8_shape_ok(n_heads, head_dim)) return WA_ERR_SHAPE;
+  if (!aligned16(codes) || !aligned16(bscales) || !aligned16(rscales) || !aligned16(out))
+    return WA_ERR_ALIGN;
+  const void* c = device_view(codes);
+  const void* b = device_view(bscales);
+  const float* r = static_cast<const float*>(device_view(rscales));
+  if (!c || !b || !r) return WA_ERR_INVALID_ARG;
+  const size_t rows = (size_t)n_tokens * n_heads;
+  return launch_nvfp4_decode(c, b, r, nullptr, 1, rows, rows, head_dim, out, (cudaStream_t)stream);
+}
+
+wa_status wa_gather_pages_nvfp4(const uint8_t* code_pages, const uint8_t* bscale_pages,
+                                const float* rscale_pages, int n_pages, int page_tokens,
+                                int n_heads, int head_dim, const int32_t* idx_dev, int k_p,
+                                void* buf_out, wa_stream_t stream) {
+  if (!code_pages || !bscale_pages || !rscale_pages || !idx_dev || !buf_out || n_pages <= 0 ||
+      page_tokens <= 0 || k_p <= 0)
+    return WA_ERR_INVALID_ARG;
+  if (!fp8_shape_ok(n_heads, head_dim)) return WA_ERR_SHAPE;
+  if (!aligned16(code_pages) || !aligned16(bscale_pages) || !aligned16(rscale_pages) ||
+      !aligned16(buf_out))
+    return WA_ERR_ALIGN;
+  const void* c = device_view(code_pages);
+  const void* b = device_view(bscale_pages);
+  const float* r = static_cast<const float*>(device_view(rscale_pages));
+  if (!c || !b || !r) return WA_ERR_INVALID_ARG;
+  const size_t page_rows = (size_t)page_tokens * n_heads;
+  return launch_nvfp4_decode(c, b, r, idx_dev, n_pages, page_rows, page_rows * k_p, head_dim,
+                             buf_out, (cudaStream_t)stream);
+}
+
 wa_status wa_block_means(const void* x, wa_dtype dt, int n_rows, int block, int n_heads,
                          int head_dim, float* means_out, wa_stream_t stream) {
   if (!dtype_ok(dt)) return WA_ERR_DTYPE;

@@ -105,6 +105,14 @@ wa_status launch_fp8_decode(const void* codes, const float* scales, const int32_
                             size_t page_rows, size_t n_rows, int head_dim, void* out,
                             cudaStream_t s);
 
+// NVFP4 page codec (k_fp4.cu): E2M1 codes [rows][d/2], E4M3 block scales
+// [rows][d/16], fp32 row scales [rows]; host-mapped pointers allowed.
+wa_status launch_nvfp4_encode(const void* src, size_t n_rows, int head_dim, void* codes,
+                              void* bscales, float* rscales, cudaStream_t s);
+wa_status launch_nvfp4_decode(const void* codes, const void* bscales, const float* rscales,
+                              const int32_t* idx, int n_pages, size_t page_rows, size_t n_rows,
+                              int head_dim, void* out, cudaStream_t s);
+
 // Block means of x [n_rows][row_elems] in blocks of `block` rows (ragged last block).
 wa_status launch_block_means(const void* x, wa_dtype dt, int n_rows, int block, int row_elems,
                              float* means_out, cudaStream_t s);
