@@ -531,9 +531,9 @@ def run_cache(args, world, rank, local):
             cache.append(ks[m], vs[m], prompts[m])
         cache.wait_copies()          # the last offloads belong to this video too
 
-    def timed(dram_fp8, clk=None):
+    def timed(fmt, clk=None):
         cache = wa.WaCache(H, D, P, PPC, hbm_pages=16, host_pages=96, max_chunks=NCH,
-                           prompt_dim=PDIM, dram_fp8=dram_fp8)
+                           prompt_dim=PDIM, dram_format=fmt)
         for _ in range(max(1, args.warmup - 2)):
             cache.reset()
             video(cache)
@@ -554,8 +554,9 @@ def run_cache(args, world, rank, local):
         return max_over_ranks(total, world) / steps, steps, st
 
     clk = Clocks(local)
-    ms, steps, st = timed(False, clk)
-    ms8, _, st8 = timed(True)
+    ms, steps, st = timed("native", clk)
+    ms8, _, st8 = timed("fp8")
+    ms4, _, st4 = timed("nvfp4")
     flops = (NCH - 1) * attn_flops(NQ, KP * P + NLOC, D, H)
     return {"metric": METRIC, "value": round(world * flops / (ms * 1e-3) / 1e12, 2),
             "unit": "TFLOP/s", "n_gpus": world, "steps": steps, "warmup": args.warmup,
@@ -572,6 +573,9 @@ def run_cache(args, world, rank, local):
             "cache_stats_per_video": st,
             "fp8_dram_tier": {"ms_per_step": round(ms8, 3), "ms_per_chunk": round(ms8 / (NCH - 1), 3),
                               "cache_stats_per_video": st8},
+            "nvfp4_dram_tier": {"ms_per_step": round(ms4, 3),
+                                "ms_per_chunk": round(ms4 / (NCH - 1), 3),
+                                "cache_stats_per_video": st4},
             "gpu_launches": steps * (NCH + 2 * (NCH - 1)),   # summaries per append; select + attention
             "clocks": clk.summary()}
 
@@ -708,6 +712,10 @@ def run_stress(args, world, rank, local):
     vc = torch.empty((NPG, P, H, D), dtype=torch.uint8, pin_memory=True)
     ksc = torch.empty((NPG, P, H), dtype=torch.float32, pin_memory=True)
     vsc = torch.empty((NPG, P, H), dtype=torch.float32, pin_memory=True)
+    # and as NVFP4: E2M1 codes, E4M3 scales per 16 values, fp32 row scales
+    nv = [(torch.empty((NPG, P, H, D // 2), dtype=torch.uint8, pin_memory=True),
+           torch.empty((NPG, P, H, D // 16), dtype=torch.uint8, pin_memory=True),
+           torch.empty((NPG, P, H), dtype=torch.float32, pin_memory=True)) for _ in range(2)]
     kbar = torch.empty((NPG, H, D), dtype=torch.float32, device=dev)
     for j in range(NPG):
         kj, vj = g((1, P, H, D), ("k", j)), g((1, P, H, D), ("v", j))
@@ -716,10 +724,13 @@ def run_stress(args, world, rank, local):
         hv[j].copy_(vj[0])
         wa.wa_fp8_encode(kj[0], kc[j], ksc[j])
         wa.wa_fp8_encode(vj[0], vc[j], vsc[j])
+        for t, x in enumerate((kj[0], vj[0])):
+            wa.wa_nvfp4_encode(x, nv[t][0][j], nv[t][1][j], nv[t][2][j])
     torch.cuda.synchronize()
     o = torch.empty((NQ, H, D), dtype=torch.float32, device=dev)
     layers = [TierLayer(g((NQ, H, D), ("q", l)), g((NLOC, H, D), ("kl", l)),
-                        g((NLOC, H, D), ("vl", l)), kbar, hk, hv, o, kc, ksc, vc, vsc)
+                        g((NLOC, H, D), ("vl", l)), kbar, hk, hv, o, kc, ksc, vc, vsc,
+                        k_nv=nv[0], v_nv=nv[1])
               for l in range(NL)]
     pipe = TieredPipeline(KP, P, H, D, device=dev)
     torch.cuda.synchronize()
@@ -745,6 +756,8 @@ def run_stress(args, world, rank, local):
     t_direct = timed("direct", reps)
     t_fp8 = timed("fp8", reps)
     t_fp8p = timed("fp8_pipeline", reps)
+    t_nv = timed("nvfp4", reps)
+    t_nvp = timed("nvfp4_pipeline", reps)
     t_copy = timed("copy", 1)
     t_attn = timed("attn", 1)
     wa.wa_check()
@@ -762,6 +775,8 @@ def run_stress(args, world, rank, local):
             "serial_ms": round(t_serial, 3), "direct_ms": round(t_direct, 3),
             "fp8_tier_ms": round(t_fp8, 3), "fp8_tier_pipeline_ms": round(t_fp8p, 3),
             "fp8_tier_link_bytes_per_layer": 2 * KP * P * H * (D + 4),
+            "nvfp4_tier_ms": round(t_nv, 3), "nvfp4_tier_pipeline_ms": round(t_nvp, 3),
+            "nvfp4_tier_link_bytes_per_layer": 2 * KP * P * H * (D // 2 + D // 16 + 4),
             "copy_only_ms": round(t_copy, 3),
             "attn_only_ms": round(t_attn, 3), "h2d_gbs": round(h2d / (t_copy * 1e-3) / 1e9, 1),
             "copy_hidden_frac": hidden, "gpu_launches": NL * 2, "clocks": clk.summary()}

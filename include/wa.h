@@ -400,10 +400,11 @@ wa_status wa_gather_pages_nvfp4(const uint8_t* code_pages, const uint8_t* bscale
  *   - the DRAM tier is inclusive: a page keeps its DRAM copy when promoted
  *     back to HBM (pages never change once appended), so evicting it again
  *     copies nothing;
- *   - dram_fp8 != 0 stores DRAM pages as FP8 E4M3 codes with per-(token, head)
- *     scales (the wa_fp8_encode format; bf16 caches with head_dim 64, 128 or
- *     256): a page read back from DRAM is decode(encode(page)), bit for bit,
- *     and stays so when promoted (its HBM copy is the decoded page);
+ *   - dram_format 1 stores DRAM pages as FP8 E4M3 codes with per-(token, head)
+ *     scales (the wa_fp8_encode format), 2 as NVFP4 (the wa_nvfp4_encode
+ *     format); both need a bf16 cache with head_dim 64, 128 or 256.  A page read
+ *     back from DRAM is decode(encode(page)), bit for bit, and stays so when
+ *     promoted (its HBM copy is the decoded page);
  *   - append: pages to free HBM slots; when none is free the least recently
  *     used resident page leaves HBM: with no copy if it has a DRAM copy, else
  *     offloaded to the lowest free DRAM slot, or, with none free, to the slot of
@@ -436,7 +437,8 @@ typedef struct {
   int host_pages;       /* pinned DRAM tier capacity (pages, >= 0) */
   int max_chunks;       /* chunks the cache can hold */
   int dry_run;          /* 1: placement only, no device memory or copies */
-  int dram_fp8;         /* 1: DRAM tier holds FP8 E4M3 codes + scales */
+  int dram_format;      /* DRAM tier: 0 the cache's dtype, 1 FP8 E4M3 codes + scales,
+                           2 NVFP4 (wa_nvfp4_encode format) */
 } wa_cache_config;
 
 typedef struct {
@@ -450,9 +452,10 @@ typedef struct {
   long long reclaims;                         /* DRAM copies dropped to free a slot */
 } wa_cache_stats;
 
-/* Errors: WA_ERR_INVALID_ARG, WA_ERR_DTYPE (also dram_fp8 with a non-bf16
- * dtype), WA_ERR_SHAPE (head rows not whole 16-byte vectors; dram_fp8 with
- * head_dim not 64, 128 or 256), WA_ERR_OOM (allocation failed). */
+/* Errors: WA_ERR_INVALID_ARG (also an unknown dram_format), WA_ERR_DTYPE (a
+ * compressed dram_format with a non-bf16 dtype), WA_ERR_SHAPE (head rows not
+ * whole 16-byte vectors; a compressed dram_format with head_dim not 64, 128 or
+ * 256), WA_ERR_OOM (allocation failed). */
 wa_status wa_cache_create(const wa_cache_config* cfg, wa_cache** out);
 /* Synchronizes the device (unless dry_run) and frees the cache. */
 wa_status wa_cache_destroy(wa_cache* cache);

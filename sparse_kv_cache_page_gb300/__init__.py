@@ -64,7 +64,7 @@ class _CacheConfig(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int) for n in ("n_heads", "head_dim", "dtype", "page_tokens",
                                              "pages_per_chunk", "prompt_dim", "hbm_pages",
                                              "host_pages", "max_chunks", "dry_run",
-                                             "dram_fp8")]
+                                             "dram_format")]
 
 
 class _CacheStats(ctypes.Structure):
@@ -380,16 +380,19 @@ def wa_gather_pages_nvfp4(code_pages: torch.Tensor, bscale_pages: torch.Tensor,
 
 class WaCache:
     """KV cache manager (libwa wa_cache_*): HBM and inclusive pinned-DRAM page
-    tiers (optionally FP8 in DRAM), summaries at insert, retrieval with LRU
+    tiers (optionally FP8 or NVFP4 in DRAM), summaries at insert, retrieval with LRU
     eviction, overlapped offloads and promotion, window access.  ``dry_run``
     caches plan placements without any CUDA work."""
 
     def __init__(self, n_heads: int, head_dim: int, page_tokens: int, pages_per_chunk: int,
                  hbm_pages: int, host_pages: int, max_chunks: int, prompt_dim: int = 0,
-                 dtype=torch.bfloat16, dry_run: bool = False, dram_fp8: bool = False):
+                 dtype=torch.bfloat16, dry_run: bool = False, dram_format: str = "native"):
+        """dram_format: "native" (the cache's dtype), "fp8" or "nvfp4"."""
+        fmt = {"native": 0, "bf16": 0, "fp8": 1, "nvfp4": 2}.get(dram_format)
+        _need(fmt is not None, "dram_format must be 'native', 'fp8' or 'nvfp4'")
         cfg = _CacheConfig(n_heads, head_dim, WA_BF16 if dtype == torch.bfloat16 else WA_F32,
                            page_tokens, pages_per_chunk, prompt_dim, hbm_pages, host_pages,
-                           max_chunks, int(bool(dry_run)), int(bool(dram_fp8)))
+                           max_chunks, int(bool(dry_run)), fmt)
         h = ctypes.c_void_p()
         _ok("wa_cache_create", load().wa_cache_create(ctypes.byref(cfg), ctypes.byref(h)))
         self._h = h

@@ -14,9 +14,10 @@
 //     page's DRAM copy stays valid after it is promoted back to HBM, and
 //     evicting such a page again moves no bytes;
 //   * HBM tier: one device pool of hbm_pages page slots (K and V); DRAM tier:
-//     one pinned, device-mapped pool of host_pages slots, holding either the
-//     cache's dtype or FP8 E4M3 codes plus per-(token, head) scales (dram_fp8,
-//     the compressed tier: half the bytes across the CPU-GPU link);
+//     one pinned, device-mapped pool of host_pages slots, holding the cache's
+//     dtype, FP8 E4M3 codes plus per-(token, head) scales, or NVFP4 (E2M1 codes,
+//     E4M3 scales per 16 values, fp32 row scales) -- dram_format, the
+//     compressed tier: 1.9x or 3.4x fewer bytes across the CPU-GPU link;
 //     summaries [max pages][H][d] and prompt embeddings [max chunks][prompt_dim]
 //     stay in HBM for every page;
 //   * append: the chunk's pages go to free HBM slots; when none is free the
@@ -54,7 +55,8 @@ struct wa_cache {
   wa_cache_config cfg;
   size_t page_bytes = 0;          // one tensor (K or V) of one page in HBM
   size_t host_page_bytes = 0;     // the same in the DRAM tier (slot stride)
-  size_t code_bytes = 0;          // FP8 tier: codes of one page tensor; its scales follow
+  size_t code_bytes = 0;          // compressed tier: codes of one page tensor, then
+  size_t bs_off = 0, rs_off = 0;  // (NVFP4) block scales and row scales at these offsets
   int n_pages = 0, n_chunks = 0;
   unsigned long long clock = 0;
   struct Entry {
@@ -95,7 +97,9 @@ using wa::cuda_status;
 
 inline bool dt_ok(wa_dtype dt) { return dt == WA_BF16 || dt == WA_F32; }
 inline size_t dt_size(wa_dtype dt) { return dt == WA_BF16 ? 2 : 4; }
-inline bool fp8(const wa_cache* c) { return c->cfg.dram_fp8 != 0; }
+inline bool fp8(const wa_cache* c) { return c->cfg.dram_format == 1; }
+inline bool nvfp4(const wa_cache* c) { return c->cfg.dram_format == 2; }
+inline size_t pad16(size_t n) { return (n + 15) / 16 * 16; }
 
 int free_slot(const std::vector<int>& owner) {
   for (size_t s = 0; s < owner.size(); ++s)
@@ -132,7 +136,9 @@ void count_bytes(wa_cache* c, cudaMemcpyKind kind, size_t bytes) {
 // Bytes of `rows` (token, head) rows in the DRAM tier's format.
 size_t host_row_bytes(const wa_cache* c, size_t rows) {
   const size_t d = (size_t)c->cfg.head_dim;
-  return fp8(c) ? rows * (d + sizeof(float)) : rows * d * dt_size(c->cfg.dtype);
+  if (fp8(c)) return rows * (d + sizeof(float));
+  if (nvfp4(c)) return rows * (d / 2 + d / 16 + sizeof(float));
+  return rows * d * dt_size(c->cfg.dtype);
 }
 
 // Make `s` wait until DRAM slot x holds its latest copy.
@@ -172,11 +178,16 @@ wa_status offload(wa_cache* c, int v, int x, cudaStream_t s) {
     const size_t rows = (size_t)c->cfg.page_tokens * c->cfg.n_heads;
     for (int t = 0; t < 2; ++t) {
       char* st = (t ? c->stage_v : c->stage_k) + (size_t)r * c->host_page_bytes;
-      wa_status rc =
-          fp8(c) ? wa::launch_fp8_encode(hbm_ptr(c, e.hbm, t), rows, c->cfg.head_dim, st,
-                                         reinterpret_cast<float*>(st + c->code_bytes), s)
-                 : cuda_status(cudaMemcpyAsync(st, hbm_ptr(c, e.hbm, t), c->page_bytes,
-                                               cudaMemcpyDeviceToDevice, s));
+      wa_status rc;
+      if (fp8(c))
+        rc = wa::launch_fp8_encode(hbm_ptr(c, e.hbm, t), rows, c->cfg.head_dim, st,
+                                   reinterpret_cast<float*>(st + c->code_bytes), s);
+      else if (nvfp4(c))
+        rc = wa::launch_nvfp4_encode(hbm_ptr(c, e.hbm, t), rows, c->cfg.head_dim, st,
+                                     st + c->bs_off, reinterpret_cast<float*>(st + c->rs_off), s);
+      else
+        rc = cuda_status(cudaMemcpyAsync(st, hbm_ptr(c, e.hbm, t), c->page_bytes,
+                                         cudaMemcpyDeviceToDevice, s));
       if (rc != WA_OK) return rc;
     }
     if (cudaEventRecord(c->filled, s) != cudaSuccess ||
@@ -274,6 +285,13 @@ wa_status read_page(wa_cache* c, int p, bool v, size_t r0, size_t rows, char* ds
     const float* scales = reinterpret_cast<const float*>(base + c->code_bytes) + r0;
     return wa::launch_fp8_decode(codes, scales, nullptr, 1, rows, rows, c->cfg.head_dim, dst, s);
   }
+  if (nvfp4(c)) {
+    const size_t d = (size_t)c->cfg.head_dim;
+    const char* base = host_ptr(c, e.host, v, true);
+    return wa::launch_nvfp4_decode(base + r0 * (d / 2), base + c->bs_off + r0 * (d / 16),
+                                   reinterpret_cast<const float*>(base + c->rs_off) + r0, nullptr,
+                                   1, rows, rows, c->cfg.head_dim, dst, s);
+  }
   return cuda_status(cudaMemcpyAsync(dst, host_ptr(c, e.host, v, false) + r0 * row_bytes,
                                      rows * row_bytes, cudaMemcpyHostToDevice, s));
 }
@@ -321,7 +339,8 @@ wa_status wa_cache_create(const wa_cache_config* cfg, wa_cache** out) {
       g.hbm_pages <= 0 || g.host_pages < 0 || g.max_chunks <= 0 || g.prompt_dim < 0)
     return WA_ERR_INVALID_ARG;
   if (((long long)g.n_heads * g.head_dim * dt_size(g.dtype)) % 16 != 0) return WA_ERR_SHAPE;
-  if (g.dram_fp8) {
+  if (g.dram_format < 0 || g.dram_format > 2) return WA_ERR_INVALID_ARG;
+  if (g.dram_format != 0) {
     if (g.dtype != WA_BF16) return WA_ERR_DTYPE;
     if (g.head_dim != 64 && g.head_dim != 128 && g.head_dim != 256) return WA_ERR_SHAPE;
   }
@@ -330,9 +349,17 @@ wa_status wa_cache_create(const wa_cache_config* cfg, wa_cache** out) {
   c->cfg = g;
   const size_t rows = (size_t)g.page_tokens * g.n_heads;
   c->page_bytes = rows * g.head_dim * dt_size(g.dtype);
-  c->code_bytes = g.dram_fp8 ? rows * g.head_dim : 0;
-  c->host_page_bytes =
-      g.dram_fp8 ? c->code_bytes + (rows * sizeof(float) + 15) / 16 * 16 : c->page_bytes;
+  if (g.dram_format == 1) {
+    c->code_bytes = rows * g.head_dim;
+    c->host_page_bytes = c->code_bytes + pad16(rows * sizeof(float));
+  } else if (g.dram_format == 2) {
+    c->code_bytes = rows * (g.head_dim / 2);
+    c->bs_off = c->code_bytes;
+    c->rs_off = c->bs_off + pad16(rows * (g.head_dim / 16));
+    c->host_page_bytes = c->rs_off + pad16(rows * sizeof(float));
+  } else {
+    c->host_page_bytes = c->page_bytes;
+  }
   c->hbm_owner.assign(g.hbm_pages, -1);
   c->host_owner.assign(g.host_pages, -1);
   c->table.reserve((size_t)g.max_chunks * g.pages_per_chunk);

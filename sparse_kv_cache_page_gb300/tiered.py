@@ -23,7 +23,8 @@ from dataclasses import dataclass
 
 import torch
 
-from . import wa_block_attn, wa_gather_pages, wa_gather_pages_fp8, wa_select_pages
+from . import (wa_block_attn, wa_gather_pages, wa_gather_pages_fp8, wa_gather_pages_nvfp4,
+               wa_select_pages)
 
 
 @dataclass
@@ -41,6 +42,11 @@ class TierLayer:
     k_scales: torch.Tensor | None = None
     v_codes: torch.Tensor | None = None
     v_scales: torch.Tensor | None = None
+    # NVFP4 copy (E2M1 codes [n_pages][P][H][d/2], E4M3 block scales
+    # [n_pages][P][H][d/16], fp32 row scales [n_pages][P][H], pinned host), used
+    # by the "nvfp4" modes
+    k_nv: tuple | None = None
+    v_nv: tuple | None = None
 
 
 class TieredPipeline:
@@ -56,6 +62,7 @@ class TieredPipeline:
         self.device = device
         self.k_p, self.page_tokens, self.n_heads, self.head_dim = k_p, page_tokens, n_heads, head_dim
         self.stage = None     # FP8 staging pages, allocated on first "fp8_pipeline" run
+        self.stage4 = None    # NVFP4 staging pages, allocated on first "nvfp4_pipeline" run
 
     def _staging(self):
         if self.stage is None:
@@ -67,6 +74,27 @@ class TieredPipeline:
                                vs=mk(self.k_p, P, H, dt=torch.float32)) for _ in range(2)]
             self.ident = torch.arange(self.k_p, dtype=torch.int32, device=self.device)
         return self.stage
+
+    def _staging4(self):
+        if self.stage4 is None:
+            P, H, d = self.page_tokens, self.n_heads, self.head_dim
+            mk = lambda *shape, dt: torch.empty(shape, dtype=dt, device=self.device)  # noqa: E731
+            self.stage4 = [{t: (mk(self.k_p, P, H, d // 2, dt=torch.uint8),
+                                mk(self.k_p, P, H, d // 16, dt=torch.uint8),
+                                mk(self.k_p, P, H, dt=torch.float32)) for t in ("k", "v")}
+                           for _ in range(2)]
+            self.ident = torch.arange(self.k_p, dtype=torch.int32, device=self.device)
+        return self.stage4
+
+    def _fetch_nvfp4(self, ly, idx_host, st):
+        """Copy-engine fetch of k_p NVFP4 pages into a staging slot: codes, block
+        scales and row scales each viewed as one row of 2-byte elements per page
+        (16-byte rows need page_tokens * n_heads % 4 == 0)."""
+        page = lambda t: t.view(t.shape[0], 1, 1, -1).view(torch.bfloat16)  # noqa: E731
+        for a in range(3):
+            kb, vb = page(st["k"][a]), page(st["v"][a])
+            wa_gather_pages(page(ly.k_nv[a]), page(ly.v_nv[a]), None, idx_host,
+                            kb.view(self.k_p, 1, -1), vb.view(self.k_p, 1, -1), stream=self.side)
 
     def _fetch_fp8(self, ly, idx_host, st):
         """Copy-engine fetch of k_p FP8 pages (codes viewed as 2-byte elements,
@@ -90,23 +118,25 @@ class TieredPipeline:
         and scales and are decoded to bf16 on the device: the compressed DRAM
         tier), "fp8_pipeline" (the FP8 pages fetched by the copy engine on the
         side stream into a staging slot, decoded on the main stream before
-        the layer's attention).  Returns the page indices [n_layers][k_p]
-        (int32; pinned host memory, or device memory in "direct" and "fp8"
-        modes)."""
+        the layer's attention), "nvfp4" / "nvfp4_pipeline" (the same with the
+        NVFP4 copy: E2M1 codes and two levels of scales).  Returns the page
+        indices [n_layers][k_p] (int32; pinned host memory, or device memory in
+        the "direct", "fp8" and "nvfp4" modes)."""
         main = torch.cuda.current_stream(self.device)
         n = len(layers)
         idx = torch.empty((n, self.k_p), dtype=torch.int32, device=self.device)
         for l, ly in enumerate(layers):
             wa_select_pages(ly.q, ly.kbar, None, None, 1, self.k_p, idx[l])
-        if mode in ("direct", "fp8"):
-            return self._run_direct(layers, idx, main, fp8=mode == "fp8")
+        if mode in ("direct", "fp8", "nvfp4"):
+            return self._run_direct(layers, idx, main, codec=mode)
         idx_h = torch.empty((n, self.k_p), dtype=torch.int32, pin_memory=True)
         idx_h.copy_(idx, non_blocking=True)
         main.synchronize()                         # indices reach the host once
         ev_copy = [torch.cuda.Event() for _ in range(n)]
         ev_attn = [torch.cuda.Event() for _ in range(n)]
-        if mode == "fp8_pipeline":
-            stage = self._staging()
+        if mode in ("fp8_pipeline", "nvfp4_pipeline"):
+            nv = mode == "nvfp4_pipeline"
+            stage = self._staging4() if nv else self._staging()
             ev_dec = [torch.cuda.Event() for _ in range(n)]
             for l, ly in enumerate(layers):
                 kb, vb = self.bufs[l % 2]
@@ -114,11 +144,15 @@ class TieredPipeline:
                 with torch.cuda.stream(self.side):
                     if l >= 2:
                         self.side.wait_event(ev_dec[l - 2])
-                    self._fetch_fp8(ly, idx_h[l], st)
+                    (self._fetch_nvfp4 if nv else self._fetch_fp8)(ly, idx_h[l], st)
                     ev_copy[l].record(self.side)
                 main.wait_event(ev_copy[l])
-                wa_gather_pages_fp8(st["kc"], st["ks"], self.ident, kb)
-                wa_gather_pages_fp8(st["vc"], st["vs"], self.ident, vb)
+                if nv:
+                    wa_gather_pages_nvfp4(*st["k"], self.ident, kb)
+                    wa_gather_pages_nvfp4(*st["v"], self.ident, vb)
+                else:
+                    wa_gather_pages_fp8(st["kc"], st["ks"], self.ident, kb)
+                    wa_gather_pages_fp8(st["vc"], st["vs"], self.ident, vb)
                 ev_dec[l].record(main)
                 wa_block_attn(ly.q, kb, vb, ly.k_loc, ly.v_loc, ly.out)
             main.wait_stream(self.side)
@@ -142,7 +176,7 @@ class TieredPipeline:
         main.wait_stream(self.side)
         return idx_h
 
-    def _run_direct(self, layers, idx, main, fp8=False):
+    def _run_direct(self, layers, idx, main, codec="direct"):
         ev_sel = torch.cuda.Event()
         ev_sel.record(main)
         n = len(layers)
@@ -152,9 +186,12 @@ class TieredPipeline:
             kb, vb = self.bufs[l % 2]
             with torch.cuda.stream(self.side):
                 self.side.wait_event(ev_sel if l < 2 else ev_attn[l - 2])
-                if fp8:
+                if codec == "fp8":
                     wa_gather_pages_fp8(ly.k_codes, ly.k_scales, idx[l], kb, stream=self.side)
                     wa_gather_pages_fp8(ly.v_codes, ly.v_scales, idx[l], vb, stream=self.side)
+                elif codec == "nvfp4":
+                    wa_gather_pages_nvfp4(*ly.k_nv, idx[l], kb, stream=self.side)
+                    wa_gather_pages_nvfp4(*ly.v_nv, idx[l], vb, stream=self.side)
                 else:
                     wa_gather_pages(ly.k_host, ly.v_host, idx[l], None, kb, vb, stream=self.side)
                 ev_copy[l].record(self.side)

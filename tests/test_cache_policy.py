@@ -120,12 +120,15 @@ def test_placement_matches_reference_model(hbm, host, ppc, seed):
         assert all(c.slots(p) != (-1, -1) for p in range(m.n))
 
 
-@pytest.mark.parametrize("dram_fp8", [False, True])
-def test_bytes_planned(dram_fp8):
+@pytest.mark.parametrize("fmt", ["native", "fp8", "nvfp4"])
+def test_bytes_planned(fmt):
     c = wa.WaCache(4, 64, 16, 2, hbm_pages=2, host_pages=4, max_chunks=64, dry_run=True,
-                   dram_fp8=dram_fp8)
-    page = 16 * 4 * 64 * 2                                  # bf16 K (or V) of one page
-    host_page = 16 * 4 * 64 + 16 * 4 * 4 if dram_fp8 else page   # FP8 codes + fp32 scales
+                   dram_format=fmt)
+    rows = 16 * 4                                           # (token, head) rows of a page
+    page = rows * 64 * 2                                    # bf16 K (or V) of one page
+    host_page = {"native": page,
+                 "fp8": rows * 64 + rows * 4,               # FP8 codes + fp32 scales
+                 "nvfp4": rows * 32 + rows * 4 + rows * 4}[fmt]   # E2M1 + E4M3 blocks + fp32
     c.append(None, None)
     c.append(None, None)            # pages 0, 1 offloaded
     c.touch([0])                    # page 0 back (keeps its DRAM copy), page 2 out
@@ -194,12 +197,12 @@ def test_capacity_and_argument_errors():
     assert e.value.status == 2      # head rows not whole 16-byte vectors
     with pytest.raises(wa.WaError) as e:
         wa.WaCache(4, 96, 16, 2, hbm_pages=2, host_pages=2, max_chunks=4, dry_run=True,
-                   dram_fp8=True)
-    assert e.value.status == 2      # FP8 tier: head_dim 64, 128 or 256
+                   dram_format="nvfp4")
+    assert e.value.status == 2      # compressed tier: head_dim 64, 128 or 256
     with pytest.raises(wa.WaError) as e:
         wa.WaCache(4, 64, 16, 2, hbm_pages=2, host_pages=2, max_chunks=4, dry_run=True,
-                   dtype=torch.float32, dram_fp8=True)
-    assert e.value.status == 3      # FP8 tier: bf16 caches only
+                   dtype=torch.float32, dram_format="fp8")
+    assert e.value.status == 3      # compressed tier: bf16 caches only
 
 
 def test_current_pages_never_evicted():

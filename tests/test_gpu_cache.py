@@ -3,9 +3,9 @@ into a small HBM tier with the rest offloaded to pinned DRAM (on the cache's
 own copy stream, overlapping later calls); retrieval picks the oracle's pages
 (two-stage selection over the whole cached sequence) and copies their bytes
 exactly from either tier; promoted and re-evicted pages keep their bytes;
-window access returns the sequence's last tokens.  With the FP8 DRAM tier a
-page that has been offloaded reads back as the oracle codec's
-decode(encode(page)), bit for bit, from either tier."""
+window access returns the sequence's last tokens.  With a compressed DRAM
+tier (FP8 or NVFP4) a page that has been offloaded reads back as the oracle
+codec's decode(encode(page)), bit for bit, from either tier."""
 
 import numpy as np
 import pytest
@@ -31,10 +31,10 @@ def _chunk(m, plant=None, u=None):
     return k.to(torch.bfloat16), v, synth.normal((PDIM,), s("prompt"), DEV)
 
 
-def _setup(n_chunks=5, hbm=6, host=24, fp8=False):
+def _setup(n_chunks=5, hbm=6, host=24, fmt="native"):
     u = synth.normal((H, D), synth.seed_of("cache", "dir"), DEV) * 0.6
     cache = wa.WaCache(H, D, P, PPC, hbm_pages=hbm, host_pages=host, max_chunks=8, prompt_dim=PDIM,
-                       dram_fp8=fp8)
+                       dram_format=fmt)
     ks, vs, ps = [], [], []
     for m in range(n_chunks):
         k, v, pr = _chunk(m, plant=(1, 3) if m == 2 else None, u=u)
@@ -56,24 +56,26 @@ def _bits(t):
     return t.view(torch.int16).cpu().numpy().view(np.uint16)
 
 
-def _expected(cache, ts, fp8):
+def _expected(cache, ts, fmt):
     """bf16 bits of every cached page as a read should return it: the page
-    itself, or (FP8 tier) decode(encode(page)) once it has a DRAM copy.  Valid
-    while no DRAM copy has been reclaimed."""
+    itself, or (compressed tier) decode(encode(page)) once it has a DRAM copy.
+    Valid while no DRAM copy has been reclaimed."""
     assert cache.stats()["reclaims"] == 0
     bank = _bank(ts)
     out = _bits(bank).copy()
-    if fp8:
+    if fmt != "native":
         for p in range(bank.shape[0]):
             if cache.slots(p)[1] >= 0:
-                c, sc = O.fp8_encode_rows(np_of(bank[p]))
-                out[p] = O.bf16_bits(O.fp8_decode_rows(c, sc))
+                x = np_of(bank[p])
+                dec = (O.fp8_decode_rows(*O.fp8_encode_rows(x)) if fmt == "fp8"
+                       else O.nvfp4_decode_rows(*O.nvfp4_encode_rows(x)))
+                out[p] = O.bf16_bits(dec)
     return out
 
 
-@pytest.mark.parametrize("fp8", [False, True])
-def test_retrieve_from_both_tiers_and_promote(fp8):
-    cache, ks, vs, ps, q, cur = _setup(fp8=fp8)
+@pytest.mark.parametrize("fmt", ["native", "fp8", "nvfp4"])
+def test_retrieve_from_both_tiers_and_promote(fmt):
+    cache, ks, vs, ps, q, cur = _setup(fmt=fmt)
     st0 = cache.stats()
     assert st0["n_pages"] == 20 and st0["in_hbm"] == 6 and st0["offloads"] == 14
     kb = torch.empty((2 * P, H, D), dtype=torch.bfloat16, device=DEV)
@@ -84,7 +86,7 @@ def test_retrieve_from_both_tiers_and_promote(fp8):
     kbar = O.page_summarize(np_of(kbank))
     ref_idx, _, ref_chunk = O.select_pages(np_of(q), kbar, np_of(cur), np_of(torch.stack(ps)), PPC, 2)
     assert ref_chunk == 2 and idx == ref_idx.tolist() == [9, 11]
-    ek, ev = _expected(cache, ks, fp8), _expected(cache, vs, fp8)
+    ek, ev = _expected(cache, ks, fmt), _expected(cache, vs, fmt)
     assert np.array_equal(_bits(kb), np.concatenate([ek[i] for i in idx]))
     assert np.array_equal(_bits(vb), np.concatenate([ev[i] for i in idx]))
     # both pages lived in DRAM (chunk 2 is old): now promoted, DRAM copies kept
@@ -103,14 +105,14 @@ def test_retrieve_from_both_tiers_and_promote(fp8):
     idx2 = cache.retrieve(q, cur, 2, kb, vb)
     wa.wa_check()
     assert idx2 == [9, 11]
-    ek, ev = _expected(cache, ks, fp8), _expected(cache, vs, fp8)
+    ek, ev = _expected(cache, ks, fmt), _expected(cache, vs, fmt)
     assert np.array_equal(_bits(kb), np.concatenate([ek[i] for i in idx2]))
     assert np.array_equal(_bits(vb), np.concatenate([ev[i] for i in idx2]))
     cache.close()
 
 
-@pytest.mark.parametrize("fp8", [False, True])
-def test_offloads_in_flight_are_waited_for(fp8):
+@pytest.mark.parametrize("fmt", ["native", "fp8", "nvfp4"])
+def test_offloads_in_flight_are_waited_for(fmt):
     """Ten chunks appended back to back into an HBM tier of one chunk (every
     append offloads the previous chunk, 36 offloads through a staging ring of
     8 pages), then, with no synchronisation, a retrieval of the planted pages
@@ -118,7 +120,7 @@ def test_offloads_in_flight_are_waited_for(fp8):
     flight -- and a window over the whole sequence."""
     u = synth.normal((H, D), synth.seed_of("cache", "dir"), DEV) * 0.6
     cache = wa.WaCache(H, D, P, PPC, hbm_pages=PPC, host_pages=40, max_chunks=10,
-                       prompt_dim=PDIM, dram_fp8=fp8)
+                       prompt_dim=PDIM, dram_format=fmt)
     ks, vs, ps = [], [], []
     for m in range(10):
         k, v, pr = _chunk(m, plant=(0, 2) if m == 8 else None, u=u)
@@ -140,7 +142,7 @@ def test_offloads_in_flight_are_waited_for(fp8):
     # 36 by the appends, 2 by the promotion of pages 32 and 34 (chunk 9's 36, 37)
     assert st["offloads"] == 38 and st["reclaims"] == 0
     assert idx == [32, 34]
-    ek, ev = _expected(cache, ks, fp8), _expected(cache, vs, fp8)
+    ek, ev = _expected(cache, ks, fmt), _expected(cache, vs, fmt)
     assert np.array_equal(_bits(kb), np.concatenate([ek[i] for i in idx]))
     assert np.array_equal(_bits(vb), np.concatenate([ev[i] for i in idx]))
     assert np.array_equal(_bits(ko), ek.reshape(40 * P, H, D))
@@ -162,15 +164,15 @@ def test_retrieve_without_prompt_stage():
     cache.close()
 
 
-@pytest.mark.parametrize("fp8", [False, True])
+@pytest.mark.parametrize("fmt", ["native", "fp8", "nvfp4"])
 @pytest.mark.parametrize("n_tok", [600, 256, 1, 17 * P + 100, 20 * P])
-def test_window(n_tok, fp8):
-    cache, ks, vs, _, _, _ = _setup(fp8=fp8)
+def test_window(n_tok, fmt):
+    cache, ks, vs, _, _, _ = _setup(fmt=fmt)
     ko = torch.empty((n_tok, H, D), dtype=torch.bfloat16, device=DEV)
     vo = torch.empty_like(ko)
     cache.window(n_tok, ko, vo)
     wa.wa_check()
-    ek = _expected(cache, ks, fp8).reshape(-1, H, D)
-    ev = _expected(cache, vs, fp8).reshape(-1, H, D)
+    ek = _expected(cache, ks, fmt).reshape(-1, H, D)
+    ev = _expected(cache, vs, fmt).reshape(-1, H, D)
     assert np.array_equal(_bits(ko), ek[-n_tok:]) and np.array_equal(_bits(vo), ev[-n_tok:])
     cache.close()

@@ -37,15 +37,17 @@ def test_denoising_reuse_of_a_21_frame_window():
     assert torch.equal(kw, kw0) and torch.equal(vw, vw0)
 
 
-@pytest.mark.parametrize("mode", ["pipeline", "serial", "direct", "fp8", "fp8_pipeline"])
+@pytest.mark.parametrize("mode", ["pipeline", "serial", "direct", "fp8", "fp8_pipeline", "nvfp4",
+                                  "nvfp4_pipeline"])
 def test_tiered_layer_pipeline(mode):
     """Three layers, 12 pages of 700 tokens each in pinned host memory, top-4
     per layer; the double-buffered side-stream fetch must give every layer the
     pages the oracle picks (bit-exact) and the oracle's attention.  The fp8
-    modes fetch the FP8 copy of the pages (compressed DRAM tier): the reference
-    attention then runs over the oracle's decoded pages."""
+    modes fetch the FP8 copy of the pages and the nvfp4 modes the NVFP4 copy
+    (compressed DRAM tier): the reference attention then runs over the
+    oracle's decoded pages."""
     H, P, NPG, NQ, NLOC, NL = 2, 700, 12, 300, 90, 3
-    fp8 = mode.startswith("fp8")
+    fp8, nv = mode.startswith("fp8"), mode.startswith("nvfp4")
     layers, refs = [], []
     for l in range(NL):
         c = synth.make_chunk_case(f"tier{l}", n_heads=H, head_dim=128, page_tokens=P,
@@ -61,9 +63,17 @@ def test_tiered_layer_pipeline(mode):
             ps = torch.empty((NPG, P, H), dtype=torch.float32).pin_memory()
             wa.wa_fp8_encode(pages.to(DEV).reshape(NPG * P, H, 128), pc, ps)
             codes += [pc, ps]
+        nvc = []
+        for pages in (c.k_pages, c.v_pages):
+            arrs = (torch.empty((NPG, P, H, 64), dtype=torch.uint8).pin_memory(),
+                    torch.empty((NPG, P, H, 8), dtype=torch.uint8).pin_memory(),
+                    torch.empty((NPG, P, H), dtype=torch.float32).pin_memory())
+            wa.wa_nvfp4_encode(pages.to(DEV).reshape(NPG * P, H, 128), *arrs)
+            nvc.append(arrs)
         wa.wa_check()
         layers.append(TierLayer(c.q.to(DEV), c.k_loc.to(DEV), c.v_loc.to(DEV), kbar,
-                                c.k_pages.pin_memory(), c.v_pages.pin_memory(), out, *codes))
+                                c.k_pages.pin_memory(), c.v_pages.pin_memory(), out, *codes,
+                                k_nv=nvc[0], v_nv=nvc[1]))
         okp, ovp = np_of(c.k_pages), np_of(c.v_pages)
         idx, _, _ = O.select_pages(np_of(c.q), O.page_summarize(okp), None, None, 1, 4)
         if fp8:
@@ -71,6 +81,11 @@ def test_tiered_layer_pipeline(mode):
                 cc, ss = O.fp8_encode_rows(pg.reshape(NPG * P, H, 128))
                 return O.bf16_bits(O.fp8_decode_rows(cc, ss)).reshape(NPG, P, H, 128)
             okp, ovp = dec(okp), dec(ovp)
+        if nv:
+            def dec4(pg):
+                return O.bf16_bits(O.nvfp4_decode_rows(*O.nvfp4_encode_rows(
+                    pg.reshape(NPG * P, H, 128)))).reshape(NPG, P, H, 128)
+            okp, ovp = dec4(okp), dec4(ovp)
         ref, _ = O.block_attn(np_of(c.q), O.gather_pages(okp, idx), O.gather_pages(ovp, idx),
                               np_of(c.k_loc), np_of(c.v_loc))
         refs.append((idx, ref))
