@@ -202,7 +202,8 @@ wa_status wa_select_pages_per_head(const void* q, wa_dtype dt, int n_q, int n_he
  * so the buffer keeps the token-major [k_p*page_tokens][n_heads][head_dim]
  * layout that wa_block_attn reads.  idx_dev: device int32 [n_heads][k_p].
  * Device sources only (pages in pinned host memory: WA_ERR_INVALID_ARG); a
- * head row must be whole 16-byte vectors (WA_ERR_SHAPE).  Bad indices zero
+ * head row must be whole 16-byte vectors, n_heads <= 1024 and k_p <= 32767
+ * (WA_ERR_SHAPE).  Bad indices zero
  * the head's slice of that slot and record WA_ERR_INDEX for wa_check.
  */
 wa_status wa_gather_pages_per_head(const void* k_pages, const void* v_pages, wa_dtype dt,

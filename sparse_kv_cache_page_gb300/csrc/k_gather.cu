@@ -60,46 +60,58 @@ k_gather_pages(const uint4* __restrict__ k_pages, const uint4* __restrict__ v_pa
 }
 
 // Per-head page sets: head h's slice of buffer token s*P + t comes from page
-// idx[h*k_p + s].  Each unit is one 16-byte vector of the destination, so
-// stores stay contiguous; a head row (d elements) is hv vectors of one page.
+// idx[h*k_p + s].  One CTA copies kPhRows token rows of one (tensor, slot);
+// the slot's page for every head is read once into shared memory, and each
+// thread walks its (row, vector) position by fixed increments, so the only
+// arithmetic per 16-byte vector is an address.  A head row (d elements) is hv
+// vectors of one page.
+constexpr int kPhRows = 32;
+constexpr int kMaxHeads = 1024;
+
 __global__ void __launch_bounds__(kThreads)
 k_gather_per_head(const uint4* __restrict__ k_pages, const uint4* __restrict__ v_pages,
-                  int n_pages, int page_tokens, int n_heads, int hv,
+                  int n_pages, int page_tokens, int n_heads, int hv, int hv_shift,
                   const int32_t* __restrict__ idx, int k_p, uint4* __restrict__ k_buf,
-                  uint4* __restrict__ v_buf, size_t vecs_per_tensor, Ctrl* ctrl) {
-  const int n_tensors = v_pages ? 2 : 1;
-  const size_t row_vecs = (size_t)n_heads * hv;            // one token row
-  const size_t slab_vecs = row_vecs * page_tokens;         // one page
-  const size_t total = vecs_per_tensor * n_tensors;
-  const size_t step = (size_t)gridDim.x * kThreads * kUnroll;
-  for (size_t base = (size_t)blockIdx.x * kThreads * kUnroll; base < total; base += step) {
+                  uint4* __restrict__ v_buf, Ctrl* ctrl) {
+  __shared__ int pg[kMaxHeads];
+  const int slot = blockIdx.y % k_p, tensor = blockIdx.y / k_p;
+  for (int h = threadIdx.x; h < n_heads; h += kThreads) {
+    const int p = __ldg(idx + h * k_p + slot);
+    const bool bad = p < 0 || p >= n_pages;
+    pg[h] = bad ? -1 : p;
+    if (bad && blockIdx.x == 0) atomicOr(&ctrl->status, kStatusIndex);   // slot zeroed, recorded
+  }
+  __syncthreads();
+  const uint4* src = tensor ? v_pages : k_pages;
+  uint4* dst = tensor ? v_buf : k_buf;
+  const int row_vecs = n_heads * hv;
+  const size_t slab_vecs = (size_t)row_vecs * page_tokens;
+  const int r0 = blockIdx.x * kPhRows;
+  const int n = (min(page_tokens, r0 + kPhRows) - r0) * row_vecs;   // vectors of this chunk
+  const int drow = kThreads / row_vecs, dvec = kThreads - drow * row_vecs;   // dvec < row_vecs
+  int row = threadIdx.x / row_vecs, vec = threadIdx.x - row * row_vecs;
+  for (int w = threadIdx.x; w < n; w += kThreads * kUnroll) {
     uint4 r[kUnroll];
-    size_t dv[kUnroll];
+    size_t at[kUnroll];
 #pragma unroll
     for (int u = 0; u < kUnroll; ++u) {
-      const size_t w = base + (size_t)u * kThreads + threadIdx.x;
-      dv[u] = w;
-      if (w >= total) continue;
-      const int tensor = w >= vecs_per_tensor;
-      const size_t v = w - (tensor ? vecs_per_tensor : 0);
-      const int slot = (int)(v / slab_vecs);
-      const size_t in_slab = v % slab_vecs;
-      const int h = (int)((in_slab % row_vecs) / hv);
-      const int page = __ldg(idx + h * k_p + slot);
-      if (page < 0 || page >= n_pages) {
-        r[u] = make_uint4(0, 0, 0, 0);
-        atomicOr(&ctrl->status, kStatusIndex);
-      } else {
-        r[u] = __ldcs((tensor ? v_pages : k_pages) + (size_t)page * slab_vecs + in_slab);
+      if (w + u * kThreads < n) {
+        const int h = hv_shift >= 0 ? (vec >> hv_shift) : vec / hv;
+        const int p = pg[h];
+        const size_t off = (size_t)(r0 + row) * row_vecs + vec;
+        at[u] = (size_t)slot * slab_vecs + off;
+        r[u] = p < 0 ? make_uint4(0, 0, 0, 0) : __ldcs(src + (size_t)p * slab_vecs + off);
+      }
+      row += drow;
+      vec += dvec;
+      if (vec >= row_vecs) {
+        vec -= row_vecs;
+        ++row;
       }
     }
 #pragma unroll
-    for (int u = 0; u < kUnroll; ++u) {
-      const size_t w = dv[u];
-      if (w >= total) continue;
-      if (w >= vecs_per_tensor) v_buf[w - vecs_per_tensor] = r[u];
-      else k_buf[w] = r[u];
-    }
+    for (int u = 0; u < kUnroll; ++u)
+      if (w + u * kThreads < n) dst[at[u]] = r[u];
   }
 }
 
@@ -133,21 +145,20 @@ wa_status launch_gather_per_head(const void* k_pages, const void* v_pages, int n
                                  int page_tokens, int n_heads, size_t head_row_bytes,
                                  const int32_t* idx_dev, int k_p, void* k_buf, void* v_buf,
                                  cudaStream_t s) {
+  const int hv = (int)(head_row_bytes / 16);
+  if (n_heads > kMaxHeads || (long long)n_heads * hv > (1 << 20) || k_p > 32767) return WA_ERR_SHAPE;
   Ctrl* ctrl = nullptr;
   wa_status rc = get_ctrl(&ctrl);
   if (rc != WA_OK) return rc;
-  const int hv = (int)(head_row_bytes / 16);
-  const size_t vecs = (size_t)k_p * page_tokens * n_heads * hv;
-  const size_t total = vecs * (v_pages ? 2 : 1);
-  int dev = 0, sms = 148;
-  cudaGetDevice(&dev);
-  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  size_t grid = (size_t)sms * 8;
-  const size_t need = (total + (size_t)kThreads * kUnroll - 1) / ((size_t)kThreads * kUnroll);
-  if (grid > need) grid = need;
-  k_gather_per_head<<<(unsigned)grid, kThreads, 0, s>>>(
-      (const uint4*)k_pages, (const uint4*)v_pages, n_pages, page_tokens, n_heads, hv, idx_dev,
-      k_p, (uint4*)k_buf, (uint4*)v_buf, vecs, ctrl);
+  int hv_shift = -1;
+  if ((hv & (hv - 1)) == 0) {
+    hv_shift = 0;
+    while ((1 << hv_shift) < hv) ++hv_shift;
+  }
+  dim3 grid((unsigned)((page_tokens + kPhRows - 1) / kPhRows), (unsigned)(k_p * (v_pages ? 2 : 1)));
+  k_gather_per_head<<<grid, kThreads, 0, s>>>((const uint4*)k_pages, (const uint4*)v_pages, n_pages,
+                                              page_tokens, n_heads, hv, hv_shift, idx_dev, k_p,
+                                              (uint4*)k_buf, (uint4*)v_buf, ctrl);
   return cuda_status(cudaPeekAtLastError());
 }
 
