@@ -117,8 +117,8 @@ class TieredPipeline:
         timing), "fp8" (as "direct", but the pages cross the link as FP8 codes
         and scales and are decoded to bf16 on the device: the compressed DRAM
         tier), "fp8_pipeline" (the FP8 pages fetched by the copy engine on the
-        side stream into a staging slot, decoded on the main stream before
-        the layer's attention), "nvfp4" / "nvfp4_pipeline" (the same with the
+        side stream into a staging slot and decoded there, overlapping the
+        previous layer's attention), "nvfp4" / "nvfp4_pipeline" (the same with the
         NVFP4 copy: E2M1 codes and two levels of scales).  Returns the page
         indices [n_layers][k_p] (int32; pinned host memory, or device memory in
         the "direct", "fp8" and "nvfp4" modes)."""
@@ -135,26 +135,28 @@ class TieredPipeline:
         ev_copy = [torch.cuda.Event() for _ in range(n)]
         ev_attn = [torch.cuda.Event() for _ in range(n)]
         if mode in ("fp8_pipeline", "nvfp4_pipeline"):
+            # side stream: fetch layer l's compressed pages into a staging slot,
+            # then (once layer l-2's attention has read the bf16 buffer) decode
+            # them; the main stream only runs attention
             nv = mode == "nvfp4_pipeline"
             stage = self._staging4() if nv else self._staging()
-            ev_dec = [torch.cuda.Event() for _ in range(n)]
             for l, ly in enumerate(layers):
                 kb, vb = self.bufs[l % 2]
                 st = stage[l % 2]
                 with torch.cuda.stream(self.side):
-                    if l >= 2:
-                        self.side.wait_event(ev_dec[l - 2])
                     (self._fetch_nvfp4 if nv else self._fetch_fp8)(ly, idx_h[l], st)
+                    if l >= 2:
+                        self.side.wait_event(ev_attn[l - 2])
+                    if nv:
+                        wa_gather_pages_nvfp4(*st["k"], self.ident, kb, stream=self.side)
+                        wa_gather_pages_nvfp4(*st["v"], self.ident, vb, stream=self.side)
+                    else:
+                        wa_gather_pages_fp8(st["kc"], st["ks"], self.ident, kb, stream=self.side)
+                        wa_gather_pages_fp8(st["vc"], st["vs"], self.ident, vb, stream=self.side)
                     ev_copy[l].record(self.side)
                 main.wait_event(ev_copy[l])
-                if nv:
-                    wa_gather_pages_nvfp4(*st["k"], self.ident, kb)
-                    wa_gather_pages_nvfp4(*st["v"], self.ident, vb)
-                else:
-                    wa_gather_pages_fp8(st["kc"], st["ks"], self.ident, kb)
-                    wa_gather_pages_fp8(st["vc"], st["vs"], self.ident, vb)
-                ev_dec[l].record(main)
                 wa_block_attn(ly.q, kb, vb, ly.k_loc, ly.v_loc, ly.out)
+                ev_attn[l].record(main)
             main.wait_stream(self.side)
             return idx_h
         for l, ly in enumerate(layers):

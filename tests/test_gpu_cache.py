@@ -176,3 +176,53 @@ def test_window(n_tok, fmt):
     ev = _expected(cache, vs, fmt).reshape(-1, H, D)
     assert np.array_equal(_bits(ko), ek[-n_tok:]) and np.array_equal(_bits(vo), ev[-n_tok:])
     cache.close()
+
+
+@pytest.mark.parametrize("fmt", ["native", "fp8", "nvfp4"])
+def test_full_size_pages(fmt):
+    """Pages at the workload's full size (12,480 tokens x 12 heads x 128): three
+    chunks of 4 pages through a 4-page HBM tier, then a retrieval whose prompt
+    recalls the offloaded first chunk; the selection equals the oracle's and a
+    sample of 400 token rows of both retrieved pages (K and V) reads back as the
+    page, or the oracle codec's round trip of it."""
+    P, H, D, PPC, PDIM = 12480, 12, 128, 4, 64
+    u = synth.normal((H, D), synth.seed_of("cachefull", "dir"), DEV) * 0.6
+    cache = wa.WaCache(H, D, P, PPC, hbm_pages=PPC, host_pages=12, max_chunks=3, prompt_dim=PDIM,
+                       dram_format=fmt)
+    ks, vs, ps = [], [], []
+    for m in range(3):
+        s = lambda t: synth.seed_of("cachefull", m, t)  # noqa: E731
+        k = synth.normal((PPC * P, H, D), s("k"), DEV)
+        if m == 0:
+            for j in (1, 2):
+                k[j * P:(j + 1) * P] += u
+        k = k.to(torch.bfloat16)
+        v = synth.normal((PPC * P, H, D), s("v"), DEV, torch.bfloat16)
+        pr = synth.normal((PDIM,), s("prompt"), DEV)
+        cache.append(k, v, pr)
+        ks.append(k)
+        vs.append(v)
+        ps.append(pr)
+    q = (synth.normal((512, H, D), synth.seed_of("cachefull", "q"), DEV) + u).to(torch.bfloat16)
+    cur = ps[0] + 0.5 * synth.normal((PDIM,), synth.seed_of("cachefull", "cur"), DEV)
+    kb = torch.empty((2 * P, H, D), dtype=torch.bfloat16, device=DEV)
+    vb = torch.empty_like(kb)
+    idx = cache.retrieve(q, cur, 2, kb, vb)
+    cache.wait_copies()
+    wa.wa_check()
+    kbar = O.page_summarize(np_of(torch.cat(ks)).reshape(-1, P, H, D))
+    ref_idx, _, ref_chunk = O.select_pages(np_of(q), kbar, np_of(cur), np_of(torch.stack(ps)),
+                                           PPC, 2)
+    assert ref_chunk == 0 and idx == ref_idx.tolist() == [1, 2]
+    assert cache.stats()["promotions"] == 2
+    rows = np.random.default_rng(8).integers(0, P, 400)
+    for buf, src in ((kb, ks[0]), (vb, vs[0])):
+        for slot, page in enumerate(idx):
+            got = _bits(buf[torch.from_numpy(slot * P + rows).to(DEV)])
+            x = np_of(src[torch.from_numpy(page * P + rows).to(DEV)])
+            if fmt == "fp8":
+                x = O.bf16_bits(O.fp8_decode_rows(*O.fp8_encode_rows(x)))
+            elif fmt == "nvfp4":
+                x = O.bf16_bits(O.nvfp4_decode_rows(*O.nvfp4_encode_rows(x)))
+            assert np.array_equal(got, x), (fmt, page)
+    cache.close()

@@ -124,3 +124,27 @@ def test_attention_over_nvfp4_pages():
     dist_ref = np.abs(ref_fp4 - ref_bf16)
     assert abs(dist_gpu.mean() - dist_ref.mean()) <= BF16_MEAN_ABS
     assert dist_gpu.max() <= dist_ref.max() + BF16_MAX_ABS
+
+
+def test_full_size_pages_sampled():
+    """Two pages at the workload's full size (12,480 tokens x 12 heads x 128):
+    row scales, block scales, codes and decoded values on a sample of 512
+    (token, head) rows plus the first and last, against the oracle."""
+    P, H, d = 12480, 12, 128
+    x = synth.normal((2 * P, H, d), synth.seed_of("fp4full"), DEV, torch.bfloat16)
+    codes = torch.empty((2 * P, H, d // 2), dtype=torch.uint8, device=DEV)
+    bsc = torch.empty((2 * P, H, d // 16), dtype=torch.uint8, device=DEV)
+    rsc = torch.empty((2 * P, H), dtype=torch.float32, device=DEV)
+    out = torch.empty_like(x)
+    wa.wa_nvfp4_encode(x, codes, bsc, rsc)
+    wa.wa_nvfp4_decode(codes, bsc, rsc, out)
+    wa.wa_check()
+    rng = np.random.default_rng(3)
+    t = np.concatenate([[0, 2 * P - 1], rng.integers(0, 2 * P, 512)])
+    xs = np_of(x[torch.from_numpy(t).to(DEV)])
+    rc, rb, rg = O.nvfp4_encode_rows(xs)
+    tt = torch.from_numpy(t).to(DEV)
+    assert np.array_equal(rsc[tt].cpu().numpy(), rg)
+    assert np.array_equal(bsc[tt].cpu().numpy(), rb)
+    assert np.array_equal(codes[tt].cpu().numpy(), rc)
+    assert np.array_equal(_bits(out[tt]), O.bf16_bits(O.nvfp4_decode_rows(rc, rb, rg)))

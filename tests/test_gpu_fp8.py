@@ -99,3 +99,24 @@ def test_attention_over_fp8_pages_close_to_bf16():
     wa.wa_check()
     err = (o1 - o2).abs()
     assert err.max().item() < 2e-2 and err.mean().item() < 2e-3, (err.max().item(), err.mean().item())
+
+
+def test_full_size_pages_sampled():
+    """Two pages at the workload's full size (12,480 tokens x 12 heads x 128):
+    codes, scales and decoded values on a sample of 512 (token, head) rows plus
+    the first and last, against the oracle."""
+    P, H, d = 12480, 12, 128
+    x = synth.normal((2 * P, H, d), synth.seed_of("fp8full"), DEV, torch.bfloat16)
+    codes = torch.empty((2 * P, H, d), dtype=torch.uint8, device=DEV)
+    scales = torch.empty((2 * P, H), dtype=torch.float32, device=DEV)
+    out = torch.empty_like(x)
+    wa.wa_fp8_encode(x, codes, scales)
+    wa.wa_fp8_decode(codes, scales, out)
+    wa.wa_check()
+    rng = np.random.default_rng(4)
+    t = torch.from_numpy(np.concatenate([[0, 2 * P - 1], rng.integers(0, 2 * P, 512)])).to(DEV)
+    rc, rs = O.fp8_encode_rows(np_of(x[t]))
+    assert np.array_equal(scales[t].cpu().numpy(), rs)
+    assert np.array_equal(codes[t].cpu().numpy(), rc)
+    ref = O.bf16_bits(O.fp8_decode_rows(rc, rs))
+    assert np.array_equal(out[t].view(torch.int16).cpu().numpy().view(np.uint16), ref)
