@@ -582,8 +582,10 @@ def run_cache(args, world, rank, local):
 
 def run_one_kernel(args, local):
     """One kernel alone at the workload's shape (inputs drawn directly, no page
-    bank): the attention over a 49,920-token buffer + 4,680 local tokens, or
-    the gather of 4 pages from a 12-page bank.  Used for profiling captures."""
+    bank): the attention over a 49,920-token buffer + 4,680 local tokens, the
+    gather of 4 pages from a 12-page bank, or a page codec (FP8 / NVFP4) encoding
+    and decoding 8 pages (307 MB of bf16, larger than L2).  Used for profiling
+    captures."""
     import torch
 
     import sparse_kv_cache_page_gb300 as wa
@@ -611,6 +613,41 @@ def run_one_kernel(args, local):
         o = torch.zeros((NQ, H, D), dtype=torch.float32, device=dev)
         fn = lambda: wa.wa_linear_branch(q, kb, vb, kl, vl, ek, ev, o)  # noqa: E731
         work, unit = (2 * H * L * R * 2 + 2 * L * H * D * 2) / 1e9, "GB/s (E + K,V read)"
+    elif args.kernel in ("fp8", "nvfp4"):
+        x = g((8 * P, H, D), "pages")
+        y = torch.empty_like(x)
+        n = 8 * P * H
+        if args.kernel == "fp8":
+            c = torch.empty((8 * P, H, D), dtype=torch.uint8, device=dev)
+            sc = torch.empty((8 * P, H), dtype=torch.float32, device=dev)
+            enc = lambda: wa.wa_fp8_encode(x, c, sc)  # noqa: E731
+            dec = lambda: wa.wa_fp8_decode(c, sc, y)  # noqa: E731
+            packed = n * (D + 4)
+        else:
+            c = torch.empty((8 * P, H, D // 2), dtype=torch.uint8, device=dev)
+            b = torch.empty((8 * P, H, D // 16), dtype=torch.uint8, device=dev)
+            r = torch.empty((8 * P, H), dtype=torch.float32, device=dev)
+            enc = lambda: wa.wa_nvfp4_encode(x, c, b, r)  # noqa: E731
+            dec = lambda: wa.wa_nvfp4_decode(c, b, r, y)  # noqa: E731
+            packed = n * (D // 2 + D // 16 + 4)
+        out = {"kernel": args.kernel, "steps": args.steps, "warmup": args.warmup,
+               "bytes_per_launch": n * D * 2 + packed}
+        hbm = peaks()[0]
+        for name, fn in (("encode", enc), ("decode", dec)):
+            for _ in range(args.warmup):
+                fn()
+            wa.wa_check()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            for _ in range(args.steps):
+                fn()
+            e1.record()
+            torch.cuda.synchronize()
+            wa.wa_check()
+            ms = e0.elapsed_time(e1) / args.steps
+            gbs = (n * D * 2 + packed) / (ms * 1e-3) / 1e9
+            out[name] = {"ms": round(ms, 4), "GB/s": round(gbs, 1), "frac_of_hbm": round(gbs / hbm, 3)}
+        return out
     else:
         kp, vp = g((12, P, H, D), "kp"), g((12, P, H, D), "vp")
         idx = torch.tensor([9, 2, 5, 11], dtype=torch.int32, device=dev)
@@ -873,7 +910,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-context", action="store_true",
                     help="skip the PyTorch attention context timing")
-    ap.add_argument("--kernel", default="all", choices=["all", "attention", "gather", "linear"],
+    ap.add_argument("--kernel", default="all",
+                    choices=["all", "attention", "gather", "linear", "fp8", "nvfp4"],
                     help="time one kernel alone on its own inputs (for profiling)")
     ap.add_argument("--workload", default="worldattention",
                     choices=["worldattention", "denoise", "hybrid", "hsa", "per_head", "cache",

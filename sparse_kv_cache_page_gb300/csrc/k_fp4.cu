@@ -12,8 +12,8 @@
 // pack two elements per byte (the even element in the low nibble).  Decoding
 // gives bf16 RNE( fp32(value(c) * fp32(value(sb) * g)) ).
 //
-// One warp per row, E = d / 32 values per lane, a block spans 16 / E lanes,
-// four rows in flight per warp.  The gather-decode reads codes and scales
+// A lane per 16-value block (d / 16 lanes per row), two row groups in flight
+// per warp.  The gather-decode reads codes and scales
 // where they live (device memory or pinned host memory through its device
 // mapping) and writes the bf16 attention buffer.
 #include <cuda_fp16.h>
@@ -24,7 +24,6 @@ namespace wa {
 namespace {
 
 constexpr int kThreads = 256;
-constexpr int kRows = 4;      // rows per warp per step
 
 // two fp32 -> one byte of E2M1 codes: `lo` in bits 0-3, `hi` in bits 4-7
 __device__ __forceinline__ uint32_t enc_e2m1x2(float lo, float hi) {
@@ -53,133 +52,169 @@ __device__ __forceinline__ float dec_e4m3(uint32_t c) {
   return __low2float(*reinterpret_cast<const __half2*>(&h2));
 }
 
-template <int E> struct V;
-template <> struct V<2> { using In = uint32_t; using Code = uint8_t; };
-template <> struct V<4> { using In = uint2; using Code = uint16_t; };
-template <> struct V<8> { using In = uint4; using Code = uint32_t; };
+// RN(x / b) from r = RN(1 / b) (b > 0, normal, 1 / b finite): q0 = RN(x r), the
+// residual e = x - b q0 is exact in one FMA, and q = RN(q0 + e r) is the
+// correctly rounded quotient (Markstein's correction: P. Markstein, "Computation
+// of elementary functions on the IBM RISC System/6000 processor", IBM J. Res.
+// Dev. 34 (1990)).  A zero quotient takes the sign of x, as the division's does.
+__device__ __forceinline__ float div_by(float x, float b, float r) {
+  const float q0 = __fmul_rn(x, r);
+  const float e = __fmaf_rn(-b, q0, x);
+  const float q = __fmaf_rn(e, r, q0);
+  return q == 0.f ? copysignf(0.f, x) : q;
+}
+// a divisor whose reciprocal is a finite normal number takes the fast path
+__device__ __forceinline__ bool div_fast_ok(float b) { return b >= 1e-37f && b <= 1e37f; }
 
-template <int E>
-__device__ __forceinline__ void unpack(const typename V<E>::In& in, float (&x)[E]) {
-  const uint32_t* w = reinterpret_cast<const uint32_t*>(&in);
-#pragma unroll
-  for (int i = 0; i < E / 2; ++i) {
-    x[2 * i] = __uint_as_float(w[i] << 16);
-    x[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
-  }
+// (d0, d1) = (a0 * b0, a1 * b1), one packed instruction, each RN
+__device__ __forceinline__ void fmul2(float& d0, float& d1, float a0, float a1, float b0, float b1) {
+  asm("{\n\t.reg .b64 ra, rb, rd;\n\tmov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
+      "mul.rn.f32x2 rd, ra, rb;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+      : "=f"(d0), "=f"(d1)
+      : "f"(a0), "f"(a1), "f"(b0), "f"(b1));
+}
+// two fp32 -> one bf16x2 word (RNE): lo in bits 0-15, hi in bits 16-31
+__device__ __forceinline__ uint32_t bf16x2(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
 }
 
-template <int E>
+// Each lane owns one 16-value block of a row (LPR = d / 16 lanes per row, 32 /
+// LPR rows per warp step): a 32-byte load, its block maximum in registers, the
+// row maximum over the row's lanes, 8 bytes of codes and its block scale.
+// kSteps row groups are in flight per warp.
+constexpr int kSteps = 2;
+constexpr int kDecSteps = 4;   // decoding: more row groups in flight (reads are small)
+
+template <int LPR>
 __global__ void __launch_bounds__(kThreads)
 k_nvfp4_encode(const __nv_bfloat16* __restrict__ src, size_t n_rows, uint8_t* __restrict__ codes,
                uint8_t* __restrict__ bscales, float* __restrict__ rscales) {
-  using In = typename V<E>::In;
-  constexpr int L = 16 / E;               // lanes per block
-  constexpr int NB = 2 * E;               // blocks per row (d / 16)
-  const int lane = threadIdx.x & 31;
-  const size_t step = (size_t)gridDim.x * (kThreads / 32) * kRows;
-  for (size_t r0 = ((size_t)blockIdx.x * (kThreads / 32) + (threadIdx.x >> 5)) * kRows; r0 < n_rows;
-       r0 += step) {
-    In in[kRows];
+  constexpr int RPW = 32 / LPR;
+  constexpr int D = 16 * LPR;
+  const int lane = threadIdx.x & 31, sub = lane / LPR, b = lane % LPR;
+  const size_t warps = (size_t)gridDim.x * (kThreads / 32);
+  for (size_t g0 = ((size_t)blockIdx.x * (kThreads / 32) + (threadIdx.x >> 5)) * RPW * kSteps;
+       g0 < n_rows; g0 += warps * RPW * kSteps) {
+    uint4 in[kSteps][2];
 #pragma unroll
-    for (int j = 0; j < kRows; ++j)
-      if (r0 + j < n_rows) in[j] = __ldcs(reinterpret_cast<const In*>(src + (r0 + j) * 32 * E) + lane);
+    for (int k = 0; k < kSteps; ++k) {
+      const size_t r = g0 + (size_t)k * RPW + sub;
+      in[k][0] = in[k][1] = make_uint4(0, 0, 0, 0);
+      if (r < n_rows) {
+        const uint4* p = reinterpret_cast<const uint4*>(src + r * D + 16 * b);
+        in[k][0] = __ldcs(p);
+        in[k][1] = __ldcs(p + 1);
+      }
+    }
 #pragma unroll
-    for (int j = 0; j < kRows; ++j) {
-      if (r0 + j >= n_rows) break;
-      const size_t r = r0 + j;
-      float x[E];
-      unpack<E>(in[j], x);
-      float lmax = 0.f;
+    for (int k = 0; k < kSteps; ++k) {
+      const size_t r = g0 + (size_t)k * RPW + sub;
+      const bool live = r < n_rows;             // uniform within a row's lanes
+      float x[16];
+      const uint32_t* w = reinterpret_cast<const uint32_t*>(in[k]);
 #pragma unroll
-      for (int i = 0; i < E; ++i) lmax = fmaxf(lmax, fabsf(x[i]));
-      float amax = lmax;
+      for (int i = 0; i < 8; ++i) {
+        x[2 * i] = __uint_as_float(w[i] << 16);
+        x[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
+      }
+      float bmax = 0.f;
 #pragma unroll
-      for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
-      float bmax = lmax;                   // this lane's block
+      for (int i = 0; i < 16; ++i) bmax = fmaxf(bmax, fabsf(x[i]));
+      float amax = bmax;
 #pragma unroll
-      for (int o = L / 2; o > 0; o >>= 1) bmax = fmaxf(bmax, __shfl_xor_sync(0xffffffffu, bmax, o));
+      for (int o = LPR / 2; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+      if (!live) continue;
       const float g = __fdiv_rn(amax, 2688.0f);
       const float den = __fmul_rn(g, 6.0f);
       const uint32_t sb = den > 0.f ? enc_e4m3(__fdiv_rn(bmax, den)) : 0u;
       const float es = __fmul_rn(dec_e4m3(sb), g);
-      typename V<E>::Code out = 0;
+      uint32_t out[2] = {0u, 0u};
+      if (div_fast_ok(es)) {
+        const float re = __frcp_rn(es);
 #pragma unroll
-      for (int i = 0; i < E / 2; ++i) {
-        const uint32_t byte = es > 0.f ? enc_e2m1x2(__fdiv_rn(x[2 * i], es), __fdiv_rn(x[2 * i + 1], es))
-                                       : 0u;
-        out |= (typename V<E>::Code)(byte << (8 * i));
+        for (int i = 0; i < 8; ++i)
+          out[i >> 2] |= enc_e2m1x2(div_by(x[2 * i], es, re), div_by(x[2 * i + 1], es, re))
+                         << (8 * (i & 3));
+      } else if (es > 0.f) {
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+          out[i >> 2] |= enc_e2m1x2(__fdiv_rn(x[2 * i], es), __fdiv_rn(x[2 * i + 1], es))
+                         << (8 * (i & 3));
       }
-      reinterpret_cast<typename V<E>::Code*>(codes + r * 16 * E)[lane] = out;
-      if (lane % L == 0) bscales[r * NB + lane / L] = (uint8_t)sb;
-      if (lane == 0) rscales[r] = g;
+      *reinterpret_cast<uint2*>(codes + r * (D / 2) + 8 * b) = make_uint2(out[0], out[1]);
+      bscales[r * LPR + b] = (uint8_t)sb;
+      if (b == 0) rscales[r] = g;
     }
   }
 }
 
 // out[s*P + t][h] = decode(pages[idx[s]][t][h]); idx NULL: out row r = row r.
-template <int E>
+template <int LPR>
 __global__ void __launch_bounds__(kThreads)
 k_nvfp4_decode(const uint8_t* __restrict__ codes, const uint8_t* __restrict__ bscales,
                const float* __restrict__ rscales, const int32_t* __restrict__ idx, int n_pages,
                size_t page_rows, size_t n_rows, __nv_bfloat16* __restrict__ out, Ctrl* ctrl) {
-  using Code = typename V<E>::Code;
-  constexpr int L = 16 / E;
-  constexpr int NB = 2 * E;
-  const int lane = threadIdx.x & 31;
-  const size_t step = (size_t)gridDim.x * (kThreads / 32) * kRows;
-  for (size_t r0 = ((size_t)blockIdx.x * (kThreads / 32) + (threadIdx.x >> 5)) * kRows; r0 < n_rows;
-       r0 += step) {
-    Code c[kRows];
-    uint32_t sb[kRows];
-    float g[kRows];
-    bool bad[kRows];
+  constexpr int RPW = 32 / LPR;
+  constexpr int D = 16 * LPR;
+  const int lane = threadIdx.x & 31, sub = lane / LPR, b = lane % LPR;
+  const size_t warps = (size_t)gridDim.x * (kThreads / 32);
+  for (size_t g0 = ((size_t)blockIdx.x * (kThreads / 32) + (threadIdx.x >> 5)) * RPW * kDecSteps;
+       g0 < n_rows; g0 += warps * RPW * kDecSteps) {
+    uint2 c[kDecSteps];
+    uint32_t sb[kDecSteps];
+    float g[kDecSteps];
+    bool bad[kDecSteps];
 #pragma unroll
-    for (int j = 0; j < kRows; ++j) {
-      const size_t r = r0 + j;
-      bad[j] = false;
+    for (int k = 0; k < kDecSteps; ++k) {
+      const size_t r = g0 + (size_t)k * RPW + sub;
+      bad[k] = false;
       if (r >= n_rows) continue;
       size_t src_row = r;
       if (idx) {
         const int page = __ldg(idx + r / page_rows);
-        bad[j] = page < 0 || page >= n_pages;
-        src_row = (size_t)(bad[j] ? 0 : page) * page_rows + r % page_rows;
+        bad[k] = page < 0 || page >= n_pages;
+        src_row = (size_t)(bad[k] ? 0 : page) * page_rows + r % page_rows;
       }
-      if (!bad[j]) {
-        c[j] = reinterpret_cast<const Code*>(codes + src_row * 16 * E)[lane];
-        sb[j] = bscales[src_row * NB + lane / L];
-        g[j] = rscales[src_row];
+      if (!bad[k]) {
+        c[k] = *reinterpret_cast<const uint2*>(codes + src_row * (D / 2) + 8 * b);
+        sb[k] = bscales[src_row * LPR + b];
+        g[k] = rscales[src_row];
       }
     }
 #pragma unroll
-    for (int j = 0; j < kRows; ++j) {
-      const size_t r = r0 + j;
-      if (r >= n_rows) break;
-      typename V<E>::In o;
-      uint32_t* ow = reinterpret_cast<uint32_t*>(&o);
-      if (bad[j]) {
+    for (int k = 0; k < kDecSteps; ++k) {
+      const size_t r = g0 + (size_t)k * RPW + sub;
+      if (r >= n_rows) continue;
+      uint32_t o[8];
+      if (bad[k]) {
 #pragma unroll
-        for (int i = 0; i < E / 2; ++i) ow[i] = 0u;
-        if (lane == 0 && r % page_rows == 0) atomicOr(&ctrl->status, kStatusIndex);
+        for (int i = 0; i < 8; ++i) o[i] = 0u;
+        if (b == 0 && r % page_rows == 0) atomicOr(&ctrl->status, kStatusIndex);
       } else {
-        const float es = __fmul_rn(dec_e4m3(sb[j]), g[j]);
+        const float es = __fmul_rn(dec_e4m3(sb[k]), g[k]);
+        const uint32_t cw[2] = {c[k].x, c[k].y};
 #pragma unroll
-        for (int i = 0; i < E / 2; ++i) {
-          const float2 v = dec_e2m1x2((uint32_t)(c[j] >> (8 * i)) & 0xFFu);
-          const __nv_bfloat16 lo = __float2bfloat16_rn(__fmul_rn(v.x, es));
-          const __nv_bfloat16 hi = __float2bfloat16_rn(__fmul_rn(v.y, es));
-          ow[i] = (uint32_t)__bfloat16_as_ushort(lo) | ((uint32_t)__bfloat16_as_ushort(hi) << 16);
+        for (int i = 0; i < 8; ++i) {
+          const float2 v = dec_e2m1x2((cw[i >> 2] >> (8 * (i & 3))) & 0xFFu);
+          float lo, hi;
+          fmul2(lo, hi, v.x, v.y, es, es);
+          o[i] = bf16x2(lo, hi);
         }
       }
-      reinterpret_cast<typename V<E>::In*>(out + r * 32 * E)[lane] = o;
+      uint4* dst = reinterpret_cast<uint4*>(out + r * D + 16 * b);
+      __stcs(dst, make_uint4(o[0], o[1], o[2], o[3]));
+      __stcs(dst + 1, make_uint4(o[4], o[5], o[6], o[7]));
     }
   }
 }
 
-unsigned grid_for(size_t rows) {
+unsigned grid_for(size_t rows, int head_dim, int steps = kSteps) {
   int dev = 0, sms = 148;
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  const size_t per_block = (size_t)(kThreads / 32) * kRows;
+  const size_t per_block = (size_t)(kThreads / 32) * (512 / head_dim) * steps;
   const size_t need = (rows + per_block - 1) / per_block;
   const size_t cap = (size_t)sms * 8;
   return (unsigned)(need < cap ? need : cap);
@@ -189,14 +224,14 @@ unsigned grid_for(size_t rows) {
 
 wa_status launch_nvfp4_encode(const void* src, size_t n_rows, int head_dim, void* codes,
                               void* bscales, float* rscales, cudaStream_t s) {
-  const unsigned g = grid_for(n_rows);
+  const unsigned g = grid_for(n_rows, head_dim);
   const auto* x = static_cast<const __nv_bfloat16*>(src);
   auto* c = static_cast<uint8_t*>(codes);
   auto* b = static_cast<uint8_t*>(bscales);
-  switch (head_dim / 32) {
-    case 2: k_nvfp4_encode<2><<<g, kThreads, 0, s>>>(x, n_rows, c, b, rscales); break;
+  switch (head_dim / 16) {
     case 4: k_nvfp4_encode<4><<<g, kThreads, 0, s>>>(x, n_rows, c, b, rscales); break;
     case 8: k_nvfp4_encode<8><<<g, kThreads, 0, s>>>(x, n_rows, c, b, rscales); break;
+    case 16: k_nvfp4_encode<16><<<g, kThreads, 0, s>>>(x, n_rows, c, b, rscales); break;
     default: return WA_ERR_SHAPE;
   }
   return cuda_status(cudaPeekAtLastError());
@@ -208,14 +243,14 @@ wa_status launch_nvfp4_decode(const void* codes, const void* bscales, const floa
   Ctrl* ctrl = nullptr;
   wa_status rc = get_ctrl(&ctrl);
   if (rc != WA_OK) return rc;
-  const unsigned g = grid_for(n_rows);
+  const unsigned g = grid_for(n_rows, head_dim, kDecSteps);
   const auto* c = static_cast<const uint8_t*>(codes);
   const auto* b = static_cast<const uint8_t*>(bscales);
   auto* o = static_cast<__nv_bfloat16*>(out);
-  switch (head_dim / 32) {
-    case 2: k_nvfp4_decode<2><<<g, kThreads, 0, s>>>(c, b, rscales, idx, n_pages, page_rows, n_rows, o, ctrl); break;
+  switch (head_dim / 16) {
     case 4: k_nvfp4_decode<4><<<g, kThreads, 0, s>>>(c, b, rscales, idx, n_pages, page_rows, n_rows, o, ctrl); break;
     case 8: k_nvfp4_decode<8><<<g, kThreads, 0, s>>>(c, b, rscales, idx, n_pages, page_rows, n_rows, o, ctrl); break;
+    case 16: k_nvfp4_decode<16><<<g, kThreads, 0, s>>>(c, b, rscales, idx, n_pages, page_rows, n_rows, o, ctrl); break;
     default: return WA_ERR_SHAPE;
   }
   return cuda_status(cudaPeekAtLastError());

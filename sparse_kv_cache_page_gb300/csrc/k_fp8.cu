@@ -9,7 +9,7 @@
 //   bf16 RNE( fp32(value(code) * s) ).
 // A zero row has s = 0 and codes 0.
 //
-// One warp per row (d = 32 e, e in {2, 4, 8} values per lane), four rows in
+// A lane per 16-value chunk of a row (d / 16 lanes per row), two row groups in
 // flight per warp.  The
 // gather-decode kernel reads the selected pages' codes and scales where they
 // live -- device memory or pinned host memory through its device mapping, so
@@ -23,7 +23,6 @@ namespace wa {
 namespace {
 
 constexpr int kThreads = 256;
-constexpr int kRows = 4;      // rows per warp per step
 
 __device__ __forceinline__ uint16_t enc2(float lo, float hi) {
   uint16_t r;
@@ -37,120 +36,158 @@ __device__ __forceinline__ float2 dec2(uint16_t c) {
   return __half22float2(h);   // .x = lower byte's value, .y = upper byte's
 }
 
-template <int E>
-struct Vec;
-template <> struct Vec<2> { using In = uint32_t; using Code = uint16_t; };
-template <> struct Vec<4> { using In = uint2; using Code = uint32_t; };
-template <> struct Vec<8> { using In = uint4; using Code = uint2; };
+// RN(x / b) from r = RN(1 / b) (b > 0, normal, 1 / b finite): q0 = RN(x r), the
+// residual e = x - b q0 is exact in one FMA, and q = RN(q0 + e r) is the
+// correctly rounded quotient (Markstein's correction: P. Markstein, "Computation
+// of elementary functions on the IBM RISC System/6000 processor", IBM J. Res.
+// Dev. 34 (1990)).  A zero quotient takes the sign of x, as the division's does.
+__device__ __forceinline__ float div_by(float x, float b, float r) {
+  const float q0 = __fmul_rn(x, r);
+  const float e = __fmaf_rn(-b, q0, x);
+  const float q = __fmaf_rn(e, r, q0);
+  return q == 0.f ? copysignf(0.f, x) : q;
+}
+// a divisor whose reciprocal is a finite normal number takes the fast path
+__device__ __forceinline__ bool div_fast_ok(float b) { return b >= 1e-37f && b <= 1e37f; }
 
-template <int E>
-__device__ __forceinline__ void unpack_bf16(const typename Vec<E>::In& in, float (&x)[E]) {
-  const uint32_t* w = reinterpret_cast<const uint32_t*>(&in);
-#pragma unroll
-  for (int i = 0; i < E / 2; ++i) {
-    x[2 * i] = __uint_as_float(w[i] << 16);
-    x[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
-  }
+// (d0, d1) = (a0 * b0, a1 * b1), one packed instruction, each RN
+__device__ __forceinline__ void fmul2(float& d0, float& d1, float a0, float a1, float b0, float b1) {
+  asm("{\n\t.reg .b64 ra, rb, rd;\n\tmov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
+      "mul.rn.f32x2 rd, ra, rb;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+      : "=f"(d0), "=f"(d1)
+      : "f"(a0), "f"(a1), "f"(b0), "f"(b1));
+}
+// two fp32 -> one bf16x2 word (RNE): lo in bits 0-15, hi in bits 16-31
+__device__ __forceinline__ uint32_t bf16x2(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
 }
 
-// Each warp takes kRows consecutive rows per step: their loads are issued
-// together, so enough bytes are in flight to stream at HBM (or link) speed.
-template <int E>
+// Each lane owns a 16-value chunk of a row (LPR = d / 16 lanes per row, 32 / LPR
+// rows per warp step): a 32-byte load, the row maximum over the row's lanes,
+// 16 codes (one 16-byte store).  kSteps row groups are in flight per warp.
+constexpr int kSteps = 2;
+constexpr int kDecSteps = 4;   // decoding: more row groups in flight (reads are small)
+
+template <int LPR>
 __global__ void __launch_bounds__(kThreads)
 k_fp8_encode(const __nv_bfloat16* __restrict__ src, size_t n_rows, uint8_t* __restrict__ codes,
              float* __restrict__ scales) {
-  using In = typename Vec<E>::In;
-  const int lane = threadIdx.x & 31;
-  const size_t step = (size_t)gridDim.x * (kThreads / 32) * kRows;
-  for (size_t r0 = ((size_t)blockIdx.x * (kThreads / 32) + (threadIdx.x >> 5)) * kRows; r0 < n_rows;
-       r0 += step) {
-    In in[kRows];
+  constexpr int RPW = 32 / LPR;                 // rows per warp step
+  constexpr int D = 16 * LPR;
+  const int lane = threadIdx.x & 31, sub = lane / LPR, b = lane % LPR;
+  const size_t warps = (size_t)gridDim.x * (kThreads / 32);
+  for (size_t g0 = ((size_t)blockIdx.x * (kThreads / 32) + (threadIdx.x >> 5)) * RPW * kSteps;
+       g0 < n_rows; g0 += warps * RPW * kSteps) {
+    uint4 in[kSteps][2];
 #pragma unroll
-    for (int j = 0; j < kRows; ++j)
-      if (r0 + j < n_rows) in[j] = __ldcs(reinterpret_cast<const In*>(src + (r0 + j) * 32 * E) + lane);
+    for (int k = 0; k < kSteps; ++k) {
+      const size_t r = g0 + (size_t)k * RPW + sub;
+      in[k][0] = in[k][1] = make_uint4(0, 0, 0, 0);
+      if (r < n_rows) {
+        const uint4* p = reinterpret_cast<const uint4*>(src + r * D + 16 * b);
+        in[k][0] = __ldcs(p);
+        in[k][1] = __ldcs(p + 1);
+      }
+    }
 #pragma unroll
-    for (int j = 0; j < kRows; ++j) {
-      if (r0 + j >= n_rows) break;
-      const size_t r = r0 + j;
-      float x[E];
-      unpack_bf16<E>(in[j], x);
+    for (int k = 0; k < kSteps; ++k) {
+      const size_t r = g0 + (size_t)k * RPW + sub;
+      const bool live = r < n_rows;             // uniform within a row's lanes
+      float x[16];
+      const uint32_t* w = reinterpret_cast<const uint32_t*>(in[k]);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        x[2 * i] = __uint_as_float(w[i] << 16);
+        x[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
+      }
       float amax = 0.f;
 #pragma unroll
-      for (int i = 0; i < E; ++i) amax = fmaxf(amax, fabsf(x[i]));
+      for (int i = 0; i < 16; ++i) amax = fmaxf(amax, fabsf(x[i]));
 #pragma unroll
-      for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+      for (int o = LPR / 2; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+      if (!live) continue;
       const float s = __fdiv_rn(amax, 448.0f);
-      typename Vec<E>::Code out;
-      uint16_t* o16 = reinterpret_cast<uint16_t*>(&out);
+      uint32_t out[4];
+      uint16_t* o16 = reinterpret_cast<uint16_t*>(out);
+      if (div_fast_ok(s)) {
+        const float rs = __frcp_rn(s);
 #pragma unroll
-      for (int i = 0; i < E / 2; ++i)
-        o16[i] = s > 0.f ? enc2(__fdiv_rn(x[2 * i], s), __fdiv_rn(x[2 * i + 1], s)) : (uint16_t)0;
-      reinterpret_cast<typename Vec<E>::Code*>(codes + r * 32 * E)[lane] = out;
-      if (lane == 0) scales[r] = s;
+        for (int i = 0; i < 8; ++i) o16[i] = enc2(div_by(x[2 * i], s, rs), div_by(x[2 * i + 1], s, rs));
+      } else {
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+          o16[i] = s > 0.f ? enc2(__fdiv_rn(x[2 * i], s), __fdiv_rn(x[2 * i + 1], s)) : (uint16_t)0;
+      }
+      *reinterpret_cast<uint4*>(codes + r * D + 16 * b) = make_uint4(out[0], out[1], out[2], out[3]);
+      if (b == 0) scales[r] = s;
     }
   }
 }
 
 // out[s*P + t][h] = decode(pages[idx[s]][t][h]); idx NULL: out row r = row r.
-template <int E>
+template <int LPR>
 __global__ void __launch_bounds__(kThreads)
 k_fp8_decode(const uint8_t* __restrict__ codes, const float* __restrict__ scales,
              const int32_t* __restrict__ idx, int n_pages, size_t page_rows, size_t n_rows,
              __nv_bfloat16* __restrict__ out, Ctrl* ctrl) {
-  using Code = typename Vec<E>::Code;
-  const int lane = threadIdx.x & 31;
-  const size_t step = (size_t)gridDim.x * (kThreads / 32) * kRows;
-  for (size_t r0 = ((size_t)blockIdx.x * (kThreads / 32) + (threadIdx.x >> 5)) * kRows; r0 < n_rows;
-       r0 += step) {
-    Code c[kRows];
-    float sc[kRows];
-    bool bad[kRows];
+  constexpr int RPW = 32 / LPR;
+  constexpr int D = 16 * LPR;
+  const int lane = threadIdx.x & 31, sub = lane / LPR, b = lane % LPR;
+  const size_t warps = (size_t)gridDim.x * (kThreads / 32);
+  for (size_t g0 = ((size_t)blockIdx.x * (kThreads / 32) + (threadIdx.x >> 5)) * RPW * kDecSteps;
+       g0 < n_rows; g0 += warps * RPW * kDecSteps) {
+    uint4 c[kDecSteps];
+    float sc[kDecSteps];
+    bool bad[kDecSteps];
 #pragma unroll
-    for (int j = 0; j < kRows; ++j) {
-      const size_t r = r0 + j;
-      bad[j] = false;
+    for (int k = 0; k < kDecSteps; ++k) {
+      const size_t r = g0 + (size_t)k * RPW + sub;
+      bad[k] = false;
       if (r >= n_rows) continue;
       size_t src_row = r;
       if (idx) {
         const int page = __ldg(idx + r / page_rows);
-        bad[j] = page < 0 || page >= n_pages;
-        src_row = (size_t)(bad[j] ? 0 : page) * page_rows + r % page_rows;
+        bad[k] = page < 0 || page >= n_pages;
+        src_row = (size_t)(bad[k] ? 0 : page) * page_rows + r % page_rows;
       }
-      if (!bad[j]) {
-        c[j] = reinterpret_cast<const Code*>(codes + src_row * 32 * E)[lane];
-        sc[j] = scales[src_row];
+      if (!bad[k]) {
+        c[k] = *reinterpret_cast<const uint4*>(codes + src_row * D + 16 * b);
+        sc[k] = scales[src_row];
       }
     }
 #pragma unroll
-    for (int j = 0; j < kRows; ++j) {
-      const size_t r = r0 + j;
-      if (r >= n_rows) break;
-      typename Vec<E>::In o;
-      uint32_t* ow = reinterpret_cast<uint32_t*>(&o);
-      if (bad[j]) {
+    for (int k = 0; k < kDecSteps; ++k) {
+      const size_t r = g0 + (size_t)k * RPW + sub;
+      if (r >= n_rows) continue;
+      uint32_t o[8];
+      if (bad[k]) {
 #pragma unroll
-        for (int i = 0; i < E / 2; ++i) ow[i] = 0u;
-        if (lane == 0 && r % page_rows == 0) atomicOr(&ctrl->status, kStatusIndex);
+        for (int i = 0; i < 8; ++i) o[i] = 0u;
+        if (b == 0 && r % page_rows == 0) atomicOr(&ctrl->status, kStatusIndex);
       } else {
-        const uint16_t* c16 = reinterpret_cast<const uint16_t*>(&c[j]);
+        const uint16_t* c16 = reinterpret_cast<const uint16_t*>(&c[k]);
 #pragma unroll
-        for (int i = 0; i < E / 2; ++i) {
+        for (int i = 0; i < 8; ++i) {
           const float2 v = dec2(c16[i]);
-          const __nv_bfloat16 lo = __float2bfloat16_rn(__fmul_rn(v.x, sc[j]));
-          const __nv_bfloat16 hi = __float2bfloat16_rn(__fmul_rn(v.y, sc[j]));
-          ow[i] = (uint32_t)__bfloat16_as_ushort(lo) | ((uint32_t)__bfloat16_as_ushort(hi) << 16);
+          float lo, hi;
+          fmul2(lo, hi, v.x, v.y, sc[k], sc[k]);
+          o[i] = bf16x2(lo, hi);
         }
       }
-      reinterpret_cast<typename Vec<E>::In*>(out + r * 32 * E)[lane] = o;
+      uint4* dst = reinterpret_cast<uint4*>(out + r * D + 16 * b);
+      __stcs(dst, make_uint4(o[0], o[1], o[2], o[3]));
+      __stcs(dst + 1, make_uint4(o[4], o[5], o[6], o[7]));
     }
   }
 }
 
-unsigned grid_for(size_t rows) {
+unsigned grid_for(size_t rows, int head_dim, int steps = kSteps) {
   int dev = 0, sms = 148;
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  const size_t per_block = (size_t)(kThreads / 32) * kRows;
+  const size_t per_block = (size_t)(kThreads / 32) * (512 / head_dim) * steps;
   const size_t need = (rows + per_block - 1) / per_block;
   const size_t cap = (size_t)sms * 8;
   return (unsigned)(need < cap ? need : cap);
@@ -160,13 +197,13 @@ unsigned grid_for(size_t rows) {
 
 wa_status launch_fp8_encode(const void* src, size_t n_rows, int head_dim, void* codes,
                             float* scales, cudaStream_t s) {
-  const unsigned g = grid_for(n_rows);
+  const unsigned g = grid_for(n_rows, head_dim);
   const auto* x = static_cast<const __nv_bfloat16*>(src);
   auto* c = static_cast<uint8_t*>(codes);
-  switch (head_dim / 32) {
-    case 2: k_fp8_encode<2><<<g, kThreads, 0, s>>>(x, n_rows, c, scales); break;
+  switch (head_dim / 16) {
     case 4: k_fp8_encode<4><<<g, kThreads, 0, s>>>(x, n_rows, c, scales); break;
     case 8: k_fp8_encode<8><<<g, kThreads, 0, s>>>(x, n_rows, c, scales); break;
+    case 16: k_fp8_encode<16><<<g, kThreads, 0, s>>>(x, n_rows, c, scales); break;
     default: return WA_ERR_SHAPE;
   }
   return cuda_status(cudaPeekAtLastError());
@@ -178,13 +215,13 @@ wa_status launch_fp8_decode(const void* codes, const float* scales, const int32_
   Ctrl* ctrl = nullptr;
   wa_status rc = get_ctrl(&ctrl);
   if (rc != WA_OK) return rc;
-  const unsigned g = grid_for(n_rows);
+  const unsigned g = grid_for(n_rows, head_dim, kDecSteps);
   const auto* c = static_cast<const uint8_t*>(codes);
   auto* o = static_cast<__nv_bfloat16*>(out);
-  switch (head_dim / 32) {
-    case 2: k_fp8_decode<2><<<g, kThreads, 0, s>>>(c, scales, idx, n_pages, page_rows, n_rows, o, ctrl); break;
+  switch (head_dim / 16) {
     case 4: k_fp8_decode<4><<<g, kThreads, 0, s>>>(c, scales, idx, n_pages, page_rows, n_rows, o, ctrl); break;
     case 8: k_fp8_decode<8><<<g, kThreads, 0, s>>>(c, scales, idx, n_pages, page_rows, n_rows, o, ctrl); break;
+    case 16: k_fp8_decode<16><<<g, kThreads, 0, s>>>(c, scales, idx, n_pages, page_rows, n_rows, o, ctrl); break;
     default: return WA_ERR_SHAPE;
   }
   return cuda_status(cudaPeekAtLastError());
