@@ -35,9 +35,9 @@
 //   * retrieve: prompt stage + page stage over the summaries (wa_select_pages),
 //     the K_p indices written to mapped host memory (one stream
 //     synchronisation, no copy-engine transfer to queue behind offloads), each selected
-//     page copied into the caller's buffer from its tier (FP8 pages decoded
-//     straight from DRAM through the device mapping); a page found only in
-//     DRAM is promoted to HBM from the caller's buffer;
+//     page copied into the caller's buffer from its tier (compressed DRAM pages
+//     first copied whole by the copy engine, then decoded from HBM); a page
+//     found only in DRAM is promoted to HBM from the caller's buffer;
 //   * window: the last n tokens of the sequence, contiguous, from either tier.
 // The least-recently-used clock ticks once per append and per retrieval.
 // dry_run caches do no CUDA work at all: moves are planned and counted, so
@@ -85,6 +85,8 @@ struct wa_cache {
   bool copies_issued = false;
   float* kbar = nullptr;          // [max_pages][H][d]
   float* prompts = nullptr;       // [max_chunks][prompt_dim]
+  char* fetch = nullptr;          // device copies of compressed DRAM slots being decoded
+  size_t fetch_cap = 0;
   int32_t* idx_host = nullptr;    // [k_p max], pinned and device-mapped
   int32_t* idx_dev = nullptr;     // its device address
   int idx_cap = 0;
@@ -265,10 +267,53 @@ wa_status promote(wa_cache* c, int p, const std::vector<char>& keep, const char*
   return WA_OK;
 }
 
+inline bool compressed(const wa_cache* c) { return fp8(c) || nvfp4(c); }
+
+// A device buffer of at least `bytes` for compressed DRAM slots.
+wa_status ensure_fetch(wa_cache* c, size_t bytes) {
+  if (c->fetch_cap >= bytes) return WA_OK;
+  if (c->fetch) {
+    cudaDeviceSynchronize();             // no decode may still read the old buffer
+    cudaFree(c->fetch);
+    c->fetch = nullptr;
+    c->fetch_cap = 0;
+  }
+  if (cudaMalloc(&c->fetch, bytes) != cudaSuccess) {
+    cudaGetLastError();
+    return WA_ERR_OOM;
+  }
+  c->fetch_cap = bytes;
+  return WA_OK;
+}
+
+// Copy the compressed DRAM slot of page p's K (v = 0) or V into fetch slot f.
+wa_status fetch_slot(wa_cache* c, int p, bool v, int f, cudaStream_t s) {
+  const wa_cache::Entry& e = c->table[p];
+  wa_status rc = wait_host_slot(c, e.host, s);
+  if (rc != WA_OK) return rc;
+  count_bytes(c, cudaMemcpyHostToDevice, c->host_page_bytes);
+  return cuda_status(cudaMemcpyAsync(c->fetch + (size_t)f * c->host_page_bytes,
+                                     host_ptr(c, e.host, v, false), c->host_page_bytes,
+                                     cudaMemcpyHostToDevice, s));
+}
+
+// Decode rows [r0, r0 + rows) of the compressed slot held in fetch slot f into dst.
+wa_status decode_fetched(wa_cache* c, int f, size_t r0, size_t rows, char* dst, cudaStream_t s) {
+  const size_t d = (size_t)c->cfg.head_dim;
+  const char* base = c->fetch + (size_t)f * c->host_page_bytes;
+  if (fp8(c))
+    return wa::launch_fp8_decode(base + r0 * d, reinterpret_cast<const float*>(base + c->code_bytes) + r0,
+                                 nullptr, 1, rows, rows, c->cfg.head_dim, dst, s);
+  return wa::launch_nvfp4_decode(base + r0 * (d / 2), base + c->bs_off + r0 * (d / 16),
+                                 reinterpret_cast<const float*>(base + c->rs_off) + r0, nullptr, 1,
+                                 rows, rows, c->cfg.head_dim, dst, s);
+}
+
 // Copy `rows` (token, head) rows of page p, starting at row r0, into dst
-// (K or V) from the page's HBM copy if it has one, else from DRAM.
+// (K or V) from the page's HBM copy if it has one, else from DRAM (a
+// compressed slot through fetch slot f).
 wa_status read_page(wa_cache* c, int p, bool v, size_t r0, size_t rows, char* dst,
-                    cudaStream_t s) {
+                    cudaStream_t s, int f = 0) {
   const wa_cache::Entry& e = c->table[p];
   const size_t row_bytes = (size_t)c->cfg.head_dim * dt_size(c->cfg.dtype);
   if (e.hbm >= 0) {
@@ -276,22 +321,15 @@ wa_status read_page(wa_cache* c, int p, bool v, size_t r0, size_t rows, char* ds
     return cuda_status(cudaMemcpyAsync(dst, hbm_ptr(c, e.hbm, v) + r0 * row_bytes,
                                        rows * row_bytes, cudaMemcpyDeviceToDevice, s));
   }
+  if (compressed(c)) {
+    wa_status rc = ensure_fetch(c, (size_t)(f + 1) * c->host_page_bytes);
+    if (rc == WA_OK) rc = fetch_slot(c, p, v, f, s);
+    if (rc == WA_OK) rc = decode_fetched(c, f, r0, rows, dst, s);
+    return rc;
+  }
   wa_status rc = wait_host_slot(c, e.host, s);
   if (rc != WA_OK) return rc;
   count_bytes(c, cudaMemcpyHostToDevice, host_row_bytes(c, rows));
-  if (fp8(c)) {
-    const char* base = host_ptr(c, e.host, v, true);
-    const uint8_t* codes = reinterpret_cast<const uint8_t*>(base) + r0 * c->cfg.head_dim;
-    const float* scales = reinterpret_cast<const float*>(base + c->code_bytes) + r0;
-    return wa::launch_fp8_decode(codes, scales, nullptr, 1, rows, rows, c->cfg.head_dim, dst, s);
-  }
-  if (nvfp4(c)) {
-    const size_t d = (size_t)c->cfg.head_dim;
-    const char* base = host_ptr(c, e.host, v, true);
-    return wa::launch_nvfp4_decode(base + r0 * (d / 2), base + c->bs_off + r0 * (d / 16),
-                                   reinterpret_cast<const float*>(base + c->rs_off) + r0, nullptr,
-                                   1, rows, rows, c->cfg.head_dim, dst, s);
-  }
   return cuda_status(cudaMemcpyAsync(dst, host_ptr(c, e.host, v, false) + r0 * row_bytes,
                                      rows * row_bytes, cudaMemcpyHostToDevice, s));
 }
@@ -306,6 +344,7 @@ void release(wa_cache* c) {
     cudaFreeHost(c->host_v);
     cudaFree(c->kbar);
     cudaFree(c->prompts);
+    cudaFree(c->fetch);
     cudaFreeHost(c->idx_host);
     for (cudaEvent_t ev : c->stage_done) cudaEventDestroy(ev);
     for (cudaEvent_t ev : c->host_ready) cudaEventDestroy(ev);
@@ -545,13 +584,37 @@ wa_status wa_cache_retrieve(wa_cache* c, const void* q, int n_q, const float* pr
   memcpy(idx_out, c->idx_host, k_p * sizeof(int32_t));
   std::vector<const char*> dk(k_p), dv(k_p);
   const size_t rows = (size_t)g.page_tokens * g.n_heads;
+  for (int i = 0; i < k_p; ++i)
+    if (idx_out[i] < 0 || idx_out[i] >= c->n_pages) return WA_ERR_INDEX;
+  // compressed DRAM pages: every copy first (the copy engine streams them back
+  // to back), then the decodes from HBM
+  if (compressed(c)) {
+    int n_f = 0;
+    for (int i = 0; i < k_p; ++i)
+      if (c->table[idx_out[i]].hbm < 0) ++n_f;
+    if (n_f > 0 && (rc = ensure_fetch(c, (size_t)2 * n_f * c->host_page_bytes)) != WA_OK) return rc;
+  }
+  int f = 0;
+  std::vector<int> fslot(k_p, -1);
+  for (int i = 0; i < k_p; ++i) {
+    if (!compressed(c) || c->table[idx_out[i]].hbm >= 0) continue;
+    fslot[i] = f;
+    if ((rc = fetch_slot(c, idx_out[i], false, f, s)) != WA_OK ||
+        (rc = fetch_slot(c, idx_out[i], true, f + 1, s)) != WA_OK)
+      return rc;
+    f += 2;
+  }
   for (int i = 0; i < k_p; ++i) {
     const int p = idx_out[i];
-    if (p < 0 || p >= c->n_pages) return WA_ERR_INDEX;
     char* dst_k = static_cast<char*>(k_buf) + (size_t)i * c->page_bytes;
     char* dst_v = static_cast<char*>(v_buf) + (size_t)i * c->page_bytes;
-    rc = read_page(c, p, false, 0, rows, dst_k, s);
-    if (rc == WA_OK) rc = read_page(c, p, true, 0, rows, dst_v, s);
+    if (fslot[i] >= 0) {
+      rc = decode_fetched(c, fslot[i], 0, rows, dst_k, s);
+      if (rc == WA_OK) rc = decode_fetched(c, fslot[i] + 1, 0, rows, dst_v, s);
+    } else {
+      rc = read_page(c, p, false, 0, rows, dst_k, s);
+      if (rc == WA_OK) rc = read_page(c, p, true, 0, rows, dst_v, s);
+    }
     if (rc != WA_OK) return rc;
     dk[i] = dst_k;
     dv[i] = dst_v;
