@@ -192,6 +192,46 @@ k_page_summarize(const T* __restrict__ pages, int page_tokens, int n_rows, int r
 // ---------------------------------------------------------------------------
 // select: mean query -> prompt top-1 -> page scores -> top-K_p
 // ---------------------------------------------------------------------------
+// sum over i in [0, n) of a[i] * b[i] (and of b[i]^2 when nb2 != nullptr) by
+// one warp: 16-byte loads, eight per lane in flight, then a fixed-order warp
+// reduction.  a, b 16-byte aligned and n % 4 == 0; otherwise one float at a time.
+__device__ __forceinline__ float warp_dot(const float* __restrict__ a, const float* __restrict__ b,
+                                          int n, float* nb2) {
+  const int lane = threadIdx.x & 31;
+  float dot = 0.f, sq = 0.f;
+  if ((n & 3) == 0 && ((reinterpret_cast<uintptr_t>(a) | reinterpret_cast<uintptr_t>(b)) & 15) == 0) {
+    const float4* a4 = reinterpret_cast<const float4*>(a);
+    const float4* b4 = reinterpret_cast<const float4*>(b);
+    const int n4 = n >> 2;
+    for (int i0 = 0; i0 < n4; i0 += 32 * 8) {
+      float4 x[8], y[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const int i = i0 + u * 32 + lane;
+        x[u] = i < n4 ? a4[i] : make_float4(0.f, 0.f, 0.f, 0.f);
+        y[u] = i < n4 ? b4[i] : make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        dot += x[u].x * y[u].x + x[u].y * y[u].y + x[u].z * y[u].z + x[u].w * y[u].w;
+        sq += y[u].x * y[u].x + y[u].y * y[u].y + y[u].z * y[u].z + y[u].w * y[u].w;
+      }
+    }
+  } else {
+    for (int i = lane; i < n; i += 32) {
+      dot += a[i] * b[i];
+      sq += b[i] * b[i];
+    }
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    dot += __shfl_xor_sync(0xffffffffu, dot, o);
+    sq += __shfl_xor_sync(0xffffffffu, sq, o);
+  }
+  if (nb2) *nb2 = sq;
+  return dot;
+}
+
 __device__ __forceinline__ float warp_sum(float v) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
@@ -299,14 +339,8 @@ k_select_pages(const T* __restrict__ q, SelectArgs a) {
     int best_m = 0x7fffffff;
     for (int m = warp; m < a.n_chunks; m += nwarps) {
       const float* cm = a.prompt_chunks + (size_t)m * a.prompt_dim;
-      float dot = 0.f, nc = 0.f;
-      for (int i = lane; i < a.prompt_dim; i += 32) {
-        const float c = cm[i];
-        dot += a.prompt_cur[i] * c;
-        nc += c * c;
-      }
-      dot = warp_sum(dot);
-      nc = warp_sum(nc);
+      float nc = 0.f;
+      const float dot = warp_dot(a.prompt_cur, cm, a.prompt_dim, &nc);
       const float cosv = (np > 0.f && nc > 0.f) ? dot / (sqrtf(np) * sqrtf(nc)) : 0.f;
       if (cosv > best) { best = cosv; best_m = m; }   // ascending m: first wins a tie
     }
@@ -336,9 +370,7 @@ k_select_pages(const T* __restrict__ q, SelectArgs a) {
     const int e1 = a.per_head ? e0 + a.head_dim : a.row_elems;
     for (int c = warp; c < n_cand; c += nwarps) {
       const float* kb = a.kbar + (size_t)(cand0 + c) * a.row_elems;
-      float dot = 0.f;
-      for (int e = e0 + lane; e < e1; e += 32) dot += qbar[e] * kb[e];
-      dot = warp_sum(dot);
+      const float dot = warp_dot(qbar + e0, kb + e0, e1 - e0, nullptr);
       if (lane == 0) alpha[c] = dot * inv_sqrt_d;
     }
     __syncthreads();
