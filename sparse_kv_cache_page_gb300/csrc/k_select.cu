@@ -246,6 +246,20 @@ __device__ __forceinline__ unsigned long long score_key(float a, unsigned c) {
   return ((unsigned long long)(~u) << 32) | c;
 }
 
+// Ascending bitonic sort of 32 keys, one per lane, by shuffles.
+__device__ __forceinline__ unsigned long long warp_sort32(unsigned long long key) {
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int k = 2; k <= 32; k <<= 1)
+#pragma unroll
+    for (int j = k >> 1; j > 0; j >>= 1) {
+      const unsigned long long other = __shfl_xor_sync(0xffffffffu, key, j);
+      const bool keep_min = ((lane & j) == 0) == ((lane & k) == 0);
+      key = keep_min ? (other < key ? other : key) : (other > key ? other : key);
+    }
+  return key;
+}
+
 __device__ void bitonic_sort(unsigned long long* keys, int n2) {
   for (int k = 2; k <= n2; k <<= 1) {
     for (int j = k >> 1; j > 0; j >>= 1) {
@@ -365,6 +379,32 @@ k_select_pages(const T* __restrict__ q, SelectArgs a) {
   // c over all heads (one page set) or over one head's slice (a set per head)
   const float inv_sqrt_d = 1.0f / sqrtf((float)a.head_dim);
   const int n_sets = a.per_head ? a.row_elems / a.head_dim : 1;
+  if (a.per_head && n_cand <= 32 && a.k_p <= n_cand) {
+    // a set per head with at most 32 candidates: a warp per head scores them,
+    // sorts the keys in registers, and sorts the chosen candidates by index
+    for (int hs = warp; hs < n_sets; hs += nwarps) {
+      const int e0 = hs * a.head_dim;
+      float my_alpha = 0.f;
+      unsigned long long key = ~0ull;
+      for (int c = 0; c < n_cand; ++c) {
+        const float dot = warp_dot(qbar + e0, a.kbar + (size_t)(cand0 + c) * a.row_elems + e0,
+                                   a.head_dim, nullptr);
+        if (lane == c) {
+          my_alpha = dot * inv_sqrt_d;
+          key = score_key(my_alpha, (unsigned)c);
+        }
+      }
+      key = warp_sort32(key);
+      unsigned long long sel = lane < a.k_p ? (key & 0xffffffffull) : ~0ull;
+      sel = warp_sort32(sel);
+      const int c = lane < a.k_p ? (int)(sel & 0xffffffffull) : 0;
+      const float alpha_c = __shfl_sync(0xffffffffu, my_alpha, c);
+      if (lane < a.k_p) {
+        a.idx_out[hs * a.k_p + lane] = cand0 + c;
+        if (a.scores_out) a.scores_out[hs * a.k_p + lane] = alpha_c;
+      }
+    }
+  } else
   for (int hs = 0; hs < n_sets; ++hs) {
     const int e0 = a.per_head ? hs * a.head_dim : 0;
     const int e1 = a.per_head ? e0 + a.head_dim : a.row_elems;
