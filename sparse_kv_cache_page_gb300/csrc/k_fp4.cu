@@ -18,10 +18,13 @@
 // mapping) and writes the bf16 attention buffer.
 #include <cuda_fp16.h>
 
+#include "codec_math.cuh"
 #include "wa_internal.cuh"
 
 namespace wa {
 namespace {
+
+using namespace codec;
 
 constexpr int kThreads = 256;
 
@@ -52,34 +55,6 @@ __device__ __forceinline__ float dec_e4m3(uint32_t c) {
   return __low2float(*reinterpret_cast<const __half2*>(&h2));
 }
 
-// RN(x / b) from r = RN(1 / b) (b > 0, normal, 1 / b finite): q0 = RN(x r), the
-// residual e = x - b q0 is exact in one FMA, and q = RN(q0 + e r) is the
-// correctly rounded quotient (Markstein's correction: P. Markstein, "Computation
-// of elementary functions on the IBM RISC System/6000 processor", IBM J. Res.
-// Dev. 34 (1990)).  A zero quotient takes the sign of x, as the division's does.
-__device__ __forceinline__ float div_by(float x, float b, float r) {
-  const float q0 = __fmul_rn(x, r);
-  const float e = __fmaf_rn(-b, q0, x);
-  const float q = __fmaf_rn(e, r, q0);
-  return q == 0.f ? copysignf(0.f, x) : q;
-}
-// a divisor whose reciprocal is a finite normal number takes the fast path
-__device__ __forceinline__ bool div_fast_ok(float b) { return b >= 1e-37f && b <= 1e37f; }
-
-// (d0, d1) = (a0 * b0, a1 * b1), one packed instruction, each RN
-__device__ __forceinline__ void fmul2(float& d0, float& d1, float a0, float a1, float b0, float b1) {
-  asm("{\n\t.reg .b64 ra, rb, rd;\n\tmov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
-      "mul.rn.f32x2 rd, ra, rb;\n\tmov.b64 {%0, %1}, rd;\n\t}"
-      : "=f"(d0), "=f"(d1)
-      : "f"(a0), "f"(a1), "f"(b0), "f"(b1));
-}
-// two fp32 -> one bf16x2 word (RNE): lo in bits 0-15, hi in bits 16-31
-__device__ __forceinline__ uint32_t bf16x2(float lo, float hi) {
-  uint32_t r;
-  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
-  return r;
-}
-
 // Each lane owns one 16-value block of a row (LPR = d / 16 lanes per row, 32 /
 // LPR rows per warp step): a 32-byte load, its block maximum in registers, the
 // row maximum over the row's lanes, 8 bytes of codes and its block scale.
@@ -95,6 +70,7 @@ k_nvfp4_encode(const __nv_bfloat16* __restrict__ src, size_t n_rows, uint8_t* __
   constexpr int D = 16 * LPR;
   const int lane = threadIdx.x & 31, sub = lane / LPR, b = lane % LPR;
   const size_t warps = (size_t)gridDim.x * (kThreads / 32);
+  const float r2688 = __frcp_rn(2688.0f);
   for (size_t g0 = ((size_t)blockIdx.x * (kThreads / 32) + (threadIdx.x >> 5)) * RPW * kSteps;
        g0 < n_rows; g0 += warps * RPW * kSteps) {
     uint4 in[kSteps][2];
@@ -112,37 +88,38 @@ k_nvfp4_encode(const __nv_bfloat16* __restrict__ src, size_t n_rows, uint8_t* __
     for (int k = 0; k < kSteps; ++k) {
       const size_t r = g0 + (size_t)k * RPW + sub;
       const bool live = r < n_rows;             // uniform within a row's lanes
-      float x[16];
-      const uint32_t* w = reinterpret_cast<const uint32_t*>(in[k]);
-#pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        x[2 * i] = __uint_as_float(w[i] << 16);
-        x[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
-      }
-      float bmax = 0.f;
-#pragma unroll
-      for (int i = 0; i < 16; ++i) bmax = fmaxf(bmax, fabsf(x[i]));
+      const uint32_t w[8] = {in[k][0].x, in[k][0].y, in[k][0].z, in[k][0].w,
+                             in[k][1].x, in[k][1].y, in[k][1].z, in[k][1].w};
+      const float bmax = absmax16_bf16(w);
       float amax = bmax;
 #pragma unroll
       for (int o = LPR / 2; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
       if (!live) continue;
-      const float g = __fdiv_rn(amax, 2688.0f);
+      const float g = dividend_ok(amax) ? div_rn(amax, 2688.0f, r2688) : __fdiv_rn(amax, 2688.0f);
       const float den = __fmul_rn(g, 6.0f);
       const uint32_t sb = den > 0.f ? enc_e4m3(__fdiv_rn(bmax, den)) : 0u;
       const float es = __fmul_rn(dec_e4m3(sb), g);
-      uint32_t out[2] = {0u, 0u};
+      uint32_t c[8];
       if (div_fast_ok(es)) {
-        const float re = __frcp_rn(es);
+        const uint64_t nb2 = dup2(-es), r2 = dup2(__frcp_rn(es));
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          float q0, q1;
+          div2_rn(q0, q1, bf16_lo(w[i]), bf16_hi(w[i]), nb2, r2);
+          c[i] = enc_e2m1x2(q0, q1);
+        }
+      } else {
 #pragma unroll
         for (int i = 0; i < 8; ++i)
-          out[i >> 2] |= enc_e2m1x2(div_by(x[2 * i], es, re), div_by(x[2 * i + 1], es, re))
-                         << (8 * (i & 3));
-      } else if (es > 0.f) {
-#pragma unroll
-        for (int i = 0; i < 8; ++i)
-          out[i >> 2] |= enc_e2m1x2(__fdiv_rn(x[2 * i], es), __fdiv_rn(x[2 * i + 1], es))
-                         << (8 * (i & 3));
+          c[i] = es > 0.f ? enc_e2m1x2(__fdiv_rn(bf16_lo(w[i]), es), __fdiv_rn(bf16_hi(w[i]), es))
+                          : 0u;
       }
+      // code bytes 0-3 and 4-7 into two words (byte i = pair i)
+      uint32_t out[2];
+#pragma unroll
+      for (int h = 0; h < 2; ++h)
+        out[h] = __byte_perm(__byte_perm(c[4 * h], c[4 * h + 1], 0x0040),
+                             __byte_perm(c[4 * h + 2], c[4 * h + 3], 0x0040), 0x5410);
       *reinterpret_cast<uint2*>(codes + r * (D / 2) + 8 * b) = make_uint2(out[0], out[1]);
       bscales[r * LPR + b] = (uint8_t)sb;
       if (b == 0) rscales[r] = g;

@@ -17,10 +17,13 @@
 // attention buffer.
 #include <cuda_fp16.h>
 
+#include "codec_math.cuh"
 #include "wa_internal.cuh"
 
 namespace wa {
 namespace {
+
+using namespace codec;
 
 constexpr int kThreads = 256;
 
@@ -36,37 +39,10 @@ __device__ __forceinline__ float2 dec2(uint16_t c) {
   return __half22float2(h);   // .x = lower byte's value, .y = upper byte's
 }
 
-// RN(x / b) from r = RN(1 / b) (b > 0, normal, 1 / b finite): q0 = RN(x r), the
-// residual e = x - b q0 is exact in one FMA, and q = RN(q0 + e r) is the
-// correctly rounded quotient (Markstein's correction: P. Markstein, "Computation
-// of elementary functions on the IBM RISC System/6000 processor", IBM J. Res.
-// Dev. 34 (1990)).  A zero quotient takes the sign of x, as the division's does.
-__device__ __forceinline__ float div_by(float x, float b, float r) {
-  const float q0 = __fmul_rn(x, r);
-  const float e = __fmaf_rn(-b, q0, x);
-  const float q = __fmaf_rn(e, r, q0);
-  return q == 0.f ? copysignf(0.f, x) : q;
-}
-// a divisor whose reciprocal is a finite normal number takes the fast path
-__device__ __forceinline__ bool div_fast_ok(float b) { return b >= 1e-37f && b <= 1e37f; }
-
-// (d0, d1) = (a0 * b0, a1 * b1), one packed instruction, each RN
-__device__ __forceinline__ void fmul2(float& d0, float& d1, float a0, float a1, float b0, float b1) {
-  asm("{\n\t.reg .b64 ra, rb, rd;\n\tmov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
-      "mul.rn.f32x2 rd, ra, rb;\n\tmov.b64 {%0, %1}, rd;\n\t}"
-      : "=f"(d0), "=f"(d1)
-      : "f"(a0), "f"(a1), "f"(b0), "f"(b1));
-}
-// two fp32 -> one bf16x2 word (RNE): lo in bits 0-15, hi in bits 16-31
-__device__ __forceinline__ uint32_t bf16x2(float lo, float hi) {
-  uint32_t r;
-  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
-  return r;
-}
-
 // Each lane owns a 16-value chunk of a row (LPR = d / 16 lanes per row, 32 / LPR
 // rows per warp step): a 32-byte load, the row maximum over the row's lanes,
-// 16 codes (one 16-byte store).  kSteps row groups are in flight per warp.
+// 16 codes (one 16-byte store), the quotients two at a time in packed fp32.
+// kSteps row groups are in flight per warp.
 constexpr int kSteps = 2;
 constexpr int kDecSteps = 4;   // decoding: more row groups in flight (reads are small)
 
@@ -78,6 +54,7 @@ k_fp8_encode(const __nv_bfloat16* __restrict__ src, size_t n_rows, uint8_t* __re
   constexpr int D = 16 * LPR;
   const int lane = threadIdx.x & 31, sub = lane / LPR, b = lane % LPR;
   const size_t warps = (size_t)gridDim.x * (kThreads / 32);
+  const float r448 = __frcp_rn(448.0f);
   for (size_t g0 = ((size_t)blockIdx.x * (kThreads / 32) + (threadIdx.x >> 5)) * RPW * kSteps;
        g0 < n_rows; g0 += warps * RPW * kSteps) {
     uint4 in[kSteps][2];
@@ -95,30 +72,28 @@ k_fp8_encode(const __nv_bfloat16* __restrict__ src, size_t n_rows, uint8_t* __re
     for (int k = 0; k < kSteps; ++k) {
       const size_t r = g0 + (size_t)k * RPW + sub;
       const bool live = r < n_rows;             // uniform within a row's lanes
-      float x[16];
-      const uint32_t* w = reinterpret_cast<const uint32_t*>(in[k]);
-#pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        x[2 * i] = __uint_as_float(w[i] << 16);
-        x[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
-      }
-      float amax = 0.f;
-#pragma unroll
-      for (int i = 0; i < 16; ++i) amax = fmaxf(amax, fabsf(x[i]));
+      const uint32_t w[8] = {in[k][0].x, in[k][0].y, in[k][0].z, in[k][0].w,
+                             in[k][1].x, in[k][1].y, in[k][1].z, in[k][1].w};
+      float amax = absmax16_bf16(w);
 #pragma unroll
       for (int o = LPR / 2; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
       if (!live) continue;
-      const float s = __fdiv_rn(amax, 448.0f);
+      const float s = dividend_ok(amax) ? div_rn(amax, 448.0f, r448) : __fdiv_rn(amax, 448.0f);
       uint32_t out[4];
       uint16_t* o16 = reinterpret_cast<uint16_t*>(out);
       if (div_fast_ok(s)) {
-        const float rs = __frcp_rn(s);
+        const uint64_t nb2 = dup2(-s), r2 = dup2(__frcp_rn(s));
 #pragma unroll
-        for (int i = 0; i < 8; ++i) o16[i] = enc2(div_by(x[2 * i], s, rs), div_by(x[2 * i + 1], s, rs));
+        for (int i = 0; i < 8; ++i) {
+          float q0, q1;
+          div2_rn(q0, q1, bf16_lo(w[i]), bf16_hi(w[i]), nb2, r2);
+          o16[i] = enc2(q0, q1);
+        }
       } else {
 #pragma unroll
         for (int i = 0; i < 8; ++i)
-          o16[i] = s > 0.f ? enc2(__fdiv_rn(x[2 * i], s), __fdiv_rn(x[2 * i + 1], s)) : (uint16_t)0;
+          o16[i] = s > 0.f ? enc2(__fdiv_rn(bf16_lo(w[i]), s), __fdiv_rn(bf16_hi(w[i]), s))
+                           : (uint16_t)0;
       }
       *reinterpret_cast<uint4*>(codes + r * D + 16 * b) = make_uint4(out[0], out[1], out[2], out[3]);
       if (b == 0) scales[r] = s;

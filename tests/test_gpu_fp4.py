@@ -28,6 +28,11 @@ def _rows(n, H, d, seed):
     x[2, 0, 16:32] = 0.0                                # a zero block
     x[3, 0] = x[3, 0] * 1e-3                            # tiny values next to a large one
     x[3, 0, 0] = 100.0
+    # row maxima of 1e-38 (bf16 subnormals: the division fallbacks), 1e-32 (a
+    # tiny row maximum with a normal scale) and 3e38 (near the top of the bf16
+    # range; finite, as the codec's inputs must be)
+    for i, top in ((4, 1e-38), (5, 1e-32), (6, 3e38)):
+        x[i, 0] = x[i, 0] / x[i, 0].abs().max() * top
     return x.to(torch.bfloat16)
 
 
