@@ -187,13 +187,14 @@ k_nvfp4_decode(const uint8_t* __restrict__ codes, const uint8_t* __restrict__ bs
   }
 }
 
-unsigned grid_for(size_t rows, int head_dim, int steps = kSteps) {
-  int dev = 0, sms = 148;
-  cudaGetDevice(&dev);
-  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+// Blocks for n_rows rows: one per row group, at most `cap`.  The encoder takes
+// the resident block count (as the FP8 encoder, where it measured faster); the
+// decoder, whose traffic is mostly writes, 8 blocks per SM, more than fit at
+// once, so that blocks that start late fill the SMs that finish early (0.079
+// against 0.084 ms with the resident count, 8 pages).
+inline unsigned grid_for(size_t rows, int head_dim, int steps, size_t cap) {
   const size_t per_block = (size_t)(kThreads / 32) * (512 / head_dim) * steps;
   const size_t need = (rows + per_block - 1) / per_block;
-  const size_t cap = (size_t)sms * 8;
   return (unsigned)(need < cap ? need : cap);
 }
 
@@ -201,17 +202,22 @@ unsigned grid_for(size_t rows, int head_dim, int steps = kSteps) {
 
 wa_status launch_nvfp4_encode(const void* src, size_t n_rows, int head_dim, void* codes,
                               void* bscales, float* rscales, cudaStream_t s) {
-  const unsigned g = grid_for(n_rows, head_dim);
   const auto* x = static_cast<const __nv_bfloat16*>(src);
   auto* c = static_cast<uint8_t*>(codes);
   auto* b = static_cast<uint8_t*>(bscales);
+  auto run = [&](auto kernel) {
+    if (n_rows == 0) return WA_OK;
+    kernel<<<grid_for(n_rows, head_dim, kSteps, resident_blocks(kernel, kThreads)), kThreads, 0,
+             s>>>(x, n_rows, c, b,
+                                                                           rscales);
+    return cuda_status(cudaPeekAtLastError());
+  };
   switch (head_dim / 16) {
-    case 4: k_nvfp4_encode<4><<<g, kThreads, 0, s>>>(x, n_rows, c, b, rscales); break;
-    case 8: k_nvfp4_encode<8><<<g, kThreads, 0, s>>>(x, n_rows, c, b, rscales); break;
-    case 16: k_nvfp4_encode<16><<<g, kThreads, 0, s>>>(x, n_rows, c, b, rscales); break;
+    case 4: return run(k_nvfp4_encode<4>);
+    case 8: return run(k_nvfp4_encode<8>);
+    case 16: return run(k_nvfp4_encode<16>);
     default: return WA_ERR_SHAPE;
   }
-  return cuda_status(cudaPeekAtLastError());
 }
 
 wa_status launch_nvfp4_decode(const void* codes, const void* bscales, const float* rscales,
@@ -220,17 +226,21 @@ wa_status launch_nvfp4_decode(const void* codes, const void* bscales, const floa
   Ctrl* ctrl = nullptr;
   wa_status rc = get_ctrl(&ctrl);
   if (rc != WA_OK) return rc;
-  const unsigned g = grid_for(n_rows, head_dim, kDecSteps);
   const auto* c = static_cast<const uint8_t*>(codes);
   const auto* b = static_cast<const uint8_t*>(bscales);
   auto* o = static_cast<__nv_bfloat16*>(out);
+  auto run = [&](auto kernel) {
+    if (n_rows == 0) return WA_OK;
+    kernel<<<grid_for(n_rows, head_dim, kDecSteps, (size_t)sm_count() * 8), kThreads, 0, s>>>(
+        c, b, rscales, idx, n_pages, page_rows, n_rows, o, ctrl);
+    return cuda_status(cudaPeekAtLastError());
+  };
   switch (head_dim / 16) {
-    case 4: k_nvfp4_decode<4><<<g, kThreads, 0, s>>>(c, b, rscales, idx, n_pages, page_rows, n_rows, o, ctrl); break;
-    case 8: k_nvfp4_decode<8><<<g, kThreads, 0, s>>>(c, b, rscales, idx, n_pages, page_rows, n_rows, o, ctrl); break;
-    case 16: k_nvfp4_decode<16><<<g, kThreads, 0, s>>>(c, b, rscales, idx, n_pages, page_rows, n_rows, o, ctrl); break;
+    case 4: return run(k_nvfp4_decode<4>);
+    case 8: return run(k_nvfp4_decode<8>);
+    case 16: return run(k_nvfp4_decode<16>);
     default: return WA_ERR_SHAPE;
   }
-  return cuda_status(cudaPeekAtLastError());
 }
 
 }  // namespace wa

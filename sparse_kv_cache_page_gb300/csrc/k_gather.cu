@@ -126,11 +126,11 @@ wa_status launch_gather_device(const void* k_pages, const void* v_pages, size_t 
   const size_t page_vecs = page_bytes / 16;
   const size_t spans = (page_bytes + kSpan - 1) / kSpan;
   const size_t total = spans * (size_t)k_p * (v_pages ? 2 : 1);
-  int dev = 0, sms = 148;
-  cudaGetDevice(&dev);
-  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  size_t grid = (size_t)sms * 8;   // 8 resident CTAs per SM, grid-stride over spans
+  // 8 CTAs per SM, more than fit at once (late starters fill the SMs that
+  // finish early: measured faster than the resident count), grid-stride over spans
+  size_t grid = (size_t)sm_count() * 8;
   if (grid > total) grid = total;
+  if (grid == 0) return WA_OK;
   k_gather_pages<<<(unsigned)grid, kThreads, 0, s>>>(
       (const uint4*)k_pages, (const uint4*)v_pages, page_vecs, n_pages, idx_dev, k_p,
       (uint4*)k_buf, (uint4*)v_buf, spans, ctrl);

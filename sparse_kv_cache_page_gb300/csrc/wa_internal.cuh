@@ -40,6 +40,24 @@ inline wa_status cuda_status(cudaError_t e) { return e == cudaSuccess ? WA_OK : 
 
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+inline int sm_count() {
+  int dev = 0, sms = 1;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  return sms;
+}
+
+// Blocks of `kernel` that are resident on the whole GPU at once (SM count x
+// blocks per SM at this block size).
+template <typename Kernel>
+size_t resident_blocks(Kernel kernel, int threads, size_t dyn_smem = 0) {
+  int per_sm = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, threads, dyn_smem) !=
+          cudaSuccess || per_sm < 1)
+    per_sm = 1;
+  return (size_t)sm_count() * (size_t)per_sm;
+}
+
 // 2-D bf16 TMA descriptor over a row-major [rows][cols] matrix with a row
 // stride of `row_stride` elements; box = box_rows x box_cols (box_cols * 2
 // bytes <= 128), 128-byte swizzle, out-of-range rows and columns read as 0.

@@ -89,6 +89,30 @@ def test_per_head_select_small(seed):
     assert len({tuple(r) for r in ref_idx.tolist()}) > 1     # heads chose different sets
 
 
+@pytest.mark.parametrize("n_pages,k_p", [(32, 1), (32, 5), (32, 31), (32, 32), (33, 5), (64, 16)])
+def test_per_head_select_no_prompt(n_pages, k_p):
+    """No prompt stage: every page is a candidate.  Up to 32 candidates are
+    scored and sorted by one warp per head (the boundary case 32 included, with
+    k_p up to all of them); 33 and more take the block-wide path.  Indices
+    bit-exact and scores against the oracle on both paths."""
+    c = synth.make_chunk_case("phnp1", n_heads=5, head_dim=64, page_tokens=32, n_pages=n_pages,
+                              pages_per_chunk=1, n_chunks=0, prompt_dim=0, k_p=k_p, n_q=64,
+                              n_loc=1, dtype=torch.bfloat16)
+    kbar = torch.empty((n_pages, c.n_heads, 64), dtype=torch.float32, device=DEV)
+    wa.wa_page_summarize(c.k_pages.to(DEV), kbar)
+    idx = torch.full((c.n_heads, k_p), -7, dtype=torch.int32, device=DEV)
+    sc = torch.empty((c.n_heads, k_p), dtype=torch.float32, device=DEV)
+    ch = torch.full((1,), -9, dtype=torch.int32, device=DEV)
+    wa.wa_select_pages_per_head(c.q.to(DEV), kbar, None, None, 1, k_p, idx, sc, ch)
+    wa.wa_check()
+    kb64 = O.page_summarize(np_of(c.k_pages))
+    ref_idx, ref_sc, ref_ch = O.select_pages_per_head(np_of(c.q), kb64, None, None, 1, k_p)
+    _check_margins(np_of(c.q), np_of(c.k_pages), kb64, ref_ch, 1, k_p)
+    assert int(ch.item()) == ref_ch == -1
+    assert idx.cpu().numpy().tolist() == ref_idx.tolist()
+    assert np.abs(sc.cpu().numpy() - ref_sc).max() < 1e-5
+
+
 def test_per_head_gather_and_attention():
     c = _case(3)
     idx = torch.tensor(O.select_pages_per_head(np_of(c.q), O.page_summarize(np_of(c.k_pages)),
