@@ -38,6 +38,7 @@
 //   query pair) combines them (no spin-wait: a ticket counter).
 //   Epilogue: O / l (fp32 or rounded to bf16; optionally fused with an
 //   existing output: o = w_old[h] * o + w_new[h] * O) and LSE = scale*m + ln l.
+#include <atomic>
 #include <math.h>
 #include <stdlib.h>
 #include <string.h>
@@ -610,14 +611,14 @@ wa_status launch_t(const CUtensorMap& tq, const CUtensorMap& tkm, const CUtensor
                    const CUtensorMap& tkl, const CUtensorMap& tvl, const Params& p, int n_heads,
                    cudaStream_t s) {
   const int smem = SmemLayout::total + 1024;
-  static bool attr_done[64] = {};
+  static std::atomic<bool> attr_done[64];   // per device; setting it twice is harmless
   int dev = 0;
   cudaGetDevice(&dev);
   auto kern = k_block_attn_tc<OutT, kLse, kSparse>;
-  if (dev < 64 && !attr_done[dev]) {
+  if (dev < 64 && !attr_done[dev].load(std::memory_order_relaxed)) {
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
       return WA_ERR_CUDA;
-    attr_done[dev] = true;
+    attr_done[dev].store(true, std::memory_order_relaxed);
   }
   dim3 grid(p.n_qpairs * p.n_split, n_heads);
   kern<<<grid, kThreads, smem, s>>>(tq, tkm, tvm, tkl, tvl, p);

@@ -18,6 +18,7 @@
 // K', V' to bf16, token-major [r][H][128], the layout the attention reads.
 // K8: the tensor-core attention kernel over the r projected keys, with its
 // fused epilogue o = w_attn o + w_lin O_lin.
+#include <atomic>
 #include <math.h>
 #include <string.h>
 
@@ -234,14 +235,14 @@ template <int RB>
 wa_status proj_t(const CUtensorMap* maps, const LinParams& p, int grid_y, cudaStream_t s) {
   using C = LinCfg<RB>;
   const int smem = C::total + 1024;
-  static bool attr_done[64] = {};
+  static std::atomic<bool> attr_done[64];   // per device; setting it twice is harmless
   int dev = 0;
   cudaGetDevice(&dev);
-  if (dev < 64 && !attr_done[dev]) {
+  if (dev < 64 && !attr_done[dev].load(std::memory_order_relaxed)) {
     if (cudaFuncSetAttribute(k_linformer_proj<RB>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              smem) != cudaSuccess)
       return WA_ERR_CUDA;
-    attr_done[dev] = true;
+    attr_done[dev].store(true, std::memory_order_relaxed);
   }
   dim3 grid(p.n_split, grid_y);
   k_linformer_proj<RB><<<grid, kThreads, smem, s>>>(maps[0], maps[1], maps[2], maps[3], maps[4],

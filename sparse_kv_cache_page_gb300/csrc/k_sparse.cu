@@ -18,6 +18,7 @@
 //      reaching tau ends the kept set (at least one block);
 //   6. the kept blocks written in ascending block order (scan of flags).
 // Every reduction and scan has a fixed order, so the result is deterministic.
+#include <atomic>
 #include <math.h>
 
 #include "wa_internal.cuh"
@@ -236,7 +237,7 @@ wa_status launch_sparse_select(const float* qbar, int n_qb, const float* kbar, i
   if (rc != WA_OK) return rc;
   float* scores = static_cast<float*>(sc.data);
   const size_t smem1 = (size_t)64 * (head_dim + 4) * sizeof(float);
-  static bool attr_done[64] = {};
+  static std::atomic<bool> attr_done[64];   // per device; setting it twice is harmless
   int dev = 0;
   cudaGetDevice(&dev);
   int n2 = 1;
@@ -246,7 +247,7 @@ wa_status launch_sparse_select(const float* qbar, int n_qb, const float* kbar, i
   // the slab offset of every head keeps 16-byte alignment when n_qb * n_kb % 4 == 0)
   const size_t slab = (size_t)n_qb * n_kb * sizeof(float) + 16;
   const bool stage = smem2 + slab <= 220 * 1024 && ((size_t)n_qb * n_kb) % 4 == 0;
-  if (dev < 64 && !attr_done[dev]) {
+  if (dev < 64 && !attr_done[dev].load(std::memory_order_relaxed)) {
     if (cudaFuncSetAttribute(k_pooled_scores, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              227 * 1024) != cudaSuccess ||
         cudaFuncSetAttribute(k_sparse_select<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -254,7 +255,7 @@ wa_status launch_sparse_select(const float* qbar, int n_qb, const float* kbar, i
         cudaFuncSetAttribute(k_sparse_select<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              227 * 1024) != cudaSuccess)
       return WA_ERR_CUDA;
-    attr_done[dev] = true;
+    attr_done[dev].store(true, std::memory_order_relaxed);
   }
   dim3 g1((n_kb + 31) / 32, (n_qb + 31) / 32, n_heads);
   k_pooled_scores<<<g1, kScoreThreads, smem1, s>>>(qbar, n_qb, kbar, n_kb, n_heads, head_dim, scale,
