@@ -163,6 +163,14 @@ def _need(cond: bool, what: str):
         raise ValueError(what)
 
 
+def _buf(t, dtype, numel: int, what: str):
+    """A buffer the library reads or writes through a plain pointer: present,
+    contiguous, of `dtype` and exactly `numel` elements (the C ABI cannot see
+    sizes, so a short buffer would be overrun)."""
+    _need(t is not None and t.is_contiguous() and t.dtype == dtype and t.numel() == numel,
+          f"{what} must be contiguous {dtype} with {numel} elements")
+
+
 def wa_version() -> str:
     return load().wa_version().decode()
 
@@ -206,7 +214,13 @@ def wa_gather_pages(k_pages: torch.Tensor, v_pages, idx_dev, idx_host, k_buf: to
     _need(k_pages.dim() == 4 and k_pages.is_contiguous(), "k_pages must be contiguous [n][P][H][d]")
     n, p, h, d = k_pages.shape
     k_p = (idx_dev if idx_dev is not None else idx_host).numel()
-    _need(k_buf.numel() == k_p * p * h * d and k_buf.dtype == k_pages.dtype, "k_buf size/dtype")
+    _buf(k_buf, k_pages.dtype, k_p * p * h * d, "k_buf")
+    _need((v_pages is None) == (v_buf is None), "v_pages and v_buf go together")
+    if v_pages is not None:
+        _buf(v_pages, k_pages.dtype, k_pages.numel(), "v_pages")
+        _buf(v_buf, k_pages.dtype, k_p * p * h * d, "v_buf")
+    idx = idx_dev if idx_dev is not None else idx_host
+    _need(idx.dtype == torch.int32 and idx.is_contiguous(), "page indices must be contiguous int32")
     _ok("wa_gather_pages", load().wa_gather_pages(
         _ptr(k_pages), _ptr(v_pages), _dt(k_pages), n, p, h, d, _ptr(idx_dev), _ptr(idx_host),
         k_p, _ptr(k_buf), _ptr(v_buf), _stream(stream)))
@@ -243,7 +257,12 @@ def wa_gather_pages_per_head(k_pages: torch.Tensor, v_pages, idx_dev: torch.Tens
     _need(idx_dev.dim() == 2 and idx_dev.shape[0] == h and idx_dev.dtype == torch.int32,
           "idx_dev must be int32 [H][k_p]")
     k_p = idx_dev.shape[1]
-    _need(k_buf.numel() == k_p * p * h * d and k_buf.dtype == k_pages.dtype, "k_buf size/dtype")
+    _need(idx_dev.is_contiguous(), "idx_dev must be contiguous")
+    _buf(k_buf, k_pages.dtype, k_p * p * h * d, "k_buf")
+    _need((v_pages is None) == (v_buf is None), "v_pages and v_buf go together")
+    if v_pages is not None:
+        _buf(v_pages, k_pages.dtype, k_pages.numel(), "v_pages")
+        _buf(v_buf, k_pages.dtype, k_p * p * h * d, "v_buf")
     _ok("wa_gather_pages_per_head", load().wa_gather_pages_per_head(
         _ptr(k_pages), _ptr(v_pages), _dt(k_pages), n, p, h, d, _ptr(idx_dev), k_p, _ptr(k_buf),
         _ptr(v_buf), _stream(stream)))
@@ -321,16 +340,22 @@ def wa_sparse_attn(q: torch.Tensor, k_main, v_main, k_loc, v_loc, sel: torch.Ten
 def wa_fp8_encode(x: torch.Tensor, codes_out: torch.Tensor, scales_out: torch.Tensor, stream=None):
     """FP8 E4M3 codes and per-(token, head) scales of a bf16 [n][H][d] tensor;
     codes uint8 [n][H][d] and scales float32 [n][H] on the device or pinned."""
+    _need(x.dim() == 3, "x must be [n][H][d]")
     n, h, d = x.shape
-    _need(codes_out.dtype == torch.uint8 and codes_out.numel() == n * h * d
-          and scales_out.dtype == torch.float32 and scales_out.numel() == n * h,
-          "codes uint8 [n][H][d], scales float32 [n][H]")
+    _buf(x, torch.bfloat16, n * h * d, "x")
+    _buf(codes_out, torch.uint8, n * h * d, "codes_out")
+    _buf(scales_out, torch.float32, n * h, "scales_out")
     _ok("wa_fp8_encode", load().wa_fp8_encode(_ptr(x), n, h, d, _ptr(codes_out), _ptr(scales_out),
                                               _stream(stream)))
 
 
 def wa_fp8_decode(codes: torch.Tensor, scales: torch.Tensor, out: torch.Tensor, stream=None):
+    """out bf16 [n][H][d] = decode(codes uint8 [n][H][d], scales float32 [n][H])."""
+    _need(out.dim() == 3, "out must be [n][H][d]")
     n, h, d = out.shape
+    _buf(out, torch.bfloat16, n * h * d, "out")
+    _buf(codes, torch.uint8, n * h * d, "codes")
+    _buf(scales, torch.float32, n * h, "scales")
     _ok("wa_fp8_decode", load().wa_fp8_decode(_ptr(codes), _ptr(scales), n, h, d, _ptr(out),
                                               _stream(stream)))
 
@@ -339,7 +364,12 @@ def wa_gather_pages_fp8(code_pages: torch.Tensor, scale_pages: torch.Tensor, idx
                         buf_out: torch.Tensor, stream=None):
     """buf_out[s*P + t] = decode(code_pages[idx[s]][t]) (bf16); pages on the
     device or in pinned host memory."""
+    _need(code_pages.dim() == 4, "code_pages must be [n][P][H][d]")
     n, p, h, d = code_pages.shape
+    _buf(code_pages, torch.uint8, n * p * h * d, "code_pages")
+    _buf(scale_pages, torch.float32, n * p * h, "scale_pages")
+    _need(idx_dev.dtype == torch.int32 and idx_dev.is_contiguous(), "idx_dev must be contiguous int32")
+    _buf(buf_out, torch.bfloat16, idx_dev.numel() * p * h * d, "buf_out")
     _ok("wa_gather_pages_fp8", load().wa_gather_pages_fp8(
         _ptr(code_pages), _ptr(scale_pages), n, p, h, d, _ptr(idx_dev), idx_dev.numel(),
         _ptr(buf_out), _stream(stream)))
@@ -349,11 +379,12 @@ def wa_nvfp4_encode(x: torch.Tensor, codes_out: torch.Tensor, bscales_out: torch
                     rscales_out: torch.Tensor, stream=None):
     """NVFP4 form of a bf16 [n][H][d] tensor: E2M1 codes uint8 [n][H][d/2], E4M3
     block scales uint8 [n][H][d/16], fp32 row scales [n][H]; on the device or pinned."""
+    _need(x.dim() == 3 and x.shape[2] % 16 == 0, "x must be [n][H][d], d a multiple of 16")
     n, h, d = x.shape
-    _need(codes_out.dtype == torch.uint8 and codes_out.numel() == n * h * d // 2
-          and bscales_out.dtype == torch.uint8 and bscales_out.numel() == n * h * d // 16
-          and rscales_out.dtype == torch.float32 and rscales_out.numel() == n * h,
-          "codes uint8 [n][H][d/2], block scales uint8 [n][H][d/16], row scales float32 [n][H]")
+    _buf(x, torch.bfloat16, n * h * d, "x")
+    _buf(codes_out, torch.uint8, n * h * d // 2, "codes_out")
+    _buf(bscales_out, torch.uint8, n * h * d // 16, "bscales_out")
+    _buf(rscales_out, torch.float32, n * h, "rscales_out")
     _ok("wa_nvfp4_encode", load().wa_nvfp4_encode(_ptr(x), n, h, d, _ptr(codes_out),
                                                   _ptr(bscales_out), _ptr(rscales_out),
                                                   _stream(stream)))
@@ -361,7 +392,13 @@ def wa_nvfp4_encode(x: torch.Tensor, codes_out: torch.Tensor, bscales_out: torch
 
 def wa_nvfp4_decode(codes: torch.Tensor, bscales: torch.Tensor, rscales: torch.Tensor,
                     out: torch.Tensor, stream=None):
+    """out bf16 [n][H][d] = decode of the NVFP4 form (codes, block scales, row scales)."""
+    _need(out.dim() == 3 and out.shape[2] % 16 == 0, "out must be [n][H][d], d a multiple of 16")
     n, h, d = out.shape
+    _buf(out, torch.bfloat16, n * h * d, "out")
+    _buf(codes, torch.uint8, n * h * d // 2, "codes")
+    _buf(bscales, torch.uint8, n * h * d // 16, "bscales")
+    _buf(rscales, torch.float32, n * h, "rscales")
     _ok("wa_nvfp4_decode", load().wa_nvfp4_decode(_ptr(codes), _ptr(bscales), _ptr(rscales), n, h,
                                                   d, _ptr(out), _stream(stream)))
 
@@ -372,7 +409,15 @@ def wa_gather_pages_nvfp4(code_pages: torch.Tensor, bscale_pages: torch.Tensor,
     """buf_out[s*P + t] = decode of page idx[s], token t (bf16); code pages
     [n][P][H][d/2], block scales [n][P][H][d/16], row scales [n][P][H], on the
     device or in pinned host memory."""
+    _need(code_pages.dim() == 4, "code_pages must be [n][P][H][d/2]")
     n, p, h, half = code_pages.shape
+    d = 2 * half
+    _need(d % 16 == 0, "d must be a multiple of 16")
+    _buf(code_pages, torch.uint8, n * p * h * half, "code_pages")
+    _buf(bscale_pages, torch.uint8, n * p * h * (d // 16), "bscale_pages")
+    _buf(rscale_pages, torch.float32, n * p * h, "rscale_pages")
+    _need(idx_dev.dtype == torch.int32 and idx_dev.is_contiguous(), "idx_dev must be contiguous int32")
+    _buf(buf_out, torch.bfloat16, idx_dev.numel() * p * h * d, "buf_out")
     _ok("wa_gather_pages_nvfp4", load().wa_gather_pages_nvfp4(
         _ptr(code_pages), _ptr(bscale_pages), _ptr(rscale_pages), n, p, h, 2 * half,
         _ptr(idx_dev), idx_dev.numel(), _ptr(buf_out), _stream(stream)))
