@@ -272,6 +272,17 @@ def _rows(t):
     return 0 if t is None else t.shape[0]
 
 
+def _kv_pair(k, v, h: int, d: int, dtype, what: str):
+    """Keys and values of one segment: both absent, or both contiguous
+    [rows][H][d] of `dtype` with the same row count."""
+    _need((k is None) == (v is None), f"{what}: keys and values go together")
+    if k is not None:
+        _need(k.dim() == 3 and k.shape[1:] == (h, d) and v.shape == k.shape,
+              f"{what}: keys and values must be [rows][H][d] with the same rows")
+        _buf(k, dtype, k.numel(), f"{what} keys")
+        _buf(v, dtype, v.numel(), f"{what} values")
+
+
 def wa_block_attn(q: torch.Tensor, k_main, v_main, k_loc, v_loc, o: torch.Tensor, lse=None,
                   scale: float = 0.0, stream=None):
     """o = softmax(q [k_main; k_loc]^T * scale) [v_main; v_loc]; lse [H][n_q] optional.
@@ -279,6 +290,11 @@ def wa_block_attn(q: torch.Tensor, k_main, v_main, k_loc, v_loc, o: torch.Tensor
     _need(q.dim() == 3 and q.is_contiguous() and o.shape == q.shape and o.is_contiguous(),
           "q and o must be contiguous [n_q][H][d]")
     n_q, h, d = q.shape
+    _need(o.dtype in (torch.float32, q.dtype), "o must be float32 or the input dtype")
+    _kv_pair(k_main, v_main, h, d, q.dtype, "main segment")
+    _kv_pair(k_loc, v_loc, h, d, q.dtype, "local segment")
+    if lse is not None:
+        _buf(lse, torch.float32, h * n_q, "lse")
     _ok("wa_block_attn", load().wa_block_attn(
         _ptr(q), n_q, _ptr(k_main), _ptr(v_main), _rows(k_main), _ptr(k_loc), _ptr(v_loc),
         _rows(k_loc), _dt(q), h, d, float(scale), _ptr(o), _dt(o), _ptr(lse), _stream(stream)))
@@ -288,8 +304,20 @@ def wa_linear_branch(q: torch.Tensor, k_main, v_main, k_loc, v_loc, e_k: torch.T
                      e_v: torch.Tensor, o: torch.Tensor, w_attn=None, w_lin=None,
                      accumulate: bool = True, scale: float = 0.0, stream=None):
     """Linformer branch; o = w_attn*o + w_lin*O_lin (accumulate) or o = O_lin."""
+    _need(q.dim() == 3 and q.is_contiguous() and o.shape == q.shape and o.is_contiguous(),
+          "q and o must be contiguous [n_q][H][d]")
     n_q, h, d = q.shape
+    _need(o.dtype in (torch.float32, q.dtype), "o must be float32 or the input dtype")
+    _kv_pair(k_main, v_main, h, d, q.dtype, "main segment")
+    _kv_pair(k_loc, v_loc, h, d, q.dtype, "local segment")
+    _need(e_k.dim() == 3 and e_k.shape[:2] == (h, _rows(k_main) + _rows(k_loc))
+          and e_v.shape == e_k.shape, "e_k, e_v must be [H][n_main + n_loc][rank]")
     rank = e_k.shape[-1]
+    _buf(e_k, q.dtype, e_k.numel(), "e_k")
+    _buf(e_v, q.dtype, e_v.numel(), "e_v")
+    for w, name in ((w_attn, "w_attn"), (w_lin, "w_lin")):
+        if w is not None:
+            _buf(w, torch.float32, h, name)
     _ok("wa_linear_branch", load().wa_linear_branch(
         _ptr(q), n_q, _ptr(k_main), _ptr(v_main), _rows(k_main), _ptr(k_loc), _ptr(v_loc),
         _rows(k_loc), _ptr(e_k), _ptr(e_v), rank, _dt(q), h, d, float(scale), _ptr(w_attn),

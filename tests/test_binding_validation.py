@@ -61,3 +61,23 @@ def test_nvfp4_codec_buffers():
     _raises(wa.wa_gather_pages_nvfp4, *pages, idx, _z(15, 2, 64))
     _raises(wa.wa_gather_pages_nvfp4, pages[0], pages[1][:, :, :, :3].contiguous(), pages[2], idx,
             _z(16, 2, 64))
+
+
+def test_attention_buffers():
+    q, kv = _z(8, 2, 64), _z(16, 2, 64)
+    o = _z(8, 2, 64, dtype=F32)
+    _raises(wa.wa_block_attn, q, kv, None, None, None, o)                          # v missing
+    _raises(wa.wa_block_attn, q, kv, _z(15, 2, 64), None, None, o)                 # rows differ
+    _raises(wa.wa_block_attn, q, kv, kv, _z(4, 3, 64), _z(4, 3, 64), o)            # heads differ
+    _raises(wa.wa_block_attn, q, kv.float(), kv.float(), None, None, o)            # dtype
+    _raises(wa.wa_block_attn, q, kv, kv, None, None, _z(8, 2, 64, dtype=torch.float16))
+    _raises(wa.wa_block_attn, q, kv, kv, None, None, o, _z(2, 7, dtype=F32))       # short lse
+
+
+def test_linear_branch_buffers():
+    q, kv, o = _z(8, 2, 128), _z(16, 2, 128), _z(8, 2, 128, dtype=F32)
+    e = _z(2, 16, 128)
+    _raises(wa.wa_linear_branch, q, kv, kv, None, None, _z(2, 15, 128), _z(2, 15, 128), o)
+    _raises(wa.wa_linear_branch, q, kv, kv, None, None, e, _z(2, 16, 256), o)
+    _raises(wa.wa_linear_branch, q, kv, kv, None, None, e, e, o, _z(3, dtype=F32))
+    _raises(wa.wa_linear_branch, q, kv, kv, None, None, e.float(), e.float(), o)
