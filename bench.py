@@ -430,9 +430,7 @@ def run_hsa(args, world, rank, local):
         mark(2)
         wa.wa_gather_pages(kp, vp, idx, None, kbuf, vbuf)
         mark(3)
-        wa.wa_block_means(q, 64, qbar)
-        wa.wa_block_means(kbuf, 128, kbb[:nmb])
-        wa.wa_block_means(kl, 64, kbb[nmb:])
+        wa.wa_block_means_segments([(q, 64, qbar), (kbuf, 128, kbb[:nmb]), (kl, 64, kbb[nmb:])])
         mark(4)
         wa.wa_sparse_select(qbar, kbb, sel, cnt, gini_out=gini)
         mark(5)
@@ -488,7 +486,10 @@ def run_hsa(args, world, rank, local):
                      "unit": "TFLOP/s", "frac": round(sp_tflops / tf_sus, 4), "traffic": None,
                      "kernel": "k_block_attn_tc (block-sparse form)",
                      "peak_source": f"{src} bf16 sustained"},
-        "gpu_launches": 12 * args.steps, "clocks": clk.summary(),
+        # per step: summaries, select, gather, block means (one launch), pooled scores,
+        # block select, sparse tiles, block-sparse attention, projection, reduce,
+        # low-rank attention
+        "gpu_launches": 11 * args.steps, "clocks": clk.summary(),
     }
 
 

@@ -277,6 +277,25 @@ wa_status wa_block_means(const void* x, wa_dtype dt, int n_rows, int block, int 
                          int head_dim, float* means_out, wa_stream_t stream);
 
 /*
+ * Block means of up to three row sets in one launch (the HSA step pools the
+ * queries, the retrieved buffer and the local KV at once; a launch per set
+ * leaves most SMs idle on the two small ones):
+ *
+ *   means_out[i][b][h][:] = mean of xs[i][r][h][:] over rows r in
+ *                           [b*blocks[i], min((b+1)*blocks[i], n_rows[i]))
+ *
+ * n_seg      : 1..3.
+ * xs, n_rows, blocks, means_out : host arrays of n_seg entries; xs[i] and
+ *              means_out[i] are device pointers laid out as in wa_block_means.
+ * Every set's means equal those of wa_block_means on that set alone, bit for
+ * bit (a set's row ranges and reduction order do not depend on the others).
+ * Errors: as wa_block_means, per set; WA_ERR_INVALID_ARG for n_seg outside 1..3.
+ */
+wa_status wa_block_means_segments(int n_seg, const void* const* xs, const int* n_rows,
+                                  const int* blocks, wa_dtype dt, int n_heads, int head_dim,
+                                  float* const* means_out, wa_stream_t stream);
+
+/*
  * Block selection of the HSA sparse branch ([WA] HSA: pooled attention map,
  * head-adaptive cumulative-mass selection; the Gini-to-threshold formula is
  * missing on the page and read as tau_h = 1 - G_h):

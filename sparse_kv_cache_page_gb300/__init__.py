@@ -35,6 +35,7 @@ __all__ = [
     "wa_nvfp4_encode",
     "wa_nvfp4_decode",
     "wa_gather_pages_nvfp4",
+    "wa_block_means_segments",
     "wa_check",
     "wa_shutdown",
     "wa_version",
@@ -49,7 +50,8 @@ WA_F32, WA_BF16 = 0, 1
 # Every symbol include/wa.h declares.
 EXPORTED_SYMBOLS = ("wa_strerror", "wa_version", "wa_page_summarize", "wa_select_pages",
                     "wa_select_pages_noalloc", "wa_gather_pages", "wa_block_attn",
-                    "wa_linear_branch", "wa_block_means", "wa_sparse_select", "wa_sparse_attn",
+                    "wa_linear_branch", "wa_block_means", "wa_block_means_segments",
+                    "wa_sparse_select", "wa_sparse_attn",
                     "wa_select_pages_per_head", "wa_gather_pages_per_head", "wa_cache_create",
                     "wa_cache_destroy", "wa_cache_reset", "wa_cache_append_chunk",
                     "wa_cache_retrieve",
@@ -105,6 +107,7 @@ def load():
         "wa_block_attn": (I, [P, I, P, P, I, P, P, I, I, I, I, F, P, I, P, P]),
         "wa_linear_branch": (I, [P, I, P, P, I, P, P, I, P, P, I, I, I, I, F, P, P, I, P, I, P]),
         "wa_block_means": (I, [P, I, I, I, I, I, P, P]),
+        "wa_block_means_segments": (I, [I, P, P, P, I, I, I, P, P]),
         "wa_sparse_select": (I, [P, I, P, I, I, I, F, P, P, P, P, P, P]),
         "wa_sparse_attn": (I, [P, I, P, P, I, P, P, I, I, I, P, P, I, I, I, F, P, I, P, P]),
         "wa_cache_create": (I, [ctypes.POINTER(_CacheConfig), ctypes.POINTER(P)]),
@@ -333,6 +336,29 @@ def wa_block_means(x: torch.Tensor, block: int, means_out: torch.Tensor, stream=
           and means_out.is_contiguous(), "means_out must be float32 [ceil(n/block)][H][d]")
     _ok("wa_block_means", load().wa_block_means(_ptr(x), _dt(x), n, int(block), h, d,
                                                 _ptr(means_out), _stream(stream)))
+
+
+def wa_block_means_segments(segments, stream=None):
+    """Block means of up to three row sets in one launch: segments is a list of
+    (x [n][H][d], block, means_out float32 [ceil(n/block)][H][d]); every set's
+    means equal wa_block_means on that set alone, bit for bit."""
+    _need(1 <= len(segments) <= 3, "one to three segments")
+    x0 = segments[0][0]
+    _need(x0.dim() == 3, "x must be [n][H][d]")
+    h, d = x0.shape[1:]
+    for x, block, out in segments:
+        _need(x.dim() == 3 and x.shape[1:] == (h, d) and x.dtype == x0.dtype and x.is_contiguous(),
+              "every x must be contiguous [n][H][d] with the same H, d and dtype")
+        _need(int(block) > 0, "block must be positive")
+        nb = (x.shape[0] + int(block) - 1) // int(block)
+        _buf(out, torch.float32, nb * h * d, "means_out")
+    n = len(segments)
+    xs = (ctypes.c_void_p * n)(*[x.data_ptr() for x, _, _ in segments])
+    rows = (ctypes.c_int * n)(*[x.shape[0] for x, _, _ in segments])
+    blocks = (ctypes.c_int * n)(*[int(b) for _, b, _ in segments])
+    outs = (ctypes.c_void_p * n)(*[o.data_ptr() for _, _, o in segments])
+    _ok("wa_block_means_segments", load().wa_block_means_segments(
+        n, xs, rows, blocks, _dt(x0), h, d, outs, _stream(stream)))
 
 
 def wa_sparse_select(qbar: torch.Tensor, kbar: torch.Tensor, sel_out: torch.Tensor,

@@ -159,34 +159,57 @@ __device__ void sum_rows4(const float* rows, int n, int row_elems, float* out, f
 // ---------------------------------------------------------------------------
 // page summaries
 // ---------------------------------------------------------------------------
+// One launch sums up to kMaxSegs independent row sets ("segments"), each cut
+// into pages of page_tokens rows and each page into `splits` row ranges; CTAs
+// [cta0, cta0 + n_pages * splits) belong to a segment.  A segment's arithmetic
+// (its ranges and the fixed-order reduction of their partials) does not depend
+// on the other segments in the launch.
+constexpr int kMaxSegs = 3;
+template <typename T>
+struct SumSeg {
+  const T* pages;
+  float* kbar;         // [n_pages][row_elems] means
+  float* partial;      // [n_pages][splits][row_elems] scratch (splits > 1)
+  int page_tokens, n_rows, splits, rows_per_split, cta0, counter0;
+};
+template <typename T>
+struct SumSegs {
+  SumSeg<T> s[kMaxSegs];
+  int n;
+};
+
 // Four resident CTAs per SM (at most 40 registers): five, which the compiler picks
 // otherwise, stream about 8% slower.
 template <typename T, int VPT>
 __global__ void __launch_bounds__(kThreads, 4)
-k_page_summarize(const T* __restrict__ pages, int page_tokens, int n_rows, int row_elems, int nvec,
-                 int R, int splits, int rows_per_split, float* __restrict__ partial,
-                 float* __restrict__ kbar, Ctrl* ctrl) {
+k_page_summarize(const SumSegs<T> segs, int row_elems, int nvec, int R, Ctrl* ctrl) {
   extern __shared__ float red[];
-  const int j = blockIdx.x / splits, s = blockIdx.x % splits;
+  // this CTA's segment (static indices: the table stays in parameter space)
+  SumSeg<T> g = segs.s[0];
+  if (segs.n > 1 && (int)blockIdx.x >= segs.s[1].cta0) g = segs.s[1];
+  if (segs.n > 2 && (int)blockIdx.x >= segs.s[2].cta0) g = segs.s[2];
+  const int local = (int)blockIdx.x - g.cta0;
+  const int j = local / g.splits, s = local % g.splits;
   // page j holds rows [j P, j P + rows_j) of the n_rows; only the last may be short
-  const int rows_j = min(page_tokens, n_rows - j * page_tokens);
-  const int r0 = s * rows_per_split;
-  const int r1 = min(rows_j, r0 + rows_per_split);
-  const T* base = pages + (size_t)j * page_tokens * row_elems;
+  const int rows_j = min(g.page_tokens, g.n_rows - j * g.page_tokens);
+  const int r0 = s * g.rows_per_split;
+  const int r1 = min(rows_j, r0 + g.rows_per_split);
+  const T* base = g.pages + (size_t)j * g.page_tokens * row_elems;
   colsum_rows<T, VPT>(base, row_elems, nvec, R, r0, r1, red);
   const float inv = 1.0f / (float)rows_j;
-  if (splits == 1) {
+  if (g.splits == 1) {
     for (int c = threadIdx.x; c < row_elems; c += blockDim.x)
-      kbar[(size_t)j * row_elems + c] = red[c] * inv;
+      g.kbar[(size_t)j * row_elems + c] = red[c] * inv;
     return;
   }
-  float* mine = partial + ((size_t)j * splits + s) * row_elems;
+  float* mine = g.partial + ((size_t)j * g.splits + s) * row_elems;
   for (int c = threadIdx.x; c < row_elems; c += blockDim.x) mine[c] = red[c];
-  if (!last_ticket(&ctrl->counters[j], (unsigned)splits)) return;
+  unsigned* counter = &ctrl->counters[g.counter0 + j];
+  if (!last_ticket(counter, (unsigned)g.splits)) return;
   // the page's partial sums in split order, then the mean
-  sum_rows4(partial + (size_t)j * splits * row_elems, splits, row_elems,
-            kbar + (size_t)j * row_elems, inv);
-  if (threadIdx.x == 0) ctrl->counters[j] = 0u;
+  sum_rows4(g.partial + (size_t)j * g.splits * row_elems, g.splits, row_elems,
+            g.kbar + (size_t)j * row_elems, inv);
+  if (threadIdx.x == 0) *counter = 0u;
 }
 
 // ---------------------------------------------------------------------------
@@ -460,35 +483,67 @@ Plan plan_rows(int row_elems) {
   return p;
 }
 
+// One segment of a summarize launch: rows x [n_rows][row_elems], means of
+// consecutive groups of `block` rows (the last may be short) into out.
+struct SegIn {
+  const void* x;
+  int n_rows, block;
+  float* out;
+};
+
 template <typename T>
-wa_status summarize_t(const T* pages, int n_pages, int page_tokens, int n_rows, int row_elems,
-                      float* kbar, cudaStream_t st) {
+wa_status summarize_t(const SegIn* in, int n_seg, int row_elems, cudaStream_t st) {
+  if (n_seg < 1 || n_seg > kMaxSegs) return WA_ERR_INVALID_ARG;
   Plan p = plan_rows<T>(row_elems);
-  // About two waves of CTAs: a single wave of long row ranges ends with the
-  // slowest range, and more, shorter ranges add partial sums (measured on the
-  // one-layer WorldAttention bank: 0.251 ms with one wave of 256-thread CTAs,
-  // 0.227 ms with two waves of 384-thread CTAs, 0.267 ms with four).
-  int splits = 2 * kTargetCtas / n_pages;
-  if (splits < 1) splits = 1;
-  const int max_splits = (page_tokens + 15) / 16;   // at least 16 rows per CTA
-  if (splits > max_splits) splits = max_splits;
-  if (splits > 256) splits = 256;
-  const int rps = (page_tokens + splits - 1) / splits;
-  splits = (page_tokens + rps - 1) / rps;
+  SumSegs<T> segs{};
+  segs.n = n_seg;
+  size_t part_off[kMaxSegs], part_floats = 0;
+  int ctas = 0, counters = 0;
+  for (int i = 0; i < n_seg; ++i) {
+    if (in[i].n_rows <= 0 || in[i].block <= 0) return WA_ERR_INVALID_ARG;
+    const int page_tokens = in[i].block;
+    const int n_pages = (in[i].n_rows + page_tokens - 1) / page_tokens;
+    // About two waves of CTAs per segment: a single wave of long row ranges
+    // ends with the slowest range, and more, shorter ranges add partial sums
+    // (measured on the one-layer WorldAttention bank: 0.251 ms with one wave of
+    // 256-thread CTAs, 0.227 ms with two waves of 384-thread CTAs, 0.267 ms
+    // with four).
+    int splits = 2 * kTargetCtas / n_pages;
+    if (splits < 1) splits = 1;
+    const int max_splits = (page_tokens + 15) / 16;   // at least 16 rows per CTA
+    if (splits > max_splits) splits = max_splits;
+    if (splits > 256) splits = 256;
+    const int rps = (page_tokens + splits - 1) / splits;
+    splits = (page_tokens + rps - 1) / rps;
+    SumSeg<T>& g = segs.s[i];
+    g.pages = static_cast<const T*>(in[i].x);
+    g.kbar = in[i].out;
+    g.page_tokens = page_tokens;
+    g.n_rows = in[i].n_rows;
+    g.splits = splits;
+    g.rows_per_split = rps;
+    g.cta0 = ctas;
+    g.counter0 = counters;
+    ctas += splits * n_pages;
+    if (splits > 1) counters += n_pages;
+    part_off[i] = part_floats;
+    part_floats += (size_t)n_pages * splits * row_elems;
+  }
+  if (counters > (int)kSelectCounter) return WA_ERR_SHAPE;   // the select kernel's ticket
   Scratch sc;
-  wa_status rc = get_scratch((size_t)n_pages * splits * row_elems * sizeof(float), &sc);
+  wa_status rc = get_scratch(part_floats * sizeof(float), &sc);
   if (rc != WA_OK) return rc;
+  for (int i = 0; i < n_seg; ++i) segs.s[i].partial = static_cast<float*>(sc.data) + part_off[i];
   const size_t smem = (size_t)p.R * row_elems * sizeof(float);
-  dim3 grid((unsigned)(splits * n_pages));
+  dim3 grid((unsigned)ctas);
   switch (p.vpt) {
 #define WA_CASE(V)                                                                          \
   case V:                                                                                   \
     if (smem > 48 * 1024)                                                                   \
       cudaFuncSetAttribute(k_page_summarize<T, V>, cudaFuncAttributeMaxDynamicSharedMemorySize, \
                            (int)smem);                                                      \
-    k_page_summarize<T, V><<<grid, p.threads, smem, st>>>(pages, page_tokens, n_rows, row_elems, \
-                                                          p.nvec, p.R, splits, rps,         \
-                                                          (float*)sc.data, kbar, sc.ctrl);  \
+    k_page_summarize<T, V><<<grid, p.threads, smem, st>>>(segs, row_elems, p.nvec, p.R,     \
+                                                          sc.ctrl);                         \
     break;
     WA_CASE(1) WA_CASE(2) WA_CASE(4) WA_CASE(8)
 #undef WA_CASE
@@ -542,19 +597,19 @@ wa_status select_t(const T* q, SelectArgs a, cudaStream_t st) {
 
 wa_status launch_page_summarize(const void* k_pages, wa_dtype dt, int n_pages, int page_tokens,
                                 int row_elems, float* kbar_out, cudaStream_t s) {
-  const int n_rows = n_pages * page_tokens;
-  if (dt == WA_BF16)
-    return summarize_t((const __nv_bfloat16*)k_pages, n_pages, page_tokens, n_rows, row_elems,
-                       kbar_out, s);
-  return summarize_t((const float*)k_pages, n_pages, page_tokens, n_rows, row_elems, kbar_out, s);
+  const SegIn seg{k_pages, n_pages * page_tokens, page_tokens, kbar_out};
+  if (dt == WA_BF16) return summarize_t<__nv_bfloat16>(&seg, 1, row_elems, s);
+  return summarize_t<float>(&seg, 1, row_elems, s);
 }
 
-wa_status launch_block_means(const void* x, wa_dtype dt, int n_rows, int block, int row_elems,
-                             float* means_out, cudaStream_t s) {
-  const int n_blocks = (n_rows + block - 1) / block;
-  if (dt == WA_BF16)
-    return summarize_t((const __nv_bfloat16*)x, n_blocks, block, n_rows, row_elems, means_out, s);
-  return summarize_t((const float*)x, n_blocks, block, n_rows, row_elems, means_out, s);
+wa_status launch_block_means(int n_seg, const void* const* xs, const int* n_rows,
+                             const int* blocks, wa_dtype dt, int row_elems,
+                             float* const* means_out, cudaStream_t s) {
+  if (n_seg < 1 || n_seg > kMaxSegs) return WA_ERR_INVALID_ARG;
+  SegIn segs[kMaxSegs];
+  for (int i = 0; i < n_seg; ++i) segs[i] = SegIn{xs[i], n_rows[i], blocks[i], means_out[i]};
+  if (dt == WA_BF16) return summarize_t<__nv_bfloat16>(segs, n_seg, row_elems, s);
+  return summarize_t<float>(segs, n_seg, row_elems, s);
 }
 
 wa_status launch_select_pages(const void* q, wa_dtype dt, int n_q, int n_heads, int head_dim,

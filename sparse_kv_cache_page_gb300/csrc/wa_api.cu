@@ -399,16 +399,26 @@ wa_status wa_gather_pages_nvfp4(const uint8_t* code_pages, const uint8_t* bscale
                              buf_out, (cudaStream_t)stream);
 }
 
-wa_status wa_block_means(const void* x, wa_dtype dt, int n_rows, int block, int n_heads,
-                         int head_dim, float* means_out, wa_stream_t stream) {
+wa_status wa_block_means_segments(int n_seg, const void* const* xs, const int* n_rows,
+                                  const int* blocks, wa_dtype dt, int n_heads, int head_dim,
+                                  float* const* means_out, wa_stream_t stream) {
   if (!dtype_ok(dt)) return WA_ERR_DTYPE;
-  if (!x || !means_out || n_rows <= 0 || block <= 0) return WA_ERR_INVALID_ARG;
+  if (n_seg < 1 || n_seg > 3 || !xs || !n_rows || !blocks || !means_out) return WA_ERR_INVALID_ARG;
   if (!row_ok(n_heads, head_dim, dt)) return WA_ERR_SHAPE;
   if ((long long)n_heads * head_dim > 8192) return WA_ERR_SHAPE;
-  if ((n_rows + (long long)block - 1) / block > 4000) return WA_ERR_SHAPE;
-  if (!aligned16(x) || !aligned16(means_out)) return WA_ERR_ALIGN;
-  return launch_block_means(x, dt, n_rows, block, n_heads * head_dim, means_out,
+  for (int i = 0; i < n_seg; ++i) {
+    if (!xs[i] || !means_out[i] || n_rows[i] <= 0 || blocks[i] <= 0) return WA_ERR_INVALID_ARG;
+    if ((n_rows[i] + (long long)blocks[i] - 1) / blocks[i] > 4000) return WA_ERR_SHAPE;
+    if (!aligned16(xs[i]) || !aligned16(means_out[i])) return WA_ERR_ALIGN;
+  }
+  return launch_block_means(n_seg, xs, n_rows, blocks, dt, n_heads * head_dim, means_out,
                             (cudaStream_t)stream);
+}
+
+wa_status wa_block_means(const void* x, wa_dtype dt, int n_rows, int block, int n_heads,
+                         int head_dim, float* means_out, wa_stream_t stream) {
+  return wa_block_means_segments(1, &x, &n_rows, &block, dt, n_heads, head_dim, &means_out,
+                                 stream);
 }
 
 wa_status wa_sparse_select(const float* qbar, int n_qb, const float* kbar, int n_kb, int n_heads,

@@ -131,9 +131,11 @@ wa_status launch_nvfp4_decode(const void* codes, const void* bscales, const floa
                               const int32_t* idx, int n_pages, size_t page_rows, size_t n_rows,
                               int head_dim, void* out, cudaStream_t s);
 
-// Block means of x [n_rows][row_elems] in blocks of `block` rows (ragged last block).
-wa_status launch_block_means(const void* x, wa_dtype dt, int n_rows, int block, int row_elems,
-                             float* means_out, cudaStream_t s);
+// Block means of n_seg (1..3) row sets xs[i] [n_rows[i]][row_elems] in blocks of
+// blocks[i] rows (ragged last block) into means_out[i], in one launch.
+wa_status launch_block_means(int n_seg, const void* const* xs, const int* n_rows,
+                             const int* blocks, wa_dtype dt, int row_elems,
+                             float* const* means_out, cudaStream_t s);
 
 // HSA block selection (k_sparse.cu) and the limits its host checks use.
 wa_status launch_sparse_select(const float* qbar, int n_qb, const float* kbar, int n_kb,

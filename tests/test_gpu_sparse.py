@@ -44,9 +44,8 @@ def _gpu_select(q, km, kl, tau=None):
     nlb = (kl.shape[0] + B_LOC - 1) // B_LOC
     qbar = torch.empty((nqb, H, 128), dtype=torch.float32, device=DEV)
     kbar = torch.empty((nmb + nlb, H, 128), dtype=torch.float32, device=DEV)
-    wa.wa_block_means(q.to(DEV), B_Q, qbar)
-    wa.wa_block_means(km.to(DEV), B_MAIN, kbar[:nmb])
-    wa.wa_block_means(kl.to(DEV), B_LOC, kbar[nmb:])
+    wa.wa_block_means_segments([(q.to(DEV), B_Q, qbar), (km.to(DEV), B_MAIN, kbar[:nmb]),
+                                (kl.to(DEV), B_LOC, kbar[nmb:])])
     sel = torch.full((H, nmb + nlb), -1, dtype=torch.int32, device=DEV)
     cnt = torch.empty(H, dtype=torch.int32, device=DEV)
     g = torch.empty(H, dtype=torch.float32, device=DEV)
@@ -84,6 +83,31 @@ def test_block_means(n, block):
     wa.wa_check()
     ref = O.block_means(np_of(x), block)
     np.testing.assert_allclose(f64(out), ref, rtol=0, atol=2e-6)
+
+
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
+def test_block_means_segments_one_launch(dtype):
+    """Queries, buffer and local KV pooled in one launch: each set's means are
+    those of its own wa_block_means call, bit for bit (ragged last blocks, a
+    set large enough to split its blocks and one that is not), and match the
+    oracle."""
+    sets = [(synth.normal((300, 3, 128), synth.seed_of("bmseg", i), dtype=dtype), blk)
+            for i, blk in enumerate((64,))]
+    sets += [(synth.normal((4999, 3, 128), synth.seed_of("bmseg", 1), dtype=dtype), 128),
+             (synth.normal((77, 3, 128), synth.seed_of("bmseg", 2), dtype=dtype), 64)]
+    fused, alone = [], []
+    for x, blk in sets:
+        nb = (x.shape[0] + blk - 1) // blk
+        fused.append(torch.full((nb, 3, 128), float("nan"), device=DEV))
+        alone.append(torch.empty((nb, 3, 128), device=DEV))
+    xs = [x.to(DEV) for x, _ in sets]
+    wa.wa_block_means_segments([(x, blk, o) for x, (_, blk), o in zip(xs, sets, fused)])
+    for x, (_, blk), o in zip(xs, sets, alone):
+        wa.wa_block_means(x, blk, o)
+    wa.wa_check()
+    for (x, blk), f, a in zip(sets, fused, alone):
+        assert torch.equal(f, a)
+        np.testing.assert_allclose(f64(f), O.block_means(np_of(x), blk), rtol=0, atol=2e-6)
 
 
 def test_select_matches_oracle_small():
