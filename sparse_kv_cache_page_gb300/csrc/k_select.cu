@@ -20,7 +20,7 @@ namespace wa {
 namespace {
 
 constexpr int kThreads = 384;           // 2 x 192 16-byte vectors of a 1,536-element bf16 row
-constexpr int kTargetCtas = 152 * 5;     // sizing unit for the row-range splits
+constexpr int kTargetCtas = 152 * 4;     // resident summarize CTAs: 152 SMs x 4
 constexpr unsigned kSelectCounter = 4095;
 
 template <typename T> struct VecOf;
@@ -506,8 +506,10 @@ wa_status summarize_t(const SegIn* in, int n_seg, int row_elems, cudaStream_t st
     // About two waves of CTAs per segment: a single wave of long row ranges
     // ends with the slowest range, and more, shorter ranges add partial sums
     // (measured on the one-layer WorldAttention bank: 0.251 ms with one wave of
-    // 256-thread CTAs, 0.227 ms with two waves of 384-thread CTAs, 0.267 ms
-    // with four).
+    // 256-thread CTAs; with 384-thread CTAs, four resident per SM, 0.2247 ms
+    // for two whole waves, 0.2278 for two and a half, 0.2280 for three, 0.2315
+    // for four; on another GB300 one whole wave measured 0.2242 against 0.2268
+    // for two, within the spread between boxes).
     int splits = 2 * kTargetCtas / n_pages;
     if (splits < 1) splits = 1;
     const int max_splits = (page_tokens + 15) / 16;   // at least 16 rows per CTA
