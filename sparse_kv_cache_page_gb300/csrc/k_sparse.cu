@@ -101,6 +101,43 @@ __device__ void bitonic_sort(unsigned long long* keys, int n2) {
   }
 }
 
+// The same ascending sort for n2 <= blockDim.x keys, one per thread: stages
+// whose partner is under 32 positions away exchange by warp shuffles, wider
+// ones through shared memory (10 of the 45 stages for 512 keys need a barrier,
+// against every stage above).  The keys are distinct, so the result is the
+// same permutation.
+__device__ void bitonic_sort_small(unsigned long long* keys, int n2) {
+  const int i = threadIdx.x;
+  const bool live = i < n2;
+  unsigned long long v = live ? keys[i] : ~0ull;
+  for (int k = 2; k <= n2; k <<= 1) {
+    for (int j = k >> 1; j > 0; j >>= 1) {
+      unsigned long long w;
+      if (j >= 32) {
+        __syncthreads();   // the previous exchange has been read
+        if (live) keys[i] = v;
+        __syncthreads();
+        w = live ? keys[i ^ j] : ~0ull;
+      } else {
+        w = __shfl_xor_sync(0xffffffffu, v, j);
+      }
+      // in an ascending run the lower position keeps the smaller key
+      const bool keep_min = ((i & j) == 0) == ((i & k) == 0);
+      v = keep_min ? (v < w ? v : w) : (v < w ? w : v);
+    }
+  }
+  __syncthreads();
+  if (live) keys[i] = v;
+  __syncthreads();
+}
+
+__device__ void sort_keys(unsigned long long* keys, int n2) {
+  if (n2 <= (int)blockDim.x)
+    bitonic_sort_small(keys, n2);
+  else
+    bitonic_sort(keys, n2);
+}
+
 // Inclusive scan of x[0..n2) in place (Hillis-Steele, fixed order); tmp has n2 floats.
 __device__ void scan_inclusive(float* x, float* tmp, int n2) {
   for (int off = 1; off < n2; off <<= 1) {
@@ -178,7 +215,7 @@ k_sparse_select(const float* __restrict__ scores, int n_qb, int n_kb, const floa
   }
   __syncthreads();
   // 3. Gini coefficient: G = sum_i (2i - n - 1) x_(i) / (n sum x), x ascending, i from 1
-  bitonic_sort(keys, n2);
+  sort_keys(keys, n2);
   float num = 0.f, tot = 0.f;
   for (int i = tid; i < n_kb; i += blockDim.x) {
     const float x = mass[(unsigned)(keys[i] & 0xffffffffu)];
@@ -196,7 +233,7 @@ k_sparse_select(const float* __restrict__ scores, int n_qb, int n_kb, const floa
     keys[kb] = kb < n_kb ? ((unsigned long long)(~__float_as_uint(mass[kb])) << 32) | (unsigned)kb
                          : ~0ull;
   __syncthreads();
-  bitonic_sort(keys, n2);
+  sort_keys(keys, n2);
   for (int i = tid; i < n2; i += blockDim.x)
     cum[i] = i < n_kb ? mass[(unsigned)(keys[i] & 0xffffffffu)] : 0.f;
   __syncthreads();
