@@ -109,21 +109,22 @@ __device__ void bitonic_sort(unsigned long long* keys, int n2) {
 __device__ void bitonic_sort_small(unsigned long long* keys, int n2) {
   const int i = threadIdx.x;
   const bool live = i < n2;
+  const bool warp_live = (i & ~31) < n2;   // warp-uniform: warps wholly past n2 only meet barriers
   unsigned long long v = live ? keys[i] : ~0ull;
   for (int k = 2; k <= n2; k <<= 1) {
     for (int j = k >> 1; j > 0; j >>= 1) {
-      unsigned long long w;
       if (j >= 32) {
         __syncthreads();   // the previous exchange has been read
         if (live) keys[i] = v;
         __syncthreads();
-        w = live ? keys[i ^ j] : ~0ull;
-      } else {
-        w = __shfl_xor_sync(0xffffffffu, v, j);
       }
-      // in an ascending run the lower position keeps the smaller key
-      const bool keep_min = ((i & j) == 0) == ((i & k) == 0);
-      v = keep_min ? (v < w ? v : w) : (v < w ? w : v);
+      if (warp_live) {
+        const unsigned long long w =
+            j >= 32 ? (live ? keys[i ^ j] : ~0ull) : __shfl_xor_sync(0xffffffffu, v, j);
+        // in an ascending run the lower position keeps the smaller key
+        const bool keep_min = ((i & j) == 0) == ((i & k) == 0);
+        v = keep_min ? (v < w ? v : w) : (v < w ? w : v);
+      }
     }
   }
   __syncthreads();
