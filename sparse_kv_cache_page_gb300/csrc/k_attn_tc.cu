@@ -181,6 +181,51 @@ __device__ __forceinline__ void softmax_bar() {   // the 256 softmax threads onl
   asm volatile("bar.sync 1, 256;" ::: "memory");
 }
 
+// AND of v over the 256 softmax threads (their barrier, with a reduction).
+__device__ __forceinline__ bool softmax_all(bool v) {
+  int r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\tsetp.ne.s32 p, %1, 0;\n\tbar.red.and.pred q, 1, 256, p;\n\t"
+      "selp.s32 %0, 1, 0, q;\n\t}"
+      : "=r"(r)
+      : "r"((int)v)
+      : "memory");
+  return r != 0;
+}
+
+// Four consecutive output values of one row, optionally fused with the values
+// already there (o = w_old * o + x), with the arithmetic of store_row32.
+__device__ __forceinline__ void store4(float* dst, float4 x, bool acc, float wo) {
+  float4* d = reinterpret_cast<float4*>(dst);
+  if (acc) {
+    const float4 old = *d;
+    x.x += wo * old.x;
+    x.y += wo * old.y;
+    x.z += wo * old.z;
+    x.w += wo * old.w;
+  }
+  *d = x;
+}
+__device__ __forceinline__ void store4(__nv_bfloat16* dst, float4 x, bool acc, float wo) {
+  uint2* d = reinterpret_cast<uint2*>(dst);
+  float y[4] = {x.x, x.y, x.z, x.w};
+  if (acc) {
+    const uint2 old = *d;
+    y[0] += wo * __uint_as_float(old.x << 16);
+    y[1] += wo * __uint_as_float(old.x & 0xffff0000u);
+    y[2] += wo * __uint_as_float(old.y << 16);
+    y[3] += wo * __uint_as_float(old.y & 0xffff0000u);
+  }
+  *d = make_uint2(pack_bf16x2(y[0], y[1]), pack_bf16x2(y[2], y[3]));
+}
+
+// Split partials are staged row-major in shared memory with this row pitch
+// (floats): 528-byte rows put the 32 rows a warp writes at once on distinct
+// bank groups.
+constexpr int kStagePitch = HD + 4;
+constexpr int kCombineRegs = 4;   // splits whose weights and partials a combine holds in registers
+static_assert(256 * kStagePitch * 4 <= SmemLayout::bars, "staging overlays Q and the ring only");
+
 template <typename OutT, bool kLse, bool kSparse>
 __global__ void __launch_bounds__(kThreads, 1)
 k_block_attn_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_km,
@@ -454,12 +499,20 @@ k_block_attn_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
           p.lse[(size_t)head * p.n_q + grow] = nloc > 0 ? m * p.scale + logf(lx) : -INFINITY;
       }
     } else {
-      // split: store this CTA's unnormalised rows, then the last CTA of the
-      // (head, query pair) combines all splits
+      // split: the CTA's unnormalised rows go to scratch through shared memory
+      // (each thread stages its TMEM row, then a warp stores one 512-byte row
+      // per instruction), and the CTA that finishes last for its (head, query
+      // pair) combines the splits with the same row-per-warp access, its own
+      // rows read back from the staging area.  Q and the K/V ring are idle
+      // once the loop is done (every copy landed and every MMA completed), so
+      // the staging area overlays them.
       const int unit = head * p.n_qpairs + qpair;
       const int prow = qt * BM + row;                     // 0..255
-      if (ok) {
-        float* dst = p.part_o + (((size_t)unit * p.n_split + split) * 256 + prow) * HD;
+      const int sw = threadIdx.x >> 5;                    // softmax warp 0..7: rows 32 sw ..
+      float* stage = reinterpret_cast<float*>(smem);      // [256][kStagePitch]
+      const bool all_ok = softmax_all(ok);
+      if (all_ok) {
+        float* mine = stage + (size_t)prow * kStagePitch;
 #pragma unroll 1
         for (int c = 0; c < 4; ++c) {
           uint32_t orow[32];
@@ -470,14 +523,21 @@ k_block_attn_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
 #pragma unroll
             for (int e = 0; e < 32; ++e) orow[e] = 0u;
           }
-          float4* d4 = reinterpret_cast<float4*>(dst + 32 * c);
+          float4* d4 = reinterpret_cast<float4*>(mine + 32 * c);
 #pragma unroll
           for (int v = 0; v < 8; ++v)
-            __stcg(d4 + v, make_float4(__uint_as_float(orow[4 * v]), __uint_as_float(orow[4 * v + 1]),
-                                       __uint_as_float(orow[4 * v + 2]),
-                                       __uint_as_float(orow[4 * v + 3])));
+            d4[v] = make_float4(__uint_as_float(orow[4 * v]), __uint_as_float(orow[4 * v + 1]),
+                                __uint_as_float(orow[4 * v + 2]), __uint_as_float(orow[4 * v + 3]));
         }
         __stcg(p.part_ml + ((size_t)unit * p.n_split + split) * 256 + prow, make_float4(m, l, lx, 0.f));
+        softmax_bar();
+        float* dst = p.part_o + ((size_t)unit * p.n_split + split) * 256 * HD;
+#pragma unroll 4
+        for (int rr = 0; rr < 32; ++rr) {
+          const int r = 32 * sw + rr;
+          __stcg(reinterpret_cast<float4*>(dst + (size_t)r * HD) + lane,
+                 reinterpret_cast<const float4*>(stage + (size_t)r * kStagePitch)[lane]);
+        }
       }
       __threadfence();
       softmax_bar();
@@ -488,41 +548,83 @@ k_block_attn_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
       if (last) {
         __threadfence();
         if (threadIdx.x == 0) p.counters[unit] = 0u;
-        if (ok && store) {
-          const float4* ml = p.part_ml + (size_t)unit * p.n_split * 256 + prow;
+        if (all_ok) {
+          // each lane first weighs the splits of one row (row 32 sw + lane), the
+          // arithmetic of a per-row combine; then the warp combines its 32 rows
+          // four at a time, their partials all loaded before any is summed
+          const int rj = 32 * sw + lane;
+          const float4* mlj = p.part_ml + (size_t)unit * p.n_split * 256 + rj;
           float mm = -INFINITY;
-          for (int s = 0; s < p.n_split; ++s) mm = fmaxf(mm, __ldcg(ml + (size_t)s * 256).x);
+          for (int s = 0; s < p.n_split; ++s) mm = fmaxf(mm, __ldcg(mlj + (size_t)s * 256).x);
           const bool none = !(mm > -INFINITY);   // no keys in any split: O = 0, LSE = -inf
           float den = 0.f, denx = 0.f;
           for (int s = 0; s < p.n_split; ++s) {
-            const float4 t = __ldcg(ml + (size_t)s * 256);
+            const float4 t = __ldcg(mlj + (size_t)s * 256);
             const float w = none ? 0.f : ex2((t.x - mm) * sl2);
             den += w * t.y;
             denx += w * t.z;
           }
           const float wn = none ? 0.f : wn0 / den;
-          const float* src = p.part_o + ((size_t)unit * p.n_split * 256 + prow) * HD;
-#pragma unroll 1
-          for (int c = 0; c < 4; ++c) {
-            float x[32];
+          float wj[kCombineRegs];
 #pragma unroll
-            for (int e = 0; e < 32; ++e) x[e] = 0.f;
-            for (int s = 0; s < p.n_split; ++s) {
-              const float w = none ? 0.f : ex2((__ldcg(ml + (size_t)s * 256).x - mm) * sl2) * wn;
-              const float4* s4 = reinterpret_cast<const float4*>(src + (size_t)s * 256 * HD + 32 * c);
+          for (int s = 0; s < kCombineRegs; ++s)
+            wj[s] = (s < p.n_split && !none) ? ex2((__ldcg(mlj + (size_t)s * 256).x - mm) * sl2) * wn
+                                              : 0.f;
+          if (kLse && p.lse && q0 + rj < p.n_q)
+            p.lse[(size_t)head * p.n_q + q0 + rj] = none ? -INFINITY : mm * p.scale + logf(denx);
+          const float* part = p.part_o + (size_t)unit * p.n_split * 256 * HD;
+          for (int r0 = 0; r0 < 32; r0 += 4) {
+            if (q0 + 32 * sw + r0 >= p.n_q) break;        // rows ascend (warp-uniform)
+            float4 t[4][kCombineRegs];
 #pragma unroll
-              for (int v = 0; v < 8; ++v) {
-                const float4 t = __ldcg(s4 + v);
-                x[4 * v] += w * t.x;
-                x[4 * v + 1] += w * t.y;
-                x[4 * v + 2] += w * t.z;
-                x[4 * v + 3] += w * t.w;
-              }
+            for (int u = 0; u < 4; ++u) {
+              const int r = 32 * sw + r0 + u;
+#pragma unroll
+              for (int s = 0; s < kCombineRegs; ++s)
+                if (s < p.n_split)
+                  t[u][s] = s == split
+                                ? reinterpret_cast<const float4*>(stage + (size_t)r * kStagePitch)[lane]
+                                : __ldcg(reinterpret_cast<const float4*>(
+                                             part + ((size_t)s * 256 + r) * HD) + lane);
             }
-            store_row32(orow_g + 32 * c, x, p.accumulate != 0, wo);
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+              const int r = 32 * sw + r0 + u;
+              const int grow_r = q0 + r;
+              if (grow_r >= p.n_q) break;
+              float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+              for (int s = 0; s < kCombineRegs; ++s) {
+                if (s < p.n_split) {
+                  const float w = __shfl_sync(0xffffffffu, wj[s], r0 + u);
+                  x.x += w * t[u][s].x;
+                  x.y += w * t[u][s].y;
+                  x.z += w * t[u][s].z;
+                  x.w += w * t[u][s].w;
+                }
+              }
+              // more splits than registers (a forced split count): weights from the row's lane
+              const float mm_r = __shfl_sync(0xffffffffu, mm, r0 + u);
+              const float wn_r = __shfl_sync(0xffffffffu, wn, r0 + u);
+              const float4* ml_r = p.part_ml + (size_t)unit * p.n_split * 256 + r;
+              for (int s = kCombineRegs; s < p.n_split; ++s) {
+                const float w = !(mm_r > -INFINITY)
+                                    ? 0.f
+                                    : ex2((__ldcg(ml_r + (size_t)s * 256).x - mm_r) * sl2) * wn_r;
+                const float4 ts = s == split
+                                      ? reinterpret_cast<const float4*>(
+                                            stage + (size_t)r * kStagePitch)[lane]
+                                      : __ldcg(reinterpret_cast<const float4*>(
+                                                   part + ((size_t)s * 256 + r) * HD) + lane);
+                x.x += w * ts.x;
+                x.y += w * ts.y;
+                x.z += w * ts.z;
+                x.w += w * ts.w;
+              }
+              store4(static_cast<OutT*>(p.o) + ((size_t)grow_r * p.n_heads + head) * HD + 4 * lane,
+                     x, p.accumulate != 0, wo);
+            }
           }
-          if (kLse && p.lse)
-            p.lse[(size_t)head * p.n_q + grow] = none ? -INFINITY : mm * p.scale + logf(denx);
         }
       }
     }

@@ -154,10 +154,11 @@ def test_attn_bf16_scale_and_reuse_of_output_buffer():
     assert torch.equal(o1, o2)            # deterministic run to run
 
 
-@pytest.mark.parametrize("n_split", [1, 2, 3, 4])
+@pytest.mark.parametrize("n_split", [1, 2, 3, 4, 6, 9])
 def test_attn_bf16_split_paths_agree(split, n_split):
     """Every key-range split count gives the oracle's result (ragged tiles,
-    two heads, output fusion off)."""
+    two heads, output fusion off); more than four splits take the combine's
+    path for weights beyond its registers."""
     q, km, vm, kl, vl = _case(300, 1000, 77, 2, 128, torch.bfloat16, 11)
     split(n_split)
     o, lse = _run(q.to(DEV), km, vm, kl, vl)
