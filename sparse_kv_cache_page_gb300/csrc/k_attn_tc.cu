@@ -138,45 +138,6 @@ __device__ __forceinline__ void split_range(int nkv, int n_split, int sp, int& j
   j1 = (int)(((long long)nkv * (sp + 1)) / n_split);
 }
 
-// Output row store: 32 values of one (query, head), optionally fused with the
-// values already there (o = w_old * o + x).
-__device__ __forceinline__ void store_row32(__nv_bfloat16* dst, const float (&x)[32], bool acc,
-                                            float wo) {
-  uint4* d = reinterpret_cast<uint4*>(dst);
-#pragma unroll
-  for (int v = 0; v < 4; ++v) {
-    float y[8];
-#pragma unroll
-    for (int e = 0; e < 8; ++e) y[e] = x[8 * v + e];
-    if (acc) {
-      const uint4 old = d[v];
-      const uint32_t ow[4] = {old.x, old.y, old.z, old.w};
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        y[2 * e] += wo * __uint_as_float(ow[e] << 16);
-        y[2 * e + 1] += wo * __uint_as_float(ow[e] & 0xffff0000u);
-      }
-    }
-    d[v] = make_uint4(pack_bf16x2(y[0], y[1]), pack_bf16x2(y[2], y[3]), pack_bf16x2(y[4], y[5]),
-                      pack_bf16x2(y[6], y[7]));
-  }
-}
-__device__ __forceinline__ void store_row32(float* dst, const float (&x)[32], bool acc, float wo) {
-  float4* d = reinterpret_cast<float4*>(dst);
-#pragma unroll
-  for (int v = 0; v < 8; ++v) {
-    float4 y = make_float4(x[4 * v], x[4 * v + 1], x[4 * v + 2], x[4 * v + 3]);
-    if (acc) {
-      const float4 old = d[v];
-      y.x += wo * old.x;
-      y.y += wo * old.y;
-      y.z += wo * old.z;
-      y.w += wo * old.w;
-    }
-    d[v] = y;
-  }
-}
-
 __device__ __forceinline__ void softmax_bar() {   // the 256 softmax threads only
   asm volatile("bar.sync 1, 256;" ::: "memory");
 }
@@ -193,30 +154,34 @@ __device__ __forceinline__ bool softmax_all(bool v) {
   return r != 0;
 }
 
-// Four consecutive output values of one row, optionally fused with the values
-// already there (o = w_old * o + x), with the arithmetic of store_row32.
-__device__ __forceinline__ void store4(float* dst, float4 x, bool acc, float wo) {
-  float4* d = reinterpret_cast<float4*>(dst);
+// Four consecutive output values of one row as fp32 (exact for bf16).
+__device__ __forceinline__ float4 load4(const float* src) {
+  return *reinterpret_cast<const float4*>(src);
+}
+__device__ __forceinline__ float4 load4(const __nv_bfloat16* src) {
+  const uint2 w = *reinterpret_cast<const uint2*>(src);
+  return make_float4(__uint_as_float(w.x << 16), __uint_as_float(w.x & 0xffff0000u),
+                     __uint_as_float(w.y << 16), __uint_as_float(w.y & 0xffff0000u));
+}
+// Store four consecutive output values, optionally fused with the old ones
+// (o = w_old * o + x); the sum in fp32, then one rounding to the output type.
+__device__ __forceinline__ void put4(float* dst, float4 x, bool acc, float4 old, float wo) {
   if (acc) {
-    const float4 old = *d;
     x.x += wo * old.x;
     x.y += wo * old.y;
     x.z += wo * old.z;
     x.w += wo * old.w;
   }
-  *d = x;
+  *reinterpret_cast<float4*>(dst) = x;
 }
-__device__ __forceinline__ void store4(__nv_bfloat16* dst, float4 x, bool acc, float wo) {
-  uint2* d = reinterpret_cast<uint2*>(dst);
-  float y[4] = {x.x, x.y, x.z, x.w};
+__device__ __forceinline__ void put4(__nv_bfloat16* dst, float4 x, bool acc, float4 old, float wo) {
   if (acc) {
-    const uint2 old = *d;
-    y[0] += wo * __uint_as_float(old.x << 16);
-    y[1] += wo * __uint_as_float(old.x & 0xffff0000u);
-    y[2] += wo * __uint_as_float(old.y << 16);
-    y[3] += wo * __uint_as_float(old.y & 0xffff0000u);
+    x.x += wo * old.x;
+    x.y += wo * old.y;
+    x.z += wo * old.z;
+    x.w += wo * old.w;
   }
-  *d = make_uint2(pack_bf16x2(y[0], y[1]), pack_bf16x2(y[2], y[3]));
+  *reinterpret_cast<uint2*>(dst) = make_uint2(pack_bf16x2(x.x, x.y), pack_bf16x2(x.z, x.w));
 }
 
 // Split partials are staged row-major in shared memory with this row pitch
@@ -473,11 +438,18 @@ k_block_attn_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     const bool store = grow < p.n_q;
     const float wo = p.accumulate ? (p.w_old ? p.w_old[head] : 1.0f) : 0.0f;
     const float wn0 = p.accumulate ? (p.w_new ? p.w_new[head] : 1.0f) : 1.0f;
-    OutT* orow_g = static_cast<OutT*>(p.o) + ((size_t)(store ? grow : 0) * p.n_heads + head) * HD;
     if (p.n_split == 1) {
-      if (ok) {
+      // normalised rows staged in shared memory (over the idle Q tiles and K/V
+      // ring), then stored a 512-byte row per warp instruction; with output
+      // fusion, four rows' old values are loaded before any is written
+      const int prow = qt * BM + row;                     // 0..255
+      const int sw = threadIdx.x >> 5;                    // softmax warp 0..7: rows 32 sw ..
+      float* stage = reinterpret_cast<float*>(smem);      // [256][kStagePitch]
+      const bool all_ok = softmax_all(ok);
+      if (all_ok) {
         // a head with no key blocks (block-sparse form) has O = 0, LSE = -inf
         const float wn = nloc > 0 ? wn0 / l : 0.0f;
+        float* mine = stage + (size_t)prow * kStagePitch;
 #pragma unroll 1
         for (int c = 0; c < 4; ++c) {
           uint32_t orow[32];
@@ -488,15 +460,36 @@ k_block_attn_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
 #pragma unroll
             for (int e = 0; e < 32; ++e) orow[e] = 0u;
           }
-          if (store) {
-            float x[32];
+          float4* d4 = reinterpret_cast<float4*>(mine + 32 * c);
 #pragma unroll
-            for (int e = 0; e < 32; ++e) x[e] = __uint_as_float(orow[e]) * wn;
-            store_row32(orow_g + 32 * c, x, p.accumulate != 0, wo);
-          }
+          for (int v = 0; v < 8; ++v)
+            d4[v] = make_float4(__uint_as_float(orow[4 * v]) * wn, __uint_as_float(orow[4 * v + 1]) * wn,
+                                __uint_as_float(orow[4 * v + 2]) * wn,
+                                __uint_as_float(orow[4 * v + 3]) * wn);
         }
         if (kLse && store && p.lse)
           p.lse[(size_t)head * p.n_q + grow] = nloc > 0 ? m * p.scale + logf(lx) : -INFINITY;
+        softmax_bar();
+        const bool acc = p.accumulate != 0;
+        for (int r0 = 0; r0 < 32; r0 += 4) {
+          if (q0 + 32 * sw + r0 >= p.n_q) break;          // rows ascend (warp-uniform)
+          float4 y[4], old[4];
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            const int r = 32 * sw + r0 + u;
+            y[u] = reinterpret_cast<const float4*>(stage + (size_t)r * kStagePitch)[lane];
+            if (acc && q0 + r < p.n_q)
+              old[u] = load4(static_cast<OutT*>(p.o) + ((size_t)(q0 + r) * p.n_heads + head) * HD +
+                             4 * lane);
+          }
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            const int r = 32 * sw + r0 + u;
+            if (q0 + r >= p.n_q) break;
+            put4(static_cast<OutT*>(p.o) + ((size_t)(q0 + r) * p.n_heads + head) * HD + 4 * lane, y[u],
+                 acc, old[u], wo);
+          }
+        }
       }
     } else {
       // split: the CTA's unnormalised rows go to scratch through shared memory
@@ -621,8 +614,9 @@ k_block_attn_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                 x.z += w * ts.z;
                 x.w += w * ts.w;
               }
-              store4(static_cast<OutT*>(p.o) + ((size_t)grow_r * p.n_heads + head) * HD + 4 * lane,
-                     x, p.accumulate != 0, wo);
+              OutT* dst = static_cast<OutT*>(p.o) + ((size_t)grow_r * p.n_heads + head) * HD + 4 * lane;
+              const bool acc = p.accumulate != 0;
+              put4(dst, x, acc, acc ? load4(dst) : x, wo);
             }
           }
         }
