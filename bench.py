@@ -39,7 +39,7 @@ H, D, P, N_PAGES, PPC, N_CHUNKS, PDIM, KP, NQ, NLOC = 12, 128, 12480, 40, 8, 5, 
 
 # DRAM bytes read + written per launch of the attention kernel, from one ncu capture of the
 # current kernel (profiles/attention_worldattention_1layer.md); None once the kernel changes.
-ATTN_TRAFFIC_BYTES = 413.65e6
+ATTN_TRAFFIC_BYTES = 414.07e6
 
 
 def attn_flops(n_q, n_kv, d, h):
