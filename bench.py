@@ -827,39 +827,49 @@ def run_stress(args, world, rank, local):
 # CPU oracle arm
 # ----------------------------------------------------------------------------
 
-def cpu_baseline_sample(c, get_page, budget_rows=24):
+def cpu_baseline_sample(c, get_page, budget_rows=24, cache=None):
     """Time the fp64 oracle, as it stands, on a bounded sample of the workload
     and scale it to one chunk: one page summary (x40 pages), the two-stage
     retrieval over 40 summaries, the 4-page gather, and attention for
     `budget_rows` query rows of every head over all 54,600 keys (x n_q/rows).
-    get_page(j) -> (K_j, V_j) as torch tensors."""
+    get_page(j) -> (K_j, V_j) as torch tensors.  `cache` (a dict kept across
+    calls) holds the inputs already converted for the oracle, so repeated
+    samples spend their time in the oracle, not in copies; only the oracle's
+    own work is timed either way."""
     import numpy as np
 
     import oracle as O
     from sparse_kv_cache_page_gb300 import synth
 
+    cache = {} if cache is None else cache
     t_cpu0, t_wall0 = time.process_time(), time.perf_counter()
-    k0, _ = get_page(0)
-    kp0 = synth.to_oracle(k0)[None]
+    if "kp0" not in cache:
+        cache["kp0"] = synth.to_oracle(get_page(0)[0])[None]
+        cache["oq"] = synth.to_oracle(c.q)
+        cache["kloc"], cache["vloc"] = synth.to_oracle(c.k_loc), synth.to_oracle(c.v_loc)
+    kp0, oq = cache["kp0"], cache["oq"]
     t = time.perf_counter()
     kbar0 = O.page_summarize(kp0)
     t_sum = (time.perf_counter() - t) * N_PAGES
     kbar = np.repeat(kbar0, N_PAGES, axis=0)   # timing stand-in for the other 39 summaries
-    oq = synth.to_oracle(c.q)
     t = time.perf_counter()
     idx, _, _ = O.select_pages(oq, kbar, synth.to_oracle(c.prompt_cur),
                                synth.to_oracle(c.prompt_chunks), PPC, KP)
     t_sel = time.perf_counter() - t
-    pages = [get_page(int(j)) for j in idx]
-    kps = np.stack([synth.to_oracle(kv[0]) for kv in pages])
-    vps = np.stack([synth.to_oracle(kv[1]) for kv in pages])
+    key = tuple(int(j) for j in idx)
+    if cache.get("idx") != key:
+        pages = [get_page(j) for j in key]
+        cache["kps"] = np.stack([synth.to_oracle(kv[0]) for kv in pages])
+        cache["vps"] = np.stack([synth.to_oracle(kv[1]) for kv in pages])
+        cache["idx"] = key
+    kps, vps = cache["kps"], cache["vps"]
     t = time.perf_counter()
     kbuf = O.gather_pages(kps, range(KP))
     vbuf = O.gather_pages(vps, range(KP))
     t_gat = time.perf_counter() - t
     rows = np.linspace(0, NQ - 1, budget_rows).astype(int)
     t = time.perf_counter()
-    O.block_attn(oq, kbuf, vbuf, synth.to_oracle(c.k_loc), synth.to_oracle(c.v_loc), rows=rows)
+    O.block_attn(oq, kbuf, vbuf, cache["kloc"], cache["vloc"], rows=rows)
     t_att = (time.perf_counter() - t) * NQ / budget_rows
     wall = time.perf_counter() - t_wall0
     cpu = time.process_time() - t_cpu0
@@ -887,11 +897,11 @@ def run_reference(args, world, rank):
             cache[j] = c.extra["page"](j, "cpu")
         return cache[j]
 
-    samples = []
+    samples, inputs = [], {}
     for _ in range(args.warmup):
-        cpu_baseline_sample(c, get_page, budget_rows=8)
+        cpu_baseline_sample(c, get_page, budget_rows=8, cache=inputs)
     for _ in range(args.steps):
-        samples.append(cpu_baseline_sample(c, get_page, budget_rows=8))
+        samples.append(cpu_baseline_sample(c, get_page, budget_rows=8, cache=inputs))
     value = statistics.mean(s["value"] for s in samples)
     ms = statistics.mean(s["chunk_ms"] for s in samples)
     return {
