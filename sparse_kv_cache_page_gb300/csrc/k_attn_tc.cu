@@ -434,6 +434,12 @@ k_block_attn_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
       ok = __all_sync(0xffffffffu, mbar_wait(&bars->o_ready[qt], (nloc - 1) & 1, abort_flag,
                                              p.status));
     tc_fence_after();
+    // The staging area below overlays the Q tiles: their copy must have landed
+    // (a CTA with no key tiles, block-sparse form, reaches here without having
+    // waited for anything).  Every K/V copy was consumed by an MMA the loop
+    // waited for.
+    const bool staging_ok =
+        ok && __all_sync(0xffffffffu, mbar_wait(&bars->q_full, 0, abort_flag, p.status));
     const int grow = q0 + qt * BM + row;
     const bool store = grow < p.n_q;
     const float wo = p.accumulate ? (p.w_old ? p.w_old[head] : 1.0f) : 0.0f;
@@ -445,7 +451,7 @@ k_block_attn_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
       const int prow = qt * BM + row;                     // 0..255
       const int sw = threadIdx.x >> 5;                    // softmax warp 0..7: rows 32 sw ..
       float* stage = reinterpret_cast<float*>(smem);      // [256][kStagePitch]
-      const bool all_ok = softmax_all(ok);
+      const bool all_ok = softmax_all(staging_ok);
       if (all_ok) {
         // a head with no key blocks (block-sparse form) has O = 0, LSE = -inf
         const float wn = nloc > 0 ? wn0 / l : 0.0f;
@@ -503,7 +509,7 @@ k_block_attn_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
       const int prow = qt * BM + row;                     // 0..255
       const int sw = threadIdx.x >> 5;                    // softmax warp 0..7: rows 32 sw ..
       float* stage = reinterpret_cast<float*>(smem);      // [256][kStagePitch]
-      const bool all_ok = softmax_all(ok);
+      const bool all_ok = softmax_all(staging_ok);
       if (all_ok) {
         float* mine = stage + (size_t)prow * kStagePitch;
 #pragma unroll 1
