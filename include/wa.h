@@ -520,6 +520,40 @@ wa_status wa_check(wa_stream_t stream);
 /* Free this device's scratch arena (after a device synchronize). */
 wa_status wa_shutdown(void);
 
+/*
+ * Upper limit, in nanoseconds, of each bounded wait inside the kernels that
+ * pipeline copies and tensor-core work (wa_block_attn, wa_linear_branch,
+ * wa_sparse_attn) for launches made after this call; 0 restores the default
+ * of 4 s.  A wait that reaches the limit records WA_ERR_TIMEOUT in the status
+ * word; the kernel then waits (with fixed limits of its own) for its copies
+ * and MMAs in flight, frees its tensor memory and returns, so the context
+ * stays usable.  Process-wide; not a property of any one stream.
+ */
+wa_status wa_set_wait_limit_ns(unsigned long long ns);
+
+/*
+ * Host-side fault injection for tests of the error paths; off by default and
+ * process-wide.  No mode makes a GPU fault, trap or hang.
+ *   WA_FAULT_NONE  : normal operation.
+ *   WA_FAULT_ALLOC : any allocation the library would make (the scratch arena,
+ *                    a cache's buffers) reports failure: the call returns
+ *                    WA_ERR_OOM and enqueues nothing.  An arena that already
+ *                    exists is used as before.
+ *   WA_FAULT_COPY  : page copies from pinned host memory (wa_gather_pages with
+ *                    host indices) report failure: WA_ERR_CUDA, nothing enqueued.
+ *   WA_FAULT_WAIT  : wa_block_attn's copy producer withholds the query tiles,
+ *                    so every wait on them runs out at the wait limit: the
+ *                    launch returns WA_OK and wa_check() then WA_ERR_TIMEOUT.
+ * The environment variable WA_FAULT (alloc | copy | wait) sets the mode when
+ * the library is loaded.  Unknown modes return WA_ERR_INVALID_ARG.
+ */
+typedef enum { WA_FAULT_NONE = 0, WA_FAULT_ALLOC = 1, WA_FAULT_COPY = 2, WA_FAULT_WAIT = 3 } wa_fault;
+wa_status wa_set_fault(int mode);
+
+/* Size in bytes of the current device's scratch arena (0 when none has been
+ * allocated yet, or after wa_shutdown); bytes_out is host memory. */
+wa_status wa_scratch_bytes(size_t* bytes_out);
+
 #ifdef __cplusplus
 }
 #endif

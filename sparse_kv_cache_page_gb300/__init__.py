@@ -59,7 +59,8 @@ EXPORTED_SYMBOLS = ("wa_strerror", "wa_version", "wa_page_summarize", "wa_select
                     "wa_cache_get_stats", "wa_cache_page_slots", "wa_cache_wait_copies",
                     "wa_fp8_encode", "wa_fp8_decode", "wa_nvfp4_encode", "wa_nvfp4_decode",
                     "wa_gather_pages_nvfp4",
-                    "wa_gather_pages_fp8", "wa_check", "wa_shutdown")
+                    "wa_gather_pages_fp8", "wa_check", "wa_shutdown", "wa_set_wait_limit_ns",
+                    "wa_set_fault", "wa_scratch_bytes")
 
 
 class _CacheConfig(ctypes.Structure):
@@ -129,6 +130,9 @@ def load():
         "wa_gather_pages_nvfp4": (I, [P, P, P, I, I, I, I, P, I, P, P]),
         "wa_check": (I, [P]),
         "wa_shutdown": (I, []),
+        "wa_set_wait_limit_ns": (I, [ctypes.c_ulonglong]),
+        "wa_set_fault": (I, [I]),
+        "wa_scratch_bytes": (I, [ctypes.POINTER(ctypes.c_size_t)]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -566,3 +570,24 @@ def wa_check(stream=None):
 
 def wa_shutdown():
     _ok("wa_shutdown", load().wa_shutdown())
+
+
+# Fault-injection modes of wa_set_fault (host side; none faults a GPU).
+WA_FAULT_NONE, WA_FAULT_ALLOC, WA_FAULT_COPY, WA_FAULT_WAIT = 0, 1, 2, 3
+
+
+def wa_set_wait_limit_ns(ns: int):
+    """Limit of each bounded device wait for later launches (0 = the 4 s default)."""
+    _ok("wa_set_wait_limit_ns", load().wa_set_wait_limit_ns(int(ns)))
+
+
+def wa_set_fault(mode: int):
+    """Process-wide host-side fault injection (WA_FAULT_* above)."""
+    _ok("wa_set_fault", load().wa_set_fault(int(mode)))
+
+
+def wa_scratch_bytes() -> int:
+    """Bytes of the current device's scratch arena (0 if none is allocated)."""
+    n = ctypes.c_size_t(0)
+    _ok("wa_scratch_bytes", load().wa_scratch_bytes(ctypes.byref(n)))
+    return int(n.value)

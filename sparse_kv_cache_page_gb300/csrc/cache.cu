@@ -96,6 +96,7 @@ struct wa_cache {
 namespace {
 
 using wa::cuda_status;
+using wa::fault_mode;
 
 inline bool dt_ok(wa_dtype dt) { return dt == WA_BF16 || dt == WA_F32; }
 inline size_t dt_size(wa_dtype dt) { return dt == WA_BF16 ? 2 : 4; }
@@ -272,6 +273,7 @@ inline bool compressed(const wa_cache* c) { return fp8(c) || nvfp4(c); }
 // A device buffer of at least `bytes` for compressed DRAM slots.
 wa_status ensure_fetch(wa_cache* c, size_t bytes) {
   if (c->fetch_cap >= bytes) return WA_OK;
+  if (fault_mode() == WA_FAULT_ALLOC) return WA_ERR_OOM;
   if (c->fetch) {
     cudaDeviceSynchronize();             // no decode may still read the old buffer
     cudaFree(c->fetch);
@@ -405,7 +407,8 @@ wa_status wa_cache_create(const wa_cache_config* cfg, wa_cache** out) {
   if (!g.dry_run) {
     const size_t max_pages = (size_t)g.max_chunks * g.pages_per_chunk;
     c->n_stage = g.host_pages > 0 ? g.pages_per_chunk + 4 : 0;
-    bool ok = cudaMalloc(&c->hbm_k, c->page_bytes * g.hbm_pages) == cudaSuccess &&
+    bool ok = fault_mode() != WA_FAULT_ALLOC &&
+              cudaMalloc(&c->hbm_k, c->page_bytes * g.hbm_pages) == cudaSuccess &&
               cudaMalloc(&c->hbm_v, c->page_bytes * g.hbm_pages) == cudaSuccess &&
               cudaMalloc(&c->kbar, max_pages * g.n_heads * g.head_dim * sizeof(float)) == cudaSuccess &&
               cudaMalloc(&c->prompts, (size_t)g.max_chunks * (g.prompt_dim > 0 ? g.prompt_dim : 1) *
@@ -557,6 +560,7 @@ wa_status wa_cache_retrieve(wa_cache* c, const void* q, int n_q, const float* pr
   // a device-to-host copy here would queue behind the offloads on the copy
   // engine, and the host waits for the indices.
   if (c->idx_cap < k_p) {
+    if (fault_mode() == WA_FAULT_ALLOC) return WA_ERR_OOM;
     if (c->idx_host) {
       cudaFreeHost(c->idx_host);
       c->idx_host = nullptr;

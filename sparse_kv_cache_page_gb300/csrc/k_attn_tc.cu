@@ -115,6 +115,8 @@ struct Params {
   const int2* tiles;
   const int32_t* tile_count;
   int tile_stride;
+  unsigned long long wait_ns;   // limit of each bounded wait (host-set)
+  int withhold_q;               // fault injection: the query tiles are never copied
 };
 
 // Key tile j of head h: segment (0 = buffer, 1 = local), first row, valid rows.
@@ -242,16 +244,20 @@ k_block_attn_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
       if (lane == 0) {
         prefetch_tmap(&tm_q);
         const int xq = head * HD;
-        mbar_arrive_expect_tx(&bars->q_full, 2 * kQTile);
-        for (int i = 0; i < 2; ++i)
-          for (int hf = 0; hf < 2; ++hf)
-            tma_load_2d(&tm_q, &bars->q_full, smem + SmemLayout::q + i * kQTile + hf * kQHalf,
-                        xq + hf * 64, q0 + i * BM);
+        // (with withhold_q the query copy is never issued: every wait on it
+        // runs out at the wait limit -- the host-side test of the timeout path)
+        if (!p.withhold_q) {
+          mbar_arrive_expect_tx(&bars->q_full, 2 * kQTile);
+          for (int i = 0; i < 2; ++i)
+            for (int hf = 0; hf < 2; ++hf)
+              tma_load_2d(&tm_q, &bars->q_full, smem + SmemLayout::q + i * kQTile + hf * kQHalf,
+                          xq + hf * 64, q0 + i * BM);
+        }
         int issued = 0;
         for (int t = 0; t < 2 * nloc; ++t) {
           const int slot = t % NS;
           if (t >= NS &&
-              !mbar_wait_sleep(&bars->kv_empty[slot], ((t / NS) - 1) & 1, abort_flag, p.status))
+              !mbar_wait_sleep(&bars->kv_empty[slot], ((t / NS) - 1) & 1, abort_flag, p.status, p.wait_ns))
             break;
           const TileRef tr = tile_ref<kSparse>(p, head, jb + (t >> 1));
           const bool is_v = t & 1;
@@ -267,7 +273,7 @@ k_block_attn_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
           // drain: wait (bounded) for the copies still in flight
           for (int t = issued - NS < 0 ? 0 : issued - NS; t < issued; ++t)
             mbar_wait_drain(&bars->kv_full[t % NS], (t / NS) & 1, 100000000ull);
-          mbar_wait_drain(&bars->q_full, 0, 100000000ull);
+          if (!p.withhold_q) mbar_wait_drain(&bars->q_full, 0, 100000000ull);
         }
       }
       __syncwarp();   // lanes 1-31 wait here for lane 0: the warp reaches the CTA barrier converged
@@ -277,18 +283,18 @@ k_block_attn_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         // TMEM columns, each once the other tile's softmax has read the last S
         const uint32_t q_base = smem_u32(smem + SmemLayout::q);
         const uint32_t ring_base = smem_u32(smem + SmemLayout::ring);
-        bool ok = mbar_wait_sleep(&bars->q_full, 0, abort_flag, p.status);
+        bool ok = mbar_wait_sleep(&bars->q_full, 0, abort_flag, p.status, p.wait_ns);
         tc_fence_after();
         for (int jj = 0; ok && jj < nloc; ++jj) {
           const int tk = 2 * jj, sk = tk % NS;
-          if (!(ok = mbar_wait_sleep(&bars->kv_full[sk], (tk / NS) & 1, abort_flag, p.status))) break;
+          if (!(ok = mbar_wait_sleep(&bars->kv_full[sk], (tk / NS) & 1, abort_flag, p.status, p.wait_ns))) break;
           const uint32_t kb = ring_base + sk * kKvTile;
           for (int i = 0; i < 2; ++i) {
             // the S columns were last read by softmax 1 (tile jj-1) or softmax 0 (tile jj)
             if (i == 0 && jj > 0 &&
-                !(ok = mbar_wait_sleep(&bars->s_free[1], (jj - 1) & 1, abort_flag, p.status)))
+                !(ok = mbar_wait_sleep(&bars->s_free[1], (jj - 1) & 1, abort_flag, p.status, p.wait_ns)))
               break;
-            if (i == 1 && !(ok = mbar_wait_sleep(&bars->s_free[0], jj & 1, abort_flag, p.status)))
+            if (i == 1 && !(ok = mbar_wait_sleep(&bars->s_free[0], jj & 1, abort_flag, p.status, p.wait_ns)))
               break;
             tc_fence_after();
             const uint32_t qb = q_base + i * kQTile;
@@ -316,10 +322,10 @@ k_block_attn_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         bool ok = true;
         for (int jj = 0; ok && jj < nloc; ++jj) {
           const int tv = 2 * jj + 1, sv = tv % NS;
-          if (!(ok = mbar_wait_sleep(&bars->kv_full[sv], (tv / NS) & 1, abort_flag, p.status))) break;
+          if (!(ok = mbar_wait_sleep(&bars->kv_full[sv], (tv / NS) & 1, abort_flag, p.status, p.wait_ns))) break;
           const uint32_t vb = ring_base + sv * kKvTile;
           for (int i = 0; i < 2; ++i) {
-            if (!(ok = mbar_wait_sleep(&bars->p_ready[i], jj & 1, abort_flag, p.status)))
+            if (!(ok = mbar_wait_sleep(&bars->p_ready[i], jj & 1, abort_flag, p.status, p.wait_ns)))
               break;
             tc_fence_after();
 #pragma unroll
@@ -353,7 +359,7 @@ k_block_attn_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     // Every tcgen05.ld/st below is .sync.aligned: all 32 lanes of the warp must
     // execute it together, so branch conditions around them are warp-uniform.
     for (int jj = 0; jj < nloc; ++jj) {
-      ok = __all_sync(0xffffffffu, mbar_wait(&bars->s_full[qt], jj & 1, abort_flag, p.status));
+      ok = __all_sync(0xffffffffu, mbar_wait(&bars->s_full[qt], jj & 1, abort_flag, p.status, p.wait_ns));
       if (!ok) break;
       tc_fence_after();
       uint32_t sr[4][32];
@@ -408,7 +414,7 @@ k_block_attn_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
       // is rescaled.  (The wait is at most one phase behind.)
       if (jj >= 1)
         ok = __all_sync(0xffffffffu, mbar_wait(&bars->o_ready[qt], (jj - 1) & 1, abort_flag,
-                                               p.status));
+                                               p.status, p.wait_ns));
       if (!ok) break;
       tc_fence_after();
       tmem_st32(lane_addr + col_p(qt), pk[0]);
@@ -432,14 +438,14 @@ k_block_attn_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     }
     if (ok && nloc > 0)
       ok = __all_sync(0xffffffffu, mbar_wait(&bars->o_ready[qt], (nloc - 1) & 1, abort_flag,
-                                             p.status));
+                                             p.status, p.wait_ns));
     tc_fence_after();
     // The staging area below overlays the Q tiles: their copy must have landed
     // (a CTA with no key tiles, block-sparse form, reaches here without having
     // waited for anything).  Every K/V copy was consumed by an MMA the loop
     // waited for.
     const bool staging_ok =
-        ok && __all_sync(0xffffffffu, mbar_wait(&bars->q_full, 0, abort_flag, p.status));
+        ok && __all_sync(0xffffffffu, mbar_wait(&bars->q_full, 0, abort_flag, p.status, p.wait_ns));
     const int grow = q0 + qt * BM + row;
     const bool store = grow < p.n_q;
     const float wo = p.accumulate ? (p.w_old ? p.w_old[head] : 1.0f) : 0.0f;
@@ -786,6 +792,8 @@ wa_status launch_attn_tc(const void* q, int n_q, const void* k_main, const void*
   p.part_o = nullptr;
   p.part_ml = nullptr;
   p.counters = nullptr;
+  p.wait_ns = wait_limit_ns();
+  p.withhold_q = fault_mode() == WA_FAULT_WAIT;
   Scratch sc;
   const size_t units = (size_t)p.n_qpairs * n_heads;
   // scratch: [tiles (block-sparse form)][split partials]

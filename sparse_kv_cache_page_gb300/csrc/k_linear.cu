@@ -52,6 +52,7 @@ struct LinParams {
   int n_main, n_loc, nt_main, nt_loc, n_split, n_heads, L;
   float* partial;   // [split][tensor][head][rank][128]
   int* status;
+  unsigned long long wait_ns;   // limit of each bounded wait (host-set)
 };
 
 template <int RB>
@@ -108,7 +109,7 @@ k_linformer_proj(const __grid_constant__ CUtensorMap tm_ek, const __grid_constan
       for (int t = 0; t < ntl; ++t) {
         const int slot = t % C::ns;
         if (t >= C::ns &&
-            !mbar_wait(&bars->empty[slot], ((t / C::ns) - 1) & 1, abort_flag, p.status))
+            !mbar_wait(&bars->empty[slot], ((t / C::ns) - 1) & 1, abort_flag, p.status, p.wait_ns))
           break;
         const int g = t0 + t;
         const CUtensorMap* tm_x;
@@ -146,7 +147,7 @@ k_linformer_proj(const __grid_constant__ CUtensorMap tm_ek, const __grid_constan
       bool ok = true;
       for (int t = 0; ok && t < ntl; ++t) {
         const int slot = t % C::ns;
-        if (!(ok = mbar_wait(&bars->full[slot], (t / C::ns) & 1, abort_flag, p.status))) break;
+        if (!(ok = mbar_wait(&bars->full[slot], (t / C::ns) & 1, abort_flag, p.status, p.wait_ns))) break;
         tc_fence_after();
         const uint32_t st = base + slot * C::stage;
 #pragma unroll
@@ -167,7 +168,7 @@ k_linformer_proj(const __grid_constant__ CUtensorMap tm_ek, const __grid_constan
     __syncwarp();
   }
   // epilogue (all four warps): TMEM lane = rank row within a block
-  bool ok = __all_sync(0xffffffffu, mbar_wait(&bars->done, 0, abort_flag, p.status));
+  bool ok = __all_sync(0xffffffffu, mbar_wait(&bars->done, 0, abort_flag, p.status, p.wait_ns));
   tc_fence_after();
   if (ok) {
     const uint32_t lane_addr = tmem + ((uint32_t)(32 * warp) << 16);
@@ -301,6 +302,7 @@ wa_status launch_linear_branch(const void* q, int n_q, const void* k_main, const
   if ((rc = get_scratch(part_bytes + kv_bytes, &sc)) != WA_OK) return rc;
   p.partial = static_cast<float*>(sc.data);
   p.status = &sc.ctrl->status;
+  p.wait_ns = wait_limit_ns();
   __nv_bfloat16* kv = reinterpret_cast<__nv_bfloat16*>(static_cast<char*>(sc.data) + part_bytes);
   const int gy = 2 * n_heads;
   switch (rank / 128) {

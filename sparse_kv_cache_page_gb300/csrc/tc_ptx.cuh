@@ -2,9 +2,10 @@
 // tcgen05 (MMA into tensor memory, TMEM alloc/ld/st), and bounded waits.
 //
 // Every wait here is bounded: it polls with try_wait, and after a time limit
-// (read from %globaltimer) it raises the CTA's abort flag and records
-// kStatusTimeout in the device status word, then returns false so that the
-// caller can leave its loop and tear down (drain copies, free TMEM).
+// (read from %globaltimer; the launch passes the limit the host set) it
+// raises the CTA's abort flag and records kStatusTimeout in the device status
+// word, then returns false so that the caller can leave its loop and tear
+// down (drain copies, free TMEM).
 #pragma once
 
 #include <cuda.h>
@@ -14,8 +15,6 @@
 
 namespace wa {
 namespace ptx {
-
-constexpr unsigned long long kWaitLimitNs = 4000000000ull;   // 4 s per wait
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -83,13 +82,14 @@ __device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t* bar, uint32_t pari
 
 // Bounded wait as mbar_wait below, sleeping between polls.
 __device__ __forceinline__ bool mbar_wait_sleep(uint64_t* bar, uint32_t parity,
-                                                volatile int* abort_flag, int* status) {
+                                                volatile int* abort_flag, int* status,
+                                                unsigned long long limit_ns) {
   if (mbar_try_wait_sleep(bar, parity, 20000u)) return true;
   const unsigned long long t0 = globaltimer();
   for (;;) {
     if (mbar_try_wait_sleep(bar, parity, 20000u)) return true;
     if (*abort_flag) return false;
-    if (globaltimer() - t0 > kWaitLimitNs) {
+    if (globaltimer() - t0 > limit_ns) {
       *abort_flag = 1;
       atomicOr(status, kStatusTimeout);
       return false;
@@ -98,17 +98,17 @@ __device__ __forceinline__ bool mbar_wait_sleep(uint64_t* bar, uint32_t parity,
 }
 
 // Wait until the phase with the given parity has completed.  Returns false
-// (and raises the abort flag / status word) after kWaitLimitNs, or at once
-// if another role of the CTA already aborted.
+// (and raises the abort flag / status word) after limit_ns, or soon after
+// another role of the CTA aborted.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
-                                          int* status) {
+                                          int* status, unsigned long long limit_ns) {
   if (mbar_try_wait(bar, parity)) return true;
   const unsigned long long t0 = globaltimer();
   for (uint32_t it = 1;; ++it) {
     if (mbar_try_wait(bar, parity)) return true;
     if ((it & 255u) == 0) {
       if (*abort_flag) return false;
-      if (globaltimer() - t0 > kWaitLimitNs) {
+      if (globaltimer() - t0 > limit_ns) {
         *abort_flag = 1;
         atomicOr(status, kStatusTimeout);
         return false;

@@ -2,9 +2,11 @@
 //
 // Every entry point validates on the host and returns a status before any
 // launch; no C++ exception escapes (all code here is exception-free).
+#include <atomic>
 #include <math.h>
 #include <mutex>
 #include <stdio.h>
+#include <stdlib.h>
 #include <string.h>
 
 #include "wa_internal.cuh"
@@ -25,7 +27,23 @@ DeviceArena g_arena[kMaxDevices];
 
 constexpr size_t ctrl_bytes() { return (sizeof(Ctrl) + 255) & ~size_t(255); }
 
+constexpr unsigned long long kDefaultWaitNs = 4000000000ull;   // 4 s
+std::atomic<unsigned long long> g_wait_ns{kDefaultWaitNs};
+
+int fault_from_env() {
+  const char* e = getenv("WA_FAULT");
+  if (!e) return WA_FAULT_NONE;
+  if (!strcmp(e, "alloc")) return WA_FAULT_ALLOC;
+  if (!strcmp(e, "copy")) return WA_FAULT_COPY;
+  if (!strcmp(e, "wait")) return WA_FAULT_WAIT;
+  return WA_FAULT_NONE;
+}
+std::atomic<int> g_fault{fault_from_env()};
+
 }  // namespace
+
+unsigned long long wait_limit_ns() { return g_wait_ns.load(std::memory_order_relaxed); }
+int fault_mode() { return g_fault.load(std::memory_order_relaxed); }
 
 wa_status get_scratch(size_t bytes, Scratch* out) {
   int dev = 0;
@@ -33,6 +51,7 @@ wa_status get_scratch(size_t bytes, Scratch* out) {
   std::lock_guard<std::mutex> lock(g_mu);
   DeviceArena& a = g_arena[dev];
   if (a.base == nullptr || a.data_bytes < bytes) {
+    if (fault_mode() == WA_FAULT_ALLOC) return WA_ERR_OOM;
     size_t want = bytes < (size_t(1) << 20) ? (size_t(1) << 20) : bytes;
     if (a.base != nullptr) {
       // Earlier launches may still read the old arena.
@@ -244,6 +263,7 @@ wa_status wa_gather_pages(const void* k_pages, const void* v_pages, wa_dtype dt,
     }
     for (int i = 0; i < k_p; ++i)
       if (idx_host[i] < 0 || idx_host[i] >= n_pages) return WA_ERR_INDEX;
+    if (fault_mode() == WA_FAULT_COPY) return WA_ERR_CUDA;
     for (int i = 0; i < k_p; ++i) {
       const char* ks = static_cast<const char*>(k_pages) + (size_t)idx_host[i] * page_bytes;
       if (cudaMemcpyAsync(static_cast<char*>(k_buf) + (size_t)i * page_bytes, ks, page_bytes,
@@ -506,6 +526,29 @@ wa_status wa_check(wa_stream_t stream) {
   }
   if (h & kStatusTimeout) return WA_ERR_TIMEOUT;
   if (h & kStatusIndex) return WA_ERR_INDEX;
+  return WA_OK;
+}
+
+wa_status wa_set_wait_limit_ns(unsigned long long ns) {
+  g_wait_ns.store(ns == 0 ? kDefaultWaitNs : ns, std::memory_order_relaxed);
+  return WA_OK;
+}
+
+wa_status wa_set_fault(int mode) {
+  if (mode < WA_FAULT_NONE || mode > WA_FAULT_WAIT) return WA_ERR_INVALID_ARG;
+  g_fault.store(mode, std::memory_order_relaxed);
+  return WA_OK;
+}
+
+wa_status wa_scratch_bytes(size_t* bytes_out) {
+  if (!bytes_out) return WA_ERR_INVALID_ARG;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+    cudaGetLastError();
+    return WA_ERR_CUDA;
+  }
+  std::lock_guard<std::mutex> lock(g_mu);
+  *bytes_out = g_arena[dev].base ? g_arena[dev].data_bytes : 0;
   return WA_OK;
 }
 

@@ -16,6 +16,10 @@ enum : int {
   kStatusTimeout = 2,   // a bounded wait gave up
 };
 
+// Process-wide settings read by the launchers (wa_set_wait_limit_ns, wa_set_fault).
+unsigned long long wait_limit_ns();
+int fault_mode();
+
 // Per-device control block at the start of the scratch arena.
 struct Ctrl {
   int status;           // kStatus* bits

@@ -161,3 +161,28 @@ def peaked_queries(k_src: torch.Tensor, n_q: int, seed: int, gain: float = 8.0) 
     pi = torch.randint(0, k_src.shape[0], (n_q,), generator=g)
     q = (gain * k_src[pi.to(k_src.device)].float()).to(k_src.dtype)
     return q, pi
+
+
+# Minute-long stress workload: layers one after another, 120 cached pages per
+# layer whose bodies live in pinned host memory (one page store shared by the
+# layers), each layer with its own queries and local KV.
+STRESS_PAGES = 120
+STRESS_LAYERS = 30
+
+
+def stress_page(j: int, device="cpu", rank: int = 0, n_heads: int = 12, head_dim: int = 128,
+                page_tokens: int = PAGE_TOKENS):
+    """(K, V) of page j of the stress workload's page store, [P][H][d] bf16."""
+    s = lambda t: seed_of("stress", rank, t)  # noqa: E731
+    shape = (page_tokens, n_heads, head_dim)
+    return (normal(shape, s(("k", j)), device, torch.bfloat16),
+            normal(shape, s(("v", j)), device, torch.bfloat16))
+
+
+def stress_layer(l: int, device="cpu", rank: int = 0, n_heads: int = 12, head_dim: int = 128,
+                 n_q: int = 3 * TOKENS_PER_FRAME, n_loc: int = 3 * TOKENS_PER_FRAME):
+    """(Q, K_loc, V_loc) of layer l of the stress workload, [tokens][H][d] bf16."""
+    s = lambda t: seed_of("stress", rank, t)  # noqa: E731
+    return (normal((n_q, n_heads, head_dim), s(("q", l)), device, torch.bfloat16),
+            normal((n_loc, n_heads, head_dim), s(("kl", l)), device, torch.bfloat16),
+            normal((n_loc, n_heads, head_dim), s(("vl", l)), device, torch.bfloat16))

@@ -108,7 +108,7 @@ class TieredPipeline:
                         idx_host, st["ks"].view(-1, 1, P * H), st["vs"].view(-1, 1, P * H),
                         stream=self.side)
 
-    def run(self, layers, mode: str = "pipeline"):
+    def run(self, layers, mode: str = "pipeline", on_layer=None):
         """Run all layers.  mode: "pipeline" (copy-engine fetches on a side
         stream overlap attention), "serial" (each layer's copy, then its
         attention, on one stream), "direct" (the gather kernel reads the pinned
@@ -119,16 +119,19 @@ class TieredPipeline:
         tier), "fp8_pipeline" (the FP8 pages fetched by the copy engine on the
         side stream into a staging slot and decoded there, overlapping the
         previous layer's attention), "nvfp4" / "nvfp4_pipeline" (the same with the
-        NVFP4 copy: E2M1 codes and two levels of scales).  Returns the page
-        indices [n_layers][k_p] (int32; pinned host memory, or device memory in
-        the "direct", "fp8" and "nvfp4" modes)."""
+        NVFP4 copy: E2M1 codes and two levels of scales).  ``on_layer(l, k_buf,
+        v_buf)``, if given, is called once layer l's attention is enqueued on
+        the current stream and before the buffers it read may be refilled: work
+        it enqueues on that stream sees the buffers as the attention did.
+        Returns the page indices [n_layers][k_p] (int32; pinned host memory, or
+        device memory in the "direct", "fp8" and "nvfp4" modes)."""
         main = torch.cuda.current_stream(self.device)
         n = len(layers)
         idx = torch.empty((n, self.k_p), dtype=torch.int32, device=self.device)
         for l, ly in enumerate(layers):
             wa_select_pages(ly.q, ly.kbar, None, None, 1, self.k_p, idx[l])
         if mode in ("direct", "fp8", "nvfp4"):
-            return self._run_direct(layers, idx, main, codec=mode)
+            return self._run_direct(layers, idx, main, codec=mode, on_layer=on_layer)
         idx_h = torch.empty((n, self.k_p), dtype=torch.int32, pin_memory=True)
         idx_h.copy_(idx, non_blocking=True)
         main.synchronize()                         # indices reach the host once
@@ -156,6 +159,8 @@ class TieredPipeline:
                     ev_copy[l].record(self.side)
                 main.wait_event(ev_copy[l])
                 wa_block_attn(ly.q, kb, vb, ly.k_loc, ly.v_loc, ly.out)
+                if on_layer is not None:
+                    on_layer(l, kb, vb)
                 ev_attn[l].record(main)
             main.wait_stream(self.side)
             return idx_h
@@ -174,11 +179,13 @@ class TieredPipeline:
                 if mode == "pipeline":
                     main.wait_event(ev_copy[l])
                 wa_block_attn(ly.q, kb, vb, ly.k_loc, ly.v_loc, ly.out)
+                if on_layer is not None:
+                    on_layer(l, kb, vb)
                 ev_attn[l].record(main)
         main.wait_stream(self.side)
         return idx_h
 
-    def _run_direct(self, layers, idx, main, codec="direct"):
+    def _run_direct(self, layers, idx, main, codec="direct", on_layer=None):
         ev_sel = torch.cuda.Event()
         ev_sel.record(main)
         n = len(layers)
@@ -199,6 +206,8 @@ class TieredPipeline:
                 ev_copy[l].record(self.side)
             main.wait_event(ev_copy[l])
             wa_block_attn(ly.q, kb, vb, ly.k_loc, ly.v_loc, ly.out)
+            if on_layer is not None:
+                on_layer(l, kb, vb)
             ev_attn[l].record(main)
         main.wait_stream(self.side)
         return idx

@@ -79,3 +79,28 @@ def test_host_validation_without_gpu(lib):
                                 ctypes.c_float(0), None, None, 1, fake, 0, None) == 3
     assert lib.wa_linear_branch(fake, 4, fake, fake, 8, None, None, 0, fake, fake, 100, 1, 1, 128,
                                 ctypes.c_float(0), None, None, 1, fake, 1, None) == 2
+
+
+def test_fault_and_wait_limit_setters(lib):
+    """The fault-injection and wait-limit setters are host-only: they accept
+    the documented modes, refuse others, and restore the defaults."""
+    for mode in (wa.WA_FAULT_ALLOC, wa.WA_FAULT_COPY, wa.WA_FAULT_WAIT, wa.WA_FAULT_NONE):
+        assert lib.wa_set_fault(mode) == 0
+    assert lib.wa_set_fault(4) == 1 and lib.wa_set_fault(-1) == 1
+    assert lib.wa_set_wait_limit_ns(1000) == 0
+    assert lib.wa_set_wait_limit_ns(0) == 0          # back to the 4 s default
+    assert lib.wa_scratch_bytes(None) == 1
+
+
+def test_library_loads_with_a_fault_mode_in_the_environment():
+    """The library reads WA_FAULT when it loads (its effect is checked on the
+    GPU); loading with it set works and the setter still behaves."""
+    import subprocess
+    import sys
+    code = ("import ctypes, sparse_kv_cache_page_gb300 as wa; lib = wa.load(); "
+            "print(lib.wa_set_fault(0), lib.wa_set_fault(9))")
+    env = dict(os.environ, WA_FAULT="alloc")
+    r = subprocess.run([sys.executable, "-c", code], cwd=ROOT, env=env, capture_output=True,
+                       text=True, timeout=120)
+    assert r.returncode == 0, r.stderr
+    assert r.stdout.split() == ["0", "1"]

@@ -98,3 +98,65 @@ def test_noalloc_select_rejects_requests_beyond_its_array():
     st = fn(_p(q), 0, 9728, 64, 128, _p(kbar), 8, None, None, 0, 0, 1, 2, _p(idx), None, None,
             stream)
     assert st == 2   # WA_ERR_SHAPE, nothing enqueued
+
+
+_FRESH = r'''
+import ctypes, sys, torch
+import sparse_kv_cache_page_gb300 as wa
+from sparse_kv_cache_page_gb300 import synth
+lib = wa.load()
+fn = lib.wa_select_pages_noalloc
+P, I = ctypes.c_void_p, ctypes.c_int
+fn.restype = I
+fn.argtypes = [P, I, I, I, I, P, I, P, P, I, I, I, I, P, P, P, P]
+p = lambda t: ctypes.c_void_p(t.data_ptr())
+s = lambda t: synth.seed_of("noalloc_fresh", t)
+q = synth.normal((4680, 12, 128), s("q"), "cuda", torch.bfloat16)
+kbar = synth.normal((40, 12, 128), s("kbar"), "cuda", std=0.05)
+pc = synth.normal((5, 4096), s("pc"), "cuda")
+cur = (pc[3] + 0.5 * synth.normal((4096,), s("cur"), "cuda")).contiguous()
+idx = torch.full((4,), -1, dtype=torch.int32, device="cuda")
+ch = torch.full((1,), -9, dtype=torch.int32, device="cuda")
+stream = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+args = (p(q), 1, 4680, 12, 128, p(kbar), 40, p(cur), p(pc), 5, 4096, 8, 4, p(idx), None, p(ch),
+        stream)
+torch.cuda.synchronize()
+before = wa.wa_scratch_bytes()
+assert fn(*args) == 0
+torch.cuda.synchronize()
+free1 = torch.cuda.mem_get_info()[0]
+for _ in range(5):
+    assert fn(*args) == 0
+torch.cuda.synchronize()
+free2 = torch.cuda.mem_get_info()[0]
+print(before, wa.wa_scratch_bytes(), free1, free2, *idx.cpu().tolist(), int(ch.item()))
+'''
+
+
+def test_noalloc_select_allocates_nothing_in_a_fresh_process():
+    """In a process where the library has made no allocation yet, calls of
+    the non-allocating entry point leave the library's arena unallocated and
+    the device's free memory unchanged (after the first call, which loads the
+    library's kernels); its indices equal the allocating entry point's."""
+    import os
+    import subprocess
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    r = subprocess.run([sys.executable, "-c", _FRESH], cwd=root, capture_output=True, text=True,
+                       timeout=300)
+    assert r.returncode == 0, r.stderr
+    before, after, free1, free2, *rest = (int(x) for x in r.stdout.split())
+    assert before == 0 and after == 0
+    assert free1 == free2
+    idx, ch = rest[:4], rest[4]
+    s = lambda t: synth.seed_of("noalloc_fresh", t)  # noqa: E731
+    q = synth.normal((4680, 12, 128), s("q"), DEV, torch.bfloat16)
+    kbar = synth.normal((40, 12, 128), s("kbar"), DEV, std=0.05)
+    pc = synth.normal((5, 4096), s("pc"), DEV)
+    cur = (pc[3] + 0.5 * synth.normal((4096,), s("cur"), DEV)).contiguous()
+    ref_idx = torch.full((4,), -1, dtype=torch.int32, device=DEV)
+    ref_ch = torch.full((1,), -9, dtype=torch.int32, device=DEV)
+    wa.wa_select_pages(q, kbar, cur, pc, 8, 4, ref_idx, chunk_out=ref_ch)
+    wa.wa_check()
+    assert ch == int(ref_ch.item()) == 3
+    assert idx == ref_idx.cpu().tolist()
