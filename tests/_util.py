@@ -36,25 +36,40 @@ def assert_attn_close(o_gpu: torch.Tensor, o_ref: np.ndarray, dtype, what=""):
     return err
 
 
-def score_error_bound(q64: np.ndarray, k_pages64_abs_means: np.ndarray, qbar: np.ndarray,
-                      kbar: np.ndarray, n_q: int, page_tokens: int, head_dim: int) -> np.ndarray:
-    """Probabilistic bound on |alpha_gpu - alpha_exact| per page for fp32
-    sums of n terms (error <= lambda*sqrt(n)*u*sum|terms|, Higham & Mary):
-    the mean query, the page means, and the final dot product.
+def mean_error_bound(x64: np.ndarray) -> np.ndarray:
+    """Probabilistic bound, per element, on the fp32 rounding error of the
+    mean over axis 0 of x64 ([n][...] fp64): lambda*u*||s||_2 / n + u*|mean|,
+    with s_k the partial sums in row order.  The error of a floating-point sum
+    is sum_k delta_k s_k with independent |delta_k| <= u, which is below
+    lambda*u*||s||_2 with probability >= 1 - 2 exp(-lambda^2 / 2) (Higham &
+    Mary, 2019, the lemma behind their sqrt(n) * u * sum|x_i| bound; that
+    simplification bounds ||s||_2 for any order but ignores the cancellation
+    of zero-mean data, by a factor of about sqrt(n)).  Blocked or tree orders,
+    as the kernels use, have partial sums no larger than the row-order ones
+    for such data."""
+    n = x64.shape[0]
+    s = np.cumsum(x64, axis=0)
+    return LAMBDA * U32 * np.sqrt(np.einsum("i...,i...->...", s, s)) / n + U32 * np.abs(s[-1]) / n
 
-    q64: [n_q][H][d] fp64 queries; k_pages64_abs_means: [n_pages][H][d] mean |k|.
-    """
-    rq = LAMBDA * math.sqrt(n_q) * U32 + U32
-    rk = LAMBDA * math.sqrt(page_tokens) * U32 + U32
-    dq = rq * np.abs(q64).mean(axis=0)                 # |dQbar| per element
-    dk = rk * k_pages64_abs_means                      # |dKbar| per page element
-    c = q64.shape[1] * q64.shape[2]
+
+def score_error_bound(dq: np.ndarray, dk: np.ndarray, qbar: np.ndarray, kbar: np.ndarray,
+                      head_dim: int) -> np.ndarray:
+    """Bound on |alpha_gpu - alpha_exact| per page from the error bounds of
+    the mean query (dq [H][d]) and of the page means (dk [n_pages][H][d],
+    see mean_error_bound), plus the fp32 dot product of H*d terms and the
+    final scaling (Higham & Mary's lambda*sqrt(n)*u*sum|terms| form)."""
+    c = qbar.size
     rd = LAMBDA * math.sqrt(c) * U32 + U32
     terms = np.abs(qbar)[None] * np.abs(kbar)
-    bound = (np.sum(dq[None] * np.abs(kbar), axis=(1, 2)) + np.sum(np.abs(qbar)[None] * dk,
-                                                                   axis=(1, 2))
-             + rd * terms.sum(axis=(1, 2))) / math.sqrt(head_dim)
-    return bound
+    return (np.sum(dq[None] * np.abs(kbar), axis=(1, 2)) + np.sum(np.abs(qbar)[None] * dk, axis=(1, 2))
+            + rd * terms.sum(axis=(1, 2))) / math.sqrt(head_dim)
+
+
+def page_mean_error_bounds(k_pages) -> np.ndarray:
+    """mean_error_bound of every page of a bank [n_pages][P][H][d] (bf16 bits
+    or float), one page at a time: [n_pages][H][d]."""
+    import oracle as O
+    return np.stack([mean_error_bound(O.as_f64(k_pages[j])) for j in range(len(k_pages))])
 
 
 def assert_selection_margin(alpha_all: np.ndarray, cand, k_p: int, bound: np.ndarray):

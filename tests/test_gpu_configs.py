@@ -26,8 +26,8 @@ import oracle as O
 import sparse_kv_cache_page_gb300 as wa
 from sparse_kv_cache_page_gb300 import synth
 from sparse_kv_cache_page_gb300.tiered import TieredPipeline, TierLayer
-from tests._util import (LSE_ABS, assert_attn_close, assert_selection_margin, f64, np_of,
-                         score_error_bound)
+from tests._util import (LSE_ABS, assert_attn_close, assert_selection_margin, f64,
+                         mean_error_bound, np_of, page_mean_error_bounds, score_error_bound)
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda"
@@ -74,8 +74,8 @@ def test_tiny_fp32_chain(recall, peaked):
                                  c.pages_per_chunk, c.k_p)
     cand = O.candidate_pages(c.n_pages, ch, c.pages_per_chunk)
     qbar = O.mean_query(oq)
-    bound = score_error_bound(O.as_f64(oq), np.abs(O.as_f64(okp)).mean(axis=1), qbar, kbar,
-                              c.n_q, c.page_tokens, c.head_dim)
+    bound = score_error_bound(mean_error_bound(O.as_f64(oq)), page_mean_error_bounds(okp), qbar,
+                              kbar, c.head_dim)
     assert_selection_margin(O.page_scores(qbar, kbar, cand, c.head_dim), cand, c.k_p, bound)
     assert g["chunk"] == ch == recall
     assert g["idx"].tolist() == idx.tolist()
@@ -122,9 +122,8 @@ def test_headline_chunk_as_benchmarked():
                                  c.pages_per_chunk, c.k_p)
     cand = O.candidate_pages(c.n_pages, ch, c.pages_per_chunk)
     alpha = O.page_scores(O.mean_query(oq), kbar, cand, c.head_dim)
-    absmean = np.stack([np.abs(O.as_f64(okp[j])).mean(axis=0) for j in range(c.n_pages)])
-    bound = score_error_bound(O.as_f64(oq), absmean, O.mean_query(oq), kbar, c.n_q,
-                              c.page_tokens, c.head_dim)
+    bound = score_error_bound(mean_error_bound(O.as_f64(oq)), page_mean_error_bounds(okp),
+                              O.mean_query(oq), kbar, c.head_dim)
     assert_selection_margin(np.array(alpha), cand, c.k_p, bound)
     assert g["chunk"] == ch == 3
     assert g["idx"].tolist() == idx.tolist()
@@ -157,10 +156,10 @@ def test_stress_workload_full_size_every_layer():
     wa.wa_check()
     okp, ovp = np_of(hk), np_of(hv)          # views of the pinned store, no copy
     ref_kbar = np.empty((NPG, H, D))
-    absmean = np.empty((NPG, H, D))
+    dk = np.empty((NPG, H, D))
     for j in range(NPG):
         ref_kbar[j] = O.page_summarize(okp[j:j + 1])[0]
-        absmean[j] = np.abs(O.as_f64(okp[j])).mean(axis=0)
+        dk[j] = mean_error_bound(O.as_f64(okp[j]))
     assert np.abs(f64(kbar) - ref_kbar).max() < 1e-6
 
     layers, ref_idx = [], []
@@ -173,7 +172,7 @@ def test_stress_workload_full_size_every_layer():
         assert ch == -1
         qbar = O.mean_query(oq)
         alpha = O.page_scores(qbar, ref_kbar, range(NPG), D)
-        bound = score_error_bound(O.as_f64(oq), absmean, qbar, ref_kbar, NQ, P, D)
+        bound = score_error_bound(mean_error_bound(O.as_f64(oq)), dk, qbar, ref_kbar, D)
         assert_selection_margin(alpha, range(NPG), 4, bound)
         ref_idx.append(idx)
 

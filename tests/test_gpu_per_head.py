@@ -11,7 +11,8 @@ import torch
 import oracle as O
 import sparse_kv_cache_page_gb300 as wa
 from sparse_kv_cache_page_gb300 import synth
-from tests._util import assert_attn_close, f64, np_of, score_error_bound
+from tests._util import (assert_attn_close, f64, mean_error_bound, np_of, page_mean_error_bounds,
+                         score_error_bound)
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda"
@@ -59,11 +60,11 @@ def _check_margins(q, k_pages, kbar64, chunk, ppc, k_p):
     cand = O.candidate_pages(kbar64.shape[0], chunk, ppc)
     qbar = O.mean_query(q)
     a = O.page_scores_per_head(qbar, kbar64, cand, kbar64.shape[2])
-    kabs = np.stack([np.abs(O.as_f64(k_pages[j])).mean(axis=0) for j in range(len(k_pages))])
+    dq = mean_error_bound(q64)
+    dk = page_mean_error_bounds(k_pages)
     for h in range(a.shape[0]):
-        bound = score_error_bound(q64[:, h:h + 1], kabs[:, h:h + 1], qbar[h:h + 1],
-                                  kbar64[:, h:h + 1], q64.shape[0], k_pages.shape[1],
-                                  kbar64.shape[2])
+        bound = score_error_bound(dq[h:h + 1], dk[:, h:h + 1], qbar[h:h + 1],
+                                  kbar64[:, h:h + 1], kbar64.shape[2])
         order = sorted(range(len(cand)), key=lambda i: (-a[h][i], cand[i]))
         if k_p < len(order):
             i0, i1 = order[k_p - 1], order[k_p]

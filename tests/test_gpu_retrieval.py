@@ -9,7 +9,8 @@ import torch
 import oracle as O
 import sparse_kv_cache_page_gb300 as wa
 from sparse_kv_cache_page_gb300 import synth
-from tests._util import assert_selection_margin, f64, np_of, score_error_bound
+from tests._util import (assert_selection_margin, f64, mean_error_bound, np_of,
+                         page_mean_error_bounds, score_error_bound)
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda"
@@ -92,8 +93,9 @@ def test_select_random_no_prompt(k_p):
     (idx, sc, ch), kbar = _oracle_select(c)
     cand = range(c.n_pages)
     alpha = O.page_scores(O.mean_query(np_of(c.q)), kbar, cand, c.head_dim)
-    bound = score_error_bound(O.as_f64(np_of(c.q)), np.abs(O.as_f64(np_of(c.k_pages))).mean(axis=1),
-                              O.mean_query(np_of(c.q)), kbar, c.n_q, c.page_tokens, c.head_dim)
+    bound = score_error_bound(mean_error_bound(O.as_f64(np_of(c.q))),
+                              page_mean_error_bounds(np_of(c.k_pages)), O.mean_query(np_of(c.q)),
+                              kbar, c.head_dim)
     assert_selection_margin(alpha, cand, k_p, bound)
     g_idx, g_sc, _ = _select(c, _summarize(c.k_pages.to(DEV)))
     assert g_idx.tolist() == idx.tolist()
@@ -147,9 +149,8 @@ def test_select_worldattention_shape_full():
                                  c.pages_per_chunk, c.k_p)
     cand = O.candidate_pages(c.n_pages, ch, c.pages_per_chunk)
     alpha = O.page_scores(O.mean_query(oq), kbar, cand, c.head_dim)
-    absmean = np.stack([np.abs(O.as_f64(okp[j])).mean(axis=0) for j in range(c.n_pages)])
-    bound = score_error_bound(O.as_f64(oq), absmean, O.mean_query(oq), kbar, c.n_q,
-                              c.page_tokens, c.head_dim)
+    bound = score_error_bound(mean_error_bound(O.as_f64(oq)), page_mean_error_bounds(okp),
+                              O.mean_query(oq), kbar, c.head_dim)
     assert_selection_margin(np.array(alpha), cand, c.k_p, bound)
     assert g_ch == ch == 3
     assert g_idx.tolist() == idx.tolist()
