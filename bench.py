@@ -216,12 +216,15 @@ def run_gpu(args, world, rank, local, hybrid=False, per_head=False):
             wa.wa_linear_branch(q, kbuf, vbuf, kl, vl, ek, ev, o)
             mark(5)
 
-    def timed_steps(n_summ, clk=None):
+    def timed_steps(n_summ, clk=None, marked=False):
+        """Time args.steps steps; with `marked`, an event between every two
+        kernels gives the per-kernel intervals (the events also serialise the
+        kernels' launches, so the headline total is taken without them)."""
         for _ in range(args.warmup):
             step(n_summ=n_summ)
         wa.wa_check()
         evs = [[torch.cuda.Event(enable_timing=True) for _ in range(len(names) + 1)]
-               for _ in range(args.steps)]
+               for _ in range(args.steps)] if marked else None
         barrier(world)
         torch.cuda.synchronize()
         with (clk if clk is not None else contextlib.nullcontext()):
@@ -229,22 +232,26 @@ def run_gpu(args, world, rank, local, hybrid=False, per_head=False):
             t1 = torch.cuda.Event(enable_timing=True)
             t0.record(stream)
             for k in range(args.steps):
-                step(evs[k], n_summ=n_summ)
+                step(evs[k] if marked else None, n_summ=n_summ)
             t1.record(stream)
             torch.cuda.synchronize()
         barrier(world)
         wa.wa_check()
         total = max_over_ranks(t0.elapsed_time(t1), world)
+        if not marked:
+            return total, None
         per_ = {n: statistics.mean(evs[k][i].elapsed_time(evs[k][i + 1])
                                    for k in range(args.steps))
                 for i, n in enumerate(names)}
         return total, per_
 
     clk = Clocks(local)
-    total_ms, per = timed_steps(N_PAGES, clk)
+    total_ms, _ = timed_steps(N_PAGES, clk)
     ms_step = total_ms / args.steps
-    total_ins, per_ins = timed_steps(PPC)
+    marked_ms, per = timed_steps(N_PAGES, marked=True)
+    total_ins, _ = timed_steps(PPC)
     ms_step_ins = total_ins / args.steps
+    _, per_ins = timed_steps(PPC, marked=True)
 
     # end to end through the public API: per step, the chunk's inputs come from
     # pinned host memory and the output goes back to pinned host memory.  The
@@ -338,6 +345,9 @@ def run_gpu(args, world, rank, local, hybrid=False, per_head=False):
         "chunk_latency_ms": round(ms_step, 4),
         "chunk_latency_is": f"worst case: each step summarises all {N_PAGES} cached pages",
         "kernels_ms": {k: round(v, 4) for k, v in per.items()},
+        "kernels_ms_are": "event intervals from a separate pass with an event between every two "
+                          f"kernels (step {marked_ms / args.steps:.4f} ms there: the events "
+                          "serialise the launches that the unmarked step overlaps)",
         "chunk_latency_ms_insert": round(ms_step_ins, 4),
         "chunk_latency_insert_is": f"summaries taken at insert: each step summarises only the "
                                    f"{PPC} pages of the newest chunk, then retrieval over all "

@@ -130,14 +130,22 @@ wa_status wa_select_pages(const void* q, wa_dtype dt, int n_q, int n_heads, int 
  *
  * Its scratch is a fixed 2 MiB array (plus a 48 KiB control block) compiled
  * into the library; every GPU that loads the library holds it until the
- * process exits.  Limit: (S + ceil(S/16)) * n_heads * head_dim * 4 bytes of
- * partial sums, S = min(304, max(1, n_q/32)), must fit in 2 MiB (e.g.
- * n_heads*head_dim = 1536 fits every n_q); larger requests return
- * WA_ERR_SHAPE and enqueue nothing.
+ * process exits.  Limit: 4 * (B * n_heads * head_dim + n_heads * n_alpha +
+ * n_chunks) bytes (each term rounded up to a multiple of 4 floats) must fit
+ * in 2 MiB, where n_alpha = n_chunks * pages_per_chunk with the prompt stage
+ * and n_pages without it, and B is the number of query row blocks:
+ * B0 = min(floor((2 * SMs - n_chunks) / C), ceil(n_q / 16)), at least 1, then
+ * B = ceil(n_q / ceil(n_q / B0)).  C, the column blocks, is n_heads / g with g
+ * the smallest power of two that divides n_heads and makes g * head_dim at
+ * least 32 16-byte vectors (doubling stops at the first g that no longer
+ * divides n_heads) when head_dim is a whole number of 16-byte vectors of at
+ * least 32 values, else C = 1.  The one-layer WorldAttention shape on 152 SMs
+ * has g = 2, C = 6, B = 49: 49 * 1536 + 12 * 40 + 5 floats, about 296 KiB.
+ * Larger requests return WA_ERR_SHAPE and enqueue nothing.
  * The first call on a device looks up the array's device address with
  * cudaGetSymbolAddress; make that first call before any stream capture.
  * Every call shares the one array, which keeps the previous call's contents:
- * the call clears its ticket counter itself (cudaMemsetAsync on `stream`),
+ * the call clears its ticket counters itself (cudaMemsetAsync on `stream`),
  * and calls that overlap on the GPU (other streams, other host threads)
  * race on the array and give wrong results; serialize them.
  */

@@ -237,6 +237,9 @@ k_block_attn_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = bars->tmem_base;
+  // set-up done (barriers, tensor memory): wait for the previous kernel on the
+  // stream before the first global access
+  pdl_wait();
 
   if (warp >= 8) {
     // ---------------- warpgroup 2: producer, two S issuers, the P V issuer
@@ -729,8 +732,8 @@ wa_status launch_t(const CUtensorMap& tq, const CUtensorMap& tkm, const CUtensor
     attr_done[dev].store(true, std::memory_order_relaxed);
   }
   dim3 grid(p.n_qpairs * p.n_split, n_heads);
-  kern<<<grid, kThreads, smem, s>>>(tq, tkm, tvm, tkl, tvl, p);
-  return cuda_status(cudaPeekAtLastError());
+  return cuda_status(launch_pdl(kern, grid, dim3(kThreads), (size_t)smem, s, tq, tkm, tvm, tkl, tvl,
+                                p));
 }
 
 }  // namespace

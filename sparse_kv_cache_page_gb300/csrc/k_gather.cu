@@ -24,6 +24,7 @@ k_gather_pages(const uint4* __restrict__ k_pages, const uint4* __restrict__ v_pa
                size_t page_vecs, int n_pages, const int32_t* __restrict__ idx, int k_p,
                uint4* __restrict__ k_buf, uint4* __restrict__ v_buf, size_t spans_per_slab,
                Ctrl* ctrl) {
+  pdl_wait();
   const int n_tensors = v_pages ? 2 : 1;
   const size_t total = spans_per_slab * (size_t)k_p * n_tensors;
   for (size_t w = blockIdx.x; w < total; w += gridDim.x) {
@@ -131,10 +132,9 @@ wa_status launch_gather_device(const void* k_pages, const void* v_pages, size_t 
   size_t grid = (size_t)sm_count() * 8;
   if (grid > total) grid = total;
   if (grid == 0) return WA_OK;
-  k_gather_pages<<<(unsigned)grid, kThreads, 0, s>>>(
-      (const uint4*)k_pages, (const uint4*)v_pages, page_vecs, n_pages, idx_dev, k_p,
-      (uint4*)k_buf, (uint4*)v_buf, spans, ctrl);
-  return cuda_status(cudaPeekAtLastError());
+  return cuda_status(launch_pdl(k_gather_pages, dim3((unsigned)grid), dim3(kThreads), 0, s,
+                                (const uint4*)k_pages, (const uint4*)v_pages, page_vecs, n_pages,
+                                idx_dev, k_p, (uint4*)k_buf, (uint4*)v_buf, (size_t)spans, ctrl));
 }
 
 }  // namespace wa

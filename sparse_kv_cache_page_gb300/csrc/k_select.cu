@@ -41,12 +41,16 @@ __device__ __forceinline__ void load_vec(const float* p, float (&f)[4]) {
   f[0] = v.x; f[1] = v.y; f[2] = v.z; f[3] = v.w;
 }
 
-// Column sums of rows [r0, r1) of a [rows][row_elems] matrix into red[0..row_elems).
+// Column sums of rows [r0, r1) of a matrix with rows `stride` elements apart,
+// over the first row_elems columns, into red[0..row_elems).
 // Thread layout: the first nvec*R threads; vec = tid % nvec, row phase = tid / nvec.
 // VPT > 1 only when R == 1 (nvec > blockDim): thread handles vec, vec+256, ...
-template <typename T, int VPT>
-__device__ void colsum_rows(const T* __restrict__ base, int row_elems, int nvec, int R, int r0,
-                            int r1, float* red /* smem, R*row_elems floats */) {
+// kBatchTail: the rows left after the whole batches go as one more batch with
+// every load in flight (rows past r1 skipped), else one row at a time (fewer
+// registers: the page summaries, whose ranges are long, keep four CTAs per SM).
+template <typename T, int VPT, bool kBatchTail = false>
+__device__ void colsum_rows(const T* __restrict__ base, size_t stride, int row_elems, int nvec,
+                            int R, int r0, int r1, float* red /* smem, R*row_elems floats */) {
   constexpr int E = VecOf<T>::E;
   constexpr int U = VPT == 1 ? 8 : (VPT == 2 ? 4 : 2);   // rows in flight
   const int tid = threadIdx.x;
@@ -68,7 +72,7 @@ __device__ void colsum_rows(const T* __restrict__ base, int row_elems, int nvec,
         for (int v = 0; v < VPT; ++v) {
           const int cv = vec + v * kThreads;
           if (VPT == 1 || cv < nvec)
-            load_vec(base + (size_t)(r + u * R) * row_elems + (size_t)cv * E, f[u][v]);
+            load_vec(base + (size_t)(r + u * R) * stride + (size_t)cv * E, f[u][v]);
           else
 #pragma unroll
             for (int e = 0; e < E; ++e) f[u][v][e] = 0.f;
@@ -80,13 +84,32 @@ __device__ void colsum_rows(const T* __restrict__ base, int row_elems, int nvec,
 #pragma unroll
           for (int e = 0; e < E; ++e) acc[v][e] += f[u][v][e];
     }
-    for (; r < r1; r += R) {
+    // the last (partial) batch: its loads all in flight, rows past r1 skipped
+    if (kBatchTail && r < r1) {
+      float f[U][VPT][E];
+#pragma unroll
+      for (int u = 0; u < U; ++u)
+#pragma unroll
+        for (int v = 0; v < VPT; ++v) {
+          const int cv = vec + v * kThreads;
+          if (r + u * R < r1 && (VPT == 1 || cv < nvec))
+            load_vec(base + (size_t)(r + u * R) * stride + (size_t)cv * E, f[u][v]);
+        }
+#pragma unroll
+      for (int u = 0; u < U; ++u)
+#pragma unroll
+        for (int v = 0; v < VPT; ++v)
+          if (r + u * R < r1 && (VPT == 1 || vec + v * kThreads < nvec))
+#pragma unroll
+            for (int e = 0; e < E; ++e) acc[v][e] += f[u][v][e];
+    }
+    for (; !kBatchTail && r < r1; r += R) {
 #pragma unroll
       for (int v = 0; v < VPT; ++v) {
         const int cv = vec + v * kThreads;
         if (VPT == 1 || cv < nvec) {
           float f[E];
-          load_vec(base + (size_t)r * row_elems + (size_t)cv * E, f);
+          load_vec(base + (size_t)r * stride + (size_t)cv * E, f);
 #pragma unroll
           for (int e = 0; e < E; ++e) acc[v][e] += f[e];
         }
@@ -184,6 +207,7 @@ template <typename T, int VPT>
 __global__ void __launch_bounds__(kThreads, 4)
 k_page_summarize(const SumSegs<T> segs, int row_elems, int nvec, int R, Ctrl* ctrl) {
   extern __shared__ float red[];
+  pdl_wait();
   // this CTA's segment (static indices: the table stays in parameter space)
   SumSeg<T> g = segs.s[0];
   if (segs.n > 1 && (int)blockIdx.x >= segs.s[1].cta0) g = segs.s[1];
@@ -195,7 +219,7 @@ k_page_summarize(const SumSegs<T> segs, int row_elems, int nvec, int R, Ctrl* ct
   const int r0 = s * g.rows_per_split;
   const int r1 = min(rows_j, r0 + g.rows_per_split);
   const T* base = g.pages + (size_t)j * g.page_tokens * row_elems;
-  colsum_rows<T, VPT>(base, row_elems, nvec, R, r0, r1, red);
+  colsum_rows<T, VPT>(base, (size_t)row_elems, row_elems, nvec, R, r0, r1, red);
   const float inv = 1.0f / (float)rows_j;
   if (g.splits == 1) {
     for (int c = threadIdx.x; c < row_elems; c += blockDim.x)
@@ -299,13 +323,30 @@ __device__ void bitonic_sort(unsigned long long* keys, int n2) {
   }
 }
 
-constexpr int kGroup = 16;   // partial sums reduced per group at the first level
-
+// The selection kernel runs three kinds of CTAs at once:
+//   * query tiles: CTA (column block cb, row block rb) sums query rows
+//     [rb*rps, ...) over the columns of heads [cb*hpb, ...) (one head per block
+//     when a head row is whole 16-byte vectors of at least 32 values, else all
+//     heads in one block) and stores the partial sums; the last CTA of a column
+//     block adds its n_rb partials in row-block order into the block's mean
+//     query, then scores every page that can be a candidate on each of its heads,
+//     alpha_part[h][j] = Qbar_h . Kbar[j][h];
+//   * prompt CTAs: CTA m computes cos(prompt_cur, prompt_chunks[m]);
+//   * the CTA that finishes last picks the chunk (largest cosine, lowest index on
+//     ties), forms alpha_j = sum_h alpha_part[h][j] / sqrt(d) in head order (or
+//     keeps alpha_part per head for a page set per head) and keeps the top k_p.
+// Every sum runs in a fixed order, so the result does not depend on timing.
 struct SelectArgs {
-  int n_q, row_elems, nvec, R, splits, rows_per_split;
-  float* partial;
+  int n_q, row_elems, head_dim, n_heads;
+  int nvec, R;                 // phase-A thread layout over one column block
+  int hpb, cw, n_cb;           // heads per column block, its width, column blocks
+  int n_rb, rows_per_block;    // row blocks of the queries
+  int n_alpha;                 // pages that can be candidates (scored per head)
+  float* partial;              // [n_cb][n_rb][cw]
+  float* alpha_part;           // [n_heads][n_alpha]
+  float* cosv;                 // [n_chunks]
   const float* kbar;
-  int n_pages, head_dim;
+  int n_pages;
   const float* prompt_cur;
   const float* prompt_chunks;
   int n_chunks, prompt_dim, ppc, k_p;
@@ -315,147 +356,305 @@ struct SelectArgs {
   Ctrl* ctrl;
   int n_cand_max2;   // power of two >= candidate count
   int per_head;      // 0: one page set scored over all heads; 1: a page set per head
+  int stage_floats;  // shared memory past alpha and keys for staging partial scores
 };
 
+// Sum of a block-wide value over the CTA's warps in warp order (every thread
+// gets the total); `scratch` holds 33 floats.
+__device__ __forceinline__ float block_sum(float v, float* scratch) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  v = warp_sum(v);
+  __syncthreads();
+  if (lane == 0) scratch[warp] = v;
+  __syncthreads();
+  if (warp == 0) {
+    float t = lane < nw ? scratch[lane] : 0.f;
+    t = warp_sum(t);
+    if (lane == 0) scratch[32] = t;
+  }
+  __syncthreads();
+  return scratch[32];
+}
+
+// Top k_p of n candidates (scores in alpha[0..n)) into out_idx / out_sc,
+// ascending by candidate; ties to the lower candidate.  keys: n2 words of smem.
+__device__ void select_topk(const float* alpha, int n, int n2, int k_p, int cand0,
+                            unsigned long long* keys, int32_t* out_idx, float* out_sc) {
+  const int tid = threadIdx.x;
+  if (n <= 32) {
+    if (tid < 32) {
+      unsigned long long key = tid < n ? score_key(alpha[tid], (unsigned)tid) : ~0ull;
+      key = warp_sort32(key);
+      unsigned long long sel = tid < k_p ? (key & 0xffffffffull) : ~0ull;
+      sel = warp_sort32(sel);
+      if (tid < k_p) {
+        const int c = (int)(sel & 0xffffffffull);
+        out_idx[tid] = cand0 + c;
+        if (out_sc) out_sc[tid] = alpha[c];
+      }
+    }
+    __syncthreads();
+    return;
+  }
+  for (int i = tid; i < n2; i += blockDim.x)
+    keys[i] = i < n ? score_key(alpha[i], (unsigned)i) : ~0ull;
+  __syncthreads();
+  bitonic_sort(keys, n2);
+  // the first k_p keys are the selection; re-sort them by candidate index
+  int k2 = 1;
+  while (k2 < k_p) k2 <<= 1;
+  for (int i = tid; i < k2; i += blockDim.x) keys[i] = i < k_p ? (keys[i] & 0xffffffffull) : ~0ull;
+  __syncthreads();
+  bitonic_sort(keys, k2);
+  for (int i = tid; i < k_p; i += blockDim.x) {
+    const int c = (int)(keys[i] & 0xffffffffull);
+    out_idx[i] = cand0 + c;
+    if (out_sc) out_sc[i] = alpha[c];
+  }
+  __syncthreads();
+}
+
+// Two CTAs per SM (at most 80 registers), so that every query tile of the
+// one-layer WorldAttention chunk (12 x 26) and the prompt CTAs run in one wave.
 template <typename T, int VPT>
-__global__ void __launch_bounds__(kThreads)
+__global__ void __launch_bounds__(kThreads, 2)
 k_select_pages(const T* __restrict__ q, SelectArgs a) {
   extern __shared__ float smem[];
-  // phase A: partial column sums of this CTA's query rows
-  const int s = blockIdx.x;
-  const int r0 = s * a.rows_per_split;
-  const int r1 = min(a.n_q, r0 + a.rows_per_split);
-  colsum_rows<T, VPT>(q, a.row_elems, a.nvec, a.R, r0, r1, smem);
-  float* mine = a.partial + (size_t)s * a.row_elems;
-  for (int c = threadIdx.x; c < a.row_elems; c += blockDim.x) mine[c] = smem[c];
-  // two-level reduction of the partial sums, each level in a fixed order:
-  // the last CTA of each group of kGroup sums the group, the last group sum
-  // finishes the mean query (short serial chains at both levels)
-  const int g = s / kGroup;
-  const int n_groups = (a.splits + kGroup - 1) / kGroup;
-  const int g0 = g * kGroup, g1 = min(a.splits, g0 + kGroup);
-  if (!last_ticket(&a.ctrl->counters[kSelectCounter - 1 - g], (unsigned)(g1 - g0))) return;
-  float* gsum = a.partial + (size_t)(a.splits + g) * a.row_elems;
-  sum_rows4(a.partial + (size_t)g0 * a.row_elems, g1 - g0, a.row_elems, gsum, 1.0f);
-  if (threadIdx.x == 0) a.ctrl->counters[kSelectCounter - 1 - g] = 0u;
-  if (!last_ticket(&a.ctrl->counters[kSelectCounter], (unsigned)n_groups)) return;
-
-  // phase B (one CTA).  smem: qbar[row_elems] | alpha[n2] | keys[n2]
+  __shared__ float s_red[33];
+  pdl_wait();
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nwarps = blockDim.x >> 5;
-  float* qbar = smem;
-  float* alpha = qbar + ((a.row_elems + 3) & ~3);
-  unsigned long long* keys =
-      reinterpret_cast<unsigned long long*>(alpha + ((a.n_cand_max2 + 3) & ~3));
-  sum_rows4(a.partial + (size_t)a.splits * a.row_elems, n_groups, a.row_elems, qbar,
-            1.0f / (float)a.n_q);
-  __syncthreads();
-
-  // stage 1: prompt top-1 chunk
-  __shared__ float s_red[32];
-  __shared__ int s_idx[32];
-  __shared__ int s_chunk;
-  int cand0 = 0, n_cand = a.n_pages, chunk = -1;
-  if (a.n_chunks > 0) {
-    float np = 0.f;
-    for (int i = tid; i < a.prompt_dim; i += blockDim.x) {
-      const float v = a.prompt_cur[i];
-      np += v * v;
+  const int n_tiles = a.n_cb * a.n_rb;
+  const int b = blockIdx.x;
+  if (b < n_tiles) {
+    // ---- query tile: partial column sums of one row block over one column block
+    const int cb = b / a.n_rb, rb = b % a.n_rb;
+    const int r0 = rb * a.rows_per_block;
+    const int r1 = min(a.n_q, r0 + a.rows_per_block);
+    colsum_rows<T, VPT, true>(q + (size_t)cb * a.cw, (size_t)a.row_elems, a.cw, a.nvec, a.R, r0, r1,
+                              smem);
+    float* mine = a.partial + ((size_t)cb * a.n_rb + rb) * a.cw;
+    for (int c = tid; c < a.cw; c += blockDim.x) mine[c] = smem[c];
+    unsigned* counter = &a.ctrl->counters[kSelectCounter - 1 - cb];
+    if (!last_ticket(counter, (unsigned)a.n_rb)) return;
+    // the column block's mean query: thread group g adds row blocks g, g + G,
+    // ... (one load each in flight), then the G group sums are added in order
+    float* qbar = smem;
+    const float* part = a.partial + (size_t)cb * a.n_rb * a.cw;
+    const int n4 = a.cw / 4;
+    const int G = n4 <= (int)blockDim.x ? min((int)blockDim.x / n4, a.n_rb) : 1;
+    if (G > 1) {
+      float4* red4 = reinterpret_cast<float4*>(smem + a.cw);   // [G][n4]
+      const int col = tid % n4, grp = tid / n4;
+      if (grp < G) {
+        // row blocks grp, grp + G, ... in order, eight loads in flight
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int r0 = grp; r0 < a.n_rb; r0 += 8 * G) {
+          float4 v[8];
+#pragma unroll
+          for (int u = 0; u < 8; ++u) {
+            const int r = r0 + u * G;
+            v[u] = r < a.n_rb ? __ldcg(reinterpret_cast<const float4*>(part + (size_t)r * a.cw) + col)
+                              : make_float4(0.f, 0.f, 0.f, 0.f);
+          }
+#pragma unroll
+          for (int u = 0; u < 8; ++u) {
+            if (r0 + u * G < a.n_rb) {
+              acc.x += v[u].x;
+              acc.y += v[u].y;
+              acc.z += v[u].z;
+              acc.w += v[u].w;
+            }
+          }
+        }
+        red4[grp * n4 + col] = acc;
+      }
+      __syncthreads();
+      const float inv = 1.0f / (float)a.n_q;
+      for (int c = tid; c < n4; c += blockDim.x) {
+        float4 t = red4[c];
+        for (int g = 1; g < G; ++g) {
+          const float4 v = red4[g * n4 + c];
+          t.x += v.x;
+          t.y += v.y;
+          t.z += v.z;
+          t.w += v.w;
+        }
+        reinterpret_cast<float4*>(qbar)[c] = make_float4(t.x * inv, t.y * inv, t.z * inv, t.w * inv);
+      }
+    } else {
+      sum_rows4(part, a.n_rb, a.cw, qbar, 1.0f / (float)a.n_q);
     }
-    np = warp_sum(np);
-    if (lane == 0) s_red[warp] = np;
+    if (tid == 0) *counter = 0u;
     __syncthreads();
-    if (warp == 0) {
-      float t = lane < nwarps ? s_red[lane] : 0.f;
-      t = warp_sum(t);
-      if (lane == 0) s_red[31] = t;
-    }
-    __syncthreads();
-    np = s_red[31];
-    __syncthreads();
-    float best = -INFINITY;
-    int best_m = 0x7fffffff;
-    for (int m = warp; m < a.n_chunks; m += nwarps) {
-      const float* cm = a.prompt_chunks + (size_t)m * a.prompt_dim;
-      float nc = 0.f;
-      const float dot = warp_dot(a.prompt_cur, cm, a.prompt_dim, &nc);
-      const float cosv = (np > 0.f && nc > 0.f) ? dot / (sqrtf(np) * sqrtf(nc)) : 0.f;
-      if (cosv > best) { best = cosv; best_m = m; }   // ascending m: first wins a tie
-    }
-    if (lane == 0) { s_red[warp] = best; s_idx[warp] = best_m; }
-    __syncthreads();
-    if (tid == 0) {
-      float b = s_red[0];
-      int bm = s_idx[0];
-      for (int w = 1; w < nwarps; ++w)
-        if (s_red[w] > b || (s_red[w] == b && s_idx[w] < bm)) { b = s_red[w]; bm = s_idx[w]; }
-      s_chunk = bm;
-    }
-    __syncthreads();
-    chunk = s_chunk;
-    cand0 = chunk * a.ppc;
-    n_cand = a.ppc;
-  } else {
-    __syncthreads();
-  }
-
-  // stage 2: alpha_j = sum_c qbar[c] * kbar[j][c] / sqrt(d) over the candidates,
-  // c over all heads (one page set) or over one head's slice (a set per head)
-  const float inv_sqrt_d = 1.0f / sqrtf((float)a.head_dim);
-  const int n_sets = a.per_head ? a.row_elems / a.head_dim : 1;
-  if (a.per_head && n_cand <= 32 && a.k_p <= n_cand) {
-    // a set per head with at most 32 candidates: a warp per head scores them,
-    // sorts the keys in registers, and sorts the chosen candidates by index
-    for (int hs = warp; hs < n_sets; hs += nwarps) {
-      const int e0 = hs * a.head_dim;
-      float my_alpha = 0.f;
-      unsigned long long key = ~0ull;
-      for (int c = 0; c < n_cand; ++c) {
-        const float dot = warp_dot(qbar + e0, a.kbar + (size_t)(cand0 + c) * a.row_elems + e0,
-                                   a.head_dim, nullptr);
-        if (lane == c) {
-          my_alpha = dot * inv_sqrt_d;
-          key = score_key(my_alpha, (unsigned)c);
+    // per-head partial scores of every page that can be a candidate, eight
+    // (head, page) items per warp in flight
+    const int h0 = cb * a.hpb;
+    const int nh = min(a.hpb, a.n_heads - h0);
+    const int n_items = nh * a.n_alpha;
+    const bool vec = (a.head_dim & 3) == 0;
+    for (int w0 = warp * 8; w0 < n_items; w0 += nwarps * 8) {
+      float acc[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) acc[u] = 0.f;
+      if (vec) {
+        const int d4 = a.head_dim / 4;
+        for (int c0 = 0; c0 < d4; c0 += 32) {
+          const int c = c0 + lane;
+          float4 y[8];
+#pragma unroll
+          for (int u = 0; u < 8; ++u) {
+            const int w = w0 + u;
+            y[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (w < n_items && c < d4) {
+              const int hh = w / a.n_alpha, j = w % a.n_alpha;
+              y[u] = __ldg(reinterpret_cast<const float4*>(a.kbar + (size_t)j * a.row_elems +
+                                                           (size_t)(h0 + hh) * a.head_dim) + c);
+            }
+          }
+#pragma unroll
+          for (int u = 0; u < 8; ++u) {
+            const int w = w0 + u;
+            if (w < n_items && c < d4) {
+              const float4 x = reinterpret_cast<const float4*>(qbar + (w / a.n_alpha) * a.head_dim)[c];
+              acc[u] += x.x * y[u].x + x.y * y[u].y + x.z * y[u].z + x.w * y[u].w;
+            }
+          }
+        }
+      } else {
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          const int w = w0 + u;
+          if (w < n_items) {
+            const int hh = w / a.n_alpha, j = w % a.n_alpha;
+            const float* kb = a.kbar + (size_t)j * a.row_elems + (size_t)(h0 + hh) * a.head_dim;
+            for (int e = lane; e < a.head_dim; e += 32) acc[u] += qbar[hh * a.head_dim + e] * kb[e];
+          }
         }
       }
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const float dot = warp_sum(acc[u]);
+        const int w = w0 + u;
+        if (lane == 0 && w < n_items) {
+          const int hh = w / a.n_alpha, j = w % a.n_alpha;
+          a.alpha_part[(size_t)(h0 + hh) * a.n_alpha + j] = dot;
+        }
+      }
+    }
+  } else {
+    // ---- prompt CTA: cosine of the current prompt with chunk m's prompt
+    const int m = b - n_tiles;
+    const float* cm = a.prompt_chunks + (size_t)m * a.prompt_dim;
+    float dot = 0.f, np = 0.f, nc = 0.f;
+    if ((a.prompt_dim & 3) == 0 &&
+        ((reinterpret_cast<uintptr_t>(a.prompt_cur) | reinterpret_cast<uintptr_t>(cm)) & 15) == 0) {
+      const float4* x4 = reinterpret_cast<const float4*>(a.prompt_cur);
+      const float4* y4 = reinterpret_cast<const float4*>(cm);
+      const int n4 = a.prompt_dim / 4;
+      for (int i0 = tid; i0 < n4; i0 += 4 * blockDim.x) {
+        float4 x[4], y[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const int i = i0 + u * blockDim.x;
+          x[u] = i < n4 ? __ldg(x4 + i) : make_float4(0.f, 0.f, 0.f, 0.f);
+          y[u] = i < n4 ? __ldg(y4 + i) : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          dot += x[u].x * y[u].x + x[u].y * y[u].y + x[u].z * y[u].z + x[u].w * y[u].w;
+          np += x[u].x * x[u].x + x[u].y * x[u].y + x[u].z * x[u].z + x[u].w * x[u].w;
+          nc += y[u].x * y[u].x + y[u].y * y[u].y + y[u].z * y[u].z + y[u].w * y[u].w;
+        }
+      }
+    } else {
+      for (int i = tid; i < a.prompt_dim; i += blockDim.x) {
+        const float x = a.prompt_cur[i], y = cm[i];
+        dot += x * y;
+        np += x * x;
+        nc += y * y;
+      }
+    }
+    dot = block_sum(dot, s_red);
+    np = block_sum(np, s_red);
+    nc = block_sum(nc, s_red);
+    if (tid == 0) a.cosv[m] = (np > 0.f && nc > 0.f) ? dot / (sqrtf(np) * sqrtf(nc)) : 0.f;
+  }
+  if (!last_ticket(&a.ctrl->counters[kSelectCounter], (unsigned)(a.n_cb + a.n_chunks))) return;
+
+  // ---- the last CTA: chunk pick, scores, top-k_p.  smem: alpha[n2] | keys[n2]
+  __shared__ int s_chunk;
+  float* cos_s = smem;   // [n_chunks], read before alpha reuses the space
+  for (int m = tid; m < a.n_chunks; m += blockDim.x) cos_s[m] = __ldcg(a.cosv + m);
+  __syncthreads();
+  if (tid == 0) {
+    int best_m = -1;
+    float best = -INFINITY;
+    for (int m = 0; m < a.n_chunks; ++m)   // ascending m: the first wins a tie
+      if (best_m < 0 || cos_s[m] > best) {
+        best = cos_s[m];
+        best_m = m;
+      }
+    s_chunk = best_m;
+  }
+  __syncthreads();
+  const int chunk = a.n_chunks > 0 ? s_chunk : -1;
+  const int cand0 = a.n_chunks > 0 ? chunk * a.ppc : 0;
+  const int n_cand = a.n_chunks > 0 ? a.ppc : a.n_pages;
+  const float inv_sqrt_d = 1.0f / sqrtf((float)a.head_dim);
+  float* alpha = smem;
+  unsigned long long* keys =
+      reinterpret_cast<unsigned long long*>(alpha + ((a.n_cand_max2 + 3) & ~3));
+  if (a.per_head && n_cand <= 32 && a.k_p <= n_cand) {
+    // a set per head with at most 32 candidates: a warp per head sorts its
+    // candidates' keys in registers, then the chosen ones by candidate index
+    for (int h = warp; h < a.n_heads; h += nwarps) {
+      const float my_alpha =
+          lane < n_cand ? __ldcg(a.alpha_part + (size_t)h * a.n_alpha + cand0 + lane) * inv_sqrt_d
+                        : 0.f;
+      unsigned long long key = lane < n_cand ? score_key(my_alpha, (unsigned)lane) : ~0ull;
       key = warp_sort32(key);
       unsigned long long sel = lane < a.k_p ? (key & 0xffffffffull) : ~0ull;
       sel = warp_sort32(sel);
       const int c = lane < a.k_p ? (int)(sel & 0xffffffffull) : 0;
       const float alpha_c = __shfl_sync(0xffffffffu, my_alpha, c);
       if (lane < a.k_p) {
-        a.idx_out[hs * a.k_p + lane] = cand0 + c;
-        if (a.scores_out) a.scores_out[hs * a.k_p + lane] = alpha_c;
+        a.idx_out[h * a.k_p + lane] = cand0 + c;
+        if (a.scores_out) a.scores_out[h * a.k_p + lane] = alpha_c;
       }
     }
-  } else
-  for (int hs = 0; hs < n_sets; ++hs) {
-    const int e0 = a.per_head ? hs * a.head_dim : 0;
-    const int e1 = a.per_head ? e0 + a.head_dim : a.row_elems;
-    for (int c = warp; c < n_cand; c += nwarps) {
-      const float* kb = a.kbar + (size_t)(cand0 + c) * a.row_elems;
-      const float dot = warp_dot(qbar + e0, kb + e0, e1 - e0, nullptr);
-      if (lane == 0) alpha[c] = dot * inv_sqrt_d;
+  } else if (a.per_head) {
+    for (int h = 0; h < a.n_heads; ++h) {
+      for (int c = tid; c < n_cand; c += blockDim.x)
+        alpha[c] = __ldcg(a.alpha_part + (size_t)h * a.n_alpha + cand0 + c) * inv_sqrt_d;
+      __syncthreads();
+      select_topk(alpha, n_cand, a.n_cand_max2, a.k_p, cand0, keys, a.idx_out + h * a.k_p,
+                  a.scores_out ? a.scores_out + h * a.k_p : nullptr);
+    }
+  } else {
+    // one page set: the heads' partial scores added in head order (staged in
+    // shared memory first when they fit, so that all loads are in flight at once)
+    float* stage = alpha + ((a.n_cand_max2 + 3) & ~3) + 2 * a.n_cand_max2;   // past the keys
+    if ((size_t)n_cand * a.n_heads <= (size_t)a.stage_floats) {
+      for (int i = tid; i < n_cand * a.n_heads; i += blockDim.x) {
+        const int h = i / n_cand, c = i % n_cand;
+        stage[i] = __ldcg(a.alpha_part + (size_t)h * a.n_alpha + cand0 + c);
+      }
+      __syncthreads();
+      for (int c = tid; c < n_cand; c += blockDim.x) {
+        float s = 0.f;
+        for (int h = 0; h < a.n_heads; ++h) s += stage[h * n_cand + c];
+        alpha[c] = s * inv_sqrt_d;
+      }
+    } else {
+      for (int c = tid; c < n_cand; c += blockDim.x) {
+        float s = 0.f;
+        for (int h = 0; h < a.n_heads; ++h)
+          s += __ldcg(a.alpha_part + (size_t)h * a.n_alpha + cand0 + c);
+        alpha[c] = s * inv_sqrt_d;
+      }
     }
     __syncthreads();
-    int n2 = 1;
-    while (n2 < n_cand) n2 <<= 1;
-    for (int i = tid; i < n2; i += blockDim.x)
-      keys[i] = i < n_cand ? score_key(alpha[i], (unsigned)i) : ~0ull;
-    __syncthreads();
-    bitonic_sort(keys, n2);
-    // the first k_p keys are the selection; re-sort them by candidate index
-    int k2 = 1;
-    while (k2 < a.k_p) k2 <<= 1;
-    for (int i = tid; i < k2; i += blockDim.x)
-      keys[i] = i < a.k_p ? (keys[i] & 0xffffffffull) : ~0ull;
-    __syncthreads();
-    bitonic_sort(keys, k2);
-    for (int i = tid; i < a.k_p; i += blockDim.x) {
-      const int c = (int)(keys[i] & 0xffffffffull);
-      a.idx_out[hs * a.k_p + i] = cand0 + c;
-      if (a.scores_out) a.scores_out[hs * a.k_p + i] = alpha[c];
-    }
-    __syncthreads();   // alpha and keys are reused by the next set
+    select_topk(alpha, n_cand, a.n_cand_max2, a.k_p, cand0, keys, a.idx_out, a.scores_out);
   }
   if (tid == 0) {
     if (a.chunk_out) a.chunk_out[0] = chunk;
@@ -544,8 +743,86 @@ wa_status summarize_t(const SegIn* in, int n_seg, int row_elems, cudaStream_t st
     if (smem > 48 * 1024)                                                                   \
       cudaFuncSetAttribute(k_page_summarize<T, V>, cudaFuncAttributeMaxDynamicSharedMemorySize, \
                            (int)smem);                                                      \
-    k_page_summarize<T, V><<<grid, p.threads, smem, st>>>(segs, row_elems, p.nvec, p.R,     \
-                                                          sc.ctrl);                         \
+    if (launch_pdl(k_page_summarize<T, V>, grid, dim3(p.threads), smem, st, segs, row_elems, \
+                   p.nvec, p.R, sc.ctrl) != cudaSuccess)                                    \
+      return WA_ERR_CUDA;                                                                   \
+    break;
+    WA_CASE(1) WA_CASE(2) WA_CASE(4) WA_CASE(8)
+#undef WA_CASE
+    default: return WA_ERR_SHAPE;
+  }
+  return cuda_status(cudaPeekAtLastError());
+}
+
+// Launch shape and scratch layout of one selection (SelectArgs fields derived
+// from the problem); returns the scratch floats it needs.
+template <typename T>
+size_t plan_select(SelectArgs& a, Plan* pl) {
+  constexpr int E = VecOf<T>::E;
+  const int d = a.head_dim;
+  // heads per column block: enough for 32 vectors a row (at most 12 row phases
+  // of 384 threads, so a row block of 8 * 12 rows is one batch of loads per
+  // thread), a divisor of n_heads; a head row that is not whole 16-byte vectors
+  // (or is under 32 values) puts all heads in one block
+  if (d % E == 0 && d >= 32) {
+    a.hpb = 1;
+    while (a.hpb * (d / E) < 32 && a.n_heads % (2 * a.hpb) == 0) a.hpb *= 2;
+  } else {
+    a.hpb = a.n_heads;
+  }
+  a.cw = a.hpb * d;
+  a.n_cb = (a.n_heads + a.hpb - 1) / a.hpb;
+  // query tiles and prompt CTAs in about one wave of two CTAs per SM, at least
+  // 16 rows a tile
+  int n_rb = (2 * sm_count() - a.n_chunks) / a.n_cb;
+  const int max_rb = (a.n_q + 15) / 16;
+  if (n_rb > max_rb) n_rb = max_rb;
+  if (n_rb < 1) n_rb = 1;
+  a.rows_per_block = (a.n_q + n_rb - 1) / n_rb;
+  a.n_rb = (a.n_q + a.rows_per_block - 1) / a.rows_per_block;
+  *pl = plan_rows<T>(a.cw);
+  a.nvec = pl->nvec;
+  a.R = pl->R;
+  a.n_alpha = a.n_chunks > 0 ? a.n_chunks * a.ppc : a.n_pages;
+  const int n_cand = a.n_chunks > 0 ? a.ppc : a.n_pages;
+  int n2 = 1;
+  while (n2 < n_cand) n2 <<= 1;
+  a.n_cand_max2 = n2;
+  const size_t part = ((size_t)a.n_cb * a.n_rb * a.cw + 3) & ~(size_t)3;
+  const size_t alpha = ((size_t)a.n_heads * a.n_alpha + 3) & ~(size_t)3;
+  return part + alpha + (((size_t)a.n_chunks + 3) & ~(size_t)3);
+}
+
+// Launch the selection over `scratch` (plan_select's floats) and `ctrl`, whose
+// counters kSelectCounter - n_cb .. kSelectCounter must be zero.
+template <typename T>
+wa_status launch_select(const T* q, SelectArgs a, const Plan& p, float* scratch, Ctrl* ctrl,
+                        cudaStream_t st) {
+  a.partial = scratch;
+  a.alpha_part = scratch + (((size_t)a.n_cb * a.n_rb * a.cw + 3) & ~(size_t)3);
+  a.cosv = a.alpha_part + (((size_t)a.n_heads * a.n_alpha + 3) & ~(size_t)3);
+  a.ctrl = ctrl;
+  // phase A: R rows of cw partial sums; then qbar + the group sums (<= blockDim
+  // float4); final stage: alpha, keys and, when they fit in 16 KiB, the staged scores
+  size_t smem_a = (size_t)p.R * a.cw * sizeof(float);
+  const size_t smem_q = (size_t)a.cw * sizeof(float) + (size_t)p.threads * 16;
+  if (smem_q > smem_a) smem_a = smem_q;
+  const size_t stage = (size_t)a.n_heads * (a.n_chunks > 0 ? a.ppc : a.n_pages);
+  a.stage_floats = stage <= 4096 ? (int)stage : 0;
+  const size_t smem_b = (size_t)((a.n_cand_max2 + 3) & ~3) * 4 + (size_t)a.n_cand_max2 * 8 +
+                        (size_t)a.stage_floats * 4;
+  size_t smem = smem_a > smem_b ? smem_a : smem_b;
+  if (smem < (size_t)a.n_chunks * sizeof(float)) smem = (size_t)a.n_chunks * sizeof(float);
+  const unsigned grid = (unsigned)(a.n_cb * a.n_rb + a.n_chunks);
+  switch (p.vpt) {
+#define WA_CASE(V)                                                                          \
+  case V:                                                                                   \
+    if (smem > 48 * 1024)                                                                   \
+      cudaFuncSetAttribute(k_select_pages<T, V>, cudaFuncAttributeMaxDynamicSharedMemorySize, \
+                           (int)smem);                                                      \
+    if (launch_pdl(k_select_pages<T, V>, dim3(grid), dim3(p.threads), smem, st, q, a) !=     \
+        cudaSuccess)                                                                        \
+      return WA_ERR_CUDA;                                                                   \
     break;
     WA_CASE(1) WA_CASE(2) WA_CASE(4) WA_CASE(8)
 #undef WA_CASE
@@ -556,43 +833,12 @@ wa_status summarize_t(const SegIn* in, int n_seg, int row_elems, cudaStream_t st
 
 template <typename T>
 wa_status select_t(const T* q, SelectArgs a, cudaStream_t st) {
-  Plan p = plan_rows<T>(a.row_elems);
-  int splits = a.n_q / 32;
-  if (splits < 1) splits = 1;
-  if (splits > 304) splits = 304;
-  const int rps = (a.n_q + splits - 1) / splits;
-  splits = (a.n_q + rps - 1) / rps;
+  Plan p;
+  const size_t floats = plan_select<T>(a, &p);
   Scratch sc;
-  const int n_groups = (splits + kGroup - 1) / kGroup;
-  wa_status rc = get_scratch((size_t)(splits + n_groups) * a.row_elems * sizeof(float), &sc);
+  wa_status rc = get_scratch(floats * sizeof(float), &sc);
   if (rc != WA_OK) return rc;
-  int n_cand = a.n_chunks > 0 ? a.ppc : a.n_pages;
-  int n2 = 1;
-  while (n2 < n_cand) n2 <<= 1;
-  a.nvec = p.nvec;
-  a.R = p.R;
-  a.splits = splits;
-  a.rows_per_split = rps;
-  a.partial = (float*)sc.data;
-  a.ctrl = sc.ctrl;
-  a.n_cand_max2 = n2;
-  size_t smem_a = (size_t)p.R * a.row_elems * sizeof(float);
-  size_t smem_b = (size_t)((a.row_elems + 3) & ~3) * 4 + (size_t)((n2 + 3) & ~3) * 4 +
-                  (size_t)n2 * 8;
-  size_t smem = smem_a > smem_b ? smem_a : smem_b;
-  switch (p.vpt) {
-#define WA_CASE(V)                                                                          \
-  case V:                                                                                   \
-    if (smem > 48 * 1024)                                                                   \
-      cudaFuncSetAttribute(k_select_pages<T, V>, cudaFuncAttributeMaxDynamicSharedMemorySize, \
-                           (int)smem);                                                      \
-    k_select_pages<T, V><<<splits, p.threads, smem, st>>>(q, a);                            \
-    break;
-    WA_CASE(1) WA_CASE(2) WA_CASE(4) WA_CASE(8)
-#undef WA_CASE
-    default: return WA_ERR_SHAPE;
-  }
-  return cuda_status(cudaPeekAtLastError());
+  return launch_select<T>(q, a, p, static_cast<float*>(sc.data), sc.ctrl, st);
 }
 
 }  // namespace
@@ -623,6 +869,7 @@ wa_status launch_select_pages(const void* q, wa_dtype dt, int n_q, int n_heads, 
   a.per_head = per_head;
   a.n_q = n_q;
   a.row_elems = n_heads * head_dim;
+  a.n_heads = n_heads;
   a.kbar = kbar;
   a.n_pages = n_pages;
   a.head_dim = head_dim;
@@ -683,50 +930,18 @@ wa_status noalloc_scratch(unsigned char** out) {
 
 template <typename T>
 wa_status select_noalloc_t(const T* q, SelectArgs a, cudaStream_t st) {
-  Plan p = plan_rows<T>(a.row_elems);
-  int splits = a.n_q / 32;   // the split rule of the allocating entry point
-  if (splits < 1) splits = 1;
-  if (splits > 304) splits = 304;
-  const int rps = (a.n_q + splits - 1) / splits;
-  splits = (a.n_q + rps - 1) / rps;
-  const int n_groups = (splits + kGroup - 1) / kGroup;
-  if ((size_t)(splits + n_groups) * a.row_elems * sizeof(float) > kNoAllocPartialBytes)
-    return WA_ERR_SHAPE;
+  Plan p;
+  const size_t floats = plan_select<T>(a, &p);   // the layout of the allocating entry point
+  if (floats * sizeof(float) > kNoAllocPartialBytes) return WA_ERR_SHAPE;
   unsigned char* base = nullptr;
   wa_status rc = noalloc_scratch(&base);
   if (rc != WA_OK) return rc;
   Ctrl* ctrl = reinterpret_cast<Ctrl*>(base);
   // the ticket counters must start at zero; the array keeps the last call's contents
-  if (cudaMemsetAsync(&ctrl->counters[kSelectCounter - n_groups], 0,
-                      (n_groups + 1) * sizeof(unsigned), st) != cudaSuccess)
+  if (cudaMemsetAsync(&ctrl->counters[kSelectCounter - a.n_cb], 0,
+                      (a.n_cb + 1) * sizeof(unsigned), st) != cudaSuccess)
     return WA_ERR_CUDA;
-  int n_cand = a.n_chunks > 0 ? a.ppc : a.n_pages;
-  int n2 = 1;
-  while (n2 < n_cand) n2 <<= 1;
-  a.nvec = p.nvec;
-  a.R = p.R;
-  a.splits = splits;
-  a.rows_per_split = rps;
-  a.partial = reinterpret_cast<float*>(base + kNoAllocCtrlBytes);
-  a.ctrl = ctrl;
-  a.n_cand_max2 = n2;
-  size_t smem_a = (size_t)p.R * a.row_elems * sizeof(float);
-  size_t smem_b = (size_t)((a.row_elems + 3) & ~3) * 4 + (size_t)((n2 + 3) & ~3) * 4 +
-                  (size_t)n2 * 8;
-  size_t smem = smem_a > smem_b ? smem_a : smem_b;
-  switch (p.vpt) {
-#define WA_CASE(V)                                                                          \
-  case V:                                                                                   \
-    if (smem > 48 * 1024)                                                                   \
-      cudaFuncSetAttribute(k_select_pages<T, V>, cudaFuncAttributeMaxDynamicSharedMemorySize, \
-                           (int)smem);                                                      \
-    k_select_pages<T, V><<<splits, p.threads, smem, st>>>(q, a);                            \
-    break;
-    WA_CASE(1) WA_CASE(2) WA_CASE(4) WA_CASE(8)
-#undef WA_CASE
-    default: return WA_ERR_SHAPE;
-  }
-  return cuda_status(cudaPeekAtLastError());
+  return launch_select<T>(q, a, p, reinterpret_cast<float*>(base + kNoAllocCtrlBytes), ctrl, st);
 }
 
 inline bool aligned16_ptr(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -760,6 +975,7 @@ extern "C" wa_status wa_select_pages_noalloc(const void* q, wa_dtype dt, int n_q
   SelectArgs a{};
   a.n_q = n_q;
   a.row_elems = (int)row;
+  a.n_heads = n_heads;
   a.kbar = kbar;
   a.n_pages = n_pages;
   a.head_dim = head_dim;

@@ -42,6 +42,33 @@ wa_status get_ctrl(Ctrl** out);
 
 inline wa_status cuda_status(cudaError_t e) { return e == cudaSuccess ? WA_OK : WA_ERR_CUDA; }
 
+// Programmatic dependent launch.  The kernels of one chunk (summaries,
+// selection, gather, attention) are launched with the programmatic-stream-
+// serialization attribute, so that the launch of a kernel overlaps the drain of
+// the previous kernel on the stream; each such kernel calls pdl_wait() before
+// its first access to global memory, which returns once every earlier kernel
+// on the stream has finished and its writes are visible (it is a no-op for a
+// kernel launched without the attribute).  None of them triggers its
+// dependents early: measured on the one-layer WorldAttention step, CTAs of the
+// next kernel placed while a kernel still ran made the step 36 us slower,
+// while launching at grid completion made it 10 us faster than no attribute.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                              cudaStream_t s, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
+
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 inline int sm_count() {

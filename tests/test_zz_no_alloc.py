@@ -90,12 +90,14 @@ def test_noalloc_select_matches_allocating_entry_point_twice():
 
 def test_noalloc_select_rejects_requests_beyond_its_array():
     fn = _noalloc_fn()
-    # 8192-wide fp32 rows with 9,728 queries need 304 x 32 KiB of partial sums
+    # 64 heads scoring 8,192 pages without a prompt stage need 64 x 8,192 floats
+    # of per-head partial scores plus 5 row blocks x 8,192 of query partials:
+    # more than the 2 MiB array (the buffers are real, though nothing runs)
     q = torch.empty((9728, 64, 128), dtype=torch.float32, device=DEV)
-    kbar = torch.empty((8, 64, 128), dtype=torch.float32, device=DEV)
+    kbar = torch.empty((8192, 64, 128), dtype=torch.float32, device=DEV)
     idx = torch.empty(2, dtype=torch.int32, device=DEV)
     stream = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
-    st = fn(_p(q), 0, 9728, 64, 128, _p(kbar), 8, None, None, 0, 0, 1, 2, _p(idx), None, None,
+    st = fn(_p(q), 0, 9728, 64, 128, _p(kbar), 8192, None, None, 0, 0, 1, 2, _p(idx), None, None,
             stream)
     assert st == 2   # WA_ERR_SHAPE, nothing enqueued
 
