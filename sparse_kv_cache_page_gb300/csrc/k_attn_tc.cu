@@ -89,6 +89,7 @@ struct Bars {
   uint64_t p_ready[2];      // P_i(j) written
   uint64_t o_ready[2];      // O_i += P_i(j) V_j done
   uint64_t drain;
+  uint64_t comb;            // bulk copy of another split's rows (split combine)
   uint32_t tmem_base;
   int abort_flag;
   unsigned ticket;
@@ -190,8 +191,9 @@ __device__ __forceinline__ void put4(__nv_bfloat16* dst, float4 x, bool acc, flo
 // (floats): 528-byte rows put the 32 rows a warp writes at once on distinct
 // bank groups.
 constexpr int kStagePitch = HD + 4;
-constexpr int kCombineRegs = 4;   // splits whose weights and partials a combine holds in registers
-static_assert(256 * kStagePitch * 4 <= SmemLayout::bars, "staging overlays Q and the ring only");
+constexpr int kMaxSplit = 16;     // ticket and done counts share one 32-bit counter
+static_assert(256 * kStagePitch * 4 + 128 * HD * 4 + kMaxSplit * 256 * 4 <= SmemLayout::bars,
+              "staging, the combine buffer and the split weights overlay Q and the ring only");
 
 template <typename OutT, bool kLse, bool kSparse>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -226,6 +228,7 @@ k_block_attn_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
       mbar_init(&bars->o_ready[i], 1);
     }
     mbar_init(&bars->drain, 2);
+    mbar_init(&bars->comb, 1);
     bars->abort_flag = 0;
     fence_mbar_init();
   }
@@ -507,17 +510,22 @@ k_block_attn_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         }
       }
     } else {
-      // split: the CTA's unnormalised rows go to scratch through shared memory
-      // (each thread stages its TMEM row, then a warp stores one 512-byte row
-      // per instruction), and the CTA that finishes last for its (head, query
-      // pair) combines the splits with the same row-per-warp access, its own
-      // rows read back from the staging area.  Q and the K/V ring are idle
-      // once the loop is done (every copy landed and every MMA completed), so
-      // the staging area overlays them.
+      // split: the unit's (head, query pair) key ranges meet through one
+      // counter.  Each CTA takes an arrival ticket (low 16 bits); the last to
+      // arrive combines, the others store their unnormalised rows and (m, l, lx)
+      // to scratch and then count themselves done (high 16 bits).  The last CTA
+      // waits (bounded) for the done count -- every CTA it waits for holds an
+      // earlier ticket, so it is running and the wait is short -- and never
+      // stores its own partial: its row statistics stay in registers and its
+      // rows in the staging area.  It brings each other split's rows into shared
+      // memory with bulk copies (64 KiB, half of the rows, at a time) and adds
+      // the splits in split order, the same arithmetic as adding stored partials.
       const int unit = head * p.n_qpairs + qpair;
-      const int prow = qt * BM + row;                     // 0..255
-      const int sw = threadIdx.x >> 5;                    // softmax warp 0..7: rows 32 sw ..
+      const int prow = qt * BM + row;                     // 0..255 (= threadIdx.x)
+      const int sw = threadIdx.x >> 5;                    // softmax warp 0..7
       float* stage = reinterpret_cast<float*>(smem);      // [256][kStagePitch]
+      float* cbuf = stage + 256 * kStagePitch;            // [128][HD]: one split's half
+      float* wts = cbuf + 128 * HD;                       // [n_split][256] row weights
       const bool all_ok = softmax_all(staging_ok);
       if (all_ok) {
         float* mine = stage + (size_t)prow * kStagePitch;
@@ -537,101 +545,141 @@ k_block_attn_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             d4[v] = make_float4(__uint_as_float(orow[4 * v]), __uint_as_float(orow[4 * v + 1]),
                                 __uint_as_float(orow[4 * v + 2]), __uint_as_float(orow[4 * v + 3]));
         }
-        __stcg(p.part_ml + ((size_t)unit * p.n_split + split) * 256 + prow, make_float4(m, l, lx, 0.f));
-        softmax_bar();
-        float* dst = p.part_o + ((size_t)unit * p.n_split + split) * 256 * HD;
-#pragma unroll 4
-        for (int rr = 0; rr < 32; ++rr) {
-          const int r = 32 * sw + rr;
-          __stcg(reinterpret_cast<float4*>(dst + (size_t)r * HD) + lane,
-                 reinterpret_cast<const float4*>(stage + (size_t)r * kStagePitch)[lane]);
-        }
       }
-      __threadfence();
       softmax_bar();
-      // every CTA takes its ticket (even after an abort) so the counter returns to 0
       if (threadIdx.x == 0) bars->ticket = atomicAdd(&p.counters[unit], 1u);
       softmax_bar();
-      const bool last = bars->ticket == (unsigned)(p.n_split - 1);
-      if (last) {
-        __threadfence();
-        if (threadIdx.x == 0) p.counters[unit] = 0u;
+      const bool last = (bars->ticket & 0xffffu) == (unsigned)(p.n_split - 1);
+      if (!last) {
         if (all_ok) {
-          // each lane first weighs the splits of one row (row 32 sw + lane), the
-          // arithmetic of a per-row combine; then the warp combines its 32 rows
-          // four at a time, their partials all loaded before any is summed
-          const int rj = 32 * sw + lane;
-          const float4* mlj = p.part_ml + (size_t)unit * p.n_split * 256 + rj;
+          __stcg(p.part_ml + ((size_t)unit * p.n_split + split) * 256 + prow,
+                 make_float4(m, l, lx, 0.f));
+          float* dst = p.part_o + ((size_t)unit * p.n_split + split) * 256 * HD;
+#pragma unroll 4
+          for (int rr = 0; rr < 32; ++rr) {
+            const int r = 32 * sw + rr;
+            __stcg(reinterpret_cast<float4*>(dst + (size_t)r * HD) + lane,
+                   reinterpret_cast<const float4*>(stage + (size_t)r * kStagePitch)[lane]);
+          }
+        }
+        __threadfence();
+        softmax_bar();
+        if (threadIdx.x == 0) atomicAdd(&p.counters[unit], 1u << 16);
+      } else {
+        if (threadIdx.x == 0) {
+          volatile unsigned* cnt = &p.counters[unit];
+          const unsigned need = (unsigned)(p.n_split - 1);
+          bool done = (*cnt >> 16) >= need;
+          const unsigned long long t0 = globaltimer();
+          for (uint32_t it = 1; !done; ++it) {
+            __nanosleep(64);
+            done = (*cnt >> 16) >= need;
+            if (!done && (it & 63u) == 0 && globaltimer() - t0 > p.wait_ns) break;
+          }
+          if (done) {
+            __threadfence();
+            // the bulk copies below read, through the async proxy, what the other
+            // splits stored through the generic one
+            asm volatile("fence.proxy.async.global;" ::: "memory");
+            *cnt = 0u;
+          } else {
+            atomicOr(p.status, kStatusTimeout);
+          }
+          bars->ticket = done ? 1u : 0u;
+        }
+        softmax_bar();
+        bool go = all_ok && bars->ticket == 1u;
+        __threadfence();
+        if (go) {
+          // this thread's row: statistics of every split (its own from registers),
+          // the common maximum, the denominators, the LSE and the split weights
+          const float4* mlp = p.part_ml + (size_t)unit * p.n_split * 256 + prow;
           float mm = -INFINITY;
-          for (int s = 0; s < p.n_split; ++s) mm = fmaxf(mm, __ldcg(mlj + (size_t)s * 256).x);
+          for (int s = 0; s < p.n_split; ++s)
+            mm = fmaxf(mm, s == split ? m : __ldcg(mlp + (size_t)s * 256).x);
           const bool none = !(mm > -INFINITY);   // no keys in any split: O = 0, LSE = -inf
           float den = 0.f, denx = 0.f;
           for (int s = 0; s < p.n_split; ++s) {
-            const float4 t = __ldcg(mlj + (size_t)s * 256);
+            const float4 t = s == split ? make_float4(m, l, lx, 0.f) : __ldcg(mlp + (size_t)s * 256);
             const float w = none ? 0.f : ex2((t.x - mm) * sl2);
             den += w * t.y;
             denx += w * t.z;
           }
           const float wn = none ? 0.f : wn0 / den;
-          float wj[kCombineRegs];
+          for (int s = 0; s < p.n_split; ++s) {
+            const float ms = s == split ? m : __ldcg(mlp + (size_t)s * 256).x;
+            wts[s * 256 + prow] = none ? 0.f : ex2((ms - mm) * sl2) * wn;
+          }
+          if (kLse && p.lse && q0 + prow < p.n_q)
+            p.lse[(size_t)head * p.n_q + q0 + prow] = none ? -INFINITY : mm * p.scale + logf(denx);
+        }
+        softmax_bar();
+        // rows in two halves of 128; warp sw adds rows 128 h + 16 sw .. + 15,
+        // lane = four output columns
+        uint32_t cphase = 0;
+        for (int h = 0; go && h < 2; ++h) {
+          float4 x[16];
 #pragma unroll
-          for (int s = 0; s < kCombineRegs; ++s)
-            wj[s] = (s < p.n_split && !none) ? ex2((__ldcg(mlj + (size_t)s * 256).x - mm) * sl2) * wn
-                                              : 0.f;
-          if (kLse && p.lse && q0 + rj < p.n_q)
-            p.lse[(size_t)head * p.n_q + q0 + rj] = none ? -INFINITY : mm * p.scale + logf(denx);
-          const float* part = p.part_o + (size_t)unit * p.n_split * 256 * HD;
-          for (int r0 = 0; r0 < 32; r0 += 4) {
-            if (q0 + 32 * sw + r0 >= p.n_q) break;        // rows ascend (warp-uniform)
-            float4 t[4][kCombineRegs];
-#pragma unroll
-            for (int u = 0; u < 4; ++u) {
-              const int r = 32 * sw + r0 + u;
-#pragma unroll
-              for (int s = 0; s < kCombineRegs; ++s)
-                if (s < p.n_split)
-                  t[u][s] = s == split
-                                ? reinterpret_cast<const float4*>(stage + (size_t)r * kStagePitch)[lane]
-                                : __ldcg(reinterpret_cast<const float4*>(
-                                             part + ((size_t)s * 256 + r) * HD) + lane);
+          for (int i = 0; i < 16; ++i) x[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+          for (int s = 0; go && s < p.n_split; ++s) {
+            const float* src;
+            int pitch;
+            if (s == split) {
+              src = stage + (size_t)(128 * h) * kStagePitch;
+              pitch = kStagePitch;
+            } else {
+              if (threadIdx.x == 0) {
+                mbar_arrive_expect_tx(&bars->comb, 128 * HD * 4);
+                bulk_g2s(cbuf, p.part_o + (((size_t)unit * p.n_split + s) * 256 + 128 * h) * HD,
+                         128 * HD * 4, &bars->comb);
+              }
+              go = softmax_all(mbar_wait(&bars->comb, cphase & 1, abort_flag, p.status, p.wait_ns));
+              // a wait that gave up: the copy still lands before the CTA leaves
+              if (!go) mbar_wait_drain(&bars->comb, cphase & 1, 100000000ull);
+              ++cphase;
+              src = cbuf;
+              pitch = HD;
             }
+            if (go) {
 #pragma unroll
-            for (int u = 0; u < 4; ++u) {
-              const int r = 32 * sw + r0 + u;
-              const int grow_r = q0 + r;
-              if (grow_r >= p.n_q) break;
-              float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
+              for (int i = 0; i < 16; ++i) {
+                const int r = 16 * sw + i;
+                const float w = wts[s * 256 + 128 * h + r];
+                const float4 y = reinterpret_cast<const float4*>(src + (size_t)r * pitch)[lane];
+                x[i].x += w * y.x;
+                x[i].y += w * y.y;
+                x[i].z += w * y.z;
+                x[i].w += w * y.w;
+              }
+            }
+            if (s != split) {
+              // the buffer's readers finish before the next copy overwrites it
+              fence_proxy_async_smem();
+              softmax_bar();
+            }
+          }
+          if (go) {
+            // four rows at a time: with output fusion their old values are all
+            // loaded before any is written
+            const bool acc = p.accumulate != 0;
 #pragma unroll
-              for (int s = 0; s < kCombineRegs; ++s) {
-                if (s < p.n_split) {
-                  const float w = __shfl_sync(0xffffffffu, wj[s], r0 + u);
-                  x.x += w * t[u][s].x;
-                  x.y += w * t[u][s].y;
-                  x.z += w * t[u][s].z;
-                  x.w += w * t[u][s].w;
-                }
+            for (int i0 = 0; i0 < 16; i0 += 4) {
+              float4 old[4];
+#pragma unroll
+              for (int u = 0; u < 4; ++u) {
+                const int grow_r = q0 + 128 * h + 16 * sw + i0 + u;
+                old[u] = (acc && grow_r < p.n_q)
+                             ? load4(static_cast<OutT*>(p.o) +
+                                     ((size_t)grow_r * p.n_heads + head) * HD + 4 * lane)
+                             : make_float4(0.f, 0.f, 0.f, 0.f);
               }
-              // more splits than registers (a forced split count): weights from the row's lane
-              const float mm_r = __shfl_sync(0xffffffffu, mm, r0 + u);
-              const float wn_r = __shfl_sync(0xffffffffu, wn, r0 + u);
-              const float4* ml_r = p.part_ml + (size_t)unit * p.n_split * 256 + r;
-              for (int s = kCombineRegs; s < p.n_split; ++s) {
-                const float w = !(mm_r > -INFINITY)
-                                    ? 0.f
-                                    : ex2((__ldcg(ml_r + (size_t)s * 256).x - mm_r) * sl2) * wn_r;
-                const float4 ts = s == split
-                                      ? reinterpret_cast<const float4*>(
-                                            stage + (size_t)r * kStagePitch)[lane]
-                                      : __ldcg(reinterpret_cast<const float4*>(
-                                                   part + ((size_t)s * 256 + r) * HD) + lane);
-                x.x += w * ts.x;
-                x.y += w * ts.y;
-                x.z += w * ts.z;
-                x.w += w * ts.w;
+#pragma unroll
+              for (int u = 0; u < 4; ++u) {
+                const int grow_r = q0 + 128 * h + 16 * sw + i0 + u;
+                if (grow_r < p.n_q)
+                  put4(static_cast<OutT*>(p.o) + ((size_t)grow_r * p.n_heads + head) * HD + 4 * lane,
+                       x[i0 + u], acc, old[u], wo);
               }
-              OutT* dst = static_cast<OutT*>(p.o) + ((size_t)grow_r * p.n_heads + head) * HD + 4 * lane;
-              const bool acc = p.accumulate != 0;
-              put4(dst, x, acc, acc ? load4(dst) : x, wo);
             }
           }
         }
@@ -782,6 +830,7 @@ wa_status launch_attn_tc(const void* q, int n_q, const void* k_main, const void*
     int f = atoi(env);
     const int nkv = nkv_max;
     if (f >= 1) p.n_split = f > nkv ? nkv : f;
+    if (p.n_split > kMaxSplit) p.n_split = kMaxSplit;
     if ((size_t)p.n_qpairs * n_heads > (size_t)kMaxUnits) p.n_split = 1;
   }
   if (max_split > 0 && p.n_split > max_split) p.n_split = max_split;
