@@ -548,8 +548,7 @@ def run_hsa(args, world, rank, local):
         "roofline": {"bound": "tensor", "achieved": round(sp_tflops, 1), "peak": tf_peak,
                      "unit": "TFLOP/s", "frac": round(sp_tflops / tf_peak, 4), "traffic": None,
                      "peak_source": peak_src, "frac_of_sustained": round(sp_tflops / tf_sus, 4),
-                     "kernel": "k_block_attn_tc (block-sparse form)",
-                     "peak_source": f"{src} bf16 sustained"},
+                     "kernel": "k_block_attn_tc (block-sparse form)"},
         # per step: summaries, select, gather, block means (one launch), pooled scores,
         # block select, sparse tiles, block-sparse attention, projection, reduce,
         # low-rank attention
