@@ -40,6 +40,9 @@ H, D, P, N_PAGES, PPC, N_CHUNKS, PDIM, KP, NQ, NLOC = 12, 128, 12480, 40, 8, 5, 
 # DRAM bytes read + written per launch of the attention kernel, from one ncu capture of the
 # current kernel (profiles/attention_worldattention_1layer.md); None once the kernel changes.
 ATTN_TRAFFIC_BYTES = 393.85e6
+# the same for the gather+attention launch, the kernel's paged form
+# (profiles/gather_attention_worldattention_1layer.md)
+FUSED_TRAFFIC_BYTES = 677.97e6
 
 
 def attn_flops(n_q, n_kv, d, h):
@@ -184,6 +187,11 @@ def run_gpu(args, world, rank, local, hybrid=False, per_head=False):
             wa.wa_gather_pages_per_head(kp, vp, idx_, kbuf, vbuf)
         else:
             wa.wa_gather_pages(kp, vp, idx_, None, kbuf, vbuf)
+
+    def gather_attn(q_, idx_, kl_, vl_, o_):
+        # gather and attention in one launch: the attention's tile copies read
+        # the selected pages, and the buffer is written from on-chip memory
+        wa.wa_gather_attn(q_, kp, vp, idx_, kl_, vl_, o_, kbuf, vbuf)
     stream = torch.cuda.current_stream()
     L, RANK = KP * P + NLOC, 256
     if hybrid:
@@ -192,36 +200,47 @@ def run_gpu(args, world, rank, local, hybrid=False, per_head=False):
         ev = synth.normal((H, L, RANK), synth.seed_of("hybrid", "ev"), dev, torch.bfloat16,
                           std=L ** -0.5)
 
-    names = ("summarize", "select", "gather", "attention") + (("linear",) if hybrid else ())
+    def names_of(fused):
+        return (("summarize", "select") + (("gather_attention",) if fused else ("gather", "attention"))
+                + (("linear",) if hybrid else ()))
 
     def summarize(n_summ):
         # n_summ = N_PAGES: every cached page (the worst case); n_summ = PPC:
         # only the newest chunk's pages, as when summaries are taken at insert
         wa.wa_page_summarize(kp[N_PAGES - n_summ:], kbar[N_PAGES - n_summ:])
 
-    def step(marks=None, n_summ=N_PAGES):
-        def mark(i):
+    def step(marks=None, n_summ=N_PAGES, fused=True):
+        """One chunk: summaries, retrieval, gather and attention (one launch,
+        or, with fused=False, the gather and the attention as two)."""
+        n = [0]
+
+        def mark():
             if marks is not None:
-                marks[i].record(stream)
-        mark(0)
+                marks[n[0]].record(stream)
+            n[0] += 1
+        mark()
         summarize(n_summ)
-        mark(1)
+        mark()
         select(q, kbar, pcur, pch, PPC, KP, idx)
-        mark(2)
-        gather(idx)
-        mark(3)
-        wa.wa_block_attn(q, kbuf, vbuf, kl, vl, o)
-        mark(4)
+        mark()
+        if fused:
+            gather_attn(q, idx, kl, vl, o)
+        else:
+            gather(idx)
+            mark()
+            wa.wa_block_attn(q, kbuf, vbuf, kl, vl, o)
+        mark()
         if hybrid:
             wa.wa_linear_branch(q, kbuf, vbuf, kl, vl, ek, ev, o)
-            mark(5)
+            mark()
 
-    def timed_steps(n_summ, clk=None, marked=False):
+    def timed_steps(n_summ, clk=None, marked=False, fused=True):
         """Time args.steps steps; with `marked`, an event between every two
         kernels gives the per-kernel intervals (the events also serialise the
         kernels' launches, so the headline total is taken without them)."""
+        names = names_of(fused)
         for _ in range(args.warmup):
-            step(n_summ=n_summ)
+            step(n_summ=n_summ, fused=fused)
         wa.wa_check()
         evs = [[torch.cuda.Event(enable_timing=True) for _ in range(len(names) + 1)]
                for _ in range(args.steps)] if marked else None
@@ -232,7 +251,7 @@ def run_gpu(args, world, rank, local, hybrid=False, per_head=False):
             t1 = torch.cuda.Event(enable_timing=True)
             t0.record(stream)
             for k in range(args.steps):
-                step(evs[k] if marked else None, n_summ=n_summ)
+                step(evs[k] if marked else None, n_summ=n_summ, fused=fused)
             t1.record(stream)
             torch.cuda.synchronize()
         barrier(world)
@@ -252,6 +271,10 @@ def run_gpu(args, world, rank, local, hybrid=False, per_head=False):
     total_ins, _ = timed_steps(PPC)
     ms_step_ins = total_ins / args.steps
     _, per_ins = timed_steps(PPC, marked=True)
+    # the same step with the gather and the attention as two launches
+    total_two, _ = timed_steps(N_PAGES, fused=False)
+    ms_step_two = total_two / args.steps
+    _, per_two = timed_steps(N_PAGES, marked=True, fused=False)
 
     # end to end through the public API: per step, the chunk's inputs come from
     # pinned host memory and the output goes back to pinned host memory.  The
@@ -297,9 +320,8 @@ def run_gpu(args, world, rank, local, hybrid=False, per_head=False):
             summarize(n_summ)
             stream.wait_event(ev_in[k])
             select(dq, kbar, dpc, pch, PPC, KP, idx)
-            gather(idx)
             ev_attn[k].record(stream)
-            wa.wa_block_attn(dq, kbuf, vbuf, dkl, dvl, do)
+            gather_attn(dq, idx, dkl, dvl, do)
             if hybrid:
                 wa.wa_linear_branch(dq, kbuf, vbuf, dkl, dvl, ek, ev, do)
             ev_done[k].record(stream)
@@ -338,13 +360,14 @@ def run_gpu(args, world, rank, local, hybrid=False, per_head=False):
     tf_peak, peak_src = tensor_peak(total_ms)
     n_kv = KP * P + NLOC
     flops = attn_flops(NQ, n_kv, D, H)
-    attn_tflops = flops / (per["attention"] * 1e-3) / 1e12
+    attn_tflops = flops / (per["gather_attention"] * 1e-3) / 1e12
+    attn_tflops_two = flops / (per_two["attention"] * 1e-3) / 1e12
     context = None if (hybrid or per_head or args.no_context) else sdpa_context(q, kbuf, vbuf, kl,
                                                                                 vl, flops)
     gather_bytes = 2 * 2 * KP * P * H * D * 2          # K and V, read + write
     summ_bytes = N_PAGES * P * H * D * 2
     value = world * flops / (ms_step * 1e-3) / 1e12
-    launches_per_step = 4 + (3 if hybrid else 0)
+    launches_per_step = 3 + (3 if hybrid else 0)
     line = {
         "metric": METRIC,
         "value": round(value, 2),
@@ -371,19 +394,32 @@ def run_gpu(args, world, rank, local, hybrid=False, per_head=False):
                                    f"{N_PAGES} summaries, gather and attention",
         "kernels_ms_insert": {k: round(v, 4) for k, v in per_ins.items()},
         "value_insert": round(world * flops / (ms_step_ins * 1e-3) / 1e12, 2),
+        "chunk_latency_ms_two_launch": round(ms_step_two, 4),
+        "two_launch_is": "the same step with the gather and the attention as separate launches "
+                         "(wa_gather_pages, then wa_block_attn over the buffer)",
+        "kernels_ms_two_launch": {k: round(v, 4) for k, v in per_two.items()},
         "attn_tflops": round(attn_tflops, 1),
-        "gather_gbs": round(gather_bytes / (per["gather"] * 1e-3) / 1e9, 1),
+        "attn_tflops_is": "attention FLOPs / the gather+attention launch (which also writes the "
+                          "gathered buffer)",
+        "attn_tflops_two_launch": round(attn_tflops_two, 1),
+        "gather_gbs": round(gather_bytes / (per_two["gather"] * 1e-3) / 1e9, 1),
         "summarize_gbs": round(summ_bytes / (per["summarize"] * 1e-3) / 1e9, 1),
         "roofline": {"bound": "tensor", "achieved": round(attn_tflops, 1), "peak": tf_peak,
                      "unit": "TFLOP/s", "frac": round(attn_tflops / tf_peak, 4),
-                     "traffic": ATTN_TRAFFIC_BYTES if not hybrid else None,
-                     "kernel": "k_block_attn_tc", "peak_source": peak_src,
-                     "frac_of_sustained": round(attn_tflops / tf_sus, 4)},
+                     "traffic": FUSED_TRAFFIC_BYTES if not hybrid else None,
+                     "kernel": "k_block_attn_tc, paged form (gather fused)",
+                     "peak_source": peak_src,
+                     "frac_of_sustained": round(attn_tflops / tf_sus, 4),
+                     "two_launch_attention": {"kernel": "k_block_attn_tc",
+                                              "achieved": round(attn_tflops_two, 1),
+                                              "frac": round(attn_tflops_two / tf_peak, 4),
+                                              "traffic": ATTN_TRAFFIC_BYTES if not hybrid
+                                              else None}},
         "e2e": {"value": round(world * flops / (e2e_ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
                 "ms_per_step": round(e2e_ms, 4), "h2d_bytes_per_step": h2d_bytes,
                 "d2h_bytes_per_step": d2h, "copies": "copy stream, double-buffered: a step's inputs "
                                                        "and the step before's output travel during "
-                                                       "the previous step's attention",
+                                                       "the previous step's gather+attention",
                 "ms_per_step_insert": round(e2e_ms_ins, 4),
                 "value_insert": round(world * flops / (e2e_ms_ins * 1e-3) / 1e12, 2)},
         "gpu_launches": launches_per_step * args.steps,
@@ -666,11 +702,11 @@ def run_cache(args, world, rank, local):
 
 
 def run_one_kernel(args, local):
-    """One kernel alone at the workload's shape (inputs drawn directly, no page
-    bank): the attention over a 49,920-token buffer + 4,680 local tokens, the
-    gather of 4 pages from a 12-page bank, or a page codec (FP8 / NVFP4) encoding
-    and decoding 8 pages (307 MB of bf16, larger than L2).  Used for profiling
-    captures."""
+    """One kernel alone at the workload's shape (inputs drawn directly): the
+    attention over a 49,920-token buffer + 4,680 local tokens, the gather of 4
+    pages from a 12-page bank, both in one launch (gather_attention), or a page
+    codec (FP8 / NVFP4) encoding and decoding 8 pages (307 MB of bf16, larger
+    than L2).  Used for profiling captures."""
     import torch
 
     import sparse_kv_cache_page_gb300 as wa
@@ -686,6 +722,15 @@ def run_one_kernel(args, local):
         kl, vl = g((NLOC, H, D), "kl"), g((NLOC, H, D), "vl")
         o = torch.empty(q.shape, dtype=torch.float32, device=dev)
         fn = lambda: wa.wa_block_attn(q, kb, vb, kl, vl, o)  # noqa: E731
+        work, unit = attn_flops(NQ, KP * P + NLOC, D, H) / 1e12, "TFLOP/s"
+    elif args.kernel == "gather_attention":
+        kp, vp = g((12, P, H, D), "kp"), g((12, P, H, D), "vp")
+        idx = torch.tensor([9, 2, 5, 11], dtype=torch.int32, device=dev)
+        q, kl, vl = g((NQ, H, D), "q"), g((NLOC, H, D), "kl"), g((NLOC, H, D), "vl")
+        kb = torch.empty((KP * P, H, D), dtype=torch.bfloat16, device=dev)
+        vb = torch.empty_like(kb)
+        o = torch.empty(q.shape, dtype=torch.float32, device=dev)
+        fn = lambda: wa.wa_gather_attn(q, kp, vp, idx, kl, vl, o, kb, vb)  # noqa: E731
         work, unit = attn_flops(NQ, KP * P + NLOC, D, H) / 1e12, "TFLOP/s"
     elif args.kernel == "linear":
         L, R = KP * P + NLOC, 256
@@ -1084,7 +1129,8 @@ def main():
     ap.add_argument("--no-context", action="store_true",
                     help="skip the PyTorch attention context timing")
     ap.add_argument("--kernel", default="all",
-                    choices=["all", "attention", "gather", "linear", "fp8", "nvfp4"],
+                    choices=["all", "attention", "gather_attention", "gather", "linear", "fp8",
+                             "nvfp4"],
                     help="time one kernel alone on its own inputs (for profiling)")
     ap.add_argument("--workload", default="worldattention",
                     choices=["worldattention", "denoise", "hybrid", "hsa", "per_head", "cache",

@@ -247,6 +247,37 @@ wa_status wa_block_attn(const void* q, int n_q, const void* k_main, const void* 
                         float* lse, wa_stream_t stream);
 
 /*
+ * Gather and block attention in one launch: the page gather ([WA] Fig. 1,
+ * custom kernels) done by the attention's own tile copies.  The result is
+ * that of wa_gather_pages (or wa_gather_pages_per_head) into k_buf, v_buf
+ * followed by wa_block_attn over [k_buf ; k_loc], [v_buf ; v_loc], bit for bit:
+ *
+ *   k_buf[s*page_tokens + t][h] = k_pages[idx[s]][t][h]          (per_head == 0)
+ *                               = k_pages[idx[h][s]][t][h]       (per_head != 0)
+ *   O, lse as wa_block_attn with n_main = k_p * page_tokens      (likewise v)
+ *
+ * The attention reads its key and value tiles straight from the pages; each
+ * buffer tile is also written to k_buf/v_buf once, from on-chip memory, so the
+ * pages are read once instead of twice (gather, then attention).
+ * k_pages, v_pages : device [n_pages][page_tokens][n_heads][head_dim] bf16.
+ * idx_dev  : device int32 [k_p] (per_head == 0) or [n_heads][k_p]; an index
+ *            outside [0, n_pages) reads as a page of zeros (its buffer rows
+ *            are written as zeros) and is recorded (WA_ERR_INDEX from wa_check).
+ * k_buf, v_buf : device [k_p*page_tokens][n_heads][head_dim] bf16, written;
+ *            or both NULL (attention only, no buffer written).
+ * k_loc, v_loc, n_loc, q, o, o_dt, lse, scale : as for wa_block_attn.
+ * Needs dt == WA_BF16 (WA_ERR_DTYPE), head_dim == 128 and page_tokens a
+ * multiple of 64 (WA_ERR_SHAPE); pages in device memory (WA_ERR_INVALID_ARG);
+ * 16-byte aligned pointers (WA_ERR_ALIGN).  Other cases: wa_gather_pages,
+ * then wa_block_attn.
+ */
+wa_status wa_gather_attn(const void* q, int n_q, const void* k_pages, const void* v_pages,
+                         int n_pages, int page_tokens, const int32_t* idx_dev, int k_p,
+                         int per_head, void* k_buf, void* v_buf, const void* k_loc,
+                         const void* v_loc, int n_loc, wa_dtype dt, int n_heads, int head_dim,
+                         float scale, void* o, wa_dtype o_dt, float* lse, wa_stream_t stream);
+
+/*
  * Linformer-style low-rank branch and gate fusion ([WA] HSA, linear branch;
  * the projection and gate equations are missing on the page and read as
  * Linformer and a per-head weighted sum):

@@ -24,6 +24,7 @@ __all__ = [
     "wa_select_pages_per_head",
     "wa_gather_pages_per_head",
     "wa_block_attn",
+    "wa_gather_attn",
     "wa_linear_branch",
     "wa_block_means",
     "wa_sparse_select",
@@ -50,6 +51,7 @@ WA_F32, WA_BF16 = 0, 1
 # Every symbol include/wa.h declares.
 EXPORTED_SYMBOLS = ("wa_strerror", "wa_version", "wa_page_summarize", "wa_select_pages",
                     "wa_select_pages_noalloc", "wa_gather_pages", "wa_block_attn",
+                    "wa_gather_attn",
                     "wa_linear_branch", "wa_block_means", "wa_block_means_segments",
                     "wa_sparse_select", "wa_sparse_attn",
                     "wa_select_pages_per_head", "wa_gather_pages_per_head", "wa_cache_create",
@@ -106,6 +108,7 @@ def load():
         "wa_select_pages_per_head": (I, [P, I, I, I, I, P, I, P, P, I, I, I, I, P, P, P, P]),
         "wa_gather_pages_per_head": (I, [P, P, I, I, I, I, I, P, I, P, P, P]),
         "wa_block_attn": (I, [P, I, P, P, I, P, P, I, I, I, I, F, P, I, P, P]),
+        "wa_gather_attn": (I, [P, I, P, P, I, I, P, I, I, P, P, P, P, I, I, I, I, F, P, I, P, P]),
         "wa_linear_branch": (I, [P, I, P, P, I, P, P, I, P, P, I, I, I, I, F, P, P, I, P, I, P]),
         "wa_block_means": (I, [P, I, I, I, I, I, P, P]),
         "wa_block_means_segments": (I, [I, P, P, P, I, I, I, P, P]),
@@ -305,6 +308,40 @@ def wa_block_attn(q: torch.Tensor, k_main, v_main, k_loc, v_loc, o: torch.Tensor
     _ok("wa_block_attn", load().wa_block_attn(
         _ptr(q), n_q, _ptr(k_main), _ptr(v_main), _rows(k_main), _ptr(k_loc), _ptr(v_loc),
         _rows(k_loc), _dt(q), h, d, float(scale), _ptr(o), _dt(o), _ptr(lse), _stream(stream)))
+
+
+def wa_gather_attn(q: torch.Tensor, k_pages: torch.Tensor, v_pages: torch.Tensor,
+                   idx_dev: torch.Tensor, k_loc, v_loc, o: torch.Tensor, k_buf=None, v_buf=None,
+                   lse=None, scale: float = 0.0, stream=None):
+    """Gather and attention in one launch: k_buf[s*P + t] = k_pages[idx[s]][t]
+    (idx int32 [k_p]; or [H][k_p], a page set per head), likewise v, and o as
+    wa_block_attn over [k_buf; k_loc], [v_buf; v_loc].  k_buf/v_buf may be None
+    (attention only)."""
+    _need(q.dim() == 3 and q.is_contiguous() and o.shape == q.shape and o.is_contiguous(),
+          "q and o must be contiguous [n_q][H][d]")
+    n_q, h, d = q.shape
+    _need(o.dtype in (torch.float32, q.dtype), "o must be float32 or the input dtype")
+    _need(k_pages.dim() == 4 and k_pages.shape[2:] == (h, d) and v_pages.shape == k_pages.shape,
+          "k_pages, v_pages must be [n_pages][P][H][d]")
+    n, p = k_pages.shape[:2]
+    _buf(k_pages, q.dtype, k_pages.numel(), "k_pages")
+    _buf(v_pages, q.dtype, v_pages.numel(), "v_pages")
+    _need(idx_dev.dtype == torch.int32 and idx_dev.is_contiguous() and idx_dev.dim() in (1, 2),
+          "idx_dev must be contiguous int32 [k_p] or [H][k_p]")
+    per_head = idx_dev.dim() == 2
+    _need(not per_head or idx_dev.shape[0] == h, "a page set per head needs idx_dev [H][k_p]")
+    k_p = idx_dev.shape[-1]
+    _need((k_buf is None) == (v_buf is None), "k_buf and v_buf go together")
+    if k_buf is not None:
+        _buf(k_buf, q.dtype, k_p * p * h * d, "k_buf")
+        _buf(v_buf, q.dtype, k_p * p * h * d, "v_buf")
+    _kv_pair(k_loc, v_loc, h, d, q.dtype, "local segment")
+    if lse is not None:
+        _buf(lse, torch.float32, h * n_q, "lse")
+    _ok("wa_gather_attn", load().wa_gather_attn(
+        _ptr(q), n_q, _ptr(k_pages), _ptr(v_pages), n, p, _ptr(idx_dev), k_p, int(per_head),
+        _ptr(k_buf), _ptr(v_buf), _ptr(k_loc), _ptr(v_loc), _rows(k_loc), _dt(q), h, d,
+        float(scale), _ptr(o), _dt(o), _ptr(lse), _stream(stream)))
 
 
 def wa_linear_branch(q: torch.Tensor, k_main, v_main, k_loc, v_loc, e_k: torch.Tensor,

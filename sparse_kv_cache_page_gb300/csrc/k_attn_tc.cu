@@ -38,6 +38,19 @@
 //   query pair) combines them (no spin-wait: a ticket counter).
 //   Epilogue: O / l (fp32 or rounded to bf16; optionally fused with an
 //   existing output: o = w_old[h] * o + w_new[h] * O) and LSE = scale*m + ln l.
+//
+// Paged form (the gather fused into the producer): the buffer segment is not
+// read from a contiguous buffer but from the page bank, buffer row r being row
+// r % P of page idx[r / P] (P = page_tokens, a multiple of 64, so each 64-row
+// box of a key tile lies in one page).  A tile inside one page comes as
+// 128-row boxes, a tile across a page boundary (or past the buffer's end) as
+// 64-row boxes (64-row boxes throughout measured 13% slower).  The ring
+// receives the same bytes as from the gathered buffer, so the results are
+// bit-identical to gather then attention.  With a buffer given, the CTA of
+// query pair j % n_qpairs also writes buffer tile j (K and V) from its ring
+// slot by TMA store -- the gather's output, without the gather's second read
+// of the pages: warp 11 issues each store as soon as the tile lands, and a
+// slot is reused once its MMA and any store have read it.
 #include <atomic>
 #include <math.h>
 #include <stdlib.h>
@@ -63,6 +76,7 @@ constexpr int kThreads = 384;
 constexpr int kProducerWarp = 8;
 constexpr int kMmaWarp = 9;              // S issuer of both query tiles, TMEM owner
 constexpr int kPvWarp = 10;              // P V issuer of both query tiles
+constexpr int kStoreWarp = 11;           // paged form: buffer stores
 constexpr int kMaxUnits = 8192;          // split attention: one ticket per (head, query pair)
 
 constexpr uint32_t kColS = 0;            // S, shared by the two query tiles in turn
@@ -90,6 +104,7 @@ struct Bars {
   uint64_t o_ready[2];      // O_i += P_i(j) V_j done
   uint64_t drain;
   uint64_t comb;            // bulk copy of another split's rows (split combine)
+  uint64_t st_done;         // paged form: every buffer store has read the ring
   uint32_t tmem_base;
   int abort_flag;
   unsigned ticket;
@@ -118,6 +133,11 @@ struct Params {
   int tile_stride;
   unsigned long long wait_ns;   // limit of each bounded wait (host-set)
   int withhold_q;               // fault injection: the query tiles are never copied
+  // paged form: buffer row r = row r % page_tokens of page idx[idx_stride * head + r / page_tokens]
+  // of the bank's bank_rows = n_pages * page_tokens rows
+  const int32_t* idx;
+  int idx_stride, page_tokens, n_pages, bank_rows;
+  int store_buf;                // write each buffer tile to the buffer (one CTA per tile)
 };
 
 // Key tile j of head h: segment (0 = buffer, 1 = local), first row, valid rows.
@@ -133,6 +153,28 @@ __device__ __forceinline__ TileRef tile_ref(const Params& p, int head, int j) {
   if (j < p.nt_main) return {0, j * BN, min(BN, p.n_main - j * BN)};
   const int r = (j - p.nt_main) * BN;
   return {1, r, min(BN, p.n_loc - r)};
+}
+
+// Paged form: bank row of buffer row r (the first of a 64-row box) for head
+// `head`; rows past the buffer and bad page indices give a row past the bank,
+// which the copy fills with zeros (a bad index is recorded, as by the gather).
+__device__ __forceinline__ int bank_row(const Params& p, int head, int r) {
+  if (r >= p.n_main) return p.bank_rows;
+  const int slot = r / p.page_tokens;
+  const int pg = __ldg(p.idx + (size_t)head * p.idx_stride + slot);
+  if (pg < 0 || pg >= p.n_pages) {
+    atomicOr(p.status, kStatusIndex);
+    return p.bank_rows;
+  }
+  return pg * p.page_tokens + (r - slot * p.page_tokens);
+}
+
+// Paged form: ring tile u of a CTA (K for even u, V for odd) is key tile
+// jb + u/2; the CTA writes it to the buffer when it is buffer tile j with
+// j % n_qpairs equal to the CTA's query pair (one writer per tile).
+__device__ __forceinline__ bool owns_tile(const Params& p, int jb, int qpair, int u) {
+  const int j = jb + (u >> 1);
+  return p.store_buf && j < p.nt_main && j % p.n_qpairs == qpair;
 }
 
 // Key tiles [j0, j1) of split `sp`: contiguous, sizes differ by at most one.
@@ -195,11 +237,14 @@ constexpr int kMaxSplit = 16;     // ticket and done counts share one 32-bit cou
 static_assert(256 * kStagePitch * 4 + 128 * HD * 4 + kMaxSplit * 256 * 4 <= SmemLayout::bars,
               "staging, the combine buffer and the split weights overlay Q and the ring only");
 
-template <typename OutT, bool kLse, bool kSparse>
+template <typename OutT, bool kLse, bool kSparse, bool kPaged>
 __global__ void __launch_bounds__(kThreads, 1)
 k_block_attn_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_km,
                 const __grid_constant__ CUtensorMap tm_vm, const __grid_constant__ CUtensorMap tm_kl,
-                const __grid_constant__ CUtensorMap tm_vl, const Params p) {
+                const __grid_constant__ CUtensorMap tm_vl, const __grid_constant__ CUtensorMap tm_kp,
+                const __grid_constant__ CUtensorMap tm_vp, const __grid_constant__ CUtensorMap tm_kq,
+                const __grid_constant__ CUtensorMap tm_vq, const Params p) {
+  static_assert(!(kSparse && kPaged), "one form at a time");
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
@@ -219,7 +264,8 @@ k_block_attn_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     mbar_init(&bars->q_full, 1);
     for (int s = 0; s < NS; ++s) {
       mbar_init(&bars->kv_full[s], 1);
-      mbar_init(&bars->kv_empty[s], 1);
+      // (paged form: the MMA's commit and the store warp's arrival)
+      mbar_init(&bars->kv_empty[s], kPaged ? 2 : 1);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&bars->s_full[i], 1);
@@ -229,6 +275,7 @@ k_block_attn_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     }
     mbar_init(&bars->drain, 2);
     mbar_init(&bars->comb, 1);
+    mbar_init(&bars->st_done, 1);
     bars->abort_flag = 0;
     fence_mbar_init();
   }
@@ -262,17 +309,43 @@ k_block_attn_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         int issued = 0;
         for (int t = 0; t < 2 * nloc; ++t) {
           const int slot = t % NS;
-          if (t >= NS &&
-              !mbar_wait_sleep(&bars->kv_empty[slot], ((t / NS) - 1) & 1, abort_flag, p.status, p.wait_ns))
-            break;
           const TileRef tr = tile_ref<kSparse>(p, head, jb + (t >> 1));
           const bool is_v = t & 1;
-          const CUtensorMap* map = tr.seg == 0 ? (is_v ? &tm_vm : &tm_km) : (is_v ? &tm_vl : &tm_kl);
-          const int row = tr.row;
+          // paged form: the tile's bank rows, looked up before its slot is free;
+          // a tile inside one page is one 128-row box per column half, else
+          // two 64-row boxes (a page boundary, or the buffer's end, between)
+          bool whole = true;
+          int y0 = 0, y1 = 0;
+          if (kPaged && tr.seg == 0) {
+            const int r0 = tr.row;
+            whole = r0 + BN - 1 < p.n_main && r0 / p.page_tokens == (r0 + BN - 1) / p.page_tokens;
+            y0 = bank_row(p, head, r0);
+            if (!whole) y1 = bank_row(p, head, r0 + 64);
+          }
+          if (t >= NS) {
+            if (!mbar_wait_sleep(&bars->kv_empty[slot], ((t / NS) - 1) & 1, abort_flag, p.status, p.wait_ns))
+              break;
+          }
           uint8_t* dst = smem + SmemLayout::ring + slot * kKvTile;
           mbar_arrive_expect_tx(&bars->kv_full[slot], kKvTile);
-          tma_load_2d(map, &bars->kv_full[slot], dst, xq, row);
-          tma_load_2d(map, &bars->kv_full[slot], dst + kKvHalf, xq + 64, row);
+          if (kPaged && tr.seg == 0) {
+            if (whole) {
+              const CUtensorMap* map = is_v ? &tm_vq : &tm_kq;
+              tma_load_2d(map, &bars->kv_full[slot], dst, xq, y0);
+              tma_load_2d(map, &bars->kv_full[slot], dst + kKvHalf, xq + 64, y0);
+            } else {
+              const CUtensorMap* map = is_v ? &tm_vp : &tm_kp;
+              tma_load_2d(map, &bars->kv_full[slot], dst, xq, y0);
+              tma_load_2d(map, &bars->kv_full[slot], dst + kKvHalf, xq + 64, y0);
+              tma_load_2d(map, &bars->kv_full[slot], dst + kKvHalf / 2, xq, y1);
+              tma_load_2d(map, &bars->kv_full[slot], dst + kKvHalf + kKvHalf / 2, xq + 64, y1);
+            }
+          } else {
+            const CUtensorMap* map = tr.seg == 0 ? (is_v ? &tm_vm : &tm_km) : (is_v ? &tm_vl : &tm_kl);
+            const int row = tr.row;
+            tma_load_2d(map, &bars->kv_full[slot], dst, xq, row);
+            tma_load_2d(map, &bars->kv_full[slot], dst + kKvHalf, xq + 64, row);
+          }
           issued = t + 1;
         }
         if (*abort_flag) {
@@ -349,6 +422,33 @@ k_block_attn_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         }
         mma_commit(&bars->drain);
         mbar_wait_drain(&bars->drain, 0, 1000000000ull);
+      }
+      __syncwarp();
+    } else if (kPaged && warp == kStoreWarp) {
+      if (lane == 0) {
+        // every ring tile in order: the ones this CTA writes to the buffer are
+        // stored as soon as they land; each slot is released (the second of the
+        // two arrivals its reuse waits for) once any store has read it.  Seeing
+        // every tile keeps each parity wait within one phase of its barrier.
+        const int xq = head * HD;
+        for (int u = 0; u < 2 * nloc; ++u) {
+          const int slot = u % NS;
+          if (!mbar_wait_sleep(&bars->kv_full[slot], (u / NS) & 1, abort_flag, p.status, p.wait_ns))
+            break;
+          if (owns_tile(p, jb, qpair, u)) {
+            const uint8_t* src = smem + SmemLayout::ring + slot * kKvTile;
+            const CUtensorMap* map = (u & 1) ? &tm_vm : &tm_km;
+            const int row = (jb + (u >> 1)) * BN;
+            tma_store_2d(map, src, xq, row);
+            tma_store_2d(map, src + kKvHalf, xq + 64, row);
+            bulk_commit();
+            bulk_wait_read_all();
+          }
+          mbar_arrive(&bars->kv_empty[slot]);
+        }
+        bulk_wait_read_all();
+        mbar_arrive(&bars->st_done);   // the epilogue may now overlay the ring
+        bulk_wait_all();               // the stores' writes, before the CTA exits
       }
       __syncwarp();
     }
@@ -450,8 +550,12 @@ k_block_attn_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     // (a CTA with no key tiles, block-sparse form, reaches here without having
     // waited for anything).  Every K/V copy was consumed by an MMA the loop
     // waited for.
-    const bool staging_ok =
+    // (paged form: and the producer's buffer stores have read the ring)
+    bool staging_ok =
         ok && __all_sync(0xffffffffu, mbar_wait(&bars->q_full, 0, abort_flag, p.status, p.wait_ns));
+    if (kPaged)
+      staging_ok = staging_ok &&
+                   __all_sync(0xffffffffu, mbar_wait(&bars->st_done, 0, abort_flag, p.status, p.wait_ns));
     const int grow = q0 + qt * BM + row;
     const bool store = grow < p.n_q;
     const float wo = p.accumulate ? (p.w_old ? p.w_old[head] : 1.0f) : 0.0f;
@@ -765,23 +869,35 @@ int choose_split(int units, int nkv, int sms) {
   return best;
 }
 
-template <typename OutT, bool kLse, bool kSparse>
-wa_status launch_t(const CUtensorMap& tq, const CUtensorMap& tkm, const CUtensorMap& tvm,
-                   const CUtensorMap& tkl, const CUtensorMap& tvl, const Params& p, int n_heads,
-                   cudaStream_t s) {
+struct Maps {
+  CUtensorMap q, km, vm, kl, vl, kp, vp, kq, vq;
+};
+
+template <typename OutT, bool kLse, bool kSparse, bool kPaged>
+wa_status launch_t(const Maps& m, const Params& p, int n_heads, cudaStream_t s) {
   const int smem = SmemLayout::total + 1024;
   static std::atomic<bool> attr_done[64];   // per device; setting it twice is harmless
   int dev = 0;
   cudaGetDevice(&dev);
-  auto kern = k_block_attn_tc<OutT, kLse, kSparse>;
+  auto kern = k_block_attn_tc<OutT, kLse, kSparse, kPaged>;
   if (dev < 64 && !attr_done[dev].load(std::memory_order_relaxed)) {
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
       return WA_ERR_CUDA;
     attr_done[dev].store(true, std::memory_order_relaxed);
   }
   dim3 grid(p.n_qpairs * p.n_split, n_heads);
-  return cuda_status(launch_pdl(kern, grid, dim3(kThreads), (size_t)smem, s, tq, tkm, tvm, tkl, tvl,
-                                p));
+  return cuda_status(launch_pdl(kern, grid, dim3(kThreads), (size_t)smem, s, m.q, m.km, m.vm, m.kl,
+                                m.vl, m.kp, m.vp, m.kq, m.vq, p));
+}
+
+template <bool kSparse, bool kPaged>
+wa_status launch_form(const Maps& m, const Params& p, int n_heads, bool o_f32, bool want_lse,
+                      cudaStream_t s) {
+  if (o_f32)
+    return want_lse ? launch_t<float, true, kSparse, kPaged>(m, p, n_heads, s)
+                    : launch_t<float, false, kSparse, kPaged>(m, p, n_heads, s);
+  return want_lse ? launch_t<__nv_bfloat16, true, kSparse, kPaged>(m, p, n_heads, s)
+                  : launch_t<__nv_bfloat16, false, kSparse, kPaged>(m, p, n_heads, s);
 }
 
 }  // namespace
@@ -790,22 +906,33 @@ wa_status launch_attn_tc(const void* q, int n_q, const void* k_main, const void*
                          int n_main, const void* k_loc, const void* v_loc, int n_loc, int n_heads,
                          float scale, void* o, int o_f32, float* lse, int accumulate,
                          const float* w_old, const float* w_new, int max_split, cudaStream_t s,
-                         const SparseBlocks* sparse) {
+                         const SparseBlocks* sparse, const PagedKV* paged) {
+  if (sparse && paged) return WA_ERR_INVALID_ARG;
   const uint64_t cols = (uint64_t)n_heads * HD;
-  CUtensorMap tq, tkm, tvm, tkl, tvl;
-  memset(&tkm, 0, sizeof(tkm));
-  memset(&tvm, 0, sizeof(tvm));
-  memset(&tkl, 0, sizeof(tkl));
-  memset(&tvl, 0, sizeof(tvl));
+  Maps m;
+  memset(&m, 0, sizeof(m));
   wa_status rc;
-  if ((rc = make_tmap_2d_bf16(&tq, q, cols, n_q, cols, 64, BM)) != WA_OK) return rc;
-  if (n_main > 0) {
-    if ((rc = make_tmap_2d_bf16(&tkm, k_main, cols, n_main, cols, 64, BN)) != WA_OK) return rc;
-    if ((rc = make_tmap_2d_bf16(&tvm, v_main, cols, n_main, cols, 64, BN)) != WA_OK) return rc;
+  if ((rc = make_tmap_2d_bf16(&m.q, q, cols, n_q, cols, 64, BM)) != WA_OK) return rc;
+  // the buffer segment (paged form: the buffer as the stores' destination, if given)
+  if (n_main > 0 && k_main) {
+    if ((rc = make_tmap_2d_bf16(&m.km, k_main, cols, n_main, cols, 64, BN)) != WA_OK) return rc;
+    if ((rc = make_tmap_2d_bf16(&m.vm, v_main, cols, n_main, cols, 64, BN)) != WA_OK) return rc;
   }
   if (n_loc > 0) {
-    if ((rc = make_tmap_2d_bf16(&tkl, k_loc, cols, n_loc, cols, 64, BN)) != WA_OK) return rc;
-    if ((rc = make_tmap_2d_bf16(&tvl, v_loc, cols, n_loc, cols, 64, BN)) != WA_OK) return rc;
+    if ((rc = make_tmap_2d_bf16(&m.kl, k_loc, cols, n_loc, cols, 64, BN)) != WA_OK) return rc;
+    if ((rc = make_tmap_2d_bf16(&m.vl, v_loc, cols, n_loc, cols, 64, BN)) != WA_OK) return rc;
+  }
+  if (paged) {
+    // the page bank, read in 64-row boxes
+    const uint64_t bank_rows = (uint64_t)paged->n_pages * paged->page_tokens;
+    if ((rc = make_tmap_2d_bf16(&m.kp, paged->k_pages, cols, bank_rows, cols, 64, 64)) != WA_OK)
+      return rc;
+    if ((rc = make_tmap_2d_bf16(&m.vp, paged->v_pages, cols, bank_rows, cols, 64, 64)) != WA_OK)
+      return rc;
+    if ((rc = make_tmap_2d_bf16(&m.kq, paged->k_pages, cols, bank_rows, cols, 64, 128)) != WA_OK)
+      return rc;
+    if ((rc = make_tmap_2d_bf16(&m.vq, paged->v_pages, cols, bank_rows, cols, 64, 128)) != WA_OK)
+      return rc;
   }
   Params p;
   p.n_q = n_q;
@@ -846,6 +973,12 @@ wa_status launch_attn_tc(const void* q, int n_q, const void* k_main, const void*
   p.counters = nullptr;
   p.wait_ns = wait_limit_ns();
   p.withhold_q = fault_mode() == WA_FAULT_WAIT;
+  p.idx = paged ? paged->idx : nullptr;
+  p.idx_stride = paged ? paged->idx_stride : 0;
+  p.page_tokens = paged ? paged->page_tokens : 0;
+  p.n_pages = paged ? paged->n_pages : 0;
+  p.bank_rows = paged ? paged->n_pages * paged->page_tokens : 0;
+  p.store_buf = paged && k_main ? 1 : 0;
   Scratch sc;
   const size_t units = (size_t)p.n_qpairs * n_heads;
   // scratch: [tiles (block-sparse form)][split partials]
@@ -875,16 +1008,9 @@ wa_status launch_attn_tc(const void* q, int n_q, const void* k_main, const void*
     p.counters = sc.ctrl->attn_counters;
   }
   const bool want_lse = lse != nullptr;
-  if (o_f32)
-    return sparse ? (want_lse ? launch_t<float, true, true>(tq, tkm, tvm, tkl, tvl, p, n_heads, s)
-                              : launch_t<float, false, true>(tq, tkm, tvm, tkl, tvl, p, n_heads, s))
-                  : (want_lse ? launch_t<float, true, false>(tq, tkm, tvm, tkl, tvl, p, n_heads, s)
-                              : launch_t<float, false, false>(tq, tkm, tvm, tkl, tvl, p, n_heads, s));
-  return sparse
-             ? (want_lse ? launch_t<__nv_bfloat16, true, true>(tq, tkm, tvm, tkl, tvl, p, n_heads, s)
-                         : launch_t<__nv_bfloat16, false, true>(tq, tkm, tvm, tkl, tvl, p, n_heads, s))
-             : (want_lse ? launch_t<__nv_bfloat16, true, false>(tq, tkm, tvm, tkl, tvl, p, n_heads, s)
-                         : launch_t<__nv_bfloat16, false, false>(tq, tkm, tvm, tkl, tvl, p, n_heads, s));
+  if (sparse) return launch_form<true, false>(m, p, n_heads, o_f32, want_lse, s);
+  if (paged) return launch_form<false, true>(m, p, n_heads, o_f32, want_lse, s);
+  return launch_form<false, false>(m, p, n_heads, o_f32, want_lse, s);
 }
 
 }  // namespace wa

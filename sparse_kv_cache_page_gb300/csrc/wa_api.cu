@@ -313,6 +313,50 @@ wa_status wa_block_attn(const void* q, int n_q, const void* k_main, const void* 
                         o_dt == WA_F32, lse, 0, nullptr, nullptr, 0, s);
 }
 
+wa_status wa_gather_attn(const void* q, int n_q, const void* k_pages, const void* v_pages,
+                         int n_pages, int page_tokens, const int32_t* idx_dev, int k_p,
+                         int per_head, void* k_buf, void* v_buf, const void* k_loc,
+                         const void* v_loc, int n_loc, wa_dtype dt, int n_heads, int head_dim,
+                         float scale, void* o, wa_dtype o_dt, float* lse, wa_stream_t stream) {
+  if (!dtype_ok(dt) || !dtype_ok(o_dt)) return WA_ERR_DTYPE;
+  if (dt != WA_BF16) return WA_ERR_DTYPE;
+  if (!q || !o || !k_pages || !v_pages || !idx_dev || n_q <= 0 || n_pages <= 0 ||
+      page_tokens <= 0 || k_p <= 0 || n_loc < 0)
+    return WA_ERR_INVALID_ARG;
+  if ((k_buf == nullptr) != (v_buf == nullptr)) return WA_ERR_INVALID_ARG;
+  if (n_loc > 0 && (!k_loc || !v_loc)) return WA_ERR_INVALID_ARG;
+  if (!row_ok(n_heads, head_dim, dt) || head_dim != 128 || (long long)n_heads * 128 > 16384)
+    return WA_ERR_SHAPE;
+  if (page_tokens % 64 != 0 || (long long)n_pages * page_tokens > 0x7fffffffLL ||
+      (long long)k_p * page_tokens > 0x7fffffffLL)
+    return WA_ERR_SHAPE;
+  if (!aligned16(q) || !aligned16(o) || !aligned16(k_pages) || !aligned16(v_pages) ||
+      (k_buf && (!aligned16(k_buf) || !aligned16(v_buf))) ||
+      (n_loc > 0 && (!aligned16(k_loc) || !aligned16(v_loc))))
+    return WA_ERR_ALIGN;
+  const void* const banks[2] = {k_pages, v_pages};
+  for (const void* pages : banks) {
+    cudaPointerAttributes attr;
+    if (cudaPointerGetAttributes(&attr, pages) != cudaSuccess) {
+      cudaGetLastError();
+      return WA_ERR_INVALID_ARG;
+    }
+    if (attr.type != cudaMemoryTypeDevice && attr.type != cudaMemoryTypeManaged)
+      return WA_ERR_INVALID_ARG;
+  }
+  if (!(scale > 0.0f)) scale = 1.0f / sqrtf((float)head_dim);
+  PagedKV pk;
+  pk.k_pages = k_pages;
+  pk.v_pages = v_pages;
+  pk.n_pages = n_pages;
+  pk.page_tokens = page_tokens;
+  pk.idx = idx_dev;
+  pk.idx_stride = per_head ? k_p : 0;
+  return launch_attn_tc(q, n_q, k_buf, v_buf, k_p * page_tokens, k_loc, v_loc, n_loc, n_heads,
+                        scale, o, o_dt == WA_F32, lse, 0, nullptr, nullptr, 0,
+                        (cudaStream_t)stream, nullptr, &pk);
+}
+
 // Device-usable address of p: device memory as is, pinned host memory through
 // its device mapping; NULL if neither.
 static const void* device_view(const void* p) {

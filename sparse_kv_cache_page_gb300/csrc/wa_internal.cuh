@@ -140,11 +140,22 @@ struct SparseBlocks {
   const int32_t* count;
   int stride, b_main, b_loc;
 };
+// Paged form: the buffer segment's n_main = k_p * page_tokens rows are read from
+// the page bank [n_pages][page_tokens][n_heads][128] through device indices
+// idx[idx_stride * h + s] (page_tokens a multiple of 64); k_main/v_main, if
+// given, receive the gathered buffer.
+struct PagedKV {
+  const void* k_pages;
+  const void* v_pages;
+  int n_pages, page_tokens;
+  const int32_t* idx;
+  int idx_stride;
+};
 wa_status launch_attn_tc(const void* q, int n_q, const void* k_main, const void* v_main,
                          int n_main, const void* k_loc, const void* v_loc, int n_loc,
                          int n_heads, float scale, void* o, int o_f32, float* lse, int accumulate,
                          const float* w_old, const float* w_new, int max_split, cudaStream_t s,
-                         const SparseBlocks* sparse = nullptr);
+                         const SparseBlocks* sparse = nullptr, const PagedKV* paged = nullptr);
 
 // FP8 E4M3 page codec (k_fp8.cu).  Rows are (token, head) rows of head_dim
 // values; codes and scales may live in pinned host memory (device-mapped pointers).

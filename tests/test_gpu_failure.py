@@ -72,6 +72,36 @@ def test_wait_limit_reached_gives_timeout_then_ordinary_calls_work(monkeypatch, 
         assert_attn_close(o, ref, torch.bfloat16, "after a timeout")
 
 
+def test_wait_limit_in_the_fused_gather_attention():
+    """The same withheld query tiles in the gather + attention launch, whose
+    store warp also waits on the ring: the launch ends with WA_ERR_TIMEOUT
+    (copies and stores drained), and an ordinary call then matches the
+    two-launch path bit for bit."""
+    q, km, vm, kl, vl = _attn_inputs("fused", n_q=600, n_main=1024, n_loc=100)
+    kp, vp = km.reshape(8, 128, 2, 128), vm.reshape(8, 128, 2, 128)
+    idx = torch.tensor([6, 1, 3], dtype=torch.int32, device=DEV)
+    kb = torch.empty((384, 2, 128), dtype=torch.bfloat16, device=DEV)
+    vb = torch.empty_like(kb)
+    o = torch.empty(q.shape, dtype=torch.float32, device=DEV)
+    wa.wa_check()
+    wa.wa_set_wait_limit_ns(20_000_000)
+    wa.wa_set_fault(wa.WA_FAULT_WAIT)
+    wa.wa_gather_attn(q, kp, vp, idx, kl, vl, o, kb, vb)
+    with pytest.raises(wa.WaError) as e:
+        wa.wa_check()
+    assert e.value.status == 8
+    wa.wa_set_fault(wa.WA_FAULT_NONE)
+    wa.wa_set_wait_limit_ns(0)
+    wa.wa_gather_attn(q, kp, vp, idx, kl, vl, o, kb, vb)
+    wa.wa_check()
+    kb2, vb2 = torch.empty_like(kb), torch.empty_like(vb)
+    o2 = torch.empty_like(o)
+    wa.wa_gather_pages(kp, vp, idx, None, kb2, vb2)
+    wa.wa_block_attn(q, kb2, vb2, kl, vl, o2)
+    wa.wa_check()
+    assert torch.equal(kb, kb2) and torch.equal(vb, vb2) and torch.equal(o, o2)
+
+
 def test_linear_branch_runs_under_a_short_wait_limit():
     """A limit far above the kernels' real waits changes nothing."""
     q, km, vm, kl, vl = _attn_inputs("lin", n_q=256, n_main=512, n_loc=128)

@@ -1,0 +1,194 @@
+"""GPU parity of gather and attention in one launch (wa_gather_attn).
+
+The gathered buffer must equal the oracle's gather bit for bit (WorldAttention
+review page, Fig. 1 and the HKV section: the selected pages copied, in slot
+order, into one contiguous buffer). The attention must be within the bf16
+tolerance of the oracle's attention over [buffer ; local] (Inferix summary
+page, §3 Step 3). Both must also be bit-identical to the two-launch path
+(wa_gather_pages, then wa_block_attn), which the fused launch reproduces.
+
+The cases cover:
+
+* pages of 64 rows, where a key tile spans two pages;
+* pages of 192 and 320 rows, where a tile straddles a page boundary;
+* an odd number of 64-row boxes, where the last tile is half past the buffer;
+* repeated and unsorted indices;
+* a page set per head;
+* no buffer output;
+* forced split counts, which move the buffer stores between CTAs;
+* bad indices;
+* the one-layer WorldAttention chunk at full size, with the pages the
+  selection picks.
+"""
+
+import numpy as np
+import pytest
+import torch
+
+import oracle as O
+import sparse_kv_cache_page_gb300 as wa
+from sparse_kv_cache_page_gb300 import synth
+from tests._util import LSE_ABS, assert_attn_close, f64, np_of
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+D = 128
+
+
+@pytest.fixture
+def split(monkeypatch):
+    def _set(n):
+        if n is None:
+            monkeypatch.delenv("WA_ATTN_SPLIT", raising=False)
+        else:
+            monkeypatch.setenv("WA_ATTN_SPLIT", str(n))
+    yield _set
+    monkeypatch.delenv("WA_ATTN_SPLIT", raising=False)
+
+
+def _bank(tag, n_pages, P, H, n_q, n_loc):
+    g = lambda shape, t: synth.normal(shape, synth.seed_of("gattn", tag, t), DEV,  # noqa: E731
+                                      torch.bfloat16, std=D ** -0.25)
+    kp, vp = g((n_pages, P, H, D), "kp"), g((n_pages, P, H, D), "vp")
+    q = g((n_q, H, D), "q")
+    kl = g((n_loc, H, D), "kl") if n_loc else None
+    vl = g((n_loc, H, D), "vl") if n_loc else None
+    return kp, vp, q, kl, vl
+
+
+def _bufs(idx, P, H):
+    n = idx.shape[-1] * P
+    return (torch.full((n, H, D), 7.0, dtype=torch.bfloat16, device=DEV),
+            torch.full((n, H, D), 7.0, dtype=torch.bfloat16, device=DEV))
+
+
+def _two_launch(q, kp, vp, idx, kl, vl, check=True):
+    P, H = kp.shape[1], kp.shape[2]
+    kb, vb = _bufs(idx, P, H)
+    if idx.dim() == 2:
+        wa.wa_gather_pages_per_head(kp, vp, idx, kb, vb)
+    else:
+        wa.wa_gather_pages(kp, vp, idx, None, kb, vb)
+    o = torch.empty(q.shape, dtype=torch.float32, device=DEV)
+    lse = torch.empty((H, q.shape[0]), dtype=torch.float32, device=DEV)
+    wa.wa_block_attn(q, kb, vb, kl, vl, o, lse)
+    if check:
+        wa.wa_check()
+    return kb, vb, o, lse
+
+
+def _fused(q, kp, vp, idx, kl, vl, with_buf=True, check=True):
+    P, H = kp.shape[1], kp.shape[2]
+    kb, vb = _bufs(idx, P, H) if with_buf else (None, None)
+    o = torch.empty(q.shape, dtype=torch.float32, device=DEV)
+    lse = torch.empty((H, q.shape[0]), dtype=torch.float32, device=DEV)
+    wa.wa_gather_attn(q, kp, vp, idx, kl, vl, o, kb, vb, lse)
+    if check:
+        wa.wa_check()
+    return kb, vb, o, lse
+
+
+def _oracle_check(q, kp, vp, idx, kl, vl, kb, vb, o, lse, what):
+    okp, ovp = np_of(kp), np_of(vp)
+    ix = idx.cpu().numpy()
+    gather = O.gather_pages_per_head if ix.ndim == 2 else O.gather_pages
+    rk, rv = gather(okp, ix), gather(ovp, ix)
+    assert np.array_equal(np_of(kb), rk), f"{what}: gathered keys"
+    assert np.array_equal(np_of(vb), rv), f"{what}: gathered values"
+    n = lambda t: None if t is None else np_of(t)  # noqa: E731
+    ref_o, ref_lse = O.block_attn(np_of(q), rk, rv, n(kl), n(vl))
+    assert_attn_close(o, ref_o, torch.bfloat16, what)
+    assert np.abs(f64(lse) - ref_lse).max() <= LSE_ABS, what
+
+
+@pytest.mark.parametrize("tag,n_pages,P,idx,H,n_q,n_loc", [
+    ("p192", 6, 192, [5, 0, 3], 2, 300, 100),      # tiles straddle page boundaries
+    ("p64odd", 5, 64, [4, 1, 1], 3, 520, 0),       # 3 boxes: the last tile half past the buffer
+    ("p128one", 4, 128, [2], 1, 17, 33),           # one page, one tile, few queries
+    ("p320", 3, 320, [2, 0], 2, 1000, 250),        # 5 boxes per page, ragged local tail
+])
+def test_fused_equals_two_launch_and_oracle(tag, n_pages, P, idx, H, n_q, n_loc):
+    kp, vp, q, kl, vl = _bank(tag, n_pages, P, H, n_q, n_loc)
+    ix = torch.tensor(idx, dtype=torch.int32, device=DEV)
+    kb, vb, o, lse = _fused(q, kp, vp, ix, kl, vl)
+    kb2, vb2, o2, lse2 = _two_launch(q, kp, vp, ix, kl, vl)
+    assert torch.equal(kb, kb2) and torch.equal(vb, vb2)
+    assert torch.equal(o, o2) and torch.equal(lse, lse2)
+    _oracle_check(q, kp, vp, ix, kl, vl, kb, vb, o, lse, tag)
+
+
+@pytest.mark.parametrize("n_split", [1, 2, 3, 5])
+def test_every_split_writes_every_buffer_tile_once(split, n_split):
+    """Three query pairs over 9 key tiles of 64-row pages: the storing CTA
+    of a tile depends on the split; every tile is written, and the result
+    equals the two-launch path under the same split."""
+    split(n_split)
+    kp, vp, q, kl, vl = _bank(f"split{n_split}", 12, 64, 2, 700, 130)
+    ix = torch.tensor([11, 3, 7, 0, 9, 2, 5, 8, 1, 4, 6, 10, 3, 3], dtype=torch.int32, device=DEV)
+    kb, vb, o, lse = _fused(q, kp, vp, ix, kl, vl)
+    kb2, vb2, o2, lse2 = _two_launch(q, kp, vp, ix, kl, vl)
+    assert torch.equal(kb, kb2) and torch.equal(vb, vb2)
+    assert torch.equal(o, o2) and torch.equal(lse, lse2)
+    _oracle_check(q, kp, vp, ix, kl, vl, kb, vb, o, lse, f"split {n_split}")
+
+
+def test_page_set_per_head():
+    H, P = 4, 128
+    kp, vp, q, kl, vl = _bank("perhead", 9, P, H, 400, 64)
+    ix = torch.tensor([[0, 4, 8], [1, 2, 3], [8, 7, 6], [5, 5, 0]], dtype=torch.int32, device=DEV)
+    kb, vb, o, lse = _fused(q, kp, vp, ix, kl, vl)
+    kb2, vb2, o2, lse2 = _two_launch(q, kp, vp, ix, kl, vl)
+    assert torch.equal(kb, kb2) and torch.equal(vb, vb2)
+    assert torch.equal(o, o2) and torch.equal(lse, lse2)
+    _oracle_check(q, kp, vp, ix, kl, vl, kb, vb, o, lse, "per head")
+
+
+def test_attention_only_without_a_buffer():
+    kp, vp, q, kl, vl = _bank("nobuf", 5, 192, 2, 260, 90)
+    ix = torch.tensor([4, 2], dtype=torch.int32, device=DEV)
+    _, _, o, lse = _fused(q, kp, vp, ix, kl, vl, with_buf=False)
+    _, _, o2, lse2 = _two_launch(q, kp, vp, ix, kl, vl)
+    assert torch.equal(o, o2) and torch.equal(lse, lse2)
+
+
+def test_bad_index_reads_zeros_and_is_recorded():
+    """An index outside [0, n_pages) gives a slot of zeros, as the gather
+    does, and WA_ERR_INDEX from wa_check; the launch is otherwise complete."""
+    kp, vp, q, kl, vl = _bank("bad", 4, 64, 2, 200, 50)
+    ix = torch.tensor([1, 4, -2], dtype=torch.int32, device=DEV)
+    wa.wa_check()
+    kb, vb, o, lse = _fused(q, kp, vp, ix, kl, vl, check=False)
+    with pytest.raises(wa.WaError) as e:
+        wa.wa_check()
+    assert e.value.status == 5
+    kb2, vb2, o2, lse2 = _two_launch(q, kp, vp, ix, kl, vl, check=False)
+    with pytest.raises(wa.WaError):
+        wa.wa_check()
+    assert torch.all(kb[64:] == 0) and torch.all(vb[64:] == 0)
+    assert torch.equal(kb, kb2) and torch.equal(vb, vb2)
+    assert torch.equal(o, o2) and torch.equal(lse, lse2)
+
+
+def test_worldattention_chunk_at_full_size():
+    """The one-layer WorldAttention chunk (40 pages of 12,480 tokens, 12
+    heads; 4,680 queries and 4,680 local tokens), with the four pages the
+    selection picks: the fused launch equals the two-launch path bit for bit,
+    the buffer equals the pages indexed on the device, and sampled rows match
+    the oracle."""
+    c = synth.worldattention_case(device=DEV, recall_chunk=3)
+    kbar = torch.empty((c.n_pages, c.n_heads, D), dtype=torch.float32, device=DEV)
+    wa.wa_page_summarize(c.k_pages, kbar)
+    ix = torch.empty(c.k_p, dtype=torch.int32, device=DEV)
+    wa.wa_select_pages(c.q, kbar, c.prompt_cur, c.prompt_chunks, c.pages_per_chunk, c.k_p, ix)
+    kb, vb, o, lse = _fused(c.q, c.k_pages, c.v_pages, ix, c.k_loc, c.v_loc)
+    kb2, vb2, o2, lse2 = _two_launch(c.q, c.k_pages, c.v_pages, ix, c.k_loc, c.v_loc)
+    assert torch.equal(o, o2) and torch.equal(lse, lse2)
+    assert torch.equal(kb, kb2) and torch.equal(vb, vb2)
+    il = ix.long()
+    assert torch.equal(kb, c.k_pages[il].reshape(kb.shape))
+    assert torch.equal(vb, c.v_pages[il].reshape(vb.shape))
+    rows = list(range(0, c.q.shape[0], 389)) + [c.q.shape[0] - 1]
+    ref_o, ref_lse = O.block_attn(np_of(c.q), np_of(kb), np_of(vb), np_of(c.k_loc),
+                                  np_of(c.v_loc), rows=rows)
+    assert_attn_close(o[rows], ref_o, torch.bfloat16, "WorldAttention chunk")
+    assert np.abs(f64(lse[:, rows]) - ref_lse).max() <= LSE_ABS
