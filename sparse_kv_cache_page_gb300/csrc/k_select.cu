@@ -179,6 +179,39 @@ __device__ void sum_rows4(const float* rows, int n, int row_elems, float* out, f
   }
 }
 
+// out[c] = scale * sum_{p < n} rows[p * stride + c] for c < width (width and
+// stride multiples of 4), p in increasing order; loads of 8 rows in flight.
+__device__ void sum_rows4_strided(const float* rows, int n, int width, size_t stride, float* out,
+                                  float scale) {
+  const int n4 = width / 4;
+  for (int c = threadIdx.x; c < n4; c += blockDim.x) {
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    int p = 0;
+    for (; p + 8 <= n; p += 8) {
+      float4 v[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u)
+        v[u] = __ldcg(reinterpret_cast<const float4*>(rows + (size_t)(p + u) * stride) + c);
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        acc.x += v[u].x;
+        acc.y += v[u].y;
+        acc.z += v[u].z;
+        acc.w += v[u].w;
+      }
+    }
+    for (; p < n; ++p) {
+      const float4 v = __ldcg(reinterpret_cast<const float4*>(rows + (size_t)p * stride) + c);
+      acc.x += v.x;
+      acc.y += v.y;
+      acc.z += v.z;
+      acc.w += v.w;
+    }
+    reinterpret_cast<float4*>(out)[c] =
+        make_float4(acc.x * scale, acc.y * scale, acc.z * scale, acc.w * scale);
+  }
+}
+
 // ---------------------------------------------------------------------------
 // page summaries
 // ---------------------------------------------------------------------------
@@ -205,34 +238,38 @@ struct SumSegs {
 // otherwise, stream about 8% slower.
 template <typename T, int VPT>
 __global__ void __launch_bounds__(kThreads, 4)
-k_page_summarize(const SumSegs<T> segs, int row_elems, int nvec, int R, Ctrl* ctrl) {
+k_page_summarize(const SumSegs<T> segs, int row_elems, int cw, int n_cb, int nvec, int R,
+                 Ctrl* ctrl) {
   extern __shared__ float red[];
   pdl_wait();
   // this CTA's segment (static indices: the table stays in parameter space)
   SumSeg<T> g = segs.s[0];
   if (segs.n > 1 && (int)blockIdx.x >= segs.s[1].cta0) g = segs.s[1];
   if (segs.n > 2 && (int)blockIdx.x >= segs.s[2].cta0) g = segs.s[2];
+  // CTA order: column block fastest, so the CTAs reading one row range start together
   const int local = (int)blockIdx.x - g.cta0;
-  const int j = local / g.splits, s = local % g.splits;
+  const int cb = local % n_cb;
+  const int js = local / n_cb;
+  const int j = js / g.splits, s = js % g.splits;
   // page j holds rows [j P, j P + rows_j) of the n_rows; only the last may be short
   const int rows_j = min(g.page_tokens, g.n_rows - j * g.page_tokens);
   const int r0 = s * g.rows_per_split;
   const int r1 = min(rows_j, r0 + g.rows_per_split);
-  const T* base = g.pages + (size_t)j * g.page_tokens * row_elems;
-  colsum_rows<T, VPT>(base, (size_t)row_elems, row_elems, nvec, R, r0, r1, red);
+  const T* base = g.pages + (size_t)j * g.page_tokens * row_elems + (size_t)cb * cw;
+  colsum_rows<T, VPT>(base, (size_t)row_elems, cw, nvec, R, r0, r1, red);
   const float inv = 1.0f / (float)rows_j;
+  float* out = g.kbar + (size_t)j * row_elems + (size_t)cb * cw;
   if (g.splits == 1) {
-    for (int c = threadIdx.x; c < row_elems; c += blockDim.x)
-      g.kbar[(size_t)j * row_elems + c] = red[c] * inv;
+    for (int c = threadIdx.x; c < cw; c += blockDim.x) out[c] = red[c] * inv;
     return;
   }
-  float* mine = g.partial + ((size_t)j * g.splits + s) * row_elems;
-  for (int c = threadIdx.x; c < row_elems; c += blockDim.x) mine[c] = red[c];
-  unsigned* counter = &ctrl->counters[g.counter0 + j];
+  float* mine = g.partial + ((size_t)j * g.splits + s) * row_elems + (size_t)cb * cw;
+  for (int c = threadIdx.x; c < cw; c += blockDim.x) mine[c] = red[c];
+  unsigned* counter = &ctrl->counters[g.counter0 + j * n_cb + cb];
   if (!last_ticket(counter, (unsigned)g.splits)) return;
-  // the page's partial sums in split order, then the mean
-  sum_rows4(g.partial + (size_t)j * g.splits * row_elems, g.splits, row_elems,
-            g.kbar + (size_t)j * row_elems, inv);
+  // the column block's partial sums in split order, then the mean
+  sum_rows4_strided(g.partial + (size_t)j * g.splits * row_elems + (size_t)cb * cw, g.splits, cw,
+                    (size_t)row_elems, out, inv);
   if (threadIdx.x == 0) *counter = 0u;
 }
 
@@ -693,7 +730,12 @@ struct SegIn {
 template <typename T>
 wa_status summarize_t(const SegIn* in, int n_seg, int row_elems, cudaStream_t st) {
   if (n_seg < 1 || n_seg > kMaxSegs) return WA_ERR_INVALID_ARG;
-  Plan p = plan_rows<T>(row_elems);
+  // column blocks of 32 16-byte vectors (one warp per row) when the row divides
+  // into them, else whole rows
+  const int E = VecOf<T>::E;
+  const int cw = (row_elems / E) % 32 == 0 ? 32 * E : row_elems;
+  const int n_cb = row_elems / cw;
+  Plan p = plan_rows<T>(cw);
   SumSegs<T> segs{};
   segs.n = n_seg;
   size_t part_off[kMaxSegs], part_floats = 0;
@@ -704,14 +746,17 @@ wa_status summarize_t(const SegIn* in, int n_seg, int row_elems, cudaStream_t st
     const int n_pages = (in[i].n_rows + page_tokens - 1) / page_tokens;
     // About two waves of CTAs per segment: a single wave of long row ranges
     // ends with the slowest range, and more, shorter ranges add partial sums
-    // (measured on the one-layer WorldAttention bank: 0.251 ms with one wave of
-    // 256-thread CTAs; with 384-thread CTAs, four resident per SM, 0.2247 ms
-    // for two whole waves, 0.2278 for two and a half, 0.2280 for three, 0.2315
-    // for four; on another GB300 one whole wave measured 0.2242 against 0.2268
-    // for two, within the spread between boxes).
-    int splits = 2 * kTargetCtas / n_pages;
+    // (measured on the one-layer WorldAttention bank with whole-row CTAs:
+    // 0.251 ms with one wave of 256-thread CTAs; with 384-thread CTAs, four
+    // resident per SM, 0.2247 ms for two whole waves, 0.2278 for two and a
+    // half, 0.2280 for three, 0.2315 for four).  Column blocks of one warp's
+    // width (512 bytes of a bf16 row) keep the partials per output few: 40
+    // pages take 5 row ranges each (0.2234 -> 0.2173 ms against whole rows in
+    // 30 ranges), 8 pages 25 (0.0675 -> 0.0555 ms against 151 ranges, whose
+    // last CTA added 151 partials one load batch after another).
+    int splits = 2 * kTargetCtas / (n_pages * n_cb);
     if (splits < 1) splits = 1;
-    const int max_splits = (page_tokens + 15) / 16;   // at least 16 rows per CTA
+    const int max_splits = (page_tokens + 63) / 64;   // at least 64 rows per CTA
     if (splits > max_splits) splits = max_splits;
     if (splits > 256) splits = 256;
     const int rps = (page_tokens + splits - 1) / splits;
@@ -725,8 +770,8 @@ wa_status summarize_t(const SegIn* in, int n_seg, int row_elems, cudaStream_t st
     g.rows_per_split = rps;
     g.cta0 = ctas;
     g.counter0 = counters;
-    ctas += splits * n_pages;
-    if (splits > 1) counters += n_pages;
+    ctas += splits * n_pages * n_cb;
+    if (splits > 1) counters += n_pages * n_cb;
     part_off[i] = part_floats;
     part_floats += (size_t)n_pages * splits * row_elems;
   }
@@ -735,7 +780,7 @@ wa_status summarize_t(const SegIn* in, int n_seg, int row_elems, cudaStream_t st
   wa_status rc = get_scratch(part_floats * sizeof(float), &sc);
   if (rc != WA_OK) return rc;
   for (int i = 0; i < n_seg; ++i) segs.s[i].partial = static_cast<float*>(sc.data) + part_off[i];
-  const size_t smem = (size_t)p.R * row_elems * sizeof(float);
+  const size_t smem = (size_t)p.R * cw * sizeof(float);
   dim3 grid((unsigned)ctas);
   switch (p.vpt) {
 #define WA_CASE(V)                                                                          \
@@ -744,7 +789,7 @@ wa_status summarize_t(const SegIn* in, int n_seg, int row_elems, cudaStream_t st
       cudaFuncSetAttribute(k_page_summarize<T, V>, cudaFuncAttributeMaxDynamicSharedMemorySize, \
                            (int)smem);                                                      \
     if (launch_pdl(k_page_summarize<T, V>, grid, dim3(p.threads), smem, st, segs, row_elems, \
-                   p.nvec, p.R, sc.ctrl) != cudaSuccess)                                    \
+                   cw, n_cb, p.nvec, p.R, sc.ctrl) != cudaSuccess)                          \
       return WA_ERR_CUDA;                                                                   \
     break;
     WA_CASE(1) WA_CASE(2) WA_CASE(4) WA_CASE(8)
