@@ -289,13 +289,16 @@ def run_gpu(args, world, rank, local, hybrid=False, per_head=False):
     cs = torch.cuda.Stream()
 
     def e2e_run(n, n_summ=N_PAGES):
-        """n steps through the public API.  The copies of a step run on the copy
-        stream while the previous step's attention (compute-bound) runs, not
-        beside the HBM-bound summaries and gather: the next step's inputs, and
-        the previous step's output, each once that attention has started."""
+        """n steps through the public API.  The copies run on the copy stream
+        beside the retrieval and the gather + attention (compute-bound), not
+        beside the HBM-bound summaries: once step k's summaries are done, so is
+        step k-1, and step k-1's output goes back and step k+1's inputs come in
+        while step k runs on.  Apart from the wait for its own inputs, no event
+        sits between a step's kernels, so each launch keeps overlapping the
+        previous kernel's drain."""
         ev_in = [torch.cuda.Event() for _ in range(n)]
-        ev_done = [torch.cuda.Event() for _ in range(n)]
-        ev_attn = [torch.cuda.Event() for _ in range(n)]
+        ev_mid = [torch.cuda.Event() for _ in range(n)]
+        ev_last = torch.cuda.Event()
         cs.wait_stream(stream)
 
         def h2d(k):
@@ -309,7 +312,6 @@ def run_gpu(args, world, rank, local, hybrid=False, per_head=False):
 
         def d2h(k):
             with torch.cuda.stream(cs):
-                cs.wait_event(ev_done[k])
                 ho[k % 2].copy_(dbuf[k % 2][4], non_blocking=True)
 
         h2d(0)
@@ -318,23 +320,24 @@ def run_gpu(args, world, rank, local, hybrid=False, per_head=False):
             # the summaries read only the resident page bank: they run while this
             # step's inputs may still be arriving
             summarize(n_summ)
+            ev_mid[k].record(stream)
             stream.wait_event(ev_in[k])
             select(dq, kbar, dpc, pch, PPC, KP, idx)
-            ev_attn[k].record(stream)
             gather_attn(dq, idx, dkl, dvl, do)
             if hybrid:
                 wa.wa_linear_branch(dq, kbuf, vbuf, dkl, dvl, ek, ev, do)
-            ev_done[k].record(stream)
-            # during this step's attention: the previous step's output goes back
-            # (its buffer is written again two steps on, after ev_in of the next
-            # step, which follows on the copy stream), then the next step's inputs
-            # arrive (their buffers were last read by the previous step)
+            # after this step's summaries (so after all of step k-1): step k-1's
+            # output goes back, then step k+1's inputs arrive into the buffers
+            # that step k-1 read
             with torch.cuda.stream(cs):
-                cs.wait_event(ev_attn[k])
+                cs.wait_event(ev_mid[k])
             if k >= 1:
                 d2h(k - 1)
             if k + 1 < n:
                 h2d(k + 1)
+        ev_last.record(stream)
+        with torch.cuda.stream(cs):
+            cs.wait_event(ev_last)
         d2h(n - 1)
         stream.wait_stream(cs)
 
@@ -417,9 +420,10 @@ def run_gpu(args, world, rank, local, hybrid=False, per_head=False):
                                               else None}},
         "e2e": {"value": round(world * flops / (e2e_ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
                 "ms_per_step": round(e2e_ms, 4), "h2d_bytes_per_step": h2d_bytes,
-                "d2h_bytes_per_step": d2h, "copies": "copy stream, double-buffered: a step's inputs "
-                                                       "and the step before's output travel during "
-                                                       "the previous step's gather+attention",
+                "d2h_bytes_per_step": d2h, "copies": "copy stream, double-buffered: once step k's "
+                                                       "summaries are done, step k-1's output goes "
+                                                       "back and step k+1's inputs come in, beside "
+                                                       "step k's retrieval and gather+attention",
                 "ms_per_step_insert": round(e2e_ms_ins, 4),
                 "value_insert": round(world * flops / (e2e_ms_ins * 1e-3) / 1e12, 2)},
         "gpu_launches": launches_per_step * args.steps,
