@@ -33,8 +33,9 @@ pytestmark = pytest.mark.gpu
 DEV = "cuda"
 
 
-def _chain(c, k_p, use_prompt, o_dtype=torch.float32):
-    """summarize -> select -> gather -> attention through the C ABI."""
+def _chain(c, k_p, use_prompt, o_dtype=torch.float32, fused=False):
+    """summarize -> select -> gather -> attention through the C ABI (with
+    `fused`, the gather and the attention as one launch, as benchmarked)."""
     H, d = c.n_heads, c.head_dim
     kp, vp, q = c.k_pages.to(DEV), c.v_pages.to(DEV), c.q.to(DEV)
     kbar = torch.empty((c.n_pages, H, d), dtype=torch.float32, device=DEV)
@@ -47,10 +48,13 @@ def _chain(c, k_p, use_prompt, o_dtype=torch.float32):
     wa.wa_select_pages(q, kbar, cur, pc, c.pages_per_chunk, k_p, idx, sc, ch)
     kb = torch.empty((k_p * c.page_tokens, H, d), dtype=c.dtype, device=DEV)
     vb = torch.empty_like(kb)
-    wa.wa_gather_pages(kp, vp, idx, None, kb, vb)
     o = torch.empty(q.shape, dtype=o_dtype, device=DEV)
     lse = torch.empty((H, c.n_q), dtype=torch.float32, device=DEV)
-    wa.wa_block_attn(q, kb, vb, c.k_loc.to(DEV), c.v_loc.to(DEV), o, lse)
+    if fused:
+        wa.wa_gather_attn(q, kp, vp, idx, c.k_loc.to(DEV), c.v_loc.to(DEV), o, kb, vb, lse)
+    else:
+        wa.wa_gather_pages(kp, vp, idx, None, kb, vb)
+        wa.wa_block_attn(q, kb, vb, c.k_loc.to(DEV), c.v_loc.to(DEV), o, lse)
     wa.wa_check()
     return dict(kbar=kbar, idx=idx.cpu().numpy(), sc=sc.cpu().numpy(), chunk=int(ch.item()),
                 kb=kb, vb=vb, o=o, lse=lse)
@@ -112,9 +116,10 @@ def test_tiny_fp32_all_pages_equals_dense(peaked):
 
 def test_headline_chunk_as_benchmarked():
     """The benchmark's one-layer chunk, unplanted: 40 pages of 12,480 tokens
-    in 5 chunks, the current prompt recalling chunk 3, top-4 of its 8 pages."""
+    in 5 chunks, the current prompt recalling chunk 3, top-4 of its 8 pages;
+    the gather and the attention in one launch, as the benchmark runs them."""
     c = synth.worldattention_case(device=DEV, recall_chunk=3)
-    g = _chain(c, c.k_p, True, o_dtype=torch.float32)
+    g = _chain(c, c.k_p, True, o_dtype=torch.float32, fused=True)
     okp, oq = np_of(c.k_pages), np_of(c.q)
     kbar = O.page_summarize(okp)
     assert np.abs(f64(g["kbar"]) - kbar).max() < 1e-6

@@ -13,8 +13,8 @@ The cases cover:
 * pages of 192 and 320 rows, where a tile straddles a page boundary;
 * an odd number of 64-row boxes, where the last tile is half past the buffer;
 * repeated and unsorted indices;
-* a page set per head;
-* no buffer output;
+* a page set per head, small and at the full WorldAttention size;
+* no buffer output; a bf16 output without LSE;
 * forced split counts, which move the buffer stores between CTAs;
 * bad indices;
 * the one-layer WorldAttention chunk at full size, with the pages the
@@ -149,6 +149,48 @@ def test_attention_only_without_a_buffer():
     _, _, o, lse = _fused(q, kp, vp, ix, kl, vl, with_buf=False)
     _, _, o2, lse2 = _two_launch(q, kp, vp, ix, kl, vl)
     assert torch.equal(o, o2) and torch.equal(lse, lse2)
+
+
+def test_bf16_output_and_no_lse():
+    """The bf16 output (rounded once, as wa_block_attn rounds it) and a call
+    without LSE give the two-launch path's bits."""
+    kp, vp, q, kl, vl = _bank("bf16out", 6, 128, 3, 333, 77)
+    ix = torch.tensor([5, 1, 2], dtype=torch.int32, device=DEV)
+    o = torch.empty(q.shape, dtype=torch.bfloat16, device=DEV)
+    wa.wa_gather_attn(q, kp, vp, ix, kl, vl, o)
+    kb, vb = _bufs(ix, 128, 3)
+    wa.wa_gather_pages(kp, vp, ix, None, kb, vb)
+    o2 = torch.empty_like(o)
+    wa.wa_block_attn(q, kb, vb, kl, vl, o2)
+    wa.wa_check()
+    assert torch.equal(o, o2)
+    ref, _ = O.block_attn(np_of(q), np_of(kb), np_of(vb), np_of(kl), np_of(vl))
+    err = np.abs(f64(o) - ref)
+    # the fp32 tolerance plus half a bf16 ulp of rounding of the output
+    assert err.max() <= 1e-2 + np.abs(ref).max() * 2.0 ** -9
+
+
+def test_page_set_per_head_at_full_size():
+    """The per-head workload: the WorldAttention bank with a top-4 page set
+    per head from the per-head selection; the one launch equals the per-head
+    gather then attention bit for bit, and the buffer equals each head's
+    pages indexed on the device."""
+    c = synth.worldattention_case(device=DEV, recall_chunk=3)
+    kbar = torch.empty((c.n_pages, c.n_heads, D), dtype=torch.float32, device=DEV)
+    wa.wa_page_summarize(c.k_pages, kbar)
+    ix = torch.empty((c.n_heads, c.k_p), dtype=torch.int32, device=DEV)
+    wa.wa_select_pages_per_head(c.q, kbar, c.prompt_cur, c.prompt_chunks, c.pages_per_chunk,
+                                c.k_p, ix)
+    kb, vb, o, lse = _fused(c.q, c.k_pages, c.v_pages, ix, c.k_loc, c.v_loc)
+    kb2, vb2, o2, lse2 = _two_launch(c.q, c.k_pages, c.v_pages, ix, c.k_loc, c.v_loc)
+    assert torch.equal(o, o2) and torch.equal(lse, lse2)
+    assert torch.equal(kb, kb2) and torch.equal(vb, vb2)
+    P = c.page_tokens
+    for h in (0, 5, 11):
+        for s_ in range(c.k_p):
+            page = int(ix[h, s_])
+            assert torch.equal(kb[s_ * P:(s_ + 1) * P, h], c.k_pages[page, :, h])
+            assert torch.equal(vb[s_ * P:(s_ + 1) * P, h], c.v_pages[page, :, h])
 
 
 def test_bad_index_reads_zeros_and_is_recorded():
