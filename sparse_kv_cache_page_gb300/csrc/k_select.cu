@@ -276,46 +276,6 @@ k_page_summarize(const SumSegs<T> segs, int row_elems, int cw, int n_cb, int nve
 // ---------------------------------------------------------------------------
 // select: mean query -> prompt top-1 -> page scores -> top-K_p
 // ---------------------------------------------------------------------------
-// sum over i in [0, n) of a[i] * b[i] (and of b[i]^2 when nb2 != nullptr) by
-// one warp: 16-byte loads, eight per lane in flight, then a fixed-order warp
-// reduction.  a, b 16-byte aligned and n % 4 == 0; otherwise one float at a time.
-__device__ __forceinline__ float warp_dot(const float* __restrict__ a, const float* __restrict__ b,
-                                          int n, float* nb2) {
-  const int lane = threadIdx.x & 31;
-  float dot = 0.f, sq = 0.f;
-  if ((n & 3) == 0 && ((reinterpret_cast<uintptr_t>(a) | reinterpret_cast<uintptr_t>(b)) & 15) == 0) {
-    const float4* a4 = reinterpret_cast<const float4*>(a);
-    const float4* b4 = reinterpret_cast<const float4*>(b);
-    const int n4 = n >> 2;
-    for (int i0 = 0; i0 < n4; i0 += 32 * 8) {
-      float4 x[8], y[8];
-#pragma unroll
-      for (int u = 0; u < 8; ++u) {
-        const int i = i0 + u * 32 + lane;
-        x[u] = i < n4 ? a4[i] : make_float4(0.f, 0.f, 0.f, 0.f);
-        y[u] = i < n4 ? b4[i] : make_float4(0.f, 0.f, 0.f, 0.f);
-      }
-#pragma unroll
-      for (int u = 0; u < 8; ++u) {
-        dot += x[u].x * y[u].x + x[u].y * y[u].y + x[u].z * y[u].z + x[u].w * y[u].w;
-        sq += y[u].x * y[u].x + y[u].y * y[u].y + y[u].z * y[u].z + y[u].w * y[u].w;
-      }
-    }
-  } else {
-    for (int i = lane; i < n; i += 32) {
-      dot += a[i] * b[i];
-      sq += b[i] * b[i];
-    }
-  }
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) {
-    dot += __shfl_xor_sync(0xffffffffu, dot, o);
-    sq += __shfl_xor_sync(0xffffffffu, sq, o);
-  }
-  if (nb2) *nb2 = sq;
-  return dot;
-}
-
 __device__ __forceinline__ float warp_sum(float v) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
@@ -730,10 +690,14 @@ struct SegIn {
 template <typename T>
 wa_status summarize_t(const SegIn* in, int n_seg, int row_elems, cudaStream_t st) {
   if (n_seg < 1 || n_seg > kMaxSegs) return WA_ERR_INVALID_ARG;
-  // column blocks of 32 16-byte vectors (one warp per row) when the row divides
-  // into them, else whole rows
+  // column blocks of 32 16-byte vectors (one warp per row) for long pages whose
+  // rows divide into them, else whole rows (short blocks, such as the HSA
+  // block means, already give one CTA per block without partials; cutting
+  // them into column blocks only multiplies small CTAs: 0.046 -> 0.049 ms)
   const int E = VecOf<T>::E;
-  const int cw = (row_elems / E) % 32 == 0 ? 32 * E : row_elems;
+  int max_block = 0;
+  for (int i = 0; i < n_seg; ++i) max_block = in[i].block > max_block ? in[i].block : max_block;
+  const int cw = (row_elems / E) % 32 == 0 && max_block >= 1024 ? 32 * E : row_elems;
   const int n_cb = row_elems / cw;
   Plan p = plan_rows<T>(cw);
   SumSegs<T> segs{};
@@ -756,7 +720,9 @@ wa_status summarize_t(const SegIn* in, int n_seg, int row_elems, cudaStream_t st
     // last CTA added 151 partials one load batch after another).
     int splits = 2 * kTargetCtas / (n_pages * n_cb);
     if (splits < 1) splits = 1;
-    const int max_splits = (page_tokens + 63) / 64;   // at least 64 rows per CTA
+    // at least 16 rows of a whole row per CTA, 64 of a column block
+    const int min_rows = n_cb > 1 ? 64 : 16;
+    const int max_splits = (page_tokens + min_rows - 1) / min_rows;
     if (splits > max_splits) splits = max_splits;
     if (splits > 256) splits = 256;
     const int rps = (page_tokens + splits - 1) / splits;
