@@ -292,7 +292,8 @@ k_block_attn_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
   pdl_wait();
 
   if (warp >= 8) {
-    // ---------------- warpgroup 2: producer, two S issuers, the P V issuer
+    // ---------------- warpgroup 2: producer, S issuer, P V issuer (and, in
+    // the paged form, the buffer store warp)
     if (warp == kProducerWarp) {
       if (lane == 0) {
         prefetch_tmap(&tm_q);
