@@ -10,12 +10,14 @@
 // k_sparse_select  one CTA per head:
 //   1. each query-block row's max and exp-sum (a warp per row, fixed order);
 //   2. mass[kb] = mean over query blocks of the row-normalised exp (fixed order);
-//   3. Gini coefficient from the ascending sort of the mass (bitonic sort of
-//      (mass bits, index) keys; mass >= 0, so the bit pattern orders it);
-//   4. tau = 1 - G unless the caller gives tau[h];
-//   5. blocks ordered by (mass descending, index ascending) with the same sort,
-//      cumulative mass by an inclusive scan in that order; the first position
-//      reaching tau ends the kept set (at least one block);
+//   3. blocks ordered by (mass descending, index ascending): one bitonic sort
+//      of (inverted mass bits, index) keys (mass >= 0, so the bit pattern
+//      orders it);
+//   4. Gini coefficient from that order (the ascending order reversed: equal
+//      masses in another order leave the sum unchanged), tau = 1 - G unless
+//      the caller gives tau[h];
+//   5. cumulative mass by an inclusive scan in the sorted order; the first
+//      position reaching tau ends the kept set (at least one block);
 //   6. the kept blocks written in ascending block order (scan of flags).
 // Every reduction and scan has a fixed order, so the result is deterministic.
 #include <atomic>
@@ -211,30 +213,25 @@ k_sparse_select(const float* __restrict__ scores, int n_qb, int n_kb, const floa
       for (int qb = 0; qb < n_qb; ++qb) acc += expf(sh[(size_t)qb * n_kb + kb] - row_max[qb]) * row_inv[qb];
     }
     mass[kb] = kb < n_kb ? acc * inv_q : 0.f;
-    keys[kb] = kb < n_kb ? ((unsigned long long)__float_as_uint(mass[kb]) << 32) | (unsigned)kb
+    keys[kb] = kb < n_kb ? ((unsigned long long)(~__float_as_uint(acc * inv_q)) << 32) | (unsigned)kb
                          : ~0ull;
   }
   __syncthreads();
-  // 3. Gini coefficient: G = sum_i (2i - n - 1) x_(i) / (n sum x), x ascending, i from 1
+  // 3. mass descending, index ascending
   sort_keys(keys, n2);
+  // 4. Gini coefficient G = sum_i (2i - n - 1) x_(i) / (n sum x) over the
+  //    ascending order x_(1..n); position j of the descending order is i = n - j
   float num = 0.f, tot = 0.f;
-  for (int i = tid; i < n_kb; i += blockDim.x) {
-    const float x = mass[(unsigned)(keys[i] & 0xffffffffu)];
-    num += (float)(2 * (i + 1) - n_kb - 1) * x;
+  for (int j = tid; j < n_kb; j += blockDim.x) {
+    const float x = mass[(unsigned)(keys[j] & 0xffffffffu)];
+    num += (float)(n_kb - 1 - 2 * j) * x;
     tot += x;
   }
   num = block_sum(num, red);
   tot = block_sum(tot, red);
   const float g = tot > 0.f ? num / ((float)n_kb * tot) : 0.f;
-  // 4. threshold
   const float t = tau ? tau[h] : 1.0f - g;
-  // 5. mass descending, index ascending; cumulative mass in that order
-  __syncthreads();
-  for (int kb = tid; kb < n2; kb += blockDim.x)
-    keys[kb] = kb < n_kb ? ((unsigned long long)(~__float_as_uint(mass[kb])) << 32) | (unsigned)kb
-                         : ~0ull;
-  __syncthreads();
-  sort_keys(keys, n2);
+  // 5. cumulative mass in the sorted order
   for (int i = tid; i < n2; i += blockDim.x)
     cum[i] = i < n_kb ? mass[(unsigned)(keys[i] & 0xffffffffu)] : 0.f;
   __syncthreads();
