@@ -417,7 +417,12 @@ def run_gpu(args, world, rank, local, hybrid=False, per_head=False):
                                               "achieved": round(attn_tflops_two, 1),
                                               "frac": round(attn_tflops_two / tf_peak, 4),
                                               "traffic": ATTN_TRAFFIC_BYTES if not hybrid
-                                              else None}},
+                                              else None},
+                     # the same attention FLOPs over the two launches' time (gather +
+                     # attention), the work the one launch replaces
+                     "two_launch_gather_attention_frac": round(
+                         flops / ((per_two["gather"] + per_two["attention"]) * 1e-3) / 1e12
+                         / tf_peak, 4)},
         "e2e": {"value": round(world * flops / (e2e_ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
                 "ms_per_step": round(e2e_ms, 4), "h2d_bytes_per_step": h2d_bytes,
                 "d2h_bytes_per_step": d2h, "copies": "copy stream, double-buffered: once step k's "
