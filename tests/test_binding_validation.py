@@ -81,3 +81,20 @@ def test_linear_branch_buffers():
     _raises(wa.wa_linear_branch, q, kv, kv, None, None, e, _z(2, 16, 256), o)
     _raises(wa.wa_linear_branch, q, kv, kv, None, None, e, e, o, _z(3, dtype=F32))
     _raises(wa.wa_linear_branch, q, kv, kv, None, None, e.float(), e.float(), o)
+
+
+def test_gather_attn_buffers():
+    q, kp = _z(20, 2, 128), _z(3, 64, 2, 128)
+    idx, kl = torch.tensor([2, 0], dtype=I32), _z(8, 2, 128)
+    o = _z(20, 2, 128, dtype=F32)
+    buf = _z(128, 2, 128)
+    ga = wa.wa_gather_attn
+    _raises(ga, q, kp, kp, idx, kl, kl, o, _z(127, 2, 128), buf)                       # short buffer
+    _raises(ga, q, kp, kp, idx, kl, kl, o, buf, None)                                   # k without v
+    _raises(ga, q, kp, kp, idx.long(), kl, kl, o, buf, buf)                             # int64 indices
+    _raises(ga, q, kp, _z(3, 64, 2, 64), idx, kl, kl, o, buf, buf)                      # v pages shape
+    _raises(ga, q, kp, kp, torch.zeros((3, 2), dtype=I32), kl, kl, o, buf, buf)         # per-head rows != H
+    _raises(ga, q, kp, kp, idx, kl, None, o, buf, buf)                                  # k_loc without v_loc
+    _raises(ga, q, kp, kp, idx, kl, kl, _z(20, 2, 128, dtype=torch.float16), buf, buf)  # o dtype
+    _raises(ga, q, kp.float(), kp.float(), idx, kl, kl, o, buf, buf)                    # pages dtype
+    _raises(ga, q, kp, kp, idx, kl, kl, o, buf, buf, _z(2, 19, dtype=F32))              # short lse
