@@ -30,8 +30,12 @@
  *   - The library keeps one internal scratch arena per device, allocated
  *     with cudaMalloc on first need and grown (after a device-wide
  *     synchronize) when a call needs more; wa_shutdown() frees it.  Calls
- *     that use scratch (wa_page_summarize, wa_select_pages,
- *     wa_linear_branch) must not run concurrently on one device.
+ *     that use scratch or its ticket counters (wa_page_summarize,
+ *     wa_block_means, wa_block_means_segments, wa_select_pages and its
+ *     per-head form, wa_sparse_select, and the attention calls
+ *     wa_block_attn, wa_gather_attn, wa_sparse_attn, wa_linear_branch,
+ *     whose key-range splits meet in scratch) must not run concurrently on
+ *     one device: issue them on one stream, or order the streams.
  *   - Errors: arguments are validated on the host before any launch; a bad
  *     argument returns a status and enqueues nothing.  A launch failure
  *     returns WA_ERR_CUDA.  Kernels never trap: a device-side problem (a
