@@ -234,3 +234,28 @@ def test_worldattention_chunk_at_full_size():
                                   np_of(c.v_loc), rows=rows)
     assert_attn_close(o[rows], ref_o, torch.bfloat16, "WorldAttention chunk")
     assert np.abs(f64(lse[:, rows]) - ref_lse).max() <= LSE_ABS
+
+
+@pytest.mark.parametrize("seed", range(8))
+def test_random_shapes_equal_two_launches(seed):
+    """Seeded random shapes: pages of 64..448 rows (multiples of 64), 1..6
+    slots with repeats, 1..5 heads, 1..700 queries, 0..300 local tokens, a
+    shared or a per-head page set; the one launch equals the two launches bit
+    for bit, and the buffer equals the pages indexed on the device."""
+    rng = np.random.default_rng(1000 + seed)
+    P = int(rng.choice([64, 128, 192, 256, 448]))
+    n_pages, k_p = int(rng.integers(2, 9)), int(rng.integers(1, 7))
+    H, n_q, n_loc = int(rng.integers(1, 6)), int(rng.integers(1, 701)), int(rng.integers(0, 301))
+    per_head = bool(rng.integers(0, 2))
+    kp, vp, q, kl, vl = _bank(f"rand{seed}", n_pages, P, H, n_q, n_loc)
+    shape = (H, k_p) if per_head else (k_p,)
+    ix = torch.from_numpy(rng.integers(0, n_pages, size=shape).astype(np.int32)).to(DEV)
+    kb, vb, o, lse = _fused(q, kp, vp, ix, kl, vl)
+    kb2, vb2, o2, lse2 = _two_launch(q, kp, vp, ix, kl, vl)
+    assert torch.equal(o, o2) and torch.equal(lse, lse2), (P, n_pages, k_p, H, n_q, n_loc, per_head)
+    assert torch.equal(kb, kb2) and torch.equal(vb, vb2)
+    il = ix.long()
+    for s_ in range(k_p):
+        for h in range(H):
+            page = int(il[h, s_]) if per_head else int(il[s_])
+            assert torch.equal(kb[s_ * P:(s_ + 1) * P, h], kp[page, :, h])
