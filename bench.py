@@ -19,6 +19,7 @@ from __future__ import annotations
 
 import argparse
 import contextlib
+import datetime
 import json
 import math
 import os
@@ -70,11 +71,14 @@ def tensor_peak(timed_ms):
 
 
 class Clocks:
-    """nvidia-smi sampling during the timed region."""
+    """nvidia-smi sampling during the timed region: the sampler is started
+    and seen producing before the region begins, and only the samples whose
+    timestamps fall inside the region are summarised."""
 
     def __init__(self, index):
         self.index = index
         self.proc = None
+        self.t0 = self.t1 = None
         # raw samples (the JSON line carries their summary); WA_CLOCKS_DIR keeps them
         self.path = os.path.join(os.environ.get("WA_CLOCKS_DIR", tempfile.gettempdir()),
                                  f"clocks_bench_{os.getpid()}.csv")
@@ -85,16 +89,25 @@ class Clocks:
             self.f = open(self.path, "w")
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--id={self.index}",
-                 "--query-gpu=index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+                 "--query-gpu=timestamp,index,clocks.sm,clocks.max.sm,power.draw,"
+                 "clocks_event_reasons.active,"
                  "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
                  "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap",
                  "--format=csv,noheader,nounits", "-lms", "20"], stdout=self.f,
                 stderr=subprocess.DEVNULL)
+            # the sampler takes a moment to start: wait (up to 5 s) for its first line
+            deadline = time.time() + 5.0
+            while time.time() < deadline and self.proc.poll() is None:
+                if os.path.getsize(self.path) > 0:
+                    break
+                time.sleep(0.01)
         except Exception:
             self.proc = None
+        self.t0 = time.time()
         return self
 
     def __exit__(self, *a):
+        self.t1 = time.time()
         if self.proc is not None:
             self.proc.terminate()
             try:
@@ -106,23 +119,34 @@ class Clocks:
     def summary(self):
         if self.proc is None:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
-        rows = []
+        rows, inside = [], []
         try:
             for line in open(self.path):
                 parts = [x.strip() for x in line.split(",")]
-                if len(parts) >= 9:
-                    rows.append(parts)
+                if len(parts) >= 10:
+                    rows.append(parts[1:])
+                    try:
+                        ts = datetime.datetime.strptime(parts[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+                    except ValueError:
+                        continue
+                    if self.t0 <= ts <= self.t1:
+                        inside.append(parts[1:])
         except Exception:
             pass
         if not rows:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        outside = not inside
+        rows = rows if outside else inside
         sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
         mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower() == "active"})
-        return {"sm_mhz": statistics.median(sm) if sm else None,
-                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons,
-                "samples": len(rows)}
+        out = {"sm_mhz": statistics.median(sm) if sm else None,
+               "sm_max_mhz": max(mx) if mx else None, "reasons": reasons,
+               "samples": len(rows)}
+        if outside:
+            out["samples_are"] = "around the timed region (none fell inside it)"
+        return out
 
 
 def dist_init(args):
