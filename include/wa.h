@@ -263,17 +263,20 @@ wa_status wa_block_attn(const void* q, int n_q, const void* k_main, const void* 
  * The attention reads its key and value tiles straight from the pages; each
  * buffer tile is also written to k_buf/v_buf once, from on-chip memory, so the
  * pages are read once instead of twice (gather, then attention).
- * k_pages, v_pages : device [n_pages][page_tokens][n_heads][head_dim] bf16.
+ * k_pages, v_pages : device [n_pages][page_tokens][n_heads][head_dim] of `dt`.
  * idx_dev  : device int32 [k_p] (per_head == 0) or [n_heads][k_p]; an index
  *            outside [0, n_pages) reads as a page of zeros (its buffer rows
  *            are written as zeros) and is recorded (WA_ERR_INDEX from wa_check).
- * k_buf, v_buf : device [k_p*page_tokens][n_heads][head_dim] bf16, written;
+ * k_buf, v_buf : device [k_p*page_tokens][n_heads][head_dim] of `dt`, written;
  *            or both NULL (attention only, no buffer written).
  * k_loc, v_loc, n_loc, q, o, o_dt, lse, scale : as for wa_block_attn.
- * Needs dt == WA_BF16 (WA_ERR_DTYPE), head_dim == 128 and page_tokens a
- * multiple of 64 (WA_ERR_SHAPE); pages in device memory (WA_ERR_INVALID_ARG);
- * 16-byte aligned pointers (WA_ERR_ALIGN).  Other cases: wa_gather_pages,
- * then wa_block_attn.
+ * WA_BF16 runs the tensor-core kernel and needs head_dim == 128 and
+ * page_tokens a multiple of 64; WA_F32 runs the CUDA-core kernel (o_dt
+ * WA_F32, head_dim <= 256 and a multiple of 4, any page_tokens), where each
+ * head's first CTA writes that head's buffer rows as it reads them
+ * (WA_ERR_SHAPE / WA_ERR_DTYPE otherwise).  Pages in device memory
+ * (WA_ERR_INVALID_ARG); 16-byte aligned pointers (WA_ERR_ALIGN).  Pages in
+ * pinned host memory: wa_gather_pages, then wa_block_attn.
  */
 wa_status wa_gather_attn(const void* q, int n_q, const void* k_pages, const void* v_pages,
                          int n_pages, int page_tokens, const int32_t* idx_dev, int k_p,

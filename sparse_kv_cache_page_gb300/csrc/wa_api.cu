@@ -319,16 +319,17 @@ wa_status wa_gather_attn(const void* q, int n_q, const void* k_pages, const void
                          const void* v_loc, int n_loc, wa_dtype dt, int n_heads, int head_dim,
                          float scale, void* o, wa_dtype o_dt, float* lse, wa_stream_t stream) {
   if (!dtype_ok(dt) || !dtype_ok(o_dt)) return WA_ERR_DTYPE;
-  if (dt != WA_BF16) return WA_ERR_DTYPE;
+  if (dt == WA_F32 && o_dt != WA_F32) return WA_ERR_DTYPE;
   if (!q || !o || !k_pages || !v_pages || !idx_dev || n_q <= 0 || n_pages <= 0 ||
       page_tokens <= 0 || k_p <= 0 || n_loc < 0)
     return WA_ERR_INVALID_ARG;
   if ((k_buf == nullptr) != (v_buf == nullptr)) return WA_ERR_INVALID_ARG;
   if (n_loc > 0 && (!k_loc || !v_loc)) return WA_ERR_INVALID_ARG;
-  if (!row_ok(n_heads, head_dim, dt) || head_dim != 128 || (long long)n_heads * 128 > 16384)
+  if (!row_ok(n_heads, head_dim, dt)) return WA_ERR_SHAPE;
+  if (dt == WA_BF16 && (head_dim != 128 || (long long)n_heads * 128 > 16384 || page_tokens % 64 != 0))
     return WA_ERR_SHAPE;
-  if (page_tokens % 64 != 0 || (long long)n_pages * page_tokens > 0x7fffffffLL ||
-      (long long)k_p * page_tokens > 0x7fffffffLL)
+  if (dt == WA_F32 && (head_dim > 256 || head_dim % 4 != 0)) return WA_ERR_SHAPE;
+  if ((long long)n_pages * page_tokens > 0x7fffffffLL || (long long)k_p * page_tokens > 0x7fffffffLL)
     return WA_ERR_SHAPE;
   if (!aligned16(q) || !aligned16(o) || !aligned16(k_pages) || !aligned16(v_pages) ||
       (k_buf && (!aligned16(k_buf) || !aligned16(v_buf))) ||
@@ -352,6 +353,10 @@ wa_status wa_gather_attn(const void* q, int n_q, const void* k_pages, const void
   pk.page_tokens = page_tokens;
   pk.idx = idx_dev;
   pk.idx_stride = per_head ? k_p : 0;
+  if (dt == WA_F32)
+    return launch_attn_f32((const float*)q, n_q, (const float*)k_buf, (const float*)v_buf,
+                           k_p * page_tokens, (const float*)k_loc, (const float*)v_loc, n_loc,
+                           n_heads, head_dim, scale, (float*)o, lse, (cudaStream_t)stream, &pk);
   return launch_attn_tc(q, n_q, k_buf, v_buf, k_p * page_tokens, k_loc, v_loc, n_loc, n_heads,
                         scale, o, o_dt == WA_F32, lse, 0, nullptr, nullptr, 0,
                         (cudaStream_t)stream, nullptr, &pk);

@@ -123,10 +123,13 @@ wa_status launch_gather_device(const void* k_pages, const void* v_pages, size_t 
                                int n_pages, const int32_t* idx_dev, int k_p, void* k_buf,
                                void* v_buf, cudaStream_t s);
 
+struct PagedKV;
+// fp32 attention on the CUDA cores; with `paged`, the buffer segment comes from
+// the page bank (k_main/v_main then name the buffer to write, or are NULL).
 wa_status launch_attn_f32(const float* q, int n_q, const float* k_main, const float* v_main,
                           int n_main, const float* k_loc, const float* v_loc, int n_loc,
                           int n_heads, int head_dim, float scale, float* o, float* lse,
-                          cudaStream_t s);
+                          cudaStream_t s, const PagedKV* paged = nullptr);
 
 // bf16 tensor-core attention.  w_old/w_new: per-head fusion weights for the
 // epilogue o = w_old[h]*o + w_new[h]*O (accumulate != 0), may be NULL.

@@ -18,7 +18,9 @@ The cases cover:
 * forced split counts, which move the buffer stores between CTAs;
 * bad indices;
 * the one-layer WorldAttention chunk at full size, with the pages the
-  selection picks.
+  selection picks;
+* fp32 inputs (the CUDA-core kernel's paged form), pages of any size, and the
+  tiny fp32 workload's chain through the one launch, within 1e-5.
 """
 
 import numpy as np
@@ -259,3 +261,66 @@ def test_random_shapes_equal_two_launches(seed):
         for h in range(H):
             page = int(il[h, s_]) if per_head else int(il[s_])
             assert torch.equal(kb[s_ * P:(s_ + 1) * P, h], kp[page, :, h])
+
+
+@pytest.mark.parametrize("P,idx,per_head", [(32, [3, 0], False), (50, [1, 1, 2], False),
+                                            (24, [[2, 0], [1, 3]], True)])
+def test_fp32_pages_of_any_size(P, idx, per_head):
+    """fp32 inputs: the CUDA-core kernel reads the pages itself (any page
+    size), writes the buffer from each head's first CTA, and equals the
+    two launches bit for bit and the oracle within 1e-5."""
+    H = 2
+    g = lambda shape, t: synth.normal(shape, synth.seed_of("gattn32", P, t), DEV,  # noqa: E731
+                                      torch.float32)
+    kp, vp = g((4, P, H, 64), "kp"), g((4, P, H, 64), "vp")
+    q, kl, vl = g((37, H, 64), "q"), g((19, H, 64), "kl"), g((19, H, 64), "vl")
+    ix = torch.tensor(idx, dtype=torch.int32, device=DEV)
+    k_p = ix.shape[-1]
+    kb = torch.full((k_p * P, H, 64), 7.0, device=DEV)
+    vb = torch.full_like(kb, 7.0)
+    o = torch.empty(q.shape, device=DEV)
+    lse = torch.empty((H, 37), device=DEV)
+    wa.wa_gather_attn(q, kp, vp, ix, kl, vl, o, kb, vb, lse)
+    kb2, vb2 = torch.empty_like(kb), torch.empty_like(vb)
+    if per_head:
+        wa.wa_gather_pages_per_head(kp, vp, ix, kb2, vb2)
+    else:
+        wa.wa_gather_pages(kp, vp, ix, None, kb2, vb2)
+    o2, lse2 = torch.empty_like(o), torch.empty_like(lse)
+    wa.wa_block_attn(q, kb2, vb2, kl, vl, o2, lse2)
+    wa.wa_check()
+    assert torch.equal(kb, kb2) and torch.equal(vb, vb2)
+    assert torch.equal(o, o2) and torch.equal(lse, lse2)
+    gather = O.gather_pages_per_head if per_head else O.gather_pages
+    rk, rv = gather(np_of(kp), ix.cpu().numpy()), gather(np_of(vp), ix.cpu().numpy())
+    assert np.array_equal(np_of(kb), rk)
+    ref, ref_lse = O.block_attn(np_of(q), rk, rv, np_of(kl), np_of(vl))
+    assert_attn_close(o, ref, torch.float32, "fp32 paged")
+    assert np.abs(f64(lse) - ref_lse).max() <= 1e-5
+
+
+def test_tiny_fp32_workload_chain_in_one_launch():
+    """The tiny fp32 workload (1 head, d_k = 64, 2-frame pages of 32 tokens,
+    8 pages in 2 chunks, K_p = 2 after the prompt stage): summaries,
+    retrieval, then the gather and the attention in one launch, against the
+    oracle within 1e-5."""
+    c = synth.tiny_fp32_case(recall_chunk=1)
+    kp, vp, q = c.k_pages.to(DEV), c.v_pages.to(DEV), c.q.to(DEV)
+    kbar = torch.empty((c.n_pages, c.n_heads, c.head_dim), dtype=torch.float32, device=DEV)
+    wa.wa_page_summarize(kp, kbar)
+    ix = torch.empty(c.k_p, dtype=torch.int32, device=DEV)
+    wa.wa_select_pages(q, kbar, c.prompt_cur.to(DEV), c.prompt_chunks.to(DEV), c.pages_per_chunk,
+                       c.k_p, ix)
+    kb = torch.empty((c.k_p * c.page_tokens, c.n_heads, c.head_dim), device=DEV)
+    vb = torch.empty_like(kb)
+    o = torch.empty(q.shape, device=DEV)
+    wa.wa_gather_attn(q, kp, vp, ix, c.k_loc.to(DEV), c.v_loc.to(DEV), o, kb, vb)
+    wa.wa_check()
+    okp, ovp, oq = np_of(c.k_pages), np_of(c.v_pages), np_of(c.q)
+    idx, _, ch = O.select_pages(oq, O.page_summarize(okp), np_of(c.prompt_cur),
+                                np_of(c.prompt_chunks), c.pages_per_chunk, c.k_p)
+    assert ch == 1 and ix.cpu().tolist() == idx.tolist()
+    rk, rv = O.gather_pages(okp, idx), O.gather_pages(ovp, idx)
+    assert np.array_equal(np_of(kb), rk) and np.array_equal(np_of(vb), rv)
+    ref, _ = O.block_attn(oq, rk, rv, np_of(c.k_loc), np_of(c.v_loc))
+    assert_attn_close(o, ref, torch.float32, "tiny chain in one launch")
