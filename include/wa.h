@@ -271,7 +271,8 @@ wa_status wa_block_attn(const void* q, int n_q, const void* k_main, const void* 
  *            or both NULL (attention only, no buffer written).
  * k_loc, v_loc, n_loc, q, o, o_dt, lse, scale : as for wa_block_attn.
  * WA_BF16 runs the tensor-core kernel and needs head_dim == 128 and
- * page_tokens a multiple of 64; WA_F32 runs the CUDA-core kernel (o_dt
+ * page_tokens a multiple of 8 (a multiple of 64 keeps the tiles that cross a
+ * page boundary at 4 copies instead of 32); WA_F32 runs the CUDA-core kernel (o_dt
  * WA_F32, head_dim <= 256 and a multiple of 4, any page_tokens), where each
  * head's first CTA writes that head's buffer rows as it reads them
  * (WA_ERR_SHAPE / WA_ERR_DTYPE otherwise).  Pages in device memory

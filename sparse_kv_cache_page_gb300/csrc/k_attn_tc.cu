@@ -41,10 +41,10 @@
 //
 // Paged form (the gather fused into the producer): the buffer segment is not
 // read from a contiguous buffer but from the page bank, buffer row r being row
-// r % P of page idx[r / P] (P = page_tokens, a multiple of 64, so each 64-row
-// box of a key tile lies in one page).  A tile inside one page comes as
-// 128-row boxes, a tile across a page boundary (or past the buffer's end) as
-// 64-row boxes (64-row boxes throughout measured 13% slower).  The ring
+// r % P of page idx[r / P] (P = page_tokens, a multiple of 8).  A tile inside
+// one page comes as 128-row boxes, a tile across a page boundary (or past the
+// buffer's end) as 64-row boxes when P is a multiple of 64, else 8-row boxes,
+// each box inside one page (64-row boxes throughout measured 13% slower).  The ring
 // receives the same bytes as from the gathered buffer, so the results are
 // bit-identical to gather then attention.  With a buffer given, the CTA of
 // query pair j % n_qpairs also writes buffer tile j (K and V) from its ring
@@ -137,6 +137,7 @@ struct Params {
   // of the bank's bank_rows = n_pages * page_tokens rows
   const int32_t* idx;
   int idx_stride, page_tokens, n_pages, bank_rows;
+  int box_rows;                 // rows of the boxes that split a tile across pages: 64 or 8
   int store_buf;                // write each buffer tile to the buffer (one CTA per tile)
 };
 
@@ -312,16 +313,17 @@ k_block_attn_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
           const int slot = t % NS;
           const TileRef tr = tile_ref<kSparse>(p, head, jb + (t >> 1));
           const bool is_v = t & 1;
-          // paged form: the tile's bank rows, looked up before its slot is free;
-          // a tile inside one page is one 128-row box per column half, else
-          // two 64-row boxes (a page boundary, or the buffer's end, between)
+          // paged form: the tile's first bank row, looked up before its slot is
+          // free; a tile inside one page is one 128-row box per column half,
+          // else boxes of box_rows (64, or 8 when the pages are not whole
+          // 64-row boxes), each from its own page (a page boundary, or the
+          // buffer's end, between)
           bool whole = true;
-          int y0 = 0, y1 = 0;
+          int y0 = 0;
           if (kPaged && tr.seg == 0) {
             const int r0 = tr.row;
             whole = r0 + BN - 1 < p.n_main && r0 / p.page_tokens == (r0 + BN - 1) / p.page_tokens;
             y0 = bank_row(p, head, r0);
-            if (!whole) y1 = bank_row(p, head, r0 + 64);
           }
           if (t >= NS) {
             if (!mbar_wait_sleep(&bars->kv_empty[slot], ((t / NS) - 1) & 1, abort_flag, p.status, p.wait_ns))
@@ -336,10 +338,12 @@ k_block_attn_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
               tma_load_2d(map, &bars->kv_full[slot], dst + kKvHalf, xq + 64, y0);
             } else {
               const CUtensorMap* map = is_v ? &tm_vp : &tm_kp;
-              tma_load_2d(map, &bars->kv_full[slot], dst, xq, y0);
-              tma_load_2d(map, &bars->kv_full[slot], dst + kKvHalf, xq + 64, y0);
-              tma_load_2d(map, &bars->kv_full[slot], dst + kKvHalf / 2, xq, y1);
-              tma_load_2d(map, &bars->kv_full[slot], dst + kKvHalf + kKvHalf / 2, xq + 64, y1);
+              const int br = p.box_rows;
+              for (int b = 0; b < BN / br; ++b) {
+                const int y = b == 0 ? y0 : bank_row(p, head, tr.row + b * br);
+                tma_load_2d(map, &bars->kv_full[slot], dst + b * br * 128, xq, y);
+                tma_load_2d(map, &bars->kv_full[slot], dst + kKvHalf + b * br * 128, xq + 64, y);
+              }
             }
           } else {
             const CUtensorMap* map = tr.seg == 0 ? (is_v ? &tm_vm : &tm_km) : (is_v ? &tm_vl : &tm_kl);
@@ -924,11 +928,12 @@ wa_status launch_attn_tc(const void* q, int n_q, const void* k_main, const void*
     if ((rc = make_tmap_2d_bf16(&m.vl, v_loc, cols, n_loc, cols, 64, BN)) != WA_OK) return rc;
   }
   if (paged) {
-    // the page bank, read in 64-row boxes
+    // the page bank, read in 128-row boxes and in boxes of box_rows
     const uint64_t bank_rows = (uint64_t)paged->n_pages * paged->page_tokens;
-    if ((rc = make_tmap_2d_bf16(&m.kp, paged->k_pages, cols, bank_rows, cols, 64, 64)) != WA_OK)
+    const uint32_t br = paged->page_tokens % 64 == 0 ? 64 : 8;
+    if ((rc = make_tmap_2d_bf16(&m.kp, paged->k_pages, cols, bank_rows, cols, 64, br)) != WA_OK)
       return rc;
-    if ((rc = make_tmap_2d_bf16(&m.vp, paged->v_pages, cols, bank_rows, cols, 64, 64)) != WA_OK)
+    if ((rc = make_tmap_2d_bf16(&m.vp, paged->v_pages, cols, bank_rows, cols, 64, br)) != WA_OK)
       return rc;
     if ((rc = make_tmap_2d_bf16(&m.kq, paged->k_pages, cols, bank_rows, cols, 64, 128)) != WA_OK)
       return rc;
@@ -979,6 +984,7 @@ wa_status launch_attn_tc(const void* q, int n_q, const void* k_main, const void*
   p.page_tokens = paged ? paged->page_tokens : 0;
   p.n_pages = paged ? paged->n_pages : 0;
   p.bank_rows = paged ? paged->n_pages * paged->page_tokens : 0;
+  p.box_rows = paged && paged->page_tokens % 64 != 0 ? 8 : 64;
   p.store_buf = paged && k_main ? 1 : 0;
   Scratch sc;
   const size_t units = (size_t)p.n_qpairs * n_heads;

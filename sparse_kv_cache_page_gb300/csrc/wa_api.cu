@@ -326,7 +326,7 @@ wa_status wa_gather_attn(const void* q, int n_q, const void* k_pages, const void
   if ((k_buf == nullptr) != (v_buf == nullptr)) return WA_ERR_INVALID_ARG;
   if (n_loc > 0 && (!k_loc || !v_loc)) return WA_ERR_INVALID_ARG;
   if (!row_ok(n_heads, head_dim, dt)) return WA_ERR_SHAPE;
-  if (dt == WA_BF16 && (head_dim != 128 || (long long)n_heads * 128 > 16384 || page_tokens % 64 != 0))
+  if (dt == WA_BF16 && (head_dim != 128 || (long long)n_heads * 128 > 16384 || page_tokens % 8 != 0))
     return WA_ERR_SHAPE;
   if (dt == WA_F32 && (head_dim > 256 || head_dim % 4 != 0)) return WA_ERR_SHAPE;
   if ((long long)n_pages * page_tokens > 0x7fffffffLL || (long long)k_p * page_tokens > 0x7fffffffLL)

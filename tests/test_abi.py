@@ -75,7 +75,7 @@ def test_host_validation_without_gpu(lib):
     # gather: v pointer without v buffer
     assert lib.wa_gather_pages(fake, fake, 1, 4, 8, 1, 128, fake, None, 2, fake, None, None) == 1
     # gather + attention: fp32 inputs with a bf16 output -> DTYPE; bf16 pages not a multiple of
-    # 64 rows, bf16 head_dim != 128, fp32 head_dim over 256 -> SHAPE; a key buffer without a value
+    # 8 rows, bf16 head_dim != 128, fp32 head_dim over 256 -> SHAPE; a key buffer without a value
     # buffer, no indices -> INVALID_ARG; misaligned -> ALIGN
     f0 = ctypes.c_float(0)
     assert lib.wa_gather_attn(fake, 4, fake, fake, 8, 64, fake, 2, 0, None, None, None, None, 0,
@@ -83,6 +83,8 @@ def test_host_validation_without_gpu(lib):
     assert lib.wa_gather_attn(fake, 4, fake, fake, 8, 100, fake, 2, 0, None, None, None, None, 0,
                               0, 1, 260, f0, fake, 0, None, None) == 2
     assert lib.wa_gather_attn(fake, 4, fake, fake, 8, 100, fake, 2, 0, None, None, None, None, 0,
+                              1, 1, 128, f0, fake, 1, None, None) == 2
+    assert lib.wa_gather_attn(fake, 4, fake, fake, 8, 12, fake, 2, 0, None, None, None, None, 0,
                               1, 1, 128, f0, fake, 1, None, None) == 2
     assert lib.wa_gather_attn(fake, 4, fake, fake, 8, 64, fake, 2, 0, None, None, None, None, 0,
                               1, 1, 64, f0, fake, 1, None, None) == 2

@@ -11,6 +11,7 @@ The cases cover:
 
 * pages of 64 rows, where a key tile spans two pages;
 * pages of 192 and 320 rows, where a tile straddles a page boundary;
+* pages that are not whole 64-row boxes (24, 200, 1,560 rows: 8-row boxes);
 * an odd number of 64-row boxes, where the last tile is half past the buffer;
 * repeated and unsorted indices;
 * a page set per head, small and at the full WorldAttention size;
@@ -108,6 +109,9 @@ def _oracle_check(q, kp, vp, idx, kl, vl, kb, vb, o, lse, what):
     ("p64odd", 5, 64, [4, 1, 1], 3, 520, 0),       # 3 boxes: the last tile half past the buffer
     ("p128one", 4, 128, [2], 1, 17, 33),           # one page, one tile, few queries
     ("p320", 3, 320, [2, 0], 2, 1000, 250),        # 5 boxes per page, ragged local tail
+    ("p200", 5, 200, [4, 1, 3], 2, 300, 60),       # not whole 64-row boxes: 8-row boxes
+    ("p24", 6, 24, [5, 0, 2, 2, 1], 1, 150, 40),   # pages smaller than a tile
+    ("p1560", 4, 1560, [3, 1], 2, 700, 100),       # one 1,560-token frame per page
 ])
 def test_fused_equals_two_launch_and_oracle(tag, n_pages, P, idx, H, n_q, n_loc):
     kp, vp, q, kl, vl = _bank(tag, n_pages, P, H, n_q, n_loc)
@@ -240,12 +244,12 @@ def test_worldattention_chunk_at_full_size():
 
 @pytest.mark.parametrize("seed", range(8))
 def test_random_shapes_equal_two_launches(seed):
-    """Seeded random shapes: pages of 64..448 rows (multiples of 64), 1..6
+    """Seeded random shapes: pages of 40..448 rows (multiples of 8), 1..6
     slots with repeats, 1..5 heads, 1..700 queries, 0..300 local tokens, a
     shared or a per-head page set; the one launch equals the two launches bit
     for bit, and the buffer equals the pages indexed on the device."""
     rng = np.random.default_rng(1000 + seed)
-    P = int(rng.choice([64, 128, 192, 256, 448]))
+    P = int(rng.choice([64, 128, 192, 256, 448, 40, 136, 264]))
     n_pages, k_p = int(rng.integers(2, 9)), int(rng.integers(1, 7))
     H, n_q, n_loc = int(rng.integers(1, 6)), int(rng.integers(1, 701)), int(rng.integers(0, 301))
     per_head = bool(rng.integers(0, 2))
