@@ -242,7 +242,7 @@ def test_worldattention_chunk_at_full_size():
     assert np.abs(f64(lse[:, rows]) - ref_lse).max() <= LSE_ABS
 
 
-@pytest.mark.parametrize("seed", range(8))
+@pytest.mark.parametrize("seed", range(16))
 def test_random_shapes_equal_two_launches(seed):
     """Seeded random shapes: pages of 40..448 rows (multiples of 8), 1..6
     slots with repeats, 1..5 heads, 1..700 queries, 0..300 local tokens, a
