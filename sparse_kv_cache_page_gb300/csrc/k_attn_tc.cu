@@ -671,9 +671,13 @@ k_block_attn_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                    reinterpret_cast<const float4*>(stage + (size_t)r * kStagePitch)[lane]);
           }
         }
-        __threadfence();
+        // one fence, by the thread that counts: the barrier orders the other
+        // threads' stores before it (a fence is cumulative)
         softmax_bar();
-        if (threadIdx.x == 0) atomicAdd(&p.counters[unit], 1u << 16);
+        if (threadIdx.x == 0) {
+          __threadfence();
+          atomicAdd(&p.counters[unit], 1u << 16);
+        }
       } else {
         if (threadIdx.x == 0) {
           volatile unsigned* cnt = &p.counters[unit];
@@ -696,9 +700,8 @@ k_block_attn_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
           }
           bars->ticket = done ? 1u : 0u;
         }
-        softmax_bar();
+        softmax_bar();   // thread 0 fenced after seeing the done count: the others read after it
         bool go = all_ok && bars->ticket == 1u;
-        __threadfence();
         if (go) {
           // this thread's row: statistics of every split (its own from registers),
           // the common maximum, the denominators, the LSE and the split weights

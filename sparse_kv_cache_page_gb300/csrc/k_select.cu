@@ -138,13 +138,16 @@ __device__ void colsum_rows(const T* __restrict__ base, size_t stride, int row_e
 // Returns true in every thread of the CTA that took the last ticket.
 __device__ bool last_ticket(unsigned* counter, unsigned n) {
   __shared__ unsigned s_ticket;
-  __threadfence();
+  // the CTA's writes are ordered before thread 0's fence by the barrier (a
+  // fence is cumulative over what happens before it), so one fence suffices
   __syncthreads();
-  if (threadIdx.x == 0) s_ticket = atomicAdd(counter, 1u);
+  if (threadIdx.x == 0) {
+    __threadfence();
+    s_ticket = atomicAdd(counter, 1u);
+    if (s_ticket == n - 1) __threadfence();
+  }
   __syncthreads();
-  const bool last = (s_ticket == n - 1);
-  if (last) __threadfence();
-  return last;
+  return s_ticket == n - 1;
 }
 
 // out[c] = scale * sum_{p < n} rows[p][c] for c < row_elems (row_elems % 4 == 0),
