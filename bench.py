@@ -40,10 +40,10 @@ H, D, P, N_PAGES, PPC, N_CHUNKS, PDIM, KP, NQ, NLOC = 12, 128, 12480, 40, 8, 5, 
 
 # DRAM bytes read + written per launch of the attention kernel, from one ncu capture of the
 # current kernel (profiles/attention_worldattention_1layer.md); None once the kernel changes.
-ATTN_TRAFFIC_BYTES = 393.58e6
+ATTN_TRAFFIC_BYTES = 393.66e6
 # the same for the gather+attention launch, the kernel's paged form
 # (profiles/gather_attention_worldattention_1layer.md)
-FUSED_TRAFFIC_BYTES = 677.97e6
+FUSED_TRAFFIC_BYTES = 678.13e6
 
 
 def attn_flops(n_q, n_kv, d, h):
