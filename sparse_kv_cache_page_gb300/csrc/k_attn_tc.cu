@@ -555,7 +555,7 @@ k_block_attn_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     // (a CTA with no key tiles, block-sparse form, reaches here without having
     // waited for anything).  Every K/V copy was consumed by an MMA the loop
     // waited for.
-    // (paged form: and the producer's buffer stores have read the ring)
+    // (paged form: and the store warp's buffer stores have read the ring)
     bool staging_ok =
         ok && __all_sync(0xffffffffu, mbar_wait(&bars->q_full, 0, abort_flag, p.status, p.wait_ns));
     if (kPaged)
