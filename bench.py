@@ -474,7 +474,8 @@ def run_gpu(args, world, rank, local, hybrid=False, per_head=False):
         line["linear_read_gbs"] = round(proj_bytes / (per["linear"] * 1e-3) / 1e9, 1)
     if rank == 0 and world == 1 and not args.no_cpu_baseline and not hybrid and not per_head:
         # the last timed step's indices and output, checked against the oracle
-        line["cpu_baseline"], line["parity"] = cpu_baseline_gpu_arm(c, kp, vp, o, idx_bench, chunk)
+        line["cpu_baseline"], line["parity"] = cpu_baseline_gpu_arm(c, kp, vp, o, idx_bench, chunk,
+                                                                    kbuf, vbuf)
     return line
 
 
@@ -1030,6 +1031,8 @@ def oracle_setup(c, fetch_k, fetch_v):
         vb[j]
     inp["idx"], inp["chunk"] = [int(j) for j in idx], chunk
     inp["rows"] = np.arange(0, NQ, SAMPLE_ROWS_STEP)
+    # buffer rows whose gathered bytes the GPU arm checks: every 997th, and the last
+    inp["buf_rows"] = np.concatenate([np.arange(0, KP * P, 997), [KP * P - 1]])
     return inp
 
 
@@ -1051,8 +1054,10 @@ def oracle_sample(inp):
     t3 = time.perf_counter()
     o, _ = O.block_attn(inp["q"], kbuf, vbuf, inp["kloc"], inp["vloc"], rows=inp["rows"])
     t4 = time.perf_counter()
+    brows = inp["buf_rows"]
     return {"summarize": t1 - t0, "select": t2 - t1, "gather": t3 - t2, "attention": t4 - t3,
-            "idx": [int(j) for j in idx], "chunk": chunk, "o": o}
+            "idx": [int(j) for j in idx], "chunk": chunk, "o": o,
+            "kbuf_rows": kbuf[brows], "vbuf_rows": vbuf[brows]}
 
 
 def oracle_sample_flops(inp):
@@ -1084,9 +1089,11 @@ def oracle_baseline(samples, inp, wall_s, cpu_s):
                                f"+ gather + {NQ / n_rows:.0f} x sampled attention"}
 
 
-def cpu_baseline_gpu_arm(c, kp, vp, o_dev, idx_dev, chunk_dev, reps=3):
+def cpu_baseline_gpu_arm(c, kp, vp, o_dev, idx_dev, chunk_dev, kbuf_dev=None, vbuf_dev=None,
+                        reps=3):
     """The oracle timed on the host cores on the GPU arm's own inputs; also
-    checks the benchmarked chunk's indices and sampled output rows against it."""
+    checks the benchmarked chunk's indices, sampled rows of its gathered
+    buffer and sampled output rows against it."""
     import numpy as np
     import torch
 
@@ -1105,7 +1112,13 @@ def cpu_baseline_gpu_arm(c, kp, vp, o_dev, idx_dev, chunk_dev, reps=3):
               "idx": inp["idx"], "chunk": inp["chunk"],
               "sampled_rows": len(inp["rows"]),
               "attn_max_abs_err": float(err.max()), "attn_mean_abs_err": float(err.mean()),
-              "tolerance": "indices bit-exact; attention max 1e-2, mean 1e-3"}
+              "tolerance": "indices and buffer bytes bit-exact; attention max 1e-2, mean 1e-3"}
+    if kbuf_dev is not None:
+        br = torch.from_numpy(inp["buf_rows"]).to(kbuf_dev.device)
+        parity["buffer_rows_match"] = bool(
+            np.array_equal(synth.to_oracle(kbuf_dev[br]), samples[0]["kbuf_rows"])
+            and np.array_equal(synth.to_oracle(vbuf_dev[br]), samples[0]["vbuf_rows"]))
+        parity["buffer_rows_checked"] = len(inp["buf_rows"])
     return rec, parity
 
 
